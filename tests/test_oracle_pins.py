@@ -1,0 +1,285 @@
+"""Pins for the float64 oracle, against things other than the oracle itself.
+
+Each test ties one part of the oracle to something independent of it:
+  * library routines: torch's float64 CPU scaled_dot_product_attention with
+    its own documented causal masks (upper-left = top-left, lower-right =
+    bottom-right), torch.logsumexp, and torch autograd for the gradients;
+  * closed forms (zero keys give a uniform average, one key gives that key's
+    value, window 0 gives the diagonal value);
+  * invariants the pages rely on (top-left and bottom-right coincide when
+    Sq == Sk and differ otherwise: TransformerEngine PR #3527,
+    "Verification"; GQA equals MHA with repeated KV heads; THD equals the
+    per-sequence BSHD runs; SBHD is a transpose of BSHD);
+  * central finite differences of L = <dO, O> for every input element.
+A plausible slip in the oracle (dropped scale, transposed operand, wrong head
+mapping, wrong mask diagonal, wrong gradient sign) fails at least one.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+import torch.nn.functional as F
+from torch.nn.attention.bias import causal_lower_right, causal_upper_left
+
+from oracle import oracle
+
+pytestmark = pytest.mark.filterwarnings("ignore::UserWarning")
+
+
+def rng(seed):
+    return np.random.Generator(np.random.PCG64(seed))
+
+
+def _bhsd(x):  # bshd numpy -> (B, H, S, D) torch float64
+    return torch.from_numpy(np.ascontiguousarray(x)).permute(0, 2, 1, 3)
+
+
+def torch_ref(q, k, v, mask, scale, dout=None, gqa=True):
+    """Library reference (float64 torch SDPA) on BSHD numpy arrays."""
+    qt, kt, vt = (_bhsd(x).clone().requires_grad_(dout is not None) for x in (q, k, v))
+    lq, lk = q.shape[1], k.shape[1]
+    attn_mask, is_causal = None, False
+    if mask == "causal":
+        attn_mask = causal_upper_left(lq, lk)._materialize()
+    elif mask == "causal_br":
+        attn_mask = causal_lower_right(lq, lk)._materialize()
+    rep = q.shape[2] // k.shape[2]
+    kr = kt.repeat_interleave(rep, dim=1)
+    vr = vt.repeat_interleave(rep, dim=1)
+    o = F.scaled_dot_product_attention(qt, kr, vr, attn_mask=attn_mask, is_causal=is_causal, scale=scale)
+    s = scale * qt @ kr.transpose(-1, -2)
+    if attn_mask is not None:
+        s = s.masked_fill(~attn_mask, -math.inf)
+    lse = torch.logsumexp(s, dim=-1)  # (B, H, S)
+    res = {"o": o.permute(0, 2, 1, 3).detach().numpy(),
+           "lse": lse.permute(0, 2, 1).reshape(-1, q.shape[2]).detach().numpy()}
+    if dout is not None:
+        o.backward(_bhsd(dout))
+        res["dq"] = qt.grad.permute(0, 2, 1, 3).numpy()
+        res["dk"] = kt.grad.permute(0, 2, 1, 3).numpy()
+        res["dv"] = vt.grad.permute(0, 2, 1, 3).numpy()
+    return res
+
+
+CASES = [
+    # (B, Sq, Sk, Hq, Hkv, D, mask)
+    (2, 7, 7, 2, 2, 8, "none"),
+    (2, 9, 9, 4, 2, 8, "causal"),
+    (1, 6, 11, 4, 1, 4, "causal"),
+    (2, 5, 12, 2, 1, 8, "causal_br"),
+    (1, 12, 12, 6, 3, 16, "causal_br"),
+    (2, 4, 13, 4, 4, 8, "none"),
+]
+
+
+@pytest.mark.parametrize("case", CASES)
+def test_forward_and_backward_match_torch_sdpa(case):
+    b, sq, sk, hq, hkv, d, mask = case
+    r = rng(sum(case[:-1]))
+    q, do = r.standard_normal((b, sq, hq, d)), r.standard_normal((b, sq, hq, d))
+    k, v = r.standard_normal((b, sk, hkv, d)), r.standard_normal((b, sk, hkv, d))
+    scale = 0.37
+    ref = torch_ref(q, k, v, mask, scale, dout=do)
+    o, lse = oracle.fwd(q, k, v, layout="bshd", mask=mask, scale=scale)
+    out = oracle.bwd(q, k, v, do, layout="bshd", mask=mask, scale=scale)
+    np.testing.assert_allclose(o, ref["o"], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, ref["lse"], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(out["o"], ref["o"], rtol=0, atol=1e-12)
+    for key in ("dq", "dk", "dv"):
+        np.testing.assert_allclose(out[key], ref[key], rtol=0, atol=1e-11, err_msg=key)
+
+
+def test_top_left_equals_bottom_right_when_square_and_differs_when_rectangular():
+    r = rng(5)
+    q, k, v = r.standard_normal((1, 10, 2, 8)), r.standard_normal((1, 10, 2, 8)), r.standard_normal((1, 10, 2, 8))
+    a, la = oracle.fwd(q, k, v, mask="causal")
+    b, lb = oracle.fwd(q, k, v, mask="causal_br")
+    np.testing.assert_array_equal(a, b)
+    np.testing.assert_array_equal(la, lb)
+    k2, v2 = r.standard_normal((1, 16, 2, 8)), r.standard_normal((1, 16, 2, 8))
+    a, _ = oracle.fwd(q, k2, v2, mask="causal")
+    b, _ = oracle.fwd(q, k2, v2, mask="causal_br")
+    assert np.abs(a - b).max() > 1e-3
+    # bottom-right: the last query row sees every key, i.e. equals the unmasked row
+    c, _ = oracle.fwd(q, k2, v2, mask="none")
+    np.testing.assert_allclose(b[:, -1], c[:, -1], atol=1e-13)
+    # top-left: the first query row sees only key 0
+    np.testing.assert_allclose(a[0, 0], v2[0, 0], atol=1e-13)
+
+
+def test_zero_keys_give_uniform_average_and_log_count():
+    r = rng(6)
+    sq = sk = 9
+    q, v = r.standard_normal((1, sq, 2, 8)), r.standard_normal((1, sk, 2, 8))
+    k = np.zeros_like(v)
+    for mask in ("none", "causal"):
+        o, lse = oracle.fwd(q, k, v, mask=mask, scale=0.5)
+        for i in range(sq):
+            n = sk if mask == "none" else i + 1
+            np.testing.assert_allclose(o[0, i], v[0, :n].mean(axis=0), atol=1e-13)
+            np.testing.assert_allclose(lse[i], [math.log(n)] * 2, atol=1e-13)
+
+
+def test_single_key_and_dominant_key():
+    r = rng(7)
+    q, k, v = r.standard_normal((2, 3, 2, 8)), r.standard_normal((2, 1, 2, 8)), r.standard_normal((2, 1, 2, 8))
+    o, lse = oracle.fwd(q, k, v, mask="none", scale=0.3)
+    np.testing.assert_allclose(o, np.broadcast_to(v, o.shape), atol=1e-14)
+    s00 = 0.3 * np.einsum("bshd,bhd->bsh", q, k[:, 0])
+    np.testing.assert_allclose(lse, s00.reshape(-1, 2), atol=1e-13)
+    # one key far above the rest dominates the softmax
+    k2 = np.zeros((1, 5, 1, 4))
+    k2[0, 3, 0, 0] = 60.0
+    q2 = np.zeros((1, 1, 1, 4))
+    q2[0, 0, 0, 0] = 1.0
+    v2 = r.standard_normal((1, 5, 1, 4))
+    o2, _ = oracle.fwd(q2, k2, v2, mask="none", scale=1.0)
+    np.testing.assert_allclose(o2[0, 0, 0], v2[0, 3, 0], atol=1e-20)
+
+
+def test_lse_rows_of_p_and_delta_identities():
+    r = rng(8)
+    q, k, v, do = (r.standard_normal(s) for s in [(1, 8, 2, 4), (1, 8, 2, 4), (1, 8, 2, 4), (1, 8, 2, 4)])
+    scale = 0.7
+    out = oracle.bwd(q, k, v, do, mask="causal", scale=scale)
+    # a value vector of ones is reproduced exactly when the rows of P sum to 1
+    o1, _ = oracle.fwd(q, k, np.ones_like(v), mask="causal", scale=scale)
+    np.testing.assert_allclose(o1, 1.0, atol=1e-14)
+    for h in range(2):
+        s = scale * q[0, :, h] @ k[0, :, h].T
+        s[np.triu_indices(8, 1)] = -np.inf
+        lse = np.log(np.exp(s).sum(axis=1))
+        np.testing.assert_allclose(out["lse"][:, h], lse, atol=1e-13)
+        p = np.exp(s - lse[:, None])
+        dp = do[0, :, h] @ v[0, :, h].T
+        # delta = rowsum(dO * O) = rowsum(P * dP)
+        np.testing.assert_allclose(out["delta"][:, h], (p * dp).sum(axis=1), atol=1e-13)
+
+
+def test_gqa_equals_mha_with_repeated_kv_and_group_sums():
+    r = rng(9)
+    hq, hkv = 6, 2
+    q, do = r.standard_normal((2, 7, hq, 8)), r.standard_normal((2, 7, hq, 8))
+    k, v = r.standard_normal((2, 7, hkv, 8)), r.standard_normal((2, 7, hkv, 8))
+    kr, vr = np.repeat(k, hq // hkv, axis=2), np.repeat(v, hq // hkv, axis=2)
+    g = oracle.bwd(q, k, v, do, mask="causal")
+    m = oracle.bwd(q, kr, vr, do, mask="causal")
+    np.testing.assert_allclose(g["o"], m["o"], atol=1e-14)
+    np.testing.assert_allclose(g["dq"], m["dq"], atol=1e-13)
+    np.testing.assert_allclose(g["dk"], m["dk"].reshape(2, 7, hkv, hq // hkv, 8).sum(axis=3), atol=1e-13)
+    np.testing.assert_allclose(g["dv"], m["dv"].reshape(2, 7, hkv, hq // hkv, 8).sum(axis=3), atol=1e-13)
+
+
+@pytest.mark.parametrize("mask", ["none", "causal", "causal_br"])
+def test_thd_equals_per_sequence_bshd_and_sbhd_is_transpose(mask):
+    r = rng(10)
+    lq = np.array([5, 9, 3])
+    lk = lq if mask != "causal_br" else np.array([7, 9, 6])
+    cq = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
+    ck = np.concatenate([[0], np.cumsum(lk)]).astype(np.int32)
+    q, do = r.standard_normal((cq[-1], 4, 8)), r.standard_normal((cq[-1], 4, 8))
+    k, v = r.standard_normal((ck[-1], 2, 8)), r.standard_normal((ck[-1], 2, 8))
+    t = oracle.bwd(q, k, v, do, layout="thd", mask=mask, cu_q=cq, cu_kv=ck)
+    for b in range(3):
+        sl, kl = slice(cq[b], cq[b + 1]), slice(ck[b], ck[b + 1])
+        s = oracle.bwd(q[None, sl], k[None, kl], v[None, kl], do[None, sl], mask=mask)
+        np.testing.assert_allclose(t["o"][sl], s["o"][0], atol=1e-14)
+        np.testing.assert_allclose(t["lse"][sl], s["lse"], atol=1e-14)
+        for key, rs in (("dq", sl), ("dk", kl), ("dv", kl)):
+            np.testing.assert_allclose(t[key][rs], s[key][0], atol=1e-13)
+    # SBHD: same numbers, rows ordered (s, b)
+    qb, kb, vb, dob = (r.standard_normal((2, 6, 2, 8)) for _ in range(4))
+    bs = oracle.bwd(qb, kb, vb, dob, layout="bshd", mask=mask)
+    tr = lambda x: np.ascontiguousarray(x.transpose(1, 0, 2, 3))
+    sb = oracle.bwd(tr(qb), tr(kb), tr(vb), tr(dob), layout="sbhd", mask=mask)
+    for key in ("o", "dq", "dk", "dv"):
+        np.testing.assert_allclose(sb[key], tr(bs[key]), atol=1e-14)
+    np.testing.assert_allclose(sb["lse"], bs["lse"].reshape(2, 6, 2).transpose(1, 0, 2).reshape(12, 2), atol=1e-14)
+
+
+def test_window_equals_unmasked_attention_over_the_band():
+    r = rng(11)
+    sq, left = 12, 3
+    q, k, v = (r.standard_normal((1, sq, 2, 8)) for _ in range(3))
+    o, lse = oracle.fwd(q, k, v, mask="causal", window=(left, 0), scale=0.4)
+    for i in range(sq):
+        lo = max(0, i - left)
+        oi, li = oracle.fwd(q[:, i:i + 1], k[:, lo:i + 1], v[:, lo:i + 1], mask="none", scale=0.4)
+        np.testing.assert_allclose(o[:, i], oi[:, 0], atol=1e-14)
+        np.testing.assert_allclose(lse[i], li[0], atol=1e-14)
+    # a window at least as long as the sequence is plain causal
+    o2, _ = oracle.fwd(q, k, v, mask="causal", window=(sq, 0), scale=0.4)
+    o3, _ = oracle.fwd(q, k, v, mask="causal", scale=0.4)
+    np.testing.assert_array_equal(o2, o3)
+    # window 0 keeps only the diagonal
+    o4, _ = oracle.fwd(q, k, v, mask="causal", window=(0, 0))
+    np.testing.assert_allclose(o4, v, atol=1e-14)
+    # bottom-right window: diagonal of row i is i + Sk - Sq
+    k5, v5 = r.standard_normal((1, 20, 2, 8)), r.standard_normal((1, 20, 2, 8))
+    o5, _ = oracle.fwd(q, k5, v5, mask="causal_br", window=(2, 0), scale=0.4)
+    for i in range(sq):
+        dg = i + 8
+        oi, _ = oracle.fwd(q[:, i:i + 1], k5[:, dg - 2:dg + 1], v5[:, dg - 2:dg + 1], mask="none", scale=0.4)
+        np.testing.assert_allclose(o5[:, i], oi[:, 0], atol=1e-14)
+
+
+def test_fully_masked_rows_are_neutral():
+    r = rng(12)
+    q, do = r.standard_normal((1, 6, 2, 4)), r.standard_normal((1, 6, 2, 4))
+    k, v = r.standard_normal((1, 3, 2, 4)), r.standard_normal((1, 3, 2, 4))
+    out = oracle.bwd(q, k, v, do, mask="causal_br")  # rows 0..2 see no key
+    assert np.all(out["o"][0, :3] == 0) and np.all(np.isneginf(out["lse"][:3]))
+    assert np.all(out["dq"][0, :3] == 0)
+    # the remaining rows equal a run without the empty rows
+    rest = oracle.bwd(q[:, 3:], k, v, do[:, 3:], mask="causal_br")
+    for key in ("dk", "dv"):
+        np.testing.assert_allclose(out[key], rest[key], atol=1e-14)
+
+
+@pytest.mark.parametrize("mask,sq,sk", [("causal", 5, 5), ("causal_br", 3, 6), ("none", 4, 3)])
+def test_gradients_match_central_differences(mask, sq, sk):
+    r = rng(13 + sq)
+    hq, hkv, d = 2, 1, 3
+    q, do = r.standard_normal((1, sq, hq, d)), r.standard_normal((1, sq, hq, d))
+    k, v = r.standard_normal((1, sk, hkv, d)), r.standard_normal((1, sk, hkv, d))
+    scale, eps = 0.8, 1e-6
+    g = oracle.bwd(q, k, v, do, mask=mask, scale=scale)
+
+    def loss(qq, kk, vv):
+        o, _ = oracle.fwd(qq, kk, vv, mask=mask, scale=scale)
+        return float(np.sum(o * do))
+
+    for name, x in (("dq", q), ("dk", k), ("dv", v)):
+        fd = np.zeros_like(x)
+        for idx in np.ndindex(x.shape):
+            xp, xm = x.copy(), x.copy()
+            xp[idx] += eps
+            xm[idx] -= eps
+            args_p = [xp if a is x else a for a in (q, k, v)]
+            args_m = [xm if a is x else a for a in (q, k, v)]
+            fd[idx] = (loss(*args_p) - loss(*args_m)) / (2 * eps)
+        np.testing.assert_allclose(g[name], fd, rtol=1e-6, atol=1e-8, err_msg=name)
+
+
+def test_row_samplers_agree_with_full_runs():
+    r = rng(14)
+    lq = np.array([40, 17])
+    cq = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
+    q, do = r.standard_normal((cq[-1], 4, 8)), r.standard_normal((cq[-1], 4, 8))
+    k, v = r.standard_normal((cq[-1], 2, 8)), r.standard_normal((cq[-1], 2, 8))
+    full = oracle.bwd(q, k, v, do, layout="thd", mask="causal", cu_q=cq, cu_kv=cq, window=(5, 0))
+    bhi = np.array([[0, 0, 0], [0, 3, 39], [1, 2, 16], [1, 1, 4]])
+    o, lse = oracle.fwd_rows(q, k, v, bhi, layout="thd", mask="causal", cu_q=cq, cu_kv=cq, window=(5, 0))
+    dq = oracle.dq_rows(q, k, v, do, bhi, layout="thd", mask="causal", cu_q=cq, cu_kv=cq, window=(5, 0))
+    for n, (b, h, i) in enumerate(bhi):
+        row = cq[b] + i
+        np.testing.assert_allclose(o[n], full["o"][row, h], atol=1e-14)
+        np.testing.assert_allclose(lse[n], full["lse"][row, h], atol=1e-14)
+        np.testing.assert_allclose(dq[n], full["dq"][row, h], atol=1e-14)
+    part = oracle.bwd(q, k, v, do, layout="thd", mask="causal", cu_q=cq, cu_kv=cq, window=(5, 0),
+                      batch_range=(1, 2), kv_head_range=(1, 2))
+    sl = slice(cq[1], cq[2])
+    np.testing.assert_allclose(part["dk"][sl, 1], full["dk"][sl, 1], atol=1e-14)
+    np.testing.assert_allclose(part["dq"][sl, 2:], full["dq"][sl, 2:], atol=1e-14)
+    assert np.all(part["dk"][sl, 0] == 0) and np.all(part["dk"][: cq[1]] == 0)
