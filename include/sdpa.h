@@ -1,0 +1,154 @@
+/*
+ * sdpa.h -- C ABI of the fused scaled-dot-product attention library for one
+ * GB300 (sm_103a) GPU: libsdpa.so.
+ *
+ * Operation (TransformerEngine PR #3527 "Approach" and PR #3705 "Execution
+ * and supported scope" describe the fused kernels this library provides;
+ * the arithmetic is standard softmax attention):
+ *
+ *   forward   S = scale * Q K^T, masked (top-left or bottom-right causal, an
+ *             optional (left, right) window), P = softmax(S) row-wise,
+ *             O = P V, and LSE = ln sum_j exp(S_ij) per query row, stored as
+ *             FP32 natural logarithms in a packed token-major array
+ *             (PR #3705: "Stats remain packed token-major FP32 natural
+ *             logarithms").
+ *   backward  given Q, K, V, O, LSE and dO: recompute P from LSE and return
+ *             dQ, dK, dV of the forward above (GQA heads summed into their
+ *             shared K/V head).
+ *
+ * Layouts (PR #3527 "Scope": bshd, sbhd; PR #3705: separate Q/K/V, compact
+ * THD with zero-based cumulative sequence lengths). Every tensor is
+ * contiguous in its layout:
+ *   SDPA_BSHD  [B, S, H, D]
+ *   SDPA_SBHD  [S, B, H, D]
+ *   SDPA_THD   [T, H, D]; sequence b owns rows cu_seqlens[b] .. cu_seqlens[b+1]-1
+ * The "token row" of a position is its index over the leading dimensions:
+ * b*S+s (BSHD), s*B+b (SBHD), cu_seqlens[b]+s (THD). LSE is float32
+ * [rows_q][Hq] indexed by Q's token row. dq/dk/dv have q/k/v's layout.
+ *
+ * Supported: dtype bf16 or fp16 (Q, K, V, O, dO, dQ, dK, dV share it);
+ * symmetric head_dim 128, 256 or 512; Hq a multiple of Hkv (q head h reads
+ * kv head h / (Hq/Hkv)); every device pointer 16-byte aligned.
+ *
+ * Ownership: the caller owns every buffer, the workspace and the stream.
+ * Pointers marked "device" must be device memory (cudaMalloc or torch);
+ * the library never allocates device memory inside sdpa_fwd / sdpa_bwd and
+ * never synchronises the stream there. Device-side faults in the inputs
+ * (bad cu_seqlens) and bounded-wait timeouts are recorded in a per-device
+ * error word that kernels check before writing outputs; read it with
+ * sdpa_get_device_error.
+ *
+ * Errors: every entry point returns an sdpa_status. Host-detectable problems
+ * are returned before anything is launched (an explicit decline, never a
+ * fallback to another implementation).
+ */
+#ifndef SDPA_GB300_H
+#define SDPA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SDPA_API __attribute__((visibility("default")))
+#else
+#define SDPA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  SDPA_OK = 0,
+  SDPA_ERR_INVALID_ARG = 1,      /* null pointer, negative size, inconsistent geometry */
+  SDPA_ERR_UNSUPPORTED = 2,      /* dtype, head_dim, layout or mask/window combination declined */
+  SDPA_ERR_ALIGNMENT = 3,        /* a pointer is not 16-byte aligned */
+  SDPA_ERR_OVERLAP = 4,          /* an output buffer overlaps an input or another output */
+  SDPA_ERR_WORKSPACE_TOO_SMALL = 5,
+  SDPA_ERR_BAD_SEQLENS = 6,      /* device-detected: cu_seqlens not compact / out of bounds */
+  SDPA_ERR_TIMEOUT = 7,          /* device-detected: a bounded wait inside a kernel gave up */
+  SDPA_ERR_CUDA = 8              /* a CUDA runtime or driver call failed */
+} sdpa_status;
+
+typedef enum { SDPA_BSHD = 0, SDPA_SBHD = 1, SDPA_THD = 2 } sdpa_layout;
+
+/* PR #3527 "Scope": mask types no_mask / causal / causal_bottom_right.
+ * Top-left: query i's diagonal is key i. Bottom-right: query i's diagonal is
+ * key i + Sk - Sq (per sequence for THD). */
+typedef enum {
+  SDPA_MASK_NONE = 0,
+  SDPA_MASK_CAUSAL_TOP_LEFT = 1,
+  SDPA_MASK_CAUSAL_BOTTOM_RIGHT = 2
+} sdpa_mask;
+
+typedef enum { SDPA_BF16 = 0, SDPA_FP16 = 1 } sdpa_dtype;
+
+typedef struct {
+  int layout;       /* sdpa_layout */
+  int dtype;        /* sdpa_dtype */
+  int mask_type;    /* sdpa_mask */
+  int batch;        /* B; THD: number of sequences */
+  int seqlen_q;     /* BSHD/SBHD: Sq. THD: the largest per-sequence q length (bounds the grid) */
+  int seqlen_kv;    /* BSHD/SBHD: Sk. THD: the largest per-sequence kv length */
+  int total_q;      /* THD only: rows of the packed q/o/dO/dq buffers (must equal cu_seqlens_q[B]) */
+  int total_kv;     /* THD only: rows of the packed k/v/dk/dv buffers (must equal cu_seqlens_kv[B]) */
+  int num_heads_q;  /* Hq */
+  int num_heads_kv; /* Hkv, divides Hq */
+  int head_dim;     /* D: 128, 256 or 512 */
+  int window_left;  /* keys allowed left of the diagonal; -1 = unbounded (PR #3693 window pair) */
+  int window_right; /* keys allowed right of the diagonal; -1 = unbounded; causal requires 0 or -1 */
+  float softmax_scale; /* multiplies Q K^T before the mask, e.g. 1/sqrt(D) */
+} sdpa_problem;
+
+/* Bytes of device workspace sdpa_fwd / sdpa_bwd need for this problem
+ * (0 when none). Returns 0 as well for a problem the library declines; call
+ * sdpa_check_problem to tell the two apart. */
+SDPA_API size_t sdpa_fwd_workspace_size(const sdpa_problem* p);
+SDPA_API size_t sdpa_bwd_workspace_size(const sdpa_problem* p);
+
+/* Host-side validation only (no CUDA call): SDPA_OK or the reason a call
+ * with this problem would be declined. Declined: head_dim not in
+ * {128,256,512}; Hq % Hkv != 0; a causal mask with window_right > 0; a
+ * bounded window on a non-causal mask when seqlen_q != seqlen_kv (PR #3527
+ * "Scope": the alignment of such a window is ambiguous, so it is declined
+ * rather than guessed). */
+SDPA_API int sdpa_check_problem(const sdpa_problem* p);
+
+/* Forward. q [.., Hq, D], k/v [.., Hkv, D] (device, read); o [.., Hq, D] and
+ * lse float32 [rows_q][Hq] (device, written). cu_seqlens_q/kv: device int32
+ * [B+1] for THD (checked on the device on every call: cu[0] == 0,
+ * non-decreasing, cu[B] == total, every length <= seqlen_q/seqlen_kv, and a
+ * non-empty kv sequence wherever the q sequence is non-empty -- PR #3705's
+ * compactness promise), NULL otherwise. workspace/ws_bytes: device scratch
+ * of at least sdpa_fwd_workspace_size bytes (may be NULL when that is 0).
+ * stream: a cudaStream_t (NULL = legacy default stream). Rows whose every
+ * key is masked get o = 0 and lse = -inf. */
+SDPA_API int sdpa_fwd(const sdpa_problem* p, const void* q, const void* k, const void* v, void* o, float* lse,
+             const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv, void* workspace, size_t ws_bytes,
+             void* stream);
+
+/* Backward. q, k, v, o, lse, dout as produced/consumed by sdpa_fwd (device,
+ * read); dq [.., Hq, D], dk, dv [.., Hkv, D] (device, written, fully
+ * overwritten). workspace: device scratch of at least
+ * sdpa_bwd_workspace_size bytes (float32 dQ accumulator and per-row
+ * statistics). dQ is accumulated with float32 atomics, so it is not bitwise
+ * reproducible run to run; dK and dV are. */
+SDPA_API int sdpa_bwd(const sdpa_problem* p, const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const void* dout, void* dq, void* dk, void* dv, const int32_t* cu_seqlens_q,
+             const int32_t* cu_seqlens_kv, void* workspace, size_t ws_bytes, void* stream);
+
+/* Synchronises `stream`, then returns and clears the current device's error
+ * word (SDPA_OK if no kernel recorded an error). */
+SDPA_API int sdpa_get_device_error(void* stream);
+
+/* Static description of a status code. */
+SDPA_API const char* sdpa_error_string(int status);
+
+/* Number of kernels the last successful sdpa_fwd / sdpa_bwd call on this
+ * host thread launched. */
+SDPA_API int sdpa_last_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SDPA_GB300_H */

@@ -1,0 +1,195 @@
+"""Python binding of libsdpa.so, the fused SDPA library for one GB300 GPU.
+
+The functions carry the C ABI's names (include/sdpa.h) and only marshal
+arguments: torch supplies device memory and the current CUDA stream, and every
+step of the computation runs in the library's CUDA kernels. There is no other
+implementation behind these calls: if libsdpa.so is missing, or the tensors
+are not CUDA tensors, the call raises.
+
+Layouts: "bshd" [B,S,H,D], "sbhd" [S,B,H,D], "thd" [T,H,D] (+ cu_seqlens).
+Masks: "none", "causal" (top-left), "causal_br" (bottom-right).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libsdpa.so")
+
+LAYOUTS = {"bshd": 0, "sbhd": 1, "thd": 2}
+MASKS = {"none": 0, "causal": 1, "causal_br": 2}
+STATUS = {0: "SDPA_OK", 1: "SDPA_ERR_INVALID_ARG", 2: "SDPA_ERR_UNSUPPORTED", 3: "SDPA_ERR_ALIGNMENT",
+          4: "SDPA_ERR_OVERLAP", 5: "SDPA_ERR_WORKSPACE_TOO_SMALL", 6: "SDPA_ERR_BAD_SEQLENS",
+          7: "SDPA_ERR_TIMEOUT", 8: "SDPA_ERR_CUDA"}
+EXPORTS = ("sdpa_fwd_workspace_size", "sdpa_bwd_workspace_size", "sdpa_check_problem", "sdpa_fwd", "sdpa_bwd",
+           "sdpa_get_device_error", "sdpa_error_string", "sdpa_last_launch_count")
+
+
+class SdpaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({error_string(status)})")
+
+
+class Problem(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int) for n in ("layout", "dtype", "mask_type", "batch", "seqlen_q", "seqlen_kv",
+                                            "total_q", "total_kv", "num_heads_q", "num_heads_kv", "head_dim",
+                                            "window_left", "window_right")] + [("softmax_scale", ctypes.c_float)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib():
+    """Load libsdpa.so (build it first with scaled_dot_product_02_gb300.build)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise ImportError(f"{LIB_PATH} is missing: run scaled_dot_product_02_gb300/build.py "
+                                  "(there is no fallback implementation)")
+            L = ctypes.CDLL(LIB_PATH)
+            vp, pp = ctypes.c_void_p, ctypes.POINTER(Problem)
+            L.sdpa_fwd_workspace_size.argtypes = [pp]
+            L.sdpa_fwd_workspace_size.restype = ctypes.c_size_t
+            L.sdpa_bwd_workspace_size.argtypes = [pp]
+            L.sdpa_bwd_workspace_size.restype = ctypes.c_size_t
+            L.sdpa_check_problem.argtypes = [pp]
+            L.sdpa_fwd.argtypes = [pp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+            L.sdpa_bwd.argtypes = [pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+            L.sdpa_get_device_error.argtypes = [vp]
+            L.sdpa_error_string.argtypes = [ctypes.c_int]
+            L.sdpa_error_string.restype = ctypes.c_char_p
+            L.sdpa_last_launch_count.restype = ctypes.c_int
+            _lib = L
+    return _lib
+
+
+def error_string(status: int) -> str:
+    return lib().sdpa_error_string(int(status)).decode()
+
+
+sdpa_error_string = error_string
+
+
+def make_problem(q, k, *, layout="bshd", mask="none", window=(-1, -1), scale=None, dtype=None, batch=None,
+                 max_seqlen_q=None, max_seqlen_kv=None) -> Problem:
+    """sdpa_problem from tensor shapes (no device access)."""
+    import torch
+
+    if dtype is None:
+        dtype = {torch.bfloat16: 0, torch.float16: 1}.get(q.dtype, -1)
+    d = q.shape[-1]
+    p = Problem()
+    p.layout, p.dtype, p.mask_type = LAYOUTS[layout], dtype, MASKS[mask]
+    if layout == "bshd":
+        p.batch, p.seqlen_q, p.num_heads_q = q.shape[0], q.shape[1], q.shape[2]
+        p.seqlen_kv, p.num_heads_kv = k.shape[1], k.shape[2]
+    elif layout == "sbhd":
+        p.seqlen_q, p.batch, p.num_heads_q = q.shape[0], q.shape[1], q.shape[2]
+        p.seqlen_kv, p.num_heads_kv = k.shape[0], k.shape[2]
+    else:
+        if batch is None or max_seqlen_q is None or max_seqlen_kv is None:
+            raise ValueError("thd needs batch, max_seqlen_q and max_seqlen_kv")
+        p.batch, p.seqlen_q, p.seqlen_kv = batch, max_seqlen_q, max_seqlen_kv
+        p.total_q, p.total_kv = q.shape[0], k.shape[0]
+        p.num_heads_q, p.num_heads_kv = q.shape[1], k.shape[1]
+    p.head_dim = d
+    p.window_left, p.window_right = int(window[0]), int(window[1])
+    p.softmax_scale = float(scale if scale is not None else d ** -0.5)
+    return p
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check_cuda(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("sdpa tensors must be CUDA tensors (there is no CPU implementation)")
+        if t is not None and not t.is_contiguous():
+            raise ValueError("sdpa tensors must be contiguous in their layout")
+
+
+def sdpa_check_problem(p: Problem) -> int:
+    return int(lib().sdpa_check_problem(ctypes.byref(p)))
+
+
+def sdpa_fwd_workspace_size(p: Problem) -> int:
+    return int(lib().sdpa_fwd_workspace_size(ctypes.byref(p)))
+
+
+def sdpa_bwd_workspace_size(p: Problem) -> int:
+    return int(lib().sdpa_bwd_workspace_size(ctypes.byref(p)))
+
+
+def sdpa_fwd(q, k, v, *, layout="bshd", mask="none", window=(-1, -1), scale=None, cu_seqlens_q=None,
+             cu_seqlens_kv=None, max_seqlen_q=None, max_seqlen_kv=None, out=None, lse=None, workspace=None,
+             stream=None):
+    """Forward. Returns (o, lse); lse is float32 [rows_q, Hq] token-major."""
+    import torch
+
+    batch = None if cu_seqlens_q is None else cu_seqlens_q.numel() - 1
+    p = make_problem(q, k, layout=layout, mask=mask, window=window, scale=scale, batch=batch,
+                     max_seqlen_q=max_seqlen_q, max_seqlen_kv=max_seqlen_kv)
+    rows_q = q.numel() // (q.shape[-1] * q.shape[-2])
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty((rows_q, q.shape[-2]), dtype=torch.float32, device=q.device)
+    need = sdpa_fwd_workspace_size(p)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check_cuda(q, k, v, out, lse, cu_seqlens_q, cu_seqlens_kv, workspace)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().sdpa_fwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q),
+                        _ptr(cu_seqlens_kv), _ptr(workspace), ws_bytes, _stream(stream))
+    if rc:
+        raise SdpaError(rc, "sdpa_fwd")
+    return out, lse
+
+
+def sdpa_bwd(q, k, v, o, lse, dout, *, layout="bshd", mask="none", window=(-1, -1), scale=None,
+             cu_seqlens_q=None, cu_seqlens_kv=None, max_seqlen_q=None, max_seqlen_kv=None, dq=None, dk=None,
+             dv=None, workspace=None, stream=None):
+    """Backward. Returns (dq, dk, dv)."""
+    import torch
+
+    batch = None if cu_seqlens_q is None else cu_seqlens_q.numel() - 1
+    p = make_problem(q, k, layout=layout, mask=mask, window=window, scale=scale, batch=batch,
+                     max_seqlen_q=max_seqlen_q, max_seqlen_kv=max_seqlen_kv)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    need = sdpa_bwd_workspace_size(p)
+    if workspace is None:
+        workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
+    _check_cuda(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens_q, cu_seqlens_kv, workspace)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    rc = lib().sdpa_bwd(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout), _ptr(dq),
+                        _ptr(dk), _ptr(dv), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv), _ptr(workspace), ws_bytes,
+                        _stream(stream))
+    if rc:
+        raise SdpaError(rc, "sdpa_bwd")
+    return dq, dk, dv
+
+
+def sdpa_get_device_error(stream=None) -> int:
+    """Synchronise the stream and return (and clear) the device error word."""
+    return int(lib().sdpa_get_device_error(_stream(stream)))
+
+
+def sdpa_last_launch_count() -> int:
+    return int(lib().sdpa_last_launch_count())

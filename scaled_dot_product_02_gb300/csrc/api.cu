@@ -1,0 +1,353 @@
+// api.cu -- the C ABI declared in include/sdpa.h: host-side validation,
+// TMA descriptor encoding, workspace carving and kernel launches. No call
+// here allocates device memory or synchronises, except
+// sdpa_get_device_error, which is documented to synchronise.
+#include <cudaTypedefs.h>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "../../include/sdpa.h"
+#include "kernels.h"
+
+// The per-device error word. Kernels receive its device address.
+static __device__ int g_sdpa_error_word;
+
+namespace sdpa {
+namespace {
+
+thread_local int t_last_launches = 0;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+int* error_word() {
+  static std::mutex mu;
+  static int* ptrs[128] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_sdpa_error_word) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int*>(p);
+  }
+  return ptrs[dev];
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct Extent {
+  uintptr_t lo, hi;
+};
+Extent extent(const void* p, size_t bytes) {
+  return {reinterpret_cast<uintptr_t>(p), reinterpret_cast<uintptr_t>(p) + bytes};
+}
+bool overlaps(Extent a, Extent b) { return a.lo < b.hi && b.lo < a.hi && a.hi > a.lo && b.hi > b.lo; }
+
+// Rows/heads of the generic row x head x D view (see common.cuh).
+void view(const sdpa_problem* p, int& rows_q, int& rows_kv, int& nh_q, int& nh_kv) {
+  if (p->layout == SDPA_THD) {
+    rows_q = p->total_q;
+    rows_kv = p->total_kv;
+    nh_q = p->num_heads_q;
+    nh_kv = p->num_heads_kv;
+  } else if (p->layout == SDPA_BSHD) {
+    rows_q = p->batch * p->seqlen_q;
+    rows_kv = p->batch * p->seqlen_kv;
+    nh_q = p->num_heads_q;
+    nh_kv = p->num_heads_kv;
+  } else {
+    rows_q = p->seqlen_q;
+    rows_kv = p->seqlen_kv;
+    nh_q = p->batch * p->num_heads_q;
+    nh_kv = p->batch * p->num_heads_kv;
+  }
+}
+
+bool causal(const sdpa_problem* p) { return p->mask_type != SDPA_MASK_NONE; }
+
+int check(const sdpa_problem* p) {
+  if (!p) return SDPA_ERR_INVALID_ARG;
+  if (p->layout < SDPA_BSHD || p->layout > SDPA_THD) return SDPA_ERR_INVALID_ARG;
+  if (p->dtype != SDPA_BF16 && p->dtype != SDPA_FP16) return SDPA_ERR_UNSUPPORTED;
+  if (p->mask_type < SDPA_MASK_NONE || p->mask_type > SDPA_MASK_CAUSAL_BOTTOM_RIGHT) return SDPA_ERR_INVALID_ARG;
+  if (p->batch < 0 || p->seqlen_q < 0 || p->seqlen_kv < 0) return SDPA_ERR_INVALID_ARG;
+  if (p->num_heads_q <= 0 || p->num_heads_kv <= 0) return SDPA_ERR_INVALID_ARG;
+  if (p->num_heads_q % p->num_heads_kv) return SDPA_ERR_INVALID_ARG;
+  if (p->head_dim != 128 && p->head_dim != 256 && p->head_dim != 512) return SDPA_ERR_UNSUPPORTED;
+  if (p->window_left < -1 || p->window_right < -1) return SDPA_ERR_INVALID_ARG;
+  if (causal(p) && p->window_right > 0) return SDPA_ERR_INVALID_ARG;
+  if (!causal(p) && (p->window_left >= 0 || p->window_right >= 0) && p->seqlen_q != p->seqlen_kv)
+    return SDPA_ERR_UNSUPPORTED;
+  if (!std::isfinite(p->softmax_scale)) return SDPA_ERR_INVALID_ARG;
+  if (p->layout == SDPA_THD) {
+    if (p->total_q < 0 || p->total_kv < 0) return SDPA_ERR_INVALID_ARG;
+  } else if (p->seqlen_q > 0 && p->seqlen_kv == 0 && p->batch > 0) {
+    return SDPA_ERR_INVALID_ARG;  // every query would attend an empty key set
+  }
+  int rq, rk, hq, hk;
+  view(p, rq, rk, hq, hk);
+  const long long q_elems = (long long)rq * hq * p->head_dim;
+  const long long k_elems = (long long)rk * hk * p->head_dim;
+  if (q_elems >= (1LL << 40) || k_elems >= (1LL << 40)) return SDPA_ERR_UNSUPPORTED;
+  if ((long long)p->batch * p->seqlen_q >= (1LL << 31) || (long long)p->batch * p->seqlen_kv >= (1LL << 31))
+    return SDPA_ERR_UNSUPPORTED;
+  return SDPA_OK;
+}
+
+Geom make_geom(const sdpa_problem* p, const int32_t* cu_q, const int32_t* cu_kv) {
+  Geom g;
+  g.layout = p->layout;
+  g.mask = p->mask_type;
+  g.batch = p->batch;
+  g.sq = p->seqlen_q;
+  g.sk = p->seqlen_kv;
+  g.hq = p->num_heads_q;
+  g.hkv = p->num_heads_kv;
+  g.d = p->head_dim;
+  g.wl = p->window_left;
+  g.wr = causal(p) ? 0 : p->window_right;
+  g.scale = p->softmax_scale;
+  g.scale_log2 = p->softmax_scale * 1.4426950408889634f;
+  view(p, g.rows_q, g.rows_kv, g.nh_q, g.nh_kv);
+  g.cu_q = cu_q;
+  g.cu_kv = cu_kv;
+  return g;
+}
+
+// 3-D map {D, heads, rows} over a contiguous [rows][heads][D] 16-bit tensor;
+// boxes are 64 columns (128 bytes, 128-byte swizzle) x 1 head x box_rows.
+int encode(CUtensorMap* m, const void* base, int d, int nh, int rows, int box_rows, bool bf16) {
+  auto fn = encode_fn();
+  if (!fn) return SDPA_ERR_CUDA;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)nh, (cuuint64_t)(rows > 0 ? rows : 1)};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)nh * d * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)box_rows};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                  const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SDPA_OK : SDPA_ERR_CUDA;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Backward workspace carve-up.
+struct BwdWs {
+  size_t guard_off, lse2_off, delta_off, acc_off, total;
+  int stat_rows;
+};
+BwdWs bwd_ws(const sdpa_problem* p) {
+  int rq, rk, hq, hk;
+  view(p, rq, rk, hq, hk);
+  BwdWs w;
+  w.stat_rows = (int)round_up((size_t)rq, 4) + 128;
+  w.guard_off = 0;
+  w.lse2_off = 256;
+  w.delta_off = round_up(w.lse2_off + (size_t)hq * w.stat_rows * 4, 256);
+  w.acc_off = round_up(w.delta_off + (size_t)hq * w.stat_rows * 4, 256);
+  w.total = round_up(w.acc_off + (size_t)hq * rq * p->head_dim * 4, 256);
+  return w;
+}
+
+}  // namespace
+}  // namespace sdpa
+
+using namespace sdpa;
+
+extern "C" {
+
+int sdpa_check_problem(const sdpa_problem* p) { return check(p); }
+
+size_t sdpa_fwd_workspace_size(const sdpa_problem* p) {
+  if (check(p) != SDPA_OK) return 0;
+  return p->layout == SDPA_THD ? 256 : 0;
+}
+
+size_t sdpa_bwd_workspace_size(const sdpa_problem* p) {
+  if (check(p) != SDPA_OK) return 0;
+  return bwd_ws(p).total;
+}
+
+int sdpa_fwd(const sdpa_problem* p, const void* q, const void* k, const void* v, void* o, float* lse,
+             const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv, void* workspace, size_t ws_bytes,
+             void* stream) {
+  t_last_launches = 0;
+  int rc = check(p);
+  if (rc) return rc;
+  int rq, rk, hq, hk;
+  view(p, rq, rk, hq, hk);
+  const bool thd = p->layout == SDPA_THD;
+  if (p->batch == 0 || rq == 0) return SDPA_OK;
+  if (!q || !k || !v || !o || !lse) return SDPA_ERR_INVALID_ARG;
+  if (thd && (!cu_seqlens_q || !cu_seqlens_kv)) return SDPA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || !aligned16(lse))
+    return SDPA_ERR_ALIGNMENT;
+  const size_t need = sdpa_fwd_workspace_size(p);
+  if (ws_bytes < need || (need && !workspace)) return SDPA_ERR_WORKSPACE_TOO_SMALL;
+  if (need && !aligned16(workspace)) return SDPA_ERR_ALIGNMENT;
+  const size_t qb = (size_t)rq * hq * p->head_dim * 2, kb = (size_t)rk * hk * p->head_dim * 2;
+  const Extent eo = extent(o, qb), el = extent(lse, (size_t)rq * hq * 4);
+  for (Extent in : {extent(q, qb), extent(k, kb), extent(v, kb)})
+    if (overlaps(eo, in) || overlaps(el, in)) return SDPA_ERR_OVERLAP;
+  if (overlaps(eo, el)) return SDPA_ERR_OVERLAP;
+  if (need && (overlaps(extent(workspace, need), eo) || overlaps(extent(workspace, need), el)))
+    return SDPA_ERR_OVERLAP;
+
+  int* err = error_word();
+  if (!err) return SDPA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool bf16 = p->dtype == SDPA_BF16;
+  FwdLaunch L;
+  std::memset(&L, 0, sizeof(L));
+  L.p.g = make_geom(p, cu_seqlens_q, cu_seqlens_kv);
+  L.p.o = o;
+  L.p.lse = lse;
+  L.p.err = err;
+  L.p.guard = thd ? static_cast<const int*>(workspace) : nullptr;
+  L.p.n_q_tiles = (p->seqlen_q + 127) / 128;
+  L.p.dv_splits = p->head_dim == 512 ? 2 : 1;
+  L.stream = s;
+  const int dv = p->head_dim == 128 ? 128 : 256;
+  if ((rc = encode(&L.tmQ, q, p->head_dim, hq, rq, 128, bf16))) return rc;
+  if ((rc = encode(&L.tmK, k, p->head_dim, hk, rk, 128, bf16))) return rc;
+  if ((rc = encode(&L.tmV, v, p->head_dim, hk, rk, 32768 / (dv * 2), bf16))) return rc;
+  int launches = 0;
+  if (thd) {
+    if ((rc = launch_guard(L.p.g, p->total_q, p->total_kv, static_cast<int*>(workspace), err, s))) return rc;
+    ++launches;
+  }
+  if ((rc = launch_fwd(L, p->head_dim, bf16))) return rc;
+  ++launches;
+  t_last_launches = launches;
+  return SDPA_OK;
+}
+
+int sdpa_bwd(const sdpa_problem* p, const void* q, const void* k, const void* v, const void* o, const float* lse,
+             const void* dout, void* dq, void* dk, void* dv, const int32_t* cu_seqlens_q,
+             const int32_t* cu_seqlens_kv, void* workspace, size_t ws_bytes, void* stream) {
+  t_last_launches = 0;
+  int rc = check(p);
+  if (rc) return rc;
+  int rq, rk, hq, hk;
+  view(p, rq, rk, hq, hk);
+  const bool thd = p->layout == SDPA_THD;
+  if (p->batch == 0 || (rq == 0 && rk == 0)) return SDPA_OK;
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv) return SDPA_ERR_INVALID_ARG;
+  if (thd && (!cu_seqlens_q || !cu_seqlens_kv)) return SDPA_ERR_INVALID_ARG;
+  for (const void* ptr : {q, k, v, o, (const void*)lse, dout, (const void*)dq, (const void*)dk, (const void*)dv})
+    if (!aligned16(ptr)) return SDPA_ERR_ALIGNMENT;
+  const BwdWs w = bwd_ws(p);
+  if (ws_bytes < w.total || !workspace) return SDPA_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned16(workspace) || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return SDPA_ERR_ALIGNMENT;
+  const size_t qb = (size_t)rq * hq * p->head_dim * 2, kb = (size_t)rk * hk * p->head_dim * 2;
+  const Extent outs[4] = {extent(dq, qb), extent(dk, kb), extent(dv, kb), extent(workspace, w.total)};
+  const Extent ins[6] = {extent(q, qb), extent(k, kb), extent(v, kb), extent(o, qb), extent(lse, (size_t)rq * hq * 4),
+                         extent(dout, qb)};
+  for (int a = 0; a < 4; ++a) {
+    for (int b = 0; b < 6; ++b)
+      if (overlaps(outs[a], ins[b])) return SDPA_ERR_OVERLAP;
+    for (int b = a + 1; b < 4; ++b)
+      if (overlaps(outs[a], outs[b])) return SDPA_ERR_OVERLAP;
+  }
+
+  int* err = error_word();
+  if (!err) return SDPA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool bf16 = p->dtype == SDPA_BF16;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int* guard = thd ? reinterpret_cast<int*>(ws + w.guard_off) : nullptr;
+  float* lse2 = reinterpret_cast<float*>(ws + w.lse2_off);
+  float* delta = reinterpret_cast<float*>(ws + w.delta_off);
+  float* acc = reinterpret_cast<float*>(ws + w.acc_off);
+  const Geom g = make_geom(p, cu_seqlens_q, cu_seqlens_kv);
+  int launches = 0;
+  if (thd) {
+    if ((rc = launch_guard(g, p->total_q, p->total_kv, guard, err, s))) return rc;
+    ++launches;
+  }
+  PrepParams pp;
+  pp.g = g;
+  pp.o = o;
+  pp.dout = dout;
+  pp.lse = lse;
+  pp.lse2 = lse2;
+  pp.delta = delta;
+  pp.stat_rows = w.stat_rows;
+  pp.dq_acc = acc;
+  pp.guard = guard;
+  if ((rc = launch_preprocess(pp, bf16, s))) return rc;
+  ++launches;
+
+  BwdLaunch L;
+  std::memset(&L, 0, sizeof(L));
+  L.p.g = g;
+  L.p.dq_acc = acc;
+  L.p.lse2 = lse2;
+  L.p.delta = delta;
+  L.p.stat_rows = w.stat_rows;
+  L.p.dk = dk;
+  L.p.dv = dv;
+  L.p.err = err;
+  L.p.guard = guard;
+  L.p.n_kv_tiles = (p->seqlen_kv + 127) / 128;
+  L.stream = s;
+  if ((rc = encode(&L.tmQ, q, p->head_dim, hq, rq, 64, bf16))) return rc;
+  if ((rc = encode(&L.tmDO, dout, p->head_dim, hq, rq, 64, bf16))) return rc;
+  if ((rc = encode(&L.tmK, k, p->head_dim, hk, rk, 128, bf16))) return rc;
+  if ((rc = encode(&L.tmV, v, p->head_dim, hk, rk, 128, bf16))) return rc;
+  int n = 0;
+  if ((rc = launch_bwd_dkdv(L, p->head_dim, bf16, &n))) return rc;
+  launches += n;
+  if ((rc = launch_dq_finalize(g, acc, dq, guard, bf16, s))) return rc;
+  ++launches;
+  t_last_launches = launches;
+  return SDPA_OK;
+}
+
+int sdpa_get_device_error(void* stream) {
+  int* err = error_word();
+  if (!err) return SDPA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return SDPA_ERR_CUDA;
+  int host = 0;
+  if (cudaMemcpyFromSymbol(&host, g_sdpa_error_word, sizeof(int)) != cudaSuccess) return SDPA_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpyToSymbol(g_sdpa_error_word, &zero, sizeof(int)) != cudaSuccess) return SDPA_ERR_CUDA;
+  return host;
+}
+
+const char* sdpa_error_string(int status) {
+  switch (status) {
+    case SDPA_OK: return "ok";
+    case SDPA_ERR_INVALID_ARG: return "invalid argument";
+    case SDPA_ERR_UNSUPPORTED: return "unsupported problem (dtype, head_dim, layout or mask/window combination)";
+    case SDPA_ERR_ALIGNMENT: return "a device pointer is not 16-byte aligned";
+    case SDPA_ERR_OVERLAP: return "an output buffer overlaps another buffer";
+    case SDPA_ERR_WORKSPACE_TOO_SMALL: return "workspace missing or smaller than the required size";
+    case SDPA_ERR_BAD_SEQLENS: return "cu_seqlens rejected by the device-side guard";
+    case SDPA_ERR_TIMEOUT: return "a bounded wait inside a kernel gave up";
+    case SDPA_ERR_CUDA: return "a CUDA runtime or driver call failed";
+    default: return "unknown status";
+  }
+}
+
+int sdpa_last_launch_count(void) { return t_last_launches; }
+
+}  // extern "C"

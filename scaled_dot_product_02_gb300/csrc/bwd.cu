@@ -1,0 +1,457 @@
+// bwd.cu -- fused attention backward for sm_103a, head_dim 128.
+//
+// One CTA owns one 128-key tile of one (batch, kv head). K and V stay in
+// shared memory; the CTA walks every q head of the GQA group and every
+// 64-row query tile that can attend its keys, so dK and dV accumulate in
+// TMEM without atomics. Per query tile (all MMAs tcgen05, fp32 in TMEM):
+//   S^T  = K Q^T                 (SS, M=128 keys, N=64 queries)
+//   dP^T = V dO^T                (SS)
+//   softmax warps: P^T = exp2(S^T*scale*log2e - LSE*log2e), masked,
+//                  dS^T = P^T * (dP^T - delta); both written back to TMEM as
+//                  16-bit values, dS^T also to shared memory
+//   dV  += P^T dO                (TS, A = P^T from TMEM)
+//   dK  += dS^T Q                (TS)
+//   dQ^T = K^T dS^T              (SS, M=128 head-dim rows, N=64 queries)
+//   drain warps: dQ^T -> shared memory -> bulk reduce-add (fp32) into the
+//                head-major dQ accumulator; a finalise kernel scales and casts.
+// The MMA order dV(i), dK(i), S(i+1), dP(i+1), dQ(i) lets the softmax of tile
+// i+1 overlap dQ(i). dQ accumulation uses no inter-CTA barriers or credits:
+// every contribution is an independent fp32 reduction.
+//
+// Roles (384 threads): warp 0 TMA producer; warp 1 TMEM allocator + MMA
+// issuer; warps 4-7 softmax (one thread per key row) and the dK/dV
+// epilogue; warps 8-11 dQ drain (one thread per head-dim row).
+// TMEM: dV [0,128) dK [128,256) S^T/P^T [256,320) dP^T/dS^T [320,384)
+//       dQ^T [384,448).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace sdpa {
+
+namespace {
+
+constexpr int BN = 128;  // keys per CTA
+constexpr int BQ = 64;   // queries per step
+constexpr int D = 128;
+constexpr int K_BYTES = BN * D * 2;   // 32 KB, two 64-column atoms of 16 KB
+constexpr int QT_BYTES = BQ * D * 2;  // 16 KB, two atoms of 8 KB
+constexpr int STAT_FLOATS = 68;       // 64 rows + up to 3 of alignment slack + 1
+constexpr int NQS = 2;                // Q/dO stages
+constexpr int DS_BYTES = BN * BQ * 2; // 16 KB
+constexpr int STG_BYTES = BQ * D * 4; // 32 KB fp32 dQ staging
+
+constexpr int OFF_K = 0;
+constexpr int OFF_V = OFF_K + K_BYTES;
+constexpr int OFF_Q = OFF_V + K_BYTES;                   // NQS x 16 KB
+constexpr int OFF_DO = OFF_Q + NQS * QT_BYTES;           // NQS x 16 KB
+constexpr int OFF_DS = OFF_DO + NQS * QT_BYTES;          // 2 x 16 KB
+constexpr int OFF_STG = OFF_DS + 2 * DS_BYTES;           // 32 KB
+constexpr int OFF_STAT = OFF_STG + STG_BYTES;            // NQS x (lse2, delta) x 68 floats
+constexpr int OFF_BAR = OFF_STAT + NQS * 2 * STAT_FLOATS * 4;
+constexpr int NBARS = 2 * NQS + 8;
+constexpr int SMEM_BYTES = 1024 + OFF_BAR + NBARS * 8 + 16;
+
+constexpr uint32_t TM_DV = 0, TM_DK = 128, TM_S = 256, TM_DP = 320, TM_DQ = 384;
+
+__device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity) {
+  uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > 200000000ull) return false;
+  return true;
+}
+
+__device__ __forceinline__ void fence_regs(uint32_t (&r)[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+
+__device__ __forceinline__ void named_barrier(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+}  // namespace
+
+template <bool BF16>
+__global__ void __launch_bounds__(384, 1)
+    bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
+               const __grid_constant__ BwdParams p) {
+  using E = Elem<BF16>;
+  using T = typename E::T;
+  const Geom& g = p.g;
+
+  // ---- which tile: first key tiles first (they have the most queries under a causal mask)
+  int idx = blockIdx.x;
+  const int kvh = idx % g.hkv;
+  idx /= g.hkv;
+  const int b = idx % g.batch;
+  const int kt = idx / g.batch;
+  const SeqInfo si = seq_info(g, b);
+  const int k0 = kt * BN;
+  if (k0 >= si.lk) return;
+  if (p.guard && *reinterpret_cast<volatile const int*>(p.guard)) return;
+
+  const KeyRange kr = key_range(g, si.lq, si.lk);
+  const int k_last = min(k0 + BN - 1, si.lk - 1);
+  const int qlo = query_lo(kr, k0), qhi = query_hi(kr, k_last, si.lq);
+  const int qt_lo = qlo / BQ;
+  const int nqt = qhi > qlo ? (qhi + BQ - 1) / BQ - qt_lo : 0;
+  const int group = g.hq / g.hkv;
+  const int n = nqt * group;
+  const int khead = si.khead0 + kvh;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float* sstat = reinterpret_cast<float*>(smem + OFF_STAT);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
+  uint64_t* full = bars;            // [NQS]
+  uint64_t* empty = bars + NQS;     // [NQS]
+  uint64_t* bar_kv = bars + 2 * NQS;
+  uint64_t* bar_sdp = bar_kv + 1;
+  uint64_t* bar_ds = bar_sdp + 1;
+  uint64_t* bar_dq = bar_ds + 1;
+  uint64_t* bar_dqfree = bar_dq + 1;
+  uint64_t* bar_final = bar_dqfree + 1;
+  uint64_t* bar_drain = bar_final + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + NBARS);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  // (head in group, query tile) of step i
+  auto step_head = [&](int i) { return kvh * group + i / nqt; };
+  auto step_q0 = [&](int i) { return (qt_lo + i % nqt) * BQ; };
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < NQS; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    mbar_init(bar_kv, 1);
+    mbar_init(bar_sdp, 1);
+    mbar_init(bar_ds, 128);
+    mbar_init(bar_dq, 1);
+    mbar_init(bar_dqfree, 128);
+    mbar_init(bar_final, 1);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (elect_one() && n > 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      prefetch_tmap(&tmDO);
+      mbar_arrive_expect_tx(bar_kv, 2 * K_BYTES);
+      const int krow = si.krow0 + k0;
+      tma_load_3d(&tmK, bar_kv, smem + OFF_K, 0, khead, krow);
+      tma_load_3d(&tmK, bar_kv, smem + OFF_K + 16384, 64, khead, krow);
+      tma_load_3d(&tmV, bar_kv, smem + OFF_V, 0, khead, krow);
+      tma_load_3d(&tmV, bar_kv, smem + OFF_V + 16384, 64, khead, krow);
+      int i = 0;
+      for (; i < n; ++i) {
+        const int st = i % NQS;
+        if (!mbar_wait(&empty[st], ((i / NQS) & 1) ^ 1, abort_flag)) break;
+        const int qhead = si.qhead0 + step_head(i);
+        const int row0 = si.qrow0 + step_q0(i);
+        const int arow = row0 & ~3;
+        mbar_arrive_expect_tx(&full[st], 2 * QT_BYTES + 2 * STAT_FLOATS * 4);
+        uint8_t* sq = smem + OFF_Q + st * QT_BYTES;
+        uint8_t* sd = smem + OFF_DO + st * QT_BYTES;
+        tma_load_3d(&tmQ, &full[st], sq, 0, qhead, row0);
+        tma_load_3d(&tmQ, &full[st], sq + 8192, 64, qhead, row0);
+        tma_load_3d(&tmDO, &full[st], sd, 0, qhead, row0);
+        tma_load_3d(&tmDO, &full[st], sd + 8192, 64, qhead, row0);
+        const long long so = (long long)qhead * p.stat_rows + arow;
+        bulk_load(sstat + st * 2 * STAT_FLOATS, p.lse2 + so, STAT_FLOATS * 4, &full[st]);
+        bulk_load(sstat + st * 2 * STAT_FLOATS + STAT_FLOATS, p.delta + so, STAT_FLOATS * 4, &full[st]);
+      }
+      if (i < n) {
+        *abort_flag = 1;
+        record_error(p.err, SDPA_ERR_TIMEOUT);
+      }
+      wait_drain(bar_kv, 0);
+      for (int k = (i > NQS ? i - NQS : 0); k < i; ++k) wait_drain(&full[k % NQS], (k / NQS) & 1);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (elect_one() && n > 0) {
+      constexpr uint32_t ID_S = idesc_f16(128, BQ, BF16, false, false);     // S^T, dP^T
+      constexpr uint32_t ID_KV = idesc_f16(128, D, BF16, false, true);      // dV, dK (B = dO/Q, N-major)
+      constexpr uint32_t ID_DQ = idesc_f16(128, BQ, BF16, true, true);      // dQ^T (A = K^T, B = dS^T)
+      const uint32_t sK = smem_u32(smem + OFF_K), sV = smem_u32(smem + OFF_V);
+      bool ok = mbar_wait(bar_kv, 0, abort_flag);
+      auto issue_sdp = [&](int i) -> bool {
+        const int st = i % NQS;
+        if (!mbar_wait(&full[st], (i / NQS) & 1, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t sq = smem_u32(smem + OFF_Q + st * QT_BYTES);
+        const uint32_t sd = smem_u32(smem + OFF_DO + st * QT_BYTES);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t ka = (ks >> 2) * 16384 + (ks & 3) * 32;
+          const uint32_t qa = (ks >> 2) * 8192 + (ks & 3) * 32;
+          mma_ss(tmem + TM_S, smem_desc_sw128(sK + ka, 16, 1024), smem_desc_sw128(sq + qa, 16, 1024), ID_S, ks > 0);
+        }
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t ka = (ks >> 2) * 16384 + (ks & 3) * 32;
+          const uint32_t qa = (ks >> 2) * 8192 + (ks & 3) * 32;
+          mma_ss(tmem + TM_DP, smem_desc_sw128(sV + ka, 16, 1024), smem_desc_sw128(sd + qa, 16, 1024), ID_S, ks > 0);
+        }
+        mma_commit(bar_sdp);
+        return true;
+      };
+      tc_fence_after();
+      if (ok) ok = issue_sdp(0);
+      for (int i = 0; i < n && ok; ++i) {
+        const int st = i % NQS;
+        if (!mbar_wait(bar_ds, i & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sq = smem_u32(smem + OFF_Q + st * QT_BYTES);
+        const uint32_t sd = smem_u32(smem + OFF_DO + st * QT_BYTES);
+#pragma unroll
+        for (int ks = 0; ks < BQ / 16; ++ks)
+          mma_ts(tmem + TM_DV, tmem + TM_S + ks * 8, smem_desc_sw128(sd + ks * 2048, 8192, 1024), ID_KV,
+                 (i | ks) != 0);
+#pragma unroll
+        for (int ks = 0; ks < BQ / 16; ++ks)
+          mma_ts(tmem + TM_DK, tmem + TM_DP + ks * 8, smem_desc_sw128(sq + ks * 2048, 8192, 1024), ID_KV,
+                 (i | ks) != 0);
+        mma_commit(&empty[st]);
+        if (i + 1 < n && !issue_sdp(i + 1)) {
+          ok = false;
+          break;
+        }
+        if (i >= 1 && !mbar_wait(bar_dqfree, (i - 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t sds = smem_u32(smem + OFF_DS + (i & 1) * DS_BYTES);
+#pragma unroll
+        for (int ks = 0; ks < BN / 16; ++ks)
+          mma_ss(tmem + TM_DQ, smem_desc_sw128(sK + ks * 2048, 16384, 1024),
+                 smem_desc_sw128(sds + ks * 2048, 16384, 1024), ID_DQ, ks > 0);
+        mma_commit(bar_dq);
+      }
+      if (ok) {
+        mma_commit(bar_final);
+      } else {
+        *abort_flag = 1;
+        record_error(p.err, SDPA_ERR_TIMEOUT);
+        mma_commit(bar_drain);
+        wait_drain(bar_drain, 0);
+      }
+    }
+  } else if (warp >= 4 && warp < 8) {
+    // ------------------------------------------------------------ softmax
+    const int wq = warp - 4;
+    const int r = wq * 32 + lane;  // key row in the tile
+    const int j = k0 + r;
+    const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
+    const float sl2 = g.scale_log2;
+    const bool key_ok = j < si.lk;
+    const int my_qlo = key_ok ? query_lo(kr, j) : 0;
+    const int my_qhi = key_ok ? query_hi(kr, j, si.lq) : 0;
+    const int lo_last = query_lo(kr, k_last), hi_first = query_hi(kr, k0, si.lq);
+    bool ok = true;
+    for (int i = 0; i < n; ++i) {
+      const int st = i % NQS;
+      const int q0 = step_q0(i);
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_sdp, i & 1, abort_flag) &&
+                                       mbar_wait(&full[st], (i / NQS) & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const bool interior = (k0 + BN <= si.lk) && (q0 + BQ <= si.lq) && lo_last <= q0 && hi_first >= q0 + BQ;
+      const int row0 = si.qrow0 + q0;
+      const float* lse2 = sstat + st * 2 * STAT_FLOATS + (row0 & 3);
+      const float* delta = lse2 + STAT_FLOATS;
+      uint8_t* ds_row = smem + OFF_DS + (i & 1) * DS_BYTES + r * 128;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t us[32], ud[32];
+        tmem_ld32(lane_base + TM_S + half * 32, us);
+        tmem_ld32(lane_base + TM_DP + half * 32, ud);
+        tmem_wait_ld();
+        fence_regs(us);
+        fence_regs(ud);
+        uint32_t pp[16], pd[16];
+#pragma unroll
+        for (int c = 0; c < 32; c += 2) {
+          float pv[2], dv[2];
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int cc = half * 32 + c + e;
+            const int q = q0 + cc;
+            const bool allowed = interior || (q >= my_qlo && q < my_qhi);
+            const float pt = allowed ? ex2(fmaf(__uint_as_float(us[c + e]), sl2, -lse2[cc])) : 0.f;
+            pv[e] = pt;
+            dv[e] = pt * (__uint_as_float(ud[c + e]) - delta[cc]);
+          }
+          pp[c / 2] = E::pack(pv[0], pv[1]);
+          pd[c / 2] = E::pack(dv[0], dv[1]);
+        }
+        tmem_st16(lane_base + TM_S + half * 16, pp);
+        tmem_st16(lane_base + TM_DP + half * 16, pd);
+        // dS^T row r, queries [32*half, 32*half+32): four 16-byte chunks,
+        // placed with the 128-byte swizzle (chunk ^ (row % 8)).
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int chunk = half * 4 + k;
+          *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) * 16)) =
+              make_uint4(pd[4 * k], pd[4 * k + 1], pd[4 * k + 2], pd[4 * k + 3]);
+        }
+      }
+      fence_proxy_async_smem();
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_ds);
+    }
+    if (ok && n > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_final, 0, abort_flag));
+      tc_fence_after();
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      record_error(p.err, SDPA_ERR_TIMEOUT);
+    } else {
+      // dK (scaled) and dV rows of this key
+      T* dvrow = reinterpret_cast<T*>(p.dv) + ((long long)(si.krow0 + j) * g.nh_kv + khead) * D;
+      T* dkrow = reinterpret_cast<T*>(p.dk) + ((long long)(si.krow0 + j) * g.nh_kv + khead) * D;
+#pragma unroll 1
+      for (int which = 0; which < 2; ++which) {
+        T* dst = which ? dkrow : dvrow;
+        const float mul = which ? g.scale : 1.f;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t packed[16];
+          if (n > 0) {
+            uint32_t u[32];
+            tmem_ld32(lane_base + (which ? TM_DK : TM_DV) + c * 32, u);
+            tmem_wait_ld();
+            fence_regs(u);
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              packed[e] = E::pack(__uint_as_float(u[2 * e]) * mul, __uint_as_float(u[2 * e + 1]) * mul);
+          } else {
+#pragma unroll
+            for (int e = 0; e < 16; ++e) packed[e] = 0u;
+          }
+          if (key_ok) {
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              d4[e] = make_uint4(packed[4 * e], packed[4 * e + 1], packed[4 * e + 2], packed[4 * e + 3]);
+          }
+        }
+      }
+    }
+  } else if (warp >= 8) {
+    // ------------------------------------------------------------ dQ drain
+    const int wq = warp - 8;
+    const int dcol = wq * 32 + lane;  // head-dim row of dQ^T
+    const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
+    float* stg = reinterpret_cast<float*>(smem + OFF_STG);
+    const bool leader = threadIdx.x == 256;
+    bool ok = true;
+    for (int i = 0; i < n; ++i) {
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_dq, i & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t u0[32], u1[32];
+      tmem_ld32(lane_base + TM_DQ, u0);
+      tmem_ld32(lane_base + TM_DQ + 32, u1);
+      tmem_wait_ld();
+      fence_regs(u0);
+      fence_regs(u1);
+      tc_fence_before();
+      mbar_arrive(bar_dqfree);
+      if (leader) bulk_wait_group_read0();
+      named_barrier(1, 128);
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        stg[c * D + dcol] = __uint_as_float(u0[c]);
+        stg[(32 + c) * D + dcol] = __uint_as_float(u1[c]);
+      }
+      fence_proxy_async_smem();
+      named_barrier(1, 128);
+      if (leader) {
+        const int q0 = step_q0(i);
+        const int rows = min(BQ, si.lq - q0);
+        if (rows > 0) {
+          const int qhead = si.qhead0 + step_head(i);
+          float* dst = p.dq_acc + ((long long)qhead * g.rows_q + si.qrow0 + q0) * D;
+          bulk_reduce_add_f32(dst, stg, rows * D * 4);
+          bulk_commit_group();
+        }
+      }
+    }
+    if (leader) bulk_wait_group0();
+    if (!ok) {
+      *abort_flag = 1;
+      record_error(p.err, SDPA_ERR_TIMEOUT);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <bool BF16>
+static int launch_t(const BwdLaunch& L) {
+  auto kern = bwd_kernel<BF16>;
+  static bool attr = false;
+  if (!attr) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
+      return SDPA_ERR_CUDA;
+    attr = true;
+  }
+  const long long grid = (long long)L.p.n_kv_tiles * L.p.g.hkv * L.p.g.batch;
+  if (grid <= 0) return SDPA_OK;
+  if (grid > 0x7fffffffLL) return SDPA_ERR_UNSUPPORTED;
+  kern<<<(unsigned)grid, 384, SMEM_BYTES, L.stream>>>(L.tmQ, L.tmK, L.tmV, L.tmDO, L.p);
+  return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+}
+
+int launch_bwd_dkdv(const BwdLaunch& L, int head_dim, bool bf16, int* launches) {
+  *launches = 0;
+  if (head_dim != 128) return SDPA_ERR_UNSUPPORTED;
+  const int rc = bf16 ? launch_t<true>(L) : launch_t<false>(L);
+  if (rc == SDPA_OK) *launches = 1;
+  return rc;
+}
+
+}  // namespace sdpa

@@ -1,0 +1,115 @@
+// common.cuh -- geometry shared by the kernels: the generic "rows x heads x D"
+// view of every layout, per-sequence bounds, and the mask/window ranges.
+#pragma once
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "../../include/sdpa.h"
+
+namespace sdpa {
+
+// Every layout is addressed as x[row][head][d] with
+//   BSHD: row = b*S + s, head = h           (rows = B*S, heads = H)
+//   SBHD: row = s,       head = b*H + h     (rows = S,   heads = B*H)
+//   THD:  row = cu[b]+s, head = h           (rows = T,   heads = H)
+// so one 3-D TMA tensor map {D, heads, rows} serves all three, and the
+// token-major LSE index is row*heads + head.
+struct Geom {
+  int layout, mask, batch, sq, sk;  // THD: sq/sk are the largest lengths
+  int hq, hkv, d;
+  int wl, wr;  // window; wr == 0 for causal masks, < 0 = unbounded
+  float scale, scale_log2;
+  int rows_q, rows_kv;  // rows of the generic view
+  int nh_q, nh_kv;      // heads of the generic view
+  const int32_t* cu_q;
+  const int32_t* cu_kv;
+};
+
+struct SeqInfo {
+  int lq, lk;          // lengths of this sequence
+  int qrow0, krow0;    // first generic row
+  int qhead0, khead0;  // generic head offset
+};
+
+__device__ __forceinline__ SeqInfo seq_info(const Geom& g, int b) {
+  SeqInfo s;
+  if (g.layout == SDPA_THD) {
+    s.qrow0 = g.cu_q[b];
+    s.lq = g.cu_q[b + 1] - s.qrow0;
+    s.krow0 = g.cu_kv[b];
+    s.lk = g.cu_kv[b + 1] - s.krow0;
+    s.qhead0 = s.khead0 = 0;
+  } else if (g.layout == SDPA_BSHD) {
+    s.lq = g.sq;
+    s.lk = g.sk;
+    s.qrow0 = b * g.sq;
+    s.krow0 = b * g.sk;
+    s.qhead0 = s.khead0 = 0;
+  } else {
+    s.lq = g.sq;
+    s.lk = g.sk;
+    s.qrow0 = s.krow0 = 0;
+    s.qhead0 = b * g.hq;
+    s.khead0 = b * g.hkv;
+  }
+  return s;
+}
+
+// Keys allowed for query i of a sequence with lengths (lq, lk): [lo, hi).
+// The diagonal of row i is key i (top-left, and no-mask windows) or
+// i + lk - lq (bottom-right).
+struct KeyRange {
+  int off, wl, wr, lk;
+  __device__ __forceinline__ int lo(int i) const { return wl >= 0 ? max(0, i + off - wl) : 0; }
+  __device__ __forceinline__ int hi(int i) const { return wr >= 0 ? min(lk, max(0, i + off + wr + 1)) : lk; }
+};
+
+__device__ __forceinline__ KeyRange key_range(const Geom& g, int lq, int lk) {
+  KeyRange r;
+  r.off = (g.mask == SDPA_MASK_CAUSAL_BOTTOM_RIGHT) ? lk - lq : 0;
+  r.wl = g.wl;
+  r.wr = g.wr;
+  r.lk = lk;
+  return r;
+}
+
+// Queries that may attend key j: [qlo, qhi) (the inverse of KeyRange).
+__device__ __forceinline__ int query_lo(const KeyRange& r, int j) { return r.wr >= 0 ? max(0, j - r.off - r.wr) : 0; }
+__device__ __forceinline__ int query_hi(const KeyRange& r, int j, int lq) {
+  return r.wl >= 0 ? min(lq, max(0, j - r.off + r.wl + 1)) : lq;
+}
+
+template <bool BF16>
+struct Elem;
+template <>
+struct Elem<true> {
+  using T = __nv_bfloat16;
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+  static __device__ __forceinline__ float2 unpack(uint32_t u) {
+    __nv_bfloat162 v = *reinterpret_cast<__nv_bfloat162*>(&u);
+    return __bfloat1622float2(v);
+  }
+};
+template <>
+struct Elem<false> {
+  using T = __half;
+  static __device__ __forceinline__ uint32_t pack(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+  static __device__ __forceinline__ float2 unpack(uint32_t u) {
+    __half2 v = *reinterpret_cast<__half2*>(&u);
+    return __half22float2(v);
+  }
+};
+
+// Record `code` in the device error word unless an error is already there.
+__device__ __forceinline__ void record_error(int* err, int code) {
+  if (err) atomicCAS(err, 0, code);
+}
+
+}  // namespace sdpa

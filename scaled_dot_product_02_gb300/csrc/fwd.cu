@@ -1,0 +1,422 @@
+// fwd.cu -- fused attention forward for sm_103a.
+//
+// One CTA owns one 128-row query tile of one (batch, q head) and, for
+// head_dim 512, one half of the value columns (the "D-split": both halves
+// recompute S = Q K^T over the full head dim, each accumulates half of O, so
+// O never needs more than 256 TMEM columns).
+//
+// Roles (256 threads):
+//   warp 0      TMA producer: Q once, then K/V tiles through a ring of 32 KB
+//               stages, in exactly the order the MMA warp consumes them.
+//   warp 1      TMEM allocator and MMA issuer (one elected thread):
+//                 S_j = Q K_j^T  (SS MMA, fp32 in TMEM, double-buffered)
+//                 O  += P_j V_j  (TS MMA, P read from TMEM)
+//               issued as S_0, S_1, PV_0, S_2, PV_1, ... so that S_{j+1} runs
+//               on the tensor pipe while the softmax warps work on S_j.
+//   warps 4-7   softmax: one thread per query row. Loads S_j from TMEM,
+//               masks edge tiles, keeps a running row max m and sum l,
+//               writes P_j = exp2((S_j - m) * scale * log2 e) as 16-bit values
+//               back into the S_j columns, and rescales O in TMEM only when
+//               the max grew by more than 2^8 (otherwise P stays <= 256).
+//               Epilogue: O / l to global memory, LSE = m*scale + ln l.
+// The TMEM plan: O at columns [0, DV), S/P buffers at DV and DV+128; with
+// DV <= 256 this fits the 512 columns of one SM.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "ptx.cuh"
+#include "kernels.h"
+
+namespace sdpa {
+
+template <int DQK, int DV>
+struct FwdCfg {
+  static constexpr int BM = 128, BN = 128;
+  static constexpr int STAGE_BYTES = 32768;
+  static constexpr int Q_BYTES = DQK * 256;  // 128 rows x DQK x 2 bytes
+  static constexpr int NSTAGES = DQK == 128 ? 5 : (DQK == 256 ? 4 : 3);
+  static constexpr int KST = DQK / 128;                    // K stages per tile (128 keys x 128 d each)
+  static constexpr int VROWS = STAGE_BYTES / (DV * 2);     // keys per V stage
+  static constexpr int VST = BN / VROWS;                   // V stages per tile
+  static constexpr int V_ATOM_BYTES = VROWS * 128;         // one 64-column swizzle atom of a V stage
+  static constexpr int TMEM_O = 0, TMEM_S = DV;
+  static constexpr int NBARS = 2 * NSTAGES + 7;
+  static constexpr int SMEM_BYTES = 1024 + Q_BYTES + NSTAGES * STAGE_BYTES + NBARS * 8 + 16;
+};
+
+// Waits that must not be cut short by the abort flag (draining copies or
+// MMAs that are already in flight before the CTA exits).
+__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
+  uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > 200000000ull) return false;
+  return true;
+}
+
+// Keep the compiler from moving uses of TMEM-loaded registers above the wait.
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+
+template <int DQK, int DV, bool BF16>
+__global__ void __launch_bounds__(256, 1)
+    fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+               const __grid_constant__ CUtensorMap tmV, const __grid_constant__ FwdParams p) {
+  using C = FwdCfg<DQK, DV>;
+  using E = Elem<BF16>;
+  const Geom& g = p.g;
+
+  // ---- which tile: heaviest (last) query tiles first, GQA heads adjacent
+  int idx = blockIdx.x;
+  const int split = idx % p.dv_splits;
+  idx /= p.dv_splits;
+  const int h = idx % g.hq;
+  idx /= g.hq;
+  const int b = idx % g.batch;
+  idx /= g.batch;
+  const int qt = p.n_q_tiles - 1 - idx;
+  const SeqInfo si = seq_info(g, b);
+  const int q0 = qt * C::BM;
+  if (q0 >= si.lq) return;
+  if (p.guard && *reinterpret_cast<volatile const int*>(p.guard)) return;
+
+  const KeyRange kr = key_range(g, si.lq, si.lk);
+  const int q_last = min(q0 + C::BM - 1, si.lq - 1);
+  const int kv_lo = kr.lo(q0), kv_hi = kr.hi(q_last);
+  const int t_lo = kv_lo / C::BN;
+  const int n_tiles = (kv_hi > kv_lo) ? (kv_hi + C::BN - 1) / C::BN - t_lo : 0;
+  const int qhead = si.qhead0 + h;
+  const int khead = si.khead0 + h / (g.hq / g.hkv);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;
+  uint8_t* sStage = smem + C::Q_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sStage + C::NSTAGES * C::STAGE_BYTES);
+  uint64_t* empty = full + C::NSTAGES;
+  uint64_t* bar_q = empty + C::NSTAGES;
+  uint64_t* bar_s = bar_q + 1;  // [2]
+  uint64_t* bar_p = bar_s + 2;  // [2]
+  uint64_t* bar_o = bar_p + 2;
+  uint64_t* bar_drain = bar_o + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NSTAGES; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(bar_q, 1);
+    mbar_init(&bar_s[0], 1);
+    mbar_init(&bar_s[1], 1);
+    mbar_init(&bar_p[0], 128);
+    mbar_init(&bar_p[1], 128);
+    mbar_init(bar_o, 1);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (elect_one() && n_tiles > 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      mbar_arrive_expect_tx(bar_q, C::Q_BYTES);
+      for (int a = 0; a < DQK / 64; ++a) tma_load_3d(&tmQ, bar_q, sQ + a * 16384, a * 64, qhead, si.qrow0 + q0);
+      int c = 0;
+      bool ok = true;
+      auto next_slot = [&](int& slot) -> bool {
+        slot = c % C::NSTAGES;
+        const uint32_t ph = (c / C::NSTAGES) & 1;
+        if (!mbar_wait(&empty[slot], ph ^ 1, abort_flag)) return false;
+        mbar_arrive_expect_tx(&full[slot], C::STAGE_BYTES);
+        return true;
+      };
+      auto load_k = [&](int j) -> bool {
+        const int key0 = si.krow0 + (t_lo + j) * C::BN;
+        for (int kb = 0; kb < C::KST; ++kb, ++c) {
+          int slot;
+          if (!next_slot(slot)) return false;
+          uint8_t* dst = sStage + slot * C::STAGE_BYTES;
+          tma_load_3d(&tmK, &full[slot], dst, kb * 128, khead, key0);
+          tma_load_3d(&tmK, &full[slot], dst + 16384, kb * 128 + 64, khead, key0);
+        }
+        return true;
+      };
+      auto load_v = [&](int j) -> bool {
+        for (int vs = 0; vs < C::VST; ++vs, ++c) {
+          int slot;
+          if (!next_slot(slot)) return false;
+          uint8_t* dst = sStage + slot * C::STAGE_BYTES;
+          const int key0 = si.krow0 + (t_lo + j) * C::BN + vs * C::VROWS;
+          for (int a = 0; a < DV / 64; ++a)
+            tma_load_3d(&tmV, &full[slot], dst + a * C::V_ATOM_BYTES, split * DV + a * 64, khead, key0);
+        }
+        return true;
+      };
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        ok = load_k(j);
+        if (ok && j >= 1) ok = load_v(j - 1);
+      }
+      if (ok) ok = load_v(n_tiles - 1);
+      if (!ok) {
+        *abort_flag = 1;
+        record_error(p.err, SDPA_ERR_TIMEOUT);
+      }
+      // Every issued copy must land before the CTA exits: the last NSTAGES
+      // stages (or fewer) are the only ones that can still be in flight.
+      const int first = c > C::NSTAGES ? c - C::NSTAGES : 0;
+      for (int k = first; k < c; ++k) mbar_wait_drain(&full[k % C::NSTAGES], (k / C::NSTAGES) & 1);
+      mbar_wait_drain(bar_q, 0);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (elect_one() && n_tiles > 0) {
+      constexpr uint32_t IDESC_S = idesc_f16(128, 128, BF16, false, false);
+      constexpr uint32_t IDESC_O = idesc_f16(128, DV, BF16, false, true);
+      int c = 0;
+      bool ok = mbar_wait(bar_q, 0, abort_flag);
+      tc_fence_after();
+      const uint32_t q_base = smem_u32(sQ);
+      auto mma_s = [&](int j) -> bool {
+        const uint32_t d = tmem + C::TMEM_S + (j & 1) * 128;
+        for (int kb = 0; kb < C::KST; ++kb, ++c) {
+          const int slot = c % C::NSTAGES;
+          if (!mbar_wait(&full[slot], (c / C::NSTAGES) & 1, abort_flag)) return false;
+          tc_fence_after();
+          const uint32_t k_base = smem_u32(sStage + slot * C::STAGE_BYTES);
+          const uint32_t qa = q_base + kb * 2 * 16384;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+            mma_ss(d, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(k_base + off, 16, 1024), IDESC_S,
+                   (kb | ks) != 0);
+          }
+          mma_commit(&empty[slot]);
+        }
+        mma_commit(&bar_s[j & 1]);
+        return true;
+      };
+      auto mma_o = [&](int j) -> bool {
+        if (!mbar_wait(&bar_p[j & 1], (j >> 1) & 1, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t pcol = tmem + C::TMEM_S + (j & 1) * 128;
+        for (int vs = 0; vs < C::VST; ++vs, ++c) {
+          const int slot = c % C::NSTAGES;
+          if (!mbar_wait(&full[slot], (c / C::NSTAGES) & 1, abort_flag)) return false;
+          tc_fence_after();
+          const uint32_t v_base = smem_u32(sStage + slot * C::STAGE_BYTES);
+#pragma unroll
+          for (int ks = 0; ks < C::VROWS / 16; ++ks) {
+            const int key_local = vs * C::VROWS + ks * 16;
+            mma_ts(tmem + C::TMEM_O, pcol + key_local / 2, smem_desc_sw128(v_base + ks * 2048, C::V_ATOM_BYTES, 1024),
+                   IDESC_O, (j | vs | ks) != 0);
+          }
+          mma_commit(&empty[slot]);
+        }
+        mma_commit(bar_o);
+        return true;
+      };
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        ok = mma_s(j);
+        if (ok && j >= 1) ok = mma_o(j - 1);
+      }
+      if (ok) ok = mma_o(n_tiles - 1);
+      if (!ok) {
+        *abort_flag = 1;
+        record_error(p.err, SDPA_ERR_TIMEOUT);
+        // let every MMA already issued finish before TMEM is released
+        mma_commit(bar_drain);
+        mbar_wait_drain(bar_drain, 0);
+      }
+    }
+  } else if (warp >= 4) {
+    // ------------------------------------------------------------ softmax
+    const int wq = warp - 4;
+    const int r = wq * 32 + lane;
+    const int i = q0 + r;
+    const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
+    const float sl2 = g.scale_log2;
+    const int lo_i = kr.lo(i), hi_i = kr.hi(i);
+    const int lo_last = kr.lo(q_last), hi_first = kr.hi(q0);
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar_s[j & 1], (j >> 1) & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t scol = lane_base + C::TMEM_S + (j & 1) * 128;
+      float s[128];
+      {
+        uint32_t u0[32], u1[32], u2[32], u3[32];
+        tmem_ld32(scol, u0);
+        tmem_ld32(scol + 32, u1);
+        tmem_ld32(scol + 64, u2);
+        tmem_ld32(scol + 96, u3);
+        tmem_wait_ld();
+        reg_fence(u0);
+        reg_fence(u1);
+        reg_fence(u2);
+        reg_fence(u3);
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          s[c] = __uint_as_float(u0[c]);
+          s[32 + c] = __uint_as_float(u1[c]);
+          s[64 + c] = __uint_as_float(u2[c]);
+          s[96 + c] = __uint_as_float(u3[c]);
+        }
+      }
+      const int kb = (t_lo + j) * C::BN;
+      if (!(lo_last <= kb && hi_first >= kb + C::BN)) {
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (kb + c < lo_i || kb + c >= hi_i) s[c] = -INFINITY;
+      }
+      float mt = s[0];
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mt = fmaxf(mt, s[c]);
+      const float m_new = fmaxf(m_used, mt);
+      bool need = false;
+      float f = 1.f;
+      if (m_used == -INFINITY) {
+        m_used = m_new;  // nothing accumulated yet for this row
+      } else if ((m_new - m_used) * sl2 > 8.f) {
+        need = true;
+        f = ex2((m_used - m_new) * sl2);
+        m_used = m_new;
+      }
+      const float mb = (m_used == -INFINITY) ? 0.f : m_used * sl2;
+      float rs = 0.f;
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const float p0 = ex2(fmaf(s[half * 64 + 2 * c], sl2, -mb));
+          const float p1 = ex2(fmaf(s[half * 64 + 2 * c + 1], sl2, -mb));
+          rs += p0 + p1;
+          pk[c] = E::pack(p0, p1);
+        }
+        tmem_st32(scol + half * 32, pk);
+      }
+      l = l * f + rs;
+      if (j >= 1) {
+        // PV_{j-1} must be complete before O is touched (and before P_j is
+        // released, which keeps this wait in step with every completion).
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_o, (j - 1) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+          for (int c = 0; c < DV / 32; ++c) {
+            uint32_t u[32];
+            tmem_ld32(lane_base + C::TMEM_O + c * 32, u);
+            tmem_wait_ld();
+            reg_fence(u);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * f);
+            tmem_st32(lane_base + C::TMEM_O + c * 32, u);
+          }
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bar_p[j & 1]);
+    }
+    if (ok && n_tiles > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_o, (n_tiles - 1) & 1, abort_flag));
+      tc_fence_after();
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      record_error(p.err, SDPA_ERR_TIMEOUT);
+    } else {
+      const bool valid = i < si.lq;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      using T = typename E::T;
+      T* orow = reinterpret_cast<T*>(p.o) + ((int64_t)(si.qrow0 + i) * g.nh_q + qhead) * g.d + split * DV;
+#pragma unroll 1
+      for (int c = 0; c < DV / 32; ++c) {
+        uint32_t packed[16];
+        if (n_tiles > 0) {
+          uint32_t u[32];
+          tmem_ld32(lane_base + C::TMEM_O + c * 32, u);
+          tmem_wait_ld();
+          reg_fence(u);
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            packed[e] = E::pack(__uint_as_float(u[2 * e]) * inv, __uint_as_float(u[2 * e + 1]) * inv);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) packed[e] = 0u;
+        }
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            dst[e] = make_uint4(packed[4 * e], packed[4 * e + 1], packed[4 * e + 2], packed[4 * e + 3]);
+        }
+      }
+      if (valid && split == 0)
+        p.lse[(int64_t)(si.qrow0 + i) * g.nh_q + qhead] = l > 0.f ? m_used * g.scale + logf(l) : -INFINITY;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int DQK, int DV, bool BF16>
+static int launch_fwd_t(const FwdLaunch& L) {
+  using C = FwdCfg<DQK, DV>;
+  auto kern = fwd_kernel<DQK, DV, BF16>;
+  static bool attr_set = false;  // per process; the attribute is per function
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
+      return SDPA_ERR_CUDA;
+    attr_set = true;
+  }
+  const long long grid = (long long)L.p.n_q_tiles * L.p.g.hq * L.p.g.batch * L.p.dv_splits;
+  if (grid <= 0) return SDPA_OK;
+  if (grid > 0x7fffffffLL) return SDPA_ERR_UNSUPPORTED;
+  kern<<<(unsigned)grid, 256, C::SMEM_BYTES, L.stream>>>(L.tmQ, L.tmK, L.tmV, L.p);
+  return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+}
+
+int launch_fwd(const FwdLaunch& L, int head_dim, bool bf16) {
+  if (head_dim == 128) return bf16 ? launch_fwd_t<128, 128, true>(L) : launch_fwd_t<128, 128, false>(L);
+  if (head_dim == 256) return bf16 ? launch_fwd_t<256, 256, true>(L) : launch_fwd_t<256, 256, false>(L);
+  if (head_dim == 512) return bf16 ? launch_fwd_t<512, 256, true>(L) : launch_fwd_t<512, 256, false>(L);
+  return SDPA_ERR_UNSUPPORTED;
+}
+
+}  // namespace sdpa

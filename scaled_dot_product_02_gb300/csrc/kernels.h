@@ -1,0 +1,67 @@
+// kernels.h -- parameter blocks and launchers shared between the C-ABI layer
+// (api.cu) and the kernel translation units.
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace sdpa {
+
+struct FwdParams {
+  Geom g;
+  void* o;
+  float* lse;
+  int* err;          // sticky per-device error word
+  const int* guard;  // per-call metadata-guard verdict (THD) or nullptr
+  int n_q_tiles;     // ceil(seqlen_q / 128)
+  int dv_splits;     // 1, or 2 when each CTA owns half of the value columns
+};
+
+struct FwdLaunch {
+  CUtensorMap tmQ, tmK, tmV;
+  FwdParams p;
+  cudaStream_t stream;
+};
+
+int launch_fwd(const FwdLaunch& L, int head_dim, bool bf16);
+
+struct BwdParams {
+  Geom g;
+  float* dq_acc;         // [nh_q][rows_q][D] fp32, zeroed by the preprocess kernel
+  const float* lse2;     // [nh_q][stat_rows] LSE * log2(e) (+inf for empty rows)
+  const float* delta;    // [nh_q][stat_rows] rowsum(dO * O)
+  int stat_rows;         // padded row count of lse2/delta (>= rows_q + 64, multiple of 4)
+  void* dk;
+  void* dv;
+  int* err;
+  const int* guard;
+  int n_kv_tiles;        // ceil(seqlen_kv / 128)
+  int d_lo, d_hi;        // dK/dV columns this launch owns (all of D for head_dim 128)
+};
+
+struct BwdLaunch {
+  CUtensorMap tmQ, tmK, tmV, tmDO;
+  BwdParams p;
+  cudaStream_t stream;
+};
+
+int launch_bwd_dkdv(const BwdLaunch& L, int head_dim, bool bf16, int* launches);
+
+// Memory-bound helpers (aux.cu).
+struct PrepParams {
+  Geom g;
+  const void* o;
+  const void* dout;
+  const float* lse;
+  float* lse2;
+  float* delta;
+  int stat_rows;
+  float* dq_acc;
+  const int* guard;
+};
+int launch_guard(const Geom& g, int total_q, int total_kv, int* guard, int* err, cudaStream_t s);
+int launch_preprocess(const PrepParams& pp, bool bf16, cudaStream_t s);
+int launch_dq_finalize(const Geom& g, const float* dq_acc, void* dq, const int* guard, bool bf16, cudaStream_t s);
+
+}  // namespace sdpa

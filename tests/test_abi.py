@@ -1,0 +1,94 @@
+"""C-ABI checks that need no GPU: the library loads, exports every entry point
+include/sdpa.h declares, and declines problems on the host as documented."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sdpa.h")
+
+
+@pytest.fixture(scope="module")
+def pkg():
+    from scaled_dot_product_02_gb300 import build
+
+    build.build()
+    import scaled_dot_product_02_gb300 as p
+
+    p.lib()
+    return p
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"SDPA_API\s+[\w\s\*]+?\b(sdpa_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for required in ("sdpa_fwd", "sdpa_bwd", "sdpa_fwd_workspace_size", "sdpa_bwd_workspace_size",
+                     "sdpa_get_device_error", "sdpa_error_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(pkg):
+    lib = ctypes.CDLL(pkg.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) <= set(pkg.EXPORTS) | {"sdpa_bwd_noalloc"}
+
+
+def test_error_strings(pkg):
+    for code in range(9):
+        assert pkg.error_string(code)
+    assert pkg.error_string(0) == "ok"
+
+
+def problem(pkg, **kw):
+    p = pkg.Problem()
+    base = dict(layout=0, dtype=0, mask_type=1, batch=2, seqlen_q=256, seqlen_kv=256, total_q=0, total_kv=0,
+                num_heads_q=8, num_heads_kv=2, head_dim=128, window_left=-1, window_right=-1, softmax_scale=0.088)
+    base.update(kw)
+    for k, v in base.items():
+        setattr(p, k, v)
+    return p
+
+
+def test_check_problem_accepts_and_declines(pkg):
+    ok = lambda **kw: pkg.sdpa_check_problem(problem(pkg, **kw))
+    assert ok() == 0
+    assert ok(head_dim=512, mask_type=2, seqlen_q=2048, seqlen_kv=8192) == 0
+    assert ok(layout=2, total_q=1000, total_kv=1000) == 0
+    assert ok(head_dim=64) == 2                                  # unsupported head dim
+    assert ok(head_dim=192) == 2
+    assert ok(dtype=5) == 2
+    assert ok(num_heads_q=6, num_heads_kv=4) == 1               # Hq % Hkv
+    assert ok(window_right=3) == 1                              # causal with a right window
+    assert ok(mask_type=0, window_left=16, seqlen_kv=300) == 2  # ambiguous non-causal window alignment
+    assert ok(mask_type=0, window_left=16, window_right=16) == 0
+    assert ok(window_left=-2) == 1
+    assert ok(softmax_scale=float("inf")) == 1
+    assert ok(seqlen_kv=0) == 1
+    assert ok(layout=7) == 1
+
+
+def test_workspace_sizes(pkg):
+    p = problem(pkg)
+    assert pkg.sdpa_fwd_workspace_size(p) == 0
+    t = problem(pkg, layout=2, total_q=1000, total_kv=1000)
+    assert pkg.sdpa_fwd_workspace_size(t) >= 4
+    ws = pkg.sdpa_bwd_workspace_size(p)
+    # dQ accumulator (fp32, rows x Hq x D) plus two padded statistics arrays
+    assert ws >= 2 * 256 * 8 * 128 * 4 + 2 * 8 * 512 * 4
+    assert ws % 256 == 0
+    assert pkg.sdpa_bwd_workspace_size(problem(pkg, head_dim=64)) == 0
+
+
+def test_product_path_refuses_cpu_tensors(pkg):
+    import torch
+
+    q = torch.zeros(1, 128, 2, 128, dtype=torch.bfloat16)
+    with pytest.raises(ValueError):
+        pkg.sdpa_fwd(q, q, q, mask="causal")

@@ -1,0 +1,44 @@
+"""Backward parity: dQ/dK/dV from the CUDA path (fed with its own forward's O
+and LSE) against the float64 oracle, under the same per-case floor rule."""
+import numpy as np
+import pytest
+
+import workloads
+from workloads import Workload
+
+pytestmark = pytest.mark.gpu
+
+BWD_CASES = [
+    workloads.TINY,
+    Workload("bshd_gqa_ragged", "bshd", "causal", 2, 300, 300, 4, 2, 128, "bf16"),
+    Workload("sbhd_fp16_nomask", "sbhd", "none", 2, 200, 200, 2, 2, 128, "fp16", std=0.5),
+    Workload("thd_varlen_gqa", "thd", "causal", 4, 300, 300, 4, 1, 128, "bf16", len_range=(1, 300)),
+    Workload("bottom_right_rect", "bshd", "causal_br", 1, 200, 333, 2, 1, 128, "bf16"),
+    Workload("window_d128", "bshd", "causal", 1, 400, 400, 2, 2, 128, "bf16", window=(100, 0)),
+    Workload("br_more_queries_than_keys", "bshd", "causal_br", 1, 300, 140, 2, 2, 128, "bf16"),
+]
+
+
+def run_fwd_bwd(w, inp):
+    from scaled_dot_product_02_gb300 import sdpa_bwd, sdpa_fwd, sdpa_get_device_error
+    from parity import gpu_kwargs, to_device
+
+    q, k, v, do = (to_device(inp[x], w.dtype) for x in ("q", "k", "v", "do"))
+    kw = gpu_kwargs(w, inp)
+    o, lse = sdpa_fwd(q, k, v, **kw)
+    dq, dk, dv = sdpa_bwd(q, k, v, o, lse, do, **kw)
+    assert sdpa_get_device_error() == 0
+    f = lambda t: t.float().cpu().numpy().astype(np.float64)
+    return f(dq), f(dk), f(dv)
+
+
+@pytest.mark.parametrize("w", BWD_CASES, ids=lambda w: w.name)
+def test_backward_matches_oracle(w):
+    from parity import check_bwd
+
+    inp = workloads.make_inputs(w, seed=11)
+    dq, dk, dv = run_fwd_bwd(w, inp)
+    results = check_bwd(w, inp, dq, dk, dv)
+    msgs = [m for _, m in results]
+    print(w.name, msgs)
+    assert all(ok for ok, _ in results), msgs
