@@ -1,0 +1,431 @@
+"""Benchmark: fused SDPA forward + backward on one GB300 per rank.
+
+A step is one pass of the whole hot path -- sdpa_fwd then sdpa_bwd through the
+C ABI -- over one batch of the varlen THD GQA training workload (8 sequences,
+lengths uniform in [512, 4096] from seed 1001, Hq 32, Hkv 8, D 128, bf16,
+top-left causal). Inputs are resident in HBM; L2 is flushed (a 256 MiB write)
+between timed steps, outside the timed events.
+
+value = TFLOP/s of fwd+bwd under the stated convention (fwd 4*Hq*D*Sq*Sk per
+sequence, halved for causal; bwd 2.5x fwd), summed over ranks.
+e2e   = the same metric with the inputs copied from pinned host memory and the
+outputs (O, LSE, dQ, dK, dV) copied back inside the timed region.
+
+--impl reference runs the float64 CPU oracle (the correctness reference) on a
+bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "attention fwd/bwd TFLOP/s and % of GB300 dense BF16 peak (D128/D512 causal)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+# ---------------------------------------------------------------- accounting
+def seq_lengths(w, inp):
+    if w.layout == "thd":
+        return np.diff(inp["cu_seqlens_q"]), np.diff(inp["cu_seqlens_kv"])
+    return np.full(w.batch, w.seqlen_q), np.full(w.batch, w.seqlen_kv)
+
+
+def pairs_per_head(w, lq, lk):
+    """Exact number of unmasked (query, key) pairs of one head, one sequence."""
+    i = np.arange(lq, dtype=np.int64)
+    off = lk - lq if w.mask == "causal_br" else 0
+    wl, wr = w.window
+    if w.mask != "none":
+        wr = 0
+    lo = np.maximum(0, i + off - wl) if wl >= 0 else np.zeros_like(i)
+    hi = np.minimum(lk, np.maximum(0, i + off + wr + 1)) if wr >= 0 else np.full_like(i, lk)
+    return int(np.maximum(0, hi - lo).sum())
+
+
+def flops(w, inp):
+    """(fwd_convention, fwd_exact) FLOPs of one forward over the workload."""
+    lqs, lks = seq_lengths(w, inp)
+    conv = exact = 0
+    for lq, lk in zip(lqs, lks):
+        c = 4 * w.heads_q * int(lq) * int(lk) * w.head_dim
+        conv += c // 2 if w.mask != "none" else c
+        exact += 4 * w.heads_q * w.head_dim * pairs_per_head(w, int(lq), int(lk))
+    return conv, exact
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower() == "active"})
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+# ---------------------------------------------------------------- oracle arm
+_sample_cache = {}
+
+
+def sample_arrays(w, inp, ls, nkv=1):
+    """The first `ls` query tokens of sequence 0 (and the keys they can see
+    under the workload's alignment), `nkv` kv heads with their q heads,
+    rounded to the workload dtype."""
+    key = (w.name, ls, nkv)
+    if key in _sample_cache:
+        return _sample_cache[key]
+    rin = workloads.rounded(inp, w.dtype)
+    group = w.heads_q // w.heads_kv * nkv
+    if w.layout == "thd":
+        lq0 = int(inp["cu_seqlens_q"][1] - inp["cu_seqlens_q"][0])
+        lk0 = int(inp["cu_seqlens_kv"][1] - inp["cu_seqlens_kv"][0])
+    else:
+        lq0, lk0 = w.seqlen_q, w.seqlen_kv
+    lq = min(ls, lq0)
+    lk = min(lk0, lq + (lk0 - lq0)) if w.mask == "causal_br" else min(lk0, lq) if lq0 == lk0 else lk0
+    if w.layout == "thd":
+        q0, k0 = int(inp["cu_seqlens_q"][0]), int(inp["cu_seqlens_kv"][0])
+        q, do = (rin[x][q0:q0 + lq, :group] for x in ("q", "do"))
+        k, v = (rin[x][k0:k0 + lk, :nkv] for x in ("k", "v"))
+        kw = dict(layout="thd", cu_q=np.array([0, lq], np.int32), cu_kv=np.array([0, lk], np.int32))
+    elif w.layout == "bshd":
+        q, do = (rin[x][:1, :lq, :group] for x in ("q", "do"))
+        k, v = (rin[x][:1, :lk, :nkv] for x in ("k", "v"))
+        kw = dict(layout="bshd")
+    else:
+        q, do = (rin[x][:lq, :1, :group] for x in ("q", "do"))
+        k, v = (rin[x][:lk, :1, :nkv] for x in ("k", "v"))
+        kw = dict(layout="sbhd")
+    arrs = tuple(np.ascontiguousarray(a) for a in (q, k, v, do))
+    sub = w.replace(layout="bshd", batch=1, seqlen_q=lq, seqlen_kv=lk, heads_q=group, heads_kv=nkv)
+    conv, _ = flops(sub, {})
+    out = (arrs, kw, 3.5 * conv, lq, group)
+    _sample_cache[key] = out
+    return out
+
+
+def time_oracle(w, inp, ls, nkv=1):
+    from oracle import oracle
+
+    (q, k, v, do), kw, fl, lq, group = sample_arrays(w, inp, ls, nkv)
+    t0 = time.perf_counter()
+    oracle.bwd(q, k, v, do, mask=w.mask, scale=w.scale, window=w.window, **kw)
+    return time.perf_counter() - t0, fl, lq, group
+
+
+def oracle_sample(w, inp, seconds_target: float):
+    """Grow the sample until one float64 oracle fwd+bwd takes about `seconds_target`."""
+    from oracle import oracle
+
+    ls, nkv = 256, 1
+    dt, fl, lq, group = time_oracle(w, inp, ls, nkv)
+    while dt < seconds_target * 0.6 and lq == ls:
+        ls = int(ls * min(2.0, max(1.15, (seconds_target / max(dt, 1e-3)) ** 0.5)))
+        dt, fl, lq, group = time_oracle(w, inp, ls, nkv)
+    while dt < seconds_target * 0.6 and nkv < w.heads_kv:
+        nkv = min(w.heads_kv, max(nkv + 1, int(nkv * seconds_target / max(dt, 1e-3))))
+        dt, fl, lq, group = time_oracle(w, inp, ls, nkv)
+    return {"seconds": dt, "flops": fl, "tflops": fl / dt / 1e12, "ls": lq, "group": group, "nkv": nkv,
+            "threads": oracle.num_threads()}
+
+
+def reference_arm(args, w, inp):
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    per_step = max(0.05, 150.0 / max(1, args.steps + args.warmup))
+    s = oracle_sample(w, inp, per_step)
+    times = []
+    for it in range(args.warmup + args.steps):
+        dt, fl, _, _ = time_oracle(w, inp, s["ls"], s["nkv"])
+        if it >= args.warmup:
+            times.append(dt)
+    t = float(np.mean(times))
+    value = s["flops"] / t / 1e12
+    sample = (f"float64 oracle fwd+bwd of the first {s['ls']} query tokens of sequence 0 with {s['nkv']} kv "
+              f"head(s) ({s['group']} q heads), per step")
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": w.name, "sample": sample},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": s["threads"], "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------- GPU arm
+def gpu_arm(args, w, inp):
+    import torch
+    import torch.distributed as dist
+
+    import scaled_dot_product_02_gb300 as sdpa
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    dev = torch.device("cuda", local)
+    td = {"bf16": torch.bfloat16, "fp16": torch.float16}[w.dtype]
+    host = {x: workloads.to_torch(inp[x], w.dtype).pin_memory() for x in ("q", "k", "v", "do")}
+    q, k, v, do = (host[x].to(dev) for x in ("q", "k", "v", "do"))
+    kw = dict(layout=w.layout, mask=w.mask, scale=w.scale, window=w.window)
+    host_cu = {}
+    if w.layout == "thd":
+        for x in ("cu_seqlens_q", "cu_seqlens_kv"):
+            host_cu[x] = torch.from_numpy(inp[x]).pin_memory()
+        kw.update(cu_seqlens_q=host_cu["cu_seqlens_q"].to(dev), cu_seqlens_kv=host_cu["cu_seqlens_kv"].to(dev),
+                  max_seqlen_q=int(np.max(np.diff(inp["cu_seqlens_q"]))),
+                  max_seqlen_kv=int(np.max(np.diff(inp["cu_seqlens_kv"]))))
+    o = torch.empty_like(q)
+    rows_q = q.numel() // (w.heads_q * w.head_dim)
+    lse = torch.empty((rows_q, w.heads_q), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    batch = len(inp["cu_seqlens_q"]) - 1 if w.layout == "thd" else None
+    prob = sdpa.make_problem(q, k, layout=w.layout, mask=w.mask, window=w.window, scale=w.scale, batch=batch,
+                             max_seqlen_q=kw.get("max_seqlen_q"), max_seqlen_kv=kw.get("max_seqlen_kv"))
+    ws_f = torch.empty(max(256, sdpa.sdpa_fwd_workspace_size(prob)), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(max(256, sdpa.sdpa_bwd_workspace_size(prob)), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        sdpa.sdpa_fwd(q, k, v, out=o, lse=lse, workspace=ws_f, **kw)
+        n = sdpa.sdpa_last_launch_count()
+        sdpa.sdpa_bwd(q, k, v, o, lse, do, dq=dq, dk=dk, dv=dv, workspace=ws_b, **kw)
+        return n + sdpa.sdpa_last_launch_count()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if sdpa.sdpa_get_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    sdpa.sdpa_profile_begin()
+    launches = 0
+    for i in range(args.steps):
+        flush.fill_(i & 255)
+        starts[i].record()
+        launches += step()
+        ends[i].record()
+    torch.cuda.synchronize()
+    prof = sdpa.sdpa_profile_end()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    ms = sum(s.elapsed_time(e) for s, e in zip(starts, ends))
+    if sdpa.sdpa_get_device_error() != 0:
+        raise RuntimeError("device error during the timed steps")
+
+    # end to end: host buffers in, results back out, every step
+    h_out = {x: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for x, t in
+             (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+    h2d = sum(t.numel() * t.element_size() for t in host.values()) + sum(
+        t.numel() * t.element_size() for t in host_cu.values())
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+    e_steps = max(1, args.steps // 2)
+
+    def e2e_step():
+        for x, dst in (("q", q), ("k", k), ("v", v), ("do", do)):
+            dst.copy_(host[x], non_blocking=True)
+        if host_cu:
+            kw["cu_seqlens_q"].copy_(host_cu["cu_seqlens_q"], non_blocking=True)
+            kw["cu_seqlens_kv"].copy_(host_cu["cu_seqlens_kv"], non_blocking=True)
+        step()
+        for x, src in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
+            h_out[x].copy_(src, non_blocking=True)
+
+    e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(e_steps):
+        e2e_step()
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e_steps
+
+    conv, exact = flops(w, inp)
+    step_flops = 3.5 * conv
+    t_max = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
+    ms, e2e_ms = float(t_max[0]), float(t_max[1])
+    value = world * step_flops * args.steps / (ms * 1e-3) / 1e12
+    e2e_value = world * step_flops / (e2e_ms * 1e-3) / 1e12
+
+    pk, pk_kind = peaks()
+    sustained = ms > 1000.0
+    peak = pk["bf16_tflops_sustained"] if sustained else pk["bf16_tflops"]
+    if w.dtype == "fp16":
+        peak = peak * 1.0  # dense fp16 and bf16 tensor rates are equal on this part
+    kern = {}
+    for kind in ("fwd", "bwd", "preprocess", "dq_finalize", "guard"):
+        tot, n = prof[kind]
+        kern[kind] = {"ms_total": tot, "launches": n, "ms_avg": tot / n if n else None}
+    fwd_alg = exact            # 4*D flop per unmasked pair per head
+    bwd_alg = 2.5 * exact      # 10*D flop per unmasked pair per head
+    dom = max(("fwd", "bwd"), key=lambda x: kern[x]["ms_total"])
+    alg = fwd_alg if dom == "fwd" else bwd_alg
+    achieved = alg / (kern[dom]["ms_avg"] * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "kernel": f"{dom}_kernel", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic_for(dom, w.name),
+                "peak_source": f"{pk_kind} {'bf16_tflops_sustained' if sustained else 'bf16_tflops'}",
+                "algorithmic_flops_per_launch": alg}
+    detail = {
+        "fwd_kernel_tflops_exact": fwd_alg / (kern["fwd"]["ms_avg"] * 1e-3) / 1e12,
+        "bwd_kernel_tflops_exact": bwd_alg / (kern["bwd"]["ms_avg"] * 1e-3) / 1e12,
+        "fwd_kernel_tflops_convention": conv / (kern["fwd"]["ms_avg"] * 1e-3) / 1e12,
+        "bwd_kernel_tflops_convention": 2.5 * conv / (kern["bwd"]["ms_avg"] * 1e-3) / 1e12,
+        "step_tflops_exact": world * 3.5 * exact * args.steps / (ms * 1e-3) / 1e12,
+        "pct_of_peak_step": 100.0 * value / world / peak,
+        "kernels": kern,
+        "preprocess_gbs": None,
+    }
+    if kern["preprocess"]["ms_avg"]:
+        # reads O and dO (2 bytes each), writes delta and LSE*log2e, zeroes the fp32 dQ accumulator
+        rows = rows_q * w.heads_q
+        byts = rows * w.head_dim * 2 * 2 + rows * 8 + rows * w.head_dim * 4
+        detail["preprocess_gbs"] = byts / (kern["preprocess"]["ms_avg"] * 1e-3) / 1e9
+    if kern["dq_finalize"]["ms_avg"]:
+        rows = rows_q * w.heads_q
+        detail["dq_finalize_gbs"] = rows * w.head_dim * 6 / (kern["dq_finalize"]["ms_avg"] * 1e-3) / 1e9
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        s = oracle_sample(w, inp, 12.0)
+        cpu = {"value": s["tflops"], "unit": "TFLOP/s", "cores": s["threads"], "kind": "oracle",
+               "sample": f"float64 oracle fwd+bwd of the first {s['ls']} query tokens of sequence 0 with "
+                         f"{s['nkv']} kv head(s) ({s['group']} q heads): {s['seconds']:.1f} s"}
+    lq, _ = seq_lengths(w, inp)
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+            "config": {"workload": w.name, "layout": w.layout, "mask": w.mask, "batch": len(lq),
+                       "seq_lengths": [int(x) for x in lq], "heads_q": w.heads_q, "heads_kv": w.heads_kv,
+                       "head_dim": w.head_dim, "window": list(w.window),
+                       "flop_convention": "fwd 4*Hq*D*Sq*Sk per sequence, halved for causal; bwd 2.5x fwd",
+                       "l2": "flushed between timed steps (256 MiB write, outside the events)",
+                       "parallelism": f"replicas x{world} (no collective)"},
+            "clocks": clk, "gpu_launches": launches,
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "roofline": roofline, "cpu_baseline": cpu, "detail": detail}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def traffic_for(kind, workload):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel sources (else None)."""
+    import hashlib
+
+    path = os.path.join(ROOT, "profiles", f"traffic_{kind}_kernel_{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    for line in open(path):
+        if ":" in line:
+            a, b = line.split(":", 1)
+            vals[a.strip()] = b.strip()
+    src = os.path.join(ROOT, "scaled_dot_product_02_gb300", "csrc", f"{kind}.cu")
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    if vals.get("source_sha256_16") != sha:
+        return None
+    try:
+        return float(vals["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="varlen_thd_gqa", choices=[w.name for w in workloads.ALL])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    w = {x.name: x for x in workloads.ALL}[args.workload]
+    inp = workloads.make_inputs(w)
+    if args.impl == "reference":
+        reference_arm(args, w, inp)
+    else:
+        gpu_arm(args, w, inp)
+
+
+if __name__ == "__main__":
+    main()

@@ -148,6 +148,23 @@ SDPA_API const char* sdpa_error_string(int status);
  * host thread launched. */
 SDPA_API int sdpa_last_launch_count(void);
 
+/* Kernel timing for benchmarks and tracing. Between sdpa_profile_begin and
+ * sdpa_profile_end, every sdpa_fwd / sdpa_bwd call made by this host thread
+ * records a pair of CUDA events on its stream around each kernel it
+ * launches. sdpa_profile_end synchronises those events and writes, per kernel
+ * kind (SDPA_KERNEL_*), the summed milliseconds and the number of launches
+ * into arrays of n_kinds entries. At most 65536 launches are recorded. */
+typedef enum {
+  SDPA_KERNEL_FWD = 0,        /* forward attention kernel */
+  SDPA_KERNEL_BWD = 1,        /* backward dK/dV/dQ kernel */
+  SDPA_KERNEL_PREPROCESS = 2, /* backward preprocess (delta, LSE rescale, dQ accumulator zeroing) */
+  SDPA_KERNEL_DQ_FINALIZE = 3,
+  SDPA_KERNEL_GUARD = 4,      /* THD metadata guard */
+  SDPA_KERNEL_KINDS = 5
+} sdpa_kernel_kind;
+SDPA_API int sdpa_profile_begin(void);
+SDPA_API int sdpa_profile_end(double* ms_by_kind, int* launches_by_kind, int n_kinds);
+
 #ifdef __cplusplus
 }
 #endif

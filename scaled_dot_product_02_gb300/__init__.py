@@ -24,7 +24,9 @@ STATUS = {0: "SDPA_OK", 1: "SDPA_ERR_INVALID_ARG", 2: "SDPA_ERR_UNSUPPORTED", 3:
           4: "SDPA_ERR_OVERLAP", 5: "SDPA_ERR_WORKSPACE_TOO_SMALL", 6: "SDPA_ERR_BAD_SEQLENS",
           7: "SDPA_ERR_TIMEOUT", 8: "SDPA_ERR_CUDA"}
 EXPORTS = ("sdpa_fwd_workspace_size", "sdpa_bwd_workspace_size", "sdpa_check_problem", "sdpa_fwd", "sdpa_bwd",
-           "sdpa_get_device_error", "sdpa_error_string", "sdpa_last_launch_count")
+           "sdpa_get_device_error", "sdpa_error_string", "sdpa_last_launch_count", "sdpa_profile_begin",
+           "sdpa_profile_end")
+KERNEL_KINDS = ("fwd", "bwd", "preprocess", "dq_finalize", "guard")
 
 
 class SdpaError(RuntimeError):
@@ -64,6 +66,8 @@ def lib():
             L.sdpa_error_string.argtypes = [ctypes.c_int]
             L.sdpa_error_string.restype = ctypes.c_char_p
             L.sdpa_last_launch_count.restype = ctypes.c_int
+            L.sdpa_profile_end.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int),
+                                           ctypes.c_int]
             _lib = L
     return _lib
 
@@ -193,3 +197,19 @@ def sdpa_get_device_error(stream=None) -> int:
 
 def sdpa_last_launch_count() -> int:
     return int(lib().sdpa_last_launch_count())
+
+
+def sdpa_profile_begin() -> None:
+    """Start recording CUDA events around every kernel this thread's calls launch."""
+    lib().sdpa_profile_begin()
+
+
+def sdpa_profile_end() -> dict:
+    """Stop recording; returns {kind: (total_ms, launches)} (synchronises)."""
+    n = len(KERNEL_KINDS)
+    ms = (ctypes.c_double * n)()
+    cnt = (ctypes.c_int * n)()
+    rc = lib().sdpa_profile_end(ms, cnt, n)
+    if rc:
+        raise SdpaError(rc, "sdpa_profile_end")
+    return {k: (ms[i], cnt[i]) for i, k in enumerate(KERNEL_KINDS)}

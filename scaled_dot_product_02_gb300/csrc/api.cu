@@ -10,6 +10,7 @@
 #include <cstdint>
 #include <cstring>
 #include <mutex>
+#include <vector>
 
 #include "../../include/sdpa.h"
 #include "kernels.h"
@@ -21,6 +22,39 @@ namespace sdpa {
 namespace {
 
 thread_local int t_last_launches = 0;
+
+// Event pairs recorded around launches while profiling is on (this thread).
+struct Profiler {
+  bool on = false;
+  struct Mark {
+    cudaEvent_t a, b;
+    int kind;
+  };
+  std::vector<Mark> marks;
+  size_t used = 0;
+  Mark* next(int kind) {
+    if (!on || used >= 65536) return nullptr;
+    if (used == marks.size()) {
+      Mark m{nullptr, nullptr, kind};
+      if (cudaEventCreate(&m.a) != cudaSuccess || cudaEventCreate(&m.b) != cudaSuccess) return nullptr;
+      marks.push_back(m);
+    }
+    Mark* m = &marks[used++];
+    m->kind = kind;
+    return m;
+  }
+};
+thread_local Profiler t_prof;
+
+// Launch `fn` (returning an sdpa_status) between two profiling events.
+template <class F>
+int timed(int kind, cudaStream_t s, F&& fn) {
+  Profiler::Mark* m = t_prof.next(kind);
+  if (m) cudaEventRecord(m->a, s);
+  const int rc = fn();
+  if (m) cudaEventRecord(m->b, s);
+  return rc;
+}
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -230,10 +264,12 @@ int sdpa_fwd(const sdpa_problem* p, const void* q, const void* k, const void* v,
   if ((rc = encode(&L.tmV, v, p->head_dim, hk, rk, 32768 / (dv * 2), bf16))) return rc;
   int launches = 0;
   if (thd) {
-    if ((rc = launch_guard(L.p.g, p->total_q, p->total_kv, static_cast<int*>(workspace), err, s))) return rc;
+    rc = timed(SDPA_KERNEL_GUARD, s,
+               [&] { return launch_guard(L.p.g, p->total_q, p->total_kv, static_cast<int*>(workspace), err, s); });
+    if (rc) return rc;
     ++launches;
   }
-  if ((rc = launch_fwd(L, p->head_dim, bf16))) return rc;
+  if ((rc = timed(SDPA_KERNEL_FWD, s, [&] { return launch_fwd(L, p->head_dim, bf16); }))) return rc;
   ++launches;
   t_last_launches = launches;
   return SDPA_OK;
@@ -279,7 +315,8 @@ int sdpa_bwd(const sdpa_problem* p, const void* q, const void* k, const void* v,
   const Geom g = make_geom(p, cu_seqlens_q, cu_seqlens_kv);
   int launches = 0;
   if (thd) {
-    if ((rc = launch_guard(g, p->total_q, p->total_kv, guard, err, s))) return rc;
+    if ((rc = timed(SDPA_KERNEL_GUARD, s, [&] { return launch_guard(g, p->total_q, p->total_kv, guard, err, s); })))
+      return rc;
     ++launches;
   }
   PrepParams pp;
@@ -292,7 +329,7 @@ int sdpa_bwd(const sdpa_problem* p, const void* q, const void* k, const void* v,
   pp.stat_rows = w.stat_rows;
   pp.dq_acc = acc;
   pp.guard = guard;
-  if ((rc = launch_preprocess(pp, bf16, s))) return rc;
+  if ((rc = timed(SDPA_KERNEL_PREPROCESS, s, [&] { return launch_preprocess(pp, bf16, s); }))) return rc;
   ++launches;
 
   BwdLaunch L;
@@ -313,9 +350,10 @@ int sdpa_bwd(const sdpa_problem* p, const void* q, const void* k, const void* v,
   if ((rc = encode(&L.tmK, k, p->head_dim, hk, rk, 128, bf16))) return rc;
   if ((rc = encode(&L.tmV, v, p->head_dim, hk, rk, 128, bf16))) return rc;
   int n = 0;
-  if ((rc = launch_bwd_dkdv(L, p->head_dim, bf16, &n))) return rc;
+  if ((rc = timed(SDPA_KERNEL_BWD, s, [&] { return launch_bwd_dkdv(L, p->head_dim, bf16, &n); }))) return rc;
   launches += n;
-  if ((rc = launch_dq_finalize(g, acc, dq, guard, bf16, s))) return rc;
+  if ((rc = timed(SDPA_KERNEL_DQ_FINALIZE, s, [&] { return launch_dq_finalize(g, acc, dq, guard, bf16, s); })))
+    return rc;
   ++launches;
   t_last_launches = launches;
   return SDPA_OK;
@@ -349,5 +387,35 @@ const char* sdpa_error_string(int status) {
 }
 
 int sdpa_last_launch_count(void) { return t_last_launches; }
+
+int sdpa_profile_begin(void) {
+  t_prof.on = true;
+  t_prof.used = 0;
+  return SDPA_OK;
+}
+
+int sdpa_profile_end(double* ms_by_kind, int* launches_by_kind, int n_kinds) {
+  if (n_kinds < 0 || (n_kinds > 0 && (!ms_by_kind || !launches_by_kind))) return SDPA_ERR_INVALID_ARG;
+  for (int k = 0; k < n_kinds; ++k) {
+    ms_by_kind[k] = 0.0;
+    launches_by_kind[k] = 0;
+  }
+  int rc = SDPA_OK;
+  for (size_t i = 0; i < t_prof.used; ++i) {
+    const Profiler::Mark& m = t_prof.marks[i];
+    float ms = 0.f;
+    if (cudaEventSynchronize(m.b) != cudaSuccess || cudaEventElapsedTime(&ms, m.a, m.b) != cudaSuccess) {
+      rc = SDPA_ERR_CUDA;
+      continue;
+    }
+    if (m.kind < n_kinds) {
+      ms_by_kind[m.kind] += ms;
+      launches_by_kind[m.kind] += 1;
+    }
+  }
+  t_prof.on = false;
+  t_prof.used = 0;
+  return rc;
+}
 
 }  // extern "C"
