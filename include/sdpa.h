@@ -148,6 +148,24 @@ SDPA_API const char* sdpa_error_string(int status);
  * host thread launched. */
 SDPA_API int sdpa_last_launch_count(void);
 
+/* Allocation-free backward (no counterpart in the pages: an addition for
+ * callers that cannot allocate device memory -- a plugin whose host owns all
+ * device allocations, a C caller with no allocator, or a path that cannot
+ * afford the device-wide synchronisation of cudaMalloc/cudaFree).
+ * Same arguments and results as sdpa_bwd, without the workspace: the scratch
+ * comes from a static array of SDPA_BWD_NOALLOC_MAX_BYTES in the library's
+ * device memory, which every GPU that loads the library holds until the
+ * process exits. Problems whose sdpa_bwd_workspace_size exceeds that maximum
+ * are rejected with SDPA_ERR_WORKSPACE_TOO_SMALL before any launch. The first
+ * call on a device looks up the array's device address (a one-time host-side
+ * set-up); make that first call before any stream capture. Every call shares
+ * the array: calls that overlap on the GPU (e.g. on two streams at once) race
+ * and must be serialised by the caller. No call allocates memory. */
+#define SDPA_BWD_NOALLOC_MAX_BYTES (32u << 20)
+SDPA_API int sdpa_bwd_noalloc(const sdpa_problem* p, const void* q, const void* k, const void* v, const void* o,
+                              const float* lse, const void* dout, void* dq, void* dk, void* dv,
+                              const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv, void* stream);
+
 /* Kernel timing for benchmarks and tracing. Between sdpa_profile_begin and
  * sdpa_profile_end, every sdpa_fwd / sdpa_bwd call made by this host thread
  * records a pair of CUDA events on its stream around each kernel it

@@ -25,7 +25,8 @@ STATUS = {0: "SDPA_OK", 1: "SDPA_ERR_INVALID_ARG", 2: "SDPA_ERR_UNSUPPORTED", 3:
           7: "SDPA_ERR_TIMEOUT", 8: "SDPA_ERR_CUDA"}
 EXPORTS = ("sdpa_fwd_workspace_size", "sdpa_bwd_workspace_size", "sdpa_check_problem", "sdpa_fwd", "sdpa_bwd",
            "sdpa_get_device_error", "sdpa_error_string", "sdpa_last_launch_count", "sdpa_profile_begin",
-           "sdpa_profile_end")
+           "sdpa_profile_end", "sdpa_bwd_noalloc")
+NOALLOC_MAX_BYTES = 32 << 20  # SDPA_BWD_NOALLOC_MAX_BYTES
 KERNEL_KINDS = ("fwd", "bwd", "preprocess", "dq_finalize", "guard")
 
 
@@ -66,6 +67,7 @@ def lib():
             L.sdpa_error_string.argtypes = [ctypes.c_int]
             L.sdpa_error_string.restype = ctypes.c_char_p
             L.sdpa_last_launch_count.restype = ctypes.c_int
+            L.sdpa_bwd_noalloc.argtypes = [pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
             L.sdpa_profile_end.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int),
                                            ctypes.c_int]
             _lib = L
@@ -187,6 +189,31 @@ def sdpa_bwd(q, k, v, o, lse, dout, *, layout="bshd", mask="none", window=(-1, -
                         _stream(stream))
     if rc:
         raise SdpaError(rc, "sdpa_bwd")
+    return dq, dk, dv
+
+
+def sdpa_bwd_noalloc(q, k, v, o, lse, dout, *, layout="bshd", mask="none", window=(-1, -1), scale=None,
+                     cu_seqlens_q=None, cu_seqlens_kv=None, max_seqlen_q=None, max_seqlen_kv=None, dq=None,
+                     dk=None, dv=None, stream=None):
+    """Backward without a workspace: the library's static scratch array is
+    used instead (for callers that cannot allocate device memory; problems
+    needing more than NOALLOC_MAX_BYTES of scratch are rejected). Calls that
+    overlap on the GPU race on that array. Returns (dq, dk, dv); pass dq/dk/dv
+    to avoid torch allocating them here."""
+    import torch
+
+    batch = None if cu_seqlens_q is None else cu_seqlens_q.numel() - 1
+    p = make_problem(q, k, layout=layout, mask=mask, window=window, scale=scale, batch=batch,
+                     max_seqlen_q=max_seqlen_q, max_seqlen_kv=max_seqlen_kv)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _check_cuda(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens_q, cu_seqlens_kv)
+    rc = lib().sdpa_bwd_noalloc(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
+                                _ptr(dq), _ptr(dk), _ptr(dv), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv),
+                                _stream(stream))
+    if rc:
+        raise SdpaError(rc, "sdpa_bwd_noalloc")
     return dq, dk, dv
 
 
