@@ -40,7 +40,7 @@ constexpr int D = 128;
 constexpr int K_BYTES = BN * D * 2;   // 32 KB, two 64-column atoms of 16 KB
 constexpr int QT_BYTES = BQ * D * 2;  // 16 KB, two atoms of 8 KB
 constexpr int STAT_FLOATS = 68;       // 64 rows + up to 3 of alignment slack + 1
-constexpr int NQS = 2;                // Q/dO stages
+constexpr int NQS = 3;                // Q/dO stages
 constexpr int DS_BYTES = BN * BQ * 2; // 16 KB
 constexpr int STG_BYTES = BQ * D * 4; // 32 KB fp32 dQ staging
 
@@ -90,12 +90,14 @@ __global__ void __launch_bounds__(384, 1)
   using T = typename E::T;
   const Geom& g = p.g;
 
-  // ---- which tile: first key tiles first (they have the most queries under a causal mask)
+  // ---- which tile: the key tiles of one (batch, kv head) are adjacent in the
+  // grid, so CTAs running together read the same Q/dO rows and reduce into the
+  // same dQ accumulator rows while those are resident in L2.
   int idx = blockIdx.x;
+  const int kt = idx % p.n_kv_tiles;
+  idx /= p.n_kv_tiles;
   const int kvh = idx % g.hkv;
-  idx /= g.hkv;
-  const int b = idx % g.batch;
-  const int kt = idx / g.batch;
+  const int b = idx / g.hkv;
   const SeqInfo si = seq_info(g, b);
   const int k0 = kt * BN;
   if (k0 >= si.lk) return;
@@ -111,7 +113,7 @@ __global__ void __launch_bounds__(384, 1)
   const int khead = si.khead0 + kvh;
 
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // stays a shared-space pointer
   float* sstat = reinterpret_cast<float*>(smem + OFF_STAT);
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + OFF_BAR);
   uint64_t* full = bars;            // [NQS]
@@ -302,18 +304,26 @@ __global__ void __launch_bounds__(384, 1)
         tmem_wait_ld();
         fence_regs(us);
         fence_regs(ud);
+        // Branch-free: every exp2 is computed and masked entries are zeroed
+        // by a select, so the 32 columns schedule as one straight-line block.
+        float l2v[32], dlv[32];
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          l2v[c] = lse2[half * 32 + c];
+          dlv[c] = delta[half * 32 + c];
+        }
         uint32_t pp[16], pd[16];
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
           float pv[2], dv[2];
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
-            const int cc = half * 32 + c + e;
-            const int q = q0 + cc;
+            const int q = q0 + half * 32 + c + e;
             const bool allowed = interior || (q >= my_qlo && q < my_qhi);
-            const float pt = allowed ? ex2(fmaf(__uint_as_float(us[c + e]), sl2, -lse2[cc])) : 0.f;
+            const float ex = ex2(fmaf(__uint_as_float(us[c + e]), sl2, -l2v[c + e]));
+            const float pt = allowed ? ex : 0.f;
             pv[e] = pt;
-            dv[e] = pt * (__uint_as_float(ud[c + e]) - delta[cc]);
+            dv[e] = pt * (__uint_as_float(ud[c + e]) - dlv[c + e]);
           }
           pp[c / 2] = E::pack(pv[0], pv[1]);
           pd[c / 2] = E::pack(dv[0], dv[1]);

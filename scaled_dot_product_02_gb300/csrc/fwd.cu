@@ -97,7 +97,7 @@ __global__ void __launch_bounds__(256, 1)
   const int khead = si.khead0 + h / (g.hq / g.hkv);
 
   extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // stays a shared-space pointer
   uint8_t* sQ = smem;
   uint8_t* sStage = smem + C::Q_BYTES;
   uint64_t* full = reinterpret_cast<uint64_t*>(sStage + C::NSTAGES * C::STAGE_BYTES);
