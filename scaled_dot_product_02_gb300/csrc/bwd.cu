@@ -14,15 +14,16 @@
 //   dQ^T = K^T dS^T              (SS, M=128 head-dim rows, N=64 queries)
 //   drain warps: dQ^T -> shared memory -> bulk reduce-add (fp32) into the
 //                head-major dQ accumulator; a finalise kernel scales and casts.
-// The MMA order dV(i), dK(i), S(i+1), dP(i+1), dQ(i) lets the softmax of tile
-// i+1 overlap dQ(i). dQ accumulation uses no inter-CTA barriers or credits:
-// every contribution is an independent fp32 reduction.
+// S^T and dP^T are double-buffered in TMEM: while the softmax warps work on
+// step i, the tensor pipe runs dV/dK/dQ of step i-1 and S^T/dP^T of step i+1,
+// so the softmax is the only serial link. dQ accumulation uses no inter-CTA
+// barriers or credits: every contribution is an independent fp32 reduction.
 //
 // Roles (384 threads): warp 0 TMA producer; warp 1 TMEM allocator + MMA
 // issuer; warps 4-7 softmax (one thread per key row) and the dK/dV
 // epilogue; warps 8-11 dQ drain (one thread per head-dim row).
-// TMEM: dV [0,128) dK [128,256) S^T/P^T [256,320) dP^T/dS^T [320,384)
-//       dQ^T [384,448).
+// TMEM: dV [0,128) dK [128,256) S^T/P^T(/dQ^T) [256,320) [320,384)
+//       dP^T/dS^T [384,448) [448,512).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -52,10 +53,14 @@ constexpr int OFF_DS = OFF_DO + NQS * QT_BYTES;          // 2 x 16 KB
 constexpr int OFF_STG = OFF_DS + 2 * DS_BYTES;           // 32 KB
 constexpr int OFF_STAT = OFF_STG + STG_BYTES;            // NQS x (lse2, delta) x 68 floats
 constexpr int OFF_BAR = OFF_STAT + NQS * 2 * STAT_FLOATS * 4;
-constexpr int NBARS = 2 * NQS + 8;
+constexpr int NBARS = 2 * NQS + 10;
 constexpr int SMEM_BYTES = 1024 + OFF_BAR + NBARS * 8 + 16;
 
-constexpr uint32_t TM_DV = 0, TM_DK = 128, TM_S = 256, TM_DP = 320, TM_DQ = 384;
+// S^T/P^T and dP^T/dS^T are double-buffered; dQ^T of step i is written into
+// step i's S^T/P^T columns once dV(i) has consumed P^T.
+constexpr uint32_t TM_DV = 0, TM_DK = 128;
+__device__ __forceinline__ uint32_t tm_s(int buf) { return 256u + 64u * buf; }
+__device__ __forceinline__ uint32_t tm_dp(int buf) { return 384u + 64u * buf; }
 
 __device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity) {
   uint64_t t0 = globaltimer_ns();
@@ -119,10 +124,10 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* full = bars;            // [NQS]
   uint64_t* empty = bars + NQS;     // [NQS]
   uint64_t* bar_kv = bars + 2 * NQS;
-  uint64_t* bar_sdp = bar_kv + 1;
-  uint64_t* bar_ds = bar_sdp + 1;
-  uint64_t* bar_dq = bar_ds + 1;
-  uint64_t* bar_dqfree = bar_dq + 1;
+  uint64_t* bar_sdp = bar_kv + 1;     // [2] S^T, dP^T of a step ready (per buffer)
+  uint64_t* bar_ds = bar_sdp + 2;     // softmax of a step done
+  uint64_t* bar_dq = bar_ds + 1;      // [2] dQ^T of a step ready (per buffer)
+  uint64_t* bar_dqfree = bar_dq + 2;  // drain has read dQ^T of a step
   uint64_t* bar_final = bar_dqfree + 1;
   uint64_t* bar_drain = bar_final + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + NBARS);
@@ -140,9 +145,11 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&empty[s], 1);
     }
     mbar_init(bar_kv, 1);
-    mbar_init(bar_sdp, 1);
+    mbar_init(&bar_sdp[0], 1);
+    mbar_init(&bar_sdp[1], 1);
     mbar_init(bar_ds, 128);
-    mbar_init(bar_dq, 1);
+    mbar_init(&bar_dq[0], 1);
+    mbar_init(&bar_dq[1], 1);
     mbar_init(bar_dqfree, 128);
     mbar_init(bar_final, 1);
     mbar_init(bar_drain, 1);
@@ -214,21 +221,25 @@ __global__ void __launch_bounds__(384, 1)
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t ka = (ks >> 2) * 16384 + (ks & 3) * 32;
           const uint32_t qa = (ks >> 2) * 8192 + (ks & 3) * 32;
-          mma_ss(tmem + TM_S, smem_desc_sw128(sK + ka, 16, 1024), smem_desc_sw128(sq + qa, 16, 1024), ID_S, ks > 0);
+          mma_ss(tmem + tm_s(i & 1), smem_desc_sw128(sK + ka, 16, 1024), smem_desc_sw128(sq + qa, 16, 1024), ID_S,
+                 ks > 0);
         }
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t ka = (ks >> 2) * 16384 + (ks & 3) * 32;
           const uint32_t qa = (ks >> 2) * 8192 + (ks & 3) * 32;
-          mma_ss(tmem + TM_DP, smem_desc_sw128(sV + ka, 16, 1024), smem_desc_sw128(sd + qa, 16, 1024), ID_S, ks > 0);
+          mma_ss(tmem + tm_dp(i & 1), smem_desc_sw128(sV + ka, 16, 1024), smem_desc_sw128(sd + qa, 16, 1024), ID_S,
+                 ks > 0);
         }
-        mma_commit(bar_sdp);
+        mma_commit(&bar_sdp[i & 1]);
         return true;
       };
       tc_fence_after();
       if (ok) ok = issue_sdp(0);
+      if (ok && n > 1) ok = issue_sdp(1);
       for (int i = 0; i < n && ok; ++i) {
         const int st = i % NQS;
+        const int buf = i & 1;
         if (!mbar_wait(bar_ds, i & 1, abort_flag)) {
           ok = false;
           break;
@@ -238,28 +249,31 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t sd = smem_u32(smem + OFF_DO + st * QT_BYTES);
 #pragma unroll
         for (int ks = 0; ks < BQ / 16; ++ks)
-          mma_ts(tmem + TM_DV, tmem + TM_S + ks * 8, smem_desc_sw128(sd + ks * 2048, 8192, 1024), ID_KV,
+          mma_ts(tmem + TM_DV, tmem + tm_s(buf) + ks * 8, smem_desc_sw128(sd + ks * 2048, 8192, 1024), ID_KV,
                  (i | ks) != 0);
 #pragma unroll
         for (int ks = 0; ks < BQ / 16; ++ks)
-          mma_ts(tmem + TM_DK, tmem + TM_DP + ks * 8, smem_desc_sw128(sq + ks * 2048, 8192, 1024), ID_KV,
+          mma_ts(tmem + TM_DK, tmem + tm_dp(buf) + ks * 8, smem_desc_sw128(sq + ks * 2048, 8192, 1024), ID_KV,
                  (i | ks) != 0);
         mma_commit(&empty[st]);
-        if (i + 1 < n && !issue_sdp(i + 1)) {
-          ok = false;
-          break;
-        }
-        if (i >= 1 && !mbar_wait(bar_dqfree, (i - 1) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t sds = smem_u32(smem + OFF_DS + (i & 1) * DS_BYTES);
+        const uint32_t sds = smem_u32(smem + OFF_DS + buf * DS_BYTES);
 #pragma unroll
         for (int ks = 0; ks < BN / 16; ++ks)
-          mma_ss(tmem + TM_DQ, smem_desc_sw128(sK + ks * 2048, 16384, 1024),
+          mma_ss(tmem + tm_s(buf), smem_desc_sw128(sK + ks * 2048, 16384, 1024),
                  smem_desc_sw128(sds + ks * 2048, 16384, 1024), ID_DQ, ks > 0);
-        mma_commit(bar_dq);
+        mma_commit(&bar_dq[buf]);
+        if (i + 2 < n) {
+          // S^T(i+2) reuses the columns dQ^T(i) sits in: wait for the drain.
+          if (!mbar_wait(bar_dqfree, i & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (!issue_sdp(i + 2)) {
+            ok = false;
+            break;
+          }
+        }
       }
       if (ok) {
         mma_commit(bar_final);
@@ -285,7 +299,8 @@ __global__ void __launch_bounds__(384, 1)
     for (int i = 0; i < n; ++i) {
       const int st = i % NQS;
       const int q0 = step_q0(i);
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_sdp, i & 1, abort_flag) &&
+      const int buf = i & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar_sdp[buf], (i >> 1) & 1, abort_flag) &&
                                        mbar_wait(&full[st], (i / NQS) & 1, abort_flag))) {
         ok = false;
         break;
@@ -299,8 +314,8 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t us[32], ud[32];
-        tmem_ld32(lane_base + TM_S + half * 32, us);
-        tmem_ld32(lane_base + TM_DP + half * 32, ud);
+        tmem_ld32(lane_base + tm_s(buf) + half * 32, us);
+        tmem_ld32(lane_base + tm_dp(buf) + half * 32, ud);
         tmem_wait_ld();
         fence_regs(us);
         fence_regs(ud);
@@ -328,8 +343,8 @@ __global__ void __launch_bounds__(384, 1)
           pp[c / 2] = E::pack(pv[0], pv[1]);
           pd[c / 2] = E::pack(dv[0], dv[1]);
         }
-        tmem_st16(lane_base + TM_S + half * 16, pp);
-        tmem_st16(lane_base + TM_DP + half * 16, pd);
+        tmem_st16(lane_base + tm_s(buf) + half * 16, pp);
+        tmem_st16(lane_base + tm_dp(buf) + half * 16, pd);
         // dS^T row r, queries [32*half, 32*half+32): four 16-byte chunks,
         // placed with the 128-byte swizzle (chunk ^ (row % 8)).
 #pragma unroll
@@ -392,14 +407,15 @@ __global__ void __launch_bounds__(384, 1)
     const bool leader = threadIdx.x == 256;
     bool ok = true;
     for (int i = 0; i < n; ++i) {
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_dq, i & 1, abort_flag))) {
+      const int buf = i & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar_dq[buf], (i >> 1) & 1, abort_flag))) {
         ok = false;
         break;
       }
       tc_fence_after();
       uint32_t u0[32], u1[32];
-      tmem_ld32(lane_base + TM_DQ, u0);
-      tmem_ld32(lane_base + TM_DQ + 32, u1);
+      tmem_ld32(lane_base + tm_s(buf), u0);
+      tmem_ld32(lane_base + tm_s(buf) + 32, u1);
       tmem_wait_ld();
       fence_regs(u0);
       fence_regs(u1);
