@@ -3,8 +3,8 @@
 //     supported scope": compactness is checked on the GPU on every
 //     execution -- zero-based cumulative lengths, valid bounds, non-empty KV
 //     for live Q);
-//   * the backward preprocess: delta = rowsum(dO * O) in fp32, LSE rescaled
-//     to base 2, and the fp32 dQ accumulator zeroed;
+//   * the backward preprocess: delta = rowsum(dO * O) in fp32, -LSE*log2(e)
+//     (-inf for rows without keys), and the fp32 dQ accumulator zeroed;
 //   * the dQ finalise: dQ = scale * accumulator, cast to the input dtype.
 #include <cuda_runtime.h>
 
@@ -77,7 +77,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const PrepParams p) {
       const float l = p.lse[(long long)row * g.nh_q + head];
       const long long si = (long long)head * p.stat_rows + row;
       p.delta[si] = acc;
-      p.lse2[si] = (l == -INFINITY) ? INFINITY : l * 1.4426950408889634f;
+      p.lse2[si] = (l == -INFINITY) ? -INFINITY : -l * 1.4426950408889634f;
     }
   }
   // padding rows of the statistics, read by tiles that overhang the end
@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const PrepParams p) {
     const int head = (int)(it / (p.stat_rows - g.rows_q));
     const int row = g.rows_q + (int)(it % (p.stat_rows - g.rows_q));
     p.delta[(long long)head * p.stat_rows + row] = 0.f;
-    p.lse2[(long long)head * p.stat_rows + row] = INFINITY;
+    p.lse2[(long long)head * p.stat_rows + row] = -INFINITY;
   }
   // zero the dQ accumulator
   const long long n4 = (long long)g.nh_q * g.rows_q * g.d / 4;

@@ -19,9 +19,10 @@
 // so the softmax is the only serial link. dQ accumulation uses no inter-CTA
 // barriers or credits: every contribution is an independent fp32 reduction.
 //
-// Roles (384 threads): warp 0 TMA producer; warp 1 TMEM allocator + MMA
-// issuer; warps 4-7 softmax (one thread per key row) and the dK/dV
-// epilogue; warps 8-11 dQ drain (one thread per head-dim row).
+// Roles (512 threads): warp 0 TMA producer; warp 1 TMEM allocator + MMA
+// issuer; warps 4-7 and 8-11 softmax (one thread per key row, each
+// warpgroup one half of the 64 query columns) and the dV / dK epilogue;
+// warps 12-15 dQ drain (one thread per head-dim row).
 // TMEM: dV [0,128) dK [128,256) S^T/P^T(/dQ^T) [256,320) [320,384)
 //       dP^T/dS^T [384,448) [448,512).
 #include <cuda.h>
@@ -84,10 +85,41 @@ __device__ __forceinline__ void named_barrier(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Column (within a 64-column S^T/dP^T buffer) of the packed 16-bit operand
+// for queries [16*ks, 16*ks+16): each half of 32 queries is packed into the
+// first 16 columns of its own 32.
+__device__ __forceinline__ uint32_t p_col(int ks) { return (uint32_t)((ks >> 1) * 32 + (ks & 1) * 8); }
+
+// P^T and dS^T for 32 query columns of one key row:
+//   P = exp2(S * scale*log2e - LSE*log2e) (zero where masked),
+//   dS = P * (dP - delta), both packed to 16-bit pairs.
+// nl2 holds -LSE*log2e (-inf for rows without keys), dl the deltas.
+template <bool MASK, class E>
+__device__ __forceinline__ void p_ds_cols(const uint32_t (&us)[32], const uint32_t (&ud)[32], const float* nl2,
+                                          const float* dl, float sl2, int q, int qlo, int qhi, uint32_t (&pp)[16],
+                                          uint32_t (&pd)[16]) {
+  const float2 sc = make_float2(sl2, sl2);
+#pragma unroll
+  for (int c = 0; c < 32; c += 2) {
+    const float2 t = ffma2(make_float2(__uint_as_float(us[c]), __uint_as_float(us[c + 1])), sc,
+                           make_float2(nl2[c], nl2[c + 1]));
+    float p0 = ex2(t.x), p1 = ex2(t.y);
+    if (MASK) {
+      p0 = (q + c >= qlo && q + c < qhi) ? p0 : 0.f;
+      p1 = (q + c + 1 >= qlo && q + c + 1 < qhi) ? p1 : 0.f;
+    }
+    const float2 d = fsub2(make_float2(__uint_as_float(ud[c]), __uint_as_float(ud[c + 1])),
+                           make_float2(dl[c], dl[c + 1]));
+    const float2 ds = fmul2(make_float2(p0, p1), d);
+    pp[c / 2] = E::pack(p0, p1);
+    pd[c / 2] = E::pack(ds.x, ds.y);
+  }
+}
+
 }  // namespace
 
 template <bool BF16>
-__global__ void __launch_bounds__(384, 1)
+__global__ void __launch_bounds__(512, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
                const __grid_constant__ BwdParams p) {
@@ -147,7 +179,7 @@ __global__ void __launch_bounds__(384, 1)
     mbar_init(bar_kv, 1);
     mbar_init(&bar_sdp[0], 1);
     mbar_init(&bar_sdp[1], 1);
-    mbar_init(bar_ds, 128);
+    mbar_init(bar_ds, 256);
     mbar_init(&bar_dq[0], 1);
     mbar_init(&bar_dq[1], 1);
     mbar_init(bar_dqfree, 128);
@@ -249,11 +281,11 @@ __global__ void __launch_bounds__(384, 1)
         const uint32_t sd = smem_u32(smem + OFF_DO + st * QT_BYTES);
 #pragma unroll
         for (int ks = 0; ks < BQ / 16; ++ks)
-          mma_ts(tmem + TM_DV, tmem + tm_s(buf) + ks * 8, smem_desc_sw128(sd + ks * 2048, 8192, 1024), ID_KV,
+          mma_ts(tmem + TM_DV, tmem + tm_s(buf) + p_col(ks), smem_desc_sw128(sd + ks * 2048, 8192, 1024), ID_KV,
                  (i | ks) != 0);
 #pragma unroll
         for (int ks = 0; ks < BQ / 16; ++ks)
-          mma_ts(tmem + TM_DK, tmem + tm_dp(buf) + ks * 8, smem_desc_sw128(sq + ks * 2048, 8192, 1024), ID_KV,
+          mma_ts(tmem + TM_DK, tmem + tm_dp(buf) + p_col(ks), smem_desc_sw128(sq + ks * 2048, 8192, 1024), ID_KV,
                  (i | ks) != 0);
         mma_commit(&empty[st]);
         const uint32_t sds = smem_u32(smem + OFF_DS + buf * DS_BYTES);
@@ -284,9 +316,14 @@ __global__ void __launch_bounds__(384, 1)
         wait_drain(bar_drain, 0);
       }
     }
-  } else if (warp >= 4 && warp < 8) {
+  } else if (warp >= 4 && warp < 12) {
     // ------------------------------------------------------------ softmax
-    const int wq = warp - 4;
+    // Two warpgroups split the 64 query columns of a step: warpgroup `half`
+    // owns columns [32*half, 32*half+32). Each writes its packed P^T / dS^T
+    // into the first 16 of its own 32 columns, so neither overwrites scores
+    // the other has not read yet.
+    const int half = (warp - 4) >> 2;
+    const int wq = warp & 3;
     const int r = wq * 32 + lane;  // key row in the tile
     const int j = k0 + r;
     const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
@@ -308,51 +345,29 @@ __global__ void __launch_bounds__(384, 1)
       tc_fence_after();
       const bool interior = (k0 + BN <= si.lk) && (q0 + BQ <= si.lq) && lo_last <= q0 && hi_first >= q0 + BQ;
       const int row0 = si.qrow0 + q0;
-      const float* lse2 = sstat + st * 2 * STAT_FLOATS + (row0 & 3);
-      const float* delta = lse2 + STAT_FLOATS;
-      uint8_t* ds_row = smem + OFF_DS + (i & 1) * DS_BYTES + r * 128;
+      const float* nl2 = sstat + st * 2 * STAT_FLOATS + (row0 & 3) + half * 32;
+      const float* dl = nl2 + STAT_FLOATS;
+      uint32_t us[32], ud[32];
+      tmem_ld32(lane_base + tm_s(buf) + half * 32, us);
+      tmem_ld32(lane_base + tm_dp(buf) + half * 32, ud);
+      tmem_wait_ld();
+      fence_regs(us);
+      fence_regs(ud);
+      uint32_t pp[16], pd[16];
+      if (interior)
+        p_ds_cols<false, E>(us, ud, nl2, dl, sl2, 0, 0, 0, pp, pd);
+      else
+        p_ds_cols<true, E>(us, ud, nl2, dl, sl2, q0 + half * 32, my_qlo, my_qhi, pp, pd);
+      tmem_st16(lane_base + tm_s(buf) + half * 32, pp);
+      tmem_st16(lane_base + tm_dp(buf) + half * 32, pd);
+      // dS^T row r, queries [32*half, 32*half+32): four 16-byte chunks placed
+      // with the 128-byte swizzle (chunk ^ (row % 8)).
+      uint8_t* ds_row = smem + OFF_DS + buf * DS_BYTES + r * 128;
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t us[32], ud[32];
-        tmem_ld32(lane_base + tm_s(buf) + half * 32, us);
-        tmem_ld32(lane_base + tm_dp(buf) + half * 32, ud);
-        tmem_wait_ld();
-        fence_regs(us);
-        fence_regs(ud);
-        // Branch-free: every exp2 is computed and masked entries are zeroed
-        // by a select, so the 32 columns schedule as one straight-line block.
-        float l2v[32], dlv[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          l2v[c] = lse2[half * 32 + c];
-          dlv[c] = delta[half * 32 + c];
-        }
-        uint32_t pp[16], pd[16];
-#pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          float pv[2], dv[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int q = q0 + half * 32 + c + e;
-            const bool allowed = interior || (q >= my_qlo && q < my_qhi);
-            const float ex = ex2(fmaf(__uint_as_float(us[c + e]), sl2, -l2v[c + e]));
-            const float pt = allowed ? ex : 0.f;
-            pv[e] = pt;
-            dv[e] = pt * (__uint_as_float(ud[c + e]) - dlv[c + e]);
-          }
-          pp[c / 2] = E::pack(pv[0], pv[1]);
-          pd[c / 2] = E::pack(dv[0], dv[1]);
-        }
-        tmem_st16(lane_base + tm_s(buf) + half * 16, pp);
-        tmem_st16(lane_base + tm_dp(buf) + half * 16, pd);
-        // dS^T row r, queries [32*half, 32*half+32): four 16-byte chunks,
-        // placed with the 128-byte swizzle (chunk ^ (row % 8)).
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int chunk = half * 4 + k;
-          *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) * 16)) =
-              make_uint4(pd[4 * k], pd[4 * k + 1], pd[4 * k + 2], pd[4 * k + 3]);
-        }
+      for (int k = 0; k < 4; ++k) {
+        const int chunk = half * 4 + k;
+        *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) * 16)) =
+            make_uint4(pd[4 * k], pd[4 * k + 1], pd[4 * k + 2], pd[4 * k + 3]);
       }
       fence_proxy_async_smem();
       tmem_wait_st();
@@ -367,44 +382,39 @@ __global__ void __launch_bounds__(384, 1)
       *abort_flag = 1;
       record_error(p.err, SDPA_ERR_TIMEOUT);
     } else {
-      // dK (scaled) and dV rows of this key
-      T* dvrow = reinterpret_cast<T*>(p.dv) + ((long long)(si.krow0 + j) * g.nh_kv + khead) * D;
-      T* dkrow = reinterpret_cast<T*>(p.dk) + ((long long)(si.krow0 + j) * g.nh_kv + khead) * D;
+      // warpgroup 0 stores dV, warpgroup 1 stores dK (scaled)
+      T* dst = reinterpret_cast<T*>(half ? p.dk : p.dv) + ((long long)(si.krow0 + j) * g.nh_kv + khead) * D;
+      const float mul = half ? g.scale : 1.f;
 #pragma unroll 1
-      for (int which = 0; which < 2; ++which) {
-        T* dst = which ? dkrow : dvrow;
-        const float mul = which ? g.scale : 1.f;
-#pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t packed[16];
-          if (n > 0) {
-            uint32_t u[32];
-            tmem_ld32(lane_base + (which ? TM_DK : TM_DV) + c * 32, u);
-            tmem_wait_ld();
-            fence_regs(u);
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t packed[16];
+        if (n > 0) {
+          uint32_t u[32];
+          tmem_ld32(lane_base + (half ? TM_DK : TM_DV) + c * 32, u);
+          tmem_wait_ld();
+          fence_regs(u);
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
-              packed[e] = E::pack(__uint_as_float(u[2 * e]) * mul, __uint_as_float(u[2 * e + 1]) * mul);
-          } else {
+          for (int e = 0; e < 16; ++e)
+            packed[e] = E::pack(__uint_as_float(u[2 * e]) * mul, __uint_as_float(u[2 * e + 1]) * mul);
+        } else {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) packed[e] = 0u;
-          }
-          if (key_ok) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+          for (int e = 0; e < 16; ++e) packed[e] = 0u;
+        }
+        if (key_ok) {
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              d4[e] = make_uint4(packed[4 * e], packed[4 * e + 1], packed[4 * e + 2], packed[4 * e + 3]);
-          }
+          for (int e = 0; e < 4; ++e)
+            d4[e] = make_uint4(packed[4 * e], packed[4 * e + 1], packed[4 * e + 2], packed[4 * e + 3]);
         }
       }
     }
-  } else if (warp >= 8) {
+  } else if (warp >= 12) {
     // ------------------------------------------------------------ dQ drain
-    const int wq = warp - 8;
+    const int wq = warp & 3;
     const int dcol = wq * 32 + lane;  // head-dim row of dQ^T
     const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
     float* stg = reinterpret_cast<float*>(smem + OFF_STG);
-    const bool leader = threadIdx.x == 256;
+    const bool leader = threadIdx.x == 384;
     bool ok = true;
     for (int i = 0; i < n; ++i) {
       const int buf = i & 1;
@@ -435,8 +445,8 @@ __global__ void __launch_bounds__(384, 1)
         const int rows = min(BQ, si.lq - q0);
         if (rows > 0) {
           const int qhead = si.qhead0 + step_head(i);
-          float* dst = p.dq_acc + ((long long)qhead * g.rows_q + si.qrow0 + q0) * D;
-          bulk_reduce_add_f32(dst, stg, rows * D * 4);
+          float* dstp = p.dq_acc + ((long long)qhead * g.rows_q + si.qrow0 + q0) * D;
+          bulk_reduce_add_f32(dstp, stg, rows * D * 4);
           bulk_commit_group();
         }
       }
@@ -468,7 +478,7 @@ static int launch_t(const BwdLaunch& L) {
   const long long grid = (long long)L.p.n_kv_tiles * L.p.g.hkv * L.p.g.batch;
   if (grid <= 0) return SDPA_OK;
   if (grid > 0x7fffffffLL) return SDPA_ERR_UNSUPPORTED;
-  kern<<<(unsigned)grid, 384, SMEM_BYTES, L.stream>>>(L.tmQ, L.tmK, L.tmV, L.tmDO, L.p);
+  kern<<<(unsigned)grid, 512, SMEM_BYTES, L.stream>>>(L.tmQ, L.tmK, L.tmV, L.tmDO, L.p);
   return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }
 

@@ -29,7 +29,7 @@ int launch_fwd(const FwdLaunch& L, int head_dim, bool bf16);
 struct BwdParams {
   Geom g;
   float* dq_acc;         // [nh_q][rows_q][D] fp32, zeroed by the preprocess kernel
-  const float* lse2;     // [nh_q][stat_rows] LSE * log2(e) (+inf for empty rows)
+  const float* lse2;     // [nh_q][stat_rows] -LSE * log2(e) (-inf for rows without keys)
   const float* delta;    // [nh_q][stat_rows] rowsum(dO * O)
   int stat_rows;         // padded row count of lse2/delta (>= rows_q + 64, multiple of 4)
   void* dk;
