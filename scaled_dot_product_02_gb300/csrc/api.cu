@@ -8,6 +8,7 @@
 
 #include <cmath>
 #include <cstdint>
+#include <algorithm>
 #include <cstring>
 #include <mutex>
 #include <vector>
@@ -182,9 +183,23 @@ int encode(CUtensorMap* m, const void* base, int d, int nh, int rows, int box_ro
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Backward workspace carve-up.
+// Key tiles one 128-row query tile can touch (the slot count of the head_dim
+// 256/512 tile arrays): the whole key range, or the window's span.
+int kv_slots(const sdpa_problem* p) {
+  const int nkt = (p->seqlen_kv + 127) / 128;
+  const int wr = causal(p) ? 0 : p->window_right;
+  if (p->window_left >= 0 && wr >= 0) {
+    const long long span = 128LL + p->window_left + wr;  // keys one query tile can see
+    return (int)std::min<long long>(nkt, span / 128 + 2);
+  }
+  return nkt;
+}
+
+// Backward workspace carve-up. head_dim 128: per-row statistics and the fp32
+// dQ accumulator. head_dim 256/512: statistics, the 16-bit P / dS tile
+// arrays and the fp32 dP - delta tiles.
 struct BwdWs {
-  size_t guard_off, lse2_off, delta_off, acc_off, total;
+  size_t guard_off, lse2_off, delta_off, acc_off, ptile_off, dstile_off, dpdtile_off, total;
   int stat_rows;
 };
 BwdWs bwd_ws(const sdpa_problem* p) {
@@ -195,8 +210,19 @@ BwdWs bwd_ws(const sdpa_problem* p) {
   w.guard_off = 0;
   w.lse2_off = 256;
   w.delta_off = round_up(w.lse2_off + (size_t)hq * w.stat_rows * 4, 256);
-  w.acc_off = round_up(w.delta_off + (size_t)hq * w.stat_rows * 4, 256);
-  w.total = round_up(w.acc_off + (size_t)hq * rq * p->head_dim * 4, 256);
+  const size_t after_stats = round_up(w.delta_off + (size_t)hq * w.stat_rows * 4, 256);
+  if (p->head_dim == 128) {
+    w.acc_off = after_stats;
+    w.ptile_off = w.dstile_off = w.dpdtile_off = 0;
+    w.total = round_up(w.acc_off + (size_t)hq * rq * p->head_dim * 4, 256);
+  } else {
+    const size_t tiles = (size_t)p->batch * p->num_heads_q * ((p->seqlen_q + 127) / 128) * kv_slots(p);
+    w.acc_off = 0;
+    w.ptile_off = round_up(after_stats, 1024);
+    w.dstile_off = w.ptile_off + tiles * 32768;
+    w.dpdtile_off = w.dstile_off + tiles * 32768;
+    w.total = w.dpdtile_off + tiles * 65536;
+  }
   return w;
 }
 
@@ -327,10 +353,39 @@ int sdpa_bwd(const sdpa_problem* p, const void* q, const void* k, const void* v,
   pp.lse2 = lse2;
   pp.delta = delta;
   pp.stat_rows = w.stat_rows;
-  pp.dq_acc = acc;
+  pp.dq_acc = p->head_dim == 128 ? acc : nullptr;
   pp.guard = guard;
   if ((rc = timed(SDPA_KERNEL_PREPROCESS, s, [&] { return launch_preprocess(pp, bf16, s); }))) return rc;
   ++launches;
+
+  if (p->head_dim != 128) {
+    BigBwdLaunch B;
+    std::memset(&B, 0, sizeof(B));
+    B.p.g = g;
+    B.p.p_tiles = ws + w.ptile_off;
+    B.p.ds_tiles = ws + w.dstile_off;
+    B.p.dpd_tiles = ws + w.dpdtile_off;
+    B.p.nlse2 = lse2;
+    B.p.delta = delta;
+    B.p.stat_rows = w.stat_rows;
+    B.p.dq = dq;
+    B.p.dk = dk;
+    B.p.dv = dv;
+    B.p.err = err;
+    B.p.guard = guard;
+    B.p.n_q_tiles = (p->seqlen_q + 127) / 128;
+    B.p.n_kv_tiles = (p->seqlen_kv + 127) / 128;
+    B.p.slots = kv_slots(p);
+    B.stream = s;
+    if ((rc = encode(&B.tmQ, q, p->head_dim, hq, rq, 128, bf16))) return rc;
+    if ((rc = encode(&B.tmDO, dout, p->head_dim, hq, rq, 128, bf16))) return rc;
+    if ((rc = encode(&B.tmK, k, p->head_dim, hk, rk, 128, bf16))) return rc;
+    if ((rc = encode(&B.tmV, v, p->head_dim, hk, rk, 128, bf16))) return rc;
+    int n = 0;
+    if ((rc = timed(SDPA_KERNEL_BWD, s, [&] { return launch_bwd_big(B, p->head_dim, bf16, &n); }))) return rc;
+    t_last_launches = launches + n;
+    return SDPA_OK;
+  }
 
   BwdLaunch L;
   std::memset(&L, 0, sizeof(L));

@@ -90,7 +90,7 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const PrepParams p) {
     p.lse2[(long long)head * p.stat_rows + row] = -INFINITY;
   }
   // zero the dQ accumulator
-  const long long n4 = (long long)g.nh_q * g.rows_q * g.d / 4;
+  const long long n4 = p.dq_acc ? (long long)g.nh_q * g.rows_q * g.d / 4 : 0;
   float4* acc4 = reinterpret_cast<float4*>(p.dq_acc);
   for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < n4; it += (long long)gridDim.x * blockDim.x)
     acc4[it] = make_float4(0.f, 0.f, 0.f, 0.f);

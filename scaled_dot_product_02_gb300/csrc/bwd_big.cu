@@ -1,0 +1,609 @@
+// bwd_big.cu -- attention backward for head_dim 256 and 512 on sm_103a.
+//
+// At these head dims the dK and dV accumulators of one 128-key tile need
+// 2*D fp32 TMEM columns (512 or 1024) and do not fit next to the score
+// tiles, so the backward runs in two phases:
+//
+// Phase 1, score kernels (one CTA per 128-query tile of one (batch, q head)):
+//   pass 0: dP = dO V^T over the full head dim (dO resident in shared
+//           memory, V streamed in 128x128 chunks); dP - delta kept as fp32;
+//   pass 1: S = Q K^T likewise, P = exp2(S*scale*log2e - LSE*log2e) masked,
+//           dS = P * (dP - delta), P and dS written as 16-bit 128x128 tiles.
+//   Each 16-bit tile is stored as the exact shared-memory image a tcgen05 operand
+//   wants (two 64-column atoms, 128-byte swizzle), so phase 2 fetches it with
+//   one 32 KB bulk copy. Tiles are indexed by (batch, head, query tile, slot)
+//   where slot = key tile - first key tile of that query tile; the host sizes
+//   the slot count from the mask (window and causal bounds).
+// Phase 2, GEMM kernels (accumulator 128 x 256 fp32 in TMEM, one CTA per
+// 256-column slice of the head dim), iterating only over unmasked tiles:
+//   MODE_DQ: dQ[q tile]  = scale * sum_t dS(q, t) K(t)
+//   MODE_DV: dV[kv tile] = sum_{heads of the group, q tiles} P^T dO
+//   MODE_DK: dK[kv tile] = scale * sum dS^T Q
+// Every FLOP executed is one the definition counts (10*D per unmasked pair),
+// at the cost of 8 bytes of workspace per pair, written once and read back.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace sdpa {
+
+namespace {
+
+constexpr int TILE_BYTES = 128 * 128 * 2;  // one 16-bit 128x128 tile image
+constexpr int CHUNK_BYTES = 32768;         // 128 rows x 128 columns of a 16-bit operand
+
+__device__ __forceinline__ bool wait_drain_big(uint64_t* bar, uint32_t parity) {
+  uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > 200000000ull) return false;
+  return true;
+}
+
+__device__ __forceinline__ void fence_regs32(uint32_t (&r)[32]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+}
+
+__device__ __forceinline__ void bar_sync_id(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// Bulk store shared -> global (16-byte aligned, size multiple of 16).
+__device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(gdst)),
+               "r"(smem_u32(ssrc)), "r"(bytes)
+               : "memory");
+}
+
+// Byte offset of 16-byte chunk `k16` (0..15, eight 16-bit values each) of row
+// r inside a tile image: two 64-column atoms of [128 rows x 128 bytes], each
+// row's chunks permuted by the 128-byte swizzle.
+__device__ __forceinline__ uint32_t tile_chunk_off(int r, int k16) {
+  return (uint32_t)((k16 >> 3) * 16384 + r * 128 + (((k16 & 7) ^ (r & 7)) * 16));
+}
+
+// First key tile and number of key tiles that query tile [q0, q0+128) sees.
+__device__ __forceinline__ void kv_tiles_of(const KeyRange& kr, int q0, int lq, int& t_lo, int& n) {
+  const int q_last = min(q0 + 127, lq - 1);
+  const int lo = kr.lo(q0), hi = kr.hi(q_last);
+  t_lo = lo / 128;
+  n = hi > lo ? (hi + 127) / 128 - t_lo : 0;
+}
+
+__device__ __forceinline__ long long tile_index(const BigBwdParams& p, int b, int h, int qt, int slot) {
+  return (((long long)b * p.g.hq + h) * p.n_q_tiles + qt) * p.slots + slot;
+}
+
+}  // namespace
+
+// ====================================================================== phase 1
+template <int DQK>
+struct ScoreCfg {
+  static constexpr int A_BYTES = DQK * 256;  // 128 rows x DQK x 2 bytes
+  static constexpr int KST = DQK / 128;      // 32 KB stages per key tile
+  static constexpr int NST = DQK == 256 ? 3 : 2;
+  static constexpr int NBARS = 2 * NST + 6;
+  static constexpr int SMEM_BYTES = 1024 + A_BYTES + NST * CHUNK_BYTES + TILE_BYTES + NBARS * 8 + 16;
+};
+
+// MODE 0 (A = dO, B = V): writes dP - delta as an fp32 tile.
+// MODE 1 (A = Q,  B = K): P = exp2(S*scale*log2e - LSE*log2e) in fp32,
+//   dS = P * (dP - delta) from MODE 0's tile, and writes P and dS as 16-bit
+//   tile images (each rounded once, as in a fused backward).
+// The fp32 tile is laid out chunk-major, [32 chunks of 4 columns][128 rows]
+// x 16 bytes, so the thread that owns a row touches 16-byte pieces that are
+// contiguous across the warp.
+template <int DQK, int MODE, bool BF16>
+__global__ void __launch_bounds__(256, 1)
+    score_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const __grid_constant__ BigBwdParams p) {
+  using C = ScoreCfg<DQK>;
+  using E = Elem<BF16>;
+  const Geom& g = p.g;
+  int idx = blockIdx.x;
+  const int h = idx % g.hq;
+  idx /= g.hq;
+  const int b = idx % g.batch;
+  const int qt = p.n_q_tiles - 1 - idx / g.batch;
+  const SeqInfo si = seq_info(g, b);
+  const int q0 = qt * 128;
+  if (q0 >= si.lq) return;
+  if (p.guard && *reinterpret_cast<volatile const int*>(p.guard)) return;
+  const KeyRange kr = key_range(g, si.lq, si.lk);
+  int t_lo, n;
+  kv_tiles_of(kr, q0, si.lq, t_lo, n);
+  if (n > p.slots) {  // cannot happen with a host-sized workspace; refuse rather than overrun it
+    if (threadIdx.x == 0) record_error(p.err, SDPA_ERR_INVALID_ARG);
+    return;
+  }
+  const int qhead = si.qhead0 + h;
+  const int khead = si.khead0 + h / (g.hq / g.hkv);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* sA = smem;
+  uint8_t* sStage = sA + C::A_BYTES;
+  uint8_t* sTile = sStage + C::NST * CHUNK_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sTile + TILE_BYTES);
+  uint64_t* empty = full + C::NST;
+  uint64_t* bar_a = empty + C::NST;
+  uint64_t* bar_s = bar_a + 1;      // [2]
+  uint64_t* bar_sfree = bar_s + 2;  // [2]
+  uint64_t* bar_drain = bar_sfree + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(bar_a, 1);
+    mbar_init(&bar_s[0], 1);
+    mbar_init(&bar_s[1], 1);
+    mbar_init(&bar_sfree[0], 128);
+    mbar_init(&bar_sfree[1], 128);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0) {
+    if (elect_one() && n > 0) {
+      prefetch_tmap(&tmA);
+      prefetch_tmap(&tmB);
+      mbar_arrive_expect_tx(bar_a, C::A_BYTES);
+      for (int a = 0; a < DQK / 64; ++a) tma_load_3d(&tmA, bar_a, sA + a * 16384, a * 64, qhead, si.qrow0 + q0);
+      int c = 0;
+      bool ok = true;
+      for (int t = 0; t < n && ok; ++t) {
+        const int krow = si.krow0 + (t_lo + t) * 128;
+        for (int kb = 0; kb < C::KST; ++kb, ++c) {
+          const int slot = c % C::NST;
+          if (!mbar_wait(&empty[slot], ((c / C::NST) & 1) ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[slot], CHUNK_BYTES);
+          uint8_t* dst = sStage + slot * CHUNK_BYTES;
+          tma_load_3d(&tmB, &full[slot], dst, kb * 128, khead, krow);
+          tma_load_3d(&tmB, &full[slot], dst + 16384, kb * 128 + 64, khead, krow);
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        record_error(p.err, SDPA_ERR_TIMEOUT);
+      }
+      const int first = c > C::NST ? c - C::NST : 0;
+      for (int k = first; k < c; ++k) wait_drain_big(&full[k % C::NST], (k / C::NST) & 1);
+      wait_drain_big(bar_a, 0);
+    }
+  } else if (warp == 1) {
+    if (elect_one() && n > 0) {
+      constexpr uint32_t IDESC = idesc_f16(128, 128, BF16, false, false);
+      bool ok = mbar_wait(bar_a, 0, abort_flag);
+      tc_fence_after();
+      const uint32_t a_base = smem_u32(sA);
+      int c = 0;
+      for (int t = 0; t < n && ok; ++t) {
+        const int buf = t & 1;
+        if (t >= 2 && !mbar_wait(&bar_sfree[buf], ((t >> 1) & 1) ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int kb = 0; kb < C::KST && ok; ++kb, ++c) {
+          const int slot = c % C::NST;
+          if (!mbar_wait(&full[slot], (c / C::NST) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t bb = smem_u32(sStage + slot * CHUNK_BYTES);
+          const uint32_t aa = a_base + kb * 2 * 16384;
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+            mma_ss(tmem + buf * 128, smem_desc_sw128(aa + off, 16, 1024), smem_desc_sw128(bb + off, 16, 1024),
+                   IDESC, (kb | ks) != 0);
+          }
+          mma_commit(&empty[slot]);
+        }
+        if (ok) mma_commit(&bar_s[buf]);
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        record_error(p.err, SDPA_ERR_TIMEOUT);
+        mma_commit(bar_drain);
+        wait_drain_big(bar_drain, 0);
+      }
+    }
+  } else if (warp >= 4) {
+    const int wq = warp - 4;
+    const int r = wq * 32 + lane;
+    const int i = q0 + r;
+    const bool valid = i < si.lq;
+    const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
+    const long long stat = (long long)qhead * p.stat_rows + si.qrow0 + i;
+    // rows past the sequence end belong to no query: their P (and so dS) is zero
+    const float nl2 = valid ? p.nlse2[stat] : -INFINITY;
+    const float dl = valid ? p.delta[stat] : 0.f;
+    const int lo_i = kr.lo(i), hi_i = kr.hi(i);
+    const float sl2 = g.scale_log2;
+    const bool leader = threadIdx.x == 128;
+    bool ok = true;
+    for (int t = 0; t < n; ++t) {
+      const int buf = t & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar_s[buf], (t >> 1) & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const long long tix = tile_index(p, b, h, qt, t);
+      float4* dpd = reinterpret_cast<float4*>(p.dpd_tiles + tix * (2 * TILE_BYTES)) + r;
+      const int kbase = (t_lo + t) * 128;
+      uint32_t dsk[64];  // MODE 1: packed dS of the whole row, written after P
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {  // 64 keys at a time
+        uint32_t u0[32], u1[32];
+        tmem_ld32(lane_base + buf * 128 + half * 64, u0);
+        tmem_ld32(lane_base + buf * 128 + half * 64 + 32, u1);
+        tmem_wait_ld();
+        fence_regs32(u0);
+        fence_regs32(u1);
+        if (half == 1) {
+          tc_fence_before();
+          mbar_arrive(&bar_sfree[buf]);
+        }
+        if (MODE == 0) {
+#pragma unroll
+          for (int c4 = 0; c4 < 16; ++c4) {
+            const uint32_t* u = c4 < 8 ? &u0[c4 * 4] : &u1[(c4 - 8) * 4];
+            dpd[(half * 16 + c4) * 128] = make_float4(__uint_as_float(u[0]) - dl, __uint_as_float(u[1]) - dl,
+                                                      __uint_as_float(u[2]) - dl, __uint_as_float(u[3]) - dl);
+          }
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {  // 8 chunks of 8 keys
+            const float4 d0 = dpd[(half * 16 + 2 * k) * 128];
+            const float4 d1 = dpd[(half * 16 + 2 * k + 1) * 128];
+            const float dv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
+            uint32_t w4[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int c0 = k * 8 + 2 * e;  // column within this 64-key half
+              const uint32_t x0 = c0 < 32 ? u0[c0] : u1[c0 - 32];
+              const uint32_t x1 = c0 + 1 < 32 ? u0[c0 + 1] : u1[c0 + 1 - 32];
+              const int key = kbase + half * 64 + c0;
+              float p0 = ex2(fmaf(__uint_as_float(x0), sl2, nl2));
+              float p1 = ex2(fmaf(__uint_as_float(x1), sl2, nl2));
+              p0 = (key >= lo_i && key < hi_i) ? p0 : 0.f;
+              p1 = (key + 1 >= lo_i && key + 1 < hi_i) ? p1 : 0.f;
+              w4[e] = E::pack(p0, p1);
+              dsk[half * 32 + k * 4 + e] = E::pack(p0 * dv[2 * e], p1 * dv[2 * e + 1]);
+            }
+            *reinterpret_cast<uint4*>(sTile + tile_chunk_off(r, half * 8 + k)) =
+                make_uint4(w4[0], w4[1], w4[2], w4[3]);
+          }
+        }
+      }
+      if (MODE == 1) {
+        // P image out, then the dS image through the same buffer
+        fence_proxy_async_smem();
+        bar_sync_id(1, 128);
+        if (leader) {
+          bulk_store(p.p_tiles + tix * TILE_BYTES, sTile, TILE_BYTES);
+          bulk_commit_group();
+          bulk_wait_group_read0();
+        }
+        bar_sync_id(1, 128);
+#pragma unroll
+        for (int k16 = 0; k16 < 16; ++k16)
+          *reinterpret_cast<uint4*>(sTile + tile_chunk_off(r, k16)) =
+              make_uint4(dsk[4 * k16], dsk[4 * k16 + 1], dsk[4 * k16 + 2], dsk[4 * k16 + 3]);
+        fence_proxy_async_smem();
+        bar_sync_id(1, 128);
+        if (leader) {
+          bulk_store(p.ds_tiles + tix * TILE_BYTES, sTile, TILE_BYTES);
+          bulk_commit_group();
+          bulk_wait_group_read0();
+        }
+        bar_sync_id(1, 128);  // the buffer is free again for the next tile
+      }
+    }
+    if (leader) bulk_wait_group0();
+    if (!ok) {
+      *abort_flag = 1;
+      record_error(p.err, SDPA_ERR_TIMEOUT);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+// ====================================================================== phase 2
+constexpr int GB_STAGE = TILE_BYTES + 4 * 16384;  // tile image + 128 rows x 256 columns of B
+constexpr int GB_NST = 2;
+constexpr int GB_NBARS = 2 * GB_NST + 3;
+constexpr int GB_SMEM = 1024 + GB_NST * GB_STAGE + GB_NBARS * 8 + 16;
+
+// MODE 0: dQ. MODE 1: dV. MODE 2: dK.
+template <int MODE, bool BF16>
+__global__ void __launch_bounds__(256, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ BigBwdParams p) {
+  using E = Elem<BF16>;
+  using T = typename E::T;
+  const Geom& g = p.g;
+  const int splits = g.d / 256;
+  int idx = blockIdx.x;
+  int split, b, head, t_own;  // head: q head (dQ) or kv head (dV/dK); t_own: own 128-row tile
+  if (MODE == 0) {
+    split = idx % splits;
+    idx /= splits;
+    head = idx % g.hq;
+    idx /= g.hq;
+    b = idx % g.batch;
+    t_own = p.n_q_tiles - 1 - idx / g.batch;
+  } else {
+    t_own = idx % p.n_kv_tiles;
+    idx /= p.n_kv_tiles;
+    split = idx % splits;
+    idx /= splits;
+    head = idx % g.hkv;
+    b = idx / g.hkv;
+  }
+  const SeqInfo si = seq_info(g, b);
+  const int r0 = t_own * 128;
+  if (r0 >= (MODE == 0 ? si.lq : si.lk)) return;
+  if (p.guard && *reinterpret_cast<volatile const int*>(p.guard)) return;
+  const KeyRange kr = key_range(g, si.lq, si.lk);
+  const int group = g.hq / g.hkv;
+  // K-loop extent
+  int t_lo = 0, n = 0, qt_lo = 0, nqt = 0;
+  if (MODE == 0) {
+    kv_tiles_of(kr, r0, si.lq, t_lo, n);
+  } else {
+    const int k_last = min(r0 + 127, si.lk - 1);
+    const int qlo = query_lo(kr, r0), qhi = query_hi(kr, k_last, si.lq);
+    qt_lo = qlo / 128;
+    nqt = qhi > qlo ? (qhi + 127) / 128 - qt_lo : 0;
+    n = nqt * group;
+  }
+  const uint8_t* atiles = MODE == 1 ? p.p_tiles : p.ds_tiles;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + GB_NST * GB_STAGE);
+  uint64_t* empty = full + GB_NST;
+  uint64_t* bar_done = empty + GB_NST;
+  uint64_t* bar_drain = bar_done + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_drain + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  // step s of the K-loop: (A tile index, B row start, B generic head)
+  auto step = [&](int s, long long& a_tile, int& b_row, int& b_head) {
+    if (MODE == 0) {
+      a_tile = tile_index(p, b, head, t_own, s);
+      b_row = si.krow0 + (t_lo + s) * 128;
+      b_head = si.khead0 + head / group;
+    } else {
+      const int h = head * group + s / nqt;
+      const int qt = qt_lo + s % nqt;
+      int tl, tn;
+      kv_tiles_of(kr, qt * 128, si.lq, tl, tn);
+      a_tile = tile_index(p, b, h, qt, t_own - tl);
+      b_row = si.qrow0 + qt * 128;
+      b_head = si.qhead0 + h;
+    }
+  };
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < GB_NST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(bar_done, 1);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0) {
+    if (elect_one() && n > 0) {
+      prefetch_tmap(&tmB);
+      int s = 0;
+      for (; s < n; ++s) {
+        const int st = s % GB_NST;
+        if (!mbar_wait(&empty[st], ((s / GB_NST) & 1) ^ 1, abort_flag)) break;
+        long long at;
+        int brow, bh;
+        step(s, at, brow, bh);
+        uint8_t* dst = smem + st * GB_STAGE;
+        mbar_arrive_expect_tx(&full[st], GB_STAGE);
+        bulk_load(dst, atiles + at * TILE_BYTES, TILE_BYTES, &full[st]);
+        for (int a = 0; a < 4; ++a)
+          tma_load_3d(&tmB, &full[st], dst + TILE_BYTES + a * 16384, split * 256 + a * 64, bh, brow);
+      }
+      if (s < n) {
+        *abort_flag = 1;
+        record_error(p.err, SDPA_ERR_TIMEOUT);
+      }
+      for (int k = (s > GB_NST ? s - GB_NST : 0); k < s; ++k) wait_drain_big(&full[k % GB_NST], (k / GB_NST) & 1);
+    }
+  } else if (warp == 1) {
+    if (elect_one() && n > 0) {
+      // dQ: A = dS tile, K-major (rows = queries). dV/dK: A = P / dS tile read
+      // transposed (M = keys, the tile's contiguous dimension). B (K rows for
+      // dQ, dO/Q rows for dV/dK) is N-major in every mode.
+      constexpr uint32_t IDESC = idesc_f16(128, 256, BF16, MODE != 0, true);
+      bool ok = true;
+      int s = 0;
+      for (; s < n; ++s) {
+        const int st = s % GB_NST;
+        if (!mbar_wait(&full[st], (s / GB_NST) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a = smem_u32(smem + st * GB_STAGE);
+        const uint32_t bb = a + TILE_BYTES;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint64_t ad = MODE == 0 ? smem_desc_sw128(a + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024)
+                                        : smem_desc_sw128(a + ks * 2048, 16384, 1024);
+          mma_ss(tmem, ad, smem_desc_sw128(bb + ks * 2048, 16384, 1024), IDESC, (s | ks) != 0);
+        }
+        mma_commit(&empty[st]);
+      }
+      if (ok) {
+        mma_commit(bar_done);
+      } else {
+        *abort_flag = 1;
+        record_error(p.err, SDPA_ERR_TIMEOUT);
+        mma_commit(bar_drain);
+        wait_drain_big(bar_drain, 0);
+      }
+    }
+  } else if (warp >= 4) {
+    const int wq = warp - 4;
+    const int r = wq * 32 + lane;
+    const int row = r0 + r;
+    const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
+    bool ok = true;
+    if (n > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_done, 0, abort_flag));
+      tc_fence_after();
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      record_error(p.err, SDPA_ERR_TIMEOUT);
+    } else {
+      T* out;
+      float mul;
+      bool valid;
+      if (MODE == 0) {
+        out = reinterpret_cast<T*>(p.dq) + ((long long)(si.qrow0 + row) * g.nh_q + si.qhead0 + head) * g.d;
+        mul = g.scale;
+        valid = row < si.lq;
+      } else {
+        out = reinterpret_cast<T*>(MODE == 1 ? p.dv : p.dk) +
+              ((long long)(si.krow0 + row) * g.nh_kv + si.khead0 + head) * g.d;
+        mul = MODE == 2 ? g.scale : 1.f;
+        valid = row < si.lk;
+      }
+      out += split * 256;
+#pragma unroll 1
+      for (int c = 0; c < 256 / 32; ++c) {
+        uint32_t packed[16];
+        if (n > 0) {
+          uint32_t u[32];
+          tmem_ld32(lane_base + c * 32, u);
+          tmem_wait_ld();
+          fence_regs32(u);
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            packed[e] = E::pack(__uint_as_float(u[2 * e]) * mul, __uint_as_float(u[2 * e + 1]) * mul);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) packed[e] = 0u;
+        }
+        if (valid) {
+          uint4* d4 = reinterpret_cast<uint4*>(out + c * 32);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            d4[e] = make_uint4(packed[4 * e], packed[4 * e + 1], packed[4 * e + 2], packed[4 * e + 3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+// ====================================================================== launch
+template <class K>
+static bool set_smem(K kern, int bytes) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess;
+}
+
+template <int DQK, bool BF16>
+static int launch_big_t(const BigBwdLaunch& L, int* launches) {
+  using C = ScoreCfg<DQK>;
+  const BigBwdParams& p = L.p;
+  const long long g1 = (long long)p.n_q_tiles * p.g.hq * p.g.batch;
+  const long long gq = g1 * (p.g.d / 256);
+  const long long gkv = (long long)p.n_kv_tiles * (p.g.d / 256) * p.g.hkv * p.g.batch;
+  if (g1 > 0x7fffffffLL || gq > 0x7fffffffLL || gkv > 0x7fffffffLL) return SDPA_ERR_UNSUPPORTED;
+  auto s0 = score_kernel<DQK, 0, BF16>;
+  auto s1 = score_kernel<DQK, 1, BF16>;
+  auto m0 = gemm_kernel<0, BF16>;
+  auto m1 = gemm_kernel<1, BF16>;
+  auto m2 = gemm_kernel<2, BF16>;
+  static bool attr = false;
+  if (!attr) {
+    if (!set_smem(s0, C::SMEM_BYTES) || !set_smem(s1, C::SMEM_BYTES) || !set_smem(m0, GB_SMEM) ||
+        !set_smem(m1, GB_SMEM) || !set_smem(m2, GB_SMEM))
+      return SDPA_ERR_CUDA;
+    attr = true;
+  }
+  int n = 0;
+  if (g1 > 0) {
+    s0<<<(unsigned)g1, 256, C::SMEM_BYTES, L.stream>>>(L.tmDO, L.tmV, p);
+    s1<<<(unsigned)g1, 256, C::SMEM_BYTES, L.stream>>>(L.tmQ, L.tmK, p);
+    m0<<<(unsigned)gq, 256, GB_SMEM, L.stream>>>(L.tmK, p);
+    n += 3;
+  }
+  if (gkv > 0) {
+    m1<<<(unsigned)gkv, 256, GB_SMEM, L.stream>>>(L.tmDO, p);
+    m2<<<(unsigned)gkv, 256, GB_SMEM, L.stream>>>(L.tmQ, p);
+    n += 2;
+  }
+  *launches = n;
+  return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+}
+
+int launch_bwd_big(const BigBwdLaunch& L, int head_dim, bool bf16, int* launches) {
+  *launches = 0;
+  if (head_dim == 256) return bf16 ? launch_big_t<256, true>(L, launches) : launch_big_t<256, false>(L, launches);
+  if (head_dim == 512) return bf16 ? launch_big_t<512, true>(L, launches) : launch_big_t<512, false>(L, launches);
+  return SDPA_ERR_UNSUPPORTED;
+}
+
+}  // namespace sdpa

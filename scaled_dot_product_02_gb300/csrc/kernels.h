@@ -48,6 +48,32 @@ struct BwdLaunch {
 
 int launch_bwd_dkdv(const BwdLaunch& L, int head_dim, bool bf16, int* launches);
 
+// head_dim 256/512 backward (bwd_big.cu): score kernels write 16-bit P and
+// dS tiles, GEMM kernels form dQ, dV, dK from them.
+struct BigBwdParams {
+  Geom g;
+  uint8_t* p_tiles;      // [B][Hq][n_q_tiles][slots] 32 KB tile images
+  uint8_t* ds_tiles;     // same shape
+  uint8_t* dpd_tiles;    // same shape, 64 KB fp32 tiles of dP - delta
+  const float* nlse2;    // [nh_q][stat_rows] -LSE * log2(e)
+  const float* delta;    // [nh_q][stat_rows]
+  int stat_rows;
+  void* dq;
+  void* dk;
+  void* dv;
+  int* err;
+  const int* guard;
+  int n_q_tiles, n_kv_tiles, slots;
+};
+
+struct BigBwdLaunch {
+  CUtensorMap tmQ, tmK, tmV, tmDO;  // 128-row boxes
+  BigBwdParams p;
+  cudaStream_t stream;
+};
+
+int launch_bwd_big(const BigBwdLaunch& L, int head_dim, bool bf16, int* launches);
+
 // Memory-bound helpers (aux.cu).
 struct PrepParams {
   Geom g;
@@ -57,7 +83,7 @@ struct PrepParams {
   float* lse2;
   float* delta;
   int stat_rows;
-  float* dq_acc;
+  float* dq_acc;  // zeroed here when non-null
   const int* guard;
 };
 int launch_guard(const Geom& g, int total_q, int total_kv, int* guard, int* err, cudaStream_t s);

@@ -16,6 +16,13 @@ BWD_CASES = [
     Workload("bottom_right_rect", "bshd", "causal_br", 1, 200, 333, 2, 1, 128, "bf16"),
     Workload("window_d128", "bshd", "causal", 1, 400, 400, 2, 2, 128, "bf16", window=(100, 0)),
     Workload("br_more_queries_than_keys", "bshd", "causal_br", 1, 300, 140, 2, 2, 128, "bf16"),
+    # head_dim 256 / 512: two-phase backward (score tiles + GEMMs)
+    Workload("window_d256", "bshd", "causal", 1, 400, 400, 2, 1, 256, "bf16", window=(100, 0)),
+    Workload("d256_fp16_sbhd_window", "sbhd", "causal", 2, 260, 260, 2, 1, 256, "fp16", window=(64, 0)),
+    Workload("d256_thd_varlen", "thd", "causal", 3, 300, 300, 4, 2, 256, "bf16", len_range=(1, 300)),
+    Workload("d512_br", "bshd", "causal_br", 1, 130, 300, 2, 1, 512, "bf16"),
+    Workload("d512_nomask_gqa", "bshd", "none", 1, 129, 257, 4, 2, 512, "bf16"),
+    Workload("d512_br_more_queries", "bshd", "causal_br", 1, 300, 140, 2, 2, 512, "bf16"),
 ]
 
 
