@@ -69,6 +69,7 @@ def _load():
             lib.sdpa_oracle_bwd_part.argtypes = [pp, dp, dp, dp, dp, ip, ip, ctypes.c_int, ctypes.c_int,
                                                  ctypes.c_int, ctypes.c_int, dp, dp, dp, dp, dp, dp]
             lib.sdpa_oracle_dq_rows.argtypes = [pp, dp, dp, dp, dp, ip, ip, ctypes.c_int, ip, dp]
+            lib.sdpa_oracle_dkdv_rows.argtypes = [pp, dp, dp, dp, dp, ip, ip, ctypes.c_int, ip, dp, dp]
             lib.sdpa_oracle_num_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -191,3 +192,19 @@ def dq_rows(q, k, v, dout, bhi, *, layout="bshd", mask="none", scale=None, windo
     if rc:
         raise ValueError(f"oracle dq_rows rejected the problem (rc={rc})")
     return dq
+
+
+def dkdv_rows(q, k, v, dout, bgj, *, layout="bshd", mask="none", scale=None, window=(-1, -1), cu_q=None,
+              cu_kv=None):
+    """dK and dV for selected (b, kv head g, key j) rows. Returns (dk (n, D), dv (n, D))."""
+    q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+    scale = 1.0 / np.sqrt(q.shape[-1]) if scale is None else scale
+    p = Problem(q, k, layout, mask, scale, window, cu_q, cu_kv)
+    bgj = np.ascontiguousarray(bgj, dtype=np.int32).reshape(-1, 3)
+    dk = np.zeros((len(bgj), p.d))
+    dv = np.zeros((len(bgj), p.d))
+    rc = _load().sdpa_oracle_dkdv_rows(ctypes.byref(p.c), _dptr(q), _dptr(k), _dptr(v), _dptr(dout), _iptr(p.cu_q),
+                                       _iptr(p.cu_kv), len(bgj), _iptr(bgj), _dptr(dk), _dptr(dv))
+    if rc:
+        raise ValueError(f"oracle dkdv_rows rejected the problem (rc={rc})")
+    return dk, dv

@@ -365,6 +365,84 @@ int sdpa_oracle_dq_rows(const oracle_problem* p, const double* q, const double* 
     return 0;
 }
 
+/*
+ * dK and dV rows for a list of n (b, g, j) triplets (kv head g, key j of
+ * sequence b). Each needs LSE_i and delta_i of every query row of the heads
+ * that read kv head g, so those are computed first (one pass over the query
+ * rows of each distinct (b, g) in the list); then each key row sums its
+ * column of dS and P as in pass 2 of the backward above.
+ */
+int sdpa_oracle_dkdv_rows(const oracle_problem* p, const double* q, const double* k, const double* v,
+                          const double* dout, const int32_t* cu_q, const int32_t* cu_kv, int n,
+                          const int32_t* bgj, double* dk_rows, double* dv_rows) {
+    if (!valid(p)) return 1;
+    int hq = p->num_heads_q, D = p->head_dim;
+    int group = hq / p->num_heads_kv;
+    int lkmax = max_len(p, cu_kv, 0);
+    int64_t nrows = rows_total(p, cu_q, 1);
+    double* lse_w = (double*)malloc(sizeof(double) * (size_t)(nrows * hq + 1));
+    double* del_w = (double*)malloc(sizeof(double) * (size_t)(nrows * hq + 1));
+    char* done = (char*)calloc((size_t)p->batch * p->num_heads_kv + 1, 1);
+    if (!lse_w || !del_w || !done) {
+        free(lse_w);
+        free(del_w);
+        free(done);
+        return 2;
+    }
+    for (int r = 0; r < n; ++r) {
+        int b = bgj[3 * r], g = bgj[3 * r + 1];
+        if (done[b * p->num_heads_kv + g]) continue;
+        done[b * p->num_heads_kv + g] = 1;
+        int lq = seq_len(p, cu_q, b, 1);
+#pragma omp parallel
+        {
+            double* s = (double*)malloc(sizeof(double) * (size_t)(lkmax > 0 ? lkmax : 1));
+            double* oi = (double*)malloc(sizeof(double) * (size_t)D);
+#pragma omp for collapse(2) schedule(dynamic, 4)
+            for (int hh = 0; hh < group; ++hh)
+                for (int i = 0; i < lq; ++i) {
+                    int h = g * group + hh;
+                    int64_t row = token_row(p, cu_q, b, i, 1);
+                    double li;
+                    row_forward(p, q, k, v, cu_q, cu_kv, b, h, i, s, oi, &li);
+                    lse_w[row * hq + h] = li;
+                    del_w[row * hq + h] = dot(qrow(p, dout, cu_q, b, i, h), oi, D);
+                }
+            free(s);
+            free(oi);
+        }
+    }
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int r = 0; r < n; ++r) {
+        int b = bgj[3 * r], g = bgj[3 * r + 1], j = bgj[3 * r + 2];
+        int lq = seq_len(p, cu_q, b, 1), lk = seq_len(p, cu_kv, b, 0);
+        double* dkj = dk_rows + (size_t)r * D;
+        double* dvj = dv_rows + (size_t)r * D;
+        for (int d = 0; d < D; ++d) dkj[d] = dvj[d] = 0.0;
+        const double* kj = kvrow(p, k, cu_kv, b, j, g);
+        const double* vj = kvrow(p, v, cu_kv, b, j, g);
+        for (int h = g * group; h < (g + 1) * group; ++h)
+            for (int i = 0; i < lq; ++i) {
+                if (!allowed(p, i, j, lq, lk)) continue;
+                int64_t row = token_row(p, cu_q, b, i, 1);
+                double li = lse_w[row * hq + h];
+                if (li == -INFINITY) continue;
+                const double* qi = qrow(p, q, cu_q, b, i, h);
+                const double* doi = qrow(p, dout, cu_q, b, i, h);
+                double pij = exp(p->scale * dot(qi, kj, D) - li);
+                double dsij = pij * (dot(doi, vj, D) - del_w[row * hq + h]);
+                for (int d = 0; d < D; ++d) {
+                    dvj[d] += pij * doi[d];
+                    dkj[d] += p->scale * dsij * qi[d];
+                }
+            }
+    }
+    free(lse_w);
+    free(del_w);
+    free(done);
+    return 0;
+}
+
 int sdpa_oracle_num_threads(void) {
 #ifdef _OPENMP
     extern int omp_get_max_threads(void);

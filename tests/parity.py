@@ -97,3 +97,89 @@ def check_bwd(w, inp, dq, dk, dv):
         judge("dK", dk, m["dk"], r["dk"], w.dtype),
         judge("dV", dv, m["dv"], r["dv"], w.dtype),
     ]
+
+
+def token_row(w, inp, b, i):
+    if w.layout == "bshd":
+        return b * w.seqlen_q + i
+    if w.layout == "sbhd":
+        return i * w.batch + b
+    return int(inp["cu_seqlens_q"][b]) + i
+
+
+def kv_token_row(w, inp, b, j):
+    if w.layout == "bshd":
+        return b * w.seqlen_kv + j
+    if w.layout == "sbhd":
+        return j * w.batch + b
+    return int(inp["cu_seqlens_kv"][b]) + j
+
+
+def seq_lens(w, inp):
+    if w.layout == "thd":
+        return np.diff(inp["cu_seqlens_q"]), np.diff(inp["cu_seqlens_kv"])
+    return np.full(w.batch, w.seqlen_q), np.full(w.batch, w.seqlen_kv)
+
+
+def sample_rows(w, inp, n, seed):
+    """(b, h, i) query rows: sequence starts and ends, 128-row tile edges, random."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    lq, _ = seq_lens(w, inp)
+    rows = set()
+    for b in range(len(lq)):
+        L = int(lq[b])
+        if L == 0:
+            continue
+        for i in (0, L - 1, min(127, L - 1), min(128, L - 1), L // 2):
+            rows.add((b, int(rng.integers(w.heads_q)), i))
+    while len(rows) < n:
+        b = int(rng.integers(len(lq)))
+        if lq[b]:
+            rows.add((b, int(rng.integers(w.heads_q)), int(rng.integers(lq[b]))))
+    return np.array(sorted(rows), dtype=np.int32)
+
+
+def sample_keys(w, inp, n, seed):
+    """(b, g, j) key rows of one (sequence, kv head): the shortest sequence for
+    THD, so the oracle's per-group pass stays cheap."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    _, lk = seq_lens(w, inp)
+    b = int(np.argmin(lk)) if w.layout == "thd" else 0
+    g = int(rng.integers(w.heads_kv))
+    L = int(lk[b])
+    keys = {0, L - 1, min(127, L - 1), min(128, L - 1), L // 2}
+    while len(keys) < min(n, L):
+        keys.add(int(rng.integers(L)))
+    return np.array([(b, g, j) for j in sorted(keys)], dtype=np.int32)
+
+
+def check_sampled(w, inp, out, n_rows=40, n_keys=12, seed=0, backward=True):
+    """Parity on sampled rows of a full-size run. `out` holds the GPU results
+    as float64 numpy arrays in their layouts: o, lse and (backward) dq, dk, dv."""
+    rin = workloads.rounded(inp, w.dtype)
+    kw = oracle_kwargs(w, inp)
+    bhi = sample_rows(w, inp, n_rows, seed)
+    tr = [token_row(w, inp, b, i) for b, _, i in bhi]
+    o_m, l_m = oracle.fwd_rows(inp["q"], inp["k"], inp["v"], bhi, **kw)
+    o_r, l_r = oracle.fwd_rows(rin["q"], rin["k"], rin["v"], bhi, **kw)
+    nh = w.heads_q
+    o_g = np.stack([out["o"].reshape(-1, nh, w.head_dim)[t, h] for t, (_, h, _) in zip(tr, bhi)])
+    l_g = np.array([out["lse"][t, h] for t, (_, h, _) in zip(tr, bhi)])
+    res = [judge("O", o_g, o_m, o_r, w.dtype, O_CAP[w.dtype]),
+           judge("LSE", l_g, l_m, l_r, w.dtype, LSE_CAP, round_out=False)]
+    if not backward:
+        return res
+    dq_m = oracle.dq_rows(inp["q"], inp["k"], inp["v"], inp["do"], bhi, **kw)
+    dq_r = oracle.dq_rows(rin["q"], rin["k"], rin["v"], rin["do"], bhi, **kw)
+    dq_g = np.stack([out["dq"].reshape(-1, nh, w.head_dim)[t, h] for t, (_, h, _) in zip(tr, bhi)])
+    res.append(judge("dQ", dq_g, dq_m, dq_r, w.dtype))
+    bgj = sample_keys(w, inp, n_keys, seed)
+    kt = [kv_token_row(w, inp, b, j) for b, _, j in bgj]
+    dk_m, dv_m = oracle.dkdv_rows(inp["q"], inp["k"], inp["v"], inp["do"], bgj, **kw)
+    dk_r, dv_r = oracle.dkdv_rows(rin["q"], rin["k"], rin["v"], rin["do"], bgj, **kw)
+    nkv = w.heads_kv
+    dk_g = np.stack([out["dk"].reshape(-1, nkv, w.head_dim)[t, g] for t, (_, g, _) in zip(kt, bgj)])
+    dv_g = np.stack([out["dv"].reshape(-1, nkv, w.head_dim)[t, g] for t, (_, g, _) in zip(kt, bgj)])
+    res.append(judge("dK", dk_g, dk_m, dk_r, w.dtype))
+    res.append(judge("dV", dv_g, dv_m, dv_r, w.dtype))
+    return res

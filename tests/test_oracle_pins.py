@@ -277,6 +277,12 @@ def test_row_samplers_agree_with_full_runs():
         np.testing.assert_allclose(o[n], full["o"][row, h], atol=1e-14)
         np.testing.assert_allclose(lse[n], full["lse"][row, h], atol=1e-14)
         np.testing.assert_allclose(dq[n], full["dq"][row, h], atol=1e-14)
+    bgj = np.array([[0, 0, 0], [0, 1, 39], [1, 1, 16], [1, 0, 3], [0, 1, 12]])
+    dk, dv = oracle.dkdv_rows(q, k, v, do, bgj, layout="thd", mask="causal", cu_q=cq, cu_kv=cq, window=(5, 0))
+    for n, (b, g, j) in enumerate(bgj):
+        row = cq[b] + j
+        np.testing.assert_allclose(dk[n], full["dk"][row, g], atol=1e-14)
+        np.testing.assert_allclose(dv[n], full["dv"][row, g], atol=1e-14)
     part = oracle.bwd(q, k, v, do, layout="thd", mask="causal", cu_q=cq, cu_kv=cq, window=(5, 0),
                       batch_range=(1, 2), kv_head_range=(1, 2))
     sl = slice(cq[1], cq[2])
