@@ -105,8 +105,8 @@ __device__ __forceinline__ void p_ds_cols(const uint32_t (&us)[32], const uint32
                            make_float2(nl2[c], nl2[c + 1]));
     float p0 = ex2(t.x), p1 = ex2(t.y);
     if (MASK) {
-      p0 = (q + c >= qlo && q + c < qhi) ? p0 : 0.f;
-      p1 = (q + c + 1 >= qlo && q + c + 1 < qhi) ? p1 : 0.f;
+      p0 = in_range(q + c, qlo, qhi) ? p0 : 0.f;
+      p1 = in_range(q + c + 1, qlo, qhi) ? p1 : 0.f;
     }
     const float2 d = fsub2(make_float2(__uint_as_float(ud[c]), __uint_as_float(ud[c + 1])),
                            make_float2(dl[c], dl[c + 1]));

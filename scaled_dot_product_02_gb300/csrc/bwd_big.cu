@@ -295,8 +295,8 @@ __global__ void __launch_bounds__(256, 1)
               const int key = kbase + half * 64 + c0;
               float p0 = ex2(fmaf(__uint_as_float(x0), sl2, nl2));
               float p1 = ex2(fmaf(__uint_as_float(x1), sl2, nl2));
-              p0 = (key >= lo_i && key < hi_i) ? p0 : 0.f;
-              p1 = (key + 1 >= lo_i && key + 1 < hi_i) ? p1 : 0.f;
+              p0 = in_range(key, lo_i, hi_i) ? p0 : 0.f;
+              p1 = in_range(key + 1, lo_i, hi_i) ? p1 : 0.f;
               w4[e] = E::pack(p0, p1);
               dsk[half * 32 + k * 4 + e] = E::pack(p0 * dv[2 * e], p1 * dv[2 * e + 1]);
             }

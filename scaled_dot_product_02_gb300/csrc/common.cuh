@@ -80,6 +80,12 @@ __device__ __forceinline__ int query_hi(const KeyRange& r, int j, int lq) {
   return r.wl >= 0 ? min(lq, max(0, j - r.off + r.wl + 1)) : lq;
 }
 
+// key in [lo, hi) as one unsigned compare, so masking compiles to a select
+// rather than a branch per element (an empty range, hi <= lo, admits nothing).
+__device__ __forceinline__ bool in_range(int key, int lo, int hi) {
+  return (unsigned)(key - lo) < (unsigned)max(hi - lo, 0);
+}
+
 template <bool BF16>
 struct Elem;
 template <>

@@ -290,10 +290,9 @@ __global__ void __launch_bounds__(256, 1)
         }
       }
       const int kb = (t_lo + j) * C::BN;
-      if (!(lo_last <= kb && hi_first >= kb + C::BN)) {
+      if (!(lo_last <= kb && hi_first >= kb + C::BN)) {  // edge tile (uniform branch)
 #pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (kb + c < lo_i || kb + c >= hi_i) s[c] = -INFINITY;
+        for (int c = 0; c < 128; ++c) s[c] = in_range(kb + c, lo_i, hi_i) ? s[c] : -INFINITY;
       }
       float mt = s[0];
 #pragma unroll
@@ -395,6 +394,338 @@ __global__ void __launch_bounds__(256, 1)
   }
 }
 
+// ---------------------------------------------------------------------------
+// head_dim 128 variant sized for two resident CTAs per SM (192 threads, at
+// most 168 registers, 96 KB of shared memory, 256 TMEM columns: O at
+// [0,128), S/P at [128,256)). With a single S buffer each CTA runs
+// S_j -> softmax_j -> PV_j strictly in turn; the tensor pipe stays busy with
+// the other CTA's MMAs while one CTA is in its softmax, and one CTA's
+// prologue and epilogue overlap the other's main loop.
+// Roles: warps 0-3 softmax + epilogue (one thread per query row), warp 4 TMA
+// producer, warp 5 TMEM allocator + MMA issuer. The softmax reads S from
+// TMEM twice (row max, then exponentials) so it never holds 128 scores in
+// registers.
+struct Fwd2Cfg {
+  static constexpr int Q_BYTES = 32768;
+  static constexpr int STAGE_BYTES = 32768;
+  static constexpr int NSTAGES = 2;
+  static constexpr int NBARS = 2 * NSTAGES + 5;
+  static constexpr int SMEM_BYTES = 1024 + Q_BYTES + NSTAGES * STAGE_BYTES + NBARS * 8 + 16;
+  static constexpr uint32_t TMEM_O = 0, TMEM_S = 128;
+};
+
+template <bool BF16>
+__global__ void __launch_bounds__(192, 2)
+    fwd128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                  const __grid_constant__ CUtensorMap tmV, const __grid_constant__ FwdParams p) {
+  using C = Fwd2Cfg;
+  using E = Elem<BF16>;
+  const Geom& g = p.g;
+  int idx = blockIdx.x;
+  const int h = idx % g.hq;
+  idx /= g.hq;
+  const int b = idx % g.batch;
+  idx /= g.batch;
+  const int qt = p.n_q_tiles - 1 - idx;
+  const SeqInfo si = seq_info(g, b);
+  const int q0 = qt * 128;
+  if (q0 >= si.lq) return;
+  if (p.guard && *reinterpret_cast<volatile const int*>(p.guard)) return;
+
+  const KeyRange kr = key_range(g, si.lq, si.lk);
+  const int q_last = min(q0 + 127, si.lq - 1);
+  const int kv_lo = kr.lo(q0), kv_hi = kr.hi(q_last);
+  const int t_lo = kv_lo / 128;
+  const int n_tiles = (kv_hi > kv_lo) ? (kv_hi + 127) / 128 - t_lo : 0;
+  const int qhead = si.qhead0 + h;
+  const int khead = si.khead0 + h / (g.hq / g.hkv);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* sQ = smem;
+  uint8_t* sStage = smem + C::Q_BYTES;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sStage + C::NSTAGES * C::STAGE_BYTES);
+  uint64_t* empty = full + C::NSTAGES;
+  uint64_t* bar_q = empty + C::NSTAGES;
+  uint64_t* bar_s = bar_q + 1;
+  uint64_t* bar_p = bar_s + 1;
+  uint64_t* bar_o = bar_p + 1;
+  uint64_t* bar_drain = bar_o + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < C::NSTAGES; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(bar_q, 1);
+    mbar_init(bar_s, 1);
+    mbar_init(bar_p, 128);
+    mbar_init(bar_o, 1);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 5) {
+    tmem_alloc(tmem_holder, 256);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer: Q, then K_0, V_0, K_1, V_1, ...
+    if (elect_one() && n_tiles > 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      mbar_arrive_expect_tx(bar_q, C::Q_BYTES);
+      tma_load_3d(&tmQ, bar_q, sQ, 0, qhead, si.qrow0 + q0);
+      tma_load_3d(&tmQ, bar_q, sQ + 16384, 64, qhead, si.qrow0 + q0);
+      int c = 0;
+      bool ok = true;
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        const int key0 = si.krow0 + (t_lo + j) * 128;
+        for (int kv = 0; kv < 2; ++kv, ++c) {
+          const int slot = c % C::NSTAGES;
+          if (!mbar_wait(&empty[slot], ((c / C::NSTAGES) & 1) ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[slot], C::STAGE_BYTES);
+          const CUtensorMap* m = kv ? &tmV : &tmK;
+          uint8_t* dst = sStage + slot * C::STAGE_BYTES;
+          tma_load_3d(m, &full[slot], dst, 0, khead, key0);
+          tma_load_3d(m, &full[slot], dst + 16384, 64, khead, key0);
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        record_error(p.err, SDPA_ERR_TIMEOUT);
+      }
+      const int first = c > C::NSTAGES ? c - C::NSTAGES : 0;
+      for (int k = first; k < c; ++k) mbar_wait_drain(&full[k % C::NSTAGES], (k / C::NSTAGES) & 1);
+      mbar_wait_drain(bar_q, 0);
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (elect_one() && n_tiles > 0) {
+      constexpr uint32_t IDESC_S = idesc_f16(128, 128, BF16, false, false);
+      constexpr uint32_t IDESC_O = idesc_f16(128, 128, BF16, false, true);
+      bool ok = mbar_wait(bar_q, 0, abort_flag);
+      tc_fence_after();
+      const uint32_t q_base = smem_u32(sQ);
+      int c = 0;
+      for (int j = 0; j < n_tiles && ok; ++j) {
+        // S_j = Q K_j^T (the previous PV has been issued, so P_{j-1} is consumed first)
+        int slot = c % C::NSTAGES;
+        if (!mbar_wait(&full[slot], (c / C::NSTAGES) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t base = smem_u32(sStage + slot * C::STAGE_BYTES);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+          mma_ss(tmem + C::TMEM_S, smem_desc_sw128(q_base + off, 16, 1024), smem_desc_sw128(base + off, 16, 1024),
+                 IDESC_S, ks != 0);
+        }
+        mma_commit(&empty[slot]);
+        mma_commit(bar_s);
+        ++c;
+        // O += P_j V_j
+        if (!mbar_wait(bar_p, j & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        slot = c % C::NSTAGES;
+        if (!mbar_wait(&full[slot], (c / C::NSTAGES) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        base = smem_u32(sStage + slot * C::STAGE_BYTES);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks)
+          mma_ts(tmem + C::TMEM_O, tmem + C::TMEM_S + ks * 8, smem_desc_sw128(base + ks * 2048, 16384, 1024),
+                 IDESC_O, (j | ks) != 0);
+        mma_commit(&empty[slot]);
+        mma_commit(bar_o);
+        ++c;
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        record_error(p.err, SDPA_ERR_TIMEOUT);
+        mma_commit(bar_drain);
+        mbar_wait_drain(bar_drain, 0);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ softmax (warps 0-3)
+    const int r = warp * 32 + lane;
+    const int i = q0 + r;
+    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    const uint32_t scol = lane_base + C::TMEM_S;
+    const float sl2 = g.scale_log2;
+    const int lo_i = kr.lo(i), hi_i = kr.hi(i);
+    const int lo_last = kr.lo(q_last), hi_first = kr.hi(q0);
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    for (int j = 0; j < n_tiles; ++j) {
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_s, j & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int kb = (t_lo + j) * 128;
+      const bool interior = lo_last <= kb && hi_first >= kb + 128;
+      // pass 1: row max
+      float mt = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t u[32];
+        tmem_ld32(scol + c * 32, u);
+        tmem_wait_ld();
+        reg_fence(u);
+        if (interior) {
+#pragma unroll
+          for (int e = 0; e < 32; ++e) mt = fmaxf(mt, __uint_as_float(u[e]));
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; ++e)
+            mt = fmaxf(mt, in_range(kb + c * 32 + e, lo_i, hi_i) ? __uint_as_float(u[e]) : -INFINITY);
+        }
+      }
+      const float m_new = fmaxf(m_used, mt);
+      bool need = false;
+      float f = 1.f;
+      if (m_used == -INFINITY) {
+        m_used = m_new;
+      } else if ((m_new - m_used) * sl2 > 8.f) {
+        need = true;
+        f = ex2((m_used - m_new) * sl2);
+        m_used = m_new;
+      }
+      const float mb = (m_used == -INFINITY) ? 0.f : m_used * sl2;
+      // pass 2: P = exp2(S*scale*log2e - m), packed into the first 64 S columns
+      float rs = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t u[32];
+        tmem_ld32(scol + c * 32, u);
+        tmem_wait_ld();
+        reg_fence(u);
+        uint32_t pk[16];
+        if (interior) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const float p0 = ex2(fmaf(__uint_as_float(u[e]), sl2, -mb));
+            const float p1 = ex2(fmaf(__uint_as_float(u[e + 1]), sl2, -mb));
+            rs += p0 + p1;
+            pk[e / 2] = E::pack(p0, p1);
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            const int key = kb + c * 32 + e;
+            const float e0 = ex2(fmaf(__uint_as_float(u[e]), sl2, -mb));
+            const float e1 = ex2(fmaf(__uint_as_float(u[e + 1]), sl2, -mb));
+            const float p0 = in_range(key, lo_i, hi_i) ? e0 : 0.f;
+            const float p1 = in_range(key + 1, lo_i, hi_i) ? e1 : 0.f;
+            rs += p0 + p1;
+            pk[e / 2] = E::pack(p0, p1);
+          }
+        }
+        tmem_st16(scol + c * 16, pk);
+      }
+      l = l * f + rs;
+      // PV_{j-1} completed before S_j was computed (single S buffer), so O
+      // can be rescaled here without waiting.
+      if (__any_sync(0xffffffffu, need) && j > 0) {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t u[32];
+          tmem_ld32(lane_base + C::TMEM_O + c * 32, u);
+          tmem_wait_ld();
+          reg_fence(u);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * f);
+          tmem_st32(lane_base + C::TMEM_O + c * 32, u);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_p);
+    }
+    if (ok && n_tiles > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_o, (n_tiles - 1) & 1, abort_flag));
+      tc_fence_after();
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      record_error(p.err, SDPA_ERR_TIMEOUT);
+    } else {
+      const bool valid = i < si.lq;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      using T = typename E::T;
+      T* orow = reinterpret_cast<T*>(p.o) + ((int64_t)(si.qrow0 + i) * g.nh_q + qhead) * 128;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t packed[16];
+        if (n_tiles > 0) {
+          uint32_t u[32];
+          tmem_ld32(lane_base + C::TMEM_O + c * 32, u);
+          tmem_wait_ld();
+          reg_fence(u);
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            packed[e] = E::pack(__uint_as_float(u[2 * e]) * inv, __uint_as_float(u[2 * e + 1]) * inv);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) packed[e] = 0u;
+        }
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            dst[e] = make_uint4(packed[4 * e], packed[4 * e + 1], packed[4 * e + 2], packed[4 * e + 3]);
+        }
+      }
+      if (valid) p.lse[(int64_t)(si.qrow0 + i) * g.nh_q + qhead] = l > 0.f ? m_used * g.scale + logf(l) : -INFINITY;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 5) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 256);
+  }
+}
+
+template <bool BF16>
+static int launch_fwd128(const FwdLaunch& L) {
+  auto kern = fwd128_kernel<BF16>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    // two CTAs per SM need the largest shared-memory carveout
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Fwd2Cfg::SMEM_BYTES) != cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+      return SDPA_ERR_CUDA;
+    attr_set = true;
+  }
+  const long long grid = (long long)L.p.n_q_tiles * L.p.g.hq * L.p.g.batch;
+  if (grid <= 0) return SDPA_OK;
+  if (grid > 0x7fffffffLL) return SDPA_ERR_UNSUPPORTED;
+  kern<<<(unsigned)grid, 192, Fwd2Cfg::SMEM_BYTES, L.stream>>>(L.tmQ, L.tmK, L.tmV, L.p);
+  return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+}
+
 template <int DQK, int DV, bool BF16>
 static int launch_fwd_t(const FwdLaunch& L) {
   using C = FwdCfg<DQK, DV>;
@@ -413,7 +744,7 @@ static int launch_fwd_t(const FwdLaunch& L) {
 }
 
 int launch_fwd(const FwdLaunch& L, int head_dim, bool bf16) {
-  if (head_dim == 128) return bf16 ? launch_fwd_t<128, 128, true>(L) : launch_fwd_t<128, 128, false>(L);
+  if (head_dim == 128) return bf16 ? launch_fwd128<true>(L) : launch_fwd128<false>(L);
   if (head_dim == 256) return bf16 ? launch_fwd_t<256, 256, true>(L) : launch_fwd_t<256, 256, false>(L);
   if (head_dim == 512) return bf16 ? launch_fwd_t<512, 256, true>(L) : launch_fwd_t<512, 256, false>(L);
   return SDPA_ERR_UNSUPPORTED;
