@@ -402,9 +402,39 @@ __global__ void __launch_bounds__(256, 1)
 // the other CTA's MMAs while one CTA is in its softmax, and one CTA's
 // prologue and epilogue overlap the other's main loop.
 // Roles: warps 0-3 softmax + epilogue (one thread per query row), warp 4 TMA
-// producer, warp 5 TMEM allocator + MMA issuer. The softmax reads S from
-// TMEM twice (row max, then exponentials) so it never holds 128 scores in
-// registers.
+// producer, warp 5 TMEM allocator + MMA issuer. The softmax makes one pass
+// over S in TMEM per key tile (a second one only when a row's max moves).
+// One pass of the head_dim 128 softmax over the 128 scores of a row held in
+// TMEM: t = S*scale*log2e - mb, P = exp2(t) packed to 16-bit pairs (zero
+// where masked), the row sum of P and the largest t among allowed keys.
+template <bool MASK, class E>
+__device__ __forceinline__ void p_pass(uint32_t scol, float sl2, float mb, int kb, int lo, int hi,
+                                       uint32_t (&pk)[64], float& rs, float& tmax) {
+  const float2 sc = make_float2(sl2, sl2), nm = make_float2(-mb, -mb);
+  float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t u[32];
+    tmem_ld32(scol + c * 32, u);
+    tmem_wait_ld();
+    reg_fence(u);
+#pragma unroll
+    for (int e = 0; e < 32; e += 2) {
+      float2 t = ffma2(make_float2(__uint_as_float(u[e]), __uint_as_float(u[e + 1])), sc, nm);
+      if (MASK) {
+        const int key = kb + c * 32 + e;
+        t.x = in_range(key, lo, hi) ? t.x : -INFINITY;
+        t.y = in_range(key + 1, lo, hi) ? t.y : -INFINITY;
+      }
+      tmax = fmaxf(tmax, fmaxf(t.x, t.y));
+      const float2 p = make_float2(ex2(t.x), ex2(t.y));
+      pk[c * 16 + e / 2] = E::pack(p.x, p.y);
+      acc = fadd2(acc, p);
+    }
+  }
+  rs = acc.x + acc.y;
+}
+
 struct Fwd2Cfg {
   static constexpr int Q_BYTES = 32768;
   static constexpr int STAGE_BYTES = 32768;
@@ -574,7 +604,7 @@ __global__ void __launch_bounds__(192, 2)
     const float sl2 = g.scale_log2;
     const int lo_i = kr.lo(i), hi_i = kr.hi(i);
     const int lo_last = kr.lo(q_last), hi_first = kr.hi(q0);
-    float m_used = -INFINITY, l = 0.f;
+    float mbs = -INFINITY, l = 0.f;  // running max of S*scale*log2e, and the row sum
     bool ok = true;
     for (int j = 0; j < n_tiles; ++j) {
       if (!__all_sync(0xffffffffu, mbar_wait(bar_s, j & 1, abort_flag))) {
@@ -584,69 +614,49 @@ __global__ void __launch_bounds__(192, 2)
       tc_fence_after();
       const int kb = (t_lo + j) * 128;
       const bool interior = lo_last <= kb && hi_first >= kb + 128;
-      // pass 1: row max
-      float mt = -INFINITY;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t u[32];
-        tmem_ld32(scol + c * 32, u);
-        tmem_wait_ld();
-        reg_fence(u);
-        if (interior) {
-#pragma unroll
-          for (int e = 0; e < 32; ++e) mt = fmaxf(mt, __uint_as_float(u[e]));
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; ++e)
-            mt = fmaxf(mt, in_range(kb + c * 32 + e, lo_i, hi_i) ? __uint_as_float(u[e]) : -INFINITY);
-        }
-      }
-      const float m_new = fmaxf(m_used, mt);
-      bool need = false;
+      // One pass: P against the running max m (P = exp2(S*scale*log2e - m)),
+      // keeping the largest exponent t. While t <= 8 every P is <= 256 and
+      // m can stay as it is. A row whose scores jumped higher (or that sees
+      // its first allowed key) is recomputed against its new max (S is still
+      // intact in TMEM: P is only written back after the check), and O and l
+      // are rescaled by exp2(-t).
+      const float mb = (mbs == -INFINITY) ? 0.f : mbs;
+      float rs = 0.f, tmax = -INFINITY;
+      uint32_t pk[64];
+      if (interior)
+        p_pass<false, E>(scol, sl2, mb, kb, lo_i, hi_i, pk, rs, tmax);
+      else
+        p_pass<true, E>(scol, sl2, mb, kb, lo_i, hi_i, pk, rs, tmax);
+      // A row's first allowed keys always take the second pass, against its
+      // exact max: its largest P is then exactly 1, so the rounding of the
+      // dominant P cannot bias O against the LSE.
+      const bool redo = tmax > 8.f || (mbs == -INFINITY && tmax > -INFINITY);
       float f = 1.f;
-      if (m_used == -INFINITY) {
-        m_used = m_new;
-      } else if ((m_new - m_used) * sl2 > 8.f) {
-        need = true;
-        f = ex2((m_used - m_new) * sl2);
-        m_used = m_new;
+      if (__any_sync(0xffffffffu, redo)) {
+        // the whole warp repeats the pass (TMEM loads are warp-wide); rows
+        // that keep their max recompute bit-identical values
+        const float mb2 = redo ? mb + tmax : mb;
+        float t2 = -INFINITY;
+        if (interior)
+          p_pass<false, E>(scol, sl2, mb2, kb, lo_i, hi_i, pk, rs, t2);
+        else
+          p_pass<true, E>(scol, sl2, mb2, kb, lo_i, hi_i, pk, rs, t2);
       }
-      const float mb = (m_used == -INFINITY) ? 0.f : m_used * sl2;
-      // pass 2: P = exp2(S*scale*log2e - m), packed into the first 64 S columns
-      float rs = 0.f;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t u[32];
-        tmem_ld32(scol + c * 32, u);
-        tmem_wait_ld();
-        reg_fence(u);
-        uint32_t pk[16];
-        if (interior) {
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const float p0 = ex2(fmaf(__uint_as_float(u[e]), sl2, -mb));
-            const float p1 = ex2(fmaf(__uint_as_float(u[e + 1]), sl2, -mb));
-            rs += p0 + p1;
-            pk[e / 2] = E::pack(p0, p1);
-          }
-        } else {
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            const int key = kb + c * 32 + e;
-            const float e0 = ex2(fmaf(__uint_as_float(u[e]), sl2, -mb));
-            const float e1 = ex2(fmaf(__uint_as_float(u[e + 1]), sl2, -mb));
-            const float p0 = in_range(key, lo_i, hi_i) ? e0 : 0.f;
-            const float p1 = in_range(key + 1, lo_i, hi_i) ? e1 : 0.f;
-            rs += p0 + p1;
-            pk[e / 2] = E::pack(p0, p1);
-          }
-        }
-        tmem_st16(scol + c * 16, pk);
+      if (redo) {
+        f = mbs == -INFINITY ? 0.f : ex2(-tmax);
+        mbs = mb + tmax;
       }
       l = l * f + rs;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t q16[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) q16[e] = pk[c * 16 + e];
+        tmem_st16(scol + c * 16, q16);
+      }
       // PV_{j-1} completed before S_j was computed (single S buffer), so O
       // can be rescaled here without waiting.
-      if (__any_sync(0xffffffffu, need) && j > 0) {
+      if (__any_sync(0xffffffffu, f != 1.f) && j > 0) {
 #pragma unroll 1
         for (int c = 0; c < 4; ++c) {
           uint32_t u[32];
@@ -696,7 +706,8 @@ __global__ void __launch_bounds__(192, 2)
             dst[e] = make_uint4(packed[4 * e], packed[4 * e + 1], packed[4 * e + 2], packed[4 * e + 3]);
         }
       }
-      if (valid) p.lse[(int64_t)(si.qrow0 + i) * g.nh_q + qhead] = l > 0.f ? m_used * g.scale + logf(l) : -INFINITY;
+      if (valid)
+        p.lse[(int64_t)(si.qrow0 + i) * g.nh_q + qhead] = l > 0.f ? mbs * 0.6931471805599453f + logf(l) : -INFINITY;
     }
   }
 
