@@ -221,7 +221,8 @@ BwdWs bwd_ws(const sdpa_problem* p) {
     w.ptile_off = round_up(after_stats, 1024);
     w.dstile_off = w.ptile_off + tiles * 32768;
     w.dpdtile_off = w.dstile_off + tiles * 32768;
-    w.total = w.dpdtile_off + tiles * 65536;
+    // the fp32 dP - delta tiles exist only for head_dim 512 (256 forms dS in one pass)
+    w.total = w.dpdtile_off + (p->head_dim == 512 ? tiles * 65536 : 0);
   }
   return w;
 }

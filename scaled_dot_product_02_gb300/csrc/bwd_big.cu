@@ -4,7 +4,8 @@
 // 2*D fp32 TMEM columns (512 or 1024) and do not fit next to the score
 // tiles, so the backward runs in two phases:
 //
-// Phase 1, score kernels (one CTA per 128-query tile of one (batch, q head)):
+// Phase 1, score kernels (one CTA per 128-query tile of one (batch, q head));
+// for head_dim 256 one fused kernel (below) does both passes, for 512:
 //   pass 0: dP = dO V^T over the full head dim (dO resident in shared
 //           memory, V streamed in 128x128 chunks); dP - delta kept as fp32;
 //   pass 1: S = Q K^T likewise, P = exp2(S*scale*log2e - LSE*log2e) masked,
@@ -344,6 +345,228 @@ __global__ void __launch_bounds__(256, 1)
   }
 }
 
+// ---------------------------------------------------------------------- head_dim 256
+// Both passes in one kernel: Q and dO stay resident (64 KB each), K and V
+// stream through a ring of 32 KB chunks, S and dP of a key tile land side by
+// side in TMEM (double-buffered, 512 columns), and the epilogue forms P and
+// dS in fp32 (each rounded once) and writes both 16-bit tile images straight
+// to global memory: nothing fp32 goes through HBM.
+constexpr int SF_NST = 3;
+constexpr int SF_NBARS = 2 * SF_NST + 8;
+constexpr int SF_SMEM = 1024 + 2 * 65536 + SF_NST * CHUNK_BYTES + SF_NBARS * 8 + 16;
+
+template <bool BF16>
+__global__ void __launch_bounds__(256, 1)
+    score_fused256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+                          const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                          const __grid_constant__ BigBwdParams p) {
+  using E = Elem<BF16>;
+  const Geom& g = p.g;
+  int idx = blockIdx.x;
+  const int h = idx % g.hq;
+  idx /= g.hq;
+  const int b = idx % g.batch;
+  const int qt = p.n_q_tiles - 1 - idx / g.batch;
+  const SeqInfo si = seq_info(g, b);
+  const int q0 = qt * 128;
+  if (q0 >= si.lq) return;
+  if (p.guard && *reinterpret_cast<volatile const int*>(p.guard)) return;
+  const KeyRange kr = key_range(g, si.lq, si.lk);
+  int t_lo, n;
+  kv_tiles_of(kr, q0, si.lq, t_lo, n);
+  if (n > p.slots) {
+    if (threadIdx.x == 0) record_error(p.err, SDPA_ERR_INVALID_ARG);
+    return;
+  }
+  const int qhead = si.qhead0 + h;
+  const int khead = si.khead0 + h / (g.hq / g.hkv);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* sQ = smem;
+  uint8_t* sDO = smem + 65536;
+  uint8_t* sStage = smem + 2 * 65536;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sStage + SF_NST * CHUNK_BYTES);
+  uint64_t* empty = full + SF_NST;
+  uint64_t* bar_a = empty + SF_NST;
+  uint64_t* bar_s = bar_a + 1;      // [2] S and dP of a key tile ready
+  uint64_t* bar_sfree = bar_s + 2;  // [2] epilogue has read them
+  uint64_t* bar_drain = bar_sfree + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < SF_NST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(bar_a, 1);
+    mbar_init(&bar_s[0], 1);
+    mbar_init(&bar_s[1], 1);
+    mbar_init(&bar_sfree[0], 128);
+    mbar_init(&bar_sfree[1], 128);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  if (warp == 0) {
+    if (elect_one() && n > 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmDO);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      mbar_arrive_expect_tx(bar_a, 2 * 65536);
+      for (int a = 0; a < 4; ++a) {
+        tma_load_3d(&tmQ, bar_a, sQ + a * 16384, a * 64, qhead, si.qrow0 + q0);
+        tma_load_3d(&tmDO, bar_a, sDO + a * 16384, a * 64, qhead, si.qrow0 + q0);
+      }
+      int c = 0;
+      bool ok = true;
+      for (int t = 0; t < n && ok; ++t) {
+        const int krow = si.krow0 + (t_lo + t) * 128;
+        for (int kc = 0; kc < 4; ++kc, ++c) {  // K chunk 0, K chunk 1, V chunk 0, V chunk 1
+          const int slot = c % SF_NST;
+          if (!mbar_wait(&empty[slot], ((c / SF_NST) & 1) ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[slot], CHUNK_BYTES);
+          const CUtensorMap* m = kc < 2 ? &tmK : &tmV;
+          const int d0 = (kc & 1) * 128;
+          uint8_t* dst = sStage + slot * CHUNK_BYTES;
+          tma_load_3d(m, &full[slot], dst, d0, khead, krow);
+          tma_load_3d(m, &full[slot], dst + 16384, d0 + 64, khead, krow);
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        record_error(p.err, SDPA_ERR_TIMEOUT);
+      }
+      const int first = c > SF_NST ? c - SF_NST : 0;
+      for (int k = first; k < c; ++k) wait_drain_big(&full[k % SF_NST], (k / SF_NST) & 1);
+      wait_drain_big(bar_a, 0);
+    }
+  } else if (warp == 1) {
+    if (elect_one() && n > 0) {
+      constexpr uint32_t IDESC = idesc_f16(128, 128, BF16, false, false);
+      bool ok = mbar_wait(bar_a, 0, abort_flag);
+      tc_fence_after();
+      int c = 0;
+      for (int t = 0; t < n && ok; ++t) {
+        const int buf = t & 1;
+        if (t >= 2 && !mbar_wait(&bar_sfree[buf], ((t >> 1) & 1) ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        for (int kc = 0; kc < 4 && ok; ++kc, ++c) {
+          const int slot = c % SF_NST;
+          if (!mbar_wait(&full[slot], (c / SF_NST) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t bb = smem_u32(sStage + slot * CHUNK_BYTES);
+          // S = Q K^T into columns [256*buf, +128), dP = dO V^T into [+128, +256)
+          const uint32_t aa = smem_u32(kc < 2 ? sQ : sDO) + (kc & 1) * 2 * 16384;
+          const uint32_t d = tmem + buf * 256 + (kc < 2 ? 0 : 128);
+#pragma unroll
+          for (int ks = 0; ks < 8; ++ks) {
+            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+            mma_ss(d, smem_desc_sw128(aa + off, 16, 1024), smem_desc_sw128(bb + off, 16, 1024), IDESC,
+                   ((kc & 1) | ks) != 0);
+          }
+          mma_commit(&empty[slot]);
+        }
+        if (ok) mma_commit(&bar_s[buf]);
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        record_error(p.err, SDPA_ERR_TIMEOUT);
+        mma_commit(bar_drain);
+        wait_drain_big(bar_drain, 0);
+      }
+    }
+  } else if (warp >= 4) {
+    const int wq = warp - 4;
+    const int r = wq * 32 + lane;
+    const int i = q0 + r;
+    const bool valid = i < si.lq;
+    const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
+    const long long stat = (long long)qhead * p.stat_rows + si.qrow0 + i;
+    // rows past the sequence end belong to no query: their P (and so dS) is zero
+    const float nl2 = valid ? p.nlse2[stat] : -INFINITY;
+    const float dl = valid ? p.delta[stat] : 0.f;
+    const int lo_i = kr.lo(i), hi_i = kr.hi(i);
+    const float sl2 = g.scale_log2;
+    bool ok = true;
+    for (int t = 0; t < n; ++t) {
+      const int buf = t & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar_s[buf], (t >> 1) & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const long long tix = tile_index(p, b, h, qt, t);
+      uint8_t* prow = p.p_tiles + tix * TILE_BYTES;
+      uint8_t* drow = p.ds_tiles + tix * TILE_BYTES;
+      const int kbase = (t_lo + t) * 128;
+#pragma unroll 1
+      for (int qd = 0; qd < 4; ++qd) {  // 32 keys at a time
+        uint32_t us[32], ud[32];
+        tmem_ld32(lane_base + buf * 256 + qd * 32, us);
+        tmem_ld32(lane_base + buf * 256 + 128 + qd * 32, ud);
+        tmem_wait_ld();
+        fence_regs32(us);
+        fence_regs32(ud);
+        if (qd == 3) {
+          tc_fence_before();
+          mbar_arrive(&bar_sfree[buf]);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {  // 4 chunks of 8 keys
+          uint32_t wp[4], wd[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c0 = k * 8 + 2 * e;
+            const int key = kbase + qd * 32 + c0;
+            const float e0 = ex2(fmaf(__uint_as_float(us[c0]), sl2, nl2));
+            const float e1 = ex2(fmaf(__uint_as_float(us[c0 + 1]), sl2, nl2));
+            const float p0 = in_range(key, lo_i, hi_i) ? e0 : 0.f;
+            const float p1 = in_range(key + 1, lo_i, hi_i) ? e1 : 0.f;
+            wp[e] = E::pack(p0, p1);
+            wd[e] = E::pack(p0 * (__uint_as_float(ud[c0]) - dl), p1 * (__uint_as_float(ud[c0 + 1]) - dl));
+          }
+          const uint32_t off = tile_chunk_off(r, qd * 4 + k);
+          *reinterpret_cast<uint4*>(prow + off) = make_uint4(wp[0], wp[1], wp[2], wp[3]);
+          *reinterpret_cast<uint4*>(drow + off) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+        }
+      }
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      record_error(p.err, SDPA_ERR_TIMEOUT);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 // ====================================================================== phase 2
 constexpr int GB_STAGE = TILE_BYTES + 4 * 16384;  // tile image + 128 rows x 256 columns of B
 constexpr int GB_NST = 2;
@@ -585,10 +808,22 @@ static int launch_big_t(const BigBwdLaunch& L, int* launches) {
   }
   int n = 0;
   if (g1 > 0) {
-    s0<<<(unsigned)g1, 256, C::SMEM_BYTES, L.stream>>>(L.tmDO, L.tmV, p);
-    s1<<<(unsigned)g1, 256, C::SMEM_BYTES, L.stream>>>(L.tmQ, L.tmK, p);
+    if (DQK == 256) {
+      auto sf = score_fused256_kernel<BF16>;
+      static bool attr_f = false;
+      if (!attr_f) {
+        if (!set_smem(sf, SF_SMEM)) return SDPA_ERR_CUDA;
+        attr_f = true;
+      }
+      sf<<<(unsigned)g1, 256, SF_SMEM, L.stream>>>(L.tmQ, L.tmDO, L.tmK, L.tmV, p);
+      n += 1;
+    } else {
+      s0<<<(unsigned)g1, 256, C::SMEM_BYTES, L.stream>>>(L.tmDO, L.tmV, p);
+      s1<<<(unsigned)g1, 256, C::SMEM_BYTES, L.stream>>>(L.tmQ, L.tmK, p);
+      n += 2;
+    }
     m0<<<(unsigned)gq, 256, GB_SMEM, L.stream>>>(L.tmK, p);
-    n += 3;
+    n += 1;
   }
   if (gkv > 0) {
     m1<<<(unsigned)gkv, 256, GB_SMEM, L.stream>>>(L.tmDO, p);
