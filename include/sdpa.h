@@ -166,6 +166,13 @@ SDPA_API int sdpa_bwd_noalloc(const sdpa_problem* p, const void* q, const void* 
                               const float* lse, const void* dout, void* dq, void* dk, void* dv,
                               const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv, void* stream);
 
+/* Failure-path self-test of the bounded waits every pipelined kernel uses:
+ * launches one thread that waits on a barrier nothing arrives on, gives up
+ * after limit_us microseconds (1 .. 1,000,000) and records SDPA_ERR_TIMEOUT
+ * in the device error word, as a stalled kernel would. The GPU context stays
+ * usable; read and clear the result with sdpa_get_device_error. */
+SDPA_API int sdpa_selftest_bounded_wait(unsigned limit_us, void* stream);
+
 /* Kernel timing for benchmarks and tracing. Between sdpa_profile_begin and
  * sdpa_profile_end, every sdpa_fwd / sdpa_bwd call made by this host thread
  * records a pair of CUDA events on its stream around each kernel it

@@ -25,7 +25,7 @@ STATUS = {0: "SDPA_OK", 1: "SDPA_ERR_INVALID_ARG", 2: "SDPA_ERR_UNSUPPORTED", 3:
           7: "SDPA_ERR_TIMEOUT", 8: "SDPA_ERR_CUDA"}
 EXPORTS = ("sdpa_fwd_workspace_size", "sdpa_bwd_workspace_size", "sdpa_check_problem", "sdpa_fwd", "sdpa_bwd",
            "sdpa_get_device_error", "sdpa_error_string", "sdpa_last_launch_count", "sdpa_profile_begin",
-           "sdpa_profile_end", "sdpa_bwd_noalloc")
+           "sdpa_profile_end", "sdpa_bwd_noalloc", "sdpa_selftest_bounded_wait")
 NOALLOC_MAX_BYTES = 32 << 20  # SDPA_BWD_NOALLOC_MAX_BYTES
 KERNEL_KINDS = ("fwd", "bwd", "preprocess", "dq_finalize", "guard")
 
@@ -67,6 +67,7 @@ def lib():
             L.sdpa_error_string.argtypes = [ctypes.c_int]
             L.sdpa_error_string.restype = ctypes.c_char_p
             L.sdpa_last_launch_count.restype = ctypes.c_int
+            L.sdpa_selftest_bounded_wait.argtypes = [ctypes.c_uint, vp]
             L.sdpa_bwd_noalloc.argtypes = [pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
             L.sdpa_profile_end.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int),
                                            ctypes.c_int]
@@ -240,3 +241,10 @@ def sdpa_profile_end() -> dict:
     if rc:
         raise SdpaError(rc, "sdpa_profile_end")
     return {k: (ms[i], cnt[i]) for i, k in enumerate(KERNEL_KINDS)}
+
+
+def sdpa_selftest_bounded_wait(limit_us: int = 20000, stream=None) -> None:
+    """Launch the bounded-wait self-test (records SDPA_ERR_TIMEOUT on the device)."""
+    rc = lib().sdpa_selftest_bounded_wait(int(limit_us), _stream(stream))
+    if rc:
+        raise SdpaError(rc, "sdpa_selftest_bounded_wait")

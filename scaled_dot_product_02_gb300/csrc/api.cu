@@ -444,6 +444,13 @@ const char* sdpa_error_string(int status) {
 
 int sdpa_last_launch_count(void) { return t_last_launches; }
 
+int sdpa_selftest_bounded_wait(unsigned limit_us, void* stream) {
+  int* err = error_word();
+  if (!err) return SDPA_ERR_CUDA;
+  if (limit_us == 0 || limit_us > 1000000u) return SDPA_ERR_INVALID_ARG;
+  return launch_wait_selftest((uint64_t)limit_us * 1000ull, err, static_cast<cudaStream_t>(stream));
+}
+
 int sdpa_profile_begin(void) {
   t_prof.on = true;
   t_prof.used = 0;

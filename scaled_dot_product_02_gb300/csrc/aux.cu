@@ -10,6 +10,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "ptx.cuh"
 
 namespace sdpa {
 
@@ -149,6 +150,26 @@ int launch_dq_finalize(const Geom& g, const float* dq_acc, void* dq, const int* 
     dq_finalize_kernel<true><<<grid, 256, 0, s>>>(g, dq_acc, dq, guard);
   else
     dq_finalize_kernel<false><<<grid, 256, 0, s>>>(g, dq_acc, dq, guard);
+  return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+}
+
+// Exercises the bounded wait every pipelined kernel uses: one thread waits on
+// an mbarrier that nothing ever arrives on, gives up after `limit_ns`, and
+// records SDPA_ERR_TIMEOUT exactly as a stalled kernel would.
+__global__ void bounded_wait_selftest_kernel(uint64_t limit_ns, int* err) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0 && !mbar_wait(&bar, 0, &abort_flag, limit_ns)) record_error(err, SDPA_ERR_TIMEOUT);
+}
+
+int launch_wait_selftest(uint64_t limit_ns, int* err, cudaStream_t s) {
+  bounded_wait_selftest_kernel<<<1, 32, 0, s>>>(limit_ns, err);
   return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }
 

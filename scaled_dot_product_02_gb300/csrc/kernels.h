@@ -88,6 +88,7 @@ struct PrepParams {
 };
 int launch_guard(const Geom& g, int total_q, int total_kv, int* guard, int* err, cudaStream_t s);
 int launch_preprocess(const PrepParams& pp, bool bf16, cudaStream_t s);
+int launch_wait_selftest(uint64_t limit_ns, int* err, cudaStream_t s);
 int launch_dq_finalize(const Geom& g, const float* dq_acc, void* dq, const int* guard, bool bf16, cudaStream_t s);
 
 }  // namespace sdpa

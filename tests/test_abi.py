@@ -37,7 +37,7 @@ def test_library_exports_every_declared_symbol(pkg):
     lib = ctypes.CDLL(pkg.LIB_PATH)
     for name in declared_functions():
         assert hasattr(lib, name), name
-    assert set(declared_functions()) <= set(pkg.EXPORTS) | {"sdpa_bwd_noalloc"}
+    assert set(declared_functions()) <= set(pkg.EXPORTS)
 
 
 def test_error_strings(pkg):
@@ -92,3 +92,49 @@ def test_product_path_refuses_cpu_tensors(pkg):
     q = torch.zeros(1, 128, 2, 128, dtype=torch.bfloat16)
     with pytest.raises(ValueError):
         pkg.sdpa_fwd(q, q, q, mask="causal")
+
+
+def test_host_validation_before_any_cuda_call(pkg):
+    """Alignment, null-pointer, workspace and overlap checks return before the
+    library touches CUDA, so they run here with made-up addresses."""
+    import ctypes
+
+    L = pkg.lib()
+    p = problem(pkg, batch=1, seqlen_q=256, seqlen_kv=256, num_heads_q=2, num_heads_kv=2)
+    n = 256 * 2 * 128 * 2  # bytes of one 16-bit [1, 256, 2, 128] tensor
+    base = 1 << 40
+    q, k, v, o = base, base + n, base + 2 * n, base + 3 * n
+    lse = base + 4 * n
+    ptr = ctypes.c_void_p
+    call = lambda *a: L.sdpa_fwd(ctypes.byref(p), *[ptr(x) if x is not None else None for x in a], 0, None)
+    assert call(q + 8, k, v, o, lse, None, None, None) == 3        # misaligned q
+    assert call(q, k, v, o, lse + 4, None, None, None) == 3        # misaligned lse
+    assert call(None, k, v, o, lse, None, None, None) == 1         # null input
+    assert call(q, k, v, q + 64, lse, None, None, None) == 4       # o overlaps q
+    assert call(q, k, v, o, o + 16, None, None, None) == 4         # lse overlaps o
+    t = problem(pkg, layout=2, batch=2, seqlen_q=128, seqlen_kv=128, total_q=256, total_kv=256, num_heads_q=2,
+                num_heads_kv=2)
+    ws = pkg.sdpa_fwd_workspace_size(t)
+    assert ws > 0
+    rc = L.sdpa_fwd(ctypes.byref(t), ptr(q), ptr(k), ptr(v), ptr(o), ptr(lse), ptr(base + 8 * n), ptr(base + 9 * n),
+                    None, 0, None)
+    assert rc == 5                                                 # THD needs its guard workspace
+    rc = L.sdpa_fwd(ctypes.byref(t), ptr(q), ptr(k), ptr(v), ptr(o), ptr(lse), None, None, ptr(base + 10 * n), ws,
+                    None)
+    assert rc == 1                                                 # THD without cu_seqlens
+    # backward: workspace too small, and an output overlapping the workspace
+    wsb = pkg.sdpa_bwd_workspace_size(p)
+    bcall = lambda wsp, wsz, dq: L.sdpa_bwd(ctypes.byref(p), ptr(q), ptr(k), ptr(v), ptr(o), ptr(lse), ptr(o),
+                                            ptr(dq), ptr(base + 7 * n), ptr(base + 8 * n), None, None, ptr(wsp), wsz,
+                                            None)
+    ws0 = base + (1 << 30)
+    assert bcall(ws0, wsb - 256, base + 6 * n) == 5
+    assert bcall(ws0, wsb, ws0 + 256) == 4
+    assert bcall(ws0 + 16, wsb, base + 6 * n) == 3                 # workspace must be 256-byte aligned
+
+
+def test_zero_sized_problems_are_no_ops(pkg):
+    import ctypes
+
+    p = problem(pkg, batch=0)
+    assert pkg.lib().sdpa_fwd(ctypes.byref(p), None, None, None, None, None, None, None, None, 0, None) == 0
