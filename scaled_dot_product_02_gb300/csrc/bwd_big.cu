@@ -347,16 +347,18 @@ __global__ void __launch_bounds__(256, 1)
 
 // ---------------------------------------------------------------------- head_dim 256
 // Both passes in one kernel: Q and dO stay resident (64 KB each), K and V
-// stream through a ring of 32 KB chunks, S and dP of a key tile land side by
-// side in TMEM (double-buffered, 512 columns), and the epilogue forms P and
-// dS in fp32 (each rounded once) and writes both 16-bit tile images straight
-// to global memory: nothing fp32 goes through HBM.
-constexpr int SF_NST = 3;
+// stream through a ring of 16 KB chunks (128 keys x 64 columns), S and dP of
+// a key tile land side by side in TMEM (double-buffered, 512 columns), and
+// the epilogue forms P and dS in fp32 (each rounded once) and writes the two
+// 16-bit tile images through one 32 KB staging buffer with bulk copies:
+// nothing fp32 goes through HBM and the stores leave in whole 32 KB blocks.
+constexpr int SF_CH = 16384;  // ring chunk: 128 keys x 64 columns
+constexpr int SF_NST = 4;
 constexpr int SF_NBARS = 2 * SF_NST + 8;
-constexpr int SF_SMEM = 1024 + 2 * 65536 + SF_NST * CHUNK_BYTES + SF_NBARS * 8 + 16;
+constexpr int SF_SMEM = 1024 + 2 * 65536 + SF_NST * SF_CH + TILE_BYTES + SF_NBARS * 8 + 16;
 
 template <bool BF16>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(384, 1)
     score_fused256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
                           const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                           const __grid_constant__ BigBwdParams p) {
@@ -386,7 +388,8 @@ __global__ void __launch_bounds__(256, 1)
   uint8_t* sQ = smem;
   uint8_t* sDO = smem + 65536;
   uint8_t* sStage = smem + 2 * 65536;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sStage + SF_NST * CHUNK_BYTES);
+  uint8_t* sTile = sStage + SF_NST * SF_CH;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sTile + TILE_BYTES);
   uint64_t* empty = full + SF_NST;
   uint64_t* bar_a = empty + SF_NST;
   uint64_t* bar_s = bar_a + 1;      // [2] S and dP of a key tile ready
@@ -404,8 +407,8 @@ __global__ void __launch_bounds__(256, 1)
     mbar_init(bar_a, 1);
     mbar_init(&bar_s[0], 1);
     mbar_init(&bar_s[1], 1);
-    mbar_init(&bar_sfree[0], 128);
-    mbar_init(&bar_sfree[1], 128);
+    mbar_init(&bar_sfree[0], 256);
+    mbar_init(&bar_sfree[1], 256);
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -434,18 +437,14 @@ __global__ void __launch_bounds__(256, 1)
       bool ok = true;
       for (int t = 0; t < n && ok; ++t) {
         const int krow = si.krow0 + (t_lo + t) * 128;
-        for (int kc = 0; kc < 4; ++kc, ++c) {  // K chunk 0, K chunk 1, V chunk 0, V chunk 1
+        for (int kc = 0; kc < 8; ++kc, ++c) {  // K columns 0..255 in four chunks, then V likewise
           const int slot = c % SF_NST;
           if (!mbar_wait(&empty[slot], ((c / SF_NST) & 1) ^ 1, abort_flag)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(&full[slot], CHUNK_BYTES);
-          const CUtensorMap* m = kc < 2 ? &tmK : &tmV;
-          const int d0 = (kc & 1) * 128;
-          uint8_t* dst = sStage + slot * CHUNK_BYTES;
-          tma_load_3d(m, &full[slot], dst, d0, khead, krow);
-          tma_load_3d(m, &full[slot], dst + 16384, d0 + 64, khead, krow);
+          mbar_arrive_expect_tx(&full[slot], SF_CH);
+          tma_load_3d(kc < 4 ? &tmK : &tmV, &full[slot], sStage + slot * SF_CH, (kc & 3) * 64, khead, krow);
         }
       }
       if (!ok) {
@@ -469,23 +468,21 @@ __global__ void __launch_bounds__(256, 1)
           break;
         }
         tc_fence_after();
-        for (int kc = 0; kc < 4 && ok; ++kc, ++c) {
+        for (int kc = 0; kc < 8 && ok; ++kc, ++c) {
           const int slot = c % SF_NST;
           if (!mbar_wait(&full[slot], (c / SF_NST) & 1, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t bb = smem_u32(sStage + slot * CHUNK_BYTES);
+          const uint32_t bb = smem_u32(sStage + slot * SF_CH);
           // S = Q K^T into columns [256*buf, +128), dP = dO V^T into [+128, +256)
-          const uint32_t aa = smem_u32(kc < 2 ? sQ : sDO) + (kc & 1) * 2 * 16384;
-          const uint32_t d = tmem + buf * 256 + (kc < 2 ? 0 : 128);
+          const uint32_t aa = smem_u32(kc < 4 ? sQ : sDO) + (kc & 3) * 16384;
+          const uint32_t d = tmem + buf * 256 + (kc < 4 ? 0 : 128);
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-            mma_ss(d, smem_desc_sw128(aa + off, 16, 1024), smem_desc_sw128(bb + off, 16, 1024), IDESC,
-                   ((kc & 1) | ks) != 0);
-          }
+          for (int ks = 0; ks < 4; ++ks)
+            mma_ss(d, smem_desc_sw128(aa + ks * 32, 16, 1024), smem_desc_sw128(bb + ks * 32, 16, 1024), IDESC,
+                   ((kc & 3) | ks) != 0);
           mma_commit(&empty[slot]);
         }
         if (ok) mma_commit(&bar_s[buf]);
@@ -498,7 +495,10 @@ __global__ void __launch_bounds__(256, 1)
       }
     }
   } else if (warp >= 4) {
-    const int wq = warp - 4;
+    // two warpgroups: keys [64*half, 64*half + 64) of every tile, i.e. one
+    // 64-column atom of each tile image
+    const int half = (warp - 4) >> 2;
+    const int wq = warp & 3;
     const int r = wq * 32 + lane;
     const int i = q0 + r;
     const bool valid = i < si.lq;
@@ -509,6 +509,7 @@ __global__ void __launch_bounds__(256, 1)
     const float dl = valid ? p.delta[stat] : 0.f;
     const int lo_i = kr.lo(i), hi_i = kr.hi(i);
     const float sl2 = g.scale_log2;
+    const bool leader = threadIdx.x == 128;
     bool ok = true;
     for (int t = 0; t < n; ++t) {
       const int buf = t & 1;
@@ -518,24 +519,26 @@ __global__ void __launch_bounds__(256, 1)
       }
       tc_fence_after();
       const long long tix = tile_index(p, b, h, qt, t);
-      uint8_t* prow = p.p_tiles + tix * TILE_BYTES;
-      uint8_t* drow = p.ds_tiles + tix * TILE_BYTES;
       const int kbase = (t_lo + t) * 128;
-#pragma unroll 1
-      for (int qd = 0; qd < 4; ++qd) {  // 32 keys at a time
+      if (leader) bulk_wait_group_read0();  // the previous tile's dS image has left the buffer
+      bar_sync_id(1, 256);
+      uint32_t dsk[32];  // packed dS of this half row, staged after the P image
+#pragma unroll
+      for (int qq = 0; qq < 2; ++qq) {  // 32 keys at a time
+        const int qd = half * 2 + qq;
         uint32_t us[32], ud[32];
         tmem_ld32(lane_base + buf * 256 + qd * 32, us);
         tmem_ld32(lane_base + buf * 256 + 128 + qd * 32, ud);
         tmem_wait_ld();
         fence_regs32(us);
         fence_regs32(ud);
-        if (qd == 3) {
+        if (qq == 1) {
           tc_fence_before();
           mbar_arrive(&bar_sfree[buf]);
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {  // 4 chunks of 8 keys
-          uint32_t wp[4], wd[4];
+          uint32_t wp[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int c0 = k * 8 + 2 * e;
@@ -545,14 +548,32 @@ __global__ void __launch_bounds__(256, 1)
             const float p0 = in_range(key, lo_i, hi_i) ? e0 : 0.f;
             const float p1 = in_range(key + 1, lo_i, hi_i) ? e1 : 0.f;
             wp[e] = E::pack(p0, p1);
-            wd[e] = E::pack(p0 * (__uint_as_float(ud[c0]) - dl), p1 * (__uint_as_float(ud[c0 + 1]) - dl));
+            dsk[qq * 16 + k * 4 + e] =
+                E::pack(p0 * (__uint_as_float(ud[c0]) - dl), p1 * (__uint_as_float(ud[c0 + 1]) - dl));
           }
-          const uint32_t off = tile_chunk_off(r, qd * 4 + k);
-          *reinterpret_cast<uint4*>(prow + off) = make_uint4(wp[0], wp[1], wp[2], wp[3]);
-          *reinterpret_cast<uint4*>(drow + off) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+          *reinterpret_cast<uint4*>(sTile + tile_chunk_off(r, qd * 4 + k)) = make_uint4(wp[0], wp[1], wp[2], wp[3]);
         }
       }
+      fence_proxy_async_smem();
+      bar_sync_id(1, 256);
+      if (leader) {
+        bulk_store(p.p_tiles + tix * TILE_BYTES, sTile, TILE_BYTES);
+        bulk_commit_group();
+        bulk_wait_group_read0();
+      }
+      bar_sync_id(1, 256);
+#pragma unroll
+      for (int k8 = 0; k8 < 8; ++k8)
+        *reinterpret_cast<uint4*>(sTile + tile_chunk_off(r, half * 8 + k8)) =
+            make_uint4(dsk[4 * k8], dsk[4 * k8 + 1], dsk[4 * k8 + 2], dsk[4 * k8 + 3]);
+      fence_proxy_async_smem();
+      bar_sync_id(1, 256);
+      if (leader) {
+        bulk_store(p.ds_tiles + tix * TILE_BYTES, sTile, TILE_BYTES);
+        bulk_commit_group();
+      }
     }
+    if (leader) bulk_wait_group0();
     if (!ok) {
       *abort_flag = 1;
       record_error(p.err, SDPA_ERR_TIMEOUT);
@@ -815,7 +836,7 @@ static int launch_big_t(const BigBwdLaunch& L, int* launches) {
         if (!set_smem(sf, SF_SMEM)) return SDPA_ERR_CUDA;
         attr_f = true;
       }
-      sf<<<(unsigned)g1, 256, SF_SMEM, L.stream>>>(L.tmQ, L.tmDO, L.tmK, L.tmV, p);
+      sf<<<(unsigned)g1, 384, SF_SMEM, L.stream>>>(L.tmQ, L.tmDO, L.tmK, L.tmV, p);
       n += 1;
     } else {
       s0<<<(unsigned)g1, 256, C::SMEM_BYTES, L.stream>>>(L.tmDO, L.tmV, p);
