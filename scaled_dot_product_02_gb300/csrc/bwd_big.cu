@@ -589,14 +589,18 @@ __global__ void __launch_bounds__(384, 1)
 }
 
 // ====================================================================== phase 2
-constexpr int GB_STAGE = TILE_BYTES + 4 * 16384;  // tile image + 128 rows x 256 columns of B
+// A stage is half a K step: 64 of the 128 contracted rows, i.e. half a tile
+// image (16 KB) and 64 rows x 256 columns of B (32 KB). At 48 KB a stage two
+// CTAs fit on an SM, so one CTA's prologue and epilogue hide under the other's
+// MMAs.
+constexpr int GB_STAGE = TILE_BYTES / 2 + 4 * 8192;
 constexpr int GB_NST = 2;
 constexpr int GB_NBARS = 2 * GB_NST + 3;
 constexpr int GB_SMEM = 1024 + GB_NST * GB_STAGE + GB_NBARS * 8 + 16;
 
 // MODE 0: dQ. MODE 1: dV. MODE 2: dK.
 template <int MODE, bool BF16>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(256, 2)
     gemm_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ BigBwdParams p) {
   using E = Elem<BF16>;
   using T = typename E::T;
@@ -688,19 +692,26 @@ __global__ void __launch_bounds__(256, 1)
     if (elect_one() && n > 0) {
       prefetch_tmap(&tmB);
       int s = 0;
-      for (; s < n; ++s) {
+      for (; s < 2 * n; ++s) {  // half steps
         const int st = s % GB_NST;
+        const int hf = s & 1;
         if (!mbar_wait(&empty[st], ((s / GB_NST) & 1) ^ 1, abort_flag)) break;
         long long at;
         int brow, bh;
-        step(s, at, brow, bh);
+        step(s >> 1, at, brow, bh);
         uint8_t* dst = smem + st * GB_STAGE;
+        const uint8_t* src = atiles + at * TILE_BYTES;
         mbar_arrive_expect_tx(&full[st], GB_STAGE);
-        bulk_load(dst, atiles + at * TILE_BYTES, TILE_BYTES, &full[st]);
+        if (MODE == 0) {  // keys 64*hf.. of the dS image: its atom hf
+          bulk_load(dst, src + hf * 16384, 16384, &full[st]);
+        } else {  // query rows 64*hf.. of the image: the same rows of both atoms
+          bulk_load(dst, src + hf * 8192, 8192, &full[st]);
+          bulk_load(dst + 8192, src + 16384 + hf * 8192, 8192, &full[st]);
+        }
         for (int a = 0; a < 4; ++a)
-          tma_load_3d(&tmB, &full[st], dst + TILE_BYTES + a * 16384, split * 256 + a * 64, bh, brow);
+          tma_load_3d(&tmB, &full[st], dst + TILE_BYTES / 2 + a * 8192, split * 256 + a * 64, bh, brow + hf * 64);
       }
-      if (s < n) {
+      if (s < 2 * n) {
         *abort_flag = 1;
         record_error(p.err, SDPA_ERR_TIMEOUT);
       }
@@ -714,7 +725,7 @@ __global__ void __launch_bounds__(256, 1)
       constexpr uint32_t IDESC = idesc_f16(128, 256, BF16, MODE != 0, true);
       bool ok = true;
       int s = 0;
-      for (; s < n; ++s) {
+      for (; s < 2 * n; ++s) {
         const int st = s % GB_NST;
         if (!mbar_wait(&full[st], (s / GB_NST) & 1, abort_flag)) {
           ok = false;
@@ -722,12 +733,12 @@ __global__ void __launch_bounds__(256, 1)
         }
         tc_fence_after();
         const uint32_t a = smem_u32(smem + st * GB_STAGE);
-        const uint32_t bb = a + TILE_BYTES;
+        const uint32_t bb = a + TILE_BYTES / 2;
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) {
-          const uint64_t ad = MODE == 0 ? smem_desc_sw128(a + (ks >> 2) * 16384 + (ks & 3) * 32, 16, 1024)
-                                        : smem_desc_sw128(a + ks * 2048, 16384, 1024);
-          mma_ss(tmem, ad, smem_desc_sw128(bb + ks * 2048, 16384, 1024), IDESC, (s | ks) != 0);
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t ad = MODE == 0 ? smem_desc_sw128(a + ks * 32, 16, 1024)
+                                        : smem_desc_sw128(a + ks * 2048, 8192, 1024);
+          mma_ss(tmem, ad, smem_desc_sw128(bb + ks * 2048, 8192, 1024), IDESC, (s | ks) != 0);
         }
         mma_commit(&empty[st]);
       }
@@ -804,7 +815,8 @@ __global__ void __launch_bounds__(256, 1)
 // ====================================================================== launch
 template <class K>
 static bool set_smem(K kern, int bytes) {
-  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess;
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess &&
+         cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess;
 }
 
 template <int DQK, bool BF16>
@@ -843,12 +855,12 @@ static int launch_big_t(const BigBwdLaunch& L, int* launches) {
       s1<<<(unsigned)g1, 256, C::SMEM_BYTES, L.stream>>>(L.tmQ, L.tmK, p);
       n += 2;
     }
-    m0<<<(unsigned)gq, 256, GB_SMEM, L.stream>>>(L.tmK, p);
+    m0<<<(unsigned)gq, 256, GB_SMEM, L.stream>>>(L.tmK64, p);
     n += 1;
   }
   if (gkv > 0) {
-    m1<<<(unsigned)gkv, 256, GB_SMEM, L.stream>>>(L.tmDO, p);
-    m2<<<(unsigned)gkv, 256, GB_SMEM, L.stream>>>(L.tmQ, p);
+    m1<<<(unsigned)gkv, 256, GB_SMEM, L.stream>>>(L.tmDO64, p);
+    m2<<<(unsigned)gkv, 256, GB_SMEM, L.stream>>>(L.tmQ64, p);
     n += 2;
   }
   *launches = n;

@@ -67,7 +67,8 @@ struct BigBwdParams {
 };
 
 struct BigBwdLaunch {
-  CUtensorMap tmQ, tmK, tmV, tmDO;  // 128-row boxes
+  CUtensorMap tmQ, tmK, tmV, tmDO;    // 128-row boxes
+  CUtensorMap tmQ64, tmK64, tmDO64;    // 64-row boxes
   BigBwdParams p;
   cudaStream_t stream;
 };
