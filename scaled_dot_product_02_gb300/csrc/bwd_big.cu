@@ -346,21 +346,39 @@ __global__ void __launch_bounds__(256, 1)
 }
 
 // ---------------------------------------------------------------------- head_dim 256
-// Both passes in one kernel: Q and dO stay resident (64 KB each), K and V
-// stream through a ring of 16 KB chunks (128 keys x 64 columns), S and dP of
-// a key tile land side by side in TMEM (double-buffered, 512 columns), and
-// the epilogue forms P and dS in fp32 (each rounded once) and writes the two
-// 16-bit tile images through one 32 KB staging buffer with bulk copies:
-// nothing fp32 goes through HBM and the stores leave in whole 32 KB blocks.
-constexpr int SF_CH = 16384;  // ring chunk: 128 keys x 64 columns
-constexpr int SF_NST = 4;
-constexpr int SF_NBARS = 2 * SF_NST + 8;
-constexpr int SF_SMEM = 1024 + 2 * 65536 + SF_NST * SF_CH + TILE_BYTES + SF_NBARS * 8 + 16;
+// Both passes in one kernel. Q and dO of the query tile live in TMEM as the A
+// operands of S = Q K^T and dP = dO V^T (columns 0-255), so shared memory is
+// left to a deep ring of K/V chunks and the staging of the outputs. S and dP
+// are computed per 64-key half of a key tile (N = 64 MMAs into columns
+// 256-511), and each half has its own epilogue warpgroup: the group forms
+// P and dS in fp32 (each rounded once), stages its 64-key atom of both tile
+// images and writes them with bulk copies, while the MMA moves on to the
+// other half. Nothing fp32 goes through HBM.
+constexpr int SF_CH = 16384;  // ring chunk: 64 keys x 128 columns (two 8 KB boxes)
+constexpr int SF_NST = 10;
+constexpr int SF_STG = 16384;  // one 64-key atom of a tile image
+constexpr int SF_NBARS = 2 * SF_NST + 6;
+constexpr int SF_SMEM = 1024 + SF_NST * SF_CH + 4 * SF_STG + SF_NBARS * 8 + 16;
+constexpr int SF_TM_Q = 0, SF_TM_DO = 128, SF_TM_S = 256;  // S of half h at 256 + 128h, dP at +64
+
+// Barrier over `threads` threads that also ANDs `v` across them, so a
+// warpgroup takes a bail-out decision together.
+__device__ __forceinline__ bool bar_and(int id, int threads, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(threads)
+      : "memory");
+  return r != 0;
+}
 
 template <bool BF16>
 __global__ void __launch_bounds__(384, 1)
-    score_fused256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
-                          const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+    score_fused256_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                           const __grid_constant__ BigBwdParams p) {
   using E = Elem<BF16>;
   const Geom& g = p.g;
@@ -380,20 +398,19 @@ __global__ void __launch_bounds__(384, 1)
     if (threadIdx.x == 0) record_error(p.err, SDPA_ERR_INVALID_ARG);
     return;
   }
+  if (n == 0) return;
   const int qhead = si.qhead0 + h;
   const int khead = si.khead0 + h / (g.hq / g.hkv);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* sQ = smem;
-  uint8_t* sDO = smem + 65536;
-  uint8_t* sStage = smem + 2 * 65536;
-  uint8_t* sTile = sStage + SF_NST * SF_CH;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sTile + TILE_BYTES);
+  uint8_t* sRing = smem;
+  uint8_t* sStg = sRing + SF_NST * SF_CH;  // [half][P, dS] atoms
+  uint64_t* full = reinterpret_cast<uint64_t*>(sStg + 4 * SF_STG);
   uint64_t* empty = full + SF_NST;
-  uint64_t* bar_a = empty + SF_NST;
-  uint64_t* bar_s = bar_a + 1;      // [2] S and dP of a key tile ready
-  uint64_t* bar_sfree = bar_s + 2;  // [2] epilogue has read them
+  uint64_t* bar_qd = empty + SF_NST;  // Q and dO are in TMEM
+  uint64_t* bar_s = bar_qd + 1;       // [2] S and dP of a half ready
+  uint64_t* bar_sfree = bar_s + 2;    // [2] its epilogue group has read them
   uint64_t* bar_drain = bar_sfree + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
@@ -404,11 +421,11 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
-    mbar_init(bar_a, 1);
+    mbar_init(bar_qd, 256);
     mbar_init(&bar_s[0], 1);
     mbar_init(&bar_s[1], 1);
-    mbar_init(&bar_sfree[0], 256);
-    mbar_init(&bar_sfree[1], 256);
+    mbar_init(&bar_sfree[0], 128);
+    mbar_init(&bar_sfree[1], 128);
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -423,28 +440,26 @@ __global__ void __launch_bounds__(384, 1)
   const uint32_t tmem = *tmem_holder;
 
   if (warp == 0) {
-    if (elect_one() && n > 0) {
-      prefetch_tmap(&tmQ);
-      prefetch_tmap(&tmDO);
+    if (elect_one()) {
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
-      mbar_arrive_expect_tx(bar_a, 2 * 65536);
-      for (int a = 0; a < 4; ++a) {
-        tma_load_3d(&tmQ, bar_a, sQ + a * 16384, a * 64, qhead, si.qrow0 + q0);
-        tma_load_3d(&tmDO, bar_a, sDO + a * 16384, a * 64, qhead, si.qrow0 + q0);
-      }
       int c = 0;
       bool ok = true;
       for (int t = 0; t < n && ok; ++t) {
-        const int krow = si.krow0 + (t_lo + t) * 128;
-        for (int kc = 0; kc < 8; ++kc, ++c) {  // K columns 0..255 in four chunks, then V likewise
-          const int slot = c % SF_NST;
-          if (!mbar_wait(&empty[slot], ((c / SF_NST) & 1) ^ 1, abort_flag)) {
-            ok = false;
-            break;
+        for (int hf = 0; hf < 2 && ok; ++hf) {
+          const int krow = si.krow0 + (t_lo + t) * 128 + hf * 64;
+          for (int kc = 0; kc < 4; ++kc, ++c) {  // K columns 0-127, 128-255, then V likewise
+            const int slot = c % SF_NST;
+            if (!mbar_wait(&empty[slot], ((c / SF_NST) & 1) ^ 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            const CUtensorMap* m = kc < 2 ? &tmK : &tmV;
+            uint8_t* dst = sRing + slot * SF_CH;
+            mbar_arrive_expect_tx(&full[slot], SF_CH);
+            tma_load_3d(m, &full[slot], dst, (kc & 1) * 128, khead, krow);
+            tma_load_3d(m, &full[slot], dst + 8192, (kc & 1) * 128 + 64, khead, krow);
           }
-          mbar_arrive_expect_tx(&full[slot], SF_CH);
-          tma_load_3d(kc < 4 ? &tmK : &tmV, &full[slot], sStage + slot * SF_CH, (kc & 3) * 64, khead, krow);
         }
       }
       if (!ok) {
@@ -453,39 +468,39 @@ __global__ void __launch_bounds__(384, 1)
       }
       const int first = c > SF_NST ? c - SF_NST : 0;
       for (int k = first; k < c; ++k) wait_drain_big(&full[k % SF_NST], (k / SF_NST) & 1);
-      wait_drain_big(bar_a, 0);
     }
   } else if (warp == 1) {
-    if (elect_one() && n > 0) {
-      constexpr uint32_t IDESC = idesc_f16(128, 128, BF16, false, false);
-      bool ok = mbar_wait(bar_a, 0, abort_flag);
+    if (elect_one()) {
+      constexpr uint32_t IDESC = idesc_f16(128, 64, BF16, false, false);
+      bool ok = mbar_wait(bar_qd, 0, abort_flag);
       tc_fence_after();
       int c = 0;
       for (int t = 0; t < n && ok; ++t) {
-        const int buf = t & 1;
-        if (t >= 2 && !mbar_wait(&bar_sfree[buf], ((t >> 1) & 1) ^ 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        for (int kc = 0; kc < 8 && ok; ++kc, ++c) {
-          const int slot = c % SF_NST;
-          if (!mbar_wait(&full[slot], (c / SF_NST) & 1, abort_flag)) {
+        for (int hf = 0; hf < 2 && ok; ++hf) {
+          if (t >= 1 && !mbar_wait(&bar_sfree[hf], (t - 1) & 1, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          const uint32_t bb = smem_u32(sStage + slot * SF_CH);
-          // S = Q K^T into columns [256*buf, +128), dP = dO V^T into [+128, +256)
-          const uint32_t aa = smem_u32(kc < 4 ? sQ : sDO) + (kc & 3) * 16384;
-          const uint32_t d = tmem + buf * 256 + (kc < 4 ? 0 : 128);
+          for (int kc = 0; kc < 4; ++kc, ++c) {
+            const int slot = c % SF_NST;
+            if (!mbar_wait(&full[slot], (c / SF_NST) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t bb = smem_u32(sRing + slot * SF_CH);
+            // S (kc 0, 1) = Q K^T, dP (kc 2, 3) = dO V^T; kc & 1 picks the 128-column half of D
+            const uint32_t d = tmem + SF_TM_S + hf * 128 + (kc < 2 ? 0 : 64);
+            const uint32_t aa = tmem + (kc < 2 ? SF_TM_Q : SF_TM_DO) + (kc & 1) * 64;
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks)
-            mma_ss(d, smem_desc_sw128(aa + ks * 32, 16, 1024), smem_desc_sw128(bb + ks * 32, 16, 1024), IDESC,
-                   ((kc & 3) | ks) != 0);
-          mma_commit(&empty[slot]);
+            for (int ks = 0; ks < 8; ++ks)
+              mma_ts(d, aa + ks * 8, smem_desc_sw128(bb + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), IDESC,
+                     ((kc & 1) | ks) != 0);
+            mma_commit(&empty[slot]);
+          }
+          if (ok) mma_commit(&bar_s[hf]);
         }
-        if (ok) mma_commit(&bar_s[buf]);
       }
       if (!ok) {
         *abort_flag = 1;
@@ -495,81 +510,93 @@ __global__ void __launch_bounds__(384, 1)
       }
     }
   } else if (warp >= 4) {
-    // two warpgroups: keys [64*half, 64*half + 64) of every tile, i.e. one
-    // 64-column atom of each tile image
-    const int half = (warp - 4) >> 2;
+    const int hf = (warp - 4) >> 2;  // key half this group forms; for the TMEM load, Q (0) or dO (1)
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
     const int i = q0 + r;
     const bool valid = i < si.lq;
     const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
+    {
+      // row r of Q (group 0) or dO (group 1) into TMEM, packed pairs along D;
+      // rows past the sequence end are zero
+      using T = typename E::T;
+      const T* base = reinterpret_cast<const T*>(hf == 0 ? p.q : p.dout);
+      const uint4* src = reinterpret_cast<const uint4*>(base + ((long long)(si.qrow0 + i) * g.nh_q + qhead) * 256);
+#pragma unroll
+      for (int part = 0; part < 2; ++part) {
+        uint32_t v[64];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+          const uint4 x = valid ? __ldg(src + part * 16 + j) : make_uint4(0u, 0u, 0u, 0u);
+          v[4 * j] = x.x;
+          v[4 * j + 1] = x.y;
+          v[4 * j + 2] = x.z;
+          v[4 * j + 3] = x.w;
+        }
+        const uint32_t col = lane_base + (hf == 0 ? SF_TM_Q : SF_TM_DO) + part * 64;
+        tmem_st32(col, *reinterpret_cast<const uint32_t(*)[32]>(v));
+        tmem_st32(col + 32, *reinterpret_cast<const uint32_t(*)[32]>(v + 32));
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_qd);
+    }
     const long long stat = (long long)qhead * p.stat_rows + si.qrow0 + i;
     // rows past the sequence end belong to no query: their P (and so dS) is zero
     const float nl2 = valid ? p.nlse2[stat] : -INFINITY;
     const float dl = valid ? p.delta[stat] : 0.f;
     const int lo_i = kr.lo(i), hi_i = kr.hi(i);
     const float sl2 = g.scale_log2;
-    const bool leader = threadIdx.x == 128;
+    const bool leader = (threadIdx.x & 127) == 0;
+    uint8_t* stP = sStg + hf * 2 * SF_STG;
+    uint8_t* stD = stP + SF_STG;
     bool ok = true;
     for (int t = 0; t < n; ++t) {
-      const int buf = t & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&bar_s[buf], (t >> 1) & 1, abort_flag))) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar_s[hf], t & 1, abort_flag));
+      if (leader) bulk_wait_group_read0();  // this group's previous atoms have left the staging
+      if (!bar_and(1 + hf, 128, ok)) {
         ok = false;
         break;
       }
       tc_fence_after();
       const long long tix = tile_index(p, b, h, qt, t);
-      const int kbase = (t_lo + t) * 128;
-      if (leader) bulk_wait_group_read0();  // the previous tile's dS image has left the buffer
-      bar_sync_id(1, 256);
-      uint32_t dsk[32];  // packed dS of this half row, staged after the P image
+      const int kbase = (t_lo + t) * 128 + hf * 64;
 #pragma unroll
       for (int qq = 0; qq < 2; ++qq) {  // 32 keys at a time
-        const int qd = half * 2 + qq;
         uint32_t us[32], ud[32];
-        tmem_ld32(lane_base + buf * 256 + qd * 32, us);
-        tmem_ld32(lane_base + buf * 256 + 128 + qd * 32, ud);
+        tmem_ld32(lane_base + SF_TM_S + hf * 128 + qq * 32, us);
+        tmem_ld32(lane_base + SF_TM_S + hf * 128 + 64 + qq * 32, ud);
         tmem_wait_ld();
         fence_regs32(us);
         fence_regs32(ud);
         if (qq == 1) {
           tc_fence_before();
-          mbar_arrive(&bar_sfree[buf]);
+          mbar_arrive(&bar_sfree[hf]);
         }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {  // 4 chunks of 8 keys
-          uint32_t wp[4];
+          uint32_t wp[4], wd[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int c0 = k * 8 + 2 * e;
-            const int key = kbase + qd * 32 + c0;
+            const int key = kbase + qq * 32 + c0;
             const float e0 = ex2(fmaf(__uint_as_float(us[c0]), sl2, nl2));
             const float e1 = ex2(fmaf(__uint_as_float(us[c0 + 1]), sl2, nl2));
             const float p0 = in_range(key, lo_i, hi_i) ? e0 : 0.f;
             const float p1 = in_range(key + 1, lo_i, hi_i) ? e1 : 0.f;
             wp[e] = E::pack(p0, p1);
-            dsk[qq * 16 + k * 4 + e] =
-                E::pack(p0 * (__uint_as_float(ud[c0]) - dl), p1 * (__uint_as_float(ud[c0 + 1]) - dl));
+            wd[e] = E::pack(p0 * (__uint_as_float(ud[c0]) - dl), p1 * (__uint_as_float(ud[c0 + 1]) - dl));
           }
-          *reinterpret_cast<uint4*>(sTile + tile_chunk_off(r, qd * 4 + k)) = make_uint4(wp[0], wp[1], wp[2], wp[3]);
+          const uint32_t off = tile_chunk_off(r, qq * 4 + k);  // within the atom (chunk index < 8)
+          *reinterpret_cast<uint4*>(stP + off) = make_uint4(wp[0], wp[1], wp[2], wp[3]);
+          *reinterpret_cast<uint4*>(stD + off) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
         }
       }
       fence_proxy_async_smem();
-      bar_sync_id(1, 256);
+      bar_sync_id(1 + hf, 128);
       if (leader) {
-        bulk_store(p.p_tiles + tix * TILE_BYTES, sTile, TILE_BYTES);
-        bulk_commit_group();
-        bulk_wait_group_read0();
-      }
-      bar_sync_id(1, 256);
-#pragma unroll
-      for (int k8 = 0; k8 < 8; ++k8)
-        *reinterpret_cast<uint4*>(sTile + tile_chunk_off(r, half * 8 + k8)) =
-            make_uint4(dsk[4 * k8], dsk[4 * k8 + 1], dsk[4 * k8 + 2], dsk[4 * k8 + 3]);
-      fence_proxy_async_smem();
-      bar_sync_id(1, 256);
-      if (leader) {
-        bulk_store(p.ds_tiles + tix * TILE_BYTES, sTile, TILE_BYTES);
+        bulk_store(p.p_tiles + tix * TILE_BYTES + hf * SF_STG, stP, SF_STG);
+        bulk_store(p.ds_tiles + tix * TILE_BYTES + hf * SF_STG, stD, SF_STG);
         bulk_commit_group();
       }
     }
@@ -848,7 +875,7 @@ static int launch_big_t(const BigBwdLaunch& L, int* launches) {
         if (!set_smem(sf, SF_SMEM)) return SDPA_ERR_CUDA;
         attr_f = true;
       }
-      sf<<<(unsigned)g1, 384, SF_SMEM, L.stream>>>(L.tmQ, L.tmDO, L.tmK, L.tmV, p);
+      sf<<<(unsigned)g1, 384, SF_SMEM, L.stream>>>(L.tmK64, L.tmV64, p);
       n += 1;
     } else {
       s0<<<(unsigned)g1, 256, C::SMEM_BYTES, L.stream>>>(L.tmDO, L.tmV, p);
