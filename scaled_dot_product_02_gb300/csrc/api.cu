@@ -369,8 +369,6 @@ int sdpa_bwd(const sdpa_problem* p, const void* q, const void* k, const void* v,
     B.p.nlse2 = lse2;
     B.p.delta = delta;
     B.p.stat_rows = w.stat_rows;
-    B.p.q = q;
-    B.p.dout = dout;
     B.p.dq = dq;
     B.p.dk = dk;
     B.p.dv = dv;
@@ -387,7 +385,6 @@ int sdpa_bwd(const sdpa_problem* p, const void* q, const void* k, const void* v,
     if ((rc = encode(&B.tmQ64, q, p->head_dim, hq, rq, 64, bf16))) return rc;
     if ((rc = encode(&B.tmDO64, dout, p->head_dim, hq, rq, 64, bf16))) return rc;
     if ((rc = encode(&B.tmK64, k, p->head_dim, hk, rk, 64, bf16))) return rc;
-    if ((rc = encode(&B.tmV64, v, p->head_dim, hk, rk, 64, bf16))) return rc;
     int n = 0;
     if ((rc = timed(SDPA_KERNEL_BWD, s, [&] { return launch_bwd_big(B, p->head_dim, bf16, &n); }))) return rc;
     t_last_launches = launches + n;

@@ -348,18 +348,21 @@ __global__ void __launch_bounds__(256, 1)
 // ---------------------------------------------------------------------- head_dim 256
 // Both passes in one kernel. Q and dO of the query tile live in TMEM as the A
 // operands of S = Q K^T and dP = dO V^T (columns 0-255), so shared memory is
-// left to a deep ring of K/V chunks and the staging of the outputs. S and dP
-// are computed per 64-key half of a key tile (N = 64 MMAs into columns
-// 256-511), and each half has its own epilogue warpgroup: the group forms
-// P and dS in fp32 (each rounded once), stages its 64-key atom of both tile
-// images and writes them with bulk copies, while the MMA moves on to the
-// other half. Nothing fp32 goes through HBM.
-constexpr int SF_CH = 16384;  // ring chunk: 64 keys x 128 columns (two 8 KB boxes)
+// left to a deep ring of 16 KB chunks and the staging of the outputs. Q and
+// dO arrive through the first eight ring chunks and are copied to TMEM by the
+// epilogue threads; K and V follow in the same ring. S (columns 256-383) and
+// dP (384-511) are single-buffered but released separately, so S of the next
+// key tile is computed while the epilogue waits for dP of this one. Two
+// epilogue warpgroups each take 64 keys of a tile: they form P and dS in fp32
+// (each rounded once), stage their 64-key atom of both 16-bit tile images and
+// write them with bulk copies. Nothing fp32 goes through HBM.
+constexpr int SF_CH = 16384;  // ring chunk: 128 rows x 64 columns (one box)
 constexpr int SF_NST = 10;
 constexpr int SF_STG = 16384;  // one 64-key atom of a tile image
 constexpr int SF_NBARS = 2 * SF_NST + 6;
 constexpr int SF_SMEM = 1024 + SF_NST * SF_CH + 4 * SF_STG + SF_NBARS * 8 + 16;
-constexpr int SF_TM_Q = 0, SF_TM_DO = 128, SF_TM_S = 256;  // S of half h at 256 + 128h, dP at +64
+constexpr int SF_THREADS = 320;  // producer, MMA, two epilogue warpgroups (warps 2-5, 6-9)
+constexpr int SF_TM_Q = 0, SF_TM_DO = 128, SF_TM_S = 256, SF_TM_DP = 384;
 
 // Barrier over `threads` threads that also ANDs `v` across them, so a
 // warpgroup takes a bail-out decision together.
@@ -377,8 +380,9 @@ __device__ __forceinline__ bool bar_and(int id, int threads, bool v) {
 }
 
 template <bool BF16>
-__global__ void __launch_bounds__(384, 1)
-    score_fused256_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+__global__ void __launch_bounds__(SF_THREADS, 1)
+    score_fused256_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+                          const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                           const __grid_constant__ BigBwdParams p) {
   using E = Elem<BF16>;
   const Geom& g = p.g;
@@ -405,13 +409,15 @@ __global__ void __launch_bounds__(384, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sRing = smem;
-  uint8_t* sStg = sRing + SF_NST * SF_CH;  // [half][P, dS] atoms
+  uint8_t* sStg = sRing + SF_NST * SF_CH;  // [group][P, dS] atoms
   uint64_t* full = reinterpret_cast<uint64_t*>(sStg + 4 * SF_STG);
   uint64_t* empty = full + SF_NST;
   uint64_t* bar_qd = empty + SF_NST;  // Q and dO are in TMEM
-  uint64_t* bar_s = bar_qd + 1;       // [2] S and dP of a half ready
-  uint64_t* bar_sfree = bar_s + 2;    // [2] its epilogue group has read them
-  uint64_t* bar_drain = bar_sfree + 2;
+  uint64_t* bar_s = bar_qd + 1;       // S of a key tile ready
+  uint64_t* bar_dp = bar_s + 1;       // dP of a key tile ready
+  uint64_t* free_s = bar_dp + 1;      // the epilogue has read S
+  uint64_t* free_dp = free_s + 1;     // ... and dP
+  uint64_t* bar_drain = free_dp + 1;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -422,10 +428,10 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&empty[i], 1);
     }
     mbar_init(bar_qd, 256);
-    mbar_init(&bar_s[0], 1);
-    mbar_init(&bar_s[1], 1);
-    mbar_init(&bar_sfree[0], 128);
-    mbar_init(&bar_sfree[1], 128);
+    mbar_init(bar_s, 1);
+    mbar_init(bar_dp, 1);
+    mbar_init(free_s, 256);
+    mbar_init(free_dp, 256);
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -439,30 +445,29 @@ __global__ void __launch_bounds__(384, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
+  // ring chunk c: c < 8 are Q (columns 64c..) and dO (64(c-4)..) of the query
+  // tile; from c = 8 on, per key tile, K columns 0, 64, 128, 192, then V
   if (warp == 0) {
     if (elect_one()) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmDO);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
+      const int total = 8 + 8 * n;
       int c = 0;
-      bool ok = true;
-      for (int t = 0; t < n && ok; ++t) {
-        for (int hf = 0; hf < 2 && ok; ++hf) {
-          const int krow = si.krow0 + (t_lo + t) * 128 + hf * 64;
-          for (int kc = 0; kc < 4; ++kc, ++c) {  // K columns 0-127, 128-255, then V likewise
-            const int slot = c % SF_NST;
-            if (!mbar_wait(&empty[slot], ((c / SF_NST) & 1) ^ 1, abort_flag)) {
-              ok = false;
-              break;
-            }
-            const CUtensorMap* m = kc < 2 ? &tmK : &tmV;
-            uint8_t* dst = sRing + slot * SF_CH;
-            mbar_arrive_expect_tx(&full[slot], SF_CH);
-            tma_load_3d(m, &full[slot], dst, (kc & 1) * 128, khead, krow);
-            tma_load_3d(m, &full[slot], dst + 8192, (kc & 1) * 128 + 64, khead, krow);
-          }
+      for (; c < total; ++c) {
+        const int slot = c % SF_NST;
+        if (!mbar_wait(&empty[slot], ((c / SF_NST) & 1) ^ 1, abort_flag)) break;
+        uint8_t* dst = sRing + slot * SF_CH;
+        mbar_arrive_expect_tx(&full[slot], SF_CH);
+        if (c < 8) {
+          tma_load_3d(c < 4 ? &tmQ : &tmDO, &full[slot], dst, (c & 3) * 64, qhead, si.qrow0 + q0);
+        } else {
+          const int t = (c - 8) >> 3, kc = (c - 8) & 7;
+          tma_load_3d(kc < 4 ? &tmK : &tmV, &full[slot], dst, (kc & 3) * 64, khead, si.krow0 + (t_lo + t) * 128);
         }
       }
-      if (!ok) {
+      if (c < total) {
         *abort_flag = 1;
         record_error(p.err, SDPA_ERR_TIMEOUT);
       }
@@ -471,17 +476,19 @@ __global__ void __launch_bounds__(384, 1)
     }
   } else if (warp == 1) {
     if (elect_one()) {
-      constexpr uint32_t IDESC = idesc_f16(128, 64, BF16, false, false);
+      constexpr uint32_t IDESC = idesc_f16(128, 128, BF16, false, false);
       bool ok = mbar_wait(bar_qd, 0, abort_flag);
       tc_fence_after();
-      int c = 0;
+      int c = 8;
       for (int t = 0; t < n && ok; ++t) {
-        for (int hf = 0; hf < 2 && ok; ++hf) {
-          if (t >= 1 && !mbar_wait(&bar_sfree[hf], (t - 1) & 1, abort_flag)) {
+        for (int pass = 0; pass < 2 && ok; ++pass) {  // S = Q K^T, then dP = dO V^T
+          if (t >= 1 && !mbar_wait(pass == 0 ? free_s : free_dp, (t - 1) & 1, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
+          const uint32_t d = tmem + (pass == 0 ? SF_TM_S : SF_TM_DP);
+          const uint32_t aa = tmem + (pass == 0 ? SF_TM_Q : SF_TM_DO);
           for (int kc = 0; kc < 4; ++kc, ++c) {
             const int slot = c % SF_NST;
             if (!mbar_wait(&full[slot], (c / SF_NST) & 1, abort_flag)) {
@@ -490,16 +497,12 @@ __global__ void __launch_bounds__(384, 1)
             }
             tc_fence_after();
             const uint32_t bb = smem_u32(sRing + slot * SF_CH);
-            // S (kc 0, 1) = Q K^T, dP (kc 2, 3) = dO V^T; kc & 1 picks the 128-column half of D
-            const uint32_t d = tmem + SF_TM_S + hf * 128 + (kc < 2 ? 0 : 64);
-            const uint32_t aa = tmem + (kc < 2 ? SF_TM_Q : SF_TM_DO) + (kc & 1) * 64;
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-              mma_ts(d, aa + ks * 8, smem_desc_sw128(bb + (ks >> 2) * 8192 + (ks & 3) * 32, 16, 1024), IDESC,
-                     ((kc & 1) | ks) != 0);
+            for (int ks = 0; ks < 4; ++ks)
+              mma_ts(d, aa + kc * 32 + ks * 8, smem_desc_sw128(bb + ks * 32, 16, 1024), IDESC, (kc | ks) != 0);
             mma_commit(&empty[slot]);
           }
-          if (ok) mma_commit(&bar_s[hf]);
+          if (ok) mma_commit(pass == 0 ? bar_s : bar_dp);
         }
       }
       if (!ok) {
@@ -509,94 +512,113 @@ __global__ void __launch_bounds__(384, 1)
         wait_drain_big(bar_drain, 0);
       }
     }
-  } else if (warp >= 4) {
-    const int hf = (warp - 4) >> 2;  // key half this group forms; for the TMEM load, Q (0) or dO (1)
-    const int wq = warp & 3;
+  } else if (warp >= 2) {
+    const int grp = (warp - 2) >> 2;  // 64-key half of each tile; for the TMEM fill, Q (0) or dO (1)
+    const int wq = warp & 3;          // TMEM lane quarter this warp may access
     const int r = wq * 32 + lane;
     const int i = q0 + r;
     const bool valid = i < si.lq;
     const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
+    const bool leader = ((threadIdx.x - 64) & 127) == 0;
+    const int bar_id = 1 + grp;
+    bool ok = true;
     {
-      // row r of Q (group 0) or dO (group 1) into TMEM, packed pairs along D;
-      // rows past the sequence end are zero
-      using T = typename E::T;
-      const T* base = reinterpret_cast<const T*>(hf == 0 ? p.q : p.dout);
-      const uint4* src = reinterpret_cast<const uint4*>(base + ((long long)(si.qrow0 + i) * g.nh_q + qhead) * 256);
+      // row r of Q (group 0) or dO (group 1): ring chunks 4*grp.. -> TMEM, packed pairs along D
+      for (int a = 0; a < 4; ++a) {
+        const int slot = grp * 4 + a;
+        ok = __all_sync(0xffffffffu, mbar_wait(&full[slot], 0, abort_flag)) && ok;
+        const uint8_t* row = sRing + slot * SF_CH + r * 128;
+        uint32_t v[32];
 #pragma unroll
-      for (int part = 0; part < 2; ++part) {
-        uint32_t v[64];
-#pragma unroll
-        for (int j = 0; j < 16; ++j) {
-          const uint4 x = valid ? __ldg(src + part * 16 + j) : make_uint4(0u, 0u, 0u, 0u);
+        for (int j = 0; j < 8; ++j) {
+          const uint4 x = *reinterpret_cast<const uint4*>(row + ((j ^ (r & 7)) << 4));
           v[4 * j] = x.x;
           v[4 * j + 1] = x.y;
           v[4 * j + 2] = x.z;
           v[4 * j + 3] = x.w;
         }
-        const uint32_t col = lane_base + (hf == 0 ? SF_TM_Q : SF_TM_DO) + part * 64;
-        tmem_st32(col, *reinterpret_cast<const uint32_t(*)[32]>(v));
-        tmem_st32(col + 32, *reinterpret_cast<const uint32_t(*)[32]>(v + 32));
+        tmem_st32(lane_base + (grp == 0 ? SF_TM_Q : SF_TM_DO) + a * 32, v);
       }
       tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar_qd);
+      ok = bar_and(bar_id, 128, ok);  // every row of this group has been read out of the ring
+      if (ok) {
+        if (leader)
+          for (int a = 0; a < 4; ++a) mbar_arrive(&empty[grp * 4 + a]);
+        tc_fence_before();
+        mbar_arrive(bar_qd);
+      }
     }
     const long long stat = (long long)qhead * p.stat_rows + si.qrow0 + i;
-    // rows past the sequence end belong to no query: their P (and so dS) is zero
-    const float nl2 = valid ? p.nlse2[stat] : -INFINITY;
+    // rows past the sequence end belong to no query: an empty key range, so
+    // their P and dS are exactly zero whatever their scores
+    const float nl2 = valid ? p.nlse2[stat] : 0.f;
     const float dl = valid ? p.delta[stat] : 0.f;
-    const int lo_i = kr.lo(i), hi_i = kr.hi(i);
+    const int lo_i = kr.lo(i), hi_i = valid ? kr.hi(i) : lo_i;
     const float sl2 = g.scale_log2;
-    const bool leader = (threadIdx.x & 127) == 0;
-    uint8_t* stP = sStg + hf * 2 * SF_STG;
+    uint8_t* stP = sStg + grp * 2 * SF_STG;
     uint8_t* stD = stP + SF_STG;
-    bool ok = true;
-    for (int t = 0; t < n; ++t) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar_s[hf], t & 1, abort_flag));
+    for (int t = 0; t < n && ok; ++t) {
+      bool okw = __all_sync(0xffffffffu, mbar_wait(bar_s, t & 1, abort_flag));
       if (leader) bulk_wait_group_read0();  // this group's previous atoms have left the staging
-      if (!bar_and(1 + hf, 128, ok)) {
+      if (!bar_and(bar_id, 128, okw)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const long long tix = tile_index(p, b, h, qt, t);
-      const int kbase = (t_lo + t) * 128 + hf * 64;
-#pragma unroll
-      for (int qq = 0; qq < 2; ++qq) {  // 32 keys at a time
-        uint32_t us[32], ud[32];
-        tmem_ld32(lane_base + SF_TM_S + hf * 128 + qq * 32, us);
-        tmem_ld32(lane_base + SF_TM_S + hf * 128 + 64 + qq * 32, ud);
+      const int kbase = (t_lo + t) * 128 + grp * 64;
+      float pv[64];
+      {
+        uint32_t u[64];
+        tmem_ld32(lane_base + SF_TM_S + grp * 64, *reinterpret_cast<uint32_t(*)[32]>(u));
+        tmem_ld32(lane_base + SF_TM_S + grp * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(u + 32));
         tmem_wait_ld();
-        fence_regs32(us);
-        fence_regs32(ud);
-        if (qq == 1) {
-          tc_fence_before();
-          mbar_arrive(&bar_sfree[hf]);
-        }
+        fence_regs32(*reinterpret_cast<uint32_t(*)[32]>(u));
+        fence_regs32(*reinterpret_cast<uint32_t(*)[32]>(u + 32));
+        tc_fence_before();
+        mbar_arrive(free_s);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {  // 4 chunks of 8 keys
-          uint32_t wp[4], wd[4];
+        for (int c0 = 0; c0 < 64; ++c0) {
+          const float e = ex2(fmaf(__uint_as_float(u[c0]), sl2, nl2));
+          pv[c0] = in_range(kbase + c0, lo_i, hi_i) ? e : 0.f;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        *reinterpret_cast<uint4*>(stP + tile_chunk_off(r, k)) =
+            make_uint4(E::pack(pv[8 * k], pv[8 * k + 1]), E::pack(pv[8 * k + 2], pv[8 * k + 3]),
+                       E::pack(pv[8 * k + 4], pv[8 * k + 5]), E::pack(pv[8 * k + 6], pv[8 * k + 7]));
+      okw = __all_sync(0xffffffffu, mbar_wait(bar_dp, t & 1, abort_flag));
+      tc_fence_after();
+      {
+        uint32_t u[64];
+        tmem_ld32(lane_base + SF_TM_DP + grp * 64, *reinterpret_cast<uint32_t(*)[32]>(u));
+        tmem_ld32(lane_base + SF_TM_DP + grp * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(u + 32));
+        tmem_wait_ld();
+        fence_regs32(*reinterpret_cast<uint32_t(*)[32]>(u));
+        fence_regs32(*reinterpret_cast<uint32_t(*)[32]>(u + 32));
+        tc_fence_before();
+        mbar_arrive(free_dp);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          uint32_t w[4];
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int c0 = k * 8 + 2 * e;
-            const int key = kbase + qq * 32 + c0;
-            const float e0 = ex2(fmaf(__uint_as_float(us[c0]), sl2, nl2));
-            const float e1 = ex2(fmaf(__uint_as_float(us[c0 + 1]), sl2, nl2));
-            const float p0 = in_range(key, lo_i, hi_i) ? e0 : 0.f;
-            const float p1 = in_range(key + 1, lo_i, hi_i) ? e1 : 0.f;
-            wp[e] = E::pack(p0, p1);
-            wd[e] = E::pack(p0 * (__uint_as_float(ud[c0]) - dl), p1 * (__uint_as_float(ud[c0 + 1]) - dl));
+            const int c0 = 8 * k + 2 * e;
+            // pv is exactly zero outside the mask, so dS is too (for finite dP)
+            w[e] = E::pack(pv[c0] * (__uint_as_float(u[c0]) - dl), pv[c0 + 1] * (__uint_as_float(u[c0 + 1]) - dl));
           }
-          const uint32_t off = tile_chunk_off(r, qq * 4 + k);  // within the atom (chunk index < 8)
-          *reinterpret_cast<uint4*>(stP + off) = make_uint4(wp[0], wp[1], wp[2], wp[3]);
-          *reinterpret_cast<uint4*>(stD + off) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+          *reinterpret_cast<uint4*>(stD + tile_chunk_off(r, k)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
       fence_proxy_async_smem();
-      bar_sync_id(1 + hf, 128);
+      if (!bar_and(bar_id, 128, okw)) {
+        ok = false;
+        break;
+      }
       if (leader) {
-        bulk_store(p.p_tiles + tix * TILE_BYTES + hf * SF_STG, stP, SF_STG);
-        bulk_store(p.ds_tiles + tix * TILE_BYTES + hf * SF_STG, stD, SF_STG);
+        const long long tix = tile_index(p, b, h, qt, t);
+        bulk_store(p.p_tiles + tix * TILE_BYTES + grp * SF_STG, stP, SF_STG);
+        bulk_store(p.ds_tiles + tix * TILE_BYTES + grp * SF_STG, stD, SF_STG);
         bulk_commit_group();
       }
     }
@@ -875,7 +897,7 @@ static int launch_big_t(const BigBwdLaunch& L, int* launches) {
         if (!set_smem(sf, SF_SMEM)) return SDPA_ERR_CUDA;
         attr_f = true;
       }
-      sf<<<(unsigned)g1, 384, SF_SMEM, L.stream>>>(L.tmK64, L.tmV64, p);
+      sf<<<(unsigned)g1, SF_THREADS, SF_SMEM, L.stream>>>(L.tmQ, L.tmDO, L.tmK, L.tmV, p);
       n += 1;
     } else {
       s0<<<(unsigned)g1, 256, C::SMEM_BYTES, L.stream>>>(L.tmDO, L.tmV, p);

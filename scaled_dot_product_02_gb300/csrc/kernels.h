@@ -58,8 +58,6 @@ struct BigBwdParams {
   const float* nlse2;    // [nh_q][stat_rows] -LSE * log2(e)
   const float* delta;    // [nh_q][stat_rows]
   int stat_rows;
-  const void* q;         // inputs, read directly by the head_dim 256 score kernel
-  const void* dout;
   void* dq;
   void* dk;
   void* dv;
@@ -70,7 +68,7 @@ struct BigBwdParams {
 
 struct BigBwdLaunch {
   CUtensorMap tmQ, tmK, tmV, tmDO;    // 128-row boxes
-  CUtensorMap tmQ64, tmK64, tmV64, tmDO64;  // 64-row boxes
+  CUtensorMap tmQ64, tmK64, tmDO64;    // 64-row boxes
   BigBwdParams p;
   cudaStream_t stream;
 };
