@@ -54,9 +54,6 @@ __device__ __forceinline__ void fence_regs32(uint32_t (&r)[32]) {
                : "memory");
 }
 
-__device__ __forceinline__ void bar_sync_id(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
 
 // Bulk store shared -> global (16-byte aligned, size multiple of 16).
 __device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
@@ -309,25 +306,25 @@ __global__ void __launch_bounds__(256, 1)
       if (MODE == 1) {
         // P image out, then the dS image through the same buffer
         fence_proxy_async_smem();
-        bar_sync_id(1, 128);
+        named_bar_sync(1, 128);
         if (leader) {
           bulk_store(p.p_tiles + tix * TILE_BYTES, sTile, TILE_BYTES);
           bulk_commit_group();
           bulk_wait_group_read0();
         }
-        bar_sync_id(1, 128);
+        named_bar_sync(1, 128);
 #pragma unroll
         for (int k16 = 0; k16 < 16; ++k16)
           *reinterpret_cast<uint4*>(sTile + tile_chunk_off(r, k16)) =
               make_uint4(dsk[4 * k16], dsk[4 * k16 + 1], dsk[4 * k16 + 2], dsk[4 * k16 + 3]);
         fence_proxy_async_smem();
-        bar_sync_id(1, 128);
+        named_bar_sync(1, 128);
         if (leader) {
           bulk_store(p.ds_tiles + tix * TILE_BYTES, sTile, TILE_BYTES);
           bulk_commit_group();
           bulk_wait_group_read0();
         }
-        bar_sync_id(1, 128);  // the buffer is free again for the next tile
+        named_bar_sync(1, 128);  // the buffer is free again for the next tile
       }
     }
     if (leader) bulk_wait_group0();
@@ -363,21 +360,6 @@ constexpr int SF_NBARS = 2 * SF_NST + 6;
 constexpr int SF_SMEM = 1024 + SF_NST * SF_CH + 4 * SF_STG + SF_NBARS * 8 + 16;
 constexpr int SF_THREADS = 320;  // producer, MMA, two epilogue warpgroups (warps 2-5, 6-9)
 constexpr int SF_TM_Q = 0, SF_TM_DO = 128, SF_TM_S = 256, SF_TM_DP = 384;
-
-// Barrier over `threads` threads that also ANDs `v` across them, so a
-// warpgroup takes a bail-out decision together.
-__device__ __forceinline__ bool bar_and(int id, int threads, bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\t"
-      "setp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.and.pred q, %2, %3, p;\n\t"
-      "selp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"((uint32_t)v), "r"(id), "r"(threads)
-      : "memory");
-  return r != 0;
-}
 
 template <bool BF16>
 __global__ void __launch_bounds__(SF_THREADS, 1)
@@ -540,7 +522,7 @@ __global__ void __launch_bounds__(SF_THREADS, 1)
         tmem_st32(lane_base + (grp == 0 ? SF_TM_Q : SF_TM_DO) + a * 32, v);
       }
       tmem_wait_st();
-      ok = bar_and(bar_id, 128, ok);  // every row of this group has been read out of the ring
+      ok = named_bar_and(bar_id, 128, ok);  // every row of this group has been read out of the ring
       if (ok) {
         if (leader)
           for (int a = 0; a < 4; ++a) mbar_arrive(&empty[grp * 4 + a]);
@@ -560,7 +542,7 @@ __global__ void __launch_bounds__(SF_THREADS, 1)
     for (int t = 0; t < n && ok; ++t) {
       bool okw = __all_sync(0xffffffffu, mbar_wait(bar_s, t & 1, abort_flag));
       if (leader) bulk_wait_group_read0();  // this group's previous atoms have left the staging
-      if (!bar_and(bar_id, 128, okw)) {
+      if (!named_bar_and(bar_id, 128, okw)) {
         ok = false;
         break;
       }
@@ -611,7 +593,7 @@ __global__ void __launch_bounds__(SF_THREADS, 1)
         }
       }
       fence_proxy_async_smem();
-      if (!bar_and(bar_id, 128, okw)) {
+      if (!named_bar_and(bar_id, 128, okw)) {
         ok = false;
         break;
       }
