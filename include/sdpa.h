@@ -102,7 +102,9 @@ typedef struct {
 
 /* Bytes of device workspace sdpa_fwd / sdpa_bwd need for this problem
  * (0 when none). Returns 0 as well for a problem the library declines; call
- * sdpa_check_problem to tell the two apart. */
+ * sdpa_check_problem to tell the two apart. The forward needs 256 bytes for
+ * THD (the metadata guard word) and for head_dim 128 (the tile counter of
+ * its persistent kernel, zeroed on the stream by every call), else none. */
 SDPA_API size_t sdpa_fwd_workspace_size(const sdpa_problem* p);
 SDPA_API size_t sdpa_bwd_workspace_size(const sdpa_problem* p);
 

@@ -238,7 +238,9 @@ int sdpa_check_problem(const sdpa_problem* p) { return check(p); }
 
 size_t sdpa_fwd_workspace_size(const sdpa_problem* p) {
   if (check(p) != SDPA_OK) return 0;
-  return p->layout == SDPA_THD ? 256 : 0;
+  // THD: the metadata guard word at offset 0; head_dim 128: the tile ticket
+  // counter of the persistent kernel at offset 128
+  return (p->layout == SDPA_THD || p->head_dim == 128) ? 256 : 0;
 }
 
 size_t sdpa_bwd_workspace_size(const sdpa_problem* p) {
@@ -284,6 +286,7 @@ int sdpa_fwd(const sdpa_problem* p, const void* q, const void* k, const void* v,
   L.p.guard = thd ? static_cast<const int*>(workspace) : nullptr;
   L.p.n_q_tiles = (p->seqlen_q + 127) / 128;
   L.p.dv_splits = p->head_dim == 512 ? 2 : 1;
+  L.p.tile_counter = p->head_dim == 128 ? reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + 128) : nullptr;
   L.stream = s;
   const int dv = p->head_dim == 128 ? 128 : 256;
   if ((rc = encode(&L.tmQ, q, p->head_dim, hq, rq, 128, bf16))) return rc;

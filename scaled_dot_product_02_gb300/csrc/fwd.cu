@@ -21,6 +21,7 @@
 //               Epilogue: O / l to global memory, LSE = m*scale + ln l.
 // The TMEM plan: O at columns [0, DV), S/P buffers at DV and DV+128; with
 // DV <= 256 this fits the 512 columns of one SM.
+#include <algorithm>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -395,15 +396,30 @@ __global__ void __launch_bounds__(256, 1)
 }
 
 // ---------------------------------------------------------------------------
-// head_dim 128 variant sized for two resident CTAs per SM (192 threads, at
-// most 168 registers, 96 KB of shared memory, 256 TMEM columns: O at
-// [0,128), S/P at [128,256)). With a single S buffer each CTA runs
-// S_j -> softmax_j -> PV_j strictly in turn; the tensor pipe stays busy with
-// the other CTA's MMAs while one CTA is in its softmax, and one CTA's
-// prologue and epilogue overlap the other's main loop.
-// Roles: warps 0-3 softmax + epilogue (one thread per query row), warp 4 TMA
-// producer, warp 5 TMEM allocator + MMA issuer. The softmax makes one pass
-// over S in TMEM per key tile (a second one only when a row's max moves).
+// head_dim 128: a persistent kernel, one CTA per SM running two independent
+// query-tile pipelines (384 threads launched at 168 registers, ~195 KB of
+// shared memory, all 512 TMEM columns: pipeline X has O at [256X, 256X+128)
+// and S/P at [256X+128, 256X+256)). The two softmax warpgroups take 192
+// registers a thread and the producer/MMA warpgroup keeps 120
+// (2 x 192 + 120 = 3 x 168: both the block's registers and each SM
+// sub-partition's, which hosts one warp of every warpgroup). Each pipeline takes query tiles,
+// heaviest first, from an atomic ticket counter; TMEM allocation and barrier
+// set-up are paid once per CTA, a tile's Q is loaded as soon as the previous
+// tile's last S has been issued, and the next tile's first S runs while the
+// softmax warps write the current tile's output.
+// Within a pipeline a tile runs S_j -> softmax_j -> PV_j in turn (one S
+// buffer). The single MMA issuer serves the two pipelines strictly in turn
+// (PV_A, S_A, PV_B, S_B, ...), which keeps them half a period apart: one
+// pipeline's softmax runs while the tensor pipe works on the other's MMAs.
+// (Two separate CTAs per SM, with nothing to order them, drift into step and
+// then contend for the same units.)
+// Roles: warps 0-3 / 4-7 softmax + epilogue of pipeline 0 / 1 (one thread
+// per query row), warps 8 / 9 TMA producer and scheduler of pipeline 0 / 1,
+// warp 10 TMEM allocator + MMA issuer, warp 11 only completes the third
+// warpgroup. A producer publishes each tile through
+// a two-entry queue in shared memory; every barrier phase counts across
+// tiles. The softmax makes one pass over S in TMEM per key tile (a second one
+// only when a row's max moves).
 // One pass of the head_dim 128 softmax over the 128 scores of a row held in
 // TMEM: t = S*scale*log2e - mb, P = exp2(t) packed to 16-bit pairs (zero
 // where masked), the row sum of P and the largest t among allowed keys.
@@ -439,67 +455,117 @@ struct Fwd2Cfg {
   static constexpr int Q_BYTES = 32768;
   static constexpr int STAGE_BYTES = 32768;
   static constexpr int NSTAGES = 2;
-  static constexpr int NBARS = 2 * NSTAGES + 5;
-  static constexpr int SMEM_BYTES = 1024 + Q_BYTES + NSTAGES * STAGE_BYTES + NBARS * 8 + 16;
-  static constexpr uint32_t TMEM_O = 0, TMEM_S = 128;
+  static constexpr int PIPE_BYTES = Q_BYTES + NSTAGES * STAGE_BYTES;  // per pipeline, 1024-aligned
+  static constexpr int PIPE_BARS = 16;                                // mbarriers + queue per pipeline (8 bytes each)
+  static constexpr int SMEM_BYTES = 1024 + 2 * PIPE_BYTES + 2 * PIPE_BARS * 8 + 32;
+  static constexpr uint32_t TMEM_O = 0, TMEM_S = 128, TMEM_PIPE = 256;
+  static constexpr int THREADS = 384;
+  static constexpr int REGS_SOFTMAX = 192, REGS_OTHER = 120;
+  static_assert(2 * REGS_SOFTMAX + REGS_OTHER <= 3 * 168, "register split");
 };
 
+// Shared-memory objects of one pipeline.
+struct Pipe128 {
+  uint8_t* sQ;
+  uint8_t* sStage;
+  uint64_t* full;         // [NSTAGES]
+  uint64_t* empty;        // [NSTAGES]
+  uint64_t* bar_q;        // Q of a tile landed
+  uint64_t* bar_s;        // S_j ready
+  uint64_t* bar_p;        // P_j written (and O rescaled)
+  uint64_t* bar_o;        // last PV of a tile done
+  uint64_t* q_free;       // every S of a tile done: Q may be replaced
+  uint64_t* o_free;       // the epilogue has read O
+  uint64_t* sched_full;   // [2] a tile published
+  uint64_t* sched_empty;  // [2] its entry read by the MMA issuer and the softmax warps
+  int* sched;             // [2] ticket, or -1 when the work is out
+};
+
+__device__ __forceinline__ Pipe128 pipe_at(uint8_t* smem, int x) {
+  using C = Fwd2Cfg;
+  Pipe128 P;
+  P.sQ = smem + x * C::PIPE_BYTES;
+  P.sStage = P.sQ + C::Q_BYTES;
+  uint64_t* b = reinterpret_cast<uint64_t*>(smem + 2 * C::PIPE_BYTES) + x * C::PIPE_BARS;
+  P.full = b;
+  P.empty = b + C::NSTAGES;
+  P.bar_q = b + 2 * C::NSTAGES;
+  P.bar_s = P.bar_q + 1;
+  P.bar_p = P.bar_q + 2;
+  P.bar_o = P.bar_q + 3;
+  P.q_free = P.bar_q + 4;
+  P.o_free = P.bar_q + 5;
+  P.sched_full = P.bar_q + 6;
+  P.sched_empty = P.bar_q + 8;
+  P.sched = reinterpret_cast<int*>(P.bar_q + 10);
+  return P;
+}
+
+// A query tile of the ticket order (heaviest first: the last query tiles of
+// every sequence come first) and the keys it sees.
+struct Tile128 {
+  int h, b, q0, q_last, t_lo, n;
+  SeqInfo si;
+  KeyRange kr;
+};
+
+__device__ __forceinline__ bool decode_tile(const FwdParams& p, int idx, Tile128& t) {
+  const Geom& g = p.g;
+  t.h = idx % g.hq;
+  idx /= g.hq;
+  t.b = idx % g.batch;
+  idx /= g.batch;
+  t.q0 = (p.n_q_tiles - 1 - idx) * 128;
+  t.si = seq_info(g, t.b);
+  if (t.q0 >= t.si.lq) return false;
+  t.kr = key_range(g, t.si.lq, t.si.lk);
+  t.q_last = min(t.q0 + 127, t.si.lq - 1);
+  const int lo = t.kr.lo(t.q0), hi = t.kr.hi(t.q_last);
+  t.t_lo = lo / 128;
+  t.n = hi > lo ? (hi + 127) / 128 - t.t_lo : 0;
+  return true;
+}
+
 template <bool BF16>
-__global__ void __launch_bounds__(192, 2)
+__global__ void __launch_bounds__(Fwd2Cfg::THREADS, 1)
     fwd128_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                   const __grid_constant__ CUtensorMap tmV, const __grid_constant__ FwdParams p) {
   using C = Fwd2Cfg;
   using E = Elem<BF16>;
   const Geom& g = p.g;
-  int idx = blockIdx.x;
-  const int h = idx % g.hq;
-  idx /= g.hq;
-  const int b = idx % g.batch;
-  idx /= g.batch;
-  const int qt = p.n_q_tiles - 1 - idx;
-  const SeqInfo si = seq_info(g, b);
-  const int q0 = qt * 128;
-  if (q0 >= si.lq) return;
   if (p.guard && *reinterpret_cast<volatile const int*>(p.guard)) return;
-
-  const KeyRange kr = key_range(g, si.lq, si.lk);
-  const int q_last = min(q0 + 127, si.lq - 1);
-  const int kv_lo = kr.lo(q0), kv_hi = kr.hi(q_last);
-  const int t_lo = kv_lo / 128;
-  const int n_tiles = (kv_hi > kv_lo) ? (kv_hi + 127) / 128 - t_lo : 0;
-  const int qhead = si.qhead0 + h;
-  const int khead = si.khead0 + h / (g.hq / g.hkv);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* sQ = smem;
-  uint8_t* sStage = smem + C::Q_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sStage + C::NSTAGES * C::STAGE_BYTES);
-  uint64_t* empty = full + C::NSTAGES;
-  uint64_t* bar_q = empty + C::NSTAGES;
-  uint64_t* bar_s = bar_q + 1;
-  uint64_t* bar_p = bar_s + 1;
-  uint64_t* bar_o = bar_p + 1;
-  uint64_t* bar_drain = bar_o + 1;
+  uint64_t* bar_drain = reinterpret_cast<uint64_t*>(smem + 2 * C::PIPE_BYTES) + 2 * C::PIPE_BARS;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < C::NSTAGES; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+    for (int x = 0; x < 2; ++x) {
+      const Pipe128 P = pipe_at(smem, x);
+      for (int i = 0; i < C::NSTAGES; ++i) {
+        mbar_init(&P.full[i], 1);
+        mbar_init(&P.empty[i], 1);
+      }
+      mbar_init(P.bar_q, 1);
+      mbar_init(P.bar_s, 1);
+      mbar_init(P.bar_p, 128);
+      mbar_init(P.bar_o, 1);
+      mbar_init(P.q_free, 1);
+      mbar_init(P.o_free, 128);
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&P.sched_full[i], 1);
+        mbar_init(&P.sched_empty[i], 129);
+      }
     }
-    mbar_init(bar_q, 1);
-    mbar_init(bar_s, 1);
-    mbar_init(bar_p, 128);
-    mbar_init(bar_o, 1);
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
-    tmem_alloc(tmem_holder, 256);
+  if (warp == 10) {
+    tmem_alloc(tmem_holder, 512);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -507,86 +573,170 @@ __global__ void __launch_bounds__(192, 2)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ producer: Q, then K_0, V_0, K_1, V_1, ...
-    if (elect_one() && n_tiles > 0) {
+  if (warp >= 8) {
+    regs_dec<C::REGS_OTHER>();
+    if (warp == 8 || warp == 9) {
+    // ------------------------------------------------------------ scheduler + producer of pipeline warp - 8
+    if (elect_one()) {
+      const Pipe128 P = pipe_at(smem, warp - 8);
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
-      mbar_arrive_expect_tx(bar_q, C::Q_BYTES);
-      tma_load_3d(&tmQ, bar_q, sQ, 0, qhead, si.qrow0 + q0);
-      tma_load_3d(&tmQ, bar_q, sQ + 16384, 64, qhead, si.qrow0 + q0);
-      int c = 0;
+      int c = 0, nq = 0, w = 0;
       bool ok = true;
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        const int key0 = si.krow0 + (t_lo + j) * 128;
-        for (int kv = 0; kv < 2; ++kv, ++c) {
-          const int slot = c % C::NSTAGES;
-          if (!mbar_wait(&empty[slot], ((c / C::NSTAGES) & 1) ^ 1, abort_flag)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&full[slot], C::STAGE_BYTES);
-          const CUtensorMap* m = kv ? &tmV : &tmK;
-          uint8_t* dst = sStage + slot * C::STAGE_BYTES;
-          tma_load_3d(m, &full[slot], dst, 0, khead, key0);
-          tma_load_3d(m, &full[slot], dst + 16384, 64, khead, key0);
+      int ticket = atomicAdd(p.tile_counter, 1);
+      while (true) {
+        Tile128 t;
+        while (ticket < p.total_tiles && !decode_tile(p, ticket, t)) ticket = atomicAdd(p.tile_counter, 1);
+        const int item = ticket < p.total_tiles ? ticket : -1;
+        const int e = w & 1;
+        if (!mbar_wait(&P.sched_empty[e], ((w >> 1) & 1) ^ 1, abort_flag)) {
+          ok = false;
+          break;
         }
+        P.sched[e] = item;
+        mbar_arrive(&P.sched_full[e]);
+        ++w;
+        if (item < 0) break;
+        ticket = atomicAdd(p.tile_counter, 1);  // in flight while this tile's loads are issued
+        if (t.n == 0) continue;
+        if (nq > 0 && !mbar_wait(P.q_free, (nq - 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        const int qhead = t.si.qhead0 + t.h;
+        const int khead = t.si.khead0 + t.h / (g.hq / g.hkv);
+        mbar_arrive_expect_tx(P.bar_q, C::Q_BYTES);
+        tma_load_3d(&tmQ, P.bar_q, P.sQ, 0, qhead, t.si.qrow0 + t.q0);
+        tma_load_3d(&tmQ, P.bar_q, P.sQ + 16384, 64, qhead, t.si.qrow0 + t.q0);
+        ++nq;
+        for (int j = 0; j < t.n && ok; ++j) {
+          const int key0 = t.si.krow0 + (t.t_lo + j) * 128;
+          for (int kv = 0; kv < 2; ++kv, ++c) {
+            const int slot = c % C::NSTAGES;
+            if (!mbar_wait(&P.empty[slot], ((c / C::NSTAGES) & 1) ^ 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&P.full[slot], C::STAGE_BYTES);
+            const CUtensorMap* m = kv ? &tmV : &tmK;
+            uint8_t* dst = P.sStage + slot * C::STAGE_BYTES;
+            tma_load_3d(m, &P.full[slot], dst, 0, khead, key0);
+            tma_load_3d(m, &P.full[slot], dst + 16384, 64, khead, key0);
+          }
+        }
+        if (!ok) break;
       }
       if (!ok) {
         *abort_flag = 1;
         record_error(p.err, SDPA_ERR_TIMEOUT);
       }
       const int first = c > C::NSTAGES ? c - C::NSTAGES : 0;
-      for (int k = first; k < c; ++k) mbar_wait_drain(&full[k % C::NSTAGES], (k / C::NSTAGES) & 1);
-      mbar_wait_drain(bar_q, 0);
+      for (int k = first; k < c; ++k) mbar_wait_drain(&P.full[k % C::NSTAGES], (k / C::NSTAGES) & 1);
+      if (nq > 0) mbar_wait_drain(P.bar_q, (nq - 1) & 1);
     }
-  } else if (warp == 5) {
-    // ------------------------------------------------------------ MMA issuer
-    if (elect_one() && n_tiles > 0) {
+    } else if (warp == 10) {
+    // ------------------------------------------------------------ MMA issuer for both pipelines
+    if (elect_one()) {
       constexpr uint32_t IDESC_S = idesc_f16(128, 128, BF16, false, false);
       constexpr uint32_t IDESC_O = idesc_f16(128, 128, BF16, false, true);
-      bool ok = mbar_wait(bar_q, 0, abort_flag);
-      tc_fence_after();
-      const uint32_t q_base = smem_u32(sQ);
-      int c = 0;
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        // S_j = Q K_j^T (the previous PV has been issued, so P_{j-1} is consumed first)
-        int slot = c % C::NSTAGES;
-        if (!mbar_wait(&full[slot], (c / C::NSTAGES) & 1, abort_flag)) {
-          ok = false;
-          break;
+      struct State {
+        int w, c, nq, tiles, no, n, j;
+        bool done;
+      };
+      State st[2];
+      for (int x = 0; x < 2; ++x) st[x] = State{0, 0, 0, 0, 0, 0, 0, false};
+      bool ok = true;
+      // next tile with keys of pipeline x (false: its work is out, or a wait failed)
+      auto next_item = [&](int x) -> bool {
+        const Pipe128 P = pipe_at(smem, x);
+        State& m = st[x];
+        while (true) {
+          const int e = m.w & 1;
+          if (!mbar_wait(&P.sched_full[e], (m.w >> 1) & 1, abort_flag)) {
+            ok = false;
+            return false;
+          }
+          const int item = *reinterpret_cast<volatile int*>(&P.sched[e]);
+          mbar_arrive(&P.sched_empty[e]);
+          ++m.w;
+          if (item < 0) {
+            m.done = true;
+            return false;
+          }
+          Tile128 t;
+          decode_tile(p, item, t);
+          if (t.n == 0) continue;
+          if (!mbar_wait(P.bar_q, m.nq & 1, abort_flag)) {
+            ok = false;
+            return false;
+          }
+          ++m.nq;
+          tc_fence_after();
+          m.n = t.n;
+          m.j = 0;
+          return true;
         }
+      };
+      // S_j = Q K_j^T of pipeline x (its previous PV has been issued, so P_{j-1} is consumed first)
+      auto issue_s = [&](int x) -> bool {
+        const Pipe128 P = pipe_at(smem, x);
+        State& m = st[x];
+        const int slot = m.c % C::NSTAGES;
+        if (!mbar_wait(&P.full[slot], (m.c / C::NSTAGES) & 1, abort_flag)) return false;
         tc_fence_after();
-        uint32_t base = smem_u32(sStage + slot * C::STAGE_BYTES);
+        const uint32_t q_base = smem_u32(P.sQ), base = smem_u32(P.sStage + slot * C::STAGE_BYTES);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks) {
           const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-          mma_ss(tmem + C::TMEM_S, smem_desc_sw128(q_base + off, 16, 1024), smem_desc_sw128(base + off, 16, 1024),
-                 IDESC_S, ks != 0);
+          mma_ss(tmem + x * C::TMEM_PIPE + C::TMEM_S, smem_desc_sw128(q_base + off, 16, 1024),
+                 smem_desc_sw128(base + off, 16, 1024), IDESC_S, ks != 0);
         }
-        mma_commit(&empty[slot]);
-        mma_commit(bar_s);
-        ++c;
-        // O += P_j V_j
-        if (!mbar_wait(bar_p, j & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        slot = c % C::NSTAGES;
-        if (!mbar_wait(&full[slot], (c / C::NSTAGES) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
+        mma_commit(&P.empty[slot]);
+        if (m.j == m.n - 1) mma_commit(P.q_free);
+        mma_commit(P.bar_s);
+        ++m.c;
+        return true;
+      };
+      // O += P_j V_j of pipeline x; the first PV of a tile overwrites O, which
+      // the previous tile's epilogue must have read
+      auto issue_pv = [&](int x) -> bool {
+        const Pipe128 P = pipe_at(smem, x);
+        State& m = st[x];
+        if (m.j == 0 && m.no > 0 && !mbar_wait(P.o_free, (m.no - 1) & 1, abort_flag)) return false;
+        if (!mbar_wait(P.bar_p, m.tiles & 1, abort_flag)) return false;
+        ++m.tiles;
+        const int slot = m.c % C::NSTAGES;
+        if (!mbar_wait(&P.full[slot], (m.c / C::NSTAGES) & 1, abort_flag)) return false;
         tc_fence_after();
-        base = smem_u32(sStage + slot * C::STAGE_BYTES);
+        const uint32_t base = smem_u32(P.sStage + slot * C::STAGE_BYTES);
 #pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-          mma_ts(tmem + C::TMEM_O, tmem + C::TMEM_S + ks * 8, smem_desc_sw128(base + ks * 2048, 16384, 1024),
-                 IDESC_O, (j | ks) != 0);
-        mma_commit(&empty[slot]);
-        mma_commit(bar_o);
-        ++c;
+          mma_ts(tmem + x * C::TMEM_PIPE + C::TMEM_O, tmem + x * C::TMEM_PIPE + C::TMEM_S + ks * 8,
+                 smem_desc_sw128(base + ks * 2048, 16384, 1024), IDESC_O, (m.j | ks) != 0);
+        mma_commit(&P.empty[slot]);
+        ++m.c;
+        return true;
+      };
+      for (int x = 0; x < 2 && ok; ++x)
+        if (next_item(x) && !issue_s(x)) ok = false;
+      while (ok && !(st[0].done && st[1].done)) {
+        for (int x = 0; x < 2 && ok; ++x) {
+          State& m = st[x];
+          if (m.done) continue;
+          if (!issue_pv(x)) {
+            ok = false;
+            break;
+          }
+          if (m.j == m.n - 1) {
+            mma_commit(pipe_at(smem, x).bar_o);
+            ++m.no;
+            if (!next_item(x)) continue;  // out of work (or ok cleared)
+          } else {
+            ++m.j;
+          }
+          if (!issue_s(x)) ok = false;
+        }
       }
       if (!ok) {
         *abort_flag = 1;
@@ -595,127 +745,168 @@ __global__ void __launch_bounds__(192, 2)
         mbar_wait_drain(bar_drain, 0);
       }
     }
+    }
   } else {
-    // ------------------------------------------------------------ softmax (warps 0-3)
-    const int r = warp * 32 + lane;
-    const int i = q0 + r;
-    const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
+    regs_inc<C::REGS_SOFTMAX>();
+    // ------------------------------------------------------------ softmax + epilogue of pipeline warp / 4
+    const int x = warp >> 2;
+    const Pipe128 P = pipe_at(smem, x);
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lane_base = tmem + x * C::TMEM_PIPE + ((uint32_t)((warp & 3) * 32) << 16);
     const uint32_t scol = lane_base + C::TMEM_S;
     const float sl2 = g.scale_log2;
-    const int lo_i = kr.lo(i), hi_i = kr.hi(i);
-    const int lo_last = kr.lo(q_last), hi_first = kr.hi(q0);
-    float mbs = -INFINITY, l = 0.f;  // running max of S*scale*log2e, and the row sum
+    int w = 0, tiles = 0, no = 0;
     bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      if (!__all_sync(0xffffffffu, mbar_wait(bar_s, j & 1, abort_flag))) {
+    while (ok) {
+      const int e = w & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&P.sched_full[e], (w >> 1) & 1, abort_flag))) {
         ok = false;
         break;
       }
-      tc_fence_after();
-      const int kb = (t_lo + j) * 128;
-      const bool interior = lo_last <= kb && hi_first >= kb + 128;
-      // One pass: P against the running max m (P = exp2(S*scale*log2e - m)),
-      // keeping the largest exponent t. While t <= 8 every P is <= 256 and
-      // m can stay as it is. A row whose scores jumped higher (or that sees
-      // its first allowed key) is recomputed against its new max (S is still
-      // intact in TMEM: P is only written back after the check), and O and l
-      // are rescaled by exp2(-t).
-      const float mb = (mbs == -INFINITY) ? 0.f : mbs;
-      float rs = 0.f, tmax = -INFINITY;
-      uint32_t pk[64];
-      if (interior)
-        p_pass<false, E>(scol, sl2, mb, kb, lo_i, hi_i, pk, rs, tmax);
-      else
-        p_pass<true, E>(scol, sl2, mb, kb, lo_i, hi_i, pk, rs, tmax);
-      // A row's first allowed keys always take the second pass, against its
-      // exact max: its largest P is then exactly 1, so the rounding of the
-      // dominant P cannot bias O against the LSE.
-      const bool redo = tmax > 8.f || (mbs == -INFINITY && tmax > -INFINITY);
-      float f = 1.f;
-      if (__any_sync(0xffffffffu, redo)) {
-        // the whole warp repeats the pass (TMEM loads are warp-wide); rows
-        // that keep their max recompute bit-identical values
-        const float mb2 = redo ? mb + tmax : mb;
-        float t2 = -INFINITY;
+      const int item = *reinterpret_cast<volatile int*>(&P.sched[e]);
+      mbar_arrive(&P.sched_empty[e]);
+      ++w;
+      if (item < 0) break;
+      int lo_i, hi_i, lo_last, hi_first, t_lo, n;
+      {
+        Tile128 t;
+        decode_tile(p, item, t);
+        const int i = t.q0 + r;
+        lo_i = t.kr.lo(i);
+        hi_i = t.kr.hi(i);
+        lo_last = t.kr.lo(t.q_last);
+        hi_first = t.kr.hi(t.q0);
+        t_lo = t.t_lo;
+        n = t.n;
+      }
+      float mbs = -INFINITY, l = 0.f;  // running max of S*scale*log2e, and the row sum
+      for (int j = 0; j < n; ++j) {
+        if (!__all_sync(0xffffffffu, mbar_wait(P.bar_s, tiles & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        ++tiles;
+        tc_fence_after();
+        const int kb = (t_lo + j) * 128;
+        const bool interior = lo_last <= kb && hi_first >= kb + 128;
+        // One pass: P against the running max m (P = exp2(S*scale*log2e - m)),
+        // keeping the largest exponent t. While t <= 8 every P is <= 256 and
+        // m can stay as it is. A row whose scores jumped higher (or that sees
+        // its first allowed key) is recomputed against its new max (S is still
+        // intact in TMEM: P is only written back after the check), and O and l
+        // are rescaled by exp2(-t).
+        const float mb = (mbs == -INFINITY) ? 0.f : mbs;
+        float rs = 0.f, tmax = -INFINITY;
+        uint32_t pk[64];
         if (interior)
-          p_pass<false, E>(scol, sl2, mb2, kb, lo_i, hi_i, pk, rs, t2);
+          p_pass<false, E>(scol, sl2, mb, kb, lo_i, hi_i, pk, rs, tmax);
         else
-          p_pass<true, E>(scol, sl2, mb2, kb, lo_i, hi_i, pk, rs, t2);
-      }
-      if (redo) {
-        f = mbs == -INFINITY ? 0.f : ex2(-tmax);
-        mbs = mb + tmax;
-      }
-      l = l * f + rs;
+          p_pass<true, E>(scol, sl2, mb, kb, lo_i, hi_i, pk, rs, tmax);
+        // A row's first allowed keys always take the second pass, against its
+        // exact max: its largest P is then exactly 1, so the rounding of the
+        // dominant P cannot bias O against the LSE.
+        const bool redo = tmax > 8.f || (mbs == -INFINITY && tmax > -INFINITY);
+        float f = 1.f;
+        if (__any_sync(0xffffffffu, redo)) {
+          // the whole warp repeats the pass (TMEM loads are warp-wide); rows
+          // that keep their max recompute bit-identical values
+          const float mb2 = redo ? mb + tmax : mb;
+          float t2 = -INFINITY;
+          if (interior)
+            p_pass<false, E>(scol, sl2, mb2, kb, lo_i, hi_i, pk, rs, t2);
+          else
+            p_pass<true, E>(scol, sl2, mb2, kb, lo_i, hi_i, pk, rs, t2);
+        }
+        if (redo) {
+          f = mbs == -INFINITY ? 0.f : ex2(-tmax);
+          mbs = mb + tmax;
+        }
+        l = l * f + rs;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t q16[16];
+        for (int cc = 0; cc < 4; ++cc) {
+          uint32_t q16[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) q16[e] = pk[c * 16 + e];
-        tmem_st16(scol + c * 16, q16);
-      }
-      // PV_{j-1} completed before S_j was computed (single S buffer), so O
-      // can be rescaled here without waiting.
-      if (__any_sync(0xffffffffu, f != 1.f) && j > 0) {
+          for (int k2 = 0; k2 < 16; ++k2) q16[k2] = pk[cc * 16 + k2];
+          tmem_st16(scol + cc * 16, q16);
+        }
+        // PV_{j-1} completed before S_j was computed (single S buffer), so O
+        // can be rescaled here without waiting.
+        if (__any_sync(0xffffffffu, f != 1.f) && j > 0) {
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t u[32];
+            tmem_ld32(lane_base + C::TMEM_O + cc * 32, u);
+            tmem_wait_ld();
+            reg_fence(u);
+#pragma unroll
+            for (int k2 = 0; k2 < 32; ++k2) u[k2] = __float_as_uint(__uint_as_float(u[k2]) * f);
+            tmem_st32(lane_base + C::TMEM_O + cc * 32, u);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(P.bar_p);
+      }
+      if (!ok) break;
+      // epilogue: O / l, 32 columns at a time; O is free for the next tile's
+      // first PV once the last chunk has been read
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      if (n > 0) {
+        if (!__all_sync(0xffffffffu, mbar_wait(P.bar_o, no & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        ++no;
+        tc_fence_after();
+      }
+      // the tile's geometry again (cheaper than keeping it live through the loop)
+      Tile128 t;
+      decode_tile(p, item, t);
+      const int i = t.q0 + r;
+      const int qhead = t.si.qhead0 + t.h;
+      const bool valid = i < t.si.lq;
+      using T = typename E::T;
+      T* orow = reinterpret_cast<T*>(p.o) + ((int64_t)(t.si.qrow0 + i) * g.nh_q + qhead) * 128;
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t packed[16];
+        if (n > 0) {
           uint32_t u[32];
-          tmem_ld32(lane_base + C::TMEM_O + c * 32, u);
+          tmem_ld32(lane_base + C::TMEM_O + cc * 32, u);
           tmem_wait_ld();
           reg_fence(u);
+          if (cc == 3) {
+            tc_fence_before();
+            mbar_arrive(P.o_free);
+          }
 #pragma unroll
-          for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * f);
-          tmem_st32(lane_base + C::TMEM_O + c * 32, u);
+          for (int k2 = 0; k2 < 16; ++k2)
+            packed[k2] = E::pack(__uint_as_float(u[2 * k2]) * inv, __uint_as_float(u[2 * k2 + 1]) * inv);
+        } else {
+#pragma unroll
+          for (int k2 = 0; k2 < 16; ++k2) packed[k2] = 0u;
+        }
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+          for (int k2 = 0; k2 < 4; ++k2)
+            dst[k2] = make_uint4(packed[4 * k2], packed[4 * k2 + 1], packed[4 * k2 + 2], packed[4 * k2 + 3]);
         }
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(bar_p);
-    }
-    if (ok && n_tiles > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_o, (n_tiles - 1) & 1, abort_flag));
-      tc_fence_after();
+      if (valid)
+        p.lse[(int64_t)(t.si.qrow0 + i) * g.nh_q + qhead] = l > 0.f ? mbs * 0.6931471805599453f + logf(l) : -INFINITY;
     }
     if (!ok) {
       *abort_flag = 1;
       record_error(p.err, SDPA_ERR_TIMEOUT);
-    } else {
-      const bool valid = i < si.lq;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      using T = typename E::T;
-      T* orow = reinterpret_cast<T*>(p.o) + ((int64_t)(si.qrow0 + i) * g.nh_q + qhead) * 128;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t packed[16];
-        if (n_tiles > 0) {
-          uint32_t u[32];
-          tmem_ld32(lane_base + C::TMEM_O + c * 32, u);
-          tmem_wait_ld();
-          reg_fence(u);
-#pragma unroll
-          for (int e = 0; e < 16; ++e)
-            packed[e] = E::pack(__uint_as_float(u[2 * e]) * inv, __uint_as_float(u[2 * e + 1]) * inv);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) packed[e] = 0u;
-        }
-        if (valid) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            dst[e] = make_uint4(packed[4 * e], packed[4 * e + 1], packed[4 * e + 2], packed[4 * e + 3]);
-        }
-      }
-      if (valid)
-        p.lse[(int64_t)(si.qrow0 + i) * g.nh_q + qhead] = l > 0.f ? mbs * 0.6931471805599453f + logf(l) : -INFINITY;
     }
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 10) {
     tc_fence_after();
-    tmem_dealloc(tmem, 256);
+    tmem_dealloc(tmem, 512);
   }
 }
 
@@ -724,16 +915,22 @@ static int launch_fwd128(const FwdLaunch& L) {
   auto kern = fwd128_kernel<BF16>;
   static bool attr_set = false;
   if (!attr_set) {
-    // two CTAs per SM need the largest shared-memory carveout
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Fwd2Cfg::SMEM_BYTES) != cudaSuccess ||
         cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
       return SDPA_ERR_CUDA;
     attr_set = true;
   }
-  const long long grid = (long long)L.p.n_q_tiles * L.p.g.hq * L.p.g.batch;
-  if (grid <= 0) return SDPA_OK;
-  if (grid > 0x7fffffffLL) return SDPA_ERR_UNSUPPORTED;
-  kern<<<(unsigned)grid, 192, Fwd2Cfg::SMEM_BYTES, L.stream>>>(L.tmQ, L.tmK, L.tmV, L.p);
+  const long long tiles = (long long)L.p.n_q_tiles * L.p.g.hq * L.p.g.batch;
+  if (tiles <= 0) return SDPA_OK;
+  if (tiles > 0x7fffffffLL - 4096) return SDPA_ERR_UNSUPPORTED;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return SDPA_ERR_CUDA;
+  FwdParams p = L.p;
+  p.total_tiles = (int)tiles;
+  const long long grid = std::min<long long>((tiles + 1) / 2, sms);
+  if (cudaMemsetAsync(p.tile_counter, 0, sizeof(int), L.stream) != cudaSuccess) return SDPA_ERR_CUDA;
+  kern<<<(unsigned)grid, Fwd2Cfg::THREADS, Fwd2Cfg::SMEM_BYTES, L.stream>>>(L.tmQ, L.tmK, L.tmV, p);
   return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }
 

@@ -16,6 +16,8 @@ struct FwdParams {
   const int* guard;  // per-call metadata-guard verdict (THD) or nullptr
   int n_q_tiles;     // ceil(seqlen_q / 128)
   int dv_splits;     // 1, or 2 when each CTA owns half of the value columns
+  int* tile_counter;  // head_dim 128: ticket counter in the workspace (zeroed per call)
+  int total_tiles;    // head_dim 128: tickets (query tiles x heads x batch)
 };
 
 struct FwdLaunch {

@@ -76,7 +76,9 @@ def test_check_problem_accepts_and_declines(pkg):
 
 def test_workspace_sizes(pkg):
     p = problem(pkg)
-    assert pkg.sdpa_fwd_workspace_size(p) == 0
+    # head_dim 128 keeps the persistent kernel's tile counter in the workspace
+    assert pkg.sdpa_fwd_workspace_size(p) == 256
+    assert pkg.sdpa_fwd_workspace_size(problem(pkg, head_dim=256)) == 0
     t = problem(pkg, layout=2, total_q=1000, total_kv=1000)
     assert pkg.sdpa_fwd_workspace_size(t) >= 4
     ws = pkg.sdpa_bwd_workspace_size(p)
@@ -106,12 +108,14 @@ def test_host_validation_before_any_cuda_call(pkg):
     q, k, v, o = base, base + n, base + 2 * n, base + 3 * n
     lse = base + 4 * n
     ptr = ctypes.c_void_p
-    call = lambda *a: L.sdpa_fwd(ctypes.byref(p), *[ptr(x) if x is not None else None for x in a], 0, None)
-    assert call(q + 8, k, v, o, lse, None, None, None) == 3        # misaligned q
-    assert call(q, k, v, o, lse + 4, None, None, None) == 3        # misaligned lse
-    assert call(None, k, v, o, lse, None, None, None) == 1         # null input
-    assert call(q, k, v, q + 64, lse, None, None, None) == 4       # o overlaps q
-    assert call(q, k, v, o, o + 16, None, None, None) == 4         # lse overlaps o
+    wsf = base + (1 << 31)
+    call = lambda *a: L.sdpa_fwd(ctypes.byref(p), *[ptr(x) if x is not None else None for x in a], 256, None)
+    assert call(q + 8, k, v, o, lse, None, None, wsf) == 3         # misaligned q
+    assert call(q, k, v, o, lse + 4, None, None, wsf) == 3         # misaligned lse
+    assert call(None, k, v, o, lse, None, None, wsf) == 1          # null input
+    assert call(q, k, v, q + 64, lse, None, None, wsf) == 4        # o overlaps q
+    assert call(q, k, v, o, o + 16, None, None, wsf) == 4          # lse overlaps o
+    assert call(q, k, v, o, lse, None, None, None) == 5            # head_dim 128 needs its workspace
     t = problem(pkg, layout=2, batch=2, seqlen_q=128, seqlen_kv=128, total_q=256, total_kv=256, num_heads_q=2,
                 num_heads_kv=2)
     ws = pkg.sdpa_fwd_workspace_size(t)
