@@ -206,7 +206,16 @@ BwdWs bwd_ws(const sdpa_problem* p) {
   int rq, rk, hq, hk;
   view(p, rq, rk, hq, hk);
   BwdWs w;
-  w.stat_rows = (int)round_up((size_t)rq, 4) + 128;
+  // rows of the per-head statistics arrays (see SeqInfo::srow0), plus 128 rows of
+  // padding for query tiles that overhang the last sequence
+  size_t srows;
+  if (p->layout == SDPA_THD)
+    srows = round_up((size_t)p->total_q + 4 * (size_t)p->batch + 3, 4);
+  else if (p->layout == SDPA_BSHD)
+    srows = (size_t)p->batch * round_up((size_t)p->seqlen_q, 4);
+  else
+    srows = round_up((size_t)p->seqlen_q, 4);
+  w.stat_rows = (int)(srows + 128);
   w.guard_off = 0;
   w.lse2_off = 256;
   w.delta_off = round_up(w.lse2_off + (size_t)hq * w.stat_rows * 4, 256);

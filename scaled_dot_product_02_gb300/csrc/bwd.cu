@@ -41,7 +41,7 @@ constexpr int BQ = 64;   // queries per step
 constexpr int D = 128;
 constexpr int K_BYTES = BN * D * 2;   // 32 KB, two 64-column atoms of 16 KB
 constexpr int QT_BYTES = BQ * D * 2;  // 16 KB, two atoms of 8 KB
-constexpr int STAT_FLOATS = 68;       // 64 rows + up to 3 of alignment slack + 1
+constexpr int STAT_FLOATS = BQ;       // a query tile's rows: one aligned block (SeqInfo::srow0)
 constexpr int NQS = 3;                // Q/dO stages
 constexpr int DS_BYTES = BN * BQ * 2; // 16 KB
 constexpr int STG_BYTES = BQ * D * 4; // 32 KB fp32 dQ staging
@@ -93,26 +93,34 @@ __device__ __forceinline__ uint32_t p_col(int ks) { return (uint32_t)((ks >> 1) 
 // P^T and dS^T for 32 query columns of one key row:
 //   P = exp2(S * scale*log2e - LSE*log2e) (zero where masked),
 //   dS = P * (dP - delta), both packed to 16-bit pairs.
-// nl2 holds -LSE*log2e (-inf for rows without keys), dl the deltas.
+// nl2 holds -LSE*log2e (-inf for rows without keys), dl the deltas; both are
+// 16-byte aligned in shared memory and read four at a time (the same address
+// for the whole warp, so one 16-byte broadcast feeds four columns).
 template <bool MASK, class E>
 __device__ __forceinline__ void p_ds_cols(const uint32_t (&us)[32], const uint32_t (&ud)[32], const float* nl2,
                                           const float* dl, float sl2, int q, int qlo, int qhi, uint32_t (&pp)[16],
                                           uint32_t (&pd)[16]) {
   const float2 sc = make_float2(sl2, sl2);
 #pragma unroll
-  for (int c = 0; c < 32; c += 2) {
-    const float2 t = ffma2(make_float2(__uint_as_float(us[c]), __uint_as_float(us[c + 1])), sc,
-                           make_float2(nl2[c], nl2[c + 1]));
-    float p0 = ex2(t.x), p1 = ex2(t.y);
-    if (MASK) {
-      p0 = in_range(q + c, qlo, qhi) ? p0 : 0.f;
-      p1 = in_range(q + c + 1, qlo, qhi) ? p1 : 0.f;
+  for (int c4 = 0; c4 < 32; c4 += 4) {
+    const float4 n4 = *reinterpret_cast<const float4*>(nl2 + c4);
+    const float4 d4 = *reinterpret_cast<const float4*>(dl + c4);
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int c = c4 + 2 * h;
+      const float2 nn = h ? make_float2(n4.z, n4.w) : make_float2(n4.x, n4.y);
+      const float2 dd = h ? make_float2(d4.z, d4.w) : make_float2(d4.x, d4.y);
+      const float2 t = ffma2(make_float2(__uint_as_float(us[c]), __uint_as_float(us[c + 1])), sc, nn);
+      float p0 = ex2(t.x), p1 = ex2(t.y);
+      if (MASK) {
+        p0 = in_range(q + c, qlo, qhi) ? p0 : 0.f;
+        p1 = in_range(q + c + 1, qlo, qhi) ? p1 : 0.f;
+      }
+      const float2 d = fsub2(make_float2(__uint_as_float(ud[c]), __uint_as_float(ud[c + 1])), dd);
+      const float2 ds = fmul2(make_float2(p0, p1), d);
+      pp[c / 2] = E::pack(p0, p1);
+      pd[c / 2] = E::pack(ds.x, ds.y);
     }
-    const float2 d = fsub2(make_float2(__uint_as_float(ud[c]), __uint_as_float(ud[c + 1])),
-                           make_float2(dl[c], dl[c + 1]));
-    const float2 ds = fmul2(make_float2(p0, p1), d);
-    pp[c / 2] = E::pack(p0, p1);
-    pd[c / 2] = E::pack(ds.x, ds.y);
   }
 }
 
@@ -216,7 +224,6 @@ __global__ void __launch_bounds__(512, 1)
         if (!mbar_wait(&empty[st], ((i / NQS) & 1) ^ 1, abort_flag)) break;
         const int qhead = si.qhead0 + step_head(i);
         const int row0 = si.qrow0 + step_q0(i);
-        const int arow = row0 & ~3;
         mbar_arrive_expect_tx(&full[st], 2 * QT_BYTES + 2 * STAT_FLOATS * 4);
         uint8_t* sq = smem + OFF_Q + st * QT_BYTES;
         uint8_t* sd = smem + OFF_DO + st * QT_BYTES;
@@ -224,7 +231,7 @@ __global__ void __launch_bounds__(512, 1)
         tma_load_3d(&tmQ, &full[st], sq + 8192, 64, qhead, row0);
         tma_load_3d(&tmDO, &full[st], sd, 0, qhead, row0);
         tma_load_3d(&tmDO, &full[st], sd + 8192, 64, qhead, row0);
-        const long long so = (long long)qhead * p.stat_rows + arow;
+        const long long so = (long long)qhead * p.stat_rows + si.srow0 + step_q0(i);
         bulk_load(sstat + st * 2 * STAT_FLOATS, p.lse2 + so, STAT_FLOATS * 4, &full[st]);
         bulk_load(sstat + st * 2 * STAT_FLOATS + STAT_FLOATS, p.delta + so, STAT_FLOATS * 4, &full[st]);
       }
@@ -344,8 +351,7 @@ __global__ void __launch_bounds__(512, 1)
       }
       tc_fence_after();
       const bool interior = (k0 + BN <= si.lk) && (q0 + BQ <= si.lq) && lo_last <= q0 && hi_first >= q0 + BQ;
-      const int row0 = si.qrow0 + q0;
-      const float* nl2 = sstat + st * 2 * STAT_FLOATS + (row0 & 3) + half * 32;
+      const float* nl2 = sstat + st * 2 * STAT_FLOATS + half * 32;
       const float* dl = nl2 + STAT_FLOATS;
       uint32_t us[32], ud[32];
       tmem_ld32(lane_base + tm_s(buf) + half * 32, us);

@@ -240,7 +240,7 @@ __global__ void __launch_bounds__(256, 1)
     const int i = q0 + r;
     const bool valid = i < si.lq;
     const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
-    const long long stat = (long long)qhead * p.stat_rows + si.qrow0 + i;
+    const long long stat = (long long)qhead * p.stat_rows + si.srow0 + i;
     // rows past the sequence end belong to no query: their P (and so dS) is zero
     const float nl2 = valid ? p.nlse2[stat] : -INFINITY;
     const float dl = valid ? p.delta[stat] : 0.f;
@@ -530,7 +530,7 @@ __global__ void __launch_bounds__(SF_THREADS, 1)
         mbar_arrive(bar_qd);
       }
     }
-    const long long stat = (long long)qhead * p.stat_rows + si.qrow0 + i;
+    const long long stat = (long long)qhead * p.stat_rows + si.srow0 + i;
     // rows past the sequence end belong to no query: an empty key range, so
     // their P and dS are exactly zero whatever their scores
     const float nl2 = valid ? p.nlse2[stat] : 0.f;

@@ -26,10 +26,18 @@ struct Geom {
   const int32_t* cu_kv;
 };
 
+// Per-row backward statistics (-LSE*log2e and delta) are stored per generic
+// head as [head][stat_rows]; query s of sequence b sits at srow0 + s. Every
+// sequence starts on a multiple of four rows (16 bytes), so a 64-row query
+// tile's statistics are one aligned block that bulk copies and vector loads
+// can take as it is:
+//   THD:  roundup4(cu_q[b]) + 4b     BSHD: b * roundup4(sq)     SBHD: 0
+// (SBHD keeps batches apart through the generic head.)
 struct SeqInfo {
   int lq, lk;          // lengths of this sequence
   int qrow0, krow0;    // first generic row
   int qhead0, khead0;  // generic head offset
+  int srow0;           // row of query 0 in the backward statistics arrays
 };
 
 __device__ __forceinline__ SeqInfo seq_info(const Geom& g, int b) {
@@ -40,18 +48,21 @@ __device__ __forceinline__ SeqInfo seq_info(const Geom& g, int b) {
     s.krow0 = g.cu_kv[b];
     s.lk = g.cu_kv[b + 1] - s.krow0;
     s.qhead0 = s.khead0 = 0;
+    s.srow0 = ((s.qrow0 + 3) & ~3) + 4 * b;
   } else if (g.layout == SDPA_BSHD) {
     s.lq = g.sq;
     s.lk = g.sk;
     s.qrow0 = b * g.sq;
     s.krow0 = b * g.sk;
     s.qhead0 = s.khead0 = 0;
+    s.srow0 = b * ((g.sq + 3) & ~3);
   } else {
     s.lq = g.sq;
     s.lk = g.sk;
     s.qrow0 = s.krow0 = 0;
     s.qhead0 = b * g.hq;
     s.khead0 = b * g.hkv;
+    s.srow0 = 0;
   }
   return s;
 }
