@@ -16,15 +16,17 @@
 //                head-major dQ accumulator; a finalise kernel scales and casts.
 // S^T and dP^T are double-buffered in TMEM: while the softmax warps work on
 // step i, the tensor pipe runs dV/dK/dQ of step i-1 and S^T/dP^T of step i+1,
-// so the softmax is the only serial link. dQ accumulation uses no inter-CTA
+// so the softmax is the only serial link. dQ^T of step i lands in step i's
+// dP^T/dS^T columns (dK has consumed dS^T by then), so S^T of step i+2 can
+// follow at once; only dP^T of step i+2 waits for the drain to read dQ^T. dQ accumulation uses no inter-CTA
 // barriers or credits: every contribution is an independent fp32 reduction.
 //
 // Roles (512 threads): warp 0 TMA producer; warp 1 TMEM allocator + MMA
 // issuer; warps 4-7 and 8-11 softmax (one thread per key row, each
 // warpgroup one half of the 64 query columns) and the dV / dK epilogue;
 // warps 12-15 dQ drain (one thread per head-dim row).
-// TMEM: dV [0,128) dK [128,256) S^T/P^T(/dQ^T) [256,320) [320,384)
-//       dP^T/dS^T [384,448) [448,512).
+// TMEM: dV [0,128) dK [128,256) S^T/P^T [256,320) [320,384)
+//       dP^T/dS^T(/dQ^T) [384,448) [448,512).
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -58,7 +60,7 @@ constexpr int NBARS = 2 * NQS + 10;
 constexpr int SMEM_BYTES = 1024 + OFF_BAR + NBARS * 8 + 16;
 
 // S^T/P^T and dP^T/dS^T are double-buffered; dQ^T of step i is written into
-// step i's S^T/P^T columns once dV(i) has consumed P^T.
+// step i's dP^T/dS^T columns once dK(i) has consumed dS^T.
 constexpr uint32_t TM_DV = 0, TM_DK = 128;
 __device__ __forceinline__ uint32_t tm_s(int buf) { return 256u + 64u * buf; }
 __device__ __forceinline__ uint32_t tm_dp(int buf) { return 384u + 64u * buf; }
@@ -250,12 +252,12 @@ __global__ void __launch_bounds__(512, 1)
       constexpr uint32_t ID_DQ = idesc_f16(128, BQ, BF16, true, true);      // dQ^T (A = K^T, B = dS^T)
       const uint32_t sK = smem_u32(smem + OFF_K), sV = smem_u32(smem + OFF_V);
       bool ok = mbar_wait(bar_kv, 0, abort_flag);
-      auto issue_sdp = [&](int i) -> bool {
+      // S^T(i) = K Q^T into its buffer (after the Q/dO stage of step i landed)
+      auto issue_s = [&](int i) -> bool {
         const int st = i % NQS;
         if (!mbar_wait(&full[st], (i / NQS) & 1, abort_flag)) return false;
         tc_fence_after();
         const uint32_t sq = smem_u32(smem + OFF_Q + st * QT_BYTES);
-        const uint32_t sd = smem_u32(smem + OFF_DO + st * QT_BYTES);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t ka = (ks >> 2) * 16384 + (ks & 3) * 32;
@@ -263,6 +265,12 @@ __global__ void __launch_bounds__(512, 1)
           mma_ss(tmem + tm_s(i & 1), smem_desc_sw128(sK + ka, 16, 1024), smem_desc_sw128(sq + qa, 16, 1024), ID_S,
                  ks > 0);
         }
+        return true;
+      };
+      // dP^T(i) = V dO^T (the stage is known to have landed), then signal S^T/dP^T(i)
+      auto issue_dp = [&](int i) {
+        const int st = i % NQS;
+        const uint32_t sd = smem_u32(smem + OFF_DO + st * QT_BYTES);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
           const uint32_t ka = (ks >> 2) * 16384 + (ks & 3) * 32;
@@ -271,11 +279,12 @@ __global__ void __launch_bounds__(512, 1)
                  ks > 0);
         }
         mma_commit(&bar_sdp[i & 1]);
-        return true;
       };
       tc_fence_after();
-      if (ok) ok = issue_sdp(0);
-      if (ok && n > 1) ok = issue_sdp(1);
+      for (int i = 0; i < 2 && i < n && ok; ++i) {
+        ok = issue_s(i);
+        if (ok) issue_dp(i);
+      }
       for (int i = 0; i < n && ok; ++i) {
         const int st = i % NQS;
         const int buf = i & 1;
@@ -295,23 +304,26 @@ __global__ void __launch_bounds__(512, 1)
           mma_ts(tmem + TM_DK, tmem + tm_dp(buf) + p_col(ks), smem_desc_sw128(sq + ks * 2048, 8192, 1024), ID_KV,
                  (i | ks) != 0);
         mma_commit(&empty[st]);
+        // dQ^T(i) into the dP^T/dS^T columns dK(i) has just read
         const uint32_t sds = smem_u32(smem + OFF_DS + buf * DS_BYTES);
 #pragma unroll
         for (int ks = 0; ks < BN / 16; ++ks)
-          mma_ss(tmem + tm_s(buf), smem_desc_sw128(sK + ks * 2048, 16384, 1024),
+          mma_ss(tmem + tm_dp(buf), smem_desc_sw128(sK + ks * 2048, 16384, 1024),
                  smem_desc_sw128(sds + ks * 2048, 16384, 1024), ID_DQ, ks > 0);
         mma_commit(&bar_dq[buf]);
         if (i + 2 < n) {
-          // S^T(i+2) reuses the columns dQ^T(i) sits in: wait for the drain.
+          // S^T(i+2) overwrites P^T(i), which dV(i) has read; dP^T(i+2)
+          // overwrites dQ^T(i): wait for the drain first.
+          if (!issue_s(i + 2)) {
+            ok = false;
+            break;
+          }
           if (!mbar_wait(bar_dqfree, i & 1, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
-          if (!issue_sdp(i + 2)) {
-            ok = false;
-            break;
-          }
+          issue_dp(i + 2);
         }
       }
       if (ok) {
@@ -430,8 +442,8 @@ __global__ void __launch_bounds__(512, 1)
       }
       tc_fence_after();
       uint32_t u0[32], u1[32];
-      tmem_ld32(lane_base + tm_s(buf), u0);
-      tmem_ld32(lane_base + tm_s(buf) + 32, u1);
+      tmem_ld32(lane_base + tm_dp(buf), u0);
+      tmem_ld32(lane_base + tm_dp(buf) + 32, u1);
       tmem_wait_ld();
       fence_regs(u0);
       fence_regs(u1);
