@@ -9,7 +9,10 @@ between timed steps, outside the timed events.
 value = TFLOP/s of fwd+bwd under the stated convention (fwd 4*Hq*D*Sq*Sk per
 sequence, halved for causal; bwd 2.5x fwd), summed over ranks.
 e2e   = the same metric with the inputs copied from pinned host memory and the
-outputs (O, LSE, dQ, dK, dV) copied back inside the timed region.
+outputs (O, LSE, dQ, dK, dV) copied back inside the timed region, every step;
+steps are pipelined (the copy in of step s+1 and the copy out of step s-1 run
+on their own streams beside the compute of step s, over two device buffer
+sets), and the copies of one step timed alone are reported beside it.
 
 --impl reference runs the float64 CPU oracle (the correctness reference) on a
 bounded sample of the same workload instead.
@@ -284,35 +287,90 @@ def gpu_arm(args, w, inp):
     if sdpa.sdpa_get_device_error() != 0:
         raise RuntimeError("device error during the timed steps")
 
-    # end to end: host buffers in, results back out, every step
+    # end to end: host buffers in, results back out, every step. Steps are
+    # pipelined over two device buffer sets and three streams: the host->device
+    # copy of step s+1 and the device->host copy of step s-1 run beside the
+    # compute of step s (the link is full duplex). Every step still copies its
+    # own inputs in and its own results out inside the timed region.
     h_out = {x: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for x, t in
              (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
     h2d = sum(t.numel() * t.element_size() for t in host.values()) + sum(
         t.numel() * t.element_size() for t in host_cu.values())
     d2h = sum(t.numel() * t.element_size() for t in h_out.values())
-    e_steps = max(1, args.steps // 2)
+    e_steps = max(2, args.steps // 2)
+    sets = []
+    for b in range(2):
+        dset = {x: torch.empty_like(t) for x, t in (("q", q), ("k", k), ("v", v), ("do", do), ("o", o), ("lse", lse),
+                                                     ("dq", dq), ("dk", dk), ("dv", dv), ("ws_f", ws_f), ("ws_b", ws_b))}
+        for x in host_cu:
+            dset[x] = torch.empty_like(kw[x])
+        sets.append(dset)
+    s_in, s_comp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
 
-    def e2e_step():
-        for x, dst in (("q", q), ("k", k), ("v", v), ("do", do)):
-            dst.copy_(host[x], non_blocking=True)
-        if host_cu:
-            kw["cu_seqlens_q"].copy_(host_cu["cu_seqlens_q"], non_blocking=True)
-            kw["cu_seqlens_kv"].copy_(host_cu["cu_seqlens_kv"], non_blocking=True)
-        step()
-        for x, src in (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv)):
-            h_out[x].copy_(src, non_blocking=True)
+    def e2e_step(i):
+        b = i & 1
+        d = sets[b]
+        with torch.cuda.stream(s_in):
+            if i >= 2:
+                s_in.wait_event(ev_comp[b])  # step i-2 has finished reading this set's inputs
+            for x in ("q", "k", "v", "do"):
+                d[x].copy_(host[x], non_blocking=True)
+            for x in host_cu:
+                d[x].copy_(host_cu[x], non_blocking=True)
+            ev_in[b].record(s_in)
+        s_comp.wait_event(ev_in[b])
+        if i >= 2:
+            s_comp.wait_event(ev_out[b])  # step i-2's results have left this set
+        kwb = dict(kw)
+        for x in host_cu:
+            kwb[x] = d[x]
+        sdpa.sdpa_fwd(d["q"], d["k"], d["v"], out=d["o"], lse=d["lse"], workspace=d["ws_f"], stream=s_comp, **kwb)
+        sdpa.sdpa_bwd(d["q"], d["k"], d["v"], d["o"], d["lse"], d["do"], dq=d["dq"], dk=d["dk"], dv=d["dv"],
+                      workspace=d["ws_b"], stream=s_comp, **kwb)
+        ev_comp[b].record(s_comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_comp[b])
+            for x in ("o", "lse", "dq", "dk", "dv"):
+                h_out[x].copy_(d[x], non_blocking=True)
+            ev_out[b].record(s_out)
 
-    e2e_step()
+    for i in range(2):
+        e2e_step(i)
     torch.cuda.synchronize()
+    if sdpa.sdpa_get_device_error() != 0:
+        raise RuntimeError("device error in the end-to-end warm-up")
     if world > 1:
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for _ in range(e_steps):
-        e2e_step()
-    e1.record()
+    e0.record(s_comp)
+    s_in.wait_event(e0)
+    s_out.wait_event(e0)
+    for i in range(e_steps):
+        e2e_step(i)
+    s_comp.wait_stream(s_in)
+    s_comp.wait_stream(s_out)
+    e1.record(s_comp)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e_steps
+    if sdpa.sdpa_get_device_error() != 0:
+        raise RuntimeError("device error during the end-to-end steps")
+    # the copies of a step, each timed alone (context for the overlap)
+    ta, tb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ta.record()
+    for x in ("q", "k", "v", "do"):
+        sets[0][x].copy_(host[x], non_blocking=True)
+    tb.record()
+    torch.cuda.synchronize()
+    h2d_ms = ta.elapsed_time(tb)
+    ta.record()
+    for x in ("o", "lse", "dq", "dk", "dv"):
+        h_out[x].copy_(sets[0][x], non_blocking=True)
+    tb.record()
+    torch.cuda.synchronize()
+    d2h_ms = ta.elapsed_time(tb)
 
     conv, exact = flops(w, inp)
     step_flops = 3.5 * conv
@@ -377,7 +435,10 @@ def gpu_arm(args, w, inp):
                        "l2": "flushed between timed steps (256 MiB write, outside the events)",
                        "parallelism": f"replicas x{world} (no collective)"},
             "clocks": clk, "gpu_launches": launches,
-            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+            "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "ms_per_step": e2e_ms, "h2d_ms_alone": h2d_ms, "d2h_ms_alone": d2h_ms,
+                    "overlap": "H2D of step s+1 and D2H of step s-1 beside the compute of step s (3 streams, "
+                               "2 device buffer sets)"},
             "roofline": roofline, "cpu_baseline": cpu, "detail": detail}
     if rank == 0:
         print(json.dumps(line), flush=True)
