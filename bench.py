@@ -192,7 +192,7 @@ def oracle_sample(w, inp, seconds_target: float):
 
 
 def reference_arm(args, w, inp):
-    if int(os.environ.get("RANK", "0")) != 0:
+    if rank_env()[1] != 0:  # the CPU baseline runs once, on rank 0
         return
     per_step = max(0.05, 150.0 / max(1, args.steps + args.warmup))
     s = oracle_sample(w, inp, per_step)
@@ -215,6 +215,32 @@ def reference_arm(args, w, inp):
     print(json.dumps(line), flush=True)
 
 
+# ---------------------------------------------------------------- ranks
+def rank_env():
+    """(world, rank, local_rank) from the torchrun environment (1, 0, 0 alone)."""
+    return (int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def max_over_ranks(values, world, device=None):
+    """Element-wise max of per-rank timings: the slowest rank sets the job's time."""
+    import torch
+
+    t = torch.tensor([float(x) for x in values], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def job_tflops(world, flops_per_step, steps, ms):
+    """Whole-job TFLOP/s: every rank runs the same workload (replicas, weak
+    scaling), so the job does world x the work of one rank in the slowest
+    rank's time."""
+    return world * flops_per_step * steps / (ms * 1e-3) / 1e12
+
+
 # ---------------------------------------------------------------- GPU arm
 def gpu_arm(args, w, inp):
     import torch
@@ -222,9 +248,7 @@ def gpu_arm(args, w, inp):
 
     import scaled_dot_product_02_gb300 as sdpa
 
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
+    world, rank, local = rank_env()
     torch.cuda.set_device(local)
     if world > 1:
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
@@ -374,12 +398,9 @@ def gpu_arm(args, w, inp):
 
     conv, exact = flops(w, inp)
     step_flops = 3.5 * conv
-    t_max = torch.tensor([ms, e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t_max, op=dist.ReduceOp.MAX)
-    ms, e2e_ms = float(t_max[0]), float(t_max[1])
-    value = world * step_flops * args.steps / (ms * 1e-3) / 1e12
-    e2e_value = world * step_flops / (e2e_ms * 1e-3) / 1e12
+    ms, e2e_ms = max_over_ranks([ms, e2e_ms], world, device=dev)
+    value = job_tflops(world, step_flops, args.steps, ms)
+    e2e_value = job_tflops(world, step_flops, 1, e2e_ms)
 
     pk, pk_kind = peaks()
     sustained = ms > 1000.0
