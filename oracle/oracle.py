@@ -70,6 +70,7 @@ def _load():
                                                  ctypes.c_int, ctypes.c_int, dp, dp, dp, dp, dp, dp]
             lib.sdpa_oracle_dq_rows.argtypes = [pp, dp, dp, dp, dp, ip, ip, ctypes.c_int, ip, dp]
             lib.sdpa_oracle_dkdv_rows.argtypes = [pp, dp, dp, dp, dp, ip, ip, ctypes.c_int, ip, dp, dp]
+            lib.sdpa_oracle_merge.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int, dp, dp, dp, dp]
             lib.sdpa_oracle_num_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -208,3 +209,23 @@ def dkdv_rows(q, k, v, dout, bgj, *, layout="bshd", mask="none", scale=None, win
     if rc:
         raise ValueError(f"oracle dkdv_rows rejected the problem (rc={rc})")
     return dk, dv
+
+
+def merge(o_parts, lse_parts):
+    """Combine partial results over a split of the keys (log-sum-exp merge).
+
+    o_parts (P, ..., D) and lse_parts (P, ...) with the same middle shape;
+    returns (o (..., D), lse (...)). Empty blocks carry lse = -inf.
+    """
+    o_parts, lse_parts = _f64(o_parts), _f64(lse_parts)
+    n = o_parts.shape[0]
+    d = o_parts.shape[-1]
+    mid = o_parts.shape[1:-1]
+    assert lse_parts.shape == (n,) + mid
+    items = int(np.prod(mid)) if mid else 1
+    o = np.zeros(mid + (d,))
+    lse = np.zeros(mid)
+    rc = _load().sdpa_oracle_merge(n, items, d, _dptr(o_parts), _dptr(lse_parts), _dptr(o), _dptr(lse))
+    if rc:
+        raise ValueError(f"oracle merge rejected the problem (rc={rc})")
+    return o, lse

@@ -443,6 +443,46 @@ int sdpa_oracle_dkdv_rows(const oracle_problem* p, const double* q, const double
     return 0;
 }
 
+/*
+ * Merge of partial attention results over a split of the keys (the
+ * context-parallel LSE handling of TransformerEngine PR #3527 and PR #3693,
+ * "neutral statistics for empty ragged ring blocks"). Written out as the
+ * log-sum-exp identity that makes attention over the union of key blocks
+ * equal to the combination of the blocks' own results: for every item
+ * (a row of one head),
+ *   LSE = ln sum_k exp(LSE_k),   O = sum_k exp(LSE_k - LSE) O_k.
+ * A block that saw no keys carries LSE_k = -inf and contributes nothing;
+ * when every block is empty, O = 0 and LSE = -inf (the forward's convention
+ * for a row without keys).
+ * o_parts[n_parts][items][d], lse_parts[n_parts][items] -> o[items][d], lse[items].
+ */
+int sdpa_oracle_merge(int n_parts, int64_t items, int d, const double* o_parts, const double* lse_parts, double* o,
+                      double* lse) {
+    if (n_parts < 1 || items < 0 || d < 1) return 1;
+#pragma omp parallel for schedule(static)
+    for (int64_t it = 0; it < items; ++it) {
+        double m = -INFINITY;
+        for (int k = 0; k < n_parts; ++k)
+            if (lse_parts[(int64_t)k * items + it] > m) m = lse_parts[(int64_t)k * items + it];
+        double* oi = o + it * d;
+        for (int c = 0; c < d; ++c) oi[c] = 0.0;
+        if (m == -INFINITY) {
+            lse[it] = -INFINITY;
+            continue;
+        }
+        double s = 0.0;
+        for (int k = 0; k < n_parts; ++k) s += exp(lse_parts[(int64_t)k * items + it] - m);
+        const double l = m + log(s);
+        lse[it] = l;
+        for (int k = 0; k < n_parts; ++k) {
+            const double w = exp(lse_parts[(int64_t)k * items + it] - l);
+            const double* ok = o_parts + ((int64_t)k * items + it) * d;
+            for (int c = 0; c < d; ++c) oi[c] += w * ok[c];
+        }
+    }
+    return 0;
+}
+
 int sdpa_oracle_num_threads(void) {
 #ifdef _OPENMP
     extern int omp_get_max_threads(void);

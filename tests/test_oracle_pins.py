@@ -289,3 +289,74 @@ def test_row_samplers_agree_with_full_runs():
     np.testing.assert_allclose(part["dk"][sl, 1], full["dk"][sl, 1], atol=1e-14)
     np.testing.assert_allclose(part["dq"][sl, 2:], full["dq"][sl, 2:], atol=1e-14)
     assert np.all(part["dk"][sl, 0] == 0) and np.all(part["dk"][: cq[1]] == 0)
+
+
+# ---------------------------------------------------------------- LSE merge
+def _split_keys_forward(q, k, v, bounds, scale):
+    """Oracle forward of the queries against each key block [a, b) alone."""
+    parts_o, parts_l = [], []
+    for a, b in bounds:
+        if b > a:
+            o, lse = oracle.fwd(q, k[:, a:b], v[:, a:b], layout="bshd", mask="none", scale=scale)
+        else:  # an empty block: neutral statistics
+            o, lse = np.zeros_like(q), np.full((q.shape[0] * q.shape[1], q.shape[2]), -np.inf)
+        parts_o.append(o)
+        parts_l.append(lse.reshape(q.shape[0], q.shape[1], q.shape[2]))
+    return np.stack(parts_o), np.stack(parts_l)
+
+
+def test_merge_of_key_blocks_equals_attention_over_all_keys():
+    """Attention over the union of key blocks is the log-sum-exp merge of the
+    blocks' results; checked against the library reference over all keys,
+    with unequal blocks, an empty block and scores large enough that an
+    unshifted exp would overflow."""
+    r = rng(41)
+    q = r.standard_normal((2, 19, 4, 16)) * 10.0  # scores of order 1e3: exp would overflow unshifted
+    k = r.standard_normal((2, 70, 2, 16)) * 10.0
+    v = r.standard_normal((2, 70, 2, 16))
+    scale = 1.3
+    po, pl = _split_keys_forward(q, k, v, [(0, 9), (9, 9), (9, 40), (40, 70)], scale)
+    o, lse = oracle.merge(po, pl)
+    ref = torch_ref(q, k, v, "none", scale)
+    assert np.all(np.isfinite(o)) and np.max(ref["lse"]) > 800.0
+    np.testing.assert_allclose(o, ref["o"], rtol=0, atol=1e-11)
+    np.testing.assert_allclose(lse.reshape(-1, 4), ref["lse"], rtol=1e-14, atol=0)
+
+
+def test_merge_single_block_is_identity_and_order_does_not_matter():
+    r = rng(42)
+    po = r.standard_normal((1, 5, 3, 8))
+    pl = r.standard_normal((1, 5, 3)) * 3
+    o, lse = oracle.merge(po, pl)
+    np.testing.assert_array_equal(o, po[0])
+    np.testing.assert_array_equal(lse, pl[0])
+    po = r.standard_normal((3, 5, 3, 8))
+    pl = r.standard_normal((3, 5, 3)) * 3
+    perm = [2, 0, 1]
+    a = oracle.merge(po, pl)
+    b = oracle.merge(po[perm], pl[perm])
+    np.testing.assert_allclose(a[0], b[0], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(a[1], b[1], rtol=0, atol=1e-14)
+
+
+def test_merge_of_two_equal_blocks_adds_ln2_and_keeps_the_average():
+    """Closed form: two blocks with equal LSE weigh one half each."""
+    r = rng(43)
+    o1, o2 = r.standard_normal((2, 4, 2, 8))
+    l0 = r.standard_normal((4, 2))
+    o, lse = oracle.merge(np.stack([o1, o2]), np.stack([l0, l0]))
+    np.testing.assert_allclose(o, 0.5 * (o1 + o2), rtol=0, atol=1e-15)
+    np.testing.assert_allclose(lse, l0 + math.log(2.0), rtol=0, atol=1e-15)
+
+
+def test_merge_empty_blocks_are_neutral_and_all_empty_rows_are_zero():
+    r = rng(44)
+    po = r.standard_normal((3, 6, 2, 8))
+    pl = r.standard_normal((3, 6, 2))
+    pl[1] = -np.inf               # block 1 saw no keys anywhere
+    po[1] = 1.0e30                # whatever it holds must not leak in
+    pl[:, 0, :] = -np.inf         # row 0: every block empty
+    o, lse = oracle.merge(po, pl)
+    keep = oracle.merge(po[[0, 2]], pl[[0, 2]])
+    np.testing.assert_allclose(o[1:], keep[0][1:], rtol=0, atol=1e-14)
+    assert np.all(o[0] == 0.0) and np.all(lse[0] == -np.inf)
