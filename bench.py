@@ -467,6 +467,65 @@ def gpu_arm(args, w, inp):
         dist.destroy_process_group()
 
 
+def merge_arm(args, w, inp):
+    """The log-sum-exp merge of key-split partial results (sdpa_merge) over the
+    workload's query rows: n_parts blocks of bf16 partial outputs and fp32
+    LSE, memory-bound. Prints its own JSON line (GB/s against the measured
+    HBM copy bandwidth)."""
+    import torch
+
+    import scaled_dot_product_02_gb300 as sdpa
+
+    world, rank, local = rank_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    rows = int(np.sum(seq_lengths(w, inp)[0]))
+    n_parts, d, heads = args.merge_parts, w.head_dim, w.heads_q
+    g = torch.Generator(device=dev)
+    g.manual_seed(2024)
+    po = torch.randn((n_parts, rows, heads, d), device=dev, generator=g).to(torch.bfloat16)
+    pl = torch.randn((n_parts, rows, heads), device=dev, generator=g) * 2.0 + 8.0
+    pl[0, ::7] = float("-inf")  # blocks without keys for some rows
+    o = torch.empty((rows, heads, d), device=dev, dtype=torch.bfloat16)
+    lse = torch.empty((rows, heads), device=dev, dtype=torch.float32)
+    items = rows * heads
+    # algorithmic bytes: every statistic, the rows of non-empty blocks, the outputs
+    n_empty = int(torch.isneginf(pl).sum().item())
+    nbytes = n_parts * items * 4 + (n_parts * items - n_empty) * d * 2 + items * (d * 2 + 4)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        sdpa.sdpa_merge(po, pl, out=o, lse=lse)
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    for i in range(args.steps):
+        flush.fill_(i & 255)
+        starts[i].record()
+        sdpa.sdpa_merge(po, pl, out=o, lse=lse)
+        ends[i].record()
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if sdpa.sdpa_get_device_error() != 0:
+        raise RuntimeError("device error during the merge")
+    ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / args.steps
+    (ms,) = max_over_ranks([ms], world, device=dev)
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    pk, pk_kind = peaks()
+    line = {"metric": "LSE merge of key-split partial results, GB/s", "value": world * gbs, "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": f"lse_merge_{w.name}", "n_parts": n_parts, "items": items, "head_dim": d,
+                       "bytes_per_launch": nbytes, "l2": "flushed between timed launches (256 MiB write)"},
+            "clocks": clk, "gpu_launches": args.steps,
+            "roofline": {"bound": "hbm", "kernel": "merge_kernel", "achieved": gbs, "peak": pk["hbm_gbs"],
+                         "unit": "GB/s", "frac": gbs / pk["hbm_gbs"], "traffic": None,
+                         "peak_source": f"{pk_kind} hbm_gbs"}}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def traffic_for(kind, workload):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel sources (else None)."""
@@ -498,12 +557,17 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="varlen_thd_gqa", choices=[w.name for w in workloads.ALL])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", default="step", choices=["step", "merge"],
+                    help="step: the fwd+bwd hot path (the headline); merge: the LSE merge of key-split results")
+    ap.add_argument("--merge-parts", type=int, default=4)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     w = {x.name: x for x in workloads.ALL}[args.workload]
     inp = workloads.make_inputs(w)
-    if args.impl == "reference":
+    if args.op == "merge":
+        merge_arm(args, w, inp)
+    elif args.impl == "reference":
         reference_arm(args, w, inp)
     else:
         gpu_arm(args, w, inp)

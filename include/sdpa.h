@@ -175,9 +175,36 @@ SDPA_API int sdpa_bwd_noalloc(const sdpa_problem* p, const void* q, const void* 
  * usable; read and clear the result with sdpa_get_device_error. */
 SDPA_API int sdpa_selftest_bounded_wait(unsigned limit_us, void* stream);
 
+/* Merge of partial results over a split of the keys (the context-parallel
+ * LSE handling of TransformerEngine PR #3527 "Context parallelism" and
+ * PR #3693, which keeps "neutral statistics for empty ragged ring blocks"):
+ * for every item (one row of one head)
+ *     LSE = ln sum_k exp(LSE_k),   O = sum_k exp(LSE_k - LSE) O_k.
+ * A block that saw no keys carries LSE_k = -inf and contributes nothing
+ * (its O rows are not read); an item whose blocks are all empty gets O = 0
+ * and LSE = -inf, the forward's convention for a row without keys.
+ * o_parts: device, n_parts blocks of [items][head_dim] 16-bit values, block
+ *   k at element offset k * items * head_dim (e.g. sdpa_fwd outputs over n
+ *   key blocks, stacked; items = rows x heads of the generic view).
+ * lse_parts: device fp32 [n_parts][items] (natural log, the forward's LSE).
+ * o: device [items][head_dim] (dtype), lse: device fp32 [items]; written.
+ * All pointers 16-byte aligned; the outputs may not overlap the inputs.
+ * Errors: SDPA_ERR_INVALID_ARG (null pointer, n_parts outside 1..64,
+ * items < 0), SDPA_ERR_UNSUPPORTED (dtype, head_dim not 128/256/512),
+ * SDPA_ERR_ALIGNMENT, SDPA_ERR_OVERLAP, SDPA_ERR_CUDA. Asynchronous on
+ * `stream` (a cudaStream_t, NULL = legacy default stream). */
+typedef struct {
+  int dtype;        /* sdpa_dtype of o_parts and o */
+  long long items;  /* rows x heads of one block */
+  int head_dim;     /* 128, 256 or 512 */
+  int n_parts;      /* number of key blocks, 1..64 */
+} sdpa_merge_problem;
+SDPA_API int sdpa_merge(const sdpa_merge_problem* p, const void* o_parts, const float* lse_parts, void* o, float* lse,
+               void* stream);
+
 /* Kernel timing for benchmarks and tracing. Between sdpa_profile_begin and
  * sdpa_profile_end, every sdpa_fwd / sdpa_bwd call made by this host thread
- * records a pair of CUDA events on its stream around each kernel it
+ * (and sdpa_merge) records a pair of CUDA events on its stream around each kernel it
  * launches. sdpa_profile_end synchronises those events and writes, per kernel
  * kind (SDPA_KERNEL_*), the summed milliseconds and the number of launches
  * into arrays of n_kinds entries. At most 65536 launches are recorded. */
@@ -187,7 +214,8 @@ typedef enum {
   SDPA_KERNEL_PREPROCESS = 2, /* backward preprocess (delta, LSE rescale, dQ accumulator zeroing) */
   SDPA_KERNEL_DQ_FINALIZE = 3,
   SDPA_KERNEL_GUARD = 4,      /* THD metadata guard */
-  SDPA_KERNEL_KINDS = 5
+  SDPA_KERNEL_MERGE = 5,      /* log-sum-exp merge of key-split partial results */
+  SDPA_KERNEL_KINDS = 6
 } sdpa_kernel_kind;
 SDPA_API int sdpa_profile_begin(void);
 SDPA_API int sdpa_profile_end(double* ms_by_kind, int* launches_by_kind, int n_kinds);

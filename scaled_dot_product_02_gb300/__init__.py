@@ -25,15 +25,21 @@ STATUS = {0: "SDPA_OK", 1: "SDPA_ERR_INVALID_ARG", 2: "SDPA_ERR_UNSUPPORTED", 3:
           7: "SDPA_ERR_TIMEOUT", 8: "SDPA_ERR_CUDA"}
 EXPORTS = ("sdpa_fwd_workspace_size", "sdpa_bwd_workspace_size", "sdpa_check_problem", "sdpa_fwd", "sdpa_bwd",
            "sdpa_get_device_error", "sdpa_error_string", "sdpa_last_launch_count", "sdpa_profile_begin",
-           "sdpa_profile_end", "sdpa_bwd_noalloc", "sdpa_selftest_bounded_wait")
+           "sdpa_profile_end", "sdpa_bwd_noalloc", "sdpa_selftest_bounded_wait", "sdpa_merge")
 NOALLOC_MAX_BYTES = 32 << 20  # SDPA_BWD_NOALLOC_MAX_BYTES
-KERNEL_KINDS = ("fwd", "bwd", "preprocess", "dq_finalize", "guard")
+KERNEL_KINDS = ("fwd", "bwd", "preprocess", "dq_finalize", "guard", "merge")
 
 
 class SdpaError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
         super().__init__(f"{where}: {STATUS.get(status, status)} ({error_string(status)})")
+
+
+class MergeProblem(ctypes.Structure):
+    """sdpa_merge_problem (include/sdpa.h)."""
+    _fields_ = [("dtype", ctypes.c_int), ("items", ctypes.c_longlong), ("head_dim", ctypes.c_int),
+                ("n_parts", ctypes.c_int)]
 
 
 class Problem(ctypes.Structure):
@@ -69,6 +75,7 @@ def lib():
             L.sdpa_last_launch_count.restype = ctypes.c_int
             L.sdpa_selftest_bounded_wait.argtypes = [ctypes.c_uint, vp]
             L.sdpa_bwd_noalloc.argtypes = [pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+            L.sdpa_merge.argtypes = [ctypes.POINTER(MergeProblem), vp, vp, vp, vp, vp]
             L.sdpa_profile_end.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int),
                                            ctypes.c_int]
             _lib = L
@@ -241,6 +248,38 @@ def sdpa_profile_end() -> dict:
     if rc:
         raise SdpaError(rc, "sdpa_profile_end")
     return {k: (ms[i], cnt[i]) for i, k in enumerate(KERNEL_KINDS)}
+
+
+def sdpa_merge(o_parts, lse_parts, *, out=None, lse=None, stream=None):
+    """Log-sum-exp merge of partial results over a split of the keys.
+
+    o_parts: [P, ..., H, D] (bf16/fp16, the forward's O over P key blocks,
+    stacked); lse_parts: fp32 [P, rows, H] (the forward's LSE). Returns
+    (o [..., H, D], lse [rows, H]).
+    """
+    import torch
+
+    n = o_parts.shape[0]
+    d = o_parts.shape[-1]
+    items = o_parts[0].numel() // d
+    if out is None:
+        out = torch.empty(o_parts.shape[1:], dtype=o_parts.dtype, device=o_parts.device)
+    if lse is None:
+        lse = torch.empty(lse_parts.shape[1:], dtype=torch.float32, device=o_parts.device)
+    if lse_parts.dtype != torch.float32 or lse_parts.numel() != n * items or lse.numel() != items:
+        raise ValueError("lse_parts must be float32 [P, rows, H] matching o_parts")
+    for t in (o_parts, lse_parts, out, lse):
+        if not t.is_contiguous():
+            raise ValueError("sdpa_merge needs contiguous tensors")
+    _check_cuda(o_parts, lse_parts, out, lse)
+    dt = {torch.bfloat16: 0, torch.float16: 1}.get(o_parts.dtype)
+    if dt is None:
+        raise ValueError("o_parts must be bf16 or fp16")
+    p = MergeProblem(dt, items, d, n)
+    rc = lib().sdpa_merge(ctypes.byref(p), _ptr(o_parts), _ptr(lse_parts), _ptr(out), _ptr(lse), _stream(stream))
+    if rc:
+        raise SdpaError(rc, "sdpa_merge")
+    return out, lse
 
 
 def sdpa_selftest_bounded_wait(limit_us: int = 20000, stream=None) -> None:

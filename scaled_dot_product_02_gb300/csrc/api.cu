@@ -430,6 +430,30 @@ int sdpa_bwd(const sdpa_problem* p, const void* q, const void* k, const void* v,
   return SDPA_OK;
 }
 
+int sdpa_merge(const sdpa_merge_problem* p, const void* o_parts, const float* lse_parts, void* o, float* lse,
+               void* stream) {
+  t_last_launches = 0;
+  if (!p) return SDPA_ERR_INVALID_ARG;
+  if (p->n_parts < 1 || p->n_parts > 64 || p->items < 0) return SDPA_ERR_INVALID_ARG;
+  if (p->dtype != SDPA_BF16 && p->dtype != SDPA_FP16) return SDPA_ERR_UNSUPPORTED;
+  if (p->head_dim != 128 && p->head_dim != 256 && p->head_dim != 512) return SDPA_ERR_UNSUPPORTED;
+  if (p->items == 0) return SDPA_OK;
+  if (!o_parts || !lse_parts || !o || !lse) return SDPA_ERR_INVALID_ARG;
+  if (!aligned16(o_parts) || !aligned16(lse_parts) || !aligned16(o) || !aligned16(lse)) return SDPA_ERR_ALIGNMENT;
+  const size_t ob = (size_t)p->items * p->head_dim * 2, lb = (size_t)p->items * 4;
+  const Extent eo = extent(o, ob), el = extent(lse, lb);
+  for (Extent in : {extent(o_parts, ob * p->n_parts), extent(lse_parts, lb * p->n_parts)})
+    if (overlaps(eo, in) || overlaps(el, in)) return SDPA_ERR_OVERLAP;
+  if (overlaps(eo, el)) return SDPA_ERR_OVERLAP;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int rc = timed(SDPA_KERNEL_MERGE, s, [&] {
+    return launch_merge(o_parts, lse_parts, o, lse, p->items, p->head_dim, p->n_parts, p->dtype == SDPA_BF16, s);
+  });
+  if (rc) return rc;
+  t_last_launches = 1;
+  return SDPA_OK;
+}
+
 int sdpa_get_device_error(void* stream) {
   int* err = error_word();
   if (!err) return SDPA_ERR_CUDA;

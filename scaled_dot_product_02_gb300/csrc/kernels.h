@@ -94,4 +94,8 @@ int launch_preprocess(const PrepParams& pp, bool bf16, cudaStream_t s);
 int launch_wait_selftest(uint64_t limit_ns, int* err, cudaStream_t s);
 int launch_dq_finalize(const Geom& g, const float* dq_acc, void* dq, const int* guard, bool bf16, cudaStream_t s);
 
+// Log-sum-exp merge of partial results over a split of the keys (merge.cu).
+int launch_merge(const void* o_parts, const float* lse_parts, void* o, float* lse, long long items, int head_dim,
+                 int n_parts, bool bf16, cudaStream_t s);
+
 }  // namespace sdpa

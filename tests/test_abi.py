@@ -142,3 +142,29 @@ def test_zero_sized_problems_are_no_ops(pkg):
 
     p = problem(pkg, batch=0)
     assert pkg.lib().sdpa_fwd(ctypes.byref(p), None, None, None, None, None, None, None, None, 0, None) == 0
+
+
+def test_merge_host_validation(pkg):
+    """sdpa_merge declines on the host before any CUDA call."""
+    import ctypes
+
+    L = pkg.lib()
+    ptr = ctypes.c_void_p
+    base = 1 << 40
+    items, d = 1000, 128
+    ob, lb = items * d * 2, items * 4
+    po, pl, o, lse = base, base + 4 * ob, base + 8 * ob, base + 9 * ob
+
+    def call(n_parts=3, dtype=0, head_dim=d, n_items=items, a=po, b=pl, c=o, e=lse):
+        p = pkg.MergeProblem(dtype, n_items, head_dim, n_parts)
+        return L.sdpa_merge(ctypes.byref(p), ptr(a), ptr(b), ptr(c), ptr(e), None)
+
+    assert call(n_parts=0) == 1                      # SDPA_ERR_INVALID_ARG
+    assert call(n_parts=65) == 1
+    assert call(head_dim=64) == 2                    # SDPA_ERR_UNSUPPORTED
+    assert call(dtype=3) == 2
+    assert call(n_items=0) == 0                      # nothing to do
+    assert call(a=po + 8) == 3                       # SDPA_ERR_ALIGNMENT
+    assert call(c=po + ob) == 4                      # output inside the partial outputs: SDPA_ERR_OVERLAP
+    assert call(e=pl) == 4                           # output LSE over the partial LSE
+    assert L.sdpa_merge(None, None, None, None, None, None) == 1
