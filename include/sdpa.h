@@ -98,6 +98,10 @@ typedef struct {
   int window_left;  /* keys allowed left of the diagonal; -1 = unbounded (PR #3693 window pair) */
   int window_right; /* keys allowed right of the diagonal; -1 = unbounded; causal requires 0 or -1 */
   float softmax_scale; /* multiplies Q K^T before the mask, e.g. 1/sqrt(D) */
+  int deterministic;   /* backward only. 0: head_dim 128 accumulates dQ with fp32 reductions (fastest,
+                          not bitwise reproducible). 1: every gradient bitwise reproducible run to run
+                          (head_dim 128 forms dQ in a separate pass that recomputes S and dP per query
+                          tile; head_dim 256/512 are always so). Must be 0 or 1. */
 } sdpa_problem;
 
 /* Bytes of device workspace sdpa_fwd / sdpa_bwd need for this problem
@@ -133,8 +137,9 @@ SDPA_API int sdpa_fwd(const sdpa_problem* p, const void* q, const void* k, const
  * read); dq [.., Hq, D], dk, dv [.., Hkv, D] (device, written, fully
  * overwritten). workspace: device scratch of at least
  * sdpa_bwd_workspace_size bytes (float32 dQ accumulator and per-row
- * statistics). dQ is accumulated with float32 atomics, so it is not bitwise
- * reproducible run to run; dK and dV are. */
+ * statistics). With p->deterministic = 0, head_dim 128 accumulates dQ with
+ * float32 reductions, so dQ is not bitwise reproducible run to run (dK and
+ * dV are); with 1, every output is. */
 SDPA_API int sdpa_bwd(const sdpa_problem* p, const void* q, const void* k, const void* v, const void* o, const float* lse,
              const void* dout, void* dq, void* dk, void* dv, const int32_t* cu_seqlens_q,
              const int32_t* cu_seqlens_kv, void* workspace, size_t ws_bytes, void* stream);

@@ -45,7 +45,8 @@ class MergeProblem(ctypes.Structure):
 class Problem(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in ("layout", "dtype", "mask_type", "batch", "seqlen_q", "seqlen_kv",
                                             "total_q", "total_kv", "num_heads_q", "num_heads_kv", "head_dim",
-                                            "window_left", "window_right")] + [("softmax_scale", ctypes.c_float)]
+                                            "window_left", "window_right")] + [("softmax_scale", ctypes.c_float),
+                                                                               ("deterministic", ctypes.c_int)]
 
 
 _lock = threading.Lock()
@@ -90,7 +91,7 @@ sdpa_error_string = error_string
 
 
 def make_problem(q, k, *, layout="bshd", mask="none", window=(-1, -1), scale=None, dtype=None, batch=None,
-                 max_seqlen_q=None, max_seqlen_kv=None) -> Problem:
+                 max_seqlen_q=None, max_seqlen_kv=None, deterministic=False) -> Problem:
     """sdpa_problem from tensor shapes (no device access)."""
     import torch
 
@@ -114,6 +115,7 @@ def make_problem(q, k, *, layout="bshd", mask="none", window=(-1, -1), scale=Non
     p.head_dim = d
     p.window_left, p.window_right = int(window[0]), int(window[1])
     p.softmax_scale = float(scale if scale is not None else d ** -0.5)
+    p.deterministic = int(bool(deterministic))
     return p
 
 
@@ -177,13 +179,14 @@ def sdpa_fwd(q, k, v, *, layout="bshd", mask="none", window=(-1, -1), scale=None
 
 def sdpa_bwd(q, k, v, o, lse, dout, *, layout="bshd", mask="none", window=(-1, -1), scale=None,
              cu_seqlens_q=None, cu_seqlens_kv=None, max_seqlen_q=None, max_seqlen_kv=None, dq=None, dk=None,
-             dv=None, workspace=None, stream=None):
-    """Backward. Returns (dq, dk, dv)."""
+             dv=None, workspace=None, stream=None, deterministic=False):
+    """Backward. Returns (dq, dk, dv). deterministic=True makes every
+    gradient bitwise reproducible run to run (see sdpa_problem.deterministic)."""
     import torch
 
     batch = None if cu_seqlens_q is None else cu_seqlens_q.numel() - 1
     p = make_problem(q, k, layout=layout, mask=mask, window=window, scale=scale, batch=batch,
-                     max_seqlen_q=max_seqlen_q, max_seqlen_kv=max_seqlen_kv)
+                     max_seqlen_q=max_seqlen_q, max_seqlen_kv=max_seqlen_kv, deterministic=deterministic)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
@@ -202,7 +205,7 @@ def sdpa_bwd(q, k, v, o, lse, dout, *, layout="bshd", mask="none", window=(-1, -
 
 def sdpa_bwd_noalloc(q, k, v, o, lse, dout, *, layout="bshd", mask="none", window=(-1, -1), scale=None,
                      cu_seqlens_q=None, cu_seqlens_kv=None, max_seqlen_q=None, max_seqlen_kv=None, dq=None,
-                     dk=None, dv=None, stream=None):
+                     dk=None, dv=None, stream=None, deterministic=False):
     """Backward without a workspace: the library's static scratch array is
     used instead (for callers that cannot allocate device memory; problems
     needing more than NOALLOC_MAX_BYTES of scratch are rejected). Calls that
@@ -212,7 +215,7 @@ def sdpa_bwd_noalloc(q, k, v, o, lse, dout, *, layout="bshd", mask="none", windo
 
     batch = None if cu_seqlens_q is None else cu_seqlens_q.numel() - 1
     p = make_problem(q, k, layout=layout, mask=mask, window=window, scale=scale, batch=batch,
-                     max_seqlen_q=max_seqlen_q, max_seqlen_kv=max_seqlen_kv)
+                     max_seqlen_q=max_seqlen_q, max_seqlen_kv=max_seqlen_kv, deterministic=deterministic)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv

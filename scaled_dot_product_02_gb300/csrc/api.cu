@@ -131,6 +131,7 @@ int check(const sdpa_problem* p) {
   if (!causal(p) && (p->window_left >= 0 || p->window_right >= 0) && p->seqlen_q != p->seqlen_kv)
     return SDPA_ERR_UNSUPPORTED;
   if (!std::isfinite(p->softmax_scale)) return SDPA_ERR_INVALID_ARG;
+  if (p->deterministic != 0 && p->deterministic != 1) return SDPA_ERR_INVALID_ARG;
   if (p->layout == SDPA_THD) {
     if (p->total_q < 0 || p->total_kv < 0) return SDPA_ERR_INVALID_ARG;
   } else if (p->seqlen_q > 0 && p->seqlen_kv == 0 && p->batch > 0) {
@@ -221,9 +222,10 @@ BwdWs bwd_ws(const sdpa_problem* p) {
   w.delta_off = round_up(w.lse2_off + (size_t)hq * w.stat_rows * 4, 256);
   const size_t after_stats = round_up(w.delta_off + (size_t)hq * w.stat_rows * 4, 256);
   if (p->head_dim == 128) {
+    // the deterministic backward writes dQ directly and needs no accumulator
     w.acc_off = after_stats;
     w.ptile_off = w.dstile_off = w.dpdtile_off = 0;
-    w.total = round_up(w.acc_off + (size_t)hq * rq * p->head_dim * 4, 256);
+    w.total = p->deterministic ? after_stats : round_up(w.acc_off + (size_t)hq * rq * p->head_dim * 4, 256);
   } else {
     const size_t tiles = (size_t)p->batch * p->num_heads_q * ((p->seqlen_q + 127) / 128) * kv_slots(p);
     w.acc_off = 0;
@@ -366,7 +368,7 @@ int sdpa_bwd(const sdpa_problem* p, const void* q, const void* k, const void* v,
   pp.lse2 = lse2;
   pp.delta = delta;
   pp.stat_rows = w.stat_rows;
-  pp.dq_acc = p->head_dim == 128 ? acc : nullptr;
+  pp.dq_acc = (p->head_dim == 128 && !p->deterministic) ? acc : nullptr;
   pp.guard = guard;
   if ((rc = timed(SDPA_KERNEL_PREPROCESS, s, [&] { return launch_preprocess(pp, bf16, s); }))) return rc;
   ++launches;
@@ -420,12 +422,35 @@ int sdpa_bwd(const sdpa_problem* p, const void* q, const void* k, const void* v,
   if ((rc = encode(&L.tmDO, dout, p->head_dim, hq, rq, 64, bf16))) return rc;
   if ((rc = encode(&L.tmK, k, p->head_dim, hk, rk, 128, bf16))) return rc;
   if ((rc = encode(&L.tmV, v, p->head_dim, hk, rk, 128, bf16))) return rc;
+  const bool det = p->deterministic != 0;
+  L.p.dq_acc = det ? nullptr : acc;
   int n = 0;
-  if ((rc = timed(SDPA_KERNEL_BWD, s, [&] { return launch_bwd_dkdv(L, p->head_dim, bf16, &n); }))) return rc;
+  if ((rc = timed(SDPA_KERNEL_BWD, s, [&] { return launch_bwd_dkdv(L, p->head_dim, bf16, !det, &n); }))) return rc;
   launches += n;
-  if ((rc = timed(SDPA_KERNEL_DQ_FINALIZE, s, [&] { return launch_dq_finalize(g, acc, dq, guard, bf16, s); })))
-    return rc;
-  ++launches;
+  if (det) {
+    // dQ per query tile, key tiles in a fixed order, written once
+    DqLaunch Dq;
+    std::memset(&Dq, 0, sizeof(Dq));
+    Dq.p.g = g;
+    Dq.p.dq = dq;
+    Dq.p.nlse2 = lse2;
+    Dq.p.delta = delta;
+    Dq.p.stat_rows = w.stat_rows;
+    Dq.p.err = err;
+    Dq.p.guard = guard;
+    Dq.p.n_q_tiles = (p->seqlen_q + 127) / 128;
+    Dq.stream = s;
+    if ((rc = encode(&Dq.tmQ, q, p->head_dim, hq, rq, 128, bf16))) return rc;
+    if ((rc = encode(&Dq.tmDO, dout, p->head_dim, hq, rq, 128, bf16))) return rc;
+    if ((rc = encode(&Dq.tmK, k, p->head_dim, hk, rk, 128, bf16))) return rc;
+    if ((rc = encode(&Dq.tmV, v, p->head_dim, hk, rk, 128, bf16))) return rc;
+    if ((rc = timed(SDPA_KERNEL_BWD, s, [&] { return launch_dq128(Dq, bf16); }))) return rc;
+    ++launches;
+  } else {
+    if ((rc = timed(SDPA_KERNEL_DQ_FINALIZE, s, [&] { return launch_dq_finalize(g, acc, dq, guard, bf16, s); })))
+      return rc;
+    ++launches;
+  }
   t_last_launches = launches;
   return SDPA_OK;
 }

@@ -128,7 +128,8 @@ __device__ __forceinline__ void p_ds_cols(const uint32_t (&us)[32], const uint32
 
 }  // namespace
 
-template <bool BF16>
+// DQ = false: dK and dV only (no dS^T copy, no dQ^T MMA, no drain).
+template <bool BF16, bool DQ>
 __global__ void __launch_bounds__(512, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmDO,
@@ -304,13 +305,15 @@ __global__ void __launch_bounds__(512, 1)
           mma_ts(tmem + TM_DK, tmem + tm_dp(buf) + p_col(ks), smem_desc_sw128(sq + ks * 2048, 8192, 1024), ID_KV,
                  (i | ks) != 0);
         mma_commit(&empty[st]);
-        // dQ^T(i) into the dP^T/dS^T columns dK(i) has just read
-        const uint32_t sds = smem_u32(smem + OFF_DS + buf * DS_BYTES);
+        if (DQ) {
+          // dQ^T(i) into the dP^T/dS^T columns dK(i) has just read
+          const uint32_t sds = smem_u32(smem + OFF_DS + buf * DS_BYTES);
 #pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks)
-          mma_ss(tmem + tm_dp(buf), smem_desc_sw128(sK + ks * 2048, 16384, 1024),
-                 smem_desc_sw128(sds + ks * 2048, 16384, 1024), ID_DQ, ks > 0);
-        mma_commit(&bar_dq[buf]);
+          for (int ks = 0; ks < BN / 16; ++ks)
+            mma_ss(tmem + tm_dp(buf), smem_desc_sw128(sK + ks * 2048, 16384, 1024),
+                   smem_desc_sw128(sds + ks * 2048, 16384, 1024), ID_DQ, ks > 0);
+          mma_commit(&bar_dq[buf]);
+        }
         if (i + 2 < n) {
           // S^T(i+2) overwrites P^T(i), which dV(i) has read; dP^T(i+2)
           // overwrites dQ^T(i): wait for the drain first.
@@ -318,7 +321,7 @@ __global__ void __launch_bounds__(512, 1)
             ok = false;
             break;
           }
-          if (!mbar_wait(bar_dqfree, i & 1, abort_flag)) {
+          if (DQ && !mbar_wait(bar_dqfree, i & 1, abort_flag)) {
             ok = false;
             break;
           }
@@ -378,16 +381,18 @@ __global__ void __launch_bounds__(512, 1)
         p_ds_cols<true, E>(us, ud, nl2, dl, sl2, q0 + half * 32, my_qlo, my_qhi, pp, pd);
       tmem_st16(lane_base + tm_s(buf) + half * 32, pp);
       tmem_st16(lane_base + tm_dp(buf) + half * 32, pd);
-      // dS^T row r, queries [32*half, 32*half+32): four 16-byte chunks placed
-      // with the 128-byte swizzle (chunk ^ (row % 8)).
-      uint8_t* ds_row = smem + OFF_DS + buf * DS_BYTES + r * 128;
+      if (DQ) {
+        // dS^T row r, queries [32*half, 32*half+32): four 16-byte chunks placed
+        // with the 128-byte swizzle (chunk ^ (row % 8)).
+        uint8_t* ds_row = smem + OFF_DS + buf * DS_BYTES + r * 128;
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int chunk = half * 4 + k;
-        *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) * 16)) =
-            make_uint4(pd[4 * k], pd[4 * k + 1], pd[4 * k + 2], pd[4 * k + 3]);
+        for (int k = 0; k < 4; ++k) {
+          const int chunk = half * 4 + k;
+          *reinterpret_cast<uint4*>(ds_row + ((chunk ^ (r & 7)) * 16)) =
+              make_uint4(pd[4 * k], pd[4 * k + 1], pd[4 * k + 2], pd[4 * k + 3]);
+        }
+        fence_proxy_async_smem();
       }
-      fence_proxy_async_smem();
       tmem_wait_st();
       tc_fence_before();
       mbar_arrive(bar_ds);
@@ -426,7 +431,7 @@ __global__ void __launch_bounds__(512, 1)
         }
       }
     }
-  } else if (warp >= 12) {
+  } else if (warp >= 12 && DQ) {
     // ------------------------------------------------------------ dQ drain
     const int wq = warp & 3;
     const int dcol = wq * 32 + lane;  // head-dim row of dQ^T
@@ -484,9 +489,9 @@ __global__ void __launch_bounds__(512, 1)
   }
 }
 
-template <bool BF16>
+template <bool BF16, bool DQ>
 static int launch_t(const BwdLaunch& L) {
-  auto kern = bwd_kernel<BF16>;
+  auto kern = bwd_kernel<BF16, DQ>;
   static bool attr = false;
   if (!attr) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
@@ -500,10 +505,11 @@ static int launch_t(const BwdLaunch& L) {
   return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }
 
-int launch_bwd_dkdv(const BwdLaunch& L, int head_dim, bool bf16, int* launches) {
+int launch_bwd_dkdv(const BwdLaunch& L, int head_dim, bool bf16, bool with_dq, int* launches) {
   *launches = 0;
   if (head_dim != 128) return SDPA_ERR_UNSUPPORTED;
-  const int rc = bf16 ? launch_t<true>(L) : launch_t<false>(L);
+  const int rc = with_dq ? (bf16 ? launch_t<true, true>(L) : launch_t<false, true>(L))
+                         : (bf16 ? launch_t<true, false>(L) : launch_t<false, false>(L));
   if (rc == SDPA_OK) *launches = 1;
   return rc;
 }

@@ -48,7 +48,28 @@ struct BwdLaunch {
   cudaStream_t stream;
 };
 
-int launch_bwd_dkdv(const BwdLaunch& L, int head_dim, bool bf16, int* launches);
+// with_dq = false: dK and dV only (the deterministic backward forms dQ with
+// launch_dq128 instead of fp32 reductions).
+int launch_bwd_dkdv(const BwdLaunch& L, int head_dim, bool bf16, bool with_dq, int* launches);
+
+// Deterministic head_dim 128 dQ (bwd_dq.cu): per query tile, key tiles in a
+// fixed order, dQ accumulated in TMEM and written once.
+struct DqParams {
+  Geom g;
+  void* dq;             // written (dtype, scaled)
+  const float* nlse2;   // [nh_q][stat_rows] -LSE * log2(e)
+  const float* delta;   // [nh_q][stat_rows]
+  int stat_rows;
+  int* err;
+  const int* guard;
+  int n_q_tiles;
+};
+struct DqLaunch {
+  CUtensorMap tmQ, tmDO, tmK, tmV;  // 128-row boxes
+  DqParams p;
+  cudaStream_t stream;
+};
+int launch_dq128(const DqLaunch& L, bool bf16);
 
 // head_dim 256/512 backward (bwd_big.cu): score kernels write 16-bit P and
 // dS tiles, GEMM kernels form dQ, dV, dK from them.

@@ -49,7 +49,8 @@ def test_error_strings(pkg):
 def problem(pkg, **kw):
     p = pkg.Problem()
     base = dict(layout=0, dtype=0, mask_type=1, batch=2, seqlen_q=256, seqlen_kv=256, total_q=0, total_kv=0,
-                num_heads_q=8, num_heads_kv=2, head_dim=128, window_left=-1, window_right=-1, softmax_scale=0.088)
+                num_heads_q=8, num_heads_kv=2, head_dim=128, window_left=-1, window_right=-1, softmax_scale=0.088,
+                deterministic=0)
     base.update(kw)
     for k, v in base.items():
         setattr(p, k, v)
@@ -72,6 +73,8 @@ def test_check_problem_accepts_and_declines(pkg):
     assert ok(softmax_scale=float("inf")) == 1
     assert ok(seqlen_kv=0) == 1
     assert ok(layout=7) == 1
+    assert ok(deterministic=1) == 0
+    assert ok(deterministic=2) == 1
 
 
 def test_workspace_sizes(pkg):
@@ -86,6 +89,9 @@ def test_workspace_sizes(pkg):
     assert ws >= 2 * 256 * 8 * 128 * 4 + 2 * 8 * 512 * 4
     assert ws % 256 == 0
     assert pkg.sdpa_bwd_workspace_size(problem(pkg, head_dim=64)) == 0
+    # the deterministic head_dim 128 backward writes dQ directly: no fp32 accumulator
+    det = pkg.sdpa_bwd_workspace_size(problem(pkg, deterministic=1))
+    assert 0 < det < ws and ws - det >= 2 * 256 * 8 * 128 * 4
 
 
 def test_product_path_refuses_cpu_tensors(pkg):
