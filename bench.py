@@ -276,10 +276,12 @@ def gpu_arm(args, w, inp):
     ws_b = torch.empty(max(256, sdpa.sdpa_bwd_workspace_size(prob)), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
+    det = bool(args.deterministic)
+
     def step():
         sdpa.sdpa_fwd(q, k, v, out=o, lse=lse, workspace=ws_f, **kw)
         n = sdpa.sdpa_last_launch_count()
-        sdpa.sdpa_bwd(q, k, v, o, lse, do, dq=dq, dk=dk, dv=dv, workspace=ws_b, **kw)
+        sdpa.sdpa_bwd(q, k, v, o, lse, do, dq=dq, dk=dk, dv=dv, workspace=ws_b, deterministic=det, **kw)
         return n + sdpa.sdpa_last_launch_count()
 
     for _ in range(args.warmup):
@@ -353,7 +355,7 @@ def gpu_arm(args, w, inp):
             kwb[x] = d[x]
         sdpa.sdpa_fwd(d["q"], d["k"], d["v"], out=d["o"], lse=d["lse"], workspace=d["ws_f"], stream=s_comp, **kwb)
         sdpa.sdpa_bwd(d["q"], d["k"], d["v"], d["o"], d["lse"], d["do"], dq=d["dq"], dk=d["dk"], dv=d["dv"],
-                      workspace=d["ws_b"], stream=s_comp, **kwb)
+                      workspace=d["ws_b"], stream=s_comp, deterministic=det, **kwb)
         ev_comp[b].record(s_comp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev_comp[b])
@@ -408,23 +410,30 @@ def gpu_arm(args, w, inp):
     if w.dtype == "fp16":
         peak = peak * 1.0  # dense fp16 and bf16 tensor rates are equal on this part
     kern = {}
-    for kind in ("fwd", "bwd", "preprocess", "dq_finalize", "guard"):
+    for kind in ("fwd", "bwd", "preprocess", "dq_finalize", "guard", "bwd_dq"):
         tot, n = prof[kind]
         kern[kind] = {"ms_total": tot, "launches": n, "ms_avg": tot / n if n else None}
     fwd_alg = exact            # 4*D flop per unmasked pair per head
     bwd_alg = 2.5 * exact      # 10*D flop per unmasked pair per head
-    dom = max(("fwd", "bwd"), key=lambda x: kern[x]["ms_total"])
-    alg = fwd_alg if dom == "fwd" else bwd_alg
+    # algorithmic flops per launch of each kernel: the deterministic backward
+    # splits the 10*D into the dK/dV kernel (8*D: S, dP, dV, dK) and the dQ
+    # pass (2*D of useful work; it also recomputes S and dP)
+    alg_of = {"fwd": fwd_alg, "bwd": (2.0 if kern["bwd_dq"]["launches"] else 2.5) * exact, "bwd_dq": 0.5 * exact}
+    dom = max((x for x in ("fwd", "bwd", "bwd_dq") if kern[x]["launches"]), key=lambda x: kern[x]["ms_total"])
+    alg = alg_of[dom]
     achieved = alg / (kern[dom]["ms_avg"] * 1e-3) / 1e12
-    roofline = {"bound": "tensor", "kernel": f"{dom}_kernel", "achieved": achieved, "peak": peak,
-                "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic_for(dom, w.name),
+    kname = {"fwd": "fwd_kernel", "bwd": "bwd_kernel", "bwd_dq": "dq128_kernel"}[dom]
+    roofline = {"bound": "tensor", "kernel": kname, "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": traffic_for(dom, w.name) if dom != "bwd_dq" and not args.deterministic else None,
                 "peak_source": f"{pk_kind} {'bf16_tflops_sustained' if sustained else 'bf16_tflops'}",
                 "algorithmic_flops_per_launch": alg}
+    bwd_ms = (kern["bwd"]["ms_total"] + kern["bwd_dq"]["ms_total"]) / args.steps  # whole backward, per step
     detail = {
         "fwd_kernel_tflops_exact": fwd_alg / (kern["fwd"]["ms_avg"] * 1e-3) / 1e12,
-        "bwd_kernel_tflops_exact": bwd_alg / (kern["bwd"]["ms_avg"] * 1e-3) / 1e12,
+        "bwd_kernel_tflops_exact": bwd_alg / (bwd_ms * 1e-3) / 1e12,
         "fwd_kernel_tflops_convention": conv / (kern["fwd"]["ms_avg"] * 1e-3) / 1e12,
-        "bwd_kernel_tflops_convention": 2.5 * conv / (kern["bwd"]["ms_avg"] * 1e-3) / 1e12,
+        "bwd_kernel_tflops_convention": 2.5 * conv / (bwd_ms * 1e-3) / 1e12,
         "step_tflops_exact": world * 3.5 * exact * args.steps / (ms * 1e-3) / 1e12,
         "pct_of_peak_step": 100.0 * value / world / peak,
         "kernels": kern,
@@ -454,7 +463,8 @@ def gpu_arm(args, w, inp):
                        "head_dim": w.head_dim, "window": list(w.window),
                        "flop_convention": "fwd 4*Hq*D*Sq*Sk per sequence, halved for causal; bwd 2.5x fwd",
                        "l2": "flushed between timed steps (256 MiB write, outside the events)",
-                       "parallelism": f"replicas x{world} (no collective)"},
+                       "parallelism": f"replicas x{world} (no collective)",
+                       "backward": "deterministic" if det else "fp32 reductions for dQ (head_dim 128)"},
             "clocks": clk, "gpu_launches": launches,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms, "h2d_ms_alone": h2d_ms, "d2h_ms_alone": d2h_ms,
@@ -560,6 +570,8 @@ def main():
     ap.add_argument("--op", default="step", choices=["step", "merge"],
                     help="step: the fwd+bwd hot path (the headline); merge: the LSE merge of key-split results")
     ap.add_argument("--merge-parts", type=int, default=4)
+    ap.add_argument("--deterministic", action="store_true",
+                    help="bitwise-reproducible backward (head_dim 128: separate dQ pass, no fp32 reductions)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -220,7 +220,8 @@ typedef enum {
   SDPA_KERNEL_DQ_FINALIZE = 3,
   SDPA_KERNEL_GUARD = 4,      /* THD metadata guard */
   SDPA_KERNEL_MERGE = 5,      /* log-sum-exp merge of key-split partial results */
-  SDPA_KERNEL_KINDS = 6
+  SDPA_KERNEL_BWD_DQ = 6,     /* deterministic backward: the separate head_dim 128 dQ pass */
+  SDPA_KERNEL_KINDS = 7
 } sdpa_kernel_kind;
 SDPA_API int sdpa_profile_begin(void);
 SDPA_API int sdpa_profile_end(double* ms_by_kind, int* launches_by_kind, int n_kinds);

@@ -27,7 +27,7 @@ EXPORTS = ("sdpa_fwd_workspace_size", "sdpa_bwd_workspace_size", "sdpa_check_pro
            "sdpa_get_device_error", "sdpa_error_string", "sdpa_last_launch_count", "sdpa_profile_begin",
            "sdpa_profile_end", "sdpa_bwd_noalloc", "sdpa_selftest_bounded_wait", "sdpa_merge")
 NOALLOC_MAX_BYTES = 32 << 20  # SDPA_BWD_NOALLOC_MAX_BYTES
-KERNEL_KINDS = ("fwd", "bwd", "preprocess", "dq_finalize", "guard", "merge")
+KERNEL_KINDS = ("fwd", "bwd", "preprocess", "dq_finalize", "guard", "merge", "bwd_dq")
 
 
 class SdpaError(RuntimeError):

@@ -444,7 +444,7 @@ int sdpa_bwd(const sdpa_problem* p, const void* q, const void* k, const void* v,
     if ((rc = encode(&Dq.tmDO, dout, p->head_dim, hq, rq, 128, bf16))) return rc;
     if ((rc = encode(&Dq.tmK, k, p->head_dim, hk, rk, 128, bf16))) return rc;
     if ((rc = encode(&Dq.tmV, v, p->head_dim, hk, rk, 128, bf16))) return rc;
-    if ((rc = timed(SDPA_KERNEL_BWD, s, [&] { return launch_dq128(Dq, bf16); }))) return rc;
+    if ((rc = timed(SDPA_KERNEL_BWD_DQ, s, [&] { return launch_dq128(Dq, bf16); }))) return rc;
     ++launches;
   } else {
     if ((rc = timed(SDPA_KERNEL_DQ_FINALIZE, s, [&] { return launch_dq_finalize(g, acc, dq, guard, bf16, s); })))
