@@ -51,62 +51,64 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const PrepParams p) {
   const Geom& g = p.g;
   // THD metadata that failed the guard is not used for addressing
   if (p.guard && *reinterpret_cast<volatile const int*>(p.guard)) return;
-  const int b = blockIdx.y;
-  const SeqInfo si = seq_info(g, b);
-  const int sb = si.srow0;
-  const int lane = threadIdx.x % 32;
-  const int sub = lane % G;
-  constexpr int PER_WARP = 32 / G;  // items one warp handles per step
-  const int items = si.lq * g.hq;  // < 2^30 (checked on the host)
-  const int warp_id = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
-  const int n_warps = gridDim.x * blockDim.x / 32;
-  // warp-uniform trip count, so the shuffles below always see all 32 lanes
-  for (int base = warp_id * PER_WARP; base < items; base += n_warps * PER_WARP) {
-    const int it = base + lane / G;
-    const bool live = it < items;
-    // (row, head) of O, dO and LSE: for THD and BSHD the items of a sequence
-    // are contiguous in the generic view, so no division is on the load path
-    long long oi = (long long)si.qrow0 * g.nh_q + it;
-    if (g.layout == SDPA_SBHD) {
-      const int s = it / g.hq;
-      oi = (long long)s * g.nh_q + si.qhead0 + (it - s * g.hq);
-    }
-    float acc = 0.f;
-    if (live) {
-      const uint4* o4 = reinterpret_cast<const uint4*>(p.o) + oi * VPR;
-      const uint4* d4 = reinterpret_cast<const uint4*>(p.dout) + oi * VPR;
+  // one block row per sequence (more sequences than grid rows: each row takes several)
+  for (int b = blockIdx.y; b < g.batch; b += gridDim.y) {
+    const SeqInfo si = seq_info(g, b);
+    const int sb = si.srow0;
+    const int lane = threadIdx.x % 32;
+    const int sub = lane % G;
+    constexpr int PER_WARP = 32 / G;  // items one warp handles per step
+    const int items = si.lq * g.hq;  // < 2^30 (checked on the host)
+    const int warp_id = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
+    const int n_warps = gridDim.x * blockDim.x / 32;
+    // warp-uniform trip count, so the shuffles below always see all 32 lanes
+    for (int base = warp_id * PER_WARP; base < items; base += n_warps * PER_WARP) {
+      const int it = base + lane / G;
+      const bool live = it < items;
+      // (row, head) of O, dO and LSE: for THD and BSHD the items of a sequence
+      // are contiguous in the generic view, so no division is on the load path
+      long long oi = (long long)si.qrow0 * g.nh_q + it;
+      if (g.layout == SDPA_SBHD) {
+        const int s = it / g.hq;
+        oi = (long long)s * g.nh_q + si.qhead0 + (it - s * g.hq);
+      }
+      float acc = 0.f;
+      if (live) {
+        const uint4* o4 = reinterpret_cast<const uint4*>(p.o) + oi * VPR;
+        const uint4* d4 = reinterpret_cast<const uint4*>(p.dout) + oi * VPR;
 #pragma unroll
-      for (int v = 0; v < PER; ++v) {
-        const uint4 a = o4[sub + v * G], c = d4[sub + v * G];
-        const uint32_t au[4] = {a.x, a.y, a.z, a.w}, cu[4] = {c.x, c.y, c.z, c.w};
+        for (int v = 0; v < PER; ++v) {
+          const uint4 a = o4[sub + v * G], c = d4[sub + v * G];
+          const uint32_t au[4] = {a.x, a.y, a.z, a.w}, cu[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float2 fa = E::unpack(au[e]), fc = E::unpack(cu[e]);
-          acc = fmaf(fa.x, fc.x, acc);
-          acc = fmaf(fa.y, fc.y, acc);
+          for (int e = 0; e < 4; ++e) {
+            const float2 fa = E::unpack(au[e]), fc = E::unpack(cu[e]);
+            acc = fmaf(fa.x, fc.x, acc);
+            acc = fmaf(fa.y, fc.y, acc);
+          }
         }
       }
-    }
 #pragma unroll
-    for (int sh = G / 2; sh > 0; sh /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, sh, G);
-    if (live && sub == 0) {
-      const int s = it / g.hq, h = it - s * g.hq;
-      const float l = p.lse[oi];
-      const long long st = (long long)(si.qhead0 + h) * p.stat_rows + sb + s;
-      p.delta[st] = acc;
-      p.lse2[st] = (l == -INFINITY) ? -INFINITY : -l * 1.4426950408889634f;
+      for (int sh = G / 2; sh > 0; sh /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, sh, G);
+      if (live && sub == 0) {
+        const int s = it / g.hq, h = it - s * g.hq;
+        const float l = p.lse[oi];
+        const long long st = (long long)(si.qhead0 + h) * p.stat_rows + sb + s;
+        p.delta[st] = acc;
+        p.lse2[st] = (l == -INFINITY) ? -INFINITY : -l * 1.4426950408889634f;
+      }
     }
-  }
-  // rows after this sequence's block up to the next block (or the end)
-  const int end = (g.layout == SDPA_SBHD || b + 1 == g.batch) ? p.stat_rows : seq_info(g, b + 1).srow0;
-  const int gap = end - (sb + si.lq);
-  const long long pad_items = gap > 0 ? (long long)g.hq * gap : 0;
-  for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < pad_items;
-       it += (long long)gridDim.x * blockDim.x) {
-    const int h = (int)(it / gap);
-    const long long st = (long long)(si.qhead0 + h) * p.stat_rows + sb + si.lq + (int)(it % gap);
-    p.delta[st] = 0.f;
-    p.lse2[st] = -INFINITY;
+    // rows after this sequence's block up to the next block (or the end)
+    const int end = (g.layout == SDPA_SBHD || b + 1 == g.batch) ? p.stat_rows : seq_info(g, b + 1).srow0;
+    const int gap = end - (sb + si.lq);
+    const long long pad_items = gap > 0 ? (long long)g.hq * gap : 0;
+    for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < pad_items;
+         it += (long long)gridDim.x * blockDim.x) {
+      const int h = (int)(it / gap);
+      const long long st = (long long)(si.qhead0 + h) * p.stat_rows + sb + si.lq + (int)(it % gap);
+      p.delta[st] = 0.f;
+      p.lse2[st] = -INFINITY;
+    }
   }
   // zero the dQ accumulator (all block rows share the work)
   const long long n4 = p.dq_acc ? (long long)g.nh_q * g.rows_q * g.d / 4 : 0;
@@ -129,8 +131,9 @@ static int sm_count() {
 
 int launch_preprocess(const PrepParams& pp, bool bf16, cudaStream_t s) {
   if (pp.g.batch <= 0) return SDPA_OK;
-  if (pp.g.batch > 65535 || (long long)pp.g.sq * pp.g.hq >= (1LL << 30)) return SDPA_ERR_UNSUPPORTED;
-  const dim3 grid((unsigned)std::max(4, (sm_count() * 8 + pp.g.batch - 1) / pp.g.batch), (unsigned)pp.g.batch);
+  if ((long long)pp.g.sq * pp.g.hq >= (1LL << 30)) return SDPA_ERR_UNSUPPORTED;
+  const int rows = std::min(pp.g.batch, 65535);
+  const dim3 grid((unsigned)std::max(4, (sm_count() * 8 + rows - 1) / rows), (unsigned)rows);
   const int d = pp.g.d;
 #define PREP(B, DD) preprocess_kernel<B, DD><<<grid, 256, 0, s>>>(pp)
   if (d == 128) { if (bf16) PREP(true, 128); else PREP(false, 128); }
