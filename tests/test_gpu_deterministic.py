@@ -67,3 +67,56 @@ def test_two_deterministic_runs_are_bitwise_identical():
     diff = (a[0].float() - c[0].float()).abs().max().item()
     assert diff <= 2.0 ** -7 * a[0].float().abs().max().item()
     assert torch.equal(a[1], c[1]) and torch.equal(a[2], c[2])  # dK, dV: the same kernel either way
+
+
+# edge shapes through the deterministic path (the dQ pass has its own masking and ragged-tile logic)
+EDGE_DET = [
+    Workload("one_query", "bshd", "none", 2, 1, 200, 2, 1, 128, "bf16"),
+    Workload("one_key", "bshd", "causal_br", 1, 130, 1, 2, 2, 128, "bf16"),
+    Workload("diagonal_only", "bshd", "causal", 1, 200, 200, 2, 2, 128, "bf16", window=(0, 0)),
+    Workload("two_sided_window", "bshd", "none", 1, 300, 300, 2, 2, 128, "bf16", window=(20, 37)),
+    Workload("gqa_16_to_1", "bshd", "causal", 1, 256, 256, 16, 1, 128, "bf16"),
+    Workload("tiny_thd_sequences", "thd", "causal", 40, 3, 3, 2, 1, 128, "bf16", len_range=(1, 3)),
+]
+
+
+@pytest.mark.parametrize("w", EDGE_DET, ids=lambda w: w.name)
+def test_deterministic_backward_edge_shapes(w):
+    from parity import check_bwd
+
+    inp = workloads.make_inputs(w, seed=5)
+    f = lambda t: t.float().cpu().numpy().astype(np.float64)
+    dq, dk, dv = (f(t) for t in _run(w, inp, True))
+    results = check_bwd(w, inp, dq, dk, dv)
+    assert all(ok for ok, _ in results), [m for _, m in results]
+
+
+def test_deterministic_backward_with_empty_thd_sequences():
+    from parity import check_bwd
+
+    w = Workload("thd_with_empty", "thd", "causal", 4, 150, 150, 2, 2, 128, "bf16")
+    inp = workloads.make_inputs(w, seed=8, lengths=np.array([150, 0, 37, 0]))
+    f = lambda t: t.float().cpu().numpy().astype(np.float64)
+    dq, dk, dv = (f(t) for t in _run(w, inp, True))
+    results = check_bwd(w, inp, dq, dk, dv)
+    assert all(ok for ok, _ in results), [m for _, m in results]
+
+
+def test_deterministic_backward_rejects_bad_cu_seqlens_and_writes_nothing():
+    import torch
+
+    import scaled_dot_product_02_gb300 as sdpa
+
+    cu = torch.tensor([0, 120, 100], dtype=torch.int32, device="cuda")  # decreasing
+    good = torch.tensor([0, 100, 200], dtype=torch.int32, device="cuda")
+    q = torch.randn(200, 2, 128, device="cuda", dtype=torch.bfloat16)
+    k = torch.randn(200, 2, 128, device="cuda", dtype=torch.bfloat16)
+    v = torch.randn_like(k)
+    kw = dict(layout="thd", mask="causal", max_seqlen_q=100, max_seqlen_kv=100)
+    o, lse = sdpa.sdpa_fwd(q, k, v, cu_seqlens_q=good, cu_seqlens_kv=good, **kw)
+    assert sdpa.sdpa_get_device_error() == 0
+    dq, dk, dv = (torch.full_like(x, 7.0) for x in (q, k, v))
+    sdpa.sdpa_bwd(q, k, v, o, lse, q, dq=dq, dk=dk, dv=dv, cu_seqlens_q=cu, cu_seqlens_kv=good, deterministic=True,
+                  **kw)
+    assert sdpa.sdpa_get_device_error() == 6  # SDPA_ERR_BAD_SEQLENS
+    assert torch.all(dq == 7.0) and torch.all(dk == 7.0) and torch.all(dv == 7.0)
