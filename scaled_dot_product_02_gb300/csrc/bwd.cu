@@ -65,28 +65,6 @@ constexpr uint32_t TM_DV = 0, TM_DK = 128;
 __device__ __forceinline__ uint32_t tm_s(int buf) { return 256u + 64u * buf; }
 __device__ __forceinline__ uint32_t tm_dp(int buf) { return 384u + 64u * buf; }
 
-__device__ __forceinline__ bool wait_drain(uint64_t* bar, uint32_t parity) {
-  uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (globaltimer_ns() - t0 > 200000000ull) return false;
-  return true;
-}
-
-__device__ __forceinline__ void fence_regs(uint32_t (&r)[32]) {
-  asm volatile(""
-               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
-                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
-                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
-                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
-                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
-               :
-               : "memory");
-}
-
-__device__ __forceinline__ void named_barrier(int id, int threads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
-}
-
 // Column (within a 64-column S^T/dP^T buffer) of the packed 16-bit operand
 // for queries [16*ks, 16*ks+16): each half of 32 queries is packed into the
 // first 16 columns of its own 32.
@@ -242,8 +220,8 @@ __global__ void __launch_bounds__(512, 1)
         *abort_flag = 1;
         record_error(p.err, SDPA_ERR_TIMEOUT);
       }
-      wait_drain(bar_kv, 0);
-      for (int k = (i > NQS ? i - NQS : 0); k < i; ++k) wait_drain(&full[k % NQS], (k / NQS) & 1);
+      mbar_wait_drain(bar_kv, 0);
+      for (int k = (i > NQS ? i - NQS : 0); k < i; ++k) mbar_wait_drain(&full[k % NQS], (k / NQS) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -335,7 +313,7 @@ __global__ void __launch_bounds__(512, 1)
         *abort_flag = 1;
         record_error(p.err, SDPA_ERR_TIMEOUT);
         mma_commit(bar_drain);
-        wait_drain(bar_drain, 0);
+        mbar_wait_drain(bar_drain, 0);
       }
     }
   } else if (warp >= 4 && warp < 12) {
@@ -372,8 +350,8 @@ __global__ void __launch_bounds__(512, 1)
       tmem_ld32(lane_base + tm_s(buf) + half * 32, us);
       tmem_ld32(lane_base + tm_dp(buf) + half * 32, ud);
       tmem_wait_ld();
-      fence_regs(us);
-      fence_regs(ud);
+      reg_fence(us);
+      reg_fence(ud);
       uint32_t pp[16], pd[16];
       if (interior)
         p_ds_cols<false, E>(us, ud, nl2, dl, sl2, 0, 0, 0, pp, pd);
@@ -415,7 +393,7 @@ __global__ void __launch_bounds__(512, 1)
           uint32_t u[32];
           tmem_ld32(lane_base + (half ? TM_DK : TM_DV) + c * 32, u);
           tmem_wait_ld();
-          fence_regs(u);
+          reg_fence(u);
 #pragma unroll
           for (int e = 0; e < 16; ++e)
             packed[e] = E::pack(__uint_as_float(u[2 * e]) * mul, __uint_as_float(u[2 * e + 1]) * mul);
@@ -450,19 +428,19 @@ __global__ void __launch_bounds__(512, 1)
       tmem_ld32(lane_base + tm_dp(buf), u0);
       tmem_ld32(lane_base + tm_dp(buf) + 32, u1);
       tmem_wait_ld();
-      fence_regs(u0);
-      fence_regs(u1);
+      reg_fence(u0);
+      reg_fence(u1);
       tc_fence_before();
       mbar_arrive(bar_dqfree);
       if (leader) bulk_wait_group_read0();
-      named_barrier(1, 128);
+      named_bar_sync(1, 128);
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
         stg[c * D + dcol] = __uint_as_float(u0[c]);
         stg[(32 + c) * D + dcol] = __uint_as_float(u1[c]);
       }
       fence_proxy_async_smem();
-      named_barrier(1, 128);
+      named_bar_sync(1, 128);
       if (leader) {
         const int q0 = step_q0(i);
         const int rows = min(BQ, si.lq - q0);

@@ -36,25 +36,6 @@ namespace {
 constexpr int TILE_BYTES = 128 * 128 * 2;  // one 16-bit 128x128 tile image
 constexpr int CHUNK_BYTES = 32768;         // 128 rows x 128 columns of a 16-bit operand
 
-__device__ __forceinline__ bool wait_drain_big(uint64_t* bar, uint32_t parity) {
-  uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (globaltimer_ns() - t0 > 200000000ull) return false;
-  return true;
-}
-
-__device__ __forceinline__ void fence_regs32(uint32_t (&r)[32]) {
-  asm volatile(""
-               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
-                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
-                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
-                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
-                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
-               :
-               : "memory");
-}
-
-
 // Bulk store shared -> global (16-byte aligned, size multiple of 16).
 __device__ __forceinline__ void bulk_store(void* gdst, const void* ssrc, uint32_t bytes) {
   asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(reinterpret_cast<uint64_t>(gdst)),
@@ -191,8 +172,8 @@ __global__ void __launch_bounds__(256, 1)
         record_error(p.err, SDPA_ERR_TIMEOUT);
       }
       const int first = c > C::NST ? c - C::NST : 0;
-      for (int k = first; k < c; ++k) wait_drain_big(&full[k % C::NST], (k / C::NST) & 1);
-      wait_drain_big(bar_a, 0);
+      for (int k = first; k < c; ++k) mbar_wait_drain(&full[k % C::NST], (k / C::NST) & 1);
+      mbar_wait_drain(bar_a, 0);
     }
   } else if (warp == 1) {
     if (elect_one() && n > 0) {
@@ -231,7 +212,7 @@ __global__ void __launch_bounds__(256, 1)
         *abort_flag = 1;
         record_error(p.err, SDPA_ERR_TIMEOUT);
         mma_commit(bar_drain);
-        wait_drain_big(bar_drain, 0);
+        mbar_wait_drain(bar_drain, 0);
       }
     }
   } else if (warp >= 4) {
@@ -265,8 +246,8 @@ __global__ void __launch_bounds__(256, 1)
         tmem_ld32(lane_base + buf * 128 + half * 64, u0);
         tmem_ld32(lane_base + buf * 128 + half * 64 + 32, u1);
         tmem_wait_ld();
-        fence_regs32(u0);
-        fence_regs32(u1);
+        reg_fence(u0);
+        reg_fence(u1);
         if (half == 1) {
           tc_fence_before();
           mbar_arrive(&bar_sfree[buf]);
@@ -454,7 +435,7 @@ __global__ void __launch_bounds__(SF_THREADS, 1)
         record_error(p.err, SDPA_ERR_TIMEOUT);
       }
       const int first = c > SF_NST ? c - SF_NST : 0;
-      for (int k = first; k < c; ++k) wait_drain_big(&full[k % SF_NST], (k / SF_NST) & 1);
+      for (int k = first; k < c; ++k) mbar_wait_drain(&full[k % SF_NST], (k / SF_NST) & 1);
     }
   } else if (warp == 1) {
     if (elect_one()) {
@@ -491,7 +472,7 @@ __global__ void __launch_bounds__(SF_THREADS, 1)
         *abort_flag = 1;
         record_error(p.err, SDPA_ERR_TIMEOUT);
         mma_commit(bar_drain);
-        wait_drain_big(bar_drain, 0);
+        mbar_wait_drain(bar_drain, 0);
       }
     }
   } else if (warp >= 2) {
@@ -554,8 +535,8 @@ __global__ void __launch_bounds__(SF_THREADS, 1)
         tmem_ld32(lane_base + SF_TM_S + grp * 64, *reinterpret_cast<uint32_t(*)[32]>(u));
         tmem_ld32(lane_base + SF_TM_S + grp * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(u + 32));
         tmem_wait_ld();
-        fence_regs32(*reinterpret_cast<uint32_t(*)[32]>(u));
-        fence_regs32(*reinterpret_cast<uint32_t(*)[32]>(u + 32));
+        reg_fence(*reinterpret_cast<uint32_t(*)[32]>(u));
+        reg_fence(*reinterpret_cast<uint32_t(*)[32]>(u + 32));
         tc_fence_before();
         mbar_arrive(free_s);
 #pragma unroll
@@ -576,8 +557,8 @@ __global__ void __launch_bounds__(SF_THREADS, 1)
         tmem_ld32(lane_base + SF_TM_DP + grp * 64, *reinterpret_cast<uint32_t(*)[32]>(u));
         tmem_ld32(lane_base + SF_TM_DP + grp * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(u + 32));
         tmem_wait_ld();
-        fence_regs32(*reinterpret_cast<uint32_t(*)[32]>(u));
-        fence_regs32(*reinterpret_cast<uint32_t(*)[32]>(u + 32));
+        reg_fence(*reinterpret_cast<uint32_t(*)[32]>(u));
+        reg_fence(*reinterpret_cast<uint32_t(*)[32]>(u + 32));
         tc_fence_before();
         mbar_arrive(free_dp);
 #pragma unroll
@@ -746,7 +727,7 @@ __global__ void __launch_bounds__(256, 2)
         *abort_flag = 1;
         record_error(p.err, SDPA_ERR_TIMEOUT);
       }
-      for (int k = (s > GB_NST ? s - GB_NST : 0); k < s; ++k) wait_drain_big(&full[k % GB_NST], (k / GB_NST) & 1);
+      for (int k = (s > GB_NST ? s - GB_NST : 0); k < s; ++k) mbar_wait_drain(&full[k % GB_NST], (k / GB_NST) & 1);
     }
   } else if (warp == 1) {
     if (elect_one() && n > 0) {
@@ -779,7 +760,7 @@ __global__ void __launch_bounds__(256, 2)
         *abort_flag = 1;
         record_error(p.err, SDPA_ERR_TIMEOUT);
         mma_commit(bar_drain);
-        wait_drain_big(bar_drain, 0);
+        mbar_wait_drain(bar_drain, 0);
       }
     }
   } else if (warp >= 4) {
@@ -817,7 +798,7 @@ __global__ void __launch_bounds__(256, 2)
           uint32_t u[32];
           tmem_ld32(lane_base + c * 32, u);
           tmem_wait_ld();
-          fence_regs32(u);
+          reg_fence(u);
 #pragma unroll
           for (int e = 0; e < 16; ++e)
             packed[e] = E::pack(__uint_as_float(u[2 * e]) * mul, __uint_as_float(u[2 * e + 1]) * mul);
@@ -852,27 +833,23 @@ static bool set_smem(K kern, int bytes) {
 
 template <int DQK, bool BF16>
 static int launch_big_t(const BigBwdLaunch& L, int* launches) {
-  using C = ScoreCfg<DQK>;
   const BigBwdParams& p = L.p;
   const long long g1 = (long long)p.n_q_tiles * p.g.hq * p.g.batch;
   const long long gq = g1 * (p.g.d / 256);
   const long long gkv = (long long)p.n_kv_tiles * (p.g.d / 256) * p.g.hkv * p.g.batch;
   if (g1 > 0x7fffffffLL || gq > 0x7fffffffLL || gkv > 0x7fffffffLL) return SDPA_ERR_UNSUPPORTED;
-  auto s0 = score_kernel<DQK, 0, BF16>;
-  auto s1 = score_kernel<DQK, 1, BF16>;
   auto m0 = gemm_kernel<0, BF16>;
   auto m1 = gemm_kernel<1, BF16>;
   auto m2 = gemm_kernel<2, BF16>;
   static bool attr = false;
   if (!attr) {
-    if (!set_smem(s0, C::SMEM_BYTES) || !set_smem(s1, C::SMEM_BYTES) || !set_smem(m0, GB_SMEM) ||
-        !set_smem(m1, GB_SMEM) || !set_smem(m2, GB_SMEM))
-      return SDPA_ERR_CUDA;
+    if (!set_smem(m0, GB_SMEM) || !set_smem(m1, GB_SMEM) || !set_smem(m2, GB_SMEM)) return SDPA_ERR_CUDA;
     attr = true;
   }
   int n = 0;
   if (g1 > 0) {
-    if (DQK == 256) {
+    if constexpr (DQK == 256) {
+      // one fused score kernel: P and dS from resident Q and dO
       auto sf = score_fused256_kernel<BF16>;
       static bool attr_f = false;
       if (!attr_f) {
@@ -882,6 +859,15 @@ static int launch_big_t(const BigBwdLaunch& L, int* launches) {
       sf<<<(unsigned)g1, SF_THREADS, SF_SMEM, L.stream>>>(L.tmQ, L.tmDO, L.tmK, L.tmV, p);
       n += 1;
     } else {
+      // two passes: dP - delta as fp32 tiles, then P and dS
+      using C = ScoreCfg<DQK>;
+      auto s0 = score_kernel<DQK, 0, BF16>;
+      auto s1 = score_kernel<DQK, 1, BF16>;
+      static bool attr_s = false;
+      if (!attr_s) {
+        if (!set_smem(s0, C::SMEM_BYTES) || !set_smem(s1, C::SMEM_BYTES)) return SDPA_ERR_CUDA;
+        attr_s = true;
+      }
       s0<<<(unsigned)g1, 256, C::SMEM_BYTES, L.stream>>>(L.tmDO, L.tmV, p);
       s1<<<(unsigned)g1, 256, C::SMEM_BYTES, L.stream>>>(L.tmQ, L.tmK, p);
       n += 2;

@@ -38,24 +38,6 @@ struct DqCfg {
   static constexpr uint32_t TMEM_S = 0, TMEM_DP = 128, TMEM_DQ = 256;
 };
 
-__device__ __forceinline__ bool dq_wait_drain(uint64_t* bar, uint32_t parity) {
-  uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (globaltimer_ns() - t0 > 200000000ull) return false;
-  return true;
-}
-
-__device__ __forceinline__ void dq_fence_regs(uint32_t (&r)[32]) {
-  asm volatile(""
-               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
-                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
-                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
-                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
-                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
-               :
-               : "memory");
-}
-
 // dS for 32 keys of one query row, packed to 16-bit pairs.
 template <bool MASK, class E>
 __device__ __forceinline__ void ds_cols(const uint32_t (&us)[32], const uint32_t (&ud)[32], float sl2, float nl2,
@@ -172,8 +154,8 @@ __global__ void __launch_bounds__(192, 1)
         record_error(p.err, SDPA_ERR_TIMEOUT);
       }
       const int first = c > C::NSTAGES ? c - C::NSTAGES : 0;
-      for (int k = first; k < c; ++k) dq_wait_drain(&full[k % C::NSTAGES], (k / C::NSTAGES) & 1);
-      dq_wait_drain(bar_q, 0);
+      for (int k = first; k < c; ++k) mbar_wait_drain(&full[k % C::NSTAGES], (k / C::NSTAGES) & 1);
+      mbar_wait_drain(bar_q, 0);
     }
   } else if (warp == 5) {
     // ------------------------------------------------------------ MMA issuer
@@ -233,7 +215,7 @@ __global__ void __launch_bounds__(192, 1)
         *abort_flag = 1;
         record_error(p.err, SDPA_ERR_TIMEOUT);
         mma_commit(bar_drain);
-        dq_wait_drain(bar_drain, 0);
+        mbar_wait_drain(bar_drain, 0);
       }
     }
   } else {
@@ -264,8 +246,8 @@ __global__ void __launch_bounds__(192, 1)
         tmem_ld32(lane_base + C::TMEM_S + cc * 32, us);
         tmem_ld32(lane_base + C::TMEM_DP + cc * 32, ud);
         tmem_wait_ld();
-        dq_fence_regs(us);
-        dq_fence_regs(ud);
+        reg_fence(us);
+        reg_fence(ud);
         if (__all_sync(0xffffffffu, interior))
           ds_cols<false, E>(us, ud, sl2, nl2, dl, 0, 0, 0, pd);
         else
@@ -297,7 +279,7 @@ __global__ void __launch_bounds__(192, 1)
           uint32_t u[32];
           tmem_ld32(lane_base + C::TMEM_DQ + cc * 32, u);
           tmem_wait_ld();
-          dq_fence_regs(u);
+          reg_fence(u);
 #pragma unroll
           for (int e = 0; e < 16; ++e)
             packed[e] = E::pack(__uint_as_float(u[2 * e]) * g.scale, __uint_as_float(u[2 * e + 1]) * g.scale);

@@ -46,27 +46,6 @@ struct FwdCfg {
   static constexpr int SMEM_BYTES = 1024 + Q_BYTES + NSTAGES * STAGE_BYTES + NBARS * 8 + 16;
 };
 
-// Waits that must not be cut short by the abort flag (draining copies or
-// MMAs that are already in flight before the CTA exits).
-__device__ __forceinline__ bool mbar_wait_drain(uint64_t* bar, uint32_t parity) {
-  uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (globaltimer_ns() - t0 > 200000000ull) return false;
-  return true;
-}
-
-// Keep the compiler from moving uses of TMEM-loaded registers above the wait.
-__device__ __forceinline__ void reg_fence(uint32_t (&r)[32]) {
-  asm volatile(""
-               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
-                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
-                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
-                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
-                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
-               :
-               : "memory");
-}
-
 template <int DQK, int DV, bool BF16>
 __global__ void __launch_bounds__(256, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
