@@ -43,6 +43,7 @@ class _Problem(ctypes.Structure):
         ("window_left", ctypes.c_int),
         ("window_right", ctypes.c_int),
         ("scale", ctypes.c_double),
+        ("head_dim_v", ctypes.c_int),
     ]
 
 
@@ -97,7 +98,7 @@ def _iptr(a):
 class Problem:
     """Geometry of one attention call, inferred from the array shapes."""
 
-    def __init__(self, q, k, layout, mask, scale, window=(-1, -1), cu_q=None, cu_kv=None):
+    def __init__(self, q, k, layout, mask, scale, window=(-1, -1), cu_q=None, cu_kv=None, v=None):
         self.layout = layout
         self.mask = mask
         if layout == "bshd":
@@ -119,9 +120,11 @@ class Problem:
         self.rows_kv = k.shape[0] * (k.shape[1] if layout != "thd" else 1)
         self.cu_q = None if cu_q is None else np.ascontiguousarray(cu_q, dtype=np.int32)
         self.cu_kv = None if cu_kv is None else np.ascontiguousarray(cu_kv, dtype=np.int32)
+        # width of v and o rows (the forward allows it to differ from q/k's)
+        self.dv = self.d if v is None else v.shape[-1]
         self.c = _Problem(LAYOUTS[layout], MASKS[mask], self.batch, self.sq if layout != "thd" else 0,
                           self.sk if layout != "thd" else 0, self.hq, self.hkv, self.d, int(window[0]),
-                          int(window[1]), float(scale))
+                          int(window[1]), float(scale), self.dv)
 
 
 def _f64(x):
@@ -129,11 +132,12 @@ def _f64(x):
 
 
 def fwd(q, k, v, *, layout="bshd", mask="none", scale=None, window=(-1, -1), cu_q=None, cu_kv=None):
-    """Full forward. Returns (o, lse): o in Q's layout, lse (rows_q, Hq)."""
+    """Full forward. Returns (o, lse): o in Q's layout with V's last dimension
+    (which may differ from Q/K's), lse (rows_q, Hq)."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     scale = 1.0 / np.sqrt(q.shape[-1]) if scale is None else scale
-    p = Problem(q, k, layout, mask, scale, window, cu_q, cu_kv)
-    o = np.zeros_like(q)
+    p = Problem(q, k, layout, mask, scale, window, cu_q, cu_kv, v=v)
+    o = np.zeros(q.shape[:-1] + (p.dv,))
     lse = np.full((p.rows_q, p.hq), -np.inf)
     rc = _load().sdpa_oracle_fwd(ctypes.byref(p.c), _dptr(q), _dptr(k), _dptr(v), _iptr(p.cu_q), _iptr(p.cu_kv),
                                  _dptr(o), _dptr(lse))
@@ -150,7 +154,7 @@ def bwd(q, k, v, dout, *, layout="bshd", mask="none", scale=None, window=(-1, -1
     """
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
     scale = 1.0 / np.sqrt(q.shape[-1]) if scale is None else scale
-    p = Problem(q, k, layout, mask, scale, window, cu_q, cu_kv)
+    p = Problem(q, k, layout, mask, scale, window, cu_q, cu_kv, v=v)
     b0, b1 = batch_range or (0, p.batch)
     g0, g1 = kv_head_range or (0, p.hkv)
     out = {
@@ -166,12 +170,12 @@ def bwd(q, k, v, dout, *, layout="bshd", mask="none", scale=None, window=(-1, -1
 
 
 def fwd_rows(q, k, v, bhi, *, layout="bshd", mask="none", scale=None, window=(-1, -1), cu_q=None, cu_kv=None):
-    """Forward for selected (b, h, i) rows. Returns (o_rows (n, D), lse_rows (n,))."""
+    """Forward for selected (b, h, i) rows. Returns (o_rows (n, Dv), lse_rows (n,))."""
     q, k, v = _f64(q), _f64(k), _f64(v)
     scale = 1.0 / np.sqrt(q.shape[-1]) if scale is None else scale
-    p = Problem(q, k, layout, mask, scale, window, cu_q, cu_kv)
+    p = Problem(q, k, layout, mask, scale, window, cu_q, cu_kv, v=v)
     bhi = np.ascontiguousarray(bhi, dtype=np.int32).reshape(-1, 3)
-    o = np.zeros((len(bhi), p.d))
+    o = np.zeros((len(bhi), p.dv))
     lse = np.zeros(len(bhi))
     rc = _load().sdpa_oracle_fwd_rows(ctypes.byref(p.c), _dptr(q), _dptr(k), _dptr(v), _iptr(p.cu_q),
                                       _iptr(p.cu_kv), len(bhi), _iptr(bhi), _dptr(o), _dptr(lse))
@@ -185,7 +189,7 @@ def dq_rows(q, k, v, dout, bhi, *, layout="bshd", mask="none", scale=None, windo
     """dQ for selected (b, h, i) rows. Returns (n, D)."""
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
     scale = 1.0 / np.sqrt(q.shape[-1]) if scale is None else scale
-    p = Problem(q, k, layout, mask, scale, window, cu_q, cu_kv)
+    p = Problem(q, k, layout, mask, scale, window, cu_q, cu_kv, v=v)
     bhi = np.ascontiguousarray(bhi, dtype=np.int32).reshape(-1, 3)
     dq = np.zeros((len(bhi), p.d))
     rc = _load().sdpa_oracle_dq_rows(ctypes.byref(p.c), _dptr(q), _dptr(k), _dptr(v), _dptr(dout), _iptr(p.cu_q),
@@ -200,7 +204,7 @@ def dkdv_rows(q, k, v, dout, bgj, *, layout="bshd", mask="none", scale=None, win
     """dK and dV for selected (b, kv head g, key j) rows. Returns (dk (n, D), dv (n, D))."""
     q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
     scale = 1.0 / np.sqrt(q.shape[-1]) if scale is None else scale
-    p = Problem(q, k, layout, mask, scale, window, cu_q, cu_kv)
+    p = Problem(q, k, layout, mask, scale, window, cu_q, cu_kv, v=v)
     bgj = np.ascontiguousarray(bgj, dtype=np.int32).reshape(-1, 3)
     dk = np.zeros((len(bgj), p.d))
     dv = np.zeros((len(bgj), p.d))

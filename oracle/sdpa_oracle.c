@@ -39,6 +39,13 @@
  *
  * Grouped-query attention: q head h reads kv head h / (Hq / Hkv).
  *
+ * Head dims: q and k rows have head_dim entries, v and o rows head_dim_v
+ * (0 = head_dim). The definition above never mixes the two widths: s_ij
+ * sums over the q/k width and o_i is a combination of v rows. The pages
+ * list the (192, 128) pair among the forward engine's native shapes
+ * (TransformerEngine PR #3527, "Scope"), and the backward there requires
+ * d_qk == d_v, so the backward entry points here reject unequal widths.
+ *
  * Layouts (PR #3527 "Scope": bshd, sbhd; PR #3705: compact thd with
  * zero-based cumulative sequence lengths):
  *   BSHD  x[b][s][h][d]       token row = b*S + s
@@ -72,6 +79,7 @@ typedef struct {
     int window_left;  /* < 0: unbounded */
     int window_right; /* < 0: unbounded; forced to 0 by a causal mask */
     double scale;
+    int head_dim_v;   /* width of v and o rows; 0 = head_dim */
 } oracle_problem;
 
 /* ---- geometry --------------------------------------------------------- */
@@ -95,6 +103,13 @@ static const double* qrow(const oracle_problem* p, const double* x, const int32_
 }
 static const double* kvrow(const oracle_problem* p, const double* x, const int32_t* cu, int b, int s, int g) {
     return x + (token_row(p, cu, b, s, 0) * p->num_heads_kv + g) * p->head_dim;
+}
+
+static int dv_of(const oracle_problem* p) { return p->head_dim_v > 0 ? p->head_dim_v : p->head_dim; }
+
+/* row s of kv head g of v (rows of dv_of(p) entries) */
+static const double* vrow(const oracle_problem* p, const double* x, const int32_t* cu, int b, int s, int g) {
+    return x + (token_row(p, cu, b, s, 0) * p->num_heads_kv + g) * dv_of(p);
 }
 
 static int kv_head_of(const oracle_problem* p, int h) {
@@ -147,14 +162,15 @@ static void row_forward(const oracle_problem* p, const double* q, const double* 
                         double* o_out, double* lse_out) {
     int lk = seq_len(p, cu_kv, b, 0);
     int g = kv_head_of(p, h);
+    int dv = dv_of(p);
     double lse = row_scores(p, q, k, cu_q, cu_kv, b, h, i, s);
-    for (int d = 0; d < p->head_dim; ++d) o_out[d] = 0.0;
+    for (int d = 0; d < dv; ++d) o_out[d] = 0.0;
     if (lse != -INFINITY) {
         for (int j = 0; j < lk; ++j) {
             if (s[j] == -INFINITY) continue;
             double pij = exp(s[j] - lse);
-            const double* vj = kvrow(p, v, cu_kv, b, j, g);
-            for (int d = 0; d < p->head_dim; ++d) o_out[d] += pij * vj[d];
+            const double* vj = vrow(p, v, cu_kv, b, j, g);
+            for (int d = 0; d < dv; ++d) o_out[d] += pij * vj[d];
         }
     }
     *lse_out = lse;
@@ -177,17 +193,21 @@ static int64_t rows_total(const oracle_problem* p, const int32_t* cu, int is_q) 
 
 static int valid(const oracle_problem* p) {
     if (p->num_heads_kv <= 0 || p->num_heads_q <= 0 || p->head_dim <= 0 || p->batch < 0) return 0;
-    if (p->num_heads_q % p->num_heads_kv) return 0;
+    if (p->head_dim_v < 0 || p->num_heads_q % p->num_heads_kv) return 0;
     return 1;
 }
 
+/* the backward is defined here for d_qk == d_v only */
+static int valid_bwd(const oracle_problem* p) { return valid(p) && dv_of(p) == p->head_dim; }
+
 /* ---- entry points ------------------------------------------------------ */
 
-/* Full forward: o in Q's layout, lse[token_row][Hq]. Returns 0 on success. */
+/* Full forward: o in Q's layout with head_dim_v columns, lse[token_row][Hq].
+ * Returns 0 on success. */
 int sdpa_oracle_fwd(const oracle_problem* p, const double* q, const double* k, const double* v,
                     const int32_t* cu_q, const int32_t* cu_kv, double* o, double* lse) {
     if (!valid(p)) return 1;
-    int hq = p->num_heads_q, D = p->head_dim;
+    int hq = p->num_heads_q, D = dv_of(p);
     int lkmax = max_len(p, cu_kv, 0);
     for (int b = 0; b < p->batch; ++b) {
         int lq = seq_len(p, cu_q, b, 1);
@@ -206,7 +226,7 @@ int sdpa_oracle_fwd(const oracle_problem* p, const double* q, const double* k, c
     return 0;
 }
 
-/* Forward for a list of n (b, h, i) triplets: o_rows[n][D], lse_rows[n]. */
+/* Forward for a list of n (b, h, i) triplets: o_rows[n][head_dim_v], lse_rows[n]. */
 int sdpa_oracle_fwd_rows(const oracle_problem* p, const double* q, const double* k, const double* v,
                          const int32_t* cu_q, const int32_t* cu_kv, int n, const int32_t* bhi,
                          double* o_rows, double* lse_rows) {
@@ -218,7 +238,7 @@ int sdpa_oracle_fwd_rows(const oracle_problem* p, const double* q, const double*
 #pragma omp for schedule(dynamic, 1)
         for (int r = 0; r < n; ++r)
             row_forward(p, q, k, v, cu_q, cu_kv, bhi[3 * r], bhi[3 * r + 1], bhi[3 * r + 2], s,
-                        o_rows + (size_t)r * p->head_dim, lse_rows + r);
+                        o_rows + (size_t)r * dv_of(p), lse_rows + r);
         free(s);
     }
     return 0;
@@ -236,7 +256,7 @@ int sdpa_oracle_bwd_part(const oracle_problem* p, const double* q, const double*
                          const double* dout, const int32_t* cu_q, const int32_t* cu_kv, int b_lo,
                          int b_hi, int g_lo, int g_hi, double* dq, double* dk, double* dv, double* o,
                          double* lse, double* delta) {
-    if (!valid(p)) return 1;
+    if (!valid_bwd(p)) return 1;
     int hq = p->num_heads_q, hkv = p->num_heads_kv, D = p->head_dim;
     int group = hq / hkv;
     int lqmax = max_len(p, cu_q, 1), lkmax = max_len(p, cu_kv, 0);
@@ -333,7 +353,7 @@ int sdpa_oracle_bwd(const oracle_problem* p, const double* q, const double* k, c
 int sdpa_oracle_dq_rows(const oracle_problem* p, const double* q, const double* k, const double* v,
                         const double* dout, const int32_t* cu_q, const int32_t* cu_kv, int n,
                         const int32_t* bhi, double* dq_rows) {
-    if (!valid(p)) return 1;
+    if (!valid_bwd(p)) return 1;
     int D = p->head_dim;
     int lkmax = max_len(p, cu_kv, 0);
 #pragma omp parallel
@@ -375,7 +395,7 @@ int sdpa_oracle_dq_rows(const oracle_problem* p, const double* q, const double* 
 int sdpa_oracle_dkdv_rows(const oracle_problem* p, const double* q, const double* k, const double* v,
                           const double* dout, const int32_t* cu_q, const int32_t* cu_kv, int n,
                           const int32_t* bgj, double* dk_rows, double* dv_rows) {
-    if (!valid(p)) return 1;
+    if (!valid_bwd(p)) return 1;
     int hq = p->num_heads_q, D = p->head_dim;
     int group = hq / p->num_heads_kv;
     int lkmax = max_len(p, cu_kv, 0);

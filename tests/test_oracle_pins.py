@@ -360,3 +360,83 @@ def test_merge_empty_blocks_are_neutral_and_all_empty_rows_are_zero():
     keep = oracle.merge(po[[0, 2]], pl[[0, 2]])
     np.testing.assert_allclose(o[1:], keep[0][1:], rtol=0, atol=1e-14)
     assert np.all(o[0] == 0.0) and np.all(lse[0] == -np.inf)
+
+
+# ------------------------------------------------- asymmetric head dims (d_qk != d_v)
+ASYM_CASES = [
+    # (B, Sq, Sk, Hq, Hkv, D_qk, D_v, mask)
+    (2, 9, 9, 4, 2, 12, 8, "causal"),
+    (1, 6, 11, 2, 1, 6, 10, "causal_br"),
+    (2, 5, 7, 2, 2, 16, 4, "none"),
+]
+
+
+@pytest.mark.parametrize("case", ASYM_CASES)
+def test_asymmetric_head_dims_match_torch_sdpa(case):
+    """Library reference: torch's float64 SDPA takes V with its own last
+    dimension (E for Q/K, Ev for V); O takes V's width and the LSE is that
+    of the Q/K scores."""
+    b, sq, sk, hq, hkv, d, dv, mask = case
+    r = rng(60 + d + dv)
+    q = r.standard_normal((b, sq, hq, d))
+    k = r.standard_normal((b, sk, hkv, d))
+    v = r.standard_normal((b, sk, hkv, dv))
+    ref = torch_ref(q, k, v, mask, 0.29)
+    o, lse = oracle.fwd(q, k, v, layout="bshd", mask=mask, scale=0.29)
+    assert o.shape == (b, sq, hq, dv)
+    np.testing.assert_allclose(o, ref["o"], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, ref["lse"], rtol=0, atol=1e-12)
+
+
+def test_asymmetric_value_width_acts_column_by_column_on_thd_and_sbhd():
+    """Invariant: each output column is the softmax average of one V column,
+    so narrowing V to its first Dv columns narrows O the same way and leaves
+    the LSE as it is (compared with the pinned symmetric forward, THD with a
+    window and SBHD), and the row sampler follows the full run."""
+    r = rng(61)
+    lq = np.array([23, 1, 40])
+    cq = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
+    q = r.standard_normal((cq[-1], 4, 12))
+    k = r.standard_normal((cq[-1], 2, 12))
+    v_wide = r.standard_normal((cq[-1], 2, 12))
+    v = np.ascontiguousarray(v_wide[..., :8])
+    kw = dict(layout="thd", mask="causal", cu_q=cq, cu_kv=cq, window=(6, 0), scale=0.4)
+    o_w, lse_w = oracle.fwd(q, k, v_wide, **kw)
+    o, lse = oracle.fwd(q, k, v, **kw)
+    np.testing.assert_allclose(o, o_w[..., :8], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse, lse_w, rtol=0, atol=0)
+    bhi = np.array([[0, 0, 0], [1, 3, 0], [2, 2, 39], [0, 1, 22]])
+    o_r, lse_r = oracle.fwd_rows(q, k, v, bhi, **kw)
+    for n, (bb, h, i) in enumerate(bhi):
+        np.testing.assert_allclose(o_r[n], o[cq[bb] + i, h], atol=1e-14)
+        np.testing.assert_allclose(lse_r[n], lse[cq[bb] + i, h], atol=1e-14)
+    qs = r.standard_normal((10, 2, 2, 12))      # SBHD (S, B, H, D)
+    ks = r.standard_normal((14, 2, 1, 12))
+    vs = r.standard_normal((14, 2, 1, 12))
+    o_w, lse_w = oracle.fwd(qs, ks, vs, layout="sbhd", mask="causal_br", scale=0.3)
+    o, lse = oracle.fwd(qs, ks, np.ascontiguousarray(vs[..., 5:]), layout="sbhd", mask="causal_br", scale=0.3)
+    np.testing.assert_allclose(o, o_w[..., 5:], rtol=0, atol=1e-14)
+    np.testing.assert_allclose(lse, lse_w, rtol=0, atol=0)
+
+
+def test_asymmetric_constant_value_column_comes_back_unchanged():
+    """Closed form: the softmax weights of a row sum to one, so a V column
+    that holds one constant gives that constant in every row with a key."""
+    r = rng(62)
+    q = r.standard_normal((1, 12, 2, 16))
+    k = r.standard_normal((1, 12, 2, 16))
+    v = r.standard_normal((1, 12, 2, 8))
+    v[..., 3] = 2.5
+    o, _ = oracle.fwd(q, k, v, layout="bshd", mask="causal", scale=0.25)
+    np.testing.assert_allclose(o[..., 3], 2.5, rtol=0, atol=1e-14)
+
+
+def test_backward_rejects_unequal_head_dims():
+    r = rng(63)
+    q = r.standard_normal((1, 4, 1, 8))
+    k = r.standard_normal((1, 4, 1, 8))
+    v = r.standard_normal((1, 4, 1, 6))
+    with pytest.raises(ValueError):
+        oracle.bwd(q, k, v, r.standard_normal((1, 4, 1, 6)), layout="bshd", mask="causal")
+    with pytest.raises(ValueError):
+        oracle.dq_rows(q, k, v, r.standard_normal((1, 4, 1, 6)), np.array([[0, 0, 1]]), layout="bshd")
