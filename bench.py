@@ -14,6 +14,10 @@ steps are pipelined (the copy in of step s+1 and the copy out of step s-1 run
 on their own streams beside the compute of step s, over two device buffer
 sets), and the copies of one step timed alone are reported beside it.
 
+--op fwd times the forward alone (the whole path of the forward-only
+workloads: asymmetric head dims, where the backward is declined); its
+value counts the forward FLOPs only.
+
 --impl reference runs the float64 CPU oracle (the correctness reference) on a
 bounded sample of the same workload instead.
 """
@@ -59,14 +63,21 @@ def pairs_per_head(w, lq, lk):
 
 
 def flops(w, inp):
-    """(fwd_convention, fwd_exact) FLOPs of one forward over the workload."""
+    """(fwd_convention, fwd_exact) FLOPs of one forward over the workload:
+    2*D (Q K^T) + 2*Dv (P V) per (query, key) pair per head, i.e. 4*D for
+    equal head dims."""
     lqs, lks = seq_lengths(w, inp)
+    per_pair = 2 * w.head_dim + 2 * w.dv
     conv = exact = 0
     for lq, lk in zip(lqs, lks):
-        c = 4 * w.heads_q * int(lq) * int(lk) * w.head_dim
+        c = per_pair * w.heads_q * int(lq) * int(lk)
         conv += c // 2 if w.mask != "none" else c
-        exact += 4 * w.heads_q * w.head_dim * pairs_per_head(w, int(lq), int(lk))
+        exact += per_pair * w.heads_q * pairs_per_head(w, int(lq), int(lk))
     return conv, exact
+
+
+def forward_only(args, w):
+    return args.op == "fwd" or w.name in workloads.FORWARD_ONLY
 
 
 def peaks():
@@ -129,11 +140,11 @@ class ClockSampler:
 _sample_cache = {}
 
 
-def sample_arrays(w, inp, ls, nkv=1):
+def sample_arrays(w, inp, ls, nkv=1, fwd_only=False):
     """The first `ls` query tokens of sequence 0 (and the keys they can see
     under the workload's alignment), `nkv` kv heads with their q heads,
     rounded to the workload dtype."""
-    key = (w.name, ls, nkv)
+    key = (w.name, ls, nkv, fwd_only)
     if key in _sample_cache:
         return _sample_cache[key]
     rin = workloads.rounded(inp, w.dtype)
@@ -161,32 +172,35 @@ def sample_arrays(w, inp, ls, nkv=1):
     arrs = tuple(np.ascontiguousarray(a) for a in (q, k, v, do))
     sub = w.replace(layout="bshd", batch=1, seqlen_q=lq, seqlen_kv=lk, heads_q=group, heads_kv=nkv)
     conv, _ = flops(sub, {})
-    out = (arrs, kw, 3.5 * conv, lq, group)
+    out = (arrs, kw, conv if fwd_only else 3.5 * conv, lq, group)
     _sample_cache[key] = out
     return out
 
 
-def time_oracle(w, inp, ls, nkv=1):
+def time_oracle(w, inp, ls, nkv=1, fwd_only=False):
     from oracle import oracle
 
-    (q, k, v, do), kw, fl, lq, group = sample_arrays(w, inp, ls, nkv)
+    (q, k, v, do), kw, fl, lq, group = sample_arrays(w, inp, ls, nkv, fwd_only)
     t0 = time.perf_counter()
-    oracle.bwd(q, k, v, do, mask=w.mask, scale=w.scale, window=w.window, **kw)
+    if fwd_only:
+        oracle.fwd(q, k, v, mask=w.mask, scale=w.scale, window=w.window, **kw)
+    else:
+        oracle.bwd(q, k, v, do, mask=w.mask, scale=w.scale, window=w.window, **kw)
     return time.perf_counter() - t0, fl, lq, group
 
 
-def oracle_sample(w, inp, seconds_target: float):
-    """Grow the sample until one float64 oracle fwd+bwd takes about `seconds_target`."""
+def oracle_sample(w, inp, seconds_target: float, fwd_only=False):
+    """Grow the sample until one float64 oracle fwd+bwd (or fwd) takes about `seconds_target`."""
     from oracle import oracle
 
     ls, nkv = 256, 1
-    dt, fl, lq, group = time_oracle(w, inp, ls, nkv)
+    dt, fl, lq, group = time_oracle(w, inp, ls, nkv, fwd_only)
     while dt < seconds_target * 0.6 and lq == ls:
         ls = int(ls * min(2.0, max(1.15, (seconds_target / max(dt, 1e-3)) ** 0.5)))
-        dt, fl, lq, group = time_oracle(w, inp, ls, nkv)
+        dt, fl, lq, group = time_oracle(w, inp, ls, nkv, fwd_only)
     while dt < seconds_target * 0.6 and nkv < w.heads_kv:
         nkv = min(w.heads_kv, max(nkv + 1, int(nkv * seconds_target / max(dt, 1e-3))))
-        dt, fl, lq, group = time_oracle(w, inp, ls, nkv)
+        dt, fl, lq, group = time_oracle(w, inp, ls, nkv, fwd_only)
     return {"seconds": dt, "flops": fl, "tflops": fl / dt / 1e12, "ls": lq, "group": group, "nkv": nkv,
             "threads": oracle.num_threads()}
 
@@ -194,17 +208,18 @@ def oracle_sample(w, inp, seconds_target: float):
 def reference_arm(args, w, inp):
     if rank_env()[1] != 0:  # the CPU baseline runs once, on rank 0
         return
+    fo = forward_only(args, w)
     per_step = max(0.05, 150.0 / max(1, args.steps + args.warmup))
-    s = oracle_sample(w, inp, per_step)
+    s = oracle_sample(w, inp, per_step, fo)
     times = []
     for it in range(args.warmup + args.steps):
-        dt, fl, _, _ = time_oracle(w, inp, s["ls"], s["nkv"])
+        dt, fl, _, _ = time_oracle(w, inp, s["ls"], s["nkv"], fo)
         if it >= args.warmup:
             times.append(dt)
     t = float(np.mean(times))
     value = s["flops"] / t / 1e12
-    sample = (f"float64 oracle fwd+bwd of the first {s['ls']} query tokens of sequence 0 with {s['nkv']} kv "
-              f"head(s) ({s['group']} q heads), per step")
+    sample = (f"float64 oracle {'fwd' if fo else 'fwd+bwd'} of the first {s['ls']} query tokens of sequence 0 "
+              f"with {s['nkv']} kv head(s) ({s['group']} q heads), per step")
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": t * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
@@ -254,9 +269,12 @@ def gpu_arm(args, w, inp):
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
 
     dev = torch.device("cuda", local)
-    td = {"bf16": torch.bfloat16, "fp16": torch.float16}[w.dtype]
-    host = {x: workloads.to_torch(inp[x], w.dtype).pin_memory() for x in ("q", "k", "v", "do")}
-    q, k, v, do = (host[x].to(dev) for x in ("q", "k", "v", "do"))
+    fo = forward_only(args, w)
+    ins = ("q", "k", "v") if fo else ("q", "k", "v", "do")
+    outs = ("o", "lse") if fo else ("o", "lse", "dq", "dk", "dv")
+    host = {x: workloads.to_torch(inp[x], w.dtype).pin_memory() for x in ins}
+    q, k, v = (host[x].to(dev) for x in ("q", "k", "v"))
+    do = None if fo else host["do"].to(dev)
     kw = dict(layout=w.layout, mask=w.mask, scale=w.scale, window=w.window)
     host_cu = {}
     if w.layout == "thd":
@@ -265,15 +283,18 @@ def gpu_arm(args, w, inp):
         kw.update(cu_seqlens_q=host_cu["cu_seqlens_q"].to(dev), cu_seqlens_kv=host_cu["cu_seqlens_kv"].to(dev),
                   max_seqlen_q=int(np.max(np.diff(inp["cu_seqlens_q"]))),
                   max_seqlen_kv=int(np.max(np.diff(inp["cu_seqlens_kv"]))))
-    o = torch.empty_like(q)
+    o = torch.empty(tuple(q.shape[:-1]) + (w.dv,), dtype=q.dtype, device=dev)
     rows_q = q.numel() // (w.heads_q * w.head_dim)
     lse = torch.empty((rows_q, w.heads_q), dtype=torch.float32, device=dev)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     batch = len(inp["cu_seqlens_q"]) - 1 if w.layout == "thd" else None
     prob = sdpa.make_problem(q, k, layout=w.layout, mask=w.mask, window=w.window, scale=w.scale, batch=batch,
-                             max_seqlen_q=kw.get("max_seqlen_q"), max_seqlen_kv=kw.get("max_seqlen_kv"))
+                             max_seqlen_q=kw.get("max_seqlen_q"), max_seqlen_kv=kw.get("max_seqlen_kv"),
+                             head_dim_v=w.dv)
     ws_f = torch.empty(max(256, sdpa.sdpa_fwd_workspace_size(prob)), dtype=torch.uint8, device=dev)
-    ws_b = torch.empty(max(256, sdpa.sdpa_bwd_workspace_size(prob)), dtype=torch.uint8, device=dev)
+    dq = dk = dv = ws_b = None
+    if not fo:
+        dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+        ws_b = torch.empty(max(256, sdpa.sdpa_bwd_workspace_size(prob)), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     det = bool(args.deterministic)
@@ -281,6 +302,8 @@ def gpu_arm(args, w, inp):
     def step():
         sdpa.sdpa_fwd(q, k, v, out=o, lse=lse, workspace=ws_f, **kw)
         n = sdpa.sdpa_last_launch_count()
+        if fo:
+            return n
         sdpa.sdpa_bwd(q, k, v, o, lse, do, dq=dq, dk=dk, dv=dv, workspace=ws_b, deterministic=det, **kw)
         return n + sdpa.sdpa_last_launch_count()
 
@@ -318,8 +341,8 @@ def gpu_arm(args, w, inp):
     # copy of step s+1 and the device->host copy of step s-1 run beside the
     # compute of step s (the link is full duplex). Every step still copies its
     # own inputs in and its own results out inside the timed region.
-    h_out = {x: torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for x, t in
-             (("o", o), ("lse", lse), ("dq", dq), ("dk", dk), ("dv", dv))}
+    dev_out = {"o": o, "lse": lse, "dq": dq, "dk": dk, "dv": dv}
+    h_out = {x: torch.empty(dev_out[x].shape, dtype=dev_out[x].dtype, pin_memory=True) for x in outs}
     h2d = sum(t.numel() * t.element_size() for t in host.values()) + sum(
         t.numel() * t.element_size() for t in host_cu.values())
     d2h = sum(t.numel() * t.element_size() for t in h_out.values())
@@ -327,7 +350,8 @@ def gpu_arm(args, w, inp):
     sets = []
     for b in range(2):
         dset = {x: torch.empty_like(t) for x, t in (("q", q), ("k", k), ("v", v), ("do", do), ("o", o), ("lse", lse),
-                                                     ("dq", dq), ("dk", dk), ("dv", dv), ("ws_f", ws_f), ("ws_b", ws_b))}
+                                                     ("dq", dq), ("dk", dk), ("dv", dv), ("ws_f", ws_f), ("ws_b", ws_b))
+                if t is not None}
         for x in host_cu:
             dset[x] = torch.empty_like(kw[x])
         sets.append(dset)
@@ -342,7 +366,7 @@ def gpu_arm(args, w, inp):
         with torch.cuda.stream(s_in):
             if i >= 2:
                 s_in.wait_event(ev_comp[b])  # step i-2 has finished reading this set's inputs
-            for x in ("q", "k", "v", "do"):
+            for x in ins:
                 d[x].copy_(host[x], non_blocking=True)
             for x in host_cu:
                 d[x].copy_(host_cu[x], non_blocking=True)
@@ -354,12 +378,13 @@ def gpu_arm(args, w, inp):
         for x in host_cu:
             kwb[x] = d[x]
         sdpa.sdpa_fwd(d["q"], d["k"], d["v"], out=d["o"], lse=d["lse"], workspace=d["ws_f"], stream=s_comp, **kwb)
-        sdpa.sdpa_bwd(d["q"], d["k"], d["v"], d["o"], d["lse"], d["do"], dq=d["dq"], dk=d["dk"], dv=d["dv"],
-                      workspace=d["ws_b"], stream=s_comp, deterministic=det, **kwb)
+        if not fo:
+            sdpa.sdpa_bwd(d["q"], d["k"], d["v"], d["o"], d["lse"], d["do"], dq=d["dq"], dk=d["dk"], dv=d["dv"],
+                          workspace=d["ws_b"], stream=s_comp, deterministic=det, **kwb)
         ev_comp[b].record(s_comp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev_comp[b])
-            for x in ("o", "lse", "dq", "dk", "dv"):
+            for x in outs:
                 h_out[x].copy_(d[x], non_blocking=True)
             ev_out[b].record(s_out)
 
@@ -386,20 +411,20 @@ def gpu_arm(args, w, inp):
     # the copies of a step, each timed alone (context for the overlap)
     ta, tb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ta.record()
-    for x in ("q", "k", "v", "do"):
+    for x in ins:
         sets[0][x].copy_(host[x], non_blocking=True)
     tb.record()
     torch.cuda.synchronize()
     h2d_ms = ta.elapsed_time(tb)
     ta.record()
-    for x in ("o", "lse", "dq", "dk", "dv"):
+    for x in outs:
         h_out[x].copy_(sets[0][x], non_blocking=True)
     tb.record()
     torch.cuda.synchronize()
     d2h_ms = ta.elapsed_time(tb)
 
     conv, exact = flops(w, inp)
-    step_flops = 3.5 * conv
+    step_flops = conv if fo else 3.5 * conv
     ms, e2e_ms = max_over_ranks([ms, e2e_ms], world, device=dev)
     value = job_tflops(world, step_flops, args.steps, ms)
     e2e_value = job_tflops(world, step_flops, 1, e2e_ms)
@@ -413,7 +438,7 @@ def gpu_arm(args, w, inp):
     for kind in ("fwd", "bwd", "preprocess", "dq_finalize", "guard", "bwd_dq"):
         tot, n = prof[kind]
         kern[kind] = {"ms_total": tot, "launches": n, "ms_avg": tot / n if n else None}
-    fwd_alg = exact            # 4*D flop per unmasked pair per head
+    fwd_alg = exact            # 2*D + 2*Dv (4*D) flop per unmasked pair per head
     bwd_alg = 2.5 * exact      # 10*D flop per unmasked pair per head
     # algorithmic flops per launch of each kernel: the deterministic backward
     # splits the 10*D into the dK/dV kernel (8*D: S, dP, dV, dK) and the dQ
@@ -431,10 +456,10 @@ def gpu_arm(args, w, inp):
     bwd_ms = (kern["bwd"]["ms_total"] + kern["bwd_dq"]["ms_total"]) / args.steps  # whole backward, per step
     detail = {
         "fwd_kernel_tflops_exact": fwd_alg / (kern["fwd"]["ms_avg"] * 1e-3) / 1e12,
-        "bwd_kernel_tflops_exact": bwd_alg / (bwd_ms * 1e-3) / 1e12,
+        "bwd_kernel_tflops_exact": bwd_alg / (bwd_ms * 1e-3) / 1e12 if not fo else None,
         "fwd_kernel_tflops_convention": conv / (kern["fwd"]["ms_avg"] * 1e-3) / 1e12,
-        "bwd_kernel_tflops_convention": 2.5 * conv / (bwd_ms * 1e-3) / 1e12,
-        "step_tflops_exact": world * 3.5 * exact * args.steps / (ms * 1e-3) / 1e12,
+        "bwd_kernel_tflops_convention": 2.5 * conv / (bwd_ms * 1e-3) / 1e12 if not fo else None,
+        "step_tflops_exact": world * (1.0 if fo else 3.5) * exact * args.steps / (ms * 1e-3) / 1e12,
         "pct_of_peak_step": 100.0 * value / world / peak,
         "kernels": kern,
         "preprocess_gbs": None,
@@ -450,21 +475,23 @@ def gpu_arm(args, w, inp):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        s = oracle_sample(w, inp, 12.0)
+        s = oracle_sample(w, inp, 12.0, fo)
         cpu = {"value": s["tflops"], "unit": "TFLOP/s", "cores": s["threads"], "kind": "oracle",
-               "sample": f"float64 oracle fwd+bwd of the first {s['ls']} query tokens of sequence 0 with "
-                         f"{s['nkv']} kv head(s) ({s['group']} q heads): {s['seconds']:.1f} s"}
+               "sample": f"float64 oracle {'fwd' if fo else 'fwd+bwd'} of the first {s['ls']} query tokens of "
+                         f"sequence 0 with {s['nkv']} kv head(s) ({s['group']} q heads): {s['seconds']:.1f} s"}
     lq, _ = seq_lengths(w, inp)
     line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
             "config": {"workload": w.name, "layout": w.layout, "mask": w.mask, "batch": len(lq),
                        "seq_lengths": [int(x) for x in lq], "heads_q": w.heads_q, "heads_kv": w.heads_kv,
-                       "head_dim": w.head_dim, "window": list(w.window),
-                       "flop_convention": "fwd 4*Hq*D*Sq*Sk per sequence, halved for causal; bwd 2.5x fwd",
+                       "head_dim": w.head_dim, "head_dim_v": w.dv, "window": list(w.window),
+                       "pass": "forward only" if fo else "forward + backward",
+                       "flop_convention": "fwd (2*D + 2*Dv)*Hq*Sq*Sk per sequence (4*Hq*D*Sq*Sk for equal dims), "
+                                          "halved for causal; bwd 2.5x fwd",
                        "l2": "flushed between timed steps (256 MiB write, outside the events)",
                        "parallelism": f"replicas x{world} (no collective)",
-                       "backward": "deterministic" if det else "fp32 reductions for dQ (head_dim 128)"},
+                       "backward": None if fo else "deterministic" if det else "fp32 reductions for dQ (head_dim 128)"},
             "clocks": clk, "gpu_launches": launches,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms, "h2d_ms_alone": h2d_ms, "d2h_ms_alone": d2h_ms,
@@ -567,8 +594,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="varlen_thd_gqa", choices=[w.name for w in workloads.ALL])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="step", choices=["step", "merge"],
-                    help="step: the fwd+bwd hot path (the headline); merge: the LSE merge of key-split results")
+    ap.add_argument("--op", default="step", choices=["step", "fwd", "merge"],
+                    help="step: the fwd+bwd hot path (the headline; the forward alone for forward-only "
+                         "workloads); fwd: the forward alone; merge: the LSE merge of key-split results")
     ap.add_argument("--merge-parts", type=int, default=4)
     ap.add_argument("--deterministic", action="store_true",
                     help="bitwise-reproducible backward (head_dim 128: separate dQ pass, no fp32 reductions)")

@@ -27,8 +27,11 @@
  * [rows_q][Hq] indexed by Q's token row. dq/dk/dv have q/k/v's layout.
  *
  * Supported: dtype bf16 or fp16 (Q, K, V, O, dO, dQ, dK, dV share it);
- * symmetric head_dim 128, 256 or 512; Hq a multiple of Hkv (q head h reads
- * kv head h / (Hq/Hkv)); every device pointer 16-byte aligned.
+ * symmetric head_dim 128, 256 or 512, and for the forward alone the
+ * asymmetric pair head_dim 192 (Q, K) with head_dim_v 128 (V, O) (PR #3527
+ * "Scope": the forward prefill engine lists (192, 128) among its native
+ * shapes, the backward requires d_qk == d_v); Hq a multiple of Hkv (q head
+ * h reads kv head h / (Hq/Hkv)); every device pointer 16-byte aligned.
  *
  * Ownership: the caller owns every buffer, the workspace and the stream.
  * Pointers marked "device" must be device memory (cudaMalloc or torch);
@@ -102,6 +105,9 @@ typedef struct {
                           not bitwise reproducible). 1: every gradient bitwise reproducible run to run
                           (head_dim 128 forms dQ in a separate pass that recomputes S and dP per query
                           tile; head_dim 256/512 are always so). Must be 0 or 1. */
+  int head_dim_v;      /* Dv, the width of V and O rows (and of dV, dO): 0 or head_dim = symmetric.
+                          The one asymmetric pair is head_dim 192 with head_dim_v 128, forward
+                          only; sdpa_bwd and sdpa_bwd_noalloc decline it (SDPA_ERR_UNSUPPORTED). */
 } sdpa_problem;
 
 /* Bytes of device workspace sdpa_fwd / sdpa_bwd need for this problem
@@ -113,14 +119,15 @@ SDPA_API size_t sdpa_fwd_workspace_size(const sdpa_problem* p);
 SDPA_API size_t sdpa_bwd_workspace_size(const sdpa_problem* p);
 
 /* Host-side validation only (no CUDA call): SDPA_OK or the reason a call
- * with this problem would be declined. Declined: head_dim not in
- * {128,256,512}; Hq % Hkv != 0; a causal mask with window_right > 0; a
+ * with this problem would be declined (by the forward; the backward declines
+ * head_dim_v != head_dim as well). Declined: (head_dim, head_dim_v) not one
+ * of (128|256|512, 0 or the same) or (192, 128); Hq % Hkv != 0; a causal mask with window_right > 0; a
  * bounded window on a non-causal mask when seqlen_q != seqlen_kv (PR #3527
  * "Scope": the alignment of such a window is ambiguous, so it is declined
  * rather than guessed). */
 SDPA_API int sdpa_check_problem(const sdpa_problem* p);
 
-/* Forward. q [.., Hq, D], k/v [.., Hkv, D] (device, read); o [.., Hq, D] and
+/* Forward. q [.., Hq, D], k [.., Hkv, D], v [.., Hkv, Dv] (device, read); o [.., Hq, Dv] and
  * lse float32 [rows_q][Hq] (device, written). cu_seqlens_q/kv: device int32
  * [B+1] for THD (checked on the device on every call: cu[0] == 0,
  * non-decreasing, cu[B] == total, every length <= seqlen_q/seqlen_kv, and a

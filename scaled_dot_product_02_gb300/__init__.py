@@ -46,7 +46,8 @@ class Problem(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int) for n in ("layout", "dtype", "mask_type", "batch", "seqlen_q", "seqlen_kv",
                                             "total_q", "total_kv", "num_heads_q", "num_heads_kv", "head_dim",
                                             "window_left", "window_right")] + [("softmax_scale", ctypes.c_float),
-                                                                               ("deterministic", ctypes.c_int)]
+                                                                               ("deterministic", ctypes.c_int),
+                                                                               ("head_dim_v", ctypes.c_int)]
 
 
 _lock = threading.Lock()
@@ -91,8 +92,9 @@ sdpa_error_string = error_string
 
 
 def make_problem(q, k, *, layout="bshd", mask="none", window=(-1, -1), scale=None, dtype=None, batch=None,
-                 max_seqlen_q=None, max_seqlen_kv=None, deterministic=False) -> Problem:
-    """sdpa_problem from tensor shapes (no device access)."""
+                 max_seqlen_q=None, max_seqlen_kv=None, deterministic=False, head_dim_v=0) -> Problem:
+    """sdpa_problem from tensor shapes (no device access). head_dim_v: the
+    width of V and O rows (0 = Q/K's head_dim)."""
     import torch
 
     if dtype is None:
@@ -116,6 +118,7 @@ def make_problem(q, k, *, layout="bshd", mask="none", window=(-1, -1), scale=Non
     p.window_left, p.window_right = int(window[0]), int(window[1])
     p.softmax_scale = float(scale if scale is not None else d ** -0.5)
     p.deterministic = int(bool(deterministic))
+    p.head_dim_v = int(head_dim_v)
     return p
 
 
@@ -154,15 +157,16 @@ def sdpa_bwd_workspace_size(p: Problem) -> int:
 def sdpa_fwd(q, k, v, *, layout="bshd", mask="none", window=(-1, -1), scale=None, cu_seqlens_q=None,
              cu_seqlens_kv=None, max_seqlen_q=None, max_seqlen_kv=None, out=None, lse=None, workspace=None,
              stream=None):
-    """Forward. Returns (o, lse); lse is float32 [rows_q, Hq] token-major."""
+    """Forward. Returns (o, lse); o has Q's shape with V's last dimension,
+    lse is float32 [rows_q, Hq] token-major."""
     import torch
 
     batch = None if cu_seqlens_q is None else cu_seqlens_q.numel() - 1
     p = make_problem(q, k, layout=layout, mask=mask, window=window, scale=scale, batch=batch,
-                     max_seqlen_q=max_seqlen_q, max_seqlen_kv=max_seqlen_kv)
+                     max_seqlen_q=max_seqlen_q, max_seqlen_kv=max_seqlen_kv, head_dim_v=v.shape[-1])
     rows_q = q.numel() // (q.shape[-1] * q.shape[-2])
     if out is None:
-        out = torch.empty_like(q)
+        out = torch.empty(tuple(q.shape[:-1]) + (v.shape[-1],), dtype=q.dtype, device=q.device)
     if lse is None:
         lse = torch.empty((rows_q, q.shape[-2]), dtype=torch.float32, device=q.device)
     need = sdpa_fwd_workspace_size(p)
@@ -186,7 +190,8 @@ def sdpa_bwd(q, k, v, o, lse, dout, *, layout="bshd", mask="none", window=(-1, -
 
     batch = None if cu_seqlens_q is None else cu_seqlens_q.numel() - 1
     p = make_problem(q, k, layout=layout, mask=mask, window=window, scale=scale, batch=batch,
-                     max_seqlen_q=max_seqlen_q, max_seqlen_kv=max_seqlen_kv, deterministic=deterministic)
+                     max_seqlen_q=max_seqlen_q, max_seqlen_kv=max_seqlen_kv, deterministic=deterministic,
+                     head_dim_v=v.shape[-1])
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
@@ -215,7 +220,8 @@ def sdpa_bwd_noalloc(q, k, v, o, lse, dout, *, layout="bshd", mask="none", windo
 
     batch = None if cu_seqlens_q is None else cu_seqlens_q.numel() - 1
     p = make_problem(q, k, layout=layout, mask=mask, window=window, scale=scale, batch=batch,
-                     max_seqlen_q=max_seqlen_q, max_seqlen_kv=max_seqlen_kv, deterministic=deterministic)
+                     max_seqlen_q=max_seqlen_q, max_seqlen_kv=max_seqlen_kv, deterministic=deterministic,
+                     head_dim_v=v.shape[-1])
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv

@@ -117,6 +117,16 @@ void view(const sdpa_problem* p, int& rows_q, int& rows_kv, int& nh_q, int& nh_k
 
 bool causal(const sdpa_problem* p) { return p->mask_type != SDPA_MASK_NONE; }
 
+// Width of V and O rows (head_dim_v 0 means the symmetric head_dim).
+int dv_of(const sdpa_problem* p) { return p->head_dim_v ? p->head_dim_v : p->head_dim; }
+
+// (head_dim, head_dim_v) pairs with a forward kernel: the symmetric 128, 256,
+// 512, and (192, 128) (the asymmetric pair the pages' forward engine lists).
+bool head_dims_supported(int d, int dv) {
+  if (d == dv) return d == 128 || d == 256 || d == 512;
+  return d == 192 && dv == 128;
+}
+
 int check(const sdpa_problem* p) {
   if (!p) return SDPA_ERR_INVALID_ARG;
   if (p->layout < SDPA_BSHD || p->layout > SDPA_THD) return SDPA_ERR_INVALID_ARG;
@@ -125,7 +135,8 @@ int check(const sdpa_problem* p) {
   if (p->batch < 0 || p->seqlen_q < 0 || p->seqlen_kv < 0) return SDPA_ERR_INVALID_ARG;
   if (p->num_heads_q <= 0 || p->num_heads_kv <= 0) return SDPA_ERR_INVALID_ARG;
   if (p->num_heads_q % p->num_heads_kv) return SDPA_ERR_INVALID_ARG;
-  if (p->head_dim != 128 && p->head_dim != 256 && p->head_dim != 512) return SDPA_ERR_UNSUPPORTED;
+  if (p->head_dim_v < 0) return SDPA_ERR_INVALID_ARG;
+  if (!head_dims_supported(p->head_dim, dv_of(p))) return SDPA_ERR_UNSUPPORTED;
   if (p->window_left < -1 || p->window_right < -1) return SDPA_ERR_INVALID_ARG;
   if (causal(p) && p->window_right > 0) return SDPA_ERR_INVALID_ARG;
   if (!causal(p) && (p->window_left >= 0 || p->window_right >= 0) && p->seqlen_q != p->seqlen_kv)
@@ -140,7 +151,7 @@ int check(const sdpa_problem* p) {
   int rq, rk, hq, hk;
   view(p, rq, rk, hq, hk);
   const long long q_elems = (long long)rq * hq * p->head_dim;
-  const long long k_elems = (long long)rk * hk * p->head_dim;
+  const long long k_elems = (long long)rk * hk * std::max(p->head_dim, dv_of(p));
   if (q_elems >= (1LL << 40) || k_elems >= (1LL << 40)) return SDPA_ERR_UNSUPPORTED;
   if ((long long)p->batch * p->seqlen_q >= (1LL << 31) || (long long)p->batch * p->seqlen_kv >= (1LL << 31))
     return SDPA_ERR_UNSUPPORTED;
@@ -157,6 +168,7 @@ Geom make_geom(const sdpa_problem* p, const int32_t* cu_q, const int32_t* cu_kv)
   g.hq = p->num_heads_q;
   g.hkv = p->num_heads_kv;
   g.d = p->head_dim;
+  g.dv = dv_of(p);
   g.wl = p->window_left;
   g.wr = causal(p) ? 0 : p->window_right;
   g.scale = p->softmax_scale;
@@ -255,7 +267,7 @@ size_t sdpa_fwd_workspace_size(const sdpa_problem* p) {
 }
 
 size_t sdpa_bwd_workspace_size(const sdpa_problem* p) {
-  if (check(p) != SDPA_OK) return 0;
+  if (check(p) != SDPA_OK || dv_of(p) != p->head_dim) return 0;
   return bwd_ws(p).total;
 }
 
@@ -277,8 +289,9 @@ int sdpa_fwd(const sdpa_problem* p, const void* q, const void* k, const void* v,
   if (ws_bytes < need || (need && !workspace)) return SDPA_ERR_WORKSPACE_TOO_SMALL;
   if (need && !aligned16(workspace)) return SDPA_ERR_ALIGNMENT;
   const size_t qb = (size_t)rq * hq * p->head_dim * 2, kb = (size_t)rk * hk * p->head_dim * 2;
-  const Extent eo = extent(o, qb), el = extent(lse, (size_t)rq * hq * 4);
-  for (Extent in : {extent(q, qb), extent(k, kb), extent(v, kb)})
+  const size_t vb = (size_t)rk * hk * dv_of(p) * 2, ob = (size_t)rq * hq * dv_of(p) * 2;
+  const Extent eo = extent(o, ob), el = extent(lse, (size_t)rq * hq * 4);
+  for (Extent in : {extent(q, qb), extent(k, kb), extent(v, vb)})
     if (overlaps(eo, in) || overlaps(el, in)) return SDPA_ERR_OVERLAP;
   if (overlaps(eo, el)) return SDPA_ERR_OVERLAP;
   if (need && (overlaps(extent(workspace, need), eo) || overlaps(extent(workspace, need), el)))
@@ -299,10 +312,10 @@ int sdpa_fwd(const sdpa_problem* p, const void* q, const void* k, const void* v,
   L.p.dv_splits = p->head_dim == 512 ? 2 : 1;
   L.p.tile_counter = p->head_dim == 128 ? reinterpret_cast<int*>(static_cast<uint8_t*>(workspace) + 128) : nullptr;
   L.stream = s;
-  const int dv = p->head_dim == 128 ? 128 : 256;
+  const int dv_cta = dv_of(p) == 512 ? 256 : dv_of(p);  // value columns one CTA accumulates
   if ((rc = encode(&L.tmQ, q, p->head_dim, hq, rq, 128, bf16))) return rc;
   if ((rc = encode(&L.tmK, k, p->head_dim, hk, rk, 128, bf16))) return rc;
-  if ((rc = encode(&L.tmV, v, p->head_dim, hk, rk, 32768 / (dv * 2), bf16))) return rc;
+  if ((rc = encode(&L.tmV, v, dv_of(p), hk, rk, 32768 / (dv_cta * 2), bf16))) return rc;
   int launches = 0;
   if (thd) {
     rc = timed(SDPA_KERNEL_GUARD, s,
@@ -310,7 +323,7 @@ int sdpa_fwd(const sdpa_problem* p, const void* q, const void* k, const void* v,
     if (rc) return rc;
     ++launches;
   }
-  if ((rc = timed(SDPA_KERNEL_FWD, s, [&] { return launch_fwd(L, p->head_dim, bf16); }))) return rc;
+  if ((rc = timed(SDPA_KERNEL_FWD, s, [&] { return launch_fwd(L, p->head_dim, dv_of(p), bf16); }))) return rc;
   ++launches;
   t_last_launches = launches;
   return SDPA_OK;
@@ -322,6 +335,7 @@ int sdpa_bwd(const sdpa_problem* p, const void* q, const void* k, const void* v,
   t_last_launches = 0;
   int rc = check(p);
   if (rc) return rc;
+  if (dv_of(p) != p->head_dim) return SDPA_ERR_UNSUPPORTED;  // the backward is symmetric only
   int rq, rk, hq, hk;
   view(p, rq, rk, hq, hk);
   const bool thd = p->layout == SDPA_THD;

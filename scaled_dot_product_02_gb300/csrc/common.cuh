@@ -18,6 +18,7 @@ namespace sdpa {
 struct Geom {
   int layout, mask, batch, sq, sk;  // THD: sq/sk are the largest lengths
   int hq, hkv, d;
+  int dv;  // width of V and O rows (== d except for the asymmetric forward)
   int wl, wr;  // window; wr == 0 for causal masks, < 0 = unbounded
   float scale, scale_log2;
   int rows_q, rows_kv;  // rows of the generic view

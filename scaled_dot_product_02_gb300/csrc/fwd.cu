@@ -3,11 +3,15 @@
 // One CTA owns one 128-row query tile of one (batch, q head) and, for
 // head_dim 512, one half of the value columns (the "D-split": both halves
 // recompute S = Q K^T over the full head dim, each accumulates half of O, so
-// O never needs more than 256 TMEM columns).
+// O never needs more than 256 TMEM columns). The same kernel serves
+// head_dim 256, 512 and the asymmetric pair Q/K 192, V/O 128.
 //
 // Roles (256 threads):
 //   warp 0      TMA producer: Q once, then K/V tiles through a ring of 32 KB
-//               stages, in exactly the order the MMA warp consumes them.
+//               stages, in exactly the order the MMA warp consumes them. A
+//               K tile takes DQK/128 stages of 128 keys x 128 columns, and a
+//               final half-filled one (64 columns) when DQK is an odd
+//               multiple of 64.
 //   warp 1      TMEM allocator and MMA issuer (one elected thread):
 //                 S_j = Q K_j^T  (SS MMA, fp32 in TMEM, double-buffered)
 //                 O  += P_j V_j  (TS MMA, P read from TMEM)
@@ -36,8 +40,11 @@ struct FwdCfg {
   static constexpr int BM = 128, BN = 128;
   static constexpr int STAGE_BYTES = 32768;
   static constexpr int Q_BYTES = DQK * 256;  // 128 rows x DQK x 2 bytes
-  static constexpr int NSTAGES = DQK == 128 ? 5 : (DQK == 256 ? 4 : 3);
-  static constexpr int KST = DQK / 128;                    // K stages per tile (128 keys x 128 d each)
+  static_assert(DQK % 64 == 0 && DV % 64 == 0, "head dims are whole 64-column swizzle atoms");
+  static constexpr int NSTAGES = DQK <= 192 ? 5 : (DQK == 256 ? 4 : 3);
+  static constexpr int KST = (DQK + 127) / 128;            // K stages per tile (128 keys x up to 128 d each)
+  // 64-column atoms of K stage kb (two, or one for the last stage of DQK = 192)
+  static __device__ __forceinline__ constexpr int k_atoms(int kb) { return DQK / 64 - 2 * kb >= 2 ? 2 : 1; }
   static constexpr int VROWS = STAGE_BYTES / (DV * 2);     // keys per V stage
   static constexpr int VST = BN / VROWS;                   // V stages per tile
   static constexpr int V_ATOM_BYTES = VROWS * 128;         // one 64-column swizzle atom of a V stage
@@ -126,28 +133,29 @@ __global__ void __launch_bounds__(256, 1)
       for (int a = 0; a < DQK / 64; ++a) tma_load_3d(&tmQ, bar_q, sQ + a * 16384, a * 64, qhead, si.qrow0 + q0);
       int c = 0;
       bool ok = true;
-      auto next_slot = [&](int& slot) -> bool {
+      auto next_slot = [&](int& slot, uint32_t bytes) -> bool {
         slot = c % C::NSTAGES;
         const uint32_t ph = (c / C::NSTAGES) & 1;
         if (!mbar_wait(&empty[slot], ph ^ 1, abort_flag)) return false;
-        mbar_arrive_expect_tx(&full[slot], C::STAGE_BYTES);
+        mbar_arrive_expect_tx(&full[slot], bytes);
         return true;
       };
       auto load_k = [&](int j) -> bool {
         const int key0 = si.krow0 + (t_lo + j) * C::BN;
         for (int kb = 0; kb < C::KST; ++kb, ++c) {
           int slot;
-          if (!next_slot(slot)) return false;
+          const int atoms = C::k_atoms(kb);
+          if (!next_slot(slot, atoms * 16384)) return false;
           uint8_t* dst = sStage + slot * C::STAGE_BYTES;
           tma_load_3d(&tmK, &full[slot], dst, kb * 128, khead, key0);
-          tma_load_3d(&tmK, &full[slot], dst + 16384, kb * 128 + 64, khead, key0);
+          if (atoms == 2) tma_load_3d(&tmK, &full[slot], dst + 16384, kb * 128 + 64, khead, key0);
         }
         return true;
       };
       auto load_v = [&](int j) -> bool {
         for (int vs = 0; vs < C::VST; ++vs, ++c) {
           int slot;
-          if (!next_slot(slot)) return false;
+          if (!next_slot(slot, C::STAGE_BYTES)) return false;
           uint8_t* dst = sStage + slot * C::STAGE_BYTES;
           const int key0 = si.krow0 + (t_lo + j) * C::BN + vs * C::VROWS;
           for (int a = 0; a < DV / 64; ++a)
@@ -187,8 +195,10 @@ __global__ void __launch_bounds__(256, 1)
           tc_fence_after();
           const uint32_t k_base = smem_u32(sStage + slot * C::STAGE_BYTES);
           const uint32_t qa = q_base + kb * 2 * 16384;
+          const int n_ks = 4 * C::k_atoms(kb);  // 16-column K steps held by this stage
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
+            if (ks >= n_ks) break;
             const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
             mma_ss(d, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(k_base + off, 16, 1024), IDESC_S,
                    (kb | ks) != 0);
@@ -338,7 +348,7 @@ __global__ void __launch_bounds__(256, 1)
       const bool valid = i < si.lq;
       const float inv = l > 0.f ? 1.f / l : 0.f;
       using T = typename E::T;
-      T* orow = reinterpret_cast<T*>(p.o) + ((int64_t)(si.qrow0 + i) * g.nh_q + qhead) * g.d + split * DV;
+      T* orow = reinterpret_cast<T*>(p.o) + ((int64_t)(si.qrow0 + i) * g.nh_q + qhead) * g.dv + split * DV;
 #pragma unroll 1
       for (int c = 0; c < DV / 32; ++c) {
         uint32_t packed[16];
@@ -930,7 +940,10 @@ static int launch_fwd_t(const FwdLaunch& L) {
   return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }
 
-int launch_fwd(const FwdLaunch& L, int head_dim, bool bf16) {
+int launch_fwd(const FwdLaunch& L, int head_dim, int head_dim_v, bool bf16) {
+  if (head_dim == 192 && head_dim_v == 128)
+    return bf16 ? launch_fwd_t<192, 128, true>(L) : launch_fwd_t<192, 128, false>(L);
+  if (head_dim != head_dim_v) return SDPA_ERR_UNSUPPORTED;
   if (head_dim == 128) return bf16 ? launch_fwd128<true>(L) : launch_fwd128<false>(L);
   if (head_dim == 256) return bf16 ? launch_fwd_t<256, 256, true>(L) : launch_fwd_t<256, 256, false>(L);
   if (head_dim == 512) return bf16 ? launch_fwd_t<512, 256, true>(L) : launch_fwd_t<512, 256, false>(L);

@@ -26,7 +26,7 @@ struct FwdLaunch {
   cudaStream_t stream;
 };
 
-int launch_fwd(const FwdLaunch& L, int head_dim, bool bf16);
+int launch_fwd(const FwdLaunch& L, int head_dim, int head_dim_v, bool bf16);
 
 struct BwdParams {
   Geom g;

@@ -52,6 +52,7 @@ extern "C" SDPA_API int sdpa_bwd_noalloc(const sdpa_problem* p, const void* q, c
                                          void* stream) {
   const int rc = sdpa_check_problem(p);
   if (rc != SDPA_OK) return rc;
+  if (p->head_dim_v && p->head_dim_v != p->head_dim) return SDPA_ERR_UNSUPPORTED;  // forward-only pair
   if (sdpa_bwd_workspace_size(p) > (size_t)SDPA_BWD_NOALLOC_MAX_BYTES) return SDPA_ERR_WORKSPACE_TOO_SMALL;
   void* scratch = nullptr;
   const int arc = scratch_address(&scratch);

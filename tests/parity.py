@@ -180,7 +180,7 @@ def check_sampled(w, inp, out, n_rows=40, n_keys=12, seed=0, backward=True):
     o_m, l_m = oracle.fwd_rows(inp["q"], inp["k"], inp["v"], bhi, **kw)
     o_r, l_r = oracle.fwd_rows(rin["q"], rin["k"], rin["v"], bhi, **kw)
     nh = w.heads_q
-    o_g = np.stack([out["o"].reshape(-1, nh, w.head_dim)[t, h] for t, (_, h, _) in zip(tr, bhi)])
+    o_g = np.stack([out["o"].reshape(-1, nh, w.dv)[t, h] for t, (_, h, _) in zip(tr, bhi)])
     l_g = np.array([out["lse"][t, h] for t, (_, h, _) in zip(tr, bhi)])
     res = [judge("O", o_g, o_m, o_r, w.dtype, O_CAP[w.dtype]),
            judge("LSE", l_g, l_m, l_r, w.dtype, LSE_CAP, round_out=False)]

@@ -75,6 +75,43 @@ def test_check_problem_accepts_and_declines(pkg):
     assert ok(layout=7) == 1
     assert ok(deterministic=1) == 0
     assert ok(deterministic=2) == 1
+    # head_dim_v: 0 or head_dim is symmetric; (192, 128) is the one asymmetric pair (forward only)
+    assert ok(head_dim_v=128) == 0
+    assert ok(head_dim=192, head_dim_v=128) == 0
+    assert ok(head_dim=192, head_dim_v=128, layout=2, total_q=1000, total_kv=1000) == 0
+    assert ok(head_dim=192, head_dim_v=192) == 2
+    assert ok(head_dim=128, head_dim_v=192) == 2
+    assert ok(head_dim=256, head_dim_v=128) == 2
+    assert ok(head_dim_v=-1) == 1
+
+
+def test_asymmetric_head_dims_are_forward_only(pkg):
+    """The backward declines d_qk != d_v before any CUDA call; the forward's
+    workspace is the THD guard only (no persistent tile counter)."""
+    import ctypes
+
+    L = pkg.lib()
+    p = problem(pkg, head_dim=192, head_dim_v=128)
+    assert pkg.sdpa_fwd_workspace_size(p) == 0
+    assert pkg.sdpa_fwd_workspace_size(problem(pkg, head_dim=192, head_dim_v=128, layout=2, total_q=100,
+                                               total_kv=100)) == 256
+    assert pkg.sdpa_bwd_workspace_size(p) == 0
+    ptr = ctypes.c_void_p
+    base = 1 << 40
+    args = [ptr(base + i * (1 << 24)) for i in range(9)]
+    assert L.sdpa_bwd(ctypes.byref(p), *args, None, None, ptr(base + (1 << 30)), 1 << 20, None) == 2
+    assert L.sdpa_bwd_noalloc(ctypes.byref(p), *args, None, None, None) == 2
+    # the forward sizes V and O by head_dim_v: an O that would overlap V at D = 192 but not at 128
+    p1 = problem(pkg, batch=1, seqlen_q=256, seqlen_kv=256, num_heads_q=2, num_heads_kv=2, head_dim=192,
+                 head_dim_v=128)
+    nv = 256 * 2 * 128 * 2     # bytes of V [1, 256, 2, 128]
+    nq = 256 * 2 * 192 * 2     # bytes of Q or K [1, 256, 2, 192]
+    q, k, v = base, base + nq, base + 2 * nq
+    o, lse = v + nv, v + nv + nv
+    f = lambda o_, lse_: L.sdpa_fwd(ctypes.byref(p1), ptr(q), ptr(k), ptr(v), ptr(o_), ptr(lse_), None, None,
+                                    None, 0, None)
+    assert f(o - 256, lse) == 4          # o starts inside v
+    assert f(o, o + nv - 256) == 4       # lse inside o (o is nv bytes long)
 
 
 def test_workspace_sizes(pkg):

@@ -11,7 +11,10 @@ same dtype-rounded copies (rounded through float32, round-to-nearest-even).
 
 Workload shapes follow the pages' workloads: D128 BF16 causal compact THD with
 Hq32/Hkv8 (TransformerEngine PR #3705), b2 hq8 hkv4 d512 causal (PR #3527,
-"Performance"), and sliding-window D256 layers (PR #3527, "Problem").
+"Performance"), and sliding-window D256 layers (PR #3527, "Problem"). The
+asymmetric forward (Q/K 192, V/O 128: PR #3527, "Scope", the forward engine's
+native (192, 128) shape) reuses the compact THD workload's lengths and heads,
+since the pages give no workload of its own.
 """
 from __future__ import annotations
 
@@ -36,6 +39,11 @@ class Workload:
     window: tuple = (-1, -1)
     std: float = 1.0
     len_range: tuple | None = None  # THD: inclusive (lo, hi) of the uniform lengths
+    head_dim_v: int = 0             # width of V, O and dO rows; 0 = head_dim
+
+    @property
+    def dv(self) -> int:
+        return self.head_dim_v or self.head_dim
 
     @property
     def scale(self) -> float:
@@ -51,10 +59,14 @@ SLIDING = Workload("sliding_window_d256", "bshd", "causal", 2, 8192, 8192, 16, 8
 D512_BR = Workload("d512_rect_bottom_right", "bshd", "causal_br", 2, 2048, 8192, 16, 4, 512, "bf16")
 D512_NC = Workload("d512_rect_noncausal", "bshd", "none", 2, 2048, 8192, 16, 4, 512, "bf16")
 LONG_FP16 = Workload("long_context_fp16_sbhd", "sbhd", "causal", 1, 32768, 32768, 16, 16, 128, "fp16", std=0.5)
+# forward only (the backward requires d_qk == d_v)
+ASYM = Workload("varlen_thd_gqa_d192_v128", "thd", "causal", 8, 4096, 4096, 32, 8, 192, "bf16", len_range=(512, 4096),
+                head_dim_v=128)
 
-ALL = [TINY, VARLEN_THD, SLIDING, D512_BR, D512_NC, LONG_FP16]
+ALL = [TINY, VARLEN_THD, SLIDING, D512_BR, D512_NC, LONG_FP16, ASYM]
+FORWARD_ONLY = {ASYM.name}
 SEEDS = {"tiny": 1000, "varlen_thd_gqa": 1001, "sliding_window_d256": 1002, "d512_rect_bottom_right": 1003,
-         "d512_rect_noncausal": 1003, "long_context_fp16_sbhd": 1004}
+         "d512_rect_noncausal": 1003, "long_context_fp16_sbhd": 1004, "varlen_thd_gqa_d192_v128": 1001}
 
 
 def round_to(x: np.ndarray, dtype: str) -> np.ndarray:
@@ -73,12 +85,15 @@ def to_torch(x: np.ndarray, dtype: str):
     return torch.from_numpy(np.asarray(x, dtype=np.float32)).to(td)
 
 
-def shapes(w: Workload, lengths_q=None, lengths_kv=None):
+def shapes(w: Workload, lengths_q=None, lengths_kv=None, d_q=None, d_kv=None):
+    """(q-side shape, kv-side shape); the last dimensions default to head_dim."""
+    d_q = w.head_dim if d_q is None else d_q
+    d_kv = w.head_dim if d_kv is None else d_kv
     if w.layout == "bshd":
-        return (w.batch, w.seqlen_q, w.heads_q, w.head_dim), (w.batch, w.seqlen_kv, w.heads_kv, w.head_dim)
+        return (w.batch, w.seqlen_q, w.heads_q, d_q), (w.batch, w.seqlen_kv, w.heads_kv, d_kv)
     if w.layout == "sbhd":
-        return (w.seqlen_q, w.batch, w.heads_q, w.head_dim), (w.seqlen_kv, w.batch, w.heads_kv, w.head_dim)
-    return (int(np.sum(lengths_q)), w.heads_q, w.head_dim), (int(np.sum(lengths_kv)), w.heads_kv, w.head_dim)
+        return (w.seqlen_q, w.batch, w.heads_q, d_q), (w.seqlen_kv, w.batch, w.heads_kv, d_kv)
+    return (int(np.sum(lengths_q)), w.heads_q, d_q), (int(np.sum(lengths_kv)), w.heads_kv, d_kv)
 
 
 def make_inputs(w: Workload, seed: int | None = None, lengths=None):
@@ -104,10 +119,11 @@ def make_inputs(w: Workload, seed: int | None = None, lengths=None):
         out["cu_seqlens_q"] = np.concatenate([[0], np.cumsum(lq)]).astype(np.int32)
         out["cu_seqlens_kv"] = np.concatenate([[0], np.cumsum(lk)]).astype(np.int32)
     sq, sk = shapes(w, lq, lk)
+    so, sv = shapes(w, lq, lk, w.dv, w.dv)  # O/dO and V rows are head_dim_v wide
     out["q"] = rng.standard_normal(sq) * w.std
     out["k"] = rng.standard_normal(sk) * w.std
-    out["v"] = rng.standard_normal(sk) * w.std
-    out["do"] = rng.standard_normal(sq) * w.std
+    out["v"] = rng.standard_normal(sv) * w.std
+    out["do"] = rng.standard_normal(so) * w.std
     return out
 
 
