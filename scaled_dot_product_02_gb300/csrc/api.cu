@@ -11,6 +11,8 @@
 #include <algorithm>
 #include <cstring>
 #include <mutex>
+#include <set>
+#include <utility>
 #include <vector>
 
 #include "../../include/sdpa.h"
@@ -251,6 +253,23 @@ BwdWs bwd_ws(const sdpa_problem* p) {
 }
 
 }  // namespace
+
+int set_kernel_smem(const void* kernel, int bytes, int carveout) {
+  static std::mutex mu;
+  static std::set<std::pair<const void*, int>> done;  // (kernel, device) already configured
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return SDPA_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done.count({kernel, dev})) return SDPA_OK;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) != cudaSuccess)
+    return SDPA_ERR_CUDA;
+  if (carveout >= 0 && cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout, carveout) !=
+                           cudaSuccess)
+    return SDPA_ERR_CUDA;
+  done.insert({kernel, dev});
+  return SDPA_OK;
+}
+
 }  // namespace sdpa
 
 using namespace sdpa;

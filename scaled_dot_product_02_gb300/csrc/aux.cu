@@ -118,14 +118,12 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const PrepParams p) {
   for (long long it = tid; it < n4; it += nthreads) acc4[it] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
+// SMs of the current device (queried per call: a process may drive several GPUs).
 static int sm_count() {
-  static int n = 0;
-  if (!n) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (n <= 0) n = 148;
-  }
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      n <= 0)
+    n = 148;
   return n;
 }
 

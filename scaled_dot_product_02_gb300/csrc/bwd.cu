@@ -470,12 +470,7 @@ __global__ void __launch_bounds__(512, 1)
 template <bool BF16, bool DQ>
 static int launch_t(const BwdLaunch& L) {
   auto kern = bwd_kernel<BF16, DQ>;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) != cudaSuccess)
-      return SDPA_ERR_CUDA;
-    attr = true;
-  }
+  if (const int rc = set_kernel_smem(reinterpret_cast<const void*>(kern), SMEM_BYTES, -1)) return rc;
   const long long grid = (long long)L.p.n_kv_tiles * L.p.g.hkv * L.p.g.batch;
   if (grid <= 0) return SDPA_OK;
   if (grid > 0x7fffffffLL) return SDPA_ERR_UNSUPPORTED;

@@ -827,8 +827,7 @@ __global__ void __launch_bounds__(256, 2)
 // ====================================================================== launch
 template <class K>
 static bool set_smem(K kern, int bytes) {
-  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess &&
-         cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) == cudaSuccess;
+  return set_kernel_smem(reinterpret_cast<const void*>(kern), bytes, 100) == SDPA_OK;
 }
 
 template <int DQK, bool BF16>
@@ -841,21 +840,13 @@ static int launch_big_t(const BigBwdLaunch& L, int* launches) {
   auto m0 = gemm_kernel<0, BF16>;
   auto m1 = gemm_kernel<1, BF16>;
   auto m2 = gemm_kernel<2, BF16>;
-  static bool attr = false;
-  if (!attr) {
-    if (!set_smem(m0, GB_SMEM) || !set_smem(m1, GB_SMEM) || !set_smem(m2, GB_SMEM)) return SDPA_ERR_CUDA;
-    attr = true;
-  }
+  if (!set_smem(m0, GB_SMEM) || !set_smem(m1, GB_SMEM) || !set_smem(m2, GB_SMEM)) return SDPA_ERR_CUDA;
   int n = 0;
   if (g1 > 0) {
     if constexpr (DQK == 256) {
       // one fused score kernel: P and dS from resident Q and dO
       auto sf = score_fused256_kernel<BF16>;
-      static bool attr_f = false;
-      if (!attr_f) {
-        if (!set_smem(sf, SF_SMEM)) return SDPA_ERR_CUDA;
-        attr_f = true;
-      }
+      if (!set_smem(sf, SF_SMEM)) return SDPA_ERR_CUDA;
       sf<<<(unsigned)g1, SF_THREADS, SF_SMEM, L.stream>>>(L.tmQ, L.tmDO, L.tmK, L.tmV, p);
       n += 1;
     } else {
@@ -863,11 +854,7 @@ static int launch_big_t(const BigBwdLaunch& L, int* launches) {
       using C = ScoreCfg<DQK>;
       auto s0 = score_kernel<DQK, 0, BF16>;
       auto s1 = score_kernel<DQK, 1, BF16>;
-      static bool attr_s = false;
-      if (!attr_s) {
-        if (!set_smem(s0, C::SMEM_BYTES) || !set_smem(s1, C::SMEM_BYTES)) return SDPA_ERR_CUDA;
-        attr_s = true;
-      }
+      if (!set_smem(s0, C::SMEM_BYTES) || !set_smem(s1, C::SMEM_BYTES)) return SDPA_ERR_CUDA;
       s0<<<(unsigned)g1, 256, C::SMEM_BYTES, L.stream>>>(L.tmDO, L.tmV, p);
       s1<<<(unsigned)g1, 256, C::SMEM_BYTES, L.stream>>>(L.tmQ, L.tmK, p);
       n += 2;

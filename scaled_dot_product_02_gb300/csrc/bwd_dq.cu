@@ -308,12 +308,7 @@ __global__ void __launch_bounds__(192, 1)
 template <bool BF16>
 static int launch_dq_t(const DqLaunch& L) {
   auto kern = dq128_kernel<BF16>;
-  static bool attr = false;
-  if (!attr) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, DqCfg::SMEM_BYTES) != cudaSuccess)
-      return SDPA_ERR_CUDA;
-    attr = true;
-  }
+  if (const int rc = set_kernel_smem(reinterpret_cast<const void*>(kern), DqCfg::SMEM_BYTES, -1)) return rc;
   const long long grid = (long long)L.p.n_q_tiles * L.p.g.hq * L.p.g.batch;
   if (grid <= 0) return SDPA_OK;
   if (grid > 0x7fffffffLL) return SDPA_ERR_UNSUPPORTED;

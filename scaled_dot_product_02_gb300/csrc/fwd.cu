@@ -902,13 +902,7 @@ __global__ void __launch_bounds__(Fwd2Cfg::THREADS, 1)
 template <bool BF16>
 static int launch_fwd128(const FwdLaunch& L) {
   auto kern = fwd128_kernel<BF16>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Fwd2Cfg::SMEM_BYTES) != cudaSuccess ||
-        cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
-      return SDPA_ERR_CUDA;
-    attr_set = true;
-  }
+  if (const int rc = set_kernel_smem(reinterpret_cast<const void*>(kern), Fwd2Cfg::SMEM_BYTES, 100)) return rc;
   const long long tiles = (long long)L.p.n_q_tiles * L.p.g.hq * L.p.g.batch;
   if (tiles <= 0) return SDPA_OK;
   if (tiles > 0x7fffffffLL - 4096) return SDPA_ERR_UNSUPPORTED;
@@ -927,12 +921,7 @@ template <int DQK, int DV, bool BF16>
 static int launch_fwd_t(const FwdLaunch& L) {
   using C = FwdCfg<DQK, DV>;
   auto kern = fwd_kernel<DQK, DV, BF16>;
-  static bool attr_set = false;  // per process; the attribute is per function
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) != cudaSuccess)
-      return SDPA_ERR_CUDA;
-    attr_set = true;
-  }
+  if (const int rc = set_kernel_smem(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, -1)) return rc;
   const long long grid = (long long)L.p.n_q_tiles * L.p.g.hq * L.p.g.batch * L.p.dv_splits;
   if (grid <= 0) return SDPA_OK;
   if (grid > 0x7fffffffLL) return SDPA_ERR_UNSUPPORTED;

@@ -8,6 +8,13 @@
 
 namespace sdpa {
 
+// Raise a kernel's dynamic shared-memory limit to `bytes` and, when
+// carveout >= 0, set its preferred shared-memory carveout (percent), once per
+// (kernel, current device): function attributes belong to each device's
+// instance of the module, and several host threads may make their first call
+// at the same time. Returns an sdpa_status.
+int set_kernel_smem(const void* kernel, int bytes, int carveout);
+
 struct FwdParams {
   Geom g;
   void* o;
