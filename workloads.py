@@ -96,6 +96,18 @@ def shapes(w: Workload, lengths_q=None, lengths_kv=None, d_q=None, d_kv=None):
     return (int(np.sum(lengths_q)), w.heads_q, d_q), (int(np.sum(lengths_kv)), w.heads_kv, d_kv)
 
 
+def _draw_lengths(w: Workload, rng) -> np.ndarray:
+    lo, hi = w.len_range if w.len_range else (1, w.seqlen_q)
+    return rng.integers(lo, hi + 1, size=w.batch)
+
+
+def thd_lengths(w: Workload, seed: int | None = None) -> np.ndarray:
+    """The per-sequence lengths make_inputs draws for a THD workload (the
+    first draw of its stream), without drawing the tensors."""
+    seed = SEEDS.get(w.name, 0) if seed is None else seed
+    return _draw_lengths(w, np.random.Generator(np.random.PCG64(seed)))
+
+
 def make_inputs(w: Workload, seed: int | None = None, lengths=None):
     """Draw the float64 masters. Returns a dict with q, k, v, do and, for THD,
     cu_seqlens_q / cu_seqlens_kv (int32, zero-based cumulative, B+1 entries).
@@ -108,8 +120,7 @@ def make_inputs(w: Workload, seed: int | None = None, lengths=None):
     out = {}
     lq = lk = None
     if w.layout == "thd":
-        lo, hi = w.len_range if w.len_range else (1, w.seqlen_q)
-        drawn = rng.integers(lo, hi + 1, size=w.batch)
+        drawn = _draw_lengths(w, rng)
         if lengths is None:
             lq = lk = drawn
         elif isinstance(lengths, tuple):
