@@ -5,6 +5,10 @@ kernel times into TFLOP/s. With K = 0 every allowed score is 0, so the
 oracle's LSE of a row is ln(number of keys it may attend) (a closed form the
 oracle pins hold); summing exp(LSE) over rows therefore counts the pairs the
 oracle's own mask allows, independently of the benchmark's formula.
+tests/golden/pair_counts.json holds those counts for every workload at full
+size (written by tests/golden/make_pair_counts.py, which calls only the
+oracle); the benchmark's counts and the closed forms of the masks must both
+reproduce them.
 """
 import math
 import os
@@ -75,3 +79,39 @@ def test_headline_workload_flops_are_the_stated_convention():
     assert conv == sum(4 * w.heads_q * int(n) * int(n) * w.head_dim // 2 for n in lq)
     # the exact count adds the diagonal: n(n+1)/2 against n^2/2 pairs
     assert math.isclose(exact / conv, sum(int(n) * (int(n) + 1) for n in lq) / sum(int(n) ** 2 for n in lq))
+
+
+def _golden():
+    import json
+
+    with open(os.path.join(ROOT, "tests", "golden", "pair_counts.json")) as f:
+        return json.load(f)["workloads"]
+
+
+def _closed_form(sq, sk, mask, window):
+    """Pairs per head from the mask definition, summed in closed form."""
+    wl = window[0]
+    if mask == "none" and wl < 0:
+        return sq * sk
+    if mask == "causal" and wl < 0 and sq == sk:
+        return sq * (sq + 1) // 2
+    if mask == "causal" and sq == sk:             # a left window of wl keys beyond the diagonal
+        full = min(sq, wl + 1)
+        return full * (full + 1) // 2 + (sq - full) * (wl + 1)
+    if mask == "causal_br" and wl < 0 and sq <= sk:  # row i sees i + (sk - sq) + 1 keys
+        return sq * (sk - sq) + sq * (sq + 1) // 2
+    raise ValueError("no closed form for this shape")
+
+
+@pytest.mark.parametrize("w", workloads.ALL, ids=lambda w: w.name)
+def test_pair_counts_of_every_workload_match_the_golden_oracle_counts(w):
+    g = _golden()[w.name]
+    if w.layout == "thd":
+        lens = workloads.thd_lengths(w)
+        assert list(lens) == g["lengths"]
+        for n, want in zip(lens, g["pairs_per_sequence"]):
+            assert bench.pairs_per_head(w, int(n), int(n)) == want == _closed_form(int(n), int(n), w.mask, w.window)
+    else:
+        want = g["pairs"]
+        assert bench.pairs_per_head(w, w.seqlen_q, w.seqlen_kv) == want
+        assert _closed_form(w.seqlen_q, w.seqlen_kv, w.mask, w.window) == want
