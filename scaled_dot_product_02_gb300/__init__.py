@@ -142,6 +142,50 @@ def _check_cuda(*ts):
             raise ValueError("sdpa tensors must be contiguous in their layout")
 
 
+def _validate(layout, q, k, v, *, o=None, lse=None, dout=None, dq=None, dk=None, dv=None, cu_q=None, cu_kv=None):
+    """Shapes, dtypes and devices of one call's tensors, from their metadata
+    alone (no device access, no synchronisation). The C ABI receives bare
+    pointers and sizes taken from q and k, so a tensor smaller than the
+    problem it is part of would let the kernels read or write past its end:
+    such calls are refused here with ValueError."""
+    import torch
+
+    if q.dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError(f"q must be bfloat16 or float16, got {q.dtype}")
+    rank = 3 if layout == "thd" else 4
+    for name, t in (("q", q), ("k", k), ("v", v)):
+        if t.dim() != rank:
+            raise ValueError(f"{name} must have {rank} dimensions in layout {layout}, got {tuple(t.shape)}")
+        if t.dtype != q.dtype or t.device != q.device:
+            raise ValueError(f"{name} must have q's dtype and device ({q.dtype}, {q.device})")
+    if k.shape[-1] != q.shape[-1]:
+        raise ValueError(f"q and k must share head_dim, got {q.shape[-1]} and {k.shape[-1]}")
+    if tuple(k.shape[:-1]) != tuple(v.shape[:-1]):
+        raise ValueError(f"k and v must agree on every dimension but the last, got {tuple(k.shape)} and "
+                         f"{tuple(v.shape)}")
+    batch_dim = {"bshd": 0, "sbhd": 1}.get(layout)
+    if batch_dim is not None and q.shape[batch_dim] != k.shape[batch_dim]:
+        raise ValueError(f"q and k must have the same batch size, got {q.shape[batch_dim]} and {k.shape[batch_dim]}")
+    o_shape = tuple(q.shape[:-1]) + (v.shape[-1],)
+    rows_q = q.numel() // max(1, q.shape[-1] * q.shape[-2])
+    for name, t, shape, dtype in (("o", o, o_shape, q.dtype), ("dout", dout, o_shape, q.dtype),
+                                  ("dq", dq, tuple(q.shape), q.dtype), ("dk", dk, tuple(k.shape), q.dtype),
+                                  ("dv", dv, tuple(v.shape), q.dtype),
+                                  ("lse", lse, (rows_q, q.shape[-2]), torch.float32)):
+        if t is None:
+            continue
+        if tuple(t.shape) != shape or t.dtype != dtype or t.device != q.device:
+            raise ValueError(f"{name} must be {dtype} of shape {shape} on {q.device}, got {t.dtype} "
+                             f"{tuple(t.shape)} on {t.device}")
+    for name, t in (("cu_seqlens_q", cu_q), ("cu_seqlens_kv", cu_kv)):
+        if t is None:
+            continue
+        if t.dtype != torch.int32 or t.dim() != 1 or t.numel() < 1 or t.device != q.device:
+            raise ValueError(f"{name} must be a 1-D int32 tensor of batch + 1 entries on {q.device}")
+    if cu_q is not None and cu_kv is not None and cu_q.numel() != cu_kv.numel():
+        raise ValueError("cu_seqlens_q and cu_seqlens_kv must have the same number of entries")
+
+
 def sdpa_check_problem(p: Problem) -> int:
     return int(lib().sdpa_check_problem(ctypes.byref(p)))
 
@@ -169,6 +213,7 @@ def sdpa_fwd(q, k, v, *, layout="bshd", mask="none", window=(-1, -1), scale=None
         out = torch.empty(tuple(q.shape[:-1]) + (v.shape[-1],), dtype=q.dtype, device=q.device)
     if lse is None:
         lse = torch.empty((rows_q, q.shape[-2]), dtype=torch.float32, device=q.device)
+    _validate(layout, q, k, v, o=out, lse=lse, cu_q=cu_seqlens_q, cu_kv=cu_seqlens_kv)
     need = sdpa_fwd_workspace_size(p)
     if workspace is None and need:
         workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
@@ -195,6 +240,7 @@ def sdpa_bwd(q, k, v, o, lse, dout, *, layout="bshd", mask="none", window=(-1, -
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    _validate(layout, q, k, v, o=o, lse=lse, dout=dout, dq=dq, dk=dk, dv=dv, cu_q=cu_seqlens_q, cu_kv=cu_seqlens_kv)
     need = sdpa_bwd_workspace_size(p)
     if workspace is None:
         workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=q.device)
@@ -225,6 +271,7 @@ def sdpa_bwd_noalloc(q, k, v, o, lse, dout, *, layout="bshd", mask="none", windo
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
+    _validate(layout, q, k, v, o=o, lse=lse, dout=dout, dq=dq, dk=dk, dv=dv, cu_q=cu_seqlens_q, cu_kv=cu_seqlens_kv)
     _check_cuda(q, k, v, o, lse, dout, dq, dk, dv, cu_seqlens_q, cu_seqlens_kv)
     rc = lib().sdpa_bwd_noalloc(ctypes.byref(p), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse), _ptr(dout),
                                 _ptr(dq), _ptr(dk), _ptr(dv), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv),
@@ -277,6 +324,10 @@ def sdpa_merge(o_parts, lse_parts, *, out=None, lse=None, stream=None):
         lse = torch.empty(lse_parts.shape[1:], dtype=torch.float32, device=o_parts.device)
     if lse_parts.dtype != torch.float32 or lse_parts.numel() != n * items or lse.numel() != items:
         raise ValueError("lse_parts must be float32 [P, rows, H] matching o_parts")
+    if lse.dtype != torch.float32 or out.dtype != o_parts.dtype or out.numel() != items * d:
+        raise ValueError("out must have o_parts' dtype and o_parts[0]'s size, lse must be float32 [rows, H]")
+    if len({t.device for t in (o_parts, lse_parts, out, lse)}) != 1:
+        raise ValueError("sdpa_merge tensors must be on one device")
     for t in (o_parts, lse_parts, out, lse):
         if not t.is_contiguous():
             raise ValueError("sdpa_merge needs contiguous tensors")

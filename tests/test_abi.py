@@ -211,3 +211,47 @@ def test_merge_host_validation(pkg):
     assert call(c=po + ob) == 4                      # output inside the partial outputs: SDPA_ERR_OVERLAP
     assert call(e=pl) == 4                           # output LSE over the partial LSE
     assert L.sdpa_merge(None, None, None, None, None, None) == 1
+
+
+def test_binding_refuses_inconsistent_tensors_before_any_device_access(pkg):
+    """The binding checks shapes, dtypes and devices from tensor metadata, so
+    a tensor smaller than the problem it belongs to never reaches a kernel."""
+    import torch
+
+    bf = torch.bfloat16
+    q = torch.zeros(2, 64, 4, 128, dtype=bf)
+    k = torch.zeros(2, 96, 2, 128, dtype=bf)
+    v = torch.zeros(2, 96, 2, 128, dtype=bf)
+    ok = lambda **kw: pkg._validate("bshd", q, k, v, **kw)
+    ok()
+    ok(o=torch.zeros(2, 64, 4, 128, dtype=bf), lse=torch.zeros(128, 4), dout=torch.zeros(2, 64, 4, 128, dtype=bf),
+       dq=torch.zeros_like(q), dk=torch.zeros_like(k), dv=torch.zeros_like(v))
+    pkg._validate("bshd", torch.zeros(1, 8, 2, 192, dtype=bf), torch.zeros(1, 8, 2, 192, dtype=bf),
+                  torch.zeros(1, 8, 2, 128, dtype=bf), o=torch.zeros(1, 8, 2, 128, dtype=bf))  # 192/128
+    bad = [
+        lambda: pkg._validate("bshd", q, k, torch.zeros(2, 95, 2, 128, dtype=bf)),               # v shorter than k
+        lambda: pkg._validate("bshd", q, torch.zeros(2, 96, 2, 64, dtype=bf), v),                # head_dim mismatch
+        lambda: pkg._validate("bshd", q, torch.zeros(1, 96, 2, 128, dtype=bf),
+                              torch.zeros(1, 96, 2, 128, dtype=bf)),                             # batch mismatch
+        lambda: pkg._validate("bshd", q, k.half(), v),                                           # dtype mismatch
+        lambda: pkg._validate("bshd", q.float(), k.float(), v.float()),                          # fp32 inputs
+        lambda: pkg._validate("thd", q, k, v),                                                   # rank for thd
+        lambda: ok(o=torch.zeros(2, 64, 4, 64, dtype=bf)),                                       # o too narrow
+        lambda: ok(lse=torch.zeros(128, 4, dtype=torch.float64)),                                # lse dtype
+        lambda: ok(lse=torch.zeros(127, 4)),                                                     # lse rows
+        lambda: ok(dout=torch.zeros(2, 63, 4, 128, dtype=bf)),                                   # dO shape
+        lambda: ok(dk=torch.zeros(2, 96, 2, 128, dtype=torch.float16)),                          # dK dtype
+        lambda: pkg._validate("thd", q[0], k[0], v[0], cu_q=torch.zeros(3, dtype=torch.int64)),  # cu dtype
+        lambda: pkg._validate("thd", q[0], k[0], v[0], cu_q=torch.zeros(3, dtype=torch.int32),
+                              cu_kv=torch.zeros(4, dtype=torch.int32)),                          # cu lengths
+    ]
+    for i, f in enumerate(bad):
+        with pytest.raises(ValueError):
+            f()
+    # merge: an output smaller than one block's rows is refused too
+    po = torch.zeros(3, 10, 2, 128, dtype=bf)
+    pl = torch.zeros(3, 10, 2)
+    with pytest.raises(ValueError):
+        pkg.sdpa_merge(po, pl, out=torch.zeros(9, 2, 128, dtype=bf))
+    with pytest.raises(ValueError):
+        pkg.sdpa_merge(po, pl, out=torch.zeros(10, 2, 128, dtype=torch.float16))
