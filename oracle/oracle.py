@@ -72,6 +72,11 @@ def _load():
             lib.sdpa_oracle_dq_rows.argtypes = [pp, dp, dp, dp, dp, ip, ip, ctypes.c_int, ip, dp]
             lib.sdpa_oracle_dkdv_rows.argtypes = [pp, dp, dp, dp, dp, ip, ip, ctypes.c_int, ip, dp, dp]
             lib.sdpa_oracle_merge.argtypes = [ctypes.c_int, ctypes.c_int64, ctypes.c_int, dp, dp, dp, dp]
+            u8p = ctypes.POINTER(ctypes.c_uint8)
+            dbl = ctypes.c_double
+            lib.sdpa_oracle_fwd_fp8.argtypes = [pp, u8p, u8p, u8p, dbl, dbl, dbl, dbl, ip, ip, dp, dp]
+            lib.sdpa_oracle_e4m3_round_array.argtypes = [ctypes.c_int64, dp, dp]
+            lib.sdpa_oracle_e4m3_decode_array.argtypes = [ctypes.c_int64, u8p, dp]
             lib.sdpa_oracle_num_threads.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -232,4 +237,44 @@ def merge(o_parts, lse_parts):
     rc = _load().sdpa_oracle_merge(n, items, d, _dptr(o_parts), _dptr(lse_parts), _dptr(o), _dptr(lse))
     if rc:
         raise ValueError(f"oracle merge rejected the problem (rc={rc})")
+    return o, lse
+
+
+# ---------------------------------------------------------------- FP8 E4M3
+def _u8ptr(a):
+    assert a.dtype == np.uint8 and a.flags["C_CONTIGUOUS"]
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8))
+
+
+def e4m3_decode(codes):
+    """Real values of E4M3 codes (uint8 array), NaN for the NaN codes."""
+    c = np.ascontiguousarray(codes, dtype=np.uint8)
+    out = np.zeros(c.shape)
+    _load().sdpa_oracle_e4m3_decode_array(c.size, _u8ptr(c), _dptr(out))
+    return out
+
+
+def e4m3_round(x):
+    """Nearest E4M3 values (ties to even; |x| >= 448 saturates to 448)."""
+    x = _f64(x)
+    out = np.zeros(x.shape)
+    _load().sdpa_oracle_e4m3_round_array(x.size, _dptr(x), _dptr(out))
+    return out
+
+
+def fwd_fp8(q8, k8, v8, *, descale=(1.0, 1.0, 1.0), scale_s=448.0, layout="bshd", mask="none", scale=None,
+            window=(-1, -1), cu_q=None, cu_kv=None):
+    """FP8 E4M3 forward: q8/k8/v8 are E4M3 codes (uint8) in their layouts with
+    per-tensor descales (d_q, d_k, d_v); the softmax output is stored as
+    E4M3(P * scale_s) and O = P8 V * d_v / scale_s. Returns (o, lse) like fwd."""
+    q8, k8, v8 = (np.ascontiguousarray(x, dtype=np.uint8) for x in (q8, k8, v8))
+    scale = 1.0 / np.sqrt(q8.shape[-1]) if scale is None else scale
+    p = Problem(q8, k8, layout, mask, scale, window, cu_q, cu_kv, v=v8)
+    o = np.zeros(q8.shape[:-1] + (p.dv,))
+    lse = np.full((p.rows_q, p.hq), -np.inf)
+    rc = _load().sdpa_oracle_fwd_fp8(ctypes.byref(p.c), _u8ptr(q8), _u8ptr(k8), _u8ptr(v8), float(descale[0]),
+                                     float(descale[1]), float(descale[2]), float(scale_s), _iptr(p.cu_q),
+                                     _iptr(p.cu_kv), _dptr(o), _dptr(lse))
+    if rc:
+        raise ValueError(f"oracle fwd_fp8 rejected the problem (rc={rc})")
     return o, lse

@@ -503,6 +503,115 @@ int sdpa_oracle_merge(int n_parts, int64_t items, int d, const double* o_parts, 
     return 0;
 }
 
+/*
+ * FP8 E4M3 forward (the FP8 variant of this kernel family; no CUDA kernel
+ * implements it yet). Reading of TransformerEngine PR #3705's closing note
+ * ("Amax S"): with E4M3 inputs the softmax output is stored in E4M3 under a
+ * fixed scale, 448 (the format's largest value) without dropout, so no
+ * amax of it is ever needed. Written out:
+ *   Q, K, V are E4M3 codes with per-tensor descales d_q, d_k, d_v (the real
+ *   value of a code c is decode(c) * d);
+ *   s_ij  = scale * d_q * d_k * sum_d decode(q_id) decode(k_jd), masked as above;
+ *   LSE_i = ln sum_j exp(s_ij);  p_ij = exp(s_ij - LSE_i);
+ *   P8_ij = e4m3(p_ij * scale_s);
+ *   o_i   = sum_j P8_ij decode(v_j) * d_v / scale_s.
+ * The softmax is exact (float64, final LSE); only the stored P is rounded.
+ */
+
+/* E4M3, the finite-only variant of the OCP 8-bit float: sign bit, 4 exponent
+ * bits with bias 7, 3 mantissa bits. Exponent field 0 holds the subnormals
+ * m/8 * 2^-6; S.1111.111 is NaN; there is no infinity; the largest finite
+ * magnitude is 1.75 * 2^8 = 448. */
+double sdpa_oracle_e4m3_decode(uint8_t c) {
+    int sign = c >> 7, e = (c >> 3) & 15, m = c & 7;
+    double v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9);          /* m/8 * 2^-6 */
+    else
+        v = ldexp(8.0 + m, e - 10);        /* (1 + m/8) * 2^(e-7) */
+    return sign ? -v : v;
+}
+
+/* Nearest E4M3 value, ties to the even mantissa; magnitudes of 448 and more
+ * saturate to 448 (NaN stays NaN). Between 2^k and 2^(k+1) (k >= -6) the
+ * representable values are 2^(k-3) apart; below 2^-6 (subnormals) 2^-9. */
+double sdpa_oracle_e4m3_round(double x) {
+    if (isnan(x)) return x;
+    double a = fabs(x);
+    if (a >= 448.0) return copysign(448.0, x);
+    int k;
+    frexp(a, &k);                          /* a in [2^(k-1), 2^k) */
+    int ex = k - 1 < -6 ? -6 : k - 1;
+    double spacing = ldexp(1.0, ex - 3);
+    return copysign(nearbyint(a / spacing) * spacing, x);  /* round-to-nearest-even mode */
+}
+
+void sdpa_oracle_e4m3_round_array(int64_t n, const double* x, double* y) {
+    for (int64_t i = 0; i < n; ++i) y[i] = sdpa_oracle_e4m3_round(x[i]);
+}
+
+void sdpa_oracle_e4m3_decode_array(int64_t n, const uint8_t* c, double* y) {
+    for (int64_t i = 0; i < n; ++i) y[i] = sdpa_oracle_e4m3_decode(c[i]);
+}
+
+/* o in Q's layout with head_dim_v columns, lse[token_row][Hq]; q8/k8/v8 are
+ * E4M3 codes in their layouts. Returns 0 on success. */
+int sdpa_oracle_fwd_fp8(const oracle_problem* p, const uint8_t* q8, const uint8_t* k8, const uint8_t* v8,
+                        double descale_q, double descale_k, double descale_v, double scale_s,
+                        const int32_t* cu_q, const int32_t* cu_kv, double* o, double* lse) {
+    if (!valid(p) || !(scale_s > 0.0)) return 1;
+    int hq = p->num_heads_q, D = p->head_dim, DV = dv_of(p);
+    int64_t nq = rows_total(p, cu_q, 1) * hq * D;
+    int64_t nk = rows_total(p, cu_kv, 0) * p->num_heads_kv * D;
+    int64_t nv = rows_total(p, cu_kv, 0) * p->num_heads_kv * DV;
+    double* qd = (double*)malloc(sizeof(double) * (size_t)(nq > 0 ? nq : 1));
+    double* kd = (double*)malloc(sizeof(double) * (size_t)(nk > 0 ? nk : 1));
+    double* vd = (double*)malloc(sizeof(double) * (size_t)(nv > 0 ? nv : 1));
+    if (!qd || !kd || !vd) {
+        free(qd);
+        free(kd);
+        free(vd);
+        return 2;
+    }
+    sdpa_oracle_e4m3_decode_array(nq, q8, qd);
+    sdpa_oracle_e4m3_decode_array(nk, k8, kd);
+    sdpa_oracle_e4m3_decode_array(nv, v8, vd);
+    oracle_problem ps = *p;
+    ps.scale = p->scale * descale_q * descale_k;   /* s_ij on the decoded codes */
+    int lkmax = max_len(p, cu_kv, 0);
+    for (int b = 0; b < p->batch; ++b) {
+        int lq = seq_len(p, cu_q, b, 1), lk = seq_len(p, cu_kv, b, 0);
+#pragma omp parallel
+        {
+            double* srow = (double*)malloc(sizeof(double) * (size_t)(lkmax > 0 ? lkmax : 1));
+#pragma omp for collapse(2) schedule(dynamic, 4)
+            for (int h = 0; h < hq; ++h)
+                for (int i = 0; i < lq; ++i) {
+                    int64_t r = token_row(p, cu_q, b, i, 1);
+                    double* orow = o + (r * hq + h) * DV;
+                    double l = row_scores(&ps, qd, kd, cu_q, cu_kv, b, h, i, srow);
+                    for (int d = 0; d < DV; ++d) orow[d] = 0.0;
+                    lse[r * hq + h] = l;
+                    if (l == -INFINITY) continue;
+                    int g = kv_head_of(p, h);
+                    for (int j = 0; j < lk; ++j) {
+                        if (srow[j] == -INFINITY) continue;
+                        double p8 = sdpa_oracle_e4m3_round(exp(srow[j] - l) * scale_s);
+                        const double* vj = vrow(p, vd, cu_kv, b, j, g);
+                        for (int d = 0; d < DV; ++d) orow[d] += p8 * vj[d];
+                    }
+                    for (int d = 0; d < DV; ++d) orow[d] *= descale_v / scale_s;
+                }
+            free(srow);
+        }
+    }
+    free(qd);
+    free(kd);
+    free(vd);
+    return 0;
+}
+
 int sdpa_oracle_num_threads(void) {
 #ifdef _OPENMP
     extern int omp_get_max_threads(void);

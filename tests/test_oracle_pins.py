@@ -440,3 +440,98 @@ def test_backward_rejects_unequal_head_dims():
         oracle.bwd(q, k, v, r.standard_normal((1, 4, 1, 6)), layout="bshd", mask="causal")
     with pytest.raises(ValueError):
         oracle.dq_rows(q, k, v, r.standard_normal((1, 4, 1, 6)), np.array([[0, 0, 1]]), layout="bshd")
+
+
+# ------------------------------------------------- FP8 E4M3 forward (oracle only)
+def _e4m3_codes(x):
+    """E4M3 codes of float values through torch's own conversion (the library routine)."""
+    return torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+def test_e4m3_decode_matches_torch_for_every_code():
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    got = oracle.e4m3_decode(codes)
+    np.testing.assert_array_equal(got, ref)                 # NaN codes in the same places
+    fin = np.isfinite(ref)
+    np.testing.assert_array_equal(np.signbit(got[fin]), np.signbit(ref[fin]))  # -0 included; NaN signs carry nothing
+    assert np.nanmax(got) == 448.0 and np.nanmin(np.abs(got[got != 0])) == 2.0 ** -9
+
+
+def test_e4m3_round_matches_torch_and_saturates():
+    """Library routine: torch's float8_e4m3fn conversion (round to nearest,
+    ties to even) on random values, every grid value and every midpoint
+    between neighbours, below the point (464) where torch turns to NaN."""
+    r = rng(70)
+    grid = np.unique(np.abs(oracle.e4m3_decode(np.arange(256, dtype=np.uint8))))
+    grid = grid[np.isfinite(grid)]
+    mids = (grid[1:] + grid[:-1]) / 2
+    rand = r.uniform(-463.0, 463.0, 20000).astype(np.float32).astype(np.float64)
+    tiny = (r.uniform(-1, 1, 5000) * 2.0 ** -6).astype(np.float32).astype(np.float64)
+    x = np.concatenate([grid, -grid, mids, -mids, rand, tiny])
+    ref = torch.from_numpy(x).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(oracle.e4m3_round(x), ref)
+    np.testing.assert_array_equal(oracle.e4m3_round(np.array([464.0, 1e6, -500.0])), [448.0, 448.0, -448.0])
+
+
+def _fp8_inputs(r, shape_q, shape_k, shape_v):
+    return (_e4m3_codes(r.standard_normal(s) * 3.0) for s in (shape_q, shape_k, shape_v))
+
+
+@pytest.mark.parametrize("layout,mask,window", [("bshd", "causal", (-1, -1)), ("thd", "causal_br", (6, -1)),
+                                                ("bshd", "none", (-1, -1))])
+def test_fp8_scores_and_lse_equal_the_float64_forward_on_decoded_inputs(layout, mask, window):
+    """With power-of-two descales the scores are bit for bit those of the
+    pinned float64 forward on the decoded, descaled inputs, so the LSE is too;
+    O differs only through the E4M3 rounding of P (next test)."""
+    r = rng(71)
+    dq, dk, dv = 0.5, 0.25, 2.0
+    if layout == "thd":
+        lens = np.array([17, 30, 1])
+        cu = np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)
+        q8, k8, v8 = _fp8_inputs(r, (cu[-1], 4, 16), (cu[-1], 2, 16), (cu[-1], 2, 16))
+        kw = dict(layout="thd", mask=mask, window=window, cu_q=cu, cu_kv=cu, scale=0.3)
+    else:
+        q8, k8, v8 = _fp8_inputs(r, (2, 12, 4, 16), (2, 19, 2, 16), (2, 19, 2, 16))
+        kw = dict(layout="bshd", mask=mask, window=window, scale=0.3)
+    o8, l8 = oracle.fwd_fp8(q8, k8, v8, descale=(dq, dk, dv), **kw)
+    o, l = oracle.fwd(oracle.e4m3_decode(q8) * dq, oracle.e4m3_decode(k8) * dk, oracle.e4m3_decode(v8) * dv, **kw)
+    np.testing.assert_array_equal(l8, l)
+    # |dO| <= d_v * max|v| * (2^-4 + n * 2^-10 / 448) per row: one E4M3 rounding of each P * 448
+    vmax = np.max(np.abs(oracle.e4m3_decode(v8))) * dv
+    n_max = k8.shape[0] if layout == "thd" else k8.shape[1]
+    err = np.abs(o8 - o)
+    assert np.max(err) <= vmax * (2.0 ** -4 + n_max * 2.0 ** -10 / 448)
+    assert np.max(err) > 1e-6 * vmax  # the rounding of P is really applied
+
+
+def test_fp8_zero_keys_give_the_quantised_uniform_average():
+    """Closed form: K = 0 makes every allowed score 0, so P = 1/n for the n
+    keys a row sees and O = e4m3(448/n)/448 * d_v * (sum of those v rows)."""
+    r = rng(72)
+    q8 = _e4m3_codes(r.standard_normal((1, 9, 2, 8)))
+    k8 = np.zeros((1, 9, 1, 8), dtype=np.uint8)
+    v8 = _e4m3_codes(r.standard_normal((1, 9, 1, 8)))
+    o, lse = oracle.fwd_fp8(q8, k8, v8, descale=(1.0, 1.0, 0.5), layout="bshd", mask="causal", scale=0.4)
+    v = oracle.e4m3_decode(v8)[0, :, 0]
+    for i in range(9):
+        n = i + 1
+        w = oracle.e4m3_round(np.array([448.0 / n]))[0] / 448.0
+        np.testing.assert_allclose(o[0, i, 0], w * 0.5 * v[:n].sum(axis=0), rtol=1e-14, atol=1e-15)
+        np.testing.assert_allclose(o[0, i, 1], o[0, i, 0], rtol=0, atol=0)   # both q heads read kv head 0
+        assert lse[i, 0] == pytest.approx(math.log(n), abs=1e-14)
+
+
+def test_fp8_dominant_key_returns_its_value_exactly():
+    """Closed form: one key scoring far above the rest gets P = 1, stored as
+    448 exactly, while the others underflow below E4M3's smallest value, so
+    O is that key's value times d_v, bit for bit."""
+    q8 = np.zeros((1, 5, 1, 4), dtype=np.uint8)
+    k8 = np.zeros((1, 5, 1, 4), dtype=np.uint8)
+    q8[..., 0] = _e4m3_codes([448.0])[0]
+    k8[0, 0, 0, 0] = _e4m3_codes([448.0])[0]
+    v8 = _e4m3_codes(rng(73).standard_normal((1, 5, 1, 4)))
+    o, _ = oracle.fwd_fp8(q8, k8, v8, descale=(1.0, 1.0, 0.25), layout="bshd", mask="causal", scale=1.0 / 16)
+    v0 = oracle.e4m3_decode(v8)[0, 0, 0] * 0.25
+    for i in range(5):
+        np.testing.assert_array_equal(o[0, i, 0], v0)
