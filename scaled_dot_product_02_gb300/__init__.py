@@ -8,6 +8,9 @@ are not CUDA tensors, the call raises.
 
 Layouts: "bshd" [B,S,H,D], "sbhd" [S,B,H,D], "thd" [T,H,D] (+ cu_seqlens).
 Masks: "none", "causal" (top-left), "causal_br" (bottom-right).
+V (and O, dO) may be narrower than Q/K for the forward's 192/128 pair; the
+binding reads that width from v. Tensor shapes, dtypes and devices are checked
+against each other from metadata before the library is called.
 """
 from __future__ import annotations
 
