@@ -255,3 +255,28 @@ def test_binding_refuses_inconsistent_tensors_before_any_device_access(pkg):
         pkg.sdpa_merge(po, pl, out=torch.zeros(9, 2, 128, dtype=bf))
     with pytest.raises(ValueError):
         pkg.sdpa_merge(po, pl, out=torch.zeros(10, 2, 128, dtype=torch.float16))
+
+
+def test_missing_library_fails_loudly_with_no_fallback(tmp_path):
+    """In a fresh interpreter whose package copy has no libsdpa.so, every entry
+    point raises ImportError: there is no other implementation to fall back to."""
+    import shutil
+    import subprocess
+    import sys
+
+    pkg_src = os.path.join(ROOT, "scaled_dot_product_02_gb300", "__init__.py")
+    dst = tmp_path / "scaled_dot_product_02_gb300"
+    dst.mkdir()
+    shutil.copy(pkg_src, dst / "__init__.py")
+    code = ("import scaled_dot_product_02_gb300 as s, torch\n"
+            "q = torch.zeros(1, 128, 2, 128, dtype=torch.bfloat16)\n"
+            "for f in (lambda: s.lib(), lambda: s.sdpa_fwd(q, q, q)):\n"
+            "    try:\n"
+            "        f()\n"
+            "    except ImportError as e:\n"
+            "        print('raised', 'libsdpa.so' in str(e))\n"
+            "    else:\n"
+            "        print('no error')\n")
+    r = subprocess.run([sys.executable, "-c", code], cwd=tmp_path, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.split("\n")[:2] == ["raised True", "raised True"], r.stdout
