@@ -280,3 +280,45 @@ def test_missing_library_fails_loudly_with_no_fallback(tmp_path):
     r = subprocess.run([sys.executable, "-c", code], cwd=tmp_path, capture_output=True, text=True, timeout=300)
     assert r.returncode == 0, r.stderr
     assert r.stdout.split("\n")[:2] == ["raised True", "raised True"], r.stdout
+
+
+def _header_struct(name, path=HEADER):
+    """(field, C type) pairs of `typedef struct { ... } name;` in a C source, in order."""
+    text = re.sub(r"/\*.*?\*/", "", open(path).read(), flags=re.S)
+    body = re.search(r"typedef struct \{([^{}]*)\}\s*" + name + r"\s*;", text).group(1)
+    fields = []
+    for decl in body.split(";"):
+        decl = " ".join(decl.split())
+        if not decl:
+            continue
+        m = re.match(r"((?:unsigned |long |short )*\w+)\s+(.*)", decl)
+        ctype, names = m.group(1), m.group(2)
+        fields += [(n.strip(), ctype) for n in names.split(",")]
+    return fields
+
+
+def test_ctypes_structs_mirror_the_header(pkg):
+    """The binding's ctypes structures must match the C structs field for
+    field (name, order and type), or every call would pass shifted values."""
+    import ctypes
+
+    ctype_of = {"int": ctypes.c_int, "float": ctypes.c_float, "long long": ctypes.c_longlong}
+    for cname, py in (("sdpa_problem", pkg.Problem), ("sdpa_merge_problem", pkg.MergeProblem)):
+        want = _header_struct(cname)
+        got = [(f, t) for f, t in py._fields_]
+        assert [f for f, _ in got] == [f for f, _ in want], cname
+        for (f, t), (_, ct) in zip(got, want):
+            assert t is ctype_of[ct], (cname, f, ct)
+
+
+def test_oracle_ctypes_struct_mirrors_its_c_struct():
+    import ctypes
+
+    from oracle import oracle
+
+    ctype_of = {"int": ctypes.c_int, "double": ctypes.c_double}
+    want = _header_struct("oracle_problem", os.path.join(ROOT, "oracle", "sdpa_oracle.c"))
+    got = list(oracle._Problem._fields_)
+    assert [f for f, _ in got] == [f for f, _ in want]
+    for (f, t), (_, ct) in zip(got, want):
+        assert t is ctype_of[ct], (f, ct)
