@@ -322,3 +322,21 @@ def test_oracle_ctypes_struct_mirrors_its_c_struct():
     assert [f for f, _ in got] == [f for f, _ in want]
     for (f, t), (_, ct) in zip(got, want):
         assert t is ctype_of[ct], (f, ct)
+
+
+def test_a_plain_c_program_uses_the_abi(pkg, tmp_path):
+    """tests/c_abi_host_check.c, compiled as C99 by gcc against include/sdpa.h
+    and linked to libsdpa.so, runs its host-side checks (no GPU needed)."""
+    import shutil
+    import subprocess
+
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("gcc not found")
+    exe = str(tmp_path / "c_abi_host_check")
+    libdir = os.path.dirname(pkg.LIB_PATH)
+    subprocess.check_call([gcc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"),
+                           os.path.join(ROOT, "tests", "c_abi_host_check.c"), "-o", exe, "-L", libdir, "-lsdpa",
+                           f"-Wl,-rpath,{libdir}"])
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout + r.stderr
