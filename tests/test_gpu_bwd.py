@@ -23,12 +23,15 @@ BWD_CASES = [
     Workload("d512_br", "bshd", "causal_br", 1, 130, 300, 2, 1, 512, "bf16"),
     Workload("d512_nomask_gqa", "bshd", "none", 1, 129, 257, 4, 2, 512, "bf16"),
     Workload("d512_br_more_queries", "bshd", "causal_br", 1, 300, 140, 2, 2, 512, "bf16"),
+    Workload("d512_fp16_br", "bshd", "causal_br", 1, 200, 333, 2, 1, 512, "fp16", std=0.5),
+    Workload("d512_thd_varlen", "thd", "causal", 3, 260, 260, 2, 1, 512, "bf16", len_range=(1, 260)),
+    Workload("d256_fp16_thd_nomask", "thd", "none", 3, 200, 200, 2, 2, 256, "fp16", len_range=(1, 200)),
 ]
 
 
 def run_fwd_bwd(w, inp):
     from scaled_dot_product_02_gb300 import sdpa_bwd, sdpa_fwd, sdpa_get_device_error
-    from parity import gpu_kwargs, to_device
+    from parity import gpu_kwargs, to_device, report
 
     q, k, v, do = (to_device(inp[x], w.dtype) for x in ("q", "k", "v", "do"))
     kw = gpu_kwargs(w, inp)
@@ -41,11 +44,9 @@ def run_fwd_bwd(w, inp):
 
 @pytest.mark.parametrize("w", BWD_CASES, ids=lambda w: w.name)
 def test_backward_matches_oracle(w):
-    from parity import check_bwd
+    from parity import check_bwd, report
 
     inp = workloads.make_inputs(w, seed=11)
     dq, dk, dv = run_fwd_bwd(w, inp)
     results = check_bwd(w, inp, dq, dk, dv)
-    msgs = [m for _, m in results]
-    print(w.name, msgs)
-    assert all(ok for ok, _ in results), msgs
+    report(w.name, results)

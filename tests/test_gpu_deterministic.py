@@ -29,7 +29,7 @@ DET_CASES = [
 
 
 def _run(w, inp, deterministic):
-    from parity import gpu_kwargs, to_device
+    from parity import gpu_kwargs, to_device, report
     from scaled_dot_product_02_gb300 import sdpa_bwd, sdpa_fwd, sdpa_get_device_error
 
     q, k, v, do = (to_device(inp[x], w.dtype) for x in ("q", "k", "v", "do"))
@@ -42,15 +42,13 @@ def _run(w, inp, deterministic):
 
 @pytest.mark.parametrize("w", DET_CASES, ids=lambda w: w.name)
 def test_deterministic_backward_matches_oracle(w):
-    from parity import check_bwd
+    from parity import check_bwd, report
 
     inp = workloads.make_inputs(w, seed=11)
     f = lambda t: t.float().cpu().numpy().astype(np.float64)
     dq, dk, dv = (f(t) for t in _run(w, inp, True))
     results = check_bwd(w, inp, dq, dk, dv)
-    msgs = [m for _, m in results]
-    print(w.name, msgs)
-    assert all(ok for ok, _ in results), msgs
+    report(w.name, results)
 
 
 def test_two_deterministic_runs_are_bitwise_identical():
@@ -82,24 +80,24 @@ EDGE_DET = [
 
 @pytest.mark.parametrize("w", EDGE_DET, ids=lambda w: w.name)
 def test_deterministic_backward_edge_shapes(w):
-    from parity import check_bwd
+    from parity import check_bwd, report
 
     inp = workloads.make_inputs(w, seed=5)
     f = lambda t: t.float().cpu().numpy().astype(np.float64)
     dq, dk, dv = (f(t) for t in _run(w, inp, True))
     results = check_bwd(w, inp, dq, dk, dv)
-    assert all(ok for ok, _ in results), [m for _, m in results]
+    report(w.name, results)
 
 
 def test_deterministic_backward_with_empty_thd_sequences():
-    from parity import check_bwd
+    from parity import check_bwd, report
 
     w = Workload("thd_with_empty", "thd", "causal", 4, 150, 150, 2, 2, 128, "bf16")
     inp = workloads.make_inputs(w, seed=8, lengths=np.array([150, 0, 37, 0]))
     f = lambda t: t.float().cpu().numpy().astype(np.float64)
     dq, dk, dv = (f(t) for t in _run(w, inp, True))
     results = check_bwd(w, inp, dq, dk, dv)
-    assert all(ok for ok, _ in results), [m for _, m in results]
+    report(w.name, results)
 
 
 def test_deterministic_backward_rejects_bad_cu_seqlens_and_writes_nothing():

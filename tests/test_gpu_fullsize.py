@@ -14,7 +14,7 @@ pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 def run_full(w, inp):
     import torch
 
-    from parity import gpu_kwargs, to_device
+    from parity import gpu_kwargs, to_device, report
     from scaled_dot_product_02_gb300 import sdpa_bwd, sdpa_fwd, sdpa_get_device_error
 
     q, k, v, do = (to_device(inp[x], w.dtype) for x in ("q", "k", "v", "do"))
@@ -37,7 +37,7 @@ def run_full(w, inp):
 
 @pytest.mark.parametrize("w", workloads.ALL, ids=lambda w: w.name)
 def test_full_size_sampled_parity(w):
-    from parity import check_bwd, check_fwd, check_sampled
+    from parity import check_bwd, check_fwd, check_sampled, report
 
     inp = workloads.make_inputs(w)
     out = run_full(w, inp)
@@ -48,6 +48,4 @@ def test_full_size_sampled_parity(w):
         results = check_fwd(w, inp, out["o"], out["lse"]) + check_bwd(w, inp, out["dq"], out["dk"], out["dv"])
     else:
         results = check_sampled(w, inp, out, n_rows=48, n_keys=24)
-    msgs = [m for _, m in results]
-    print(w.name, msgs)
-    assert all(ok for ok, _ in results), msgs
+    report(w.name, results)

@@ -23,12 +23,14 @@ FWD_CASES = [
     Workload("d512_nomask", "bshd", "none", 1, 129, 257, 2, 2, 512, "bf16"),
     Workload("br_more_queries_than_keys", "bshd", "causal_br", 1, 300, 140, 2, 2, 128, "bf16"),
     Workload("d256_fp16_sbhd_window", "sbhd", "causal", 2, 260, 260, 2, 1, 256, "fp16", window=(64, 0)),
+    Workload("d512_fp16_br", "bshd", "causal_br", 1, 200, 333, 2, 1, 512, "fp16", std=0.5),
+    Workload("d512_thd_varlen", "thd", "causal", 3, 260, 260, 2, 1, 512, "bf16", len_range=(1, 260)),
 ]
 
 
 def run_fwd(w, inp):
     from scaled_dot_product_02_gb300 import sdpa_fwd, sdpa_get_device_error
-    from parity import gpu_kwargs, to_device
+    from parity import gpu_kwargs, to_device, report
 
     q, k, v = (to_device(inp[x], w.dtype) for x in ("q", "k", "v"))
     o, lse = sdpa_fwd(q, k, v, **gpu_kwargs(w, inp))
@@ -38,11 +40,9 @@ def run_fwd(w, inp):
 
 @pytest.mark.parametrize("w", FWD_CASES, ids=lambda w: w.name)
 def test_forward_matches_oracle(w):
-    from parity import check_fwd
+    from parity import check_fwd, report
 
     inp = workloads.make_inputs(w, seed=7)
     o, lse = run_fwd(w, inp)
     results = check_fwd(w, inp, o, lse)
-    msgs = [m for _, m in results]
-    print(w.name, msgs)
-    assert all(ok for ok, _ in results), msgs
+    report(w.name, results)
