@@ -289,7 +289,7 @@ def gpu_arm(args, w, inp):
     batch = len(inp["cu_seqlens_q"]) - 1 if w.layout == "thd" else None
     prob = sdpa.make_problem(q, k, layout=w.layout, mask=w.mask, window=w.window, scale=w.scale, batch=batch,
                              max_seqlen_q=kw.get("max_seqlen_q"), max_seqlen_kv=kw.get("max_seqlen_kv"),
-                             head_dim_v=w.dv)
+                             head_dim_v=w.dv, kv_chunk=args.kv_chunk)
     ws_f = torch.empty(max(256, sdpa.sdpa_fwd_workspace_size(prob)), dtype=torch.uint8, device=dev)
     dq = dk = dv = ws_b = None
     if not fo:
@@ -304,7 +304,8 @@ def gpu_arm(args, w, inp):
         n = sdpa.sdpa_last_launch_count()
         if fo:
             return n
-        sdpa.sdpa_bwd(q, k, v, o, lse, do, dq=dq, dk=dk, dv=dv, workspace=ws_b, deterministic=det, **kw)
+        sdpa.sdpa_bwd(q, k, v, o, lse, do, dq=dq, dk=dk, dv=dv, workspace=ws_b, deterministic=det,
+                      kv_chunk=args.kv_chunk, **kw)
         return n + sdpa.sdpa_last_launch_count()
 
     for _ in range(args.warmup):
@@ -380,7 +381,7 @@ def gpu_arm(args, w, inp):
         sdpa.sdpa_fwd(d["q"], d["k"], d["v"], out=d["o"], lse=d["lse"], workspace=d["ws_f"], stream=s_comp, **kwb)
         if not fo:
             sdpa.sdpa_bwd(d["q"], d["k"], d["v"], d["o"], d["lse"], d["do"], dq=d["dq"], dk=d["dk"], dv=d["dv"],
-                          workspace=d["ws_b"], stream=s_comp, deterministic=det, **kwb)
+                          workspace=d["ws_b"], stream=s_comp, deterministic=det, kv_chunk=args.kv_chunk, **kwb)
         ev_comp[b].record(s_comp)
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev_comp[b])
@@ -467,7 +468,8 @@ def gpu_arm(args, w, inp):
     if kern["preprocess"]["ms_avg"]:
         # reads O and dO (2 bytes each), writes delta and LSE*log2e, zeroes the fp32 dQ accumulator
         rows = rows_q * w.heads_q
-        byts = rows * w.head_dim * 2 * 2 + rows * 8 + rows * w.head_dim * 4
+        zeroed = rows * w.head_dim * 4 if kern["dq_finalize"]["launches"] else 0  # fp32 dQ accumulator
+        byts = rows * w.head_dim * 2 * 2 + rows * 8 + zeroed
         detail["preprocess_gbs"] = byts / (kern["preprocess"]["ms_avg"] * 1e-3) / 1e9
     if kern["dq_finalize"]["ms_avg"]:
         rows = rows_q * w.heads_q
@@ -491,7 +493,9 @@ def gpu_arm(args, w, inp):
                                           "halved for causal; bwd 2.5x fwd",
                        "l2": "flushed between timed steps (256 MiB write, outside the events)",
                        "parallelism": f"replicas x{world} (no collective)",
-                       "backward": None if fo else "deterministic" if det else "fp32 reductions for dQ (head_dim 128)"},
+                       "backward": None if fo else "deterministic" if det else "fp32 reductions for dQ (head_dim 128)",
+                       "bwd_workspace_bytes": None if fo else int(ws_b.numel()),
+                       "kv_chunk": None if fo or w.head_dim == 128 else args.kv_chunk or "library choice"},
             "clocks": clk, "gpu_launches": launches,
             "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": e2e_ms, "h2d_ms_alone": h2d_ms, "d2h_ms_alone": d2h_ms,
@@ -598,6 +602,8 @@ def main():
                     help="step: the fwd+bwd hot path (the headline; the forward alone for forward-only "
                          "workloads); fwd: the forward alone; merge: the LSE merge of key-split results")
     ap.add_argument("--merge-parts", type=int, default=4)
+    ap.add_argument("--kv-chunk", type=int, default=0,
+                    help="head_dim 256/512 backward: key positions per chunk (multiple of 128; 0 = library choice)")
     ap.add_argument("--deterministic", action="store_true",
                     help="bitwise-reproducible backward (head_dim 128: separate dQ pass, no fp32 reductions)")
     args = ap.parse_args()

@@ -108,13 +108,34 @@ typedef struct {
   int head_dim_v;      /* Dv, the width of V and O rows (and of dV, dO): 0 or head_dim = symmetric.
                           The one asymmetric pair is head_dim 192 with head_dim_v 128, forward
                           only; sdpa_bwd and sdpa_bwd_noalloc decline it (SDPA_ERR_UNSUPPORTED). */
+  int kv_chunk;        /* backward, head_dim 256/512 only (ignored elsewhere): key positions per
+                          chunk of the two-phase backward, a multiple of 128; 0 = the library's
+                          choice. The workspace holds the score tiles of one chunk of keys, so it
+                          stays bounded however long the keys are (TransformerEngine PR #3527
+                          "Known limitations": the prior art's backward workspace grows to 74 GiB
+                          at 64k tokens and caps the context). Smaller chunks need less
+                          workspace and repeat more per-chunk work. The library's choice keeps one
+                          chunk when a bounded (left, right) window already bounds the keys a query
+                          tile sees or the tile arrays fit in 512 MiB, else the largest chunk that
+                          fits that budget. Negative or not a multiple of 128:
+                          SDPA_ERR_INVALID_ARG. */
 } sdpa_problem;
 
 /* Bytes of device workspace sdpa_fwd / sdpa_bwd need for this problem
  * (0 when none). Returns 0 as well for a problem the library declines; call
- * sdpa_check_problem to tell the two apart. The forward needs 256 bytes for
- * THD (the metadata guard word) and for head_dim 128 (the tile counter of
- * its persistent kernel, zeroed on the stream by every call), else none. */
+ * sdpa_check_problem to tell the two apart. The workspace is caller-owned and
+ * per call (TransformerEngine PR #3527, "Known limitations", where the
+ * backward's workspace request is what caps the context length).
+ * The forward needs 256 bytes for THD (the metadata guard word) and for
+ * head_dim 128 (the tile counter of its persistent kernel, zeroed on the
+ * stream by every call), else none. The backward needs per-row statistics
+ * (8 bytes per query row and head, padded) plus: head_dim 128, a float32 dQ
+ * accumulator (4 * D bytes per query row and head; none with
+ * deterministic = 1); head_dim 256/512, the 16-bit P and dS score tiles of one
+ * chunk of keys (see kv_chunk: 64 KiB per (query tile, key tile) pair of the
+ * chunk) and, when the keys are split into several chunks, the float32 dQ
+ * accumulator. It does not
+ * grow with the key length beyond one chunk. */
 SDPA_API size_t sdpa_fwd_workspace_size(const sdpa_problem* p);
 SDPA_API size_t sdpa_bwd_workspace_size(const sdpa_problem* p);
 
@@ -152,7 +173,11 @@ SDPA_API int sdpa_bwd(const sdpa_problem* p, const void* q, const void* k, const
              const int32_t* cu_seqlens_kv, void* workspace, size_t ws_bytes, void* stream);
 
 /* Synchronises `stream`, then returns and clears the current device's error
- * word (SDPA_OK if no kernel recorded an error). */
+ * word (SDPA_OK if no kernel recorded an error). The word records what the
+ * kernels detect on the device: cu_seqlens that break the compactness
+ * promise of TransformerEngine PR #3705 ("Execution and supported scope":
+ * zero-based cumulative lengths, checked on the GPU on every execution) as
+ * SDPA_ERR_BAD_SEQLENS, and a bounded wait that gave up as SDPA_ERR_TIMEOUT. */
 SDPA_API int sdpa_get_device_error(void* stream);
 
 /* Static description of a status code. */

@@ -50,7 +50,8 @@ class Problem(ctypes.Structure):
                                             "total_q", "total_kv", "num_heads_q", "num_heads_kv", "head_dim",
                                             "window_left", "window_right")] + [("softmax_scale", ctypes.c_float),
                                                                                ("deterministic", ctypes.c_int),
-                                                                               ("head_dim_v", ctypes.c_int)]
+                                                                               ("head_dim_v", ctypes.c_int),
+                                                                               ("kv_chunk", ctypes.c_int)]
 
 
 _lock = threading.Lock()
@@ -95,9 +96,11 @@ sdpa_error_string = error_string
 
 
 def make_problem(q, k, *, layout="bshd", mask="none", window=(-1, -1), scale=None, dtype=None, batch=None,
-                 max_seqlen_q=None, max_seqlen_kv=None, deterministic=False, head_dim_v=0) -> Problem:
+                 max_seqlen_q=None, max_seqlen_kv=None, deterministic=False, head_dim_v=0, kv_chunk=0) -> Problem:
     """sdpa_problem from tensor shapes (no device access). head_dim_v: the
-    width of V and O rows (0 = Q/K's head_dim)."""
+    width of V and O rows (0 = Q/K's head_dim). kv_chunk: key positions per
+    chunk of the head_dim 256/512 backward (a multiple of 128; 0 = the
+    library's choice)."""
     import torch
 
     if dtype is None:
@@ -122,6 +125,7 @@ def make_problem(q, k, *, layout="bshd", mask="none", window=(-1, -1), scale=Non
     p.softmax_scale = float(scale if scale is not None else d ** -0.5)
     p.deterministic = int(bool(deterministic))
     p.head_dim_v = int(head_dim_v)
+    p.kv_chunk = int(kv_chunk)
     return p
 
 
@@ -231,15 +235,16 @@ def sdpa_fwd(q, k, v, *, layout="bshd", mask="none", window=(-1, -1), scale=None
 
 def sdpa_bwd(q, k, v, o, lse, dout, *, layout="bshd", mask="none", window=(-1, -1), scale=None,
              cu_seqlens_q=None, cu_seqlens_kv=None, max_seqlen_q=None, max_seqlen_kv=None, dq=None, dk=None,
-             dv=None, workspace=None, stream=None, deterministic=False):
+             dv=None, workspace=None, stream=None, deterministic=False, kv_chunk=0):
     """Backward. Returns (dq, dk, dv). deterministic=True makes every
-    gradient bitwise reproducible run to run (see sdpa_problem.deterministic)."""
+    gradient bitwise reproducible run to run (see sdpa_problem.deterministic);
+    kv_chunk sets sdpa_problem.kv_chunk (head_dim 256/512)."""
     import torch
 
     batch = None if cu_seqlens_q is None else cu_seqlens_q.numel() - 1
     p = make_problem(q, k, layout=layout, mask=mask, window=window, scale=scale, batch=batch,
                      max_seqlen_q=max_seqlen_q, max_seqlen_kv=max_seqlen_kv, deterministic=deterministic,
-                     head_dim_v=v.shape[-1])
+                     head_dim_v=v.shape[-1], kv_chunk=kv_chunk)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv
@@ -259,7 +264,7 @@ def sdpa_bwd(q, k, v, o, lse, dout, *, layout="bshd", mask="none", window=(-1, -
 
 def sdpa_bwd_noalloc(q, k, v, o, lse, dout, *, layout="bshd", mask="none", window=(-1, -1), scale=None,
                      cu_seqlens_q=None, cu_seqlens_kv=None, max_seqlen_q=None, max_seqlen_kv=None, dq=None,
-                     dk=None, dv=None, stream=None, deterministic=False):
+                     dk=None, dv=None, stream=None, deterministic=False, kv_chunk=0):
     """Backward without a workspace: the library's static scratch array is
     used instead (for callers that cannot allocate device memory; problems
     needing more than NOALLOC_MAX_BYTES of scratch are rejected). Calls that
@@ -270,7 +275,7 @@ def sdpa_bwd_noalloc(q, k, v, o, lse, dout, *, layout="bshd", mask="none", windo
     batch = None if cu_seqlens_q is None else cu_seqlens_q.numel() - 1
     p = make_problem(q, k, layout=layout, mask=mask, window=window, scale=scale, batch=batch,
                      max_seqlen_q=max_seqlen_q, max_seqlen_kv=max_seqlen_kv, deterministic=deterministic,
-                     head_dim_v=v.shape[-1])
+                     head_dim_v=v.shape[-1], kv_chunk=kv_chunk)
     dq = torch.empty_like(q) if dq is None else dq
     dk = torch.empty_like(k) if dk is None else dk
     dv = torch.empty_like(v) if dv is None else dv

@@ -145,6 +145,7 @@ int check(const sdpa_problem* p) {
     return SDPA_ERR_UNSUPPORTED;
   if (!std::isfinite(p->softmax_scale)) return SDPA_ERR_INVALID_ARG;
   if (p->deterministic != 0 && p->deterministic != 1) return SDPA_ERR_INVALID_ARG;
+  if (p->kv_chunk < 0 || p->kv_chunk % 128) return SDPA_ERR_INVALID_ARG;
   if (p->layout == SDPA_THD) {
     if (p->total_q < 0 || p->total_kv < 0) return SDPA_ERR_INVALID_ARG;
   } else if (p->seqlen_q > 0 && p->seqlen_kv == 0 && p->batch > 0) {
@@ -210,12 +211,49 @@ int kv_slots(const sdpa_problem* p) {
   return nkt;
 }
 
+// Key-tile chunking of the head_dim 256/512 backward (bwd_big.cu): the P / dS
+// tile arrays hold one chunk of key tiles at a time, so their size does not
+// grow with the key length (TransformerEngine PR #3527, "Known limitations":
+// the prior art's workspace grows to 74 GiB at 64k tokens and caps the
+// context). A bounded (left, right) window already bounds the key tiles one
+// query tile sees; otherwise the chunk is as many key tiles as fit the
+// budget below (at least one).
+constexpr size_t kBwdTileBudget = size_t(512) << 20;
+
+struct BigPlan {
+  int chunk;   // key tiles per chunk
+  int slots;   // tile slots per (batch, q head, q tile)
+  int chunks;  // number of chunks
+};
+BigPlan big_plan(const sdpa_problem* p) {
+  const int nkt = (p->seqlen_kv + 127) / 128;
+  const int kvs = kv_slots(p);
+  const size_t tile_bytes = 2 * 32768;  // the P and dS images of one (query tile, key tile) pair
+  const size_t per_slot = (size_t)p->batch * p->num_heads_q * ((p->seqlen_q + 127) / 128) * tile_bytes;
+  const int wr = causal(p) ? 0 : p->window_right;
+  BigPlan pl;
+  if (p->kv_chunk > 0) {  // the caller's chunk
+    pl.chunk = std::max(1, std::min(nkt, p->kv_chunk / 128));
+    pl.slots = std::min(pl.chunk, kvs);
+  } else if ((p->window_left >= 0 && wr >= 0) || (size_t)kvs * per_slot <= kBwdTileBudget || nkt <= 1) {
+    pl.chunk = std::max(nkt, 1);
+    pl.slots = kvs;
+  } else {
+    pl.chunk = (int)std::max<size_t>(1, std::min<size_t>(kBwdTileBudget / std::max<size_t>(per_slot, 1), nkt));
+    pl.slots = std::min(pl.chunk, kvs);
+  }
+  pl.chunks = (nkt + pl.chunk - 1) / pl.chunk;
+  return pl;
+}
+
 // Backward workspace carve-up. head_dim 128: per-row statistics and the fp32
-// dQ accumulator. head_dim 256/512: statistics, the 16-bit P / dS tile
-// arrays and the fp32 dP - delta tiles.
+// dQ accumulator. head_dim 256/512: statistics, the fp32 dQ accumulator when
+// the key tiles are split into chunks, and the 16-bit P / dS tile arrays of
+// one chunk.
 struct BwdWs {
-  size_t guard_off, lse2_off, delta_off, acc_off, ptile_off, dstile_off, dpdtile_off, total;
+  size_t guard_off, lse2_off, delta_off, acc_off, ptile_off, dstile_off, total;
   int stat_rows;
+  bool has_acc;
 };
 BwdWs bwd_ws(const sdpa_problem* p) {
   int rq, rk, hq, hk;
@@ -235,19 +273,22 @@ BwdWs bwd_ws(const sdpa_problem* p) {
   w.lse2_off = 256;
   w.delta_off = round_up(w.lse2_off + (size_t)hq * w.stat_rows * 4, 256);
   const size_t after_stats = round_up(w.delta_off + (size_t)hq * w.stat_rows * 4, 256);
+  const size_t acc_bytes = (size_t)hq * rq * p->head_dim * 4;
   if (p->head_dim == 128) {
     // the deterministic backward writes dQ directly and needs no accumulator
     w.acc_off = after_stats;
-    w.ptile_off = w.dstile_off = w.dpdtile_off = 0;
-    w.total = p->deterministic ? after_stats : round_up(w.acc_off + (size_t)hq * rq * p->head_dim * 4, 256);
+    w.has_acc = !p->deterministic;
+    w.ptile_off = w.dstile_off = 0;
+    w.total = p->deterministic ? after_stats : round_up(w.acc_off + acc_bytes, 256);
   } else {
-    const size_t tiles = (size_t)p->batch * p->num_heads_q * ((p->seqlen_q + 127) / 128) * kv_slots(p);
-    w.acc_off = 0;
-    w.ptile_off = round_up(after_stats, 1024);
+    const BigPlan pl = big_plan(p);
+    const size_t tiles = (size_t)p->batch * p->num_heads_q * ((p->seqlen_q + 127) / 128) * pl.slots;
+    w.has_acc = pl.chunks > 1;
+    w.acc_off = after_stats;
+    const size_t after_acc = w.has_acc ? w.acc_off + acc_bytes : after_stats;
+    w.ptile_off = round_up(after_acc, 1024);
     w.dstile_off = w.ptile_off + tiles * 32768;
-    w.dpdtile_off = w.dstile_off + tiles * 32768;
-    // the fp32 dP - delta tiles exist only for head_dim 512 (256 forms dS in one pass)
-    w.total = w.dpdtile_off + (p->head_dim == 512 ? tiles * 65536 : 0);
+    w.total = w.dstile_off + tiles * 32768;
   }
   return w;
 }
@@ -401,7 +442,7 @@ int sdpa_bwd(const sdpa_problem* p, const void* q, const void* k, const void* v,
   pp.lse2 = lse2;
   pp.delta = delta;
   pp.stat_rows = w.stat_rows;
-  pp.dq_acc = (p->head_dim == 128 && !p->deterministic) ? acc : nullptr;
+  pp.dq_acc = w.has_acc ? acc : nullptr;
   pp.guard = guard;
   if ((rc = timed(SDPA_KERNEL_PREPROCESS, s, [&] { return launch_preprocess(pp, bf16, s); }))) return rc;
   ++launches;
@@ -412,7 +453,6 @@ int sdpa_bwd(const sdpa_problem* p, const void* q, const void* k, const void* v,
     B.p.g = g;
     B.p.p_tiles = ws + w.ptile_off;
     B.p.ds_tiles = ws + w.dstile_off;
-    B.p.dpd_tiles = ws + w.dpdtile_off;
     B.p.nlse2 = lse2;
     B.p.delta = delta;
     B.p.stat_rows = w.stat_rows;
@@ -423,7 +463,12 @@ int sdpa_bwd(const sdpa_problem* p, const void* q, const void* k, const void* v,
     B.p.guard = guard;
     B.p.n_q_tiles = (p->seqlen_q + 127) / 128;
     B.p.n_kv_tiles = (p->seqlen_kv + 127) / 128;
-    B.p.slots = kv_slots(p);
+    const BigPlan pl = big_plan(p);
+    B.p.slots = pl.slots;
+    B.p.chunk = pl.chunk;
+    B.p.chunk_lo = 0;
+    B.p.chunk_hi = B.p.n_kv_tiles;
+    B.p.dq_acc = w.has_acc ? acc : nullptr;
     B.stream = s;
     if ((rc = encode(&B.tmQ, q, p->head_dim, hq, rq, 128, bf16))) return rc;
     if ((rc = encode(&B.tmDO, dout, p->head_dim, hq, rq, 128, bf16))) return rc;
@@ -434,7 +479,13 @@ int sdpa_bwd(const sdpa_problem* p, const void* q, const void* k, const void* v,
     if ((rc = encode(&B.tmK64, k, p->head_dim, hk, rk, 64, bf16))) return rc;
     int n = 0;
     if ((rc = timed(SDPA_KERNEL_BWD, s, [&] { return launch_bwd_big(B, p->head_dim, bf16, &n); }))) return rc;
-    t_last_launches = launches + n;
+    launches += n;
+    if (w.has_acc) {  // dQ summed over the key-tile chunks: scale and convert once
+      if ((rc = timed(SDPA_KERNEL_DQ_FINALIZE, s, [&] { return launch_dq_finalize(g, acc, dq, guard, bf16, s); })))
+        return rc;
+      ++launches;
+    }
+    t_last_launches = launches;
     return SDPA_OK;
   }
 

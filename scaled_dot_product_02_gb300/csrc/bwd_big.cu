@@ -4,24 +4,36 @@
 // 2*D fp32 TMEM columns (512 or 1024) and do not fit next to the score
 // tiles, so the backward runs in two phases:
 //
-// Phase 1, score kernels (one CTA per 128-query tile of one (batch, q head));
-// for head_dim 256 one fused kernel (below) does both passes, for 512:
-//   pass 0: dP = dO V^T over the full head dim (dO resident in shared
-//           memory, V streamed in 128x128 chunks); dP - delta kept as fp32;
-//   pass 1: S = Q K^T likewise, P = exp2(S*scale*log2e - LSE*log2e) masked,
-//           dS = P * (dP - delta), P and dS written as 16-bit 128x128 tiles.
+// Phase 1, score kernels (one CTA per 128-query tile of one (batch, q head),
+// one kernel per head dim, below): S = Q K^T and dP = dO V^T over the full
+// head dim for each key tile, P = exp2(S*scale*log2e - LSE*log2e) masked and
+// dS = P * (dP - delta) in fp32, P and dS written as 16-bit 128x128 tiles.
 //   Each 16-bit tile is stored as the exact shared-memory image a tcgen05 operand
 //   wants (two 64-column atoms, 128-byte swizzle), so phase 2 fetches it with
-//   one 32 KB bulk copy. Tiles are indexed by (batch, head, query tile, slot)
-//   where slot = key tile - first key tile of that query tile; the host sizes
-//   the slot count from the mask (window and causal bounds).
+//   one 32 KB bulk copy.
 // Phase 2, GEMM kernels (accumulator 128 x 256 fp32 in TMEM, one CTA per
 // 256-column slice of the head dim), iterating only over unmasked tiles:
 //   MODE_DQ: dQ[q tile]  = scale * sum_t dS(q, t) K(t)
 //   MODE_DV: dV[kv tile] = sum_{heads of the group, q tiles} P^T dO
 //   MODE_DK: dK[kv tile] = scale * sum dS^T Q
 // Every FLOP executed is one the definition counts (10*D per unmasked pair),
-// at the cost of 8 bytes of workspace per pair, written once and read back.
+// at the cost of 4 bytes of workspace per pair, written once and read back.
+//
+// Bounded workspace (TransformerEngine PR #3527, "Known limitations": the
+// prior art's backward workspace grows from 1.6 GiB at 4k to 74 GiB at 64k
+// tokens and caps the context length). The key tiles are processed in chunks
+// [chunk_lo, chunk_hi): phase 1 then phase 2 per chunk, so the tile arrays
+// hold one chunk at a time, indexed by (batch, head, query tile, slot) with
+// slot = key tile - max(first key tile of the query tile, chunk_lo). The host
+// sizes the slot count from the mask (a bounded window's span) and from the
+// chunk length, never from the whole key range when that would exceed its
+// budget. dK and dV of a chunk's key tiles are final after the chunk; dQ of
+// a chunk is added (fp32 vector reduce-add, one per element per chunk, the
+// chunks ordered by the stream, so the sum is bitwise reproducible) into an
+// fp32 accumulator that a last pass scales and converts. With one chunk, dQ
+// is written directly.
+#include <algorithm>
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -58,6 +70,13 @@ __device__ __forceinline__ void kv_tiles_of(const KeyRange& kr, int q0, int lq, 
   n = hi > lo ? (hi + 127) / 128 - t_lo : 0;
 }
 
+// Restrict a query tile's key tiles [t_lo, t_lo + n) to this launch's chunk.
+__device__ __forceinline__ void chunk_clip(const BigBwdParams& p, int& t_lo, int& n) {
+  const int a = max(t_lo, p.chunk_lo), e = min(t_lo + n, p.chunk_hi);
+  t_lo = a;
+  n = max(0, e - a);
+}
+
 __device__ __forceinline__ long long tile_index(const BigBwdParams& p, int b, int h, int qt, int slot) {
   return (((long long)b * p.g.hq + h) * p.n_q_tiles + qt) * p.slots + slot;
 }
@@ -65,264 +84,6 @@ __device__ __forceinline__ long long tile_index(const BigBwdParams& p, int b, in
 }  // namespace
 
 // ====================================================================== phase 1
-template <int DQK>
-struct ScoreCfg {
-  static constexpr int A_BYTES = DQK * 256;  // 128 rows x DQK x 2 bytes
-  static constexpr int KST = DQK / 128;      // 32 KB stages per key tile
-  static constexpr int NST = DQK == 256 ? 3 : 2;
-  static constexpr int NBARS = 2 * NST + 6;
-  static constexpr int SMEM_BYTES = 1024 + A_BYTES + NST * CHUNK_BYTES + TILE_BYTES + NBARS * 8 + 16;
-};
-
-// MODE 0 (A = dO, B = V): writes dP - delta as an fp32 tile.
-// MODE 1 (A = Q,  B = K): P = exp2(S*scale*log2e - LSE*log2e) in fp32,
-//   dS = P * (dP - delta) from MODE 0's tile, and writes P and dS as 16-bit
-//   tile images (each rounded once, as in a fused backward).
-// The fp32 tile is laid out chunk-major, [32 chunks of 4 columns][128 rows]
-// x 16 bytes, so the thread that owns a row touches 16-byte pieces that are
-// contiguous across the warp.
-template <int DQK, int MODE, bool BF16>
-__global__ void __launch_bounds__(256, 1)
-    score_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                 const __grid_constant__ BigBwdParams p) {
-  using C = ScoreCfg<DQK>;
-  using E = Elem<BF16>;
-  const Geom& g = p.g;
-  int idx = blockIdx.x;
-  const int h = idx % g.hq;
-  idx /= g.hq;
-  const int b = idx % g.batch;
-  const int qt = p.n_q_tiles - 1 - idx / g.batch;
-  const SeqInfo si = seq_info(g, b);
-  const int q0 = qt * 128;
-  if (q0 >= si.lq) return;
-  if (p.guard && *reinterpret_cast<volatile const int*>(p.guard)) return;
-  const KeyRange kr = key_range(g, si.lq, si.lk);
-  int t_lo, n;
-  kv_tiles_of(kr, q0, si.lq, t_lo, n);
-  if (n > p.slots) {  // cannot happen with a host-sized workspace; refuse rather than overrun it
-    if (threadIdx.x == 0) record_error(p.err, SDPA_ERR_INVALID_ARG);
-    return;
-  }
-  const int qhead = si.qhead0 + h;
-  const int khead = si.khead0 + h / (g.hq / g.hkv);
-
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* sA = smem;
-  uint8_t* sStage = sA + C::A_BYTES;
-  uint8_t* sTile = sStage + C::NST * CHUNK_BYTES;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sTile + TILE_BYTES);
-  uint64_t* empty = full + C::NST;
-  uint64_t* bar_a = empty + C::NST;
-  uint64_t* bar_s = bar_a + 1;      // [2]
-  uint64_t* bar_sfree = bar_s + 2;  // [2]
-  uint64_t* bar_drain = bar_sfree + 2;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_drain + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-
-  if (threadIdx.x == 0) {
-    for (int i = 0; i < C::NST; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
-    }
-    mbar_init(bar_a, 1);
-    mbar_init(&bar_s[0], 1);
-    mbar_init(&bar_s[1], 1);
-    mbar_init(&bar_sfree[0], 128);
-    mbar_init(&bar_sfree[1], 128);
-    mbar_init(bar_drain, 1);
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  if (warp == 1) {
-    tmem_alloc(tmem_holder, 256);
-    tmem_relinquish();
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_holder;
-
-  if (warp == 0) {
-    if (elect_one() && n > 0) {
-      prefetch_tmap(&tmA);
-      prefetch_tmap(&tmB);
-      mbar_arrive_expect_tx(bar_a, C::A_BYTES);
-      for (int a = 0; a < DQK / 64; ++a) tma_load_3d(&tmA, bar_a, sA + a * 16384, a * 64, qhead, si.qrow0 + q0);
-      int c = 0;
-      bool ok = true;
-      for (int t = 0; t < n && ok; ++t) {
-        const int krow = si.krow0 + (t_lo + t) * 128;
-        for (int kb = 0; kb < C::KST; ++kb, ++c) {
-          const int slot = c % C::NST;
-          if (!mbar_wait(&empty[slot], ((c / C::NST) & 1) ^ 1, abort_flag)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(&full[slot], CHUNK_BYTES);
-          uint8_t* dst = sStage + slot * CHUNK_BYTES;
-          tma_load_3d(&tmB, &full[slot], dst, kb * 128, khead, krow);
-          tma_load_3d(&tmB, &full[slot], dst + 16384, kb * 128 + 64, khead, krow);
-        }
-      }
-      if (!ok) {
-        *abort_flag = 1;
-        record_error(p.err, SDPA_ERR_TIMEOUT);
-      }
-      const int first = c > C::NST ? c - C::NST : 0;
-      for (int k = first; k < c; ++k) mbar_wait_drain(&full[k % C::NST], (k / C::NST) & 1);
-      mbar_wait_drain(bar_a, 0);
-    }
-  } else if (warp == 1) {
-    if (elect_one() && n > 0) {
-      constexpr uint32_t IDESC = idesc_f16(128, 128, BF16, false, false);
-      bool ok = mbar_wait(bar_a, 0, abort_flag);
-      tc_fence_after();
-      const uint32_t a_base = smem_u32(sA);
-      int c = 0;
-      for (int t = 0; t < n && ok; ++t) {
-        const int buf = t & 1;
-        if (t >= 2 && !mbar_wait(&bar_sfree[buf], ((t >> 1) & 1) ^ 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        for (int kb = 0; kb < C::KST && ok; ++kb, ++c) {
-          const int slot = c % C::NST;
-          if (!mbar_wait(&full[slot], (c / C::NST) & 1, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t bb = smem_u32(sStage + slot * CHUNK_BYTES);
-          const uint32_t aa = a_base + kb * 2 * 16384;
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-            mma_ss(tmem + buf * 128, smem_desc_sw128(aa + off, 16, 1024), smem_desc_sw128(bb + off, 16, 1024),
-                   IDESC, (kb | ks) != 0);
-          }
-          mma_commit(&empty[slot]);
-        }
-        if (ok) mma_commit(&bar_s[buf]);
-      }
-      if (!ok) {
-        *abort_flag = 1;
-        record_error(p.err, SDPA_ERR_TIMEOUT);
-        mma_commit(bar_drain);
-        mbar_wait_drain(bar_drain, 0);
-      }
-    }
-  } else if (warp >= 4) {
-    const int wq = warp - 4;
-    const int r = wq * 32 + lane;
-    const int i = q0 + r;
-    const bool valid = i < si.lq;
-    const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
-    const long long stat = (long long)qhead * p.stat_rows + si.srow0 + i;
-    // rows past the sequence end belong to no query: their P (and so dS) is zero
-    const float nl2 = valid ? p.nlse2[stat] : -INFINITY;
-    const float dl = valid ? p.delta[stat] : 0.f;
-    const int lo_i = kr.lo(i), hi_i = kr.hi(i);
-    const float sl2 = g.scale_log2;
-    const bool leader = threadIdx.x == 128;
-    bool ok = true;
-    for (int t = 0; t < n; ++t) {
-      const int buf = t & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&bar_s[buf], (t >> 1) & 1, abort_flag))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const long long tix = tile_index(p, b, h, qt, t);
-      float4* dpd = reinterpret_cast<float4*>(p.dpd_tiles + tix * (2 * TILE_BYTES)) + r;
-      const int kbase = (t_lo + t) * 128;
-      uint32_t dsk[64];  // MODE 1: packed dS of the whole row, written after P
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {  // 64 keys at a time
-        uint32_t u0[32], u1[32];
-        tmem_ld32(lane_base + buf * 128 + half * 64, u0);
-        tmem_ld32(lane_base + buf * 128 + half * 64 + 32, u1);
-        tmem_wait_ld();
-        reg_fence(u0);
-        reg_fence(u1);
-        if (half == 1) {
-          tc_fence_before();
-          mbar_arrive(&bar_sfree[buf]);
-        }
-        if (MODE == 0) {
-#pragma unroll
-          for (int c4 = 0; c4 < 16; ++c4) {
-            const uint32_t* u = c4 < 8 ? &u0[c4 * 4] : &u1[(c4 - 8) * 4];
-            dpd[(half * 16 + c4) * 128] = make_float4(__uint_as_float(u[0]) - dl, __uint_as_float(u[1]) - dl,
-                                                      __uint_as_float(u[2]) - dl, __uint_as_float(u[3]) - dl);
-          }
-        } else {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {  // 8 chunks of 8 keys
-            const float4 d0 = dpd[(half * 16 + 2 * k) * 128];
-            const float4 d1 = dpd[(half * 16 + 2 * k + 1) * 128];
-            const float dv[8] = {d0.x, d0.y, d0.z, d0.w, d1.x, d1.y, d1.z, d1.w};
-            uint32_t w4[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int c0 = k * 8 + 2 * e;  // column within this 64-key half
-              const uint32_t x0 = c0 < 32 ? u0[c0] : u1[c0 - 32];
-              const uint32_t x1 = c0 + 1 < 32 ? u0[c0 + 1] : u1[c0 + 1 - 32];
-              const int key = kbase + half * 64 + c0;
-              float p0 = ex2(fmaf(__uint_as_float(x0), sl2, nl2));
-              float p1 = ex2(fmaf(__uint_as_float(x1), sl2, nl2));
-              p0 = in_range(key, lo_i, hi_i) ? p0 : 0.f;
-              p1 = in_range(key + 1, lo_i, hi_i) ? p1 : 0.f;
-              w4[e] = E::pack(p0, p1);
-              dsk[half * 32 + k * 4 + e] = E::pack(p0 * dv[2 * e], p1 * dv[2 * e + 1]);
-            }
-            *reinterpret_cast<uint4*>(sTile + tile_chunk_off(r, half * 8 + k)) =
-                make_uint4(w4[0], w4[1], w4[2], w4[3]);
-          }
-        }
-      }
-      if (MODE == 1) {
-        // P image out, then the dS image through the same buffer
-        fence_proxy_async_smem();
-        named_bar_sync(1, 128);
-        if (leader) {
-          bulk_store(p.p_tiles + tix * TILE_BYTES, sTile, TILE_BYTES);
-          bulk_commit_group();
-          bulk_wait_group_read0();
-        }
-        named_bar_sync(1, 128);
-#pragma unroll
-        for (int k16 = 0; k16 < 16; ++k16)
-          *reinterpret_cast<uint4*>(sTile + tile_chunk_off(r, k16)) =
-              make_uint4(dsk[4 * k16], dsk[4 * k16 + 1], dsk[4 * k16 + 2], dsk[4 * k16 + 3]);
-        fence_proxy_async_smem();
-        named_bar_sync(1, 128);
-        if (leader) {
-          bulk_store(p.ds_tiles + tix * TILE_BYTES, sTile, TILE_BYTES);
-          bulk_commit_group();
-          bulk_wait_group_read0();
-        }
-        named_bar_sync(1, 128);  // the buffer is free again for the next tile
-      }
-    }
-    if (leader) bulk_wait_group0();
-    if (!ok) {
-      *abort_flag = 1;
-      record_error(p.err, SDPA_ERR_TIMEOUT);
-    }
-  }
-
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    tc_fence_after();
-    tmem_dealloc(tmem, 256);
-  }
-}
-
 // ---------------------------------------------------------------------- head_dim 256
 // Both passes in one kernel. Q and dO of the query tile live in TMEM as the A
 // operands of S = Q K^T and dP = dO V^T (columns 0-255), so shared memory is
@@ -361,6 +122,7 @@ __global__ void __launch_bounds__(SF_THREADS, 1)
   const KeyRange kr = key_range(g, si.lq, si.lk);
   int t_lo, n;
   kv_tiles_of(kr, q0, si.lq, t_lo, n);
+  chunk_clip(p, t_lo, n);
   if (n > p.slots) {
     if (threadIdx.x == 0) record_error(p.err, SDPA_ERR_INVALID_ARG);
     return;
@@ -600,6 +362,306 @@ __global__ void __launch_bounds__(SF_THREADS, 1)
   }
 }
 
+// ---------------------------------------------------------------------- head_dim 512
+// Both passes in one kernel. A 128 x 512 operand is 128 KB, so Q and dO
+// cannot both stay in shared memory, nor both in TMEM: Q is copied into TMEM
+// (columns 0-255, the A operand of S = Q K^T) and dO stays in shared memory
+// (the A operand of dP = dO V^T), which leaves TMEM columns 256-383 for S and
+// 384-511 for dP, and 96 KB of shared memory for a ring of six 16 KB K/V
+// chunks. Q arrives first in the 128 KB buffer that dO then occupies: the
+// epilogue threads copy it into TMEM and only then does the producer load dO
+// over it. S and dP are single-buffered but released separately, so S of the
+// next key tile is computed while the epilogue waits for dP of this one. Two
+// epilogue warpgroups each take 64 keys of a tile and form P and dS in fp32
+// (each rounded once); with no shared memory left to stage them, each thread
+// stores its row's 16-byte pieces of the two tile images directly. Nothing
+// fp32 goes through HBM.
+constexpr int S5_CH = 16384;  // ring chunk: 128 rows x 64 columns (one box)
+constexpr int S5_NST = 6;
+constexpr int S5_A = 8 * S5_CH;  // Q, then dO: eight 64-column atoms
+constexpr int S5_NBARS = 2 * S5_NST + 8;
+constexpr int S5_SMEM = 1024 + S5_A + S5_NST * S5_CH + S5_NBARS * 8 + 16;
+constexpr int S5_THREADS = 320;  // producer, MMA, two epilogue warpgroups (warps 2-5, 6-9)
+constexpr int S5_TM_Q = 0, S5_TM_S = 256, S5_TM_DP = 384;
+static_assert(S5_SMEM <= 232448, "the head_dim 512 score kernel must fit one CTA's shared memory");
+
+template <bool BF16>
+__global__ void __launch_bounds__(S5_THREADS, 1)
+    score_fused512_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmDO,
+                          const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                          const __grid_constant__ BigBwdParams p) {
+  using E = Elem<BF16>;
+  const Geom& g = p.g;
+  int idx = blockIdx.x;
+  const int h = idx % g.hq;
+  idx /= g.hq;
+  const int b = idx % g.batch;
+  const int qt = p.n_q_tiles - 1 - idx / g.batch;
+  const SeqInfo si = seq_info(g, b);
+  const int q0 = qt * 128;
+  if (q0 >= si.lq) return;
+  if (p.guard && *reinterpret_cast<volatile const int*>(p.guard)) return;
+  const KeyRange kr = key_range(g, si.lq, si.lk);
+  int t_lo, n;
+  kv_tiles_of(kr, q0, si.lq, t_lo, n);
+  chunk_clip(p, t_lo, n);
+  if (n > p.slots) {
+    if (threadIdx.x == 0) record_error(p.err, SDPA_ERR_INVALID_ARG);
+    return;
+  }
+  if (n == 0) return;
+  const int qhead = si.qhead0 + h;
+  const int khead = si.khead0 + h / (g.hq / g.hkv);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* sA = smem;                // Q, then dO
+  uint8_t* sRing = sA + S5_A;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sRing + S5_NST * S5_CH);
+  uint64_t* empty = full + S5_NST;
+  uint64_t* bar_qa = empty + S5_NST;  // Q has landed in sA
+  uint64_t* bar_q = bar_qa + 1;       // Q is in TMEM (and sA may be overwritten)
+  uint64_t* bar_do = bar_q + 1;       // dO has landed in sA
+  uint64_t* bar_s = bar_do + 1;       // S of a key tile ready
+  uint64_t* bar_dp = bar_s + 1;       // dP of a key tile ready
+  uint64_t* free_s = bar_dp + 1;      // the epilogue has read S
+  uint64_t* free_dp = free_s + 1;     // ... and dP
+  uint64_t* bar_drain = free_dp + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S5_NST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(bar_qa, 1);
+    mbar_init(bar_q, 256);
+    mbar_init(bar_do, 1);
+    mbar_init(bar_s, 1);
+    mbar_init(bar_dp, 1);
+    mbar_init(free_s, 256);
+    mbar_init(free_dp, 256);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  // ring chunk c: key tile c / 16, K columns 64 (c % 16) for c % 16 < 8, then V
+  if (warp == 0) {
+    if (elect_one()) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmDO);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmV);
+      mbar_arrive_expect_tx(bar_qa, S5_A);
+      for (int a = 0; a < 8; ++a) tma_load_3d(&tmQ, bar_qa, sA + a * S5_CH, a * 64, qhead, si.qrow0 + q0);
+      const int total = 16 * n;
+      bool do_issued = false, ok = true;
+      int c = 0;
+      for (; c < total && ok; ++c) {
+        if (c == S5_NST && !do_issued) {
+          // the first ring fill is in flight: once Q has left sA, bring dO in
+          if (!mbar_wait(bar_q, 0, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar_do, S5_A);
+          for (int a = 0; a < 8; ++a) tma_load_3d(&tmDO, bar_do, sA + a * S5_CH, a * 64, qhead, si.qrow0 + q0);
+          do_issued = true;
+        }
+        const int slot = c % S5_NST;
+        if (!mbar_wait(&empty[slot], ((c / S5_NST) & 1) ^ 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&full[slot], S5_CH);
+        const int t = c >> 4, kc = c & 15;
+        tma_load_3d(kc < 8 ? &tmK : &tmV, &full[slot], sRing + slot * S5_CH, (kc & 7) * 64, khead,
+                    si.krow0 + (t_lo + t) * 128);
+      }
+      if (ok && !do_issued) {  // fewer ring chunks than slots
+        if (mbar_wait(bar_q, 0, abort_flag)) {
+          mbar_arrive_expect_tx(bar_do, S5_A);
+          for (int a = 0; a < 8; ++a) tma_load_3d(&tmDO, bar_do, sA + a * S5_CH, a * 64, qhead, si.qrow0 + q0);
+          do_issued = true;
+        } else {
+          ok = false;
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        record_error(p.err, SDPA_ERR_TIMEOUT);
+      }
+      const int first = c > S5_NST ? c - S5_NST : 0;
+      for (int k = first; k < c; ++k) mbar_wait_drain(&full[k % S5_NST], (k / S5_NST) & 1);
+      mbar_wait_drain(bar_qa, 0);
+      if (do_issued) mbar_wait_drain(bar_do, 0);
+    }
+  } else if (warp == 1) {
+    if (elect_one()) {
+      constexpr uint32_t IDESC = idesc_f16(128, 128, BF16, false, false);
+      bool ok = mbar_wait(bar_q, 0, abort_flag);
+      tc_fence_after();
+      const uint32_t a_base = smem_u32(sA);
+      int c = 0;
+      for (int t = 0; t < n && ok; ++t) {
+        for (int pass = 0; pass < 2 && ok; ++pass) {  // S = Q K^T (A in TMEM), then dP = dO V^T (A in sA)
+          if (t >= 1 && !mbar_wait(pass == 0 ? free_s : free_dp, (t - 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          if (pass == 1 && t == 0 && !mbar_wait(bar_do, 0, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem + (pass == 0 ? S5_TM_S : S5_TM_DP);
+          for (int kc = 0; kc < 8; ++kc, ++c) {
+            const int slot = c % S5_NST;
+            if (!mbar_wait(&full[slot], (c / S5_NST) & 1, abort_flag)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t bb = smem_u32(sRing + slot * S5_CH);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) {
+              if (pass == 0)
+                mma_ts(d, tmem + S5_TM_Q + kc * 32 + ks * 8, smem_desc_sw128(bb + ks * 32, 16, 1024), IDESC,
+                       (kc | ks) != 0);
+              else
+                mma_ss(d, smem_desc_sw128(a_base + kc * S5_CH + ks * 32, 16, 1024),
+                       smem_desc_sw128(bb + ks * 32, 16, 1024), IDESC, (kc | ks) != 0);
+            }
+            mma_commit(&empty[slot]);
+          }
+          if (ok) mma_commit(pass == 0 ? bar_s : bar_dp);
+        }
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        record_error(p.err, SDPA_ERR_TIMEOUT);
+        mma_commit(bar_drain);
+        mbar_wait_drain(bar_drain, 0);
+      }
+    }
+  } else if (warp >= 2) {
+    const int grp = (warp - 2) >> 2;  // 64-key half of each tile; for the TMEM fill, Q atoms 4*grp..
+    const int wq = warp & 3;          // TMEM lane quarter this warp may access
+    const int r = wq * 32 + lane;
+    const int i = q0 + r;
+    const bool valid = i < si.lq;
+    const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
+    bool ok = __all_sync(0xffffffffu, mbar_wait(bar_qa, 0, abort_flag));
+    if (ok) {
+      // row r of Q atoms 4*grp..4*grp+3 -> TMEM columns 32*atom.., packed pairs along D
+      for (int a = 4 * grp; a < 4 * grp + 4; ++a) {
+        const uint8_t* row = sA + a * S5_CH + r * 128;
+        uint32_t v[32];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const uint4 x = *reinterpret_cast<const uint4*>(row + ((j ^ (r & 7)) << 4));
+          v[4 * j] = x.x;
+          v[4 * j + 1] = x.y;
+          v[4 * j + 2] = x.z;
+          v[4 * j + 3] = x.w;
+        }
+        tmem_st32(lane_base + S5_TM_Q + a * 32, v);
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar_q);
+    }
+    const long long stat = (long long)qhead * p.stat_rows + si.srow0 + i;
+    // rows past the sequence end belong to no query: an empty key range, so
+    // their P and dS are exactly zero whatever their scores
+    const float nl2 = valid ? p.nlse2[stat] : 0.f;
+    const float dl = valid ? p.delta[stat] : 0.f;
+    const int lo_i = kr.lo(i), hi_i = valid ? kr.hi(i) : lo_i;
+    const float sl2 = g.scale_log2;
+    for (int t = 0; t < n && ok; ++t) {
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_s, t & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const int kbase = (t_lo + t) * 128 + grp * 64;
+      const long long tix = tile_index(p, b, h, qt, t);
+      // this thread's row of this group's 64-key atom in the two tile images
+      uint8_t* prow = p.p_tiles + tix * TILE_BYTES + grp * 16384 + r * 128;
+      uint8_t* drow = p.ds_tiles + tix * TILE_BYTES + grp * 16384 + r * 128;
+      float pv[64];
+      {
+        uint32_t u[64];
+        tmem_ld32(lane_base + S5_TM_S + grp * 64, *reinterpret_cast<uint32_t(*)[32]>(u));
+        tmem_ld32(lane_base + S5_TM_S + grp * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(u + 32));
+        tmem_wait_ld();
+        reg_fence(*reinterpret_cast<uint32_t(*)[32]>(u));
+        reg_fence(*reinterpret_cast<uint32_t(*)[32]>(u + 32));
+        tc_fence_before();
+        mbar_arrive(free_s);
+#pragma unroll
+        for (int c0 = 0; c0 < 64; ++c0) {
+          const float e = ex2(fmaf(__uint_as_float(u[c0]), sl2, nl2));
+          pv[c0] = in_range(kbase + c0, lo_i, hi_i) ? e : 0.f;
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        *reinterpret_cast<uint4*>(prow + ((k ^ (r & 7)) << 4)) =
+            make_uint4(E::pack(pv[8 * k], pv[8 * k + 1]), E::pack(pv[8 * k + 2], pv[8 * k + 3]),
+                       E::pack(pv[8 * k + 4], pv[8 * k + 5]), E::pack(pv[8 * k + 6], pv[8 * k + 7]));
+      if (!__all_sync(0xffffffffu, mbar_wait(bar_dp, t & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      {
+        uint32_t u[64];
+        tmem_ld32(lane_base + S5_TM_DP + grp * 64, *reinterpret_cast<uint32_t(*)[32]>(u));
+        tmem_ld32(lane_base + S5_TM_DP + grp * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(u + 32));
+        tmem_wait_ld();
+        reg_fence(*reinterpret_cast<uint32_t(*)[32]>(u));
+        reg_fence(*reinterpret_cast<uint32_t(*)[32]>(u + 32));
+        tc_fence_before();
+        mbar_arrive(free_dp);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          uint32_t w[4];
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c0 = 8 * k + 2 * e;
+            // pv is exactly zero outside the mask, so dS is too (for finite dP)
+            w[e] = E::pack(pv[c0] * (__uint_as_float(u[c0]) - dl), pv[c0 + 1] * (__uint_as_float(u[c0 + 1]) - dl));
+          }
+          *reinterpret_cast<uint4*>(drow + ((k ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        }
+      }
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      record_error(p.err, SDPA_ERR_TIMEOUT);
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 // ====================================================================== phase 2
 // A stage is half a K step: 64 of the 128 contracted rows, i.e. half a tile
 // image (16 KB) and 64 rows x 256 columns of B (32 KB). At 48 KB a stage two
@@ -610,15 +672,15 @@ constexpr int GB_NST = 2;
 constexpr int GB_NBARS = 2 * GB_NST + 3;
 constexpr int GB_SMEM = 1024 + GB_NST * GB_STAGE + GB_NBARS * 8 + 16;
 
-// MODE 0: dQ. MODE 1: dV. MODE 2: dK.
+// One output tile of one mode. MODE 0: dQ. MODE 1: dV. MODE 2: dK. `idx`
+// numbers the tiles of that mode; tmB is the mode's B operand (K, dO or Q
+// with 64-row boxes).
 template <int MODE, bool BF16>
-__global__ void __launch_bounds__(256, 2)
-    gemm_kernel(const __grid_constant__ CUtensorMap tmB, const __grid_constant__ BigBwdParams p) {
+__device__ __forceinline__ void gemm_tile(const CUtensorMap* tmB, const BigBwdParams& p, int idx) {
   using E = Elem<BF16>;
   using T = typename E::T;
   const Geom& g = p.g;
   const int splits = g.d / 256;
-  int idx = blockIdx.x;
   int split, b, head, t_own;  // head: q head (dQ) or kv head (dV/dK); t_own: own 128-row tile
   if (MODE == 0) {
     split = idx % splits;
@@ -628,8 +690,9 @@ __global__ void __launch_bounds__(256, 2)
     b = idx % g.batch;
     t_own = p.n_q_tiles - 1 - idx / g.batch;
   } else {
-    t_own = idx % p.n_kv_tiles;
-    idx /= p.n_kv_tiles;
+    const int chunk_tiles = p.chunk_hi - p.chunk_lo;  // the key tiles of this chunk
+    t_own = p.chunk_lo + idx % chunk_tiles;
+    idx /= chunk_tiles;
     split = idx % splits;
     idx /= splits;
     head = idx % g.hkv;
@@ -645,6 +708,9 @@ __global__ void __launch_bounds__(256, 2)
   int t_lo = 0, n = 0, qt_lo = 0, nqt = 0;
   if (MODE == 0) {
     kv_tiles_of(kr, r0, si.lq, t_lo, n);
+    chunk_clip(p, t_lo, n);
+    // a split key range adds each chunk's part into the accumulator: nothing to add
+    if (p.dq_acc && n == 0) return;
   } else {
     const int k_last = min(r0 + 127, si.lk - 1);
     const int qlo = query_lo(kr, r0), qhi = query_hi(kr, k_last, si.lq);
@@ -675,7 +741,7 @@ __global__ void __launch_bounds__(256, 2)
       const int qt = qt_lo + s % nqt;
       int tl, tn;
       kv_tiles_of(kr, qt * 128, si.lq, tl, tn);
-      a_tile = tile_index(p, b, h, qt, t_own - tl);
+      a_tile = tile_index(p, b, h, qt, t_own - max(tl, p.chunk_lo));
       b_row = si.qrow0 + qt * 128;
       b_head = si.qhead0 + h;
     }
@@ -702,7 +768,7 @@ __global__ void __launch_bounds__(256, 2)
 
   if (warp == 0) {
     if (elect_one() && n > 0) {
-      prefetch_tmap(&tmB);
+      prefetch_tmap(tmB);
       int s = 0;
       for (; s < 2 * n; ++s) {  // half steps
         const int st = s % GB_NST;
@@ -721,7 +787,7 @@ __global__ void __launch_bounds__(256, 2)
           bulk_load(dst + 8192, src + 16384 + hf * 8192, 8192, &full[st]);
         }
         for (int a = 0; a < 4; ++a)
-          tma_load_3d(&tmB, &full[st], dst + TILE_BYTES / 2 + a * 8192, split * 256 + a * 64, bh, brow + hf * 64);
+          tma_load_3d(tmB, &full[st], dst + TILE_BYTES / 2 + a * 8192, split * 256 + a * 64, bh, brow + hf * 64);
       }
       if (s < 2 * n) {
         *abort_flag = 1;
@@ -791,6 +857,24 @@ __global__ void __launch_bounds__(256, 2)
         valid = row < si.lk;
       }
       out += split * 256;
+      if (MODE == 0 && p.dq_acc) {
+        // key range split into chunks: add this chunk's unscaled part into the
+        // head-major fp32 accumulator (the dQ finalise scales and converts it)
+        float* acc = p.dq_acc + ((long long)(si.qhead0 + head) * g.rows_q + si.qrow0 + row) * g.d + split * 256;
+#pragma unroll 1
+        for (int c = 0; c < 256 / 32; ++c) {
+          uint32_t u[32];
+          tmem_ld32(lane_base + c * 32, u);
+          tmem_wait_ld();
+          reg_fence(u);
+          if (valid) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              red_add_v4_f32(acc + c * 32 + 4 * e, __uint_as_float(u[4 * e]), __uint_as_float(u[4 * e + 1]),
+                             __uint_as_float(u[4 * e + 2]), __uint_as_float(u[4 * e + 3]));
+          }
+        }
+      } else {
 #pragma unroll 1
       for (int c = 0; c < 256 / 32; ++c) {
         uint32_t packed[16];
@@ -813,6 +897,7 @@ __global__ void __launch_bounds__(256, 2)
             d4[e] = make_uint4(packed[4 * e], packed[4 * e + 1], packed[4 * e + 2], packed[4 * e + 3]);
         }
       }
+      }
     }
   }
 
@@ -824,6 +909,24 @@ __global__ void __launch_bounds__(256, 2)
   }
 }
 
+// Phase 2 of one chunk in one launch: the dV tiles, then the dK tiles (the
+// longer K-loops, over every q head of the group and every query tile that
+// sees the key tile), then the dQ tiles. The three modes only read the
+// chunk's P / dS images and Q, dO, K, so they run side by side and the grid
+// fills the GPU even when a chunk holds few key tiles.
+template <bool BF16>
+__global__ void __launch_bounds__(256, 2)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmK64, const __grid_constant__ CUtensorMap tmDO64,
+                const __grid_constant__ CUtensorMap tmQ64, const __grid_constant__ BigBwdParams p, int n_kv_ctas) {
+  const int idx = blockIdx.x;
+  if (idx < n_kv_ctas)
+    gemm_tile<1, BF16>(&tmDO64, p, idx);
+  else if (idx < 2 * n_kv_ctas)
+    gemm_tile<2, BF16>(&tmQ64, p, idx - n_kv_ctas);
+  else
+    gemm_tile<0, BF16>(&tmK64, p, idx - 2 * n_kv_ctas);
+}
+
 // ====================================================================== launch
 template <class K>
 static bool set_smem(K kern, int bytes) {
@@ -832,40 +935,36 @@ static bool set_smem(K kern, int bytes) {
 
 template <int DQK, bool BF16>
 static int launch_big_t(const BigBwdLaunch& L, int* launches) {
-  const BigBwdParams& p = L.p;
-  const long long g1 = (long long)p.n_q_tiles * p.g.hq * p.g.batch;
-  const long long gq = g1 * (p.g.d / 256);
-  const long long gkv = (long long)p.n_kv_tiles * (p.g.d / 256) * p.g.hkv * p.g.batch;
-  if (g1 > 0x7fffffffLL || gq > 0x7fffffffLL || gkv > 0x7fffffffLL) return SDPA_ERR_UNSUPPORTED;
-  auto m0 = gemm_kernel<0, BF16>;
-  auto m1 = gemm_kernel<1, BF16>;
-  auto m2 = gemm_kernel<2, BF16>;
-  if (!set_smem(m0, GB_SMEM) || !set_smem(m1, GB_SMEM) || !set_smem(m2, GB_SMEM)) return SDPA_ERR_CUDA;
+  const BigBwdParams& p0 = L.p;
+  const int splits = p0.g.d / 256;
+  const long long g1 = (long long)p0.n_q_tiles * p0.g.hq * p0.g.batch;
+  const long long gq = g1 * splits;
+  const long long gkv = (long long)std::min(p0.chunk, p0.n_kv_tiles) * splits * p0.g.hkv * p0.g.batch;
+  if (g1 > 0x7fffffffLL || gq + 2 * gkv > 0x7fffffffLL) return SDPA_ERR_UNSUPPORTED;
+  if (p0.chunk <= 0 || (p0.chunk < p0.n_kv_tiles && !p0.dq_acc)) return SDPA_ERR_INVALID_ARG;
+  auto gm = gemm_kernel<BF16>;
+  if (!set_smem(gm, GB_SMEM)) return SDPA_ERR_CUDA;
+  auto sf = DQK == 256 ? score_fused256_kernel<BF16> : score_fused512_kernel<BF16>;
+  const int sf_smem = DQK == 256 ? SF_SMEM : S5_SMEM;
+  const int sf_threads = DQK == 256 ? SF_THREADS : S5_THREADS;
+  if (!set_smem(sf, sf_smem)) return SDPA_ERR_CUDA;
   int n = 0;
-  if (g1 > 0) {
-    if constexpr (DQK == 256) {
-      // one fused score kernel: P and dS from resident Q and dO
-      auto sf = score_fused256_kernel<BF16>;
-      if (!set_smem(sf, SF_SMEM)) return SDPA_ERR_CUDA;
-      sf<<<(unsigned)g1, SF_THREADS, SF_SMEM, L.stream>>>(L.tmQ, L.tmDO, L.tmK, L.tmV, p);
+  // one chunk of key tiles at a time: phase 1 writes its P / dS tiles, phase 2
+  // consumes them before the next chunk's phase 1 overwrites the arrays
+  for (int lo = 0; lo < p0.n_kv_tiles; lo += p0.chunk) {
+    BigBwdParams p = p0;
+    p.chunk_lo = lo;
+    p.chunk_hi = std::min(lo + p0.chunk, p0.n_kv_tiles);
+    const long long gkv_c = (long long)(p.chunk_hi - p.chunk_lo) * splits * p.g.hkv * p.g.batch;
+    if (g1 > 0) {  // phase 1: P and dS tiles of this chunk from S and dP
+      sf<<<(unsigned)g1, sf_threads, sf_smem, L.stream>>>(L.tmQ, L.tmDO, L.tmK, L.tmV, p);
       n += 1;
-    } else {
-      // two passes: dP - delta as fp32 tiles, then P and dS
-      using C = ScoreCfg<DQK>;
-      auto s0 = score_kernel<DQK, 0, BF16>;
-      auto s1 = score_kernel<DQK, 1, BF16>;
-      if (!set_smem(s0, C::SMEM_BYTES) || !set_smem(s1, C::SMEM_BYTES)) return SDPA_ERR_CUDA;
-      s0<<<(unsigned)g1, 256, C::SMEM_BYTES, L.stream>>>(L.tmDO, L.tmV, p);
-      s1<<<(unsigned)g1, 256, C::SMEM_BYTES, L.stream>>>(L.tmQ, L.tmK, p);
-      n += 2;
     }
-    m0<<<(unsigned)gq, 256, GB_SMEM, L.stream>>>(L.tmK64, p);
-    n += 1;
-  }
-  if (gkv > 0) {
-    m1<<<(unsigned)gkv, 256, GB_SMEM, L.stream>>>(L.tmDO64, p);
-    m2<<<(unsigned)gkv, 256, GB_SMEM, L.stream>>>(L.tmQ64, p);
-    n += 2;
+    const long long g2 = 2 * gkv_c + (g1 > 0 ? gq : 0);
+    if (g2 > 0) {  // phase 2: dV, dK of the chunk's key tiles, its part of dQ
+      gm<<<(unsigned)g2, 256, GB_SMEM, L.stream>>>(L.tmK64, L.tmDO64, L.tmQ64, p, (int)gkv_c);
+      n += 1;
+    }
   }
   *launches = n;
   return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;

@@ -82,9 +82,8 @@ int launch_dq128(const DqLaunch& L, bool bf16);
 // dS tiles, GEMM kernels form dQ, dV, dK from them.
 struct BigBwdParams {
   Geom g;
-  uint8_t* p_tiles;      // [B][Hq][n_q_tiles][slots] 32 KB tile images
+  uint8_t* p_tiles;      // [B][Hq][n_q_tiles][slots] 32 KB tile images of one key-tile chunk
   uint8_t* ds_tiles;     // same shape
-  uint8_t* dpd_tiles;    // same shape, 64 KB fp32 tiles of dP - delta
   const float* nlse2;    // [nh_q][stat_rows] -LSE * log2(e)
   const float* delta;    // [nh_q][stat_rows]
   int stat_rows;
@@ -94,6 +93,10 @@ struct BigBwdParams {
   int* err;
   const int* guard;
   int n_q_tiles, n_kv_tiles, slots;
+  int chunk_lo, chunk_hi;  // key tiles [chunk_lo, chunk_hi) of this launch set
+  int chunk;               // key tiles per chunk (the last chunk may be shorter)
+  float* dq_acc;           // [nh_q][rows_q][D] fp32 dQ sum over chunks, zeroed by the
+                           // preprocess; nullptr when one chunk covers every key tile
 };
 
 struct BigBwdLaunch {

@@ -155,6 +155,12 @@ __device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, const void* ssr
                "r"(smem_u32(ssrc)), "r"(bytes)
                : "memory");
 }
+// Four fp32 reduce-adds into 16 aligned bytes of global memory (one L2
+// transaction; no return value).
+__device__ __forceinline__ void red_add_v4_f32(float* gdst, float a, float b, float c, float d) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(gdst), "f"(a), "f"(b), "f"(c), "f"(d)
+               : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_group_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");

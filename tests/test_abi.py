@@ -50,7 +50,7 @@ def problem(pkg, **kw):
     p = pkg.Problem()
     base = dict(layout=0, dtype=0, mask_type=1, batch=2, seqlen_q=256, seqlen_kv=256, total_q=0, total_kv=0,
                 num_heads_q=8, num_heads_kv=2, head_dim=128, window_left=-1, window_right=-1, softmax_scale=0.088,
-                deterministic=0)
+                deterministic=0, kv_chunk=0)
     base.update(kw)
     for k, v in base.items():
         setattr(p, k, v)
@@ -129,6 +129,42 @@ def test_workspace_sizes(pkg):
     # the deterministic head_dim 128 backward writes dQ directly: no fp32 accumulator
     det = pkg.sdpa_bwd_workspace_size(problem(pkg, deterministic=1))
     assert 0 < det < ws and ws - det >= 2 * 256 * 8 * 128 * 4
+
+
+def test_kv_chunk_is_validated(pkg):
+    for bad in (-128, 1, 100, 129):
+        assert pkg.sdpa_check_problem(problem(pkg, head_dim=512, kv_chunk=bad)) == 1
+    for good in (0, 128, 1024):
+        assert pkg.sdpa_check_problem(problem(pkg, head_dim=512, kv_chunk=good)) == 0
+
+
+@pytest.mark.parametrize("d,mask", [(512, 2), (512, 0), (256, 1)])
+def test_big_backward_workspace_does_not_grow_with_the_keys(pkg, d, mask):
+    """head_dim 256/512: the score tiles are held one chunk of keys at a time
+    (TransformerEngine PR #3527, "Known limitations": the workspace, not the
+    compute, caps the prior art's context length), so past one chunk the
+    backward workspace is the same for every key length."""
+    base = dict(head_dim=d, mask_type=mask, batch=2, seqlen_q=2048, num_heads_q=16, num_heads_kv=4)
+    sizes = [pkg.sdpa_bwd_workspace_size(problem(pkg, seqlen_kv=sk, **base)) for sk in (8192, 16384, 65536, 262144)]
+    assert len(set(sizes)) == 1 and sizes[0] > 0, sizes
+    assert sizes[0] < (1 << 30)  # the 8192-key D512 workload would hold 4 GiB of tiles unchunked
+    # a short key range fits one chunk and needs less
+    assert pkg.sdpa_bwd_workspace_size(problem(pkg, seqlen_kv=512, **base)) < sizes[0]
+    # a caller-chosen chunk bounds it further; chunking adds the fp32 dQ accumulator
+    small = pkg.sdpa_bwd_workspace_size(problem(pkg, seqlen_kv=65536, kv_chunk=128, **base))
+    tile_pairs = 2 * 16 * 16  # (batch, q head, q tile) x one key tile
+    acc = 2 * 2048 * 16 * d * 4
+    assert small < sizes[0] and small >= acc + tile_pairs * 65536  # a 16-bit P and dS image per pair
+
+
+def test_window_bounds_the_big_backward_workspace(pkg):
+    """A bounded window already bounds the keys a query tile sees: the tile
+    arrays hold the window's span, whatever the key length."""
+    base = dict(head_dim=256, mask_type=1, batch=2, num_heads_q=16, num_heads_kv=8, window_left=1024, window_right=0)
+    sizes = {sk: pkg.sdpa_bwd_workspace_size(problem(pkg, seqlen_q=sk, seqlen_kv=sk, **base)) for sk in (8192, 16384)}
+    per_q_tile = (sizes[16384] - sizes[8192]) / ((16384 - 8192) // 128)
+    # per added query tile: 11 slots of P and dS for every (batch, head), plus statistics
+    assert abs(per_q_tile - 2 * 16 * 11 * 65536) < 2 * 16 * 128 * 8 + 4096
 
 
 def test_product_path_refuses_cpu_tensors(pkg):
