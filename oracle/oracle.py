@@ -78,6 +78,7 @@ def _load():
             lib.sdpa_oracle_e4m3_round_array.argtypes = [ctypes.c_int64, dp, dp]
             lib.sdpa_oracle_e4m3_decode_array.argtypes = [ctypes.c_int64, u8p, dp]
             lib.sdpa_oracle_num_threads.restype = ctypes.c_int
+            lib.sdpa_oracle_probs.argtypes = [pp, dp, dp, ip, ip, dp]
             _lib = lib
     return _lib
 
@@ -218,6 +219,20 @@ def dkdv_rows(q, k, v, dout, bgj, *, layout="bshd", mask="none", scale=None, win
     if rc:
         raise ValueError(f"oracle dkdv_rows rejected the problem (rc={rc})")
     return dk, dv
+
+
+def probs(q, k, *, layout="bshd", mask="none", scale=None, window=(-1, -1), cu_q=None, cu_kv=None):
+    """Softmax probabilities p_ij = exp(s_ij - LSE_i) of every query row:
+    array (rows_q, Hq, lk_max), zero at masked keys and past a sequence's
+    keys (lk_max = the longest key sequence)."""
+    q, k = _f64(q), _f64(k)
+    scale = 1.0 / np.sqrt(q.shape[-1]) if scale is None else scale
+    p = Problem(q, k, layout, mask, scale, window, cu_q, cu_kv)
+    out = np.zeros((p.rows_q, p.hq, max(p.sk, 1)))
+    rc = _load().sdpa_oracle_probs(ctypes.byref(p.c), _dptr(q), _dptr(k), _iptr(p.cu_q), _iptr(p.cu_kv), _dptr(out))
+    if rc:
+        raise ValueError(f"oracle probs rejected the problem (rc={rc})")
+    return out
 
 
 def merge(o_parts, lse_parts):

@@ -503,9 +503,35 @@ int sdpa_oracle_merge(int n_parts, int64_t items, int d, const double* o_parts, 
     return 0;
 }
 
+/* The softmax probabilities of the definition, p_ij = exp(s_ij - LSE_i) for
+ * every allowed key j of row i's sequence and 0 elsewhere, written to
+ * probs[(token_row * Hq + h) * lk_max + j] (lk_max = the longest key
+ * sequence). Returns 0 on success. */
+int sdpa_oracle_probs(const oracle_problem* p, const double* q, const double* k, const int32_t* cu_q,
+                      const int32_t* cu_kv, double* probs) {
+    if (!valid(p)) return 1;
+    int hq = p->num_heads_q, lkmax = max_len(p, cu_kv, 0);
+    for (int b = 0; b < p->batch; ++b) {
+        int lq = seq_len(p, cu_q, b, 1), lk = seq_len(p, cu_kv, b, 0);
+#pragma omp parallel
+        {
+            double* srow = (double*)malloc(sizeof(double) * (size_t)(lkmax > 0 ? lkmax : 1));
+#pragma omp for collapse(2) schedule(dynamic, 4)
+            for (int h = 0; h < hq; ++h)
+                for (int i = 0; i < lq; ++i) {
+                    double* prow = probs + (token_row(p, cu_q, b, i, 1) * hq + h) * lkmax;
+                    double l = row_scores(p, q, k, cu_q, cu_kv, b, h, i, srow);
+                    for (int j = 0; j < lkmax; ++j)
+                        prow[j] = (j < lk && l != -INFINITY && srow[j] != -INFINITY) ? exp(srow[j] - l) : 0.0;
+                }
+            free(srow);
+        }
+    }
+    return 0;
+}
+
 /*
- * FP8 E4M3 forward (the FP8 variant of this kernel family; no CUDA kernel
- * implements it yet). Reading of TransformerEngine PR #3705's closing note
+ * FP8 E4M3 forward (the FP8 variant of this kernel family). Reading of TransformerEngine PR #3705's closing note
  * ("Amax S"): with E4M3 inputs the softmax output is stored in E4M3 under a
  * fixed scale, 448 (the format's largest value) without dropout, so no
  * amax of it is ever needed. Written out:

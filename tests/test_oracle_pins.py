@@ -443,6 +443,36 @@ def test_backward_rejects_unequal_head_dims():
 
 
 # ------------------------------------------------- FP8 E4M3 forward (oracle only)
+@pytest.mark.parametrize("case", CASES)
+def test_probabilities_match_torch_sdpa_with_identity_values(case):
+    """sdpa_oracle_probs against a library routine: torch's float64 SDPA with
+    V = the identity over the keys returns P itself (its own causal masks)."""
+    b, sq, sk, hq, hkv, d, mask = case
+    r = rng(801 + sq)
+    q, k = r.standard_normal((b, sq, hq, d)), r.standard_normal((b, sk, hkv, d))
+    eye = np.broadcast_to(np.eye(sk)[None, :, None, :], (b, sk, hkv, sk)).copy()
+    ref = torch_ref(q, k, eye, mask, 0.4)["o"]  # (B, Sq, Hq, Sk)
+    got = oracle.probs(q, k, layout="bshd", mask=mask, scale=0.4).reshape(b, sq, hq, sk)
+    np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-14)
+
+
+def test_probabilities_on_thd_rows_sum_to_one_and_vanish_outside_the_mask():
+    r = rng(811)
+    cu = np.array([0, 5, 5, 12], dtype=np.int32)
+    cuk = np.array([0, 3, 9, 13], dtype=np.int32)
+    q, k = r.standard_normal((12, 2, 8)), r.standard_normal((13, 1, 8))
+    got = oracle.probs(q, k, layout="thd", mask="causal_br", scale=0.5, cu_q=cu, cu_kv=cuk)
+    assert got.shape == (12, 2, 6)
+    # sequence 0: 5 queries, 3 keys, bottom-right: query i sees keys <= i - 2
+    for i in range(5):
+        n = max(0, min(3, i - 1))
+        assert np.all(got[i, :, n:] == 0)
+        np.testing.assert_allclose(got[i].sum(-1), 1.0 if n else 0.0, rtol=1e-14)
+    # sequence 2: 7 queries, 4 keys: rows 0..2 see nothing
+    assert np.all(got[5:8] == 0)
+    np.testing.assert_allclose(got[8:12].sum(-1), 1.0, rtol=1e-14)
+
+
 def _e4m3_codes(x):
     """E4M3 codes of float values through torch's own conversion (the library routine)."""
     return torch.from_numpy(np.asarray(x, dtype=np.float32)).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
