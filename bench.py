@@ -475,6 +475,11 @@ def gpu_arm(args, w, inp):
         rows = rows_q * w.heads_q
         detail["dq_finalize_gbs"] = rows * w.head_dim * 6 / (kern["dq_finalize"]["ms_avg"] * 1e-3) / 1e9
 
+    if w.name == workloads.VARLEN_THD.name and not fo and not args.no_companion:
+        # the other half of the headline metric (head_dim 512), same process and timing
+        detail["d512"] = companion_measure(workloads.D512_BR, max(10, args.steps // 10), args.warmup, dev, flush,
+                                           peak)
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         s = oracle_sample(w, inp, 12.0, fo)
@@ -567,6 +572,72 @@ def merge_arm(args, w, inp):
         print(json.dumps(line), flush=True)
 
 
+def companion_measure(w, steps, warmup, dev, flush, peak):
+    """Forward and backward of a second workload, timed in the same process
+    the same way (CUDA events around each step, L2 flushed between steps,
+    per-kernel events from the library's profiler): the headline metric
+    names head_dim 128 and 512, and the default step is the head_dim 128
+    one. Exact-mask FLOPs (4*D per unmasked pair forward, 10*D backward)."""
+    import torch
+
+    import scaled_dot_product_02_gb300 as sdpa
+
+    inp = workloads.make_inputs(w)
+    q, k, v, do = (workloads.to_torch(inp[x], w.dtype).to(dev) for x in ("q", "k", "v", "do"))
+    kw = dict(layout=w.layout, mask=w.mask, scale=w.scale, window=w.window)
+    o = torch.empty_like(q)
+    lse = torch.empty((q.numel() // (w.heads_q * w.head_dim), w.heads_q), dtype=torch.float32, device=dev)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    prob = sdpa.make_problem(q, k, layout=w.layout, mask=w.mask, window=w.window, scale=w.scale)
+    ws_f = torch.empty(max(256, sdpa.sdpa_fwd_workspace_size(prob)), dtype=torch.uint8, device=dev)
+    ws_b = torch.empty(max(256, sdpa.sdpa_bwd_workspace_size(prob)), dtype=torch.uint8, device=dev)
+
+    def step():
+        sdpa.sdpa_fwd(q, k, v, out=o, lse=lse, workspace=ws_f, **kw)
+        n = sdpa.sdpa_last_launch_count()
+        sdpa.sdpa_bwd(q, k, v, o, lse, do, dq=dq, dk=dk, dv=dv, workspace=ws_b, **kw)
+        return n, sdpa.sdpa_last_launch_count()
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    if sdpa.sdpa_get_device_error() != 0:
+        raise RuntimeError(f"device error during the {w.name} warm-up")
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    torch.cuda.synchronize()
+    sdpa.sdpa_profile_begin()
+    launches = (0, 0)
+    for i in range(steps):
+        flush.fill_(i & 255)
+        starts[i].record()
+        launches = step()
+        ends[i].record()
+    torch.cuda.synchronize()
+    prof = sdpa.sdpa_profile_end()
+    if sdpa.sdpa_get_device_error() != 0:
+        raise RuntimeError(f"device error during the {w.name} steps")
+    ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends)) / steps
+    conv, exact = flops(w, inp)
+    fwd_ms = prof["fwd"][0] / steps
+    bwd_ms = sum(prof[x][0] for x in ("preprocess", "bwd", "dq_finalize")) / steps
+    out = {"workload": w.name, "steps": steps, "ms_per_step": ms, "fwd_ms": fwd_ms, "bwd_ms": bwd_ms,
+           "fwd_launches_per_step": launches[0], "bwd_launches_per_step": launches[1],
+           "fwd_tflops_exact": exact / (fwd_ms * 1e-3) / 1e12,
+           "bwd_tflops_exact": 2.5 * exact / (bwd_ms * 1e-3) / 1e12,
+           "fwd_tflops_convention": conv / (fwd_ms * 1e-3) / 1e12,
+           "bwd_tflops_convention": 2.5 * conv / (bwd_ms * 1e-3) / 1e12,
+           "step_tflops_convention": 3.5 * conv / (ms * 1e-3) / 1e12,
+           "peak": peak,
+           "bwd_workspace_bytes": int(ws_b.numel()),
+           "note": "bwd_ms covers every kernel of the backward call (preprocess, score, GEMMs, dQ finalise)"}
+    out["fwd_frac_of_peak"] = out["fwd_tflops_exact"] / peak
+    out["bwd_frac_of_peak"] = out["bwd_tflops_exact"] / peak
+    del q, k, v, do, o, lse, dq, dk, dv, ws_f, ws_b
+    torch.cuda.empty_cache()
+    return out
+
+
 def traffic_for(kind, workload):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel sources (else None)."""
@@ -604,6 +675,8 @@ def main():
     ap.add_argument("--merge-parts", type=int, default=4)
     ap.add_argument("--kv-chunk", type=int, default=0,
                     help="head_dim 256/512 backward: key positions per chunk (multiple of 128; 0 = library choice)")
+    ap.add_argument("--no-companion", action="store_true",
+                    help="skip timing the head_dim 512 workload beside the default head_dim 128 step")
     ap.add_argument("--deterministic", action="store_true",
                     help="bitwise-reproducible backward (head_dim 128: separate dQ pass, no fp32 reductions)")
     args = ap.parse_args()

@@ -39,7 +39,10 @@
  * never synchronises the stream there. Device-side faults in the inputs
  * (bad cu_seqlens) and bounded-wait timeouts are recorded in a per-device
  * error word that kernels check before writing outputs; read it with
- * sdpa_get_device_error.
+ * sdpa_get_device_error. The first call on each device does a one-time
+ * host-side set-up (the error word's device address, kernel attributes); a
+ * device reset (cudaDeviceReset) invalidates it, so a process must not call
+ * the library on a device it has reset.
  *
  * Errors: every entry point returns an sdpa_status. Host-detectable problems
  * are returned before anything is launched (an explicit decline, never a
@@ -197,13 +200,30 @@ SDPA_API int sdpa_last_launch_count(void);
  * process exits. Problems whose sdpa_bwd_workspace_size exceeds that maximum
  * are rejected with SDPA_ERR_WORKSPACE_TOO_SMALL before any launch. The first
  * call on a device looks up the array's device address (a one-time host-side
- * set-up); make that first call before any stream capture. Every call shares
+ * set-up); make that first call before any stream capture. A device reset
+ * (cudaDeviceReset) unloads the library's device code and with it the array:
+ * the address looked up before it is stale, so do not call this entry point
+ * (or any other, see the per-device set-up under "Ownership") on a device
+ * after resetting it in the same process. Every call shares
  * the array: calls that overlap on the GPU (e.g. on two streams at once) race
  * and must be serialised by the caller. No call allocates memory. */
 #define SDPA_BWD_NOALLOC_MAX_BYTES (32u << 20)
 SDPA_API int sdpa_bwd_noalloc(const sdpa_problem* p, const void* q, const void* k, const void* v, const void* o,
                               const float* lse, const void* dout, void* dq, void* dk, void* dv,
                               const int32_t* cu_seqlens_q, const int32_t* cu_seqlens_kv, void* stream);
+
+/* Testing aid, off by default: caps how many CTAs any tcgen05 kernel of the
+ * library has in flight at once (0 = no cap, the default; negative:
+ * SDPA_ERR_INVALID_ARG). The persistent head_dim 128 forward launches at most
+ * max_ctas CTAs, which then take every query tile from the ticket counter;
+ * every other attention kernel is launched as successive grids of at most
+ * max_ctas CTAs. Results must not depend on the cap (dQ of the head_dim 128
+ * backward with deterministic = 0 only up to the order of its fp32
+ * reductions): it reschedules the same work, which is how a test shakes out
+ * ordering, ticket, queue and barrier-phase assumptions that element-wise
+ * parity at one schedule cannot (the sanitizers' race and sync checks are
+ * the other route). Process-wide; slow for large problems. */
+SDPA_API int sdpa_debug_set_max_ctas(int max_ctas);
 
 /* Failure-path self-test of the bounded waits every pipelined kernel uses:
  * launches one thread that waits on a barrier nothing arrives on, gives up
@@ -239,6 +259,28 @@ typedef struct {
 SDPA_API int sdpa_merge(const sdpa_merge_problem* p, const void* o_parts, const float* lse_parts, void* o, float* lse,
                void* stream);
 
+/* FP8 E4M3 forward, head_dim 128 (TransformerEngine PR #3705's closing note
+ * on FP8: with E4M3 inputs the softmax output is stored in E4M3 under the
+ * fixed scale 448, so no amax of it is needed; PR #3527 "Scope" lists the
+ * FP8 fused path). Computes, with the decoded values of the codes,
+ *   S = softmax_scale * descale_q * descale_k * Q8 K8^T, masked as sdpa_fwd;
+ *   LSE = ln sum_j exp(S_ij)   (float32, token-major, as sdpa_fwd);
+ *   P8  = E4M3(exp(S - LSE) * 448)   (round to nearest even, saturating);
+ *   O   = P8 V8 * descale_v / 448    (written in p->dtype: bf16 or fp16).
+ * q8 [.., Hq, 128], k8 and v8 [.., Hkv, 128]: device E4M3 codes (the finite-
+ * only OCP format: bias 7, largest 448, S.1111.111 = NaN), one byte each, in
+ * p->layout; o [.., Hq, 128] and lse as for sdpa_fwd (device, written).
+ * p->head_dim must be 128 (head_dim_v 0 or 128), else SDPA_ERR_UNSUPPORTED;
+ * p->dtype is O's type. Descales: finite and > 0, else SDPA_ERR_INVALID_ARG.
+ * workspace: at least sdpa_fwd_fp8_workspace_size bytes, 256-byte aligned
+ * (the THD guard word and V transposed to [Hkv][128][keys], one byte per key,
+ * every sequence starting on a 16-byte boundary). Launches (THD guard), the
+ * transpose and the attention kernel on `stream`; errors as sdpa_fwd. */
+SDPA_API size_t sdpa_fwd_fp8_workspace_size(const sdpa_problem* p);
+SDPA_API int sdpa_fwd_fp8(const sdpa_problem* p, const void* q8, const void* k8, const void* v8, float descale_q,
+                          float descale_k, float descale_v, void* o, float* lse, const int32_t* cu_seqlens_q,
+                          const int32_t* cu_seqlens_kv, void* workspace, size_t ws_bytes, void* stream);
+
 /* Kernel timing for benchmarks and tracing. Between sdpa_profile_begin and
  * sdpa_profile_end, every sdpa_fwd / sdpa_bwd call made by this host thread
  * (and sdpa_merge) records a pair of CUDA events on its stream around each kernel it
@@ -253,7 +295,8 @@ typedef enum {
   SDPA_KERNEL_GUARD = 4,      /* THD metadata guard */
   SDPA_KERNEL_MERGE = 5,      /* log-sum-exp merge of key-split partial results */
   SDPA_KERNEL_BWD_DQ = 6,     /* deterministic backward: the separate head_dim 128 dQ pass */
-  SDPA_KERNEL_KINDS = 7
+  SDPA_KERNEL_V_TRANSPOSE = 7, /* FP8 forward: V transposed into the workspace */
+  SDPA_KERNEL_KINDS = 8
 } sdpa_kernel_kind;
 SDPA_API int sdpa_profile_begin(void);
 SDPA_API int sdpa_profile_end(double* ms_by_kind, int* launches_by_kind, int n_kinds);

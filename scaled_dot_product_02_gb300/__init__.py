@@ -28,9 +28,10 @@ STATUS = {0: "SDPA_OK", 1: "SDPA_ERR_INVALID_ARG", 2: "SDPA_ERR_UNSUPPORTED", 3:
           7: "SDPA_ERR_TIMEOUT", 8: "SDPA_ERR_CUDA"}
 EXPORTS = ("sdpa_fwd_workspace_size", "sdpa_bwd_workspace_size", "sdpa_check_problem", "sdpa_fwd", "sdpa_bwd",
            "sdpa_get_device_error", "sdpa_error_string", "sdpa_last_launch_count", "sdpa_profile_begin",
-           "sdpa_profile_end", "sdpa_bwd_noalloc", "sdpa_selftest_bounded_wait", "sdpa_merge")
+           "sdpa_profile_end", "sdpa_bwd_noalloc", "sdpa_selftest_bounded_wait", "sdpa_merge",
+           "sdpa_fwd_fp8_workspace_size", "sdpa_fwd_fp8", "sdpa_debug_set_max_ctas")
 NOALLOC_MAX_BYTES = 32 << 20  # SDPA_BWD_NOALLOC_MAX_BYTES
-KERNEL_KINDS = ("fwd", "bwd", "preprocess", "dq_finalize", "guard", "merge", "bwd_dq")
+KERNEL_KINDS = ("fwd", "bwd", "preprocess", "dq_finalize", "guard", "merge", "bwd_dq", "v_transpose")
 
 
 class SdpaError(RuntimeError):
@@ -80,10 +81,15 @@ def lib():
             L.sdpa_error_string.restype = ctypes.c_char_p
             L.sdpa_last_launch_count.restype = ctypes.c_int
             L.sdpa_selftest_bounded_wait.argtypes = [ctypes.c_uint, vp]
+            L.sdpa_debug_set_max_ctas.argtypes = [ctypes.c_int]
             L.sdpa_bwd_noalloc.argtypes = [pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
             L.sdpa_merge.argtypes = [ctypes.POINTER(MergeProblem), vp, vp, vp, vp, vp]
             L.sdpa_profile_end.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int),
                                            ctypes.c_int]
+            L.sdpa_fwd_fp8_workspace_size.argtypes = [pp]
+            L.sdpa_fwd_fp8_workspace_size.restype = ctypes.c_size_t
+            fl = ctypes.c_float
+            L.sdpa_fwd_fp8.argtypes = [pp, vp, vp, vp, fl, fl, fl, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
             _lib = L
     return _lib
 
@@ -289,9 +295,74 @@ def sdpa_bwd_noalloc(q, k, v, o, lse, dout, *, layout="bshd", mask="none", windo
     return dq, dk, dv
 
 
+def sdpa_fwd_fp8_workspace_size(p: Problem) -> int:
+    return int(lib().sdpa_fwd_fp8_workspace_size(ctypes.byref(p)))
+
+
+def sdpa_fwd_fp8(q8, k8, v8, *, descale=(1.0, 1.0, 1.0), layout="bshd", mask="none", window=(-1, -1), scale=None,
+                 cu_seqlens_q=None, cu_seqlens_kv=None, max_seqlen_q=None, max_seqlen_kv=None, out_dtype=None,
+                 out=None, lse=None, workspace=None, stream=None):
+    """FP8 E4M3 forward (head_dim 128). q8, k8, v8: torch.uint8 codes or
+    torch.float8_e4m3fn tensors in `layout`; descale = (d_q, d_k, d_v), the
+    per-tensor factors that turn codes into values. The softmax output is
+    stored as E4M3(P * 448) against the row's final LSE (see sdpa_fwd_fp8 in
+    include/sdpa.h). Returns (o, lse): o in out_dtype (default bfloat16) with
+    q8's shape, lse float32 [rows_q, Hq]."""
+    import torch
+
+    f8 = getattr(torch, "float8_e4m3fn", None)
+    for name, t in (("q8", q8), ("k8", k8), ("v8", v8)):
+        if t.dtype not in (torch.uint8, f8):
+            raise ValueError(f"{name} must hold E4M3 codes (torch.uint8 or torch.float8_e4m3fn), got {t.dtype}")
+        if t.device != q8.device:
+            raise ValueError(f"{name} must be on q8's device")
+    out_dtype = torch.bfloat16 if out_dtype is None else out_dtype
+    if out_dtype not in (torch.bfloat16, torch.float16):
+        raise ValueError("out_dtype must be bfloat16 or float16")
+    rank = 3 if layout == "thd" else 4
+    if any(t.dim() != rank for t in (q8, k8, v8)):
+        raise ValueError(f"q8, k8, v8 must have {rank} dimensions in layout {layout}")
+    if tuple(k8.shape) != tuple(v8.shape) or k8.shape[-1] != q8.shape[-1]:
+        raise ValueError("k8 and v8 must have the same shape, and the same head_dim as q8")
+    batch = None if cu_seqlens_q is None else cu_seqlens_q.numel() - 1
+    p = make_problem(q8, k8, layout=layout, mask=mask, window=window, scale=scale, batch=batch,
+                     dtype={torch.bfloat16: 0, torch.float16: 1}[out_dtype], max_seqlen_q=max_seqlen_q,
+                     max_seqlen_kv=max_seqlen_kv)
+    rows_q = q8.numel() // (q8.shape[-1] * q8.shape[-2])
+    if out is None:
+        out = torch.empty(tuple(q8.shape), dtype=out_dtype, device=q8.device)
+    if lse is None:
+        lse = torch.empty((rows_q, q8.shape[-2]), dtype=torch.float32, device=q8.device)
+    if tuple(out.shape) != tuple(q8.shape) or out.dtype != out_dtype or tuple(lse.shape) != (rows_q, q8.shape[-2]) \
+            or lse.dtype != torch.float32:
+        raise ValueError("out must have q8's shape in out_dtype and lse float32 [rows_q, Hq]")
+    for name, t in (("cu_seqlens_q", cu_seqlens_q), ("cu_seqlens_kv", cu_seqlens_kv)):
+        if t is not None and (t.dtype != torch.int32 or t.dim() != 1 or t.device != q8.device):
+            raise ValueError(f"{name} must be a 1-D int32 tensor on q8's device")
+    need = sdpa_fwd_fp8_workspace_size(p)
+    if workspace is None and need:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q8.device)
+    _check_cuda(q8, k8, v8, out, lse, cu_seqlens_q, cu_seqlens_kv, workspace)
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    rc = lib().sdpa_fwd_fp8(ctypes.byref(p), _ptr(q8), _ptr(k8), _ptr(v8), float(descale[0]), float(descale[1]),
+                            float(descale[2]), _ptr(out), _ptr(lse), _ptr(cu_seqlens_q), _ptr(cu_seqlens_kv),
+                            _ptr(workspace), ws_bytes, _stream(stream))
+    if rc:
+        raise SdpaError(rc, "sdpa_fwd_fp8")
+    return out, lse
+
+
 def sdpa_get_device_error(stream=None) -> int:
     """Synchronise the stream and return (and clear) the device error word."""
     return int(lib().sdpa_get_device_error(_stream(stream)))
+
+
+def sdpa_debug_set_max_ctas(max_ctas: int) -> None:
+    """Testing aid: cap the CTAs of every attention kernel launch (0 = no
+    cap). See sdpa_debug_set_max_ctas in include/sdpa.h."""
+    rc = lib().sdpa_debug_set_max_ctas(int(max_ctas))
+    if rc:
+        raise SdpaError(rc, "sdpa_debug_set_max_ctas")
 
 
 def sdpa_last_launch_count() -> int:

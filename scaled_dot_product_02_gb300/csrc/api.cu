@@ -9,6 +9,7 @@
 #include <cmath>
 #include <cstdint>
 #include <algorithm>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 #include <set>
@@ -197,7 +198,36 @@ int encode(CUtensorMap* m, const void* base, int d, int nh, int rows, int box_ro
   return r == CUDA_SUCCESS ? SDPA_OK : SDPA_ERR_CUDA;
 }
 
+// 3-D map over a contiguous one-byte (E4M3) tensor with 128-byte-swizzled boxes:
+// dims[0] is the innermost (contiguous) extent, strides[i] the byte stride of dims[i+1].
+int encode_u8(CUtensorMap* m, const void* base, const cuuint64_t (&dims)[3], const cuuint64_t (&strides)[2],
+              const cuuint32_t (&box)[3]) {
+  auto fn = encode_fn();
+  if (!fn) return SDPA_ERR_CUDA;
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? SDPA_OK : SDPA_ERR_CUDA;
+}
+
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// Keys of the FP8 forward's transposed V per (kv head, d): every sequence's
+// keys start on a multiple of 16 (see vt_row0 in fwd_fp8.cu).
+size_t fp8_vt_rows(const sdpa_problem* p) {
+  if (p->layout == SDPA_THD) return round_up((size_t)p->total_kv + 16 * (size_t)p->batch, 16);
+  if (p->layout == SDPA_BSHD) return (size_t)p->batch * round_up((size_t)p->seqlen_kv, 16);
+  return round_up((size_t)p->seqlen_kv, 16);
+}
+
+// FP8 forward: head_dim 128 only (PR #3527 "Scope" serves FP8 at head dims up
+// to 256; this library builds the 128 of the benchmark workloads).
+int check_fp8(const sdpa_problem* p) {
+  const int rc = check(p);
+  if (rc) return rc;
+  return (p->head_dim == 128 && dv_of(p) == 128) ? SDPA_OK : SDPA_ERR_UNSUPPORTED;
+}
 
 // Key tiles one 128-row query tile can touch (the slot count of the head_dim
 // 256/512 tile arrays): the whole key range, or the window's span.
@@ -294,6 +324,9 @@ BwdWs bwd_ws(const sdpa_problem* p) {
 }
 
 }  // namespace
+
+static std::atomic<int> g_max_ctas{0};
+int debug_max_ctas() { return g_max_ctas.load(std::memory_order_relaxed); }
 
 int set_kernel_smem(const void* kernel, int bytes, int carveout) {
   static std::mutex mu;
@@ -539,6 +572,89 @@ int sdpa_bwd(const sdpa_problem* p, const void* q, const void* k, const void* v,
   return SDPA_OK;
 }
 
+size_t sdpa_fwd_fp8_workspace_size(const sdpa_problem* p) {
+  if (check_fp8(p) != SDPA_OK) return 0;
+  int rq, rk, hq, hk;
+  view(p, rq, rk, hq, hk);
+  return 256 + (size_t)hk * 128 * fp8_vt_rows(p);
+}
+
+int sdpa_fwd_fp8(const sdpa_problem* p, const void* q8, const void* k8, const void* v8, float descale_q,
+                 float descale_k, float descale_v, void* o, float* lse, const int32_t* cu_seqlens_q,
+                 const int32_t* cu_seqlens_kv, void* workspace, size_t ws_bytes, void* stream) {
+  t_last_launches = 0;
+  int rc = check_fp8(p);
+  if (rc) return rc;
+  if (!std::isfinite(descale_q) || !std::isfinite(descale_k) || !std::isfinite(descale_v) || !(descale_q > 0.f) ||
+      !(descale_k > 0.f) || !(descale_v > 0.f))
+    return SDPA_ERR_INVALID_ARG;
+  int rq, rk, hq, hk;
+  view(p, rq, rk, hq, hk);
+  const bool thd = p->layout == SDPA_THD;
+  if (p->batch == 0 || rq == 0) return SDPA_OK;
+  if (!q8 || !k8 || !v8 || !o || !lse) return SDPA_ERR_INVALID_ARG;
+  if (thd && (!cu_seqlens_q || !cu_seqlens_kv)) return SDPA_ERR_INVALID_ARG;
+  if (!aligned16(q8) || !aligned16(k8) || !aligned16(v8) || !aligned16(o) || !aligned16(lse))
+    return SDPA_ERR_ALIGNMENT;
+  const size_t need = sdpa_fwd_fp8_workspace_size(p);
+  if (ws_bytes < need || !workspace) return SDPA_ERR_WORKSPACE_TOO_SMALL;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255u) return SDPA_ERR_ALIGNMENT;
+  const size_t qb = (size_t)rq * hq * 128, kb = (size_t)rk * hk * 128, ob = (size_t)rq * hq * 128 * 2;
+  const Extent outs[3] = {extent(o, ob), extent(lse, (size_t)rq * hq * 4), extent(workspace, need)};
+  const Extent ins[3] = {extent(q8, qb), extent(k8, kb), extent(v8, kb)};
+  for (int x = 0; x < 3; ++x) {
+    for (int y = 0; y < 3; ++y)
+      if (overlaps(outs[x], ins[y])) return SDPA_ERR_OVERLAP;
+    for (int y = x + 1; y < 3; ++y)
+      if (overlaps(outs[x], outs[y])) return SDPA_ERR_OVERLAP;
+  }
+  int* err = error_word();
+  if (!err) return SDPA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  Fp8Launch L;
+  std::memset(&L, 0, sizeof(L));
+  L.p.g = make_geom(p, cu_seqlens_q, cu_seqlens_kv);
+  L.p.g.scale = p->softmax_scale * descale_q * descale_k;  // scores of the decoded codes
+  L.p.g.scale_log2 = L.p.g.scale * 1.4426950408889634f;
+  L.p.v = static_cast<const uint8_t*>(v8);
+  L.p.vt = ws + 256;
+  L.p.vt_rows = (int)fp8_vt_rows(p);
+  L.p.o = o;
+  L.p.lse = lse;
+  L.p.err = err;
+  L.p.guard = thd ? reinterpret_cast<const int*>(ws) : nullptr;
+  L.p.n_q_tiles = (p->seqlen_q + 127) / 128;
+  L.p.o_scale = descale_v / 448.f;
+  L.stream = s;
+  if ((size_t)L.p.vt_rows * hk * 128 >= (1ull << 40)) return SDPA_ERR_UNSUPPORTED;
+  {
+    const cuuint64_t dq[3] = {128, (cuuint64_t)hq, (cuuint64_t)(rq > 0 ? rq : 1)};
+    const cuuint64_t sq[2] = {128, (cuuint64_t)hq * 128};
+    const cuuint64_t dk[3] = {128, (cuuint64_t)hk, (cuuint64_t)(rk > 0 ? rk : 1)};
+    const cuuint64_t sk[2] = {128, (cuuint64_t)hk * 128};
+    const cuuint64_t dvt[3] = {(cuuint64_t)L.p.vt_rows, 128, (cuuint64_t)hk};
+    const cuuint64_t svt[2] = {(cuuint64_t)L.p.vt_rows, (cuuint64_t)L.p.vt_rows * 128};
+    const cuuint32_t box_rows[3] = {128, 1, 128}, box_vt[3] = {128, 128, 1};
+    if ((rc = encode_u8(&L.tmQ, q8, dq, sq, box_rows))) return rc;
+    if ((rc = encode_u8(&L.tmK, k8, dk, sk, box_rows))) return rc;
+    if ((rc = encode_u8(&L.tmVt, L.p.vt, dvt, svt, box_vt))) return rc;
+  }
+  int launches = 0;
+  if (thd) {
+    if ((rc = timed(SDPA_KERNEL_GUARD, s,
+                    [&] { return launch_guard(L.p.g, p->total_q, p->total_kv, reinterpret_cast<int*>(ws), err, s); })))
+      return rc;
+    ++launches;
+  }
+  if ((rc = timed(SDPA_KERNEL_V_TRANSPOSE, s, [&] { return launch_vt(L.p, s); }))) return rc;
+  ++launches;
+  if ((rc = timed(SDPA_KERNEL_FWD, s, [&] { return launch_fwd_fp8(L, p->dtype == SDPA_BF16); }))) return rc;
+  ++launches;
+  t_last_launches = launches;
+  return SDPA_OK;
+}
+
 int sdpa_merge(const sdpa_merge_problem* p, const void* o_parts, const float* lse_parts, void* o, float* lse,
                void* stream) {
   t_last_launches = 0;
@@ -591,6 +707,12 @@ const char* sdpa_error_string(int status) {
 }
 
 int sdpa_last_launch_count(void) { return t_last_launches; }
+
+int sdpa_debug_set_max_ctas(int max_ctas) {
+  if (max_ctas < 0) return SDPA_ERR_INVALID_ARG;
+  g_max_ctas.store(max_ctas, std::memory_order_relaxed);
+  return SDPA_OK;
+}
 
 int sdpa_selftest_bounded_wait(unsigned limit_us, void* stream) {
   int* err = error_word();

@@ -119,7 +119,7 @@ __global__ void __launch_bounds__(512, 1)
   // ---- which tile: the key tiles of one (batch, kv head) are adjacent in the
   // grid, so CTAs running together read the same Q/dO rows and reduce into the
   // same dQ accumulator rows while those are resident in L2.
-  int idx = blockIdx.x;
+  int idx = blockIdx.x + p.item_offset;
   const int kt = idx % p.n_kv_tiles;
   idx /= p.n_kv_tiles;
   const int kvh = idx % g.hkv;
@@ -474,8 +474,12 @@ static int launch_t(const BwdLaunch& L) {
   const long long grid = (long long)L.p.n_kv_tiles * L.p.g.hkv * L.p.g.batch;
   if (grid <= 0) return SDPA_OK;
   if (grid > 0x7fffffffLL) return SDPA_ERR_UNSUPPORTED;
-  kern<<<(unsigned)grid, 512, SMEM_BYTES, L.stream>>>(L.tmQ, L.tmK, L.tmV, L.tmDO, L.p);
-  return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+  return launch_in_grids(grid, [&](long long off, long long n) {
+    BwdParams p = L.p;
+    p.item_offset = (int)off;
+    kern<<<(unsigned)n, 512, SMEM_BYTES, L.stream>>>(L.tmQ, L.tmK, L.tmV, L.tmDO, p);
+    return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+  });
 }
 
 int launch_bwd_dkdv(const BwdLaunch& L, int head_dim, bool bf16, bool with_dq, int* launches) {

@@ -110,7 +110,7 @@ __global__ void __launch_bounds__(SF_THREADS, 1)
                           const __grid_constant__ BigBwdParams p) {
   using E = Elem<BF16>;
   const Geom& g = p.g;
-  int idx = blockIdx.x;
+  int idx = blockIdx.x + p.item_offset;
   const int h = idx % g.hq;
   idx /= g.hq;
   const int b = idx % g.batch;
@@ -392,7 +392,7 @@ __global__ void __launch_bounds__(S5_THREADS, 1)
                           const __grid_constant__ BigBwdParams p) {
   using E = Elem<BF16>;
   const Geom& g = p.g;
-  int idx = blockIdx.x;
+  int idx = blockIdx.x + p.item_offset;
   const int h = idx % g.hq;
   idx /= g.hq;
   const int b = idx % g.batch;
@@ -918,7 +918,7 @@ template <bool BF16>
 __global__ void __launch_bounds__(256, 2)
     gemm_kernel(const __grid_constant__ CUtensorMap tmK64, const __grid_constant__ CUtensorMap tmDO64,
                 const __grid_constant__ CUtensorMap tmQ64, const __grid_constant__ BigBwdParams p, int n_kv_ctas) {
-  const int idx = blockIdx.x;
+  const int idx = blockIdx.x + p.item_offset;
   if (idx < n_kv_ctas)
     gemm_tile<1, BF16>(&tmDO64, p, idx);
   else if (idx < 2 * n_kv_ctas)
@@ -956,14 +956,27 @@ static int launch_big_t(const BigBwdLaunch& L, int* launches) {
     p.chunk_lo = lo;
     p.chunk_hi = std::min(lo + p0.chunk, p0.n_kv_tiles);
     const long long gkv_c = (long long)(p.chunk_hi - p.chunk_lo) * splits * p.g.hkv * p.g.batch;
+    int rc = SDPA_OK;
     if (g1 > 0) {  // phase 1: P and dS tiles of this chunk from S and dP
-      sf<<<(unsigned)g1, sf_threads, sf_smem, L.stream>>>(L.tmQ, L.tmDO, L.tmK, L.tmV, p);
-      n += 1;
+      rc = launch_in_grids(g1, [&](long long off, long long cnt) {
+        BigBwdParams pp = p;
+        pp.item_offset = (int)off;
+        sf<<<(unsigned)cnt, sf_threads, sf_smem, L.stream>>>(L.tmQ, L.tmDO, L.tmK, L.tmV, pp);
+        ++n;
+        return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+      });
+      if (rc) return rc;
     }
     const long long g2 = 2 * gkv_c + (g1 > 0 ? gq : 0);
     if (g2 > 0) {  // phase 2: dV, dK of the chunk's key tiles, its part of dQ
-      gm<<<(unsigned)g2, 256, GB_SMEM, L.stream>>>(L.tmK64, L.tmDO64, L.tmQ64, p, (int)gkv_c);
-      n += 1;
+      rc = launch_in_grids(g2, [&](long long off, long long cnt) {
+        BigBwdParams pp = p;
+        pp.item_offset = (int)off;
+        gm<<<(unsigned)cnt, 256, GB_SMEM, L.stream>>>(L.tmK64, L.tmDO64, L.tmQ64, pp, (int)gkv_c);
+        ++n;
+        return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+      });
+      if (rc) return rc;
     }
   }
   *launches = n;

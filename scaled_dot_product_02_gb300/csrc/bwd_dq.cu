@@ -64,7 +64,7 @@ __global__ void __launch_bounds__(192, 1)
   using C = DqCfg;
   using E = Elem<BF16>;
   const Geom& g = p.g;
-  int idx = blockIdx.x;
+  int idx = blockIdx.x + p.item_offset;
   const int h = idx % g.hq;
   idx /= g.hq;
   const int b = idx % g.batch;
@@ -312,8 +312,12 @@ static int launch_dq_t(const DqLaunch& L) {
   const long long grid = (long long)L.p.n_q_tiles * L.p.g.hq * L.p.g.batch;
   if (grid <= 0) return SDPA_OK;
   if (grid > 0x7fffffffLL) return SDPA_ERR_UNSUPPORTED;
-  kern<<<(unsigned)grid, 192, DqCfg::SMEM_BYTES, L.stream>>>(L.tmQ, L.tmDO, L.tmK, L.tmV, L.p);
-  return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+  return launch_in_grids(grid, [&](long long off, long long n) {
+    DqParams p = L.p;
+    p.item_offset = (int)off;
+    kern<<<(unsigned)n, 192, DqCfg::SMEM_BYTES, L.stream>>>(L.tmQ, L.tmDO, L.tmK, L.tmV, p);
+    return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+  });
 }
 
 int launch_dq128(const DqLaunch& L, bool bf16) { return bf16 ? launch_dq_t<true>(L) : launch_dq_t<false>(L); }

@@ -62,7 +62,7 @@ __global__ void __launch_bounds__(256, 1)
   const Geom& g = p.g;
 
   // ---- which tile: heaviest (last) query tiles first, GQA heads adjacent
-  int idx = blockIdx.x;
+  int idx = blockIdx.x + p.item_offset;
   const int split = idx % p.dv_splits;
   idx /= p.dv_splits;
   const int h = idx % g.hq;
@@ -911,7 +911,8 @@ static int launch_fwd128(const FwdLaunch& L) {
     return SDPA_ERR_CUDA;
   FwdParams p = L.p;
   p.total_tiles = (int)tiles;
-  const long long grid = std::min<long long>((tiles + 1) / 2, sms);
+  long long grid = std::min<long long>((tiles + 1) / 2, sms);
+  if (debug_max_ctas() > 0) grid = std::min<long long>(grid, debug_max_ctas());  // tickets cover every tile
   if (cudaMemsetAsync(p.tile_counter, 0, sizeof(int), L.stream) != cudaSuccess) return SDPA_ERR_CUDA;
   kern<<<(unsigned)grid, Fwd2Cfg::THREADS, Fwd2Cfg::SMEM_BYTES, L.stream>>>(L.tmQ, L.tmK, L.tmV, p);
   return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
@@ -925,8 +926,12 @@ static int launch_fwd_t(const FwdLaunch& L) {
   const long long grid = (long long)L.p.n_q_tiles * L.p.g.hq * L.p.g.batch * L.p.dv_splits;
   if (grid <= 0) return SDPA_OK;
   if (grid > 0x7fffffffLL) return SDPA_ERR_UNSUPPORTED;
-  kern<<<(unsigned)grid, 256, C::SMEM_BYTES, L.stream>>>(L.tmQ, L.tmK, L.tmV, L.p);
-  return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+  return launch_in_grids(grid, [&](long long off, long long n) {
+    FwdParams p = L.p;
+    p.item_offset = (int)off;
+    kern<<<(unsigned)n, 256, C::SMEM_BYTES, L.stream>>>(L.tmQ, L.tmK, L.tmV, p);
+    return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+  });
 }
 
 int launch_fwd(const FwdLaunch& L, int head_dim, int head_dim_v, bool bf16) {

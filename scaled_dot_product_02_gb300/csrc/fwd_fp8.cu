@@ -1,0 +1,428 @@
+// fwd_fp8.cu -- FP8 (E4M3) attention forward for sm_103a, head_dim 128.
+//
+// Reading of TransformerEngine PR #3705's closing note on FP8 ("Amax S"):
+// with E4M3 inputs the softmax output is stored in E4M3 under the fixed
+// scale 448 (the format's largest value; no dropout), so no amax of it is
+// needed. Q, K, V are E4M3 codes with per-tensor descales d_q, d_k, d_v:
+//   S   = scale * d_q * d_k * Q8 K8^T            (tcgen05 kind::f8f6f4, fp32)
+//   P   = exp(S - LSE)  (masked; <= 1)            LSE = ln sum_j exp(S_ij)
+//   P8  = E4M3(P * 448)                           (round to nearest even)
+//   O   = P8 V8 * d_v / 448                       (kind::f8f6f4, written bf16/fp16)
+// P is normalised by the row's final LSE before it is rounded, so the kernel
+// makes two passes over the keys of a query tile: pass 1 computes S for
+// every key tile and keeps the row max and sum; pass 2 computes S again,
+// forms P and P8 against the final LSE and accumulates P8 V in TMEM. The
+// extra S costs 2*D flop per pair (1.5x the forward's MMA work, at the 8-bit
+// rate); in exchange O is never rescaled.
+//
+// Operands are K-major 128-byte-swizzled E4M3 tiles (128 rows x 128 bytes,
+// 16 KB): Q and K straight from their [row][head][128] tensors, and V from a
+// transposed copy Vt[head][d][key] that vt_kernel writes into the workspace
+// on every call (V is key-major in memory; as the B operand of P V it must
+// be contracted over keys). Each sequence's keys start on a 16-byte boundary
+// of Vt (TMA's alignment rule for the innermost coordinate), and the gaps
+// between sequences hold zeros.
+//
+// Roles (256 threads): warp 0 TMA producer, warp 1 TMEM allocator and MMA
+// issuer, warps 4-7 softmax and epilogue (one thread per query row).
+// TMEM: O [0,128), S/P buffers [128,256) and [256,384).
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace sdpa {
+
+namespace {
+
+constexpr int F8_BM = 128, F8_BN = 128, F8_D = 128;
+constexpr int F8_TILE = 16384;  // 128 rows x 128 one-byte columns
+constexpr int F8_NST = 8;
+constexpr int F8_NBARS = 2 * F8_NST + 7;
+constexpr int F8_SMEM = 1024 + F8_TILE + F8_NST * F8_TILE + F8_NBARS * 8 + 16;
+constexpr int F8_TM_O = 0, F8_TM_S = 128;
+
+// Instruction descriptor for kind::f8f6f4 with E4M3 A and B (format code 0),
+// both K-major, fp32 accumulator.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f8_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_f8_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Four fp32 values -> four E4M3 codes (round to nearest even, saturating to
+// +-448), x0 in the lowest byte: consecutive keys of the A operand in TMEM.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float x0, float x1, float x2, float x3) {
+  uint16_t lo, hi;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(lo) : "f"(x1), "f"(x0));
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(hi) : "f"(x3), "f"(x2));
+  return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+}  // namespace
+
+// First row of sequence b's keys in the transposed V (a multiple of 16):
+//   THD: roundup16(cu_kv[b]) + 16b    BSHD: b * roundup16(sk)    SBHD: 0
+__device__ __forceinline__ int vt_row0(const Geom& g, int b, const SeqInfo& si) {
+  if (g.layout == SDPA_THD) return ((si.krow0 + 15) & ~15) + 16 * b;
+  if (g.layout == SDPA_BSHD) return b * ((g.sk + 15) & ~15);
+  return 0;
+}
+
+// Vt[head][d][vt_row0(b) + key] = V[key row][head][d] for every key of every
+// sequence; the rows from the end of a sequence's keys up to the next
+// sequence's first row (and up to vt_rows after the last) are zeroed. One
+// block per (128-key slice, kv head, sequence).
+__global__ void __launch_bounds__(256) vt_kernel(const Fp8Params p) {
+  const Geom& g = p.g;
+  if (p.guard && *reinterpret_cast<volatile const int*>(p.guard)) return;
+  const int b = blockIdx.z, h = blockIdx.y, k0 = blockIdx.x * 128;
+  const SeqInfo si = seq_info(g, b);
+  const int r0 = vt_row0(g, b, si);
+  int seg;  // rows of this sequence's segment of Vt (a multiple of 16)
+  if (g.layout == SDPA_THD)
+    seg = (b + 1 < g.batch ? vt_row0(g, b + 1, seq_info(g, b + 1)) : p.vt_rows) - r0;
+  else
+    seg = (g.sk + 15) & ~15;
+  if (k0 >= seg) return;
+  const int kh = si.khead0 + h;
+  __shared__ __align__(16) uint8_t t[128][128 + 16];  // [key][d], rows padded against bank conflicts
+  for (int it = threadIdx.x; it < 128 * 8; it += 256) {
+    const int kk = it >> 3, c = it & 7;
+    const int key = k0 + kk;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (key < si.lk) v = *reinterpret_cast<const uint4*>(p.v + ((long long)(si.krow0 + key) * g.nh_kv + kh) * F8_D + c * 16);
+    *reinterpret_cast<uint4*>(&t[kk][c * 16]) = v;
+  }
+  __syncthreads();
+  for (int it = threadIdx.x; it < 128 * 8; it += 256) {
+    const int d = it >> 3, c = it & 7;
+    if (k0 + c * 16 >= seg) continue;
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      w[e] = (uint32_t)t[c * 16 + 4 * e][d] | ((uint32_t)t[c * 16 + 4 * e + 1][d] << 8) |
+             ((uint32_t)t[c * 16 + 4 * e + 2][d] << 16) | ((uint32_t)t[c * 16 + 4 * e + 3][d] << 24);
+    *reinterpret_cast<uint4*>(p.vt + ((long long)kh * F8_D + d) * p.vt_rows + r0 + k0 + c * 16) =
+        make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+template <bool BF16>
+__global__ void __launch_bounds__(256, 1)
+    fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                   const __grid_constant__ CUtensorMap tmVt, const __grid_constant__ Fp8Params p) {
+  using E = Elem<BF16>;
+  const Geom& g = p.g;
+
+  // ---- which tile: heaviest (last) query tiles first, GQA heads adjacent
+  int idx = blockIdx.x + p.item_offset;
+  const int h = idx % g.hq;
+  idx /= g.hq;
+  const int b = idx % g.batch;
+  idx /= g.batch;
+  const int qt = p.n_q_tiles - 1 - idx;
+  const SeqInfo si = seq_info(g, b);
+  const int q0 = qt * F8_BM;
+  if (q0 >= si.lq) return;
+  if (p.guard && *reinterpret_cast<volatile const int*>(p.guard)) return;
+
+  const KeyRange kr = key_range(g, si.lq, si.lk);
+  const int q_last = min(q0 + F8_BM - 1, si.lq - 1);
+  const int kv_lo = kr.lo(q0), kv_hi = kr.hi(q_last);
+  const int t_lo = kv_lo / F8_BN;
+  const int n = (kv_hi > kv_lo) ? (kv_hi + F8_BN - 1) / F8_BN - t_lo : 0;
+  const int steps = 2 * n;  // pass 1 (max, sum) then pass 2 (P8, P8 V) over the same key tiles
+  const int qhead = si.qhead0 + h;
+  const int khead = si.khead0 + h / (g.hq / g.hkv);
+  const int vrow0 = vt_row0(g, b, si);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* sQ = smem;
+  uint8_t* sStage = smem + F8_TILE;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sStage + F8_NST * F8_TILE);
+  uint64_t* empty = full + F8_NST;
+  uint64_t* bar_q = empty + F8_NST;
+  uint64_t* bar_s = bar_q + 1;  // [2] S of a step ready
+  uint64_t* bar_p = bar_s + 2;  // [2] the softmax is done with a step's buffer (pass 2: P8 written)
+  uint64_t* bar_o = bar_p + 2;  // the last P8 V (and so every MMA) complete
+  uint64_t* bar_drain = bar_o + 1;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < F8_NST; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    mbar_init(bar_q, 1);
+    mbar_init(&bar_s[0], 1);
+    mbar_init(&bar_s[1], 1);
+    mbar_init(&bar_p[0], 128);
+    mbar_init(&bar_p[1], 128);
+    mbar_init(bar_o, 1);
+    mbar_init(bar_drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_holder;
+
+  // Ring order (the MMA warp consumes in the same order): K of steps 0 and 1;
+  // then for every step u, Vt of its key tile if u is a pass-2 step, and K of
+  // step u + 2. Step u covers key tile (u < n ? u : u - n).
+  if (warp == 0) {
+    if (elect_one() && n > 0) {
+      prefetch_tmap(&tmQ);
+      prefetch_tmap(&tmK);
+      prefetch_tmap(&tmVt);
+      mbar_arrive_expect_tx(bar_q, F8_TILE);
+      tma_load_3d(&tmQ, bar_q, sQ, 0, qhead, si.qrow0 + q0);
+      int c = 0;
+      bool ok = true;
+      auto load = [&](bool v_tile, int tile) -> bool {
+        const int slot = c % F8_NST;
+        if (!mbar_wait(&empty[slot], ((c / F8_NST) & 1) ^ 1, abort_flag)) return false;
+        mbar_arrive_expect_tx(&full[slot], F8_TILE);
+        uint8_t* dst = sStage + slot * F8_TILE;
+        if (v_tile)
+          tma_load_3d(&tmVt, &full[slot], dst, vrow0 + (t_lo + tile) * F8_BN, 0, khead);
+        else
+          tma_load_3d(&tmK, &full[slot], dst, 0, khead, si.krow0 + (t_lo + tile) * F8_BN);
+        ++c;
+        return true;
+      };
+      for (int u = 0; u < 2 && u < steps && ok; ++u) ok = load(false, u < n ? u : u - n);
+      for (int u = 0; u < steps && ok; ++u) {
+        if (u >= n) ok = load(true, u - n);
+        if (ok && u + 2 < steps) ok = load(false, u + 2 < n ? u + 2 : u + 2 - n);
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        record_error(p.err, SDPA_ERR_TIMEOUT);
+      }
+      const int first = c > F8_NST ? c - F8_NST : 0;
+      for (int k = first; k < c; ++k) mbar_wait_drain(&full[k % F8_NST], (k / F8_NST) & 1);
+      mbar_wait_drain(bar_q, 0);
+    }
+  } else if (warp == 1) {
+    if (elect_one() && n > 0) {
+      constexpr uint32_t IDESC = idesc_e4m3(128, 128);
+      int c = 0;
+      bool ok = mbar_wait(bar_q, 0, abort_flag);
+      tc_fence_after();
+      const uint32_t q_base = smem_u32(sQ);
+      auto mma_s = [&](int u) -> bool {
+        const int slot = c % F8_NST;
+        if (!mbar_wait(&full[slot], (c / F8_NST) & 1, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t kb = smem_u32(sStage + slot * F8_TILE);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)  // 32 one-byte columns per MMA
+          mma_f8_ss(tmem + F8_TM_S + (u & 1) * 128, smem_desc_sw128(q_base + ks * 32, 16, 1024),
+                    smem_desc_sw128(kb + ks * 32, 16, 1024), IDESC, ks != 0);
+        mma_commit(&empty[slot]);
+        mma_commit(&bar_s[u & 1]);
+        ++c;
+        return true;
+      };
+      auto mma_o = [&](int u) -> bool {
+        const int slot = c % F8_NST;
+        if (!mbar_wait(&full[slot], (c / F8_NST) & 1, abort_flag)) return false;
+        tc_fence_after();
+        const uint32_t vb = smem_u32(sStage + slot * F8_TILE);
+        const uint32_t pcol = tmem + F8_TM_S + (u & 1) * 128;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)  // 32 keys per MMA: 8 TMEM columns of packed P8
+          mma_f8_ts(tmem + F8_TM_O, pcol + ks * 8, smem_desc_sw128(vb + ks * 32, 16, 1024), IDESC,
+                    (u - n) > 0 || ks != 0);
+        mma_commit(&empty[slot]);
+        if (u == steps - 1) mma_commit(bar_o);  // one completion: every P8 V is done
+        ++c;
+        return true;
+      };
+      for (int u = 0; u < 2 && u < steps && ok; ++u) ok = mma_s(u);
+      for (int u = 0; u < steps && ok; ++u) {
+        if (!mbar_wait(&bar_p[u & 1], (u >> 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (u >= n) ok = mma_o(u);
+        // S of step u + 2 reuses step u's buffer: the MMAs run in issue order, so
+        // it lands after P8 V of step u has read the buffer
+        if (ok && u + 2 < steps) ok = mma_s(u + 2);
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        record_error(p.err, SDPA_ERR_TIMEOUT);
+        mma_commit(bar_drain);
+        mbar_wait_drain(bar_drain, 0);
+      }
+    }
+  } else if (warp >= 4) {
+    const int wq = warp - 4;
+    const int r = wq * 32 + lane;
+    const int i = q0 + r;
+    const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
+    const float sl2 = g.scale_log2;
+    const int lo_i = kr.lo(i), hi_i = kr.hi(i);
+    const int lo_last = kr.lo(q_last), hi_first = kr.hi(q0);
+    float m = -INFINITY, l = 0.f;  // pass 1: running max (raw score units) and sum
+    float mb2 = INFINITY;          // pass 2: log2 of the row's normaliser, LSE * log2e
+    bool ok = true;
+    for (int u = 0; u < steps; ++u) {
+      if (!__all_sync(0xffffffffu, mbar_wait(&bar_s[u & 1], (u >> 1) & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t scol = lane_base + F8_TM_S + (u & 1) * 128;
+      float s[128];
+      {
+        uint32_t u0[32], u1[32], u2[32], u3[32];
+        tmem_ld32(scol, u0);
+        tmem_ld32(scol + 32, u1);
+        tmem_ld32(scol + 64, u2);
+        tmem_ld32(scol + 96, u3);
+        tmem_wait_ld();
+        reg_fence(u0);
+        reg_fence(u1);
+        reg_fence(u2);
+        reg_fence(u3);
+#pragma unroll
+        for (int cc = 0; cc < 32; ++cc) {
+          s[cc] = __uint_as_float(u0[cc]);
+          s[32 + cc] = __uint_as_float(u1[cc]);
+          s[64 + cc] = __uint_as_float(u2[cc]);
+          s[96 + cc] = __uint_as_float(u3[cc]);
+        }
+      }
+      const int kb = (t_lo + (u < n ? u : u - n)) * F8_BN;
+      if (!(lo_last <= kb && hi_first >= kb + F8_BN)) {  // edge tile (uniform branch)
+#pragma unroll
+        for (int cc = 0; cc < 128; ++cc) s[cc] = in_range(kb + cc, lo_i, hi_i) ? s[cc] : -INFINITY;
+      }
+      if (u < n) {
+        float mt = s[0];
+#pragma unroll
+        for (int cc = 1; cc < 128; ++cc) mt = fmaxf(mt, s[cc]);
+        const float m_new = fmaxf(m, mt);
+        if (m_new != -INFINITY) {
+          const float mb = m_new * sl2;
+          float rs = 0.f;
+#pragma unroll
+          for (int cc = 0; cc < 128; ++cc) rs += ex2(fmaf(s[cc], sl2, -mb));
+          l = (m == -INFINITY ? 0.f : l * ex2((m - m_new) * sl2)) + rs;
+          m = m_new;
+        }
+        if (u == n - 1) mb2 = l > 0.f ? m * sl2 + __log2f(l) : INFINITY;
+      } else {
+        uint32_t pk[32];
+#pragma unroll
+        for (int cc = 0; cc < 32; ++cc)
+          pk[cc] = pack_e4m3x4(ex2(fmaf(s[4 * cc], sl2, -mb2)) * 448.f, ex2(fmaf(s[4 * cc + 1], sl2, -mb2)) * 448.f,
+                               ex2(fmaf(s[4 * cc + 2], sl2, -mb2)) * 448.f, ex2(fmaf(s[4 * cc + 3], sl2, -mb2)) * 448.f);
+        tmem_st32(scol, pk);
+        tmem_wait_st();
+      }
+      tc_fence_before();
+      mbar_arrive(&bar_p[u & 1]);
+    }
+    if (ok && n > 0) {
+      ok = __all_sync(0xffffffffu, mbar_wait(bar_o, 0, abort_flag));
+      tc_fence_after();
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      record_error(p.err, SDPA_ERR_TIMEOUT);
+    } else {
+      const bool valid = i < si.lq;
+      const float mul = l > 0.f ? p.o_scale : 0.f;
+      using T = typename E::T;
+      T* orow = reinterpret_cast<T*>(p.o) + ((long long)(si.qrow0 + i) * g.nh_q + qhead) * F8_D;
+#pragma unroll 1
+      for (int cc = 0; cc < F8_D / 32; ++cc) {
+        uint32_t packed[16];
+        if (n > 0) {
+          uint32_t uu[32];
+          tmem_ld32(lane_base + F8_TM_O + cc * 32, uu);
+          tmem_wait_ld();
+          reg_fence(uu);
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            packed[e] = E::pack(__uint_as_float(uu[2 * e]) * mul, __uint_as_float(uu[2 * e + 1]) * mul);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) packed[e] = 0u;
+        }
+        if (valid) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            dst[e] = make_uint4(packed[4 * e], packed[4 * e + 1], packed[4 * e + 2], packed[4 * e + 3]);
+        }
+      }
+      if (valid) p.lse[(long long)(si.qrow0 + i) * g.nh_q + qhead] = l > 0.f ? m * g.scale + logf(l) : -INFINITY;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+int launch_vt(const Fp8Params& p, cudaStream_t stream) {
+  const int max_seg = p.g.layout == SDPA_THD ? p.g.sk + 32 : ((p.g.sk + 15) & ~15);
+  if (p.g.batch <= 0 || max_seg <= 0) return SDPA_OK;
+  if (p.g.batch > 65535 || p.g.hkv > 65535) return SDPA_ERR_UNSUPPORTED;
+  const dim3 grid((unsigned)((max_seg + 127) / 128), (unsigned)p.g.hkv, (unsigned)p.g.batch);
+  vt_kernel<<<grid, 256, 0, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+}
+
+int launch_fwd_fp8(const Fp8Launch& L, bool bf16) {
+  const Fp8Params& p = L.p;
+  const long long grid = (long long)p.n_q_tiles * p.g.hq * p.g.batch;
+  if (grid > 0x7fffffffLL) return SDPA_ERR_UNSUPPORTED;
+  auto kern = bf16 ? fwd_fp8_kernel<true> : fwd_fp8_kernel<false>;
+  if (const int rc = set_kernel_smem(reinterpret_cast<const void*>(kern), F8_SMEM, -1)) return rc;
+  return launch_in_grids(grid, [&](long long off, long long count) {
+    Fp8Params pp = p;
+    pp.item_offset = (int)off;
+    kern<<<(unsigned)count, 256, F8_SMEM, L.stream>>>(L.tmQ, L.tmK, L.tmVt, pp);
+    return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+  });
+}
+
+}  // namespace sdpa

@@ -8,6 +8,25 @@
 
 namespace sdpa {
 
+// Testing aid (sdpa_debug_set_max_ctas): the most CTAs a kernel may have in
+// one launch, 0 = no cap.
+int debug_max_ctas();
+
+// Launch `total` CTAs as one grid, or, under a CTA cap, as successive grids of
+// at most that many CTAs: fn(offset, count) launches CTAs [offset,
+// offset + count) of the index space (kernels add their params' item_offset
+// to blockIdx.x). Returns the first failing status.
+template <class F>
+int launch_in_grids(long long total, F&& fn) {
+  const long long cap = debug_max_ctas();
+  if (cap <= 0 || total <= cap) return total > 0 ? fn(0LL, total) : 0;
+  for (long long off = 0; off < total; off += cap) {
+    const int rc = fn(off, total - off < cap ? total - off : cap);
+    if (rc) return rc;
+  }
+  return 0;
+}
+
 // Raise a kernel's dynamic shared-memory limit to `bytes` and, when
 // carveout >= 0, set its preferred shared-memory carveout (percent), once per
 // (kernel, current device): function attributes belong to each device's
@@ -25,6 +44,7 @@ struct FwdParams {
   int dv_splits;     // 1, or 2 when each CTA owns half of the value columns
   int* tile_counter;  // head_dim 128: ticket counter in the workspace (zeroed per call)
   int total_tiles;    // head_dim 128: tickets (query tiles x heads x batch)
+  int item_offset;       // added to blockIdx.x (launches split under a CTA cap)
 };
 
 struct FwdLaunch {
@@ -47,6 +67,7 @@ struct BwdParams {
   const int* guard;
   int n_kv_tiles;        // ceil(seqlen_kv / 128)
   int d_lo, d_hi;        // dK/dV columns this launch owns (all of D for head_dim 128)
+  int item_offset;       // added to blockIdx.x (launches split under a CTA cap)
 };
 
 struct BwdLaunch {
@@ -70,6 +91,7 @@ struct DqParams {
   int* err;
   const int* guard;
   int n_q_tiles;
+  int item_offset;       // added to blockIdx.x (launches split under a CTA cap)
 };
 struct DqLaunch {
   CUtensorMap tmQ, tmDO, tmK, tmV;  // 128-row boxes
@@ -97,6 +119,7 @@ struct BigBwdParams {
   int chunk;               // key tiles per chunk (the last chunk may be shorter)
   float* dq_acc;           // [nh_q][rows_q][D] fp32 dQ sum over chunks, zeroed by the
                            // preprocess; nullptr when one chunk covers every key tile
+  int item_offset;       // added to blockIdx.x (launches split under a CTA cap)
 };
 
 struct BigBwdLaunch {
@@ -107,6 +130,29 @@ struct BigBwdLaunch {
 };
 
 int launch_bwd_big(const BigBwdLaunch& L, int head_dim, bool bf16, int* launches);
+
+// FP8 E4M3 forward, head_dim 128 (fwd_fp8.cu): vt_kernel writes V transposed
+// into the workspace, fwd_fp8_kernel computes O and LSE.
+struct Fp8Params {
+  Geom g;               // scale / scale_log2 include the Q and K descales
+  const uint8_t* v;     // E4M3 V [rows_kv][nh_kv][128]
+  uint8_t* vt;          // transposed V [nh_kv][128][vt_rows] (workspace)
+  int vt_rows;          // keys of Vt per (head, d): every sequence 16-aligned, gaps zero
+  void* o;              // [rows_q][nh_q][128], bf16 or fp16
+  float* lse;
+  int* err;
+  const int* guard;
+  int n_q_tiles;
+  float o_scale;        // d_v / 448
+  int item_offset;       // added to blockIdx.x (launches split under a CTA cap)
+};
+struct Fp8Launch {
+  CUtensorMap tmQ, tmK, tmVt;  // E4M3 128-byte rows, 128-row boxes; Vt 128 keys x 128 d boxes
+  Fp8Params p;
+  cudaStream_t stream;
+};
+int launch_vt(const Fp8Params& p, cudaStream_t stream);
+int launch_fwd_fp8(const Fp8Launch& L, bool bf16);
 
 // Memory-bound helpers (aux.cu).
 struct PrepParams {

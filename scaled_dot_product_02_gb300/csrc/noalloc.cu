@@ -5,15 +5,17 @@
 // host application owns every device allocation and forbids others, a C
 // program with no allocator of its own, or a latency-critical path that must
 // not pay the device-wide synchronisation a cudaMalloc/cudaFree can cause.
-// This entry point takes the backward's scratch (per-row statistics and the
-// fp32 dQ accumulator) from a fixed array in the library's own device memory
-// instead, so it needs no workspace argument and allocates nothing.
+// This entry point takes the backward's scratch (per-row statistics, the fp32
+// dQ accumulator and, at head_dim 256/512, the P / dS score tiles of a chunk
+// of keys) from a fixed array in the library's own device memory instead, so
+// it needs no workspace argument and allocates nothing.
 //
 // The array below is created when the library's device code is loaded and
 // every GPU that loads it holds SDPA_BWD_NOALLOC_MAX_BYTES until the process
 // exits. All calls share it and it keeps the previous call's contents; the
-// backward's kernels rewrite everything they read from it (the statistics and
-// the accumulator are rebuilt by the preprocess kernel on every call), so
+// backward's kernels rewrite everything they read from it (the preprocess
+// kernel rebuilds the statistics and zeroes the accumulator on every call,
+// and each score tile is written before the GEMMs of its chunk read it), so
 // nothing stale is used. Calls that overlap on the GPU (for example on two
 // streams at once) race on the array and must be serialised by the caller.
 #include <cuda_runtime.h>

@@ -1,0 +1,123 @@
+"""FP8 E4M3 forward (sdpa_fwd_fp8, head_dim 128) against the float64 oracle.
+
+The kernel follows the oracle's definition step for step (TransformerEngine
+PR #3705, closing note on FP8: the softmax output is stored in E4M3 under the
+fixed scale 448): S on the decoded codes, P = exp(S - LSE) against the row's
+final LSE, P8 = E4M3(P * 448) rounded once, O = P8 V * d_v / 448. The two
+computations of P differ only by float32 rounding (relative error well under
+2^-12), so a P8 code can differ from the oracle's only where P * 448 lies
+within 2^-12 of its value of an E4M3 rounding midpoint, and then by one E4M3
+step. The bound for every element of O is therefore
+    (d_v/448) * sum over those near-midpoint keys of step * |v|
+  + (d_v/448) * 4e-5 * sum_j P8_j |v_j|        (fp32 accumulation of the MMA)
+  + u * |O_ref|            (rounding O to bf16 / fp16: u = 2^-8 / 2^-11)
+with the near-midpoint keys found from the oracle's own probabilities, and
+LSE within 1e-4. Rows with no allowed key give O = 0 and LSE = -inf exactly.
+"""
+import numpy as np
+import pytest
+
+import workloads
+from workloads import Workload
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    (Workload("fp8_bshd_causal_gqa", "bshd", "causal", 2, 300, 300, 4, 2, 128, "bf16"), None),
+    (Workload("fp8_thd_varlen", "thd", "causal", 4, 300, 300, 4, 1, 128, "bf16", len_range=(1, 300)), None),
+    (Workload("fp8_sbhd_nomask_fp16", "sbhd", "none", 2, 200, 260, 2, 2, 128, "fp16"), None),
+    (Workload("fp8_bottom_right_more_queries", "bshd", "causal_br", 1, 300, 140, 2, 1, 128, "bf16"), None),
+    (Workload("fp8_window", "bshd", "causal", 1, 400, 400, 2, 2, 128, "bf16", window=(100, 0)), None),
+    (Workload("fp8_thd_unequal_bottom_right", "thd", "causal_br", 5, 300, 333, 4, 2, 128, "bf16"),
+     ([300, 1, 129, 200, 64], [140, 250, 129, 333, 1])),
+]
+UNIT = {"bf16": 2.0 ** -8, "fp16": 2.0 ** -11}  # unit roundoff of the output format
+
+
+def _e4m3_step(x):
+    """Distance between adjacent E4M3 values around x >= 0 (2^-9 among the
+    subnormals, 2^(e-3) in [2^e, 2^(e+1)))."""
+    e = np.floor(np.log2(np.maximum(x, 2.0 ** -30)))
+    return 2.0 ** (np.maximum(e, -6.0) - 3.0)
+
+
+def _kv_rows(w, inp, b):
+    if w.layout == "thd":
+        return slice(int(inp["cu_seqlens_kv"][b]), int(inp["cu_seqlens_kv"][b + 1]))
+    return b
+
+
+def _q_rows(w, inp, b):
+    """Token rows of sequence b's queries, in order."""
+    if w.layout == "thd":
+        return np.arange(int(inp["cu_seqlens_q"][b]), int(inp["cu_seqlens_q"][b + 1]))
+    if w.layout == "bshd":
+        return b * w.seqlen_q + np.arange(w.seqlen_q)
+    return np.arange(w.seqlen_q) * w.batch + b
+
+
+def _bound(w, inp, probs, o_ref, v):
+    """Elementwise bound on |O - O_ref| (see the module docstring)."""
+    dvs = workloads.FP8_DESCALE[2]
+    x = probs * 448.0
+    step = _e4m3_step(x)
+    frac = x / step - np.floor(x / step)
+    near = (np.abs(frac - 0.5) * step <= 2.0 ** -12 * x) & (x > 0)
+    tie_w = np.where(near, step, 0.0)
+    acc_w = x * 4e-5
+    o_flat = o_ref.reshape(-1, w.heads_q, w.head_dim)
+    bound = np.zeros_like(o_flat)
+    group = w.heads_q // w.heads_kv
+    nb = len(inp["cu_seqlens_q"]) - 1 if w.layout == "thd" else w.batch
+    for b in range(nb):
+        rows = _q_rows(w, inp, b)
+        if w.layout == "sbhd":
+            vb = np.abs(v[:, b])  # (Sk, Hkv, 128)
+        else:
+            vb = np.abs(v[_kv_rows(w, inp, b)])
+        lk = vb.shape[0]
+        for h in range(w.heads_q):
+            vh = vb[:, h // group, :]
+            bound[rows, h] = (tie_w[rows, h, :lk] @ vh) * (1 + 2.0 ** -8) + acc_w[rows, h, :lk] @ vh
+    bound *= dvs / 448.0
+    return bound + UNIT[w.dtype] * np.abs(o_flat) + 1e-7
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: c[0].name)
+def test_fp8_forward_matches_oracle(case):
+    import torch
+
+    from oracle import oracle
+    from parity import gpu_kwargs
+    from scaled_dot_product_02_gb300 import sdpa_fwd_fp8, sdpa_get_device_error
+
+    w, lens = case
+    inp = workloads.fp8_inputs(w, seed=61, lengths=None if lens is None else tuple(np.array(x) for x in lens))
+    kw = gpu_kwargs(w, inp)
+    q8, k8, v8 = (torch.from_numpy(inp[x]).cuda() for x in ("q8", "k8", "v8"))
+    out_dtype = {"bf16": torch.bfloat16, "fp16": torch.float16}[w.dtype]
+    o, lse = sdpa_fwd_fp8(q8, k8, v8, descale=workloads.FP8_DESCALE, out_dtype=out_dtype, **kw)
+    assert sdpa_get_device_error() == 0
+    o = o.float().cpu().numpy().astype(np.float64)
+    lse = lse.cpu().numpy().astype(np.float64)
+
+    okw = dict(layout=w.layout, mask=w.mask, scale=w.scale, window=w.window)
+    if w.layout == "thd":
+        okw.update(cu_q=inp["cu_seqlens_q"], cu_kv=inp["cu_seqlens_kv"])
+    o_ref, l_ref = oracle.fwd_fp8(inp["q8"], inp["k8"], inp["v8"], descale=workloads.FP8_DESCALE, **okw)
+    dq, dk, dv = workloads.FP8_DESCALE
+    qd, kd, vd = (oracle.e4m3_decode(inp[x]) for x in ("q8", "k8", "v8"))
+    probs = oracle.probs(qd * dq, kd * dk, **okw)
+    bound = _bound(w, inp, probs, o_ref, vd).reshape(o.shape)
+
+    empty = np.isneginf(l_ref)
+    assert np.all(np.isneginf(lse[empty])), "rows without keys must have LSE = -inf"
+    assert np.all(o.reshape(-1, w.heads_q, w.head_dim)[empty] == 0), "rows without keys must have O = 0"
+    with np.errstate(invalid="ignore"):
+        lse_err = float(np.max(np.abs(np.where(empty, 0.0, lse - l_ref))))
+    excess = np.abs(o - o_ref) / bound
+    worst = float(np.max(excess))
+    print(f"[{w.name}] O: max|O-O_ref|={np.max(np.abs(o - o_ref)):.3e} worst err/bound={worst:.3f} "
+          f"median bound={np.median(bound):.3e}; LSE err={lse_err:.3e} ({int(empty.sum())} empty rows)")
+    assert lse_err <= 1e-4
+    assert worst <= 1.0, f"O exceeds its bound by {worst:.2f}x"

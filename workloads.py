@@ -138,6 +138,30 @@ def make_inputs(w: Workload, seed: int | None = None, lengths=None):
     return out
 
 
+def e4m3_codes(x: np.ndarray) -> np.ndarray:
+    """E4M3 codes (uint8, the finite-only OCP format) nearest to float64
+    values, through torch's float8_e4m3fn conversion (round to nearest even,
+    saturating): the FP8 inputs are these codes of seeded normal masters."""
+    import torch
+
+    t = torch.from_numpy(np.asarray(x, dtype=np.float32)).clamp(-448.0, 448.0)
+    return t.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+
+
+FP8_STD = 3.0                     # the codes' masters are N(0, 1) * 3 (a spread over most of E4M3's range)
+FP8_DESCALE = (0.5, 0.25, 0.125)  # per-tensor descales of Q, K, V
+
+
+def fp8_inputs(w: Workload, seed: int | None = None, lengths=None) -> dict:
+    """make_inputs' draws for `w`, each master times FP8_STD, as E4M3 codes
+    q8, k8, v8 (cu_seqlens copied); dO is not drawn into codes."""
+    inp = make_inputs(w, seed=seed, lengths=lengths)
+    out = {key: val for key, val in inp.items() if key.startswith("cu_")}
+    for key in ("q", "k", "v"):
+        out[key + "8"] = e4m3_codes(inp[key] * FP8_STD)
+    return out
+
+
 def rounded(inputs: dict, dtype: str) -> dict:
     """The dtype-rounded copies (as float64) of q, k, v, do; other keys copied."""
     out = dict(inputs)
