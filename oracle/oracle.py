@@ -280,8 +280,9 @@ def e4m3_round(x):
 def fwd_fp8(q8, k8, v8, *, descale=(1.0, 1.0, 1.0), scale_s=448.0, layout="bshd", mask="none", scale=None,
             window=(-1, -1), cu_q=None, cu_kv=None):
     """FP8 E4M3 forward: q8/k8/v8 are E4M3 codes (uint8) in their layouts with
-    per-tensor descales (d_q, d_k, d_v); the softmax output is stored as
-    E4M3(P * scale_s) and O = P8 V * d_v / scale_s. Returns (o, lse) like fwd."""
+    per-tensor descales (d_q, d_k, d_v); the softmax output normalised by its
+    row maximum is stored as P8 = E4M3(exp(s - m) * scale_s) and
+    O = P8 V * d_v / (scale_s * sum_j exp(s_j - m)). Returns (o, lse) like fwd."""
     q8, k8, v8 = (np.ascontiguousarray(x, dtype=np.uint8) for x in (q8, k8, v8))
     scale = 1.0 / np.sqrt(q8.shape[-1]) if scale is None else scale
     p = Problem(q8, k8, layout, mask, scale, window, cu_q, cu_kv, v=v8)

@@ -531,17 +531,20 @@ int sdpa_oracle_probs(const oracle_problem* p, const double* q, const double* k,
 }
 
 /*
- * FP8 E4M3 forward (the FP8 variant of this kernel family). Reading of TransformerEngine PR #3705's closing note
- * ("Amax S"): with E4M3 inputs the softmax output is stored in E4M3 under a
- * fixed scale, 448 (the format's largest value) without dropout, so no
- * amax of it is ever needed. Written out:
+ * FP8 E4M3 forward (the FP8 variant of this kernel family). Reading of
+ * TransformerEngine PR #3705's closing note ("Amax S"): with E4M3 inputs the
+ * softmax output is stored in E4M3 under a fixed scale, 448 (the format's
+ * largest value) without dropout, so no amax of it is ever needed. A fixed
+ * scale does that only if the stored probabilities are normalised by the
+ * row's largest one (then the largest is stored as 448 exactly); they are
+ * divided by the row sum after the product with V. Written out:
  *   Q, K, V are E4M3 codes with per-tensor descales d_q, d_k, d_v (the real
  *   value of a code c is decode(c) * d);
  *   s_ij  = scale * d_q * d_k * sum_d decode(q_id) decode(k_jd), masked as above;
- *   LSE_i = ln sum_j exp(s_ij);  p_ij = exp(s_ij - LSE_i);
- *   P8_ij = e4m3(p_ij * scale_s);
- *   o_i   = sum_j P8_ij decode(v_j) * d_v / scale_s.
- * The softmax is exact (float64, final LSE); only the stored P is rounded.
+ *   m_i   = max_j s_ij;  L_i = sum_j exp(s_ij - m_i);  LSE_i = m_i + ln L_i;
+ *   P8_ij = e4m3(exp(s_ij - m_i) * scale_s);
+ *   o_i   = sum_j P8_ij decode(v_j) * d_v / (scale_s * L_i).
+ * The softmax is exact (float64); only the stored P is rounded.
  */
 
 /* E4M3, the finite-only variant of the OCP 8-bit float: sign bit, 4 exponent
@@ -621,13 +624,17 @@ int sdpa_oracle_fwd_fp8(const oracle_problem* p, const uint8_t* q8, const uint8_
                     lse[r * hq + h] = l;
                     if (l == -INFINITY) continue;
                     int g = kv_head_of(p, h);
+                    double m = -INFINITY, sum = 0.0;
+                    for (int j = 0; j < lk; ++j)
+                        if (srow[j] > m) m = srow[j];
                     for (int j = 0; j < lk; ++j) {
                         if (srow[j] == -INFINITY) continue;
-                        double p8 = sdpa_oracle_e4m3_round(exp(srow[j] - l) * scale_s);
+                        sum += exp(srow[j] - m);
+                        double p8 = sdpa_oracle_e4m3_round(exp(srow[j] - m) * scale_s);
                         const double* vj = vrow(p, vd, cu_kv, b, j, g);
                         for (int d = 0; d < DV; ++d) orow[d] += p8 * vj[d];
                     }
-                    for (int d = 0; d < DV; ++d) orow[d] *= descale_v / scale_s;
+                    for (int d = 0; d < DV; ++d) orow[d] *= descale_v / (scale_s * sum);
                 }
             free(srow);
         }

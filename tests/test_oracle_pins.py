@@ -535,9 +535,12 @@ def test_fp8_scores_and_lse_equal_the_float64_forward_on_decoded_inputs(layout, 
     assert np.max(err) > 1e-6 * vmax  # the rounding of P is really applied
 
 
-def test_fp8_zero_keys_give_the_quantised_uniform_average():
-    """Closed form: K = 0 makes every allowed score 0, so P = 1/n for the n
-    keys a row sees and O = e4m3(448/n)/448 * d_v * (sum of those v rows)."""
+def test_fp8_zero_keys_give_the_exact_uniform_average():
+    """Closed form: K = 0 makes every allowed score equal, so every
+    probability normalised by the row maximum is exp(0) = 1, stored as 448
+    exactly, and O is d_v times the mean of the n value rows a row sees, with
+    no rounding at all (normalising by the row sum instead would store
+    e4m3(448 / n) and miss the mean for most n)."""
     r = rng(72)
     q8 = _e4m3_codes(r.standard_normal((1, 9, 2, 8)))
     k8 = np.zeros((1, 9, 1, 8), dtype=np.uint8)
@@ -546,10 +549,25 @@ def test_fp8_zero_keys_give_the_quantised_uniform_average():
     v = oracle.e4m3_decode(v8)[0, :, 0]
     for i in range(9):
         n = i + 1
-        w = oracle.e4m3_round(np.array([448.0 / n]))[0] / 448.0
-        np.testing.assert_allclose(o[0, i, 0], w * 0.5 * v[:n].sum(axis=0), rtol=1e-14, atol=1e-15)
+        np.testing.assert_allclose(o[0, i, 0], 0.5 * v[:n].mean(axis=0), rtol=1e-14, atol=1e-15)
         np.testing.assert_allclose(o[0, i, 1], o[0, i, 0], rtol=0, atol=0)   # both q heads read kv head 0
         assert lse[i, 0] == pytest.approx(math.log(n), abs=1e-14)
+
+
+def test_fp8_stored_probabilities_are_relative_to_the_row_maximum():
+    """Two keys with scores s and s - ln 2: normalised by the row maximum the
+    stored values are 448 and 224, both exact in E4M3, so O is the weighted
+    mean (v0 + v1 / 2) / 1.5 without rounding, whatever the row's scale."""
+    q8 = np.zeros((1, 2, 1, 4), dtype=np.uint8)
+    k8 = np.zeros((1, 2, 1, 4), dtype=np.uint8)
+    q8[..., 0] = _e4m3_codes([1.0])[0]
+    k8[0, 0, 0, 0] = _e4m3_codes([2.0])[0]
+    k8[0, 1, 0, 0] = _e4m3_codes([1.0])[0]
+    v8 = _e4m3_codes(rng(74).standard_normal((1, 2, 1, 4)))
+    o, lse = oracle.fwd_fp8(q8, k8, v8, layout="bshd", mask="none", scale=math.log(2.0))
+    v = oracle.e4m3_decode(v8)[0, :, 0]
+    np.testing.assert_allclose(o[0, 1, 0], (v[0] + 0.5 * v[1]) / 1.5, rtol=1e-15, atol=1e-16)
+    assert lse[1, 0] == pytest.approx(2 * math.log(2.0) + math.log(1.5), abs=1e-14)
 
 
 def test_fp8_dominant_key_returns_its_value_exactly():
