@@ -638,6 +638,158 @@ def companion_measure(w, steps, warmup, dev, flush, peak):
     return out
 
 
+def fp8_oracle_sample(w, inp8, seconds_target):
+    """The float64 FP8 oracle on the first query tokens of sequence 0 with one
+    kv head and its q heads, grown until one run takes about
+    `seconds_target`; returns its TFLOP/s under the exact-mask count."""
+    import time
+
+    from oracle import oracle
+
+    group = w.heads_q // w.heads_kv
+    lq0 = int(inp8["cu_seqlens_q"][1]) if w.layout == "thd" else w.seqlen_q
+    ls, dt, fl = 128, 0.0, 0
+    while True:
+        lq = min(ls, lq0)
+        if w.layout == "thd":
+            q8, k8, v8 = inp8["q8"][:lq, :group], inp8["k8"][:lq, :1], inp8["v8"][:lq, :1]
+            kw = dict(layout="thd", cu_q=np.array([0, lq], np.int32), cu_kv=np.array([0, lq], np.int32))
+        elif w.layout == "bshd":
+            q8, k8, v8 = inp8["q8"][:1, :lq, :group], inp8["k8"][:1, :lq, :1], inp8["v8"][:1, :lq, :1]
+            kw = dict(layout="bshd")
+        else:
+            q8, k8, v8 = inp8["q8"][:lq, :1, :group], inp8["k8"][:lq, :1, :1], inp8["v8"][:lq, :1, :1]
+            kw = dict(layout="sbhd")
+        q8, k8, v8 = (np.ascontiguousarray(x) for x in (q8, k8, v8))
+        t0 = time.perf_counter()
+        oracle.fwd_fp8(q8, k8, v8, descale=workloads.FP8_DESCALE, mask=w.mask, scale=w.scale, **kw)
+        dt = time.perf_counter() - t0
+        sub = w.replace(layout="bshd", batch=1, seqlen_q=lq, seqlen_kv=lq, heads_q=group, heads_kv=1)
+        _, fl = flops(sub, {})
+        if dt >= seconds_target * 0.6 or lq == lq0:
+            break
+        ls = int(ls * min(2.0, max(1.15, (seconds_target / max(dt, 1e-3)) ** 0.5)))
+    return {"seconds": dt, "tflops": fl / dt / 1e12, "ls": lq, "group": group, "threads": oracle.num_threads()}
+
+
+def fp8_arm(args, w, inp):
+    """FP8 E4M3 forward (sdpa_fwd_fp8) on the workload's shape with seeded E4M3
+    inputs: TFLOP/s under the exact-mask count (4*D per unmasked pair; the
+    kernel executes 6*D, S twice), roofline against the dense FP8 peak taken as
+    twice the measured bf16 figure (the nominal 4.5 / 2.25 PFLOP/s ratio)."""
+    import torch
+
+    import scaled_dot_product_02_gb300 as sdpa
+
+    if w.head_dim != 128 or w.dv != 128:
+        raise SystemExit("--op fp8 needs a head_dim 128 workload")
+    world, rank, local = rank_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    inp8 = workloads.fp8_inputs(w)
+    host = {x: torch.from_numpy(inp8[x]).pin_memory() for x in ("q8", "k8", "v8")}
+    q8, k8, v8 = (host[x].to(dev) for x in ("q8", "k8", "v8"))
+    kw = dict(layout=w.layout, mask=w.mask, scale=w.scale, window=w.window)
+    host_cu = {}
+    if w.layout == "thd":
+        for x in ("cu_seqlens_q", "cu_seqlens_kv"):
+            host_cu[x] = torch.from_numpy(inp8[x]).pin_memory()
+        kw.update(cu_seqlens_q=host_cu["cu_seqlens_q"].to(dev), cu_seqlens_kv=host_cu["cu_seqlens_kv"].to(dev),
+                  max_seqlen_q=int(np.max(np.diff(inp8["cu_seqlens_q"]))),
+                  max_seqlen_kv=int(np.max(np.diff(inp8["cu_seqlens_kv"]))))
+    o = torch.empty(tuple(q8.shape), dtype=torch.bfloat16, device=dev)
+    rows_q = q8.numel() // (w.heads_q * 128)
+    lse = torch.empty((rows_q, w.heads_q), dtype=torch.float32, device=dev)
+    batch = len(inp8["cu_seqlens_q"]) - 1 if w.layout == "thd" else None
+    prob = sdpa.make_problem(q8, k8, layout=w.layout, mask=w.mask, window=w.window, scale=w.scale, batch=batch,
+                             dtype=0, max_seqlen_q=kw.get("max_seqlen_q"), max_seqlen_kv=kw.get("max_seqlen_kv"))
+    ws = torch.empty(max(256, sdpa.sdpa_fwd_fp8_workspace_size(prob)), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        sdpa.sdpa_fwd_fp8(q8, k8, v8, descale=workloads.FP8_DESCALE, out=o, lse=lse, workspace=ws, **kw)
+        return sdpa.sdpa_last_launch_count()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if sdpa.sdpa_get_device_error() != 0:
+        raise RuntimeError("device error during warm-up")
+    clocks = ClockSampler(local)
+    clocks.start()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    sdpa.sdpa_profile_begin()
+    launches = 0
+    for i in range(args.steps):
+        flush.fill_(i & 255)
+        starts[i].record()
+        launches += step()
+        ends[i].record()
+    torch.cuda.synchronize()
+    prof = sdpa.sdpa_profile_end()
+    clk = clocks.stop()
+    if sdpa.sdpa_get_device_error() != 0:
+        raise RuntimeError("device error during the timed steps")
+    ms = sum(a.elapsed_time(b) for a, b in zip(starts, ends))
+    # end to end through the same call: E4M3 inputs in from pinned host memory,
+    # O and LSE out, every step, serialised
+    h_o = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    h_l = torch.empty(lse.shape, dtype=lse.dtype, pin_memory=True)
+    h2d = sum(t.numel() for t in host.values()) + sum(t.numel() * 4 for t in host_cu.values())
+    d2h = h_o.numel() * 2 + h_l.numel() * 4
+    e_steps = max(2, args.steps // 2)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(e_steps):
+        for x, t in (("q8", q8), ("k8", k8), ("v8", v8)):
+            t.copy_(host[x], non_blocking=True)
+        for x in host_cu:
+            kw[x].copy_(host_cu[x], non_blocking=True)
+        step()
+        h_o.copy_(o, non_blocking=True)
+        h_l.copy_(lse, non_blocking=True)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e_steps
+    if sdpa.sdpa_get_device_error() != 0:
+        raise RuntimeError("device error during the end-to-end steps")
+    conv, exact = flops(w, inp)
+    value = job_tflops(world, exact, args.steps, ms)
+    pk, pk_kind = peaks()
+    peak = 2.0 * pk["bf16_tflops"]
+    kern_ms = prof["fwd"][0] / max(prof["fwd"][1], 1)
+    achieved = exact / (kern_ms * 1e-3) / 1e12
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        s = fp8_oracle_sample(w, inp8, 12.0)
+        cpu = {"value": s["tflops"], "unit": "TFLOP/s", "cores": s["threads"], "kind": "oracle",
+               "sample": f"float64 FP8 oracle forward of the first {s['ls']} query tokens of sequence 0 with one "
+                         f"kv head ({s['group']} q heads): {s['seconds']:.1f} s"}
+    line = {"metric": "FP8 E4M3 attention forward TFLOP/s (exact-mask 4*D per unmasked pair)", "value": value,
+            "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "e4m3 (fp32 accumulate, bf16 O)", "data": "synthetic",
+            "config": {"workload": f"{w.name}_fp8", "layout": w.layout, "mask": w.mask, "heads_q": w.heads_q,
+                       "heads_kv": w.heads_kv, "head_dim": 128, "descale": list(workloads.FP8_DESCALE),
+                       "inputs": "E4M3 codes of the workload's seeded N(0,1) masters times 3",
+                       "l2": "flushed between timed steps (256 MiB write, outside the events)",
+                       "parallelism": f"replicas x{world} (no collective)"},
+            "clocks": clk, "gpu_launches": launches,
+            "e2e": {"value": job_tflops(world, exact, 1, e2e_ms), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "overlap": "none (serial copies)"},
+            "roofline": {"bound": "tensor", "kernel": "fwd_fp8_kernel", "achieved": achieved, "peak": peak,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                         "peak_source": f"{pk_kind} bf16_tflops x 2 (nominal dense fp8/bf16 ratio 4.5/2.25)",
+                         "algorithmic_flops_per_launch": exact, "executed_flops_per_launch": 1.5 * exact},
+            "cpu_baseline": cpu,
+            "detail": {"kernels_ms_per_step": {k: prof[k][0] / args.steps for k in ("guard", "v_transpose", "fwd")},
+                       "fwd_fp8_kernel_tflops_executed": 1.5 * achieved}}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def traffic_for(kind, workload):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
     the current kernel sources (else None)."""
@@ -669,9 +821,10 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="varlen_thd_gqa", choices=[w.name for w in workloads.ALL])
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--op", default="step", choices=["step", "fwd", "merge"],
+    ap.add_argument("--op", default="step", choices=["step", "fwd", "merge", "fp8"],
                     help="step: the fwd+bwd hot path (the headline; the forward alone for forward-only "
-                         "workloads); fwd: the forward alone; merge: the LSE merge of key-split results")
+                         "workloads); fwd: the forward alone; merge: the LSE merge of key-split results; "
+                         "fp8: the FP8 E4M3 forward (head_dim 128 workloads)")
     ap.add_argument("--merge-parts", type=int, default=4)
     ap.add_argument("--kv-chunk", type=int, default=0,
                     help="head_dim 256/512 backward: key positions per chunk (multiple of 128; 0 = library choice)")
@@ -686,6 +839,8 @@ def main():
     inp = workloads.make_inputs(w)
     if args.op == "merge":
         merge_arm(args, w, inp)
+    elif args.op == "fp8" and args.impl == "ours":
+        fp8_arm(args, w, inp)
     elif args.impl == "reference":
         reference_arm(args, w, inp)
     else:

@@ -264,9 +264,11 @@ SDPA_API int sdpa_merge(const sdpa_merge_problem* p, const void* o_parts, const 
  * fixed scale 448, so no amax of it is needed; PR #3527 "Scope" lists the
  * FP8 fused path). Computes, with the decoded values of the codes,
  *   S = softmax_scale * descale_q * descale_k * Q8 K8^T, masked as sdpa_fwd;
- *   LSE = ln sum_j exp(S_ij)   (float32, token-major, as sdpa_fwd);
- *   P8  = E4M3(exp(S - LSE) * 448)   (round to nearest even, saturating);
- *   O   = P8 V8 * descale_v / 448    (written in p->dtype: bf16 or fp16).
+ *   m = max_j S_ij, l = sum_j exp(S_ij - m), LSE = m + ln l   (float32,
+ *       token-major, as sdpa_fwd);
+ *   P8  = E4M3(exp(S - m) * 448)   (round to nearest even; the row's largest
+ *         probability is stored as 448, so no amax is needed);
+ *   O   = P8 V8 * descale_v / (448 * l)   (written in p->dtype: bf16 or fp16).
  * q8 [.., Hq, 128], k8 and v8 [.., Hkv, 128]: device E4M3 codes (the finite-
  * only OCP format: bias 7, largest 448, S.1111.111 = NaN), one byte each, in
  * p->layout; o [.., Hq, 128] and lse as for sdpa_fwd (device, written).

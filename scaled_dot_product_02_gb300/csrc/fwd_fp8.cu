@@ -3,17 +3,18 @@
 // Reading of TransformerEngine PR #3705's closing note on FP8 ("Amax S"):
 // with E4M3 inputs the softmax output is stored in E4M3 under the fixed
 // scale 448 (the format's largest value; no dropout), so no amax of it is
-// needed. Q, K, V are E4M3 codes with per-tensor descales d_q, d_k, d_v:
+// needed -- which holds when the stored probabilities are normalised by the
+// row's largest. Q, K, V are E4M3 codes with per-tensor descales d_q, d_k, d_v:
 //   S   = scale * d_q * d_k * Q8 K8^T            (tcgen05 kind::f8f6f4, fp32)
-//   P   = exp(S - LSE)  (masked; <= 1)            LSE = ln sum_j exp(S_ij)
-//   P8  = E4M3(P * 448)                           (round to nearest even)
-//   O   = P8 V8 * d_v / 448                       (kind::f8f6f4, written bf16/fp16)
-// P is normalised by the row's final LSE before it is rounded, so the kernel
-// makes two passes over the keys of a query tile: pass 1 computes S for
-// every key tile and keeps the row max and sum; pass 2 computes S again,
-// forms P and P8 against the final LSE and accumulates P8 V in TMEM. The
-// extra S costs 2*D flop per pair (1.5x the forward's MMA work, at the 8-bit
-// rate); in exchange O is never rescaled.
+//   m   = max_j S_ij (masked),  P~ = exp(S - m) <= 1,  l = sum_j P~_ij
+//   P8  = E4M3(P~ * 448)                          (round to nearest even)
+//   O   = P8 V8 * d_v / (448 * l),  LSE = m + ln l
+// The kernel makes two passes over the keys of a query tile: pass 1 computes
+// S for every key tile and keeps only the row max (no exponentials); pass 2
+// computes S again, forms P~ against the final max, sums it, rounds it to
+// E4M3 into TMEM and accumulates P8 V there. The extra S costs 2*D flop per
+// pair at the 8-bit rate; in exchange P is rounded on the definition's own
+// grid, exp runs once per score, and O is never rescaled.
 //
 // Operands are K-major 128-byte-swizzled E4M3 tiles (128 rows x 128 bytes,
 // 16 KB): Q and K straight from their [row][head][128] tensors, and V from a
@@ -295,8 +296,8 @@ __global__ void __launch_bounds__(256, 1)
     const float sl2 = g.scale_log2;
     const int lo_i = kr.lo(i), hi_i = kr.hi(i);
     const int lo_last = kr.lo(q_last), hi_first = kr.hi(q0);
-    float m = -INFINITY, l = 0.f;  // pass 1: running max (raw score units) and sum
-    float mb2 = INFINITY;          // pass 2: log2 of the row's normaliser, LSE * log2e
+    float m = -INFINITY;  // pass 1: the row max (raw score units)
+    float mb = 0.f, l = 0.f;  // pass 2: m * scale * log2e, and the sum of P~
     bool ok = true;
     for (int u = 0; u < steps; ++u) {
       if (!__all_sync(0xffffffffu, mbar_wait(&bar_s[u & 1], (u >> 1) & 1, abort_flag))) {
@@ -331,25 +332,20 @@ __global__ void __launch_bounds__(256, 1)
         for (int cc = 0; cc < 128; ++cc) s[cc] = in_range(kb + cc, lo_i, hi_i) ? s[cc] : -INFINITY;
       }
       if (u < n) {
-        float mt = s[0];
 #pragma unroll
-        for (int cc = 1; cc < 128; ++cc) mt = fmaxf(mt, s[cc]);
-        const float m_new = fmaxf(m, mt);
-        if (m_new != -INFINITY) {
-          const float mb = m_new * sl2;
-          float rs = 0.f;
-#pragma unroll
-          for (int cc = 0; cc < 128; ++cc) rs += ex2(fmaf(s[cc], sl2, -mb));
-          l = (m == -INFINITY ? 0.f : l * ex2((m - m_new) * sl2)) + rs;
-          m = m_new;
-        }
-        if (u == n - 1) mb2 = l > 0.f ? m * sl2 + __log2f(l) : INFINITY;
+        for (int cc = 0; cc < 128; ++cc) m = fmaxf(m, s[cc]);
+        if (u == n - 1) mb = m == -INFINITY ? 0.f : m * sl2;
       } else {
         uint32_t pk[32];
+        float rs = 0.f;
 #pragma unroll
-        for (int cc = 0; cc < 32; ++cc)
-          pk[cc] = pack_e4m3x4(ex2(fmaf(s[4 * cc], sl2, -mb2)) * 448.f, ex2(fmaf(s[4 * cc + 1], sl2, -mb2)) * 448.f,
-                               ex2(fmaf(s[4 * cc + 2], sl2, -mb2)) * 448.f, ex2(fmaf(s[4 * cc + 3], sl2, -mb2)) * 448.f);
+        for (int cc = 0; cc < 32; ++cc) {
+          const float p0 = ex2(fmaf(s[4 * cc], sl2, -mb)), p1 = ex2(fmaf(s[4 * cc + 1], sl2, -mb));
+          const float p2 = ex2(fmaf(s[4 * cc + 2], sl2, -mb)), p3 = ex2(fmaf(s[4 * cc + 3], sl2, -mb));
+          rs += (p0 + p1) + (p2 + p3);
+          pk[cc] = pack_e4m3x4(p0 * 448.f, p1 * 448.f, p2 * 448.f, p3 * 448.f);
+        }
+        l += rs;
         tmem_st32(scol, pk);
         tmem_wait_st();
       }
@@ -365,7 +361,7 @@ __global__ void __launch_bounds__(256, 1)
       record_error(p.err, SDPA_ERR_TIMEOUT);
     } else {
       const bool valid = i < si.lq;
-      const float mul = l > 0.f ? p.o_scale : 0.f;
+      const float mul = l > 0.f ? p.o_scale / l : 0.f;
       using T = typename E::T;
       T* orow = reinterpret_cast<T*>(p.o) + ((long long)(si.qrow0 + i) * g.nh_q + qhead) * F8_D;
 #pragma unroll 1

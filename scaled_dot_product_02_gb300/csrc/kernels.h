@@ -143,7 +143,7 @@ struct Fp8Params {
   int* err;
   const int* guard;
   int n_q_tiles;
-  float o_scale;        // d_v / 448
+  float o_scale;        // d_v / 448 (the epilogue divides by the row sum as well)
   int item_offset;       // added to blockIdx.x (launches split under a CTA cap)
 };
 struct Fp8Launch {

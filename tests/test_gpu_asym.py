@@ -76,6 +76,7 @@ def test_asymmetric_backward_is_declined():
     k = torch.randn_like(q)
     v = torch.randn(1, 128, 2, 128, device="cuda", dtype=torch.bfloat16)
     o, lse = sdpa.sdpa_fwd(q, k, v, mask="causal")
+    assert sdpa.sdpa_get_device_error() == 0
     with pytest.raises(sdpa.SdpaError) as e:
         sdpa.sdpa_bwd(q, k, v, o, lse, torch.randn_like(o), mask="causal")
     assert e.value.status == 2  # SDPA_ERR_UNSUPPORTED

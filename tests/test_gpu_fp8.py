@@ -2,14 +2,16 @@
 
 The kernel follows the oracle's definition step for step (TransformerEngine
 PR #3705, closing note on FP8: the softmax output is stored in E4M3 under the
-fixed scale 448): S on the decoded codes, P = exp(S - LSE) against the row's
-final LSE, P8 = E4M3(P * 448) rounded once, O = P8 V * d_v / 448. The two
-computations of P differ only by float32 rounding (relative error well under
-2^-12), so a P8 code can differ from the oracle's only where P * 448 lies
-within 2^-12 of its value of an E4M3 rounding midpoint, and then by one E4M3
-step. The bound for every element of O is therefore
-    (d_v/448) * sum over those near-midpoint keys of step * |v|
-  + (d_v/448) * 4e-5 * sum_j P8_j |v_j|        (fp32 accumulation of the MMA)
+fixed scale 448, normalised by the row's largest probability): S on the
+decoded codes, P~ = exp(S - m) against the row's final max m, P8 =
+E4M3(P~ * 448) rounded once, O = P8 V * d_v / (448 * l) with l = sum P~.
+The two computations of P~ differ only by float32 rounding (relative error
+well under 2^-12), so a P8 code can differ from the oracle's only where
+P~ * 448 lies within 2^-12 of its value of an E4M3 rounding midpoint, and then
+by one E4M3 step. With P~ = p / max_j p (p the oracle's probabilities) and
+l = 1 / max_j p, the bound for every element of O is therefore
+    (d_v * max p / 448) * sum over those near-midpoint keys of step * |v|
+  + (d_v * max p / 448) * 4e-5 * sum_j P8_j |v_j|     (fp32 accumulation)
   + u * |O_ref|            (rounding O to bf16 / fp16: u = 2^-8 / 2^-11)
 with the near-midpoint keys found from the oracle's own probabilities, and
 LSE within 1e-4. Rows with no allowed key give O = 0 and LSE = -inf exactly.
@@ -59,12 +61,13 @@ def _q_rows(w, inp, b):
 def _bound(w, inp, probs, o_ref, v):
     """Elementwise bound on |O - O_ref| (see the module docstring)."""
     dvs = workloads.FP8_DESCALE[2]
-    x = probs * 448.0
+    pmax = probs.max(axis=-1, keepdims=True)  # the row's largest probability (0 for rows without keys)
+    x = np.divide(probs, pmax, out=np.zeros_like(probs), where=pmax > 0) * 448.0
     step = _e4m3_step(x)
     frac = x / step - np.floor(x / step)
     near = (np.abs(frac - 0.5) * step <= 2.0 ** -12 * x) & (x > 0)
-    tie_w = np.where(near, step, 0.0)
-    acc_w = x * 4e-5
+    tie_w = np.where(near, step, 0.0) * pmax  # the division by l = 1 / max p
+    acc_w = x * 4e-5 * pmax
     o_flat = o_ref.reshape(-1, w.heads_q, w.head_dim)
     bound = np.zeros_like(o_flat)
     group = w.heads_q // w.heads_kv
