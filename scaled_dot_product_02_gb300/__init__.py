@@ -305,8 +305,8 @@ def sdpa_fwd_fp8(q8, k8, v8, *, descale=(1.0, 1.0, 1.0), layout="bshd", mask="no
     """FP8 E4M3 forward (head_dim 128). q8, k8, v8: torch.uint8 codes or
     torch.float8_e4m3fn tensors in `layout`; descale = (d_q, d_k, d_v), the
     per-tensor factors that turn codes into values. The softmax output is
-    stored as E4M3(P * 448) against the row's final LSE (see sdpa_fwd_fp8 in
-    include/sdpa.h). Returns (o, lse): o in out_dtype (default bfloat16) with
+    stored as E4M3(exp(S - m) * 448), m the row's final maximum, and O divides
+    by 448 times the row sum (see sdpa_fwd_fp8 in include/sdpa.h). Returns (o, lse): o in out_dtype (default bfloat16) with
     q8's shape, lse float32 [rows_q, Hq]."""
     import torch
 
