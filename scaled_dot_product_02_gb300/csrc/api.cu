@@ -281,7 +281,7 @@ BigPlan big_plan(const sdpa_problem* p) {
 // the key tiles are split into chunks, and the 16-bit P / dS tile arrays of
 // one chunk.
 struct BwdWs {
-  size_t guard_off, lse2_off, delta_off, acc_off, ptile_off, dstile_off, total;
+  size_t guard_off, order_off, lse2_off, delta_off, acc_off, ptile_off, dstile_off, total;
   int stat_rows;
   bool has_acc;
 };
@@ -300,7 +300,10 @@ BwdWs bwd_ws(const sdpa_problem* p) {
     srows = round_up((size_t)p->seqlen_q, 4);
   w.stat_rows = (int)(srows + 128);
   w.guard_off = 0;
-  w.lse2_off = 256;
+  // THD, head_dim 128: the sequence order the guard writes (longest first)
+  const bool ordered = p->layout == SDPA_THD && p->head_dim == 128;
+  w.order_off = ordered ? 256 : 0;
+  w.lse2_off = ordered ? 256 + round_up((size_t)p->batch * 4, 256) : 256;
   w.delta_off = round_up(w.lse2_off + (size_t)hq * w.stat_rows * 4, 256);
   const size_t after_stats = round_up(w.delta_off + (size_t)hq * w.stat_rows * 4, 256);
   const size_t acc_bytes = (size_t)hq * rq * p->head_dim * 4;
@@ -321,6 +324,21 @@ BwdWs bwd_ws(const sdpa_problem* p) {
     w.total = w.dstile_off + tiles * 32768;
   }
   return w;
+}
+
+// kv heads whose key tiles interleave in the D128 backward grid: the largest
+// divisor of num_heads_kv whose query-side rows (Q and dO, plus the fp32 dQ
+// accumulator unless deterministic) fit in 128 MiB, about the L2. Interleaving
+// heads lets the heavy first key tiles of every head start early; keeping their
+// rows within the L2 keeps the CTAs that walk the same rows from re-reading
+// them from HBM.
+int bwd_head_block(const sdpa_problem* p) {
+  const int group = p->num_heads_q / p->num_heads_kv;
+  const size_t per_head = (size_t)p->seqlen_q * group * p->head_dim * (p->deterministic ? 4 : 8);
+  int hb = 1;
+  for (int d = 1; d <= p->num_heads_kv; ++d)
+    if (p->num_heads_kv % d == 0 && (size_t)d * per_head <= (size_t)128 << 20) hb = d;
+  return hb;
 }
 
 }  // namespace
@@ -457,13 +475,14 @@ int sdpa_bwd(const sdpa_problem* p, const void* q, const void* k, const void* v,
   const bool bf16 = p->dtype == SDPA_BF16;
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   int* guard = thd ? reinterpret_cast<int*>(ws + w.guard_off) : nullptr;
+  int* order = w.order_off ? reinterpret_cast<int*>(ws + w.order_off) : nullptr;
   float* lse2 = reinterpret_cast<float*>(ws + w.lse2_off);
   float* delta = reinterpret_cast<float*>(ws + w.delta_off);
   float* acc = reinterpret_cast<float*>(ws + w.acc_off);
   const Geom g = make_geom(p, cu_seqlens_q, cu_seqlens_kv);
   int launches = 0;
   if (thd) {
-    if ((rc = timed(SDPA_KERNEL_GUARD, s, [&] { return launch_guard(g, p->total_q, p->total_kv, guard, err, s); })))
+    if ((rc = timed(SDPA_KERNEL_GUARD, s, [&] { return launch_guard(g, p->total_q, p->total_kv, guard, err, s, order); })))
       return rc;
     ++launches;
   }
@@ -533,6 +552,8 @@ int sdpa_bwd(const sdpa_problem* p, const void* q, const void* k, const void* v,
   L.p.dv = dv;
   L.p.err = err;
   L.p.guard = guard;
+  L.p.order = order;
+  L.p.head_block = bwd_head_block(p);
   L.p.n_kv_tiles = (p->seqlen_kv + 127) / 128;
   L.stream = s;
   if ((rc = encode(&L.tmQ, q, p->head_dim, hq, rq, 64, bf16))) return rc;

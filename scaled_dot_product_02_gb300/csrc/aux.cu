@@ -15,15 +15,66 @@
 
 namespace sdpa {
 
-__global__ void guard_kernel(const int32_t* cu_q, const int32_t* cu_kv, int batch, int total_q, int total_kv,
-                             int max_q, int max_kv, int* guard, int* err) {
+// order (may be null): the sequence indices ordered by query-tile count,
+// longest first -- a counting sort over min(max_q/64 + 1, kOrderBins) bins,
+// so it is a permutation of [0, batch) whatever the lengths hold. Sequences
+// of one bin keep no fixed order among themselves; the order only decides
+// when a sequence's CTAs start, never what they compute.
+constexpr int kOrderBins = 4096;
+
+__device__ __forceinline__ int order_bin(int lq, int n_bins) {
+  if (lq <= 0) return 0;
+  const int t = (lq - 1) / 64 + 1;
+  return t < n_bins ? t : n_bins - 1;
+}
+
+__global__ void __launch_bounds__(256) guard_kernel(const int32_t* cu_q, const int32_t* cu_kv, int batch, int total_q,
+                                                    int total_kv, int max_q, int max_kv, int* guard, int* err,
+                                                    int* order, int n_bins) {
   __shared__ int bad;
+  __shared__ int bins[kOrderBins];
+  __shared__ int warp_sum[8];
   if (threadIdx.x == 0) bad = (cu_q[0] != 0) || (cu_kv[0] != 0) || (cu_q[batch] != total_q) || (cu_kv[batch] != total_kv);
+  if (order)
+    for (int x = threadIdx.x; x < n_bins; x += blockDim.x) bins[x] = 0;
   __syncthreads();
   for (int b = threadIdx.x; b < batch; b += blockDim.x) {
     const int lq = cu_q[b + 1] - cu_q[b];
     const int lk = cu_kv[b + 1] - cu_kv[b];
     if (lq < 0 || lk < 0 || lq > max_q || lk > max_kv || (lq > 0 && lk == 0)) atomicOr(&bad, 1);
+    if (order) atomicAdd(&bins[order_bin(lq, n_bins)], 1);
+  }
+  __syncthreads();
+  if (order) {
+    // bins[x] <- sequences in bins above x (exclusive scan from the top):
+    // thread t owns the bins n_bins-1-per*t ... n_bins-per*(t+1)
+    const int per = (n_bins + blockDim.x - 1) / blockDim.x;
+    int own = 0;
+    for (int j = 0; j < per; ++j) {
+      const int x = n_bins - 1 - (per * (int)threadIdx.x + j);
+      if (x >= 0) own += bins[x];
+    }
+    const int lane = threadIdx.x % 32, wid = threadIdx.x / 32;
+    int incl = own;
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    if (lane == 31) warp_sum[wid] = incl;
+    __syncthreads();
+    int run = incl - own;
+    for (int w = 0; w < wid; ++w) run += warp_sum[w];
+    for (int j = 0; j < per; ++j) {
+      const int x = n_bins - 1 - (per * (int)threadIdx.x + j);
+      if (x >= 0) {
+        const int c = bins[x];
+        bins[x] = run;
+        run += c;
+      }
+    }
+    __syncthreads();
+    for (int b = threadIdx.x; b < batch; b += blockDim.x)
+      order[atomicAdd(&bins[order_bin(cu_q[b + 1] - cu_q[b], n_bins)], 1)] = b;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -32,8 +83,9 @@ __global__ void guard_kernel(const int32_t* cu_q, const int32_t* cu_kv, int batc
   }
 }
 
-int launch_guard(const Geom& g, int total_q, int total_kv, int* guard, int* err, cudaStream_t s) {
-  guard_kernel<<<1, 256, 0, s>>>(g.cu_q, g.cu_kv, g.batch, total_q, total_kv, g.sq, g.sk, guard, err);
+int launch_guard(const Geom& g, int total_q, int total_kv, int* guard, int* err, cudaStream_t s, int* order) {
+  const int n_bins = std::min(g.sq / 64 + 2, kOrderBins);
+  guard_kernel<<<1, 256, 0, s>>>(g.cu_q, g.cu_kv, g.batch, total_q, total_kv, g.sq, g.sk, guard, err, order, n_bins);
   return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }
 

@@ -116,14 +116,28 @@ __global__ void __launch_bounds__(512, 1)
   using T = typename E::T;
   const Geom& g = p.g;
 
-  // ---- which tile: the key tiles of one (batch, kv head) are adjacent in the
-  // grid, so CTAs running together read the same Q/dO rows and reduce into the
-  // same dQ accumulator rows while those are resident in L2.
+  // ---- which tile. Grid order: sequence (THD: longest first, through the
+  // order the guard kernel wrote), then blocks of head_block kv heads, then
+  // key tile, then kv head within the block. A key tile is attended by no
+  // more query tiles than the tile before it under every supported mask, so
+  // each sequence's heaviest CTAs start first and the grid ends on light
+  // ones; the key tiles of one (sequence, kv head) start close together and
+  // walk the same Q/dO rows and dQ accumulator rows while those are resident
+  // in L2 (head_block bounds how many heads' rows are in use at once).
   int idx = blockIdx.x + p.item_offset;
-  const int kt = idx % p.n_kv_tiles;
-  idx /= p.n_kv_tiles;
-  const int kvh = idx % g.hkv;
-  const int b = idx / g.hkv;
+  const int per_seq = p.n_kv_tiles * g.hkv;
+  const int hb = p.head_block;
+  int b = idx / per_seq;
+  idx %= per_seq;
+  const int blk = idx / (p.n_kv_tiles * hb);
+  idx %= p.n_kv_tiles * hb;
+  const int kt = idx / hb;
+  const int kvh = blk * hb + idx % hb;
+  if (p.order) b = p.order[b];
+  if (kvh >= g.hkv || (unsigned)b >= (unsigned)g.batch) {
+    if (threadIdx.x == 0) record_error(p.err, SDPA_ERR_INVALID_ARG);
+    return;
+  }
   const SeqInfo si = seq_info(g, b);
   const int k0 = kt * BN;
   if (k0 >= si.lk) return;

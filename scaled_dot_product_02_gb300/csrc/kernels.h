@@ -68,6 +68,8 @@ struct BwdParams {
   int n_kv_tiles;        // ceil(seqlen_kv / 128)
   int d_lo, d_hi;        // dK/dV columns this launch owns (all of D for head_dim 128)
   int item_offset;       // added to blockIdx.x (launches split under a CTA cap)
+  const int* order;      // THD: sequence indices, longest first (written by the guard); else null
+  int head_block;        // kv heads whose key tiles interleave in the grid (divides hkv)
 };
 
 struct BwdLaunch {
@@ -166,7 +168,9 @@ struct PrepParams {
   float* dq_acc;  // zeroed here when non-null
   const int* guard;
 };
-int launch_guard(const Geom& g, int total_q, int total_kv, int* guard, int* err, cudaStream_t s);
+// order (THD backward, else null): receives the sequence indices, longest first
+int launch_guard(const Geom& g, int total_q, int total_kv, int* guard, int* err, cudaStream_t s,
+                 int* order = nullptr);
 int launch_preprocess(const PrepParams& pp, bool bf16, cudaStream_t s);
 int launch_wait_selftest(uint64_t limit_ns, int* err, cudaStream_t s);
 int launch_dq_finalize(const Geom& g, const float* dq_acc, void* dq, const int* guard, bool bf16, cudaStream_t s);
