@@ -273,52 +273,75 @@ __global__ void __launch_bounds__(512, 1)
         }
         mma_commit(&bar_sdp[i & 1]);
       };
+      auto wait_ds = [&](int i) -> bool {
+        if (!mbar_wait(bar_ds, i & 1, abort_flag)) return false;
+        tc_fence_after();
+        return true;
+      };
+      // dV += P^T(i) dO(i)
+      auto issue_dv = [&](int i) {
+        const uint32_t sd = smem_u32(smem + OFF_DO + (i % NQS) * QT_BYTES);
+#pragma unroll
+        for (int ks = 0; ks < BQ / 16; ++ks)
+          mma_ts(tmem + TM_DV, tmem + tm_s(i & 1) + p_col(ks), smem_desc_sw128(sd + ks * 2048, 8192, 1024), ID_KV,
+                 (i | ks) != 0);
+      };
+      // dK += dS^T(i) Q(i); the Q/dO stage of step i is then free
+      auto issue_dk = [&](int i) {
+        const int st = i % NQS;
+        const uint32_t sq = smem_u32(smem + OFF_Q + st * QT_BYTES);
+#pragma unroll
+        for (int ks = 0; ks < BQ / 16; ++ks)
+          mma_ts(tmem + TM_DK, tmem + tm_dp(i & 1) + p_col(ks), smem_desc_sw128(sq + ks * 2048, 8192, 1024), ID_KV,
+                 (i | ks) != 0);
+        mma_commit(&empty[st]);
+      };
+      // dQ^T(i) into the dP^T/dS^T columns dK(i) has just read
+      auto issue_dq = [&](int i) {
+        const uint32_t sds = smem_u32(smem + OFF_DS + (i & 1) * DS_BYTES);
+#pragma unroll
+        for (int ks = 0; ks < BN / 16; ++ks)
+          mma_ss(tmem + tm_dp(i & 1), smem_desc_sw128(sK + ks * 2048, 16384, 1024),
+                 smem_desc_sw128(sds + ks * 2048, 16384, 1024), ID_DQ, ks > 0);
+        mma_commit(&bar_dq[i & 1]);
+      };
+      // Issue stream: ... dQ^T(i), S^T(i+2), dV(i+1), [drain has read dQ^T(i)] dP^T(i+2), dK(i+1),
+      // dQ^T(i+1), S^T(i+3), dV(i+2), ... Each write follows every read of the
+      // columns it overwrites in issue order (S^T(i+2) after dV(i), dP^T(i+2)
+      // after dK(i) and the drain of dQ^T(i), dQ^T(i+1) after dK(i+1)), the
+      // drain of dQ^T(i) is covered by S^T(i+2) and dV(i+1), and the softmax of
+      // step i+2 by dK(i+1), dQ^T(i+1) and S^T(i+3).
       tc_fence_after();
       for (int i = 0; i < 2 && i < n && ok; ++i) {
         ok = issue_s(i);
         if (ok) issue_dp(i);
       }
-      for (int i = 0; i < n && ok; ++i) {
-        const int st = i % NQS;
-        const int buf = i & 1;
-        if (!mbar_wait(bar_ds, i & 1, abort_flag)) {
-          ok = false;
-          break;
+      if (ok && n > 0) {
+        ok = wait_ds(0);
+        if (ok) {
+          issue_dv(0);
+          issue_dk(0);
+          if (DQ) issue_dq(0);
+          if (n > 2) ok = issue_s(2);
         }
-        tc_fence_after();
-        const uint32_t sq = smem_u32(smem + OFF_Q + st * QT_BYTES);
-        const uint32_t sd = smem_u32(smem + OFF_DO + st * QT_BYTES);
-#pragma unroll
-        for (int ks = 0; ks < BQ / 16; ++ks)
-          mma_ts(tmem + TM_DV, tmem + tm_s(buf) + p_col(ks), smem_desc_sw128(sd + ks * 2048, 8192, 1024), ID_KV,
-                 (i | ks) != 0);
-#pragma unroll
-        for (int ks = 0; ks < BQ / 16; ++ks)
-          mma_ts(tmem + TM_DK, tmem + tm_dp(buf) + p_col(ks), smem_desc_sw128(sq + ks * 2048, 8192, 1024), ID_KV,
-                 (i | ks) != 0);
-        mma_commit(&empty[st]);
-        if (DQ) {
-          // dQ^T(i) into the dP^T/dS^T columns dK(i) has just read
-          const uint32_t sds = smem_u32(smem + OFF_DS + buf * DS_BYTES);
-#pragma unroll
-          for (int ks = 0; ks < BN / 16; ++ks)
-            mma_ss(tmem + tm_dp(buf), smem_desc_sw128(sK + ks * 2048, 16384, 1024),
-                   smem_desc_sw128(sds + ks * 2048, 16384, 1024), ID_DQ, ks > 0);
-          mma_commit(&bar_dq[buf]);
+      }
+      for (int i = 0; i < n && ok; ++i) {
+        if (i + 1 < n) {
+          if (!(ok = wait_ds(i + 1))) break;
+          issue_dv(i + 1);
         }
         if (i + 2 < n) {
-          // S^T(i+2) overwrites P^T(i), which dV(i) has read; dP^T(i+2)
-          // overwrites dQ^T(i): wait for the drain first.
-          if (!issue_s(i + 2)) {
-            ok = false;
-            break;
-          }
           if (DQ && !mbar_wait(bar_dqfree, i & 1, abort_flag)) {
             ok = false;
             break;
           }
           tc_fence_after();
           issue_dp(i + 2);
+        }
+        if (i + 1 < n) {
+          issue_dk(i + 1);
+          if (DQ) issue_dq(i + 1);
+          if (i + 3 < n && !(ok = issue_s(i + 3))) break;
         }
       }
       if (ok) {
