@@ -73,7 +73,9 @@ typedef enum {
   SDPA_ERR_WORKSPACE_TOO_SMALL = 5,
   SDPA_ERR_BAD_SEQLENS = 6,      /* device-detected: cu_seqlens not compact / out of bounds */
   SDPA_ERR_TIMEOUT = 7,          /* device-detected: a bounded wait inside a kernel gave up */
-  SDPA_ERR_CUDA = 8              /* a CUDA runtime or driver call failed */
+  SDPA_ERR_CUDA = 8,             /* a CUDA runtime or driver call failed */
+  SDPA_ERR_ADDRESS = 9           /* device-detected, address-checked library only: a kernel access
+                                    fell outside the call's buffers and was skipped */
 } sdpa_status;
 
 typedef enum { SDPA_BSHD = 0, SDPA_SBHD = 1, SDPA_THD = 2 } sdpa_layout;
@@ -224,6 +226,35 @@ SDPA_API int sdpa_bwd_noalloc(const sdpa_problem* p, const void* q, const void* 
  * parity at one schedule cannot (the sanitizers' race and sync checks are
  * the other route). Process-wide; slow for large problems. */
 SDPA_API int sdpa_debug_set_max_ctas(int max_ctas);
+
+/* Address checking (testing aid; a stand-in for a memory checker, which
+ * answers the sanitizers' out-of-bounds question that element-wise parity
+ * cannot: a stray write can land where no test looks). Only the separately
+ * built checked library, libsdpa_checked.so (the same sources compiled with
+ * SDPA_ADDR_CHECK), answers these; the normal library returns
+ * SDPA_ERR_UNSUPPORTED and checks nothing.
+ *
+ * In the checked library every entry point registers the byte extents of the
+ * buffers it was given (inputs, outputs, cu_seqlens, workspace) in a
+ * per-device table, and every kernel load or store at a computed global
+ * address -- each access that is not a tensor-map (TMA) copy, which the
+ * hardware bounds against its map -- first tests its bytes against those
+ * extents. An access outside all of them is skipped (a skipped bulk load still
+ * completes its transaction count, so no pipeline waits on it), counted, and
+ * its address kept; the call's device error word becomes SDPA_ERR_ADDRESS.
+ * The table is per device, so calls on several streams at once share it:
+ * check one stream at a time.
+ *
+ * sdpa_debug_address_report synchronises the current device, stores the
+ * number of violations since the last report, the first offending address
+ * and its size (any pointer may be NULL), and clears them.
+ * sdpa_debug_address_shrink(bytes) pulls the end of every extent registered
+ * from then on in by `bytes` (0 restores them): the last bytes of each buffer
+ * become out of bounds for the checker while staying valid memory, which
+ * tests the checker itself without any access outside a real allocation. */
+SDPA_API int sdpa_debug_address_report(unsigned long long* violations, unsigned long long* first_addr,
+                                       unsigned long long* first_bytes);
+SDPA_API int sdpa_debug_address_shrink(long long bytes);
 
 /* Failure-path self-test of the bounded waits every pipelined kernel uses:
  * launches one thread that waits on a barrier nothing arrives on, gives up

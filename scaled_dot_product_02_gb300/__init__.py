@@ -14,22 +14,25 @@ against each other from metadata before the library is called.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
 
 PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libsdpa.so")
+CHECKED_LIB_PATH = os.path.join(PKG, "libsdpa_checked.so")  # the address-checked testing build
 
 LAYOUTS = {"bshd": 0, "sbhd": 1, "thd": 2}
 MASKS = {"none": 0, "causal": 1, "causal_br": 2}
 STATUS = {0: "SDPA_OK", 1: "SDPA_ERR_INVALID_ARG", 2: "SDPA_ERR_UNSUPPORTED", 3: "SDPA_ERR_ALIGNMENT",
           4: "SDPA_ERR_OVERLAP", 5: "SDPA_ERR_WORKSPACE_TOO_SMALL", 6: "SDPA_ERR_BAD_SEQLENS",
-          7: "SDPA_ERR_TIMEOUT", 8: "SDPA_ERR_CUDA"}
+          7: "SDPA_ERR_TIMEOUT", 8: "SDPA_ERR_CUDA", 9: "SDPA_ERR_ADDRESS"}
 EXPORTS = ("sdpa_fwd_workspace_size", "sdpa_bwd_workspace_size", "sdpa_check_problem", "sdpa_fwd", "sdpa_bwd",
            "sdpa_get_device_error", "sdpa_error_string", "sdpa_last_launch_count", "sdpa_profile_begin",
            "sdpa_profile_end", "sdpa_bwd_noalloc", "sdpa_selftest_bounded_wait", "sdpa_merge",
-           "sdpa_fwd_fp8_workspace_size", "sdpa_fwd_fp8", "sdpa_debug_set_max_ctas")
+           "sdpa_fwd_fp8_workspace_size", "sdpa_fwd_fp8", "sdpa_debug_set_max_ctas", "sdpa_debug_address_report",
+           "sdpa_debug_address_shrink")
 NOALLOC_MAX_BYTES = 32 << 20  # SDPA_BWD_NOALLOC_MAX_BYTES
 KERNEL_KINDS = ("fwd", "bwd", "preprocess", "dq_finalize", "guard", "merge", "bwd_dq", "v_transpose")
 
@@ -56,42 +59,86 @@ class Problem(ctypes.Structure):
 
 
 _lock = threading.Lock()
-_lib = None
+_libs = {}
+_active = LIB_PATH
+
+
+def _load(path):
+    if path not in _libs:
+        if not os.path.exists(path):
+            raise ImportError(f"{path} is missing: run scaled_dot_product_02_gb300/build.py "
+                              "(there is no fallback implementation)")
+        L = ctypes.CDLL(path)
+        vp, pp = ctypes.c_void_p, ctypes.POINTER(Problem)
+        L.sdpa_fwd_workspace_size.argtypes = [pp]
+        L.sdpa_fwd_workspace_size.restype = ctypes.c_size_t
+        L.sdpa_bwd_workspace_size.argtypes = [pp]
+        L.sdpa_bwd_workspace_size.restype = ctypes.c_size_t
+        L.sdpa_check_problem.argtypes = [pp]
+        L.sdpa_fwd.argtypes = [pp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+        L.sdpa_bwd.argtypes = [pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+        L.sdpa_get_device_error.argtypes = [vp]
+        L.sdpa_error_string.argtypes = [ctypes.c_int]
+        L.sdpa_error_string.restype = ctypes.c_char_p
+        L.sdpa_last_launch_count.restype = ctypes.c_int
+        L.sdpa_selftest_bounded_wait.argtypes = [ctypes.c_uint, vp]
+        L.sdpa_debug_set_max_ctas.argtypes = [ctypes.c_int]
+        u64p = ctypes.POINTER(ctypes.c_ulonglong)
+        L.sdpa_debug_address_report.argtypes = [u64p, u64p, u64p]
+        L.sdpa_debug_address_shrink.argtypes = [ctypes.c_longlong]
+        L.sdpa_bwd_noalloc.argtypes = [pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.sdpa_merge.argtypes = [ctypes.POINTER(MergeProblem), vp, vp, vp, vp, vp]
+        L.sdpa_profile_end.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int),
+                                       ctypes.c_int]
+        L.sdpa_fwd_fp8_workspace_size.argtypes = [pp]
+        L.sdpa_fwd_fp8_workspace_size.restype = ctypes.c_size_t
+        fl = ctypes.c_float
+        L.sdpa_fwd_fp8.argtypes = [pp, vp, vp, vp, fl, fl, fl, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
+        _libs[path] = L
+    return _libs[path]
 
 
 def lib():
-    """Load libsdpa.so (build it first with scaled_dot_product_02_gb300.build)."""
-    global _lib
+    """The loaded library every call goes through: libsdpa.so, or
+    libsdpa_checked.so inside `address_checked()` (build them first with
+    scaled_dot_product_02_gb300.build)."""
     with _lock:
-        if _lib is None:
-            if not os.path.exists(LIB_PATH):
-                raise ImportError(f"{LIB_PATH} is missing: run scaled_dot_product_02_gb300/build.py "
-                                  "(there is no fallback implementation)")
-            L = ctypes.CDLL(LIB_PATH)
-            vp, pp = ctypes.c_void_p, ctypes.POINTER(Problem)
-            L.sdpa_fwd_workspace_size.argtypes = [pp]
-            L.sdpa_fwd_workspace_size.restype = ctypes.c_size_t
-            L.sdpa_bwd_workspace_size.argtypes = [pp]
-            L.sdpa_bwd_workspace_size.restype = ctypes.c_size_t
-            L.sdpa_check_problem.argtypes = [pp]
-            L.sdpa_fwd.argtypes = [pp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
-            L.sdpa_bwd.argtypes = [pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
-            L.sdpa_get_device_error.argtypes = [vp]
-            L.sdpa_error_string.argtypes = [ctypes.c_int]
-            L.sdpa_error_string.restype = ctypes.c_char_p
-            L.sdpa_last_launch_count.restype = ctypes.c_int
-            L.sdpa_selftest_bounded_wait.argtypes = [ctypes.c_uint, vp]
-            L.sdpa_debug_set_max_ctas.argtypes = [ctypes.c_int]
-            L.sdpa_bwd_noalloc.argtypes = [pp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp]
-            L.sdpa_merge.argtypes = [ctypes.POINTER(MergeProblem), vp, vp, vp, vp, vp]
-            L.sdpa_profile_end.argtypes = [ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_int),
-                                           ctypes.c_int]
-            L.sdpa_fwd_fp8_workspace_size.argtypes = [pp]
-            L.sdpa_fwd_fp8_workspace_size.restype = ctypes.c_size_t
-            fl = ctypes.c_float
-            L.sdpa_fwd_fp8.argtypes = [pp, vp, vp, vp, fl, fl, fl, vp, vp, vp, vp, vp, ctypes.c_size_t, vp]
-            _lib = L
-    return _lib
+        return _load(_active)
+
+
+@contextlib.contextmanager
+def address_checked():
+    """Testing aid: route the calls made inside the block through
+    libsdpa_checked.so, whose kernels test every computed global access
+    against the call's buffers (sdpa_debug_address_report in include/sdpa.h).
+    Both libraries stay loaded; each keeps its own device error word."""
+    global _active
+    with _lock:
+        prev, _active = _active, CHECKED_LIB_PATH
+        _load(CHECKED_LIB_PATH)
+    try:
+        yield
+    finally:
+        with _lock:
+            _active = prev
+
+
+def sdpa_debug_address_report():
+    """(violations, first address, its size) since the last report, then
+    cleared (synchronises the device). Address-checked library only."""
+    v, a, n = ctypes.c_ulonglong(0), ctypes.c_ulonglong(0), ctypes.c_ulonglong(0)
+    rc = lib().sdpa_debug_address_report(ctypes.byref(v), ctypes.byref(a), ctypes.byref(n))
+    if rc:
+        raise SdpaError(rc, "sdpa_debug_address_report")
+    return v.value, a.value, n.value
+
+
+def sdpa_debug_address_shrink(nbytes: int) -> None:
+    """Pull the end of every extent registered from now on in by nbytes (0
+    restores them). Address-checked library only."""
+    rc = lib().sdpa_debug_address_shrink(int(nbytes))
+    if rc:
+        raise SdpaError(rc, "sdpa_debug_address_shrink")
 
 
 def error_string(status: int) -> str:

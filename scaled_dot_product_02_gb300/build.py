@@ -2,7 +2,10 @@
 
 Each translation unit under csrc/ compiles in parallel; the objects link into
 scaled_dot_product_02_gb300/libsdpa.so with the CUDA runtime linked statically
-(the library only needs the NVIDIA driver at run time).
+(the library only needs the NVIDIA driver at run time). The same sources
+compiled with SDPA_ADDR_CHECK link into libsdpa_checked.so, the testing build
+whose kernels test every computed global access against the call's buffers
+(see sdpa_debug_address_report in include/sdpa.h).
 """
 from __future__ import annotations
 
@@ -16,6 +19,10 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsdpa.so")
+VARIANTS = {  # name: (object folder, library, extra nvcc flags)
+    "normal": (BUILD, LIB, []),
+    "checked": (os.path.join(PKG, "_build_checked"), os.path.join(PKG, "libsdpa_checked.so"), ["-DSDPA_ADDR_CHECK"]),
+}
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -40,11 +47,12 @@ def _headers_mtime():
     return max(os.path.getmtime(h) for h in hs)
 
 
-def _compile(src: str, verbose: bool) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+def _compile(src: str, variant: str, verbose: bool) -> str:
+    objdir, _, extra = VARIANTS[variant]
+    obj = os.path.join(objdir, os.path.basename(src) + ".o")
     if os.path.exists(obj) and os.path.getmtime(obj) >= max(os.path.getmtime(src), _headers_mtime()):
         return obj
-    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-c", src, "-o", obj + ".tmp"]
+    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, *extra, "-c", src, "-o", obj + ".tmp"]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -56,18 +64,29 @@ def _compile(src: str, verbose: bool) -> str:
     return obj
 
 
-def build(verbose: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
-    srcs = sources()
-    with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose), srcs))
-    if not os.path.exists(LIB) or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+def _link(variant: str, objs) -> str:
+    _, lib, _ = VARIANTS[variant]
+    if not os.path.exists(lib) or os.path.getmtime(lib) < max(os.path.getmtime(o) for o in objs):
+        tmp = lib + f".tmp{os.getpid()}"
         cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
+        os.replace(tmp, lib)
+    return lib
+
+
+def build(verbose: bool = False, variants=("normal", "checked")) -> str:
+    """Compile every translation unit of each variant in parallel and link the
+    libraries; returns the path of libsdpa.so."""
+    for v in variants:
+        os.makedirs(VARIANTS[v][0], exist_ok=True)
+    srcs = sources()
+    jobs = [(s, v) for v in variants for s in srcs]
+    with cf.ThreadPoolExecutor(max_workers=min(os.cpu_count() or 8, len(jobs), 16)) as ex:
+        objs = list(ex.map(lambda j: _compile(j[0], j[1], verbose), jobs))
+    for v in variants:
+        _link(v, [o for (s, vv), o in zip(jobs, objs) if vv == v])
     return LIB
 
 

@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <cstddef>
 #include <cstdint>
 #include <algorithm>
 #include <atomic>
@@ -98,6 +99,54 @@ Extent extent(const void* p, size_t bytes) {
 }
 bool overlaps(Extent a, Extent b) { return a.lo < b.hi && b.lo < a.hi && a.hi > a.lo && b.hi > b.lo; }
 
+// ---- address-checked build (SDPA_ADDR_CHECK): each entry point registers the
+// extents of the buffers it was given; its kernels test every computed access
+// against them (addr_ok in common.cuh).
+#ifdef SDPA_ADDR_CHECK
+constexpr bool kAddrCheck = true;
+static __device__ AddrTable g_sdpa_addr_table;
+std::atomic<long long> g_addr_shrink{0};
+
+AddrTable* addr_table() {
+  static std::mutex mu;
+  static AddrTable* ptrs[128] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_sdpa_addr_table) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<AddrTable*>(p);
+  }
+  return ptrs[dev];
+}
+
+// Writes the call's extents (less the debug shrink) ahead of its kernels on
+// stream s; the violation counters are left as they are.
+AddrTable* bind_extents(std::initializer_list<Extent> ex, int* err, cudaStream_t s) {
+  AddrTable* t = addr_table();
+  if (!t) return nullptr;
+  AddrTable h;
+  std::memset(&h, 0, sizeof(h));
+  const long long shrink = g_addr_shrink.load(std::memory_order_relaxed);
+  for (const Extent& e : ex) {
+    if (e.hi <= e.lo || h.n >= (unsigned long long)kAddrExtents) continue;
+    const uintptr_t cut = shrink > 0 ? std::min<uintptr_t>((uintptr_t)shrink, e.hi - e.lo) : 0;
+    h.lo[h.n] = e.lo;
+    h.hi[h.n] = e.hi - cut;
+    ++h.n;
+  }
+  h.err = err;
+  // pageable source: the call returns once the bytes are staged, in stream order
+  if (cudaMemcpyAsync(t, &h, offsetof(AddrTable, violations), cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return nullptr;
+  return t;
+}
+#else
+constexpr bool kAddrCheck = false;
+AddrTable* bind_extents(std::initializer_list<Extent>, int*, cudaStream_t) { return nullptr; }
+#endif
+
 // Rows/heads of the generic row x head x D view (see common.cuh).
 void view(const sdpa_problem* p, int& rows_q, int& rows_kv, int& nh_q, int& nh_kv) {
   if (p->layout == SDPA_THD) {
@@ -180,6 +229,7 @@ Geom make_geom(const sdpa_problem* p, const int32_t* cu_q, const int32_t* cu_kv)
   view(p, g.rows_q, g.rows_kv, g.nh_q, g.nh_kv);
   g.cu_q = cu_q;
   g.cu_kv = cu_kv;
+  g.chk = nullptr;
   return g;
 }
 
@@ -415,6 +465,11 @@ int sdpa_fwd(const sdpa_problem* p, const void* q, const void* k, const void* v,
   FwdLaunch L;
   std::memset(&L, 0, sizeof(L));
   L.p.g = make_geom(p, cu_seqlens_q, cu_seqlens_kv);
+  const size_t cub = thd ? 4 * ((size_t)p->batch + 1) : 0;
+  L.p.g.chk = bind_extents({extent(q, qb), extent(k, kb), extent(v, vb), eo, el, extent(cu_seqlens_q, cub),
+                            extent(cu_seqlens_kv, cub), extent(workspace, need)},
+                           err, s);
+  if (kAddrCheck && !L.p.g.chk) return SDPA_ERR_CUDA;
   L.p.o = o;
   L.p.lse = lse;
   L.p.err = err;
@@ -479,7 +534,12 @@ int sdpa_bwd(const sdpa_problem* p, const void* q, const void* k, const void* v,
   float* lse2 = reinterpret_cast<float*>(ws + w.lse2_off);
   float* delta = reinterpret_cast<float*>(ws + w.delta_off);
   float* acc = reinterpret_cast<float*>(ws + w.acc_off);
-  const Geom g = make_geom(p, cu_seqlens_q, cu_seqlens_kv);
+  Geom g = make_geom(p, cu_seqlens_q, cu_seqlens_kv);
+  const size_t cub = thd ? 4 * ((size_t)p->batch + 1) : 0;
+  g.chk = bind_extents({outs[0], outs[1], outs[2], outs[3], ins[0], ins[1], ins[2], ins[3], ins[4], ins[5],
+                        extent(cu_seqlens_q, cub), extent(cu_seqlens_kv, cub)},
+                       err, s);
+  if (kAddrCheck && !g.chk) return SDPA_ERR_CUDA;
   int launches = 0;
   if (thd) {
     if ((rc = timed(SDPA_KERNEL_GUARD, s, [&] { return launch_guard(g, p->total_q, p->total_kv, guard, err, s, order); })))
@@ -636,6 +696,11 @@ int sdpa_fwd_fp8(const sdpa_problem* p, const void* q8, const void* k8, const vo
   Fp8Launch L;
   std::memset(&L, 0, sizeof(L));
   L.p.g = make_geom(p, cu_seqlens_q, cu_seqlens_kv);
+  const size_t cub = thd ? 4 * ((size_t)p->batch + 1) : 0;
+  L.p.g.chk = bind_extents({outs[0], outs[1], outs[2], ins[0], ins[1], ins[2], extent(cu_seqlens_q, cub),
+                            extent(cu_seqlens_kv, cub)},
+                           err, s);
+  if (kAddrCheck && !L.p.g.chk) return SDPA_ERR_CUDA;
   L.p.g.scale = p->softmax_scale * descale_q * descale_k;  // scores of the decoded codes
   L.p.g.scale_log2 = L.p.g.scale * 1.4426950408889634f;
   L.p.v = static_cast<const uint8_t*>(v8);
@@ -692,8 +757,12 @@ int sdpa_merge(const sdpa_merge_problem* p, const void* o_parts, const float* ls
     if (overlaps(eo, in) || overlaps(el, in)) return SDPA_ERR_OVERLAP;
   if (overlaps(eo, el)) return SDPA_ERR_OVERLAP;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  AddrTable* chk = bind_extents({eo, el, extent(o_parts, ob * p->n_parts), extent(lse_parts, lb * p->n_parts)},
+                                error_word(), s);
+  if (kAddrCheck && !chk) return SDPA_ERR_CUDA;
   const int rc = timed(SDPA_KERNEL_MERGE, s, [&] {
-    return launch_merge(o_parts, lse_parts, o, lse, p->items, p->head_dim, p->n_parts, p->dtype == SDPA_BF16, s);
+    return launch_merge(o_parts, lse_parts, o, lse, p->items, p->head_dim, p->n_parts, p->dtype == SDPA_BF16, chk,
+                        s);
   });
   if (rc) return rc;
   t_last_launches = 1;
@@ -723,6 +792,7 @@ const char* sdpa_error_string(int status) {
     case SDPA_ERR_BAD_SEQLENS: return "cu_seqlens rejected by the device-side guard";
     case SDPA_ERR_TIMEOUT: return "a bounded wait inside a kernel gave up";
     case SDPA_ERR_CUDA: return "a CUDA runtime or driver call failed";
+    case SDPA_ERR_ADDRESS: return "a kernel access fell outside the call's buffers (address-checked library)";
     default: return "unknown status";
   }
 }
@@ -733,6 +803,39 @@ int sdpa_debug_set_max_ctas(int max_ctas) {
   if (max_ctas < 0) return SDPA_ERR_INVALID_ARG;
   g_max_ctas.store(max_ctas, std::memory_order_relaxed);
   return SDPA_OK;
+}
+
+int sdpa_debug_address_report(unsigned long long* violations, unsigned long long* first_addr,
+                              unsigned long long* first_bytes) {
+#ifdef SDPA_ADDR_CHECK
+  AddrTable* t = addr_table();
+  if (!t || cudaDeviceSynchronize() != cudaSuccess) return SDPA_ERR_CUDA;
+  unsigned long long v[3] = {0, 0, 0};
+  uint8_t* counters = reinterpret_cast<uint8_t*>(t) + offsetof(AddrTable, violations);
+  if (cudaMemcpy(v, counters, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return SDPA_ERR_CUDA;
+  const unsigned long long zero[3] = {0, 0, 0};
+  if (cudaMemcpy(counters, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return SDPA_ERR_CUDA;
+  if (violations) *violations = v[0];
+  if (first_addr) *first_addr = v[1];
+  if (first_bytes) *first_bytes = v[2];
+  return SDPA_OK;
+#else
+  (void)violations;
+  (void)first_addr;
+  (void)first_bytes;
+  return SDPA_ERR_UNSUPPORTED;
+#endif
+}
+
+int sdpa_debug_address_shrink(long long bytes) {
+#ifdef SDPA_ADDR_CHECK
+  if (bytes < 0) return SDPA_ERR_INVALID_ARG;
+  g_addr_shrink.store(bytes, std::memory_order_relaxed);
+  return SDPA_OK;
+#else
+  (void)bytes;
+  return SDPA_ERR_UNSUPPORTED;
+#endif
 }
 
 int sdpa_selftest_bounded_wait(unsigned limit_us, void* stream) {

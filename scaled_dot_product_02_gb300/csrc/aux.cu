@@ -30,10 +30,18 @@ __device__ __forceinline__ int order_bin(int lq, int n_bins) {
 
 __global__ void __launch_bounds__(256) guard_kernel(const int32_t* cu_q, const int32_t* cu_kv, int batch, int total_q,
                                                     int total_kv, int max_q, int max_kv, int* guard, int* err,
-                                                    int* order, int n_bins) {
+                                                    int* order, int n_bins, AddrTable* chk) {
   __shared__ int bad;
   __shared__ int bins[kOrderBins];
   __shared__ int warp_sum[8];
+  // the address-checked build reads the two arrays and writes the guard word
+  // and the order only where the call registered them (else: rejected)
+  const bool in_bounds = SDPA_ADDR_OK(chk, cu_q, 4ull * (batch + 1)) && SDPA_ADDR_OK(chk, cu_kv, 4ull * (batch + 1)) &&
+                         SDPA_ADDR_OK(chk, guard, 4) && (!order || SDPA_ADDR_OK(chk, order, 4ull * batch));
+  if (!in_bounds) {
+    if (threadIdx.x == 0 && SDPA_ADDR_OK(chk, guard, 4)) *guard = SDPA_ERR_ADDRESS;
+    return;
+  }
   if (threadIdx.x == 0) bad = (cu_q[0] != 0) || (cu_kv[0] != 0) || (cu_q[batch] != total_q) || (cu_kv[batch] != total_kv);
   if (order)
     for (int x = threadIdx.x; x < n_bins; x += blockDim.x) bins[x] = 0;
@@ -85,7 +93,8 @@ __global__ void __launch_bounds__(256) guard_kernel(const int32_t* cu_q, const i
 
 int launch_guard(const Geom& g, int total_q, int total_kv, int* guard, int* err, cudaStream_t s, int* order) {
   const int n_bins = std::min(g.sq / 64 + 2, kOrderBins);
-  guard_kernel<<<1, 256, 0, s>>>(g.cu_q, g.cu_kv, g.batch, total_q, total_kv, g.sq, g.sk, guard, err, order, n_bins);
+  guard_kernel<<<1, 256, 0, s>>>(g.cu_q, g.cu_kv, g.batch, total_q, total_kv, g.sq, g.sk, guard, err, order, n_bins,
+                                 g.chk);
   return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }
 
@@ -130,7 +139,9 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const PrepParams p) {
         const uint4* d4 = reinterpret_cast<const uint4*>(p.dout) + oi * VPR;
 #pragma unroll
         for (int v = 0; v < PER; ++v) {
-          const uint4 a = o4[sub + v * G], c = d4[sub + v * G];
+          const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+          const uint4 a = SDPA_ADDR_OK(g.chk, o4 + sub + v * G, 16) ? o4[sub + v * G] : z;
+          const uint4 c = SDPA_ADDR_OK(g.chk, d4 + sub + v * G, 16) ? d4[sub + v * G] : z;
           const uint32_t au[4] = {a.x, a.y, a.z, a.w}, cu[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -144,10 +155,10 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const PrepParams p) {
       for (int sh = G / 2; sh > 0; sh /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, sh, G);
       if (live && sub == 0) {
         const int s = it / g.hq, h = it - s * g.hq;
-        const float l = p.lse[oi];
+        const float l = SDPA_ADDR_OK(g.chk, p.lse + oi, 4) ? p.lse[oi] : -INFINITY;
         const long long st = (long long)(si.qhead0 + h) * p.stat_rows + sb + s;
-        p.delta[st] = acc;
-        p.lse2[st] = (l == -INFINITY) ? -INFINITY : -l * 1.4426950408889634f;
+        if (SDPA_ADDR_OK(g.chk, p.delta + st, 4)) p.delta[st] = acc;
+        if (SDPA_ADDR_OK(g.chk, p.lse2 + st, 4)) p.lse2[st] = (l == -INFINITY) ? -INFINITY : -l * 1.4426950408889634f;
       }
     }
     // rows after this sequence's block up to the next block (or the end)
@@ -158,8 +169,8 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const PrepParams p) {
          it += (long long)gridDim.x * blockDim.x) {
       const int h = (int)(it / gap);
       const long long st = (long long)(si.qhead0 + h) * p.stat_rows + sb + si.lq + (int)(it % gap);
-      p.delta[st] = 0.f;
-      p.lse2[st] = -INFINITY;
+      if (SDPA_ADDR_OK(g.chk, p.delta + st, 4)) p.delta[st] = 0.f;
+      if (SDPA_ADDR_OK(g.chk, p.lse2 + st, 4)) p.lse2[st] = -INFINITY;
     }
   }
   // zero the dQ accumulator (all block rows share the work)
@@ -167,7 +178,8 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const PrepParams p) {
   float4* acc4 = reinterpret_cast<float4*>(p.dq_acc);
   const long long tid = ((long long)blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
   const long long nthreads = (long long)gridDim.x * gridDim.y * blockDim.x;
-  for (long long it = tid; it < n4; it += nthreads) acc4[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (long long it = tid; it < n4; it += nthreads)
+    if (SDPA_ADDR_OK(g.chk, acc4 + it, 16)) acc4[it] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
 
 // SMs of the current device (queried per call: a process may drive several GPUs).
@@ -208,13 +220,15 @@ __global__ void __launch_bounds__(256) dq_finalize_kernel(const Geom g, const fl
     const long long hr = it / d8;  // head * rows + row
     const int head = (int)(hr / g.rows_q), row = (int)(hr % g.rows_q);
     const float4* src = reinterpret_cast<const float4*>(acc + hr * g.d + c * 8);
+    uint4* dst = reinterpret_cast<uint4*>(dq) + ((long long)row * g.nh_q + head) * d8 + c;
+    if (!SDPA_ADDR_OK(g.chk, src, 32) || !SDPA_ADDR_OK(g.chk, dst, 16)) continue;
     const float4 a = src[0], b = src[1];
     uint4 out;
     out.x = E::pack(a.x * g.scale, a.y * g.scale);
     out.y = E::pack(a.z * g.scale, a.w * g.scale);
     out.z = E::pack(b.x * g.scale, b.y * g.scale);
     out.w = E::pack(b.z * g.scale, b.w * g.scale);
-    reinterpret_cast<uint4*>(dq)[((long long)row * g.nh_q + head) * d8 + c] = out;
+    *dst = out;
   }
 }
 

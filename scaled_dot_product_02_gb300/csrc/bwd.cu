@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(512, 1)
   idx %= p.n_kv_tiles * hb;
   const int kt = idx / hb;
   const int kvh = blk * hb + idx % hb;
-  if (p.order) b = p.order[b];
+  if (p.order) b = SDPA_ADDR_OK(g.chk, p.order + b, 4) ? p.order[b] : -1;
   if (kvh >= g.hkv || (unsigned)b >= (unsigned)g.batch) {
     if (threadIdx.x == 0) record_error(p.err, SDPA_ERR_INVALID_ARG);
     return;
@@ -227,8 +227,14 @@ __global__ void __launch_bounds__(512, 1)
         tma_load_3d(&tmDO, &full[st], sd, 0, qhead, row0);
         tma_load_3d(&tmDO, &full[st], sd + 8192, 64, qhead, row0);
         const long long so = (long long)qhead * p.stat_rows + si.srow0 + step_q0(i);
-        bulk_load(sstat + st * 2 * STAT_FLOATS, p.lse2 + so, STAT_FLOATS * 4, &full[st]);
-        bulk_load(sstat + st * 2 * STAT_FLOATS + STAT_FLOATS, p.delta + so, STAT_FLOATS * 4, &full[st]);
+        if (SDPA_ADDR_OK(g.chk, p.lse2 + so, STAT_FLOATS * 4))
+          bulk_load(sstat + st * 2 * STAT_FLOATS, p.lse2 + so, STAT_FLOATS * 4, &full[st]);
+        else
+          mbar_complete_tx(&full[st], STAT_FLOATS * 4);
+        if (SDPA_ADDR_OK(g.chk, p.delta + so, STAT_FLOATS * 4))
+          bulk_load(sstat + st * 2 * STAT_FLOATS + STAT_FLOATS, p.delta + so, STAT_FLOATS * 4, &full[st]);
+        else
+          mbar_complete_tx(&full[st], STAT_FLOATS * 4);
       }
       if (i < n) {
         *abort_flag = 1;
@@ -438,7 +444,7 @@ __global__ void __launch_bounds__(512, 1)
 #pragma unroll
           for (int e = 0; e < 16; ++e) packed[e] = 0u;
         }
-        if (key_ok) {
+        if (key_ok && SDPA_ADDR_OK(g.chk, dst + c * 32, 64)) {
           uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
 #pragma unroll
           for (int e = 0; e < 4; ++e)
@@ -484,7 +490,7 @@ __global__ void __launch_bounds__(512, 1)
         if (rows > 0) {
           const int qhead = si.qhead0 + step_head(i);
           float* dstp = p.dq_acc + ((long long)qhead * g.rows_q + si.qrow0 + q0) * D;
-          bulk_reduce_add_f32(dstp, stg, rows * D * 4);
+          if (SDPA_ADDR_OK(g.chk, dstp, rows * D * 4)) bulk_reduce_add_f32(dstp, stg, rows * D * 4);
           bulk_commit_group();
         }
       }

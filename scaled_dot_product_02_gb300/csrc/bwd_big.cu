@@ -276,8 +276,8 @@ __global__ void __launch_bounds__(SF_THREADS, 1)
     const long long stat = (long long)qhead * p.stat_rows + si.srow0 + i;
     // rows past the sequence end belong to no query: an empty key range, so
     // their P and dS are exactly zero whatever their scores
-    const float nl2 = valid ? p.nlse2[stat] : 0.f;
-    const float dl = valid ? p.delta[stat] : 0.f;
+    const float nl2 = valid && SDPA_ADDR_OK(g.chk, p.nlse2 + stat, 4) ? p.nlse2[stat] : 0.f;
+    const float dl = valid && SDPA_ADDR_OK(g.chk, p.delta + stat, 4) ? p.delta[stat] : 0.f;
     const int lo_i = kr.lo(i), hi_i = valid ? kr.hi(i) : lo_i;
     const float sl2 = g.scale_log2;
     uint8_t* stP = sStg + grp * 2 * SF_STG;
@@ -342,8 +342,10 @@ __global__ void __launch_bounds__(SF_THREADS, 1)
       }
       if (leader) {
         const long long tix = tile_index(p, b, h, qt, t);
-        bulk_store(p.p_tiles + tix * TILE_BYTES + grp * SF_STG, stP, SF_STG);
-        bulk_store(p.ds_tiles + tix * TILE_BYTES + grp * SF_STG, stD, SF_STG);
+        uint8_t* gp = p.p_tiles + tix * TILE_BYTES + grp * SF_STG;
+        uint8_t* gd = p.ds_tiles + tix * TILE_BYTES + grp * SF_STG;
+        if (SDPA_ADDR_OK(g.chk, gp, SF_STG)) bulk_store(gp, stP, SF_STG);
+        if (SDPA_ADDR_OK(g.chk, gd, SF_STG)) bulk_store(gd, stD, SF_STG);
         bulk_commit_group();
       }
     }
@@ -585,8 +587,8 @@ __global__ void __launch_bounds__(S5_THREADS, 1)
     const long long stat = (long long)qhead * p.stat_rows + si.srow0 + i;
     // rows past the sequence end belong to no query: an empty key range, so
     // their P and dS are exactly zero whatever their scores
-    const float nl2 = valid ? p.nlse2[stat] : 0.f;
-    const float dl = valid ? p.delta[stat] : 0.f;
+    const float nl2 = valid && SDPA_ADDR_OK(g.chk, p.nlse2 + stat, 4) ? p.nlse2[stat] : 0.f;
+    const float dl = valid && SDPA_ADDR_OK(g.chk, p.delta + stat, 4) ? p.delta[stat] : 0.f;
     const int lo_i = kr.lo(i), hi_i = valid ? kr.hi(i) : lo_i;
     const float sl2 = g.scale_log2;
     for (int t = 0; t < n && ok; ++t) {
@@ -600,6 +602,7 @@ __global__ void __launch_bounds__(S5_THREADS, 1)
       // this thread's row of this group's 64-key atom in the two tile images
       uint8_t* prow = p.p_tiles + tix * TILE_BYTES + grp * 16384 + r * 128;
       uint8_t* drow = p.ds_tiles + tix * TILE_BYTES + grp * 16384 + r * 128;
+      const bool prow_ok = SDPA_ADDR_OK(g.chk, prow, 128), drow_ok = SDPA_ADDR_OK(g.chk, drow, 128);
       float pv[64];
       {
         uint32_t u[64];
@@ -618,7 +621,8 @@ __global__ void __launch_bounds__(S5_THREADS, 1)
       }
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        *reinterpret_cast<uint4*>(prow + ((k ^ (r & 7)) << 4)) =
+        if (prow_ok)
+          *reinterpret_cast<uint4*>(prow + ((k ^ (r & 7)) << 4)) =
             make_uint4(E::pack(pv[8 * k], pv[8 * k + 1]), E::pack(pv[8 * k + 2], pv[8 * k + 3]),
                        E::pack(pv[8 * k + 4], pv[8 * k + 5]), E::pack(pv[8 * k + 6], pv[8 * k + 7]));
       if (!__all_sync(0xffffffffu, mbar_wait(bar_dp, t & 1, abort_flag))) {
@@ -644,7 +648,7 @@ __global__ void __launch_bounds__(S5_THREADS, 1)
             // pv is exactly zero outside the mask, so dS is too (for finite dP)
             w[e] = E::pack(pv[c0] * (__uint_as_float(u[c0]) - dl), pv[c0 + 1] * (__uint_as_float(u[c0 + 1]) - dl));
           }
-          *reinterpret_cast<uint4*>(drow + ((k ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+          if (drow_ok) *reinterpret_cast<uint4*>(drow + ((k ^ (r & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
         }
       }
     }
@@ -780,11 +784,18 @@ __device__ __forceinline__ void gemm_tile(const CUtensorMap* tmB, const BigBwdPa
         uint8_t* dst = smem + st * GB_STAGE;
         const uint8_t* src = atiles + at * TILE_BYTES;
         mbar_arrive_expect_tx(&full[st], GB_STAGE);
+        // a copy the address check rejects still completes its bytes
+        auto load = [&](uint8_t* d, const uint8_t* g_src, uint32_t bytes) {
+          if (SDPA_ADDR_OK(g.chk, g_src, bytes))
+            bulk_load(d, g_src, bytes, &full[st]);
+          else
+            mbar_complete_tx(&full[st], bytes);
+        };
         if (MODE == 0) {  // keys 64*hf.. of the dS image: its atom hf
-          bulk_load(dst, src + hf * 16384, 16384, &full[st]);
+          load(dst, src + hf * 16384, 16384);
         } else {  // query rows 64*hf.. of the image: the same rows of both atoms
-          bulk_load(dst, src + hf * 8192, 8192, &full[st]);
-          bulk_load(dst + 8192, src + 16384 + hf * 8192, 8192, &full[st]);
+          load(dst, src + hf * 8192, 8192);
+          load(dst + 8192, src + 16384 + hf * 8192, 8192);
         }
         for (int a = 0; a < 4; ++a)
           tma_load_3d(tmB, &full[st], dst + TILE_BYTES / 2 + a * 8192, split * 256 + a * 64, bh, brow + hf * 64);
@@ -867,7 +878,7 @@ __device__ __forceinline__ void gemm_tile(const CUtensorMap* tmB, const BigBwdPa
           tmem_ld32(lane_base + c * 32, u);
           tmem_wait_ld();
           reg_fence(u);
-          if (valid) {
+          if (valid && SDPA_ADDR_OK(g.chk, acc + c * 32, 128)) {
 #pragma unroll
             for (int e = 0; e < 8; ++e)
               red_add_v4_f32(acc + c * 32 + 4 * e, __uint_as_float(u[4 * e]), __uint_as_float(u[4 * e + 1]),
@@ -890,7 +901,7 @@ __device__ __forceinline__ void gemm_tile(const CUtensorMap* tmB, const BigBwdPa
 #pragma unroll
           for (int e = 0; e < 16; ++e) packed[e] = 0u;
         }
-        if (valid) {
+        if (valid && SDPA_ADDR_OK(g.chk, out + c * 32, 64)) {
           uint4* d4 = reinterpret_cast<uint4*>(out + c * 32);
 #pragma unroll
           for (int e = 0; e < 4; ++e)

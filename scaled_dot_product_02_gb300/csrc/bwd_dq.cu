@@ -226,8 +226,8 @@ __global__ void __launch_bounds__(192, 1)
     const uint32_t lane_base = tmem + ((uint32_t)(warp * 32) << 16);
     const long long stat = (long long)qhead * p.stat_rows + si.srow0 + i;
     // rows past the sequence end belong to no query: an empty key range
-    const float nl2 = valid ? p.nlse2[stat] : 0.f;
-    const float dl = valid ? p.delta[stat] : 0.f;
+    const float nl2 = valid && SDPA_ADDR_OK(g.chk, p.nlse2 + stat, 4) ? p.nlse2[stat] : 0.f;
+    const float dl = valid && SDPA_ADDR_OK(g.chk, p.delta + stat, 4) ? p.delta[stat] : 0.f;
     const int lo_i = kr.lo(i), hi_i = valid ? kr.hi(i) : lo_i;
     const int lo_last = kr.lo(q_last), hi_first = kr.hi(q0);
     const float sl2 = g.scale_log2;
@@ -287,7 +287,7 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
           for (int e = 0; e < 16; ++e) packed[e] = 0u;
         }
-        if (valid) {
+        if (valid && SDPA_ADDR_OK(g.chk, row + cc * 32, 64)) {
           uint4* d4 = reinterpret_cast<uint4*>(row + cc * 32);
 #pragma unroll
           for (int e = 0; e < 4; ++e)

@@ -15,6 +15,16 @@ namespace sdpa {
 //   THD:  row = cu[b]+s, head = h           (rows = T,   heads = H)
 // so one 3-D TMA tensor map {D, heads, rows} serves all three, and the
 // token-major LSE index is row*heads + head.
+// Extents of the buffers one call was given, for the address-checked build
+// (SDPA_ADDR_CHECK; see addr_ok). One table per device, in device memory.
+constexpr int kAddrExtents = 16;
+struct AddrTable {
+  unsigned long long n;                                   // extents in use
+  unsigned long long lo[kAddrExtents], hi[kAddrExtents];  // [lo, hi) byte ranges
+  int* err;                                               // the device error word
+  unsigned long long violations, first_addr, first_bytes;
+};
+
 struct Geom {
   int layout, mask, batch, sq, sk;  // THD: sq/sk are the largest lengths
   int hq, hkv, d;
@@ -25,7 +35,32 @@ struct Geom {
   int nh_q, nh_kv;      // heads of the generic view
   const int32_t* cu_q;
   const int32_t* cu_kv;
+  AddrTable* chk;  // address-checked build: this call's extents; else null
 };
+
+// Address check of a load or store at a computed global address (every access
+// that is not a tensor-map copy, which the hardware bounds against its map).
+// The checked build tests [p, p + bytes) against the call's extents; outside
+// all of them the access is to be skipped: the violation is counted, its
+// address kept and SDPA_ERR_ADDRESS recorded. Elsewhere the test is `true`.
+#ifdef SDPA_ADDR_CHECK
+static __device__ __forceinline__ bool addr_ok(AddrTable* t, const void* p, unsigned long long bytes) {
+  if (!t) return true;
+  const unsigned long long a = reinterpret_cast<unsigned long long>(p);
+  const unsigned long long n = t->n < (unsigned long long)kAddrExtents ? t->n : kAddrExtents;
+  for (unsigned long long i = 0; i < n; ++i)
+    if (a >= t->lo[i] && bytes <= t->hi[i] - t->lo[i] && a - t->lo[i] <= t->hi[i] - t->lo[i] - bytes) return true;
+  if (atomicAdd(&t->violations, 1ull) == 0ull) {
+    t->first_addr = a;
+    t->first_bytes = bytes;
+  }
+  if (t->err) atomicCAS(t->err, 0, (int)SDPA_ERR_ADDRESS);
+  return false;
+}
+#define SDPA_ADDR_OK(t, p, bytes) ::sdpa::addr_ok((t), (p), (unsigned long long)(bytes))
+#else
+#define SDPA_ADDR_OK(t, p, bytes) true
+#endif
 
 // Per-row backward statistics (-LSE*log2e and delta) are stored per generic
 // head as [head][stat_rows]; query s of sequence b sits at srow0 + s. Every
@@ -44,6 +79,10 @@ struct SeqInfo {
 __device__ __forceinline__ SeqInfo seq_info(const Geom& g, int b) {
   SeqInfo s;
   if (g.layout == SDPA_THD) {
+    if (!SDPA_ADDR_OK(g.chk, g.cu_q + b, 8) || !SDPA_ADDR_OK(g.chk, g.cu_kv + b, 8)) {
+      s.qrow0 = s.krow0 = s.lq = s.lk = s.qhead0 = s.khead0 = s.srow0 = 0;  // an empty sequence
+      return s;
+    }
     s.qrow0 = g.cu_q[b];
     s.lq = g.cu_q[b + 1] - s.qrow0;
     s.krow0 = g.cu_kv[b];

@@ -364,15 +364,16 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
           for (int e = 0; e < 16; ++e) packed[e] = 0u;
         }
-        if (valid) {
+        if (valid && SDPA_ADDR_OK(g.chk, orow + c * 32, 64)) {
           uint4* dst = reinterpret_cast<uint4*>(orow + c * 32);
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             dst[e] = make_uint4(packed[4 * e], packed[4 * e + 1], packed[4 * e + 2], packed[4 * e + 3]);
         }
       }
-      if (valid && split == 0)
-        p.lse[(int64_t)(si.qrow0 + i) * g.nh_q + qhead] = l > 0.f ? m_used * g.scale + logf(l) : -INFINITY;
+      float* lse_at = p.lse + (int64_t)(si.qrow0 + i) * g.nh_q + qhead;
+      if (valid && split == 0 && SDPA_ADDR_OK(g.chk, lse_at, 4))
+        *lse_at = l > 0.f ? m_used * g.scale + logf(l) : -INFINITY;
     }
   }
 
@@ -573,10 +574,12 @@ __global__ void __launch_bounds__(Fwd2Cfg::THREADS, 1)
       prefetch_tmap(&tmV);
       int c = 0, nq = 0, w = 0;
       bool ok = true;
-      int ticket = atomicAdd(p.tile_counter, 1);
+      // the next ticket (a counter the address check rejects hands out none)
+      auto take = [&]() { return SDPA_ADDR_OK(g.chk, p.tile_counter, 4) ? atomicAdd(p.tile_counter, 1) : p.total_tiles; };
+      int ticket = take();
       while (true) {
         Tile128 t;
-        while (ticket < p.total_tiles && !decode_tile(p, ticket, t)) ticket = atomicAdd(p.tile_counter, 1);
+        while (ticket < p.total_tiles && !decode_tile(p, ticket, t)) ticket = take();
         const int item = ticket < p.total_tiles ? ticket : -1;
         const int e = w & 1;
         if (!mbar_wait(&P.sched_empty[e], ((w >> 1) & 1) ^ 1, abort_flag)) {
@@ -587,7 +590,7 @@ __global__ void __launch_bounds__(Fwd2Cfg::THREADS, 1)
         mbar_arrive(&P.sched_full[e]);
         ++w;
         if (item < 0) break;
-        ticket = atomicAdd(p.tile_counter, 1);  // in flight while this tile's loads are issued
+        ticket = take();  // in flight while this tile's loads are issued
         if (t.n == 0) continue;
         if (nq > 0 && !mbar_wait(P.q_free, (nq - 1) & 1, abort_flag)) {
           ok = false;
@@ -875,15 +878,15 @@ __global__ void __launch_bounds__(Fwd2Cfg::THREADS, 1)
 #pragma unroll
           for (int k2 = 0; k2 < 16; ++k2) packed[k2] = 0u;
         }
-        if (valid) {
+        if (valid && SDPA_ADDR_OK(g.chk, orow + cc * 32, 64)) {
           uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
 #pragma unroll
           for (int k2 = 0; k2 < 4; ++k2)
             dst[k2] = make_uint4(packed[4 * k2], packed[4 * k2 + 1], packed[4 * k2 + 2], packed[4 * k2 + 3]);
         }
       }
-      if (valid)
-        p.lse[(int64_t)(t.si.qrow0 + i) * g.nh_q + qhead] = l > 0.f ? mbs * 0.6931471805599453f + logf(l) : -INFINITY;
+      float* lse_at = p.lse + (int64_t)(t.si.qrow0 + i) * g.nh_q + qhead;
+      if (valid && SDPA_ADDR_OK(g.chk, lse_at, 4)) *lse_at = l > 0.f ? mbs * 0.6931471805599453f + logf(l) : -INFINITY;
     }
     if (!ok) {
       *abort_flag = 1;

@@ -111,7 +111,8 @@ __global__ void __launch_bounds__(256) vt_kernel(const Fp8Params p) {
     const int kk = it >> 3, c = it & 7;
     const int key = k0 + kk;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (key < si.lk) v = *reinterpret_cast<const uint4*>(p.v + ((long long)(si.krow0 + key) * g.nh_kv + kh) * F8_D + c * 16);
+    const uint8_t* src = p.v + ((long long)(si.krow0 + key) * g.nh_kv + kh) * F8_D + c * 16;
+    if (key < si.lk && SDPA_ADDR_OK(g.chk, src, 16)) v = *reinterpret_cast<const uint4*>(src);
     *reinterpret_cast<uint4*>(&t[kk][c * 16]) = v;
   }
   __syncthreads();
@@ -123,8 +124,8 @@ __global__ void __launch_bounds__(256) vt_kernel(const Fp8Params p) {
     for (int e = 0; e < 4; ++e)
       w[e] = (uint32_t)t[c * 16 + 4 * e][d] | ((uint32_t)t[c * 16 + 4 * e + 1][d] << 8) |
              ((uint32_t)t[c * 16 + 4 * e + 2][d] << 16) | ((uint32_t)t[c * 16 + 4 * e + 3][d] << 24);
-    *reinterpret_cast<uint4*>(p.vt + ((long long)kh * F8_D + d) * p.vt_rows + r0 + k0 + c * 16) =
-        make_uint4(w[0], w[1], w[2], w[3]);
+    uint8_t* dst = p.vt + ((long long)kh * F8_D + d) * p.vt_rows + r0 + k0 + c * 16;
+    if (SDPA_ADDR_OK(g.chk, dst, 16)) *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
 
@@ -379,14 +380,15 @@ __global__ void __launch_bounds__(256, 1)
 #pragma unroll
           for (int e = 0; e < 16; ++e) packed[e] = 0u;
         }
-        if (valid) {
+        if (valid && SDPA_ADDR_OK(g.chk, orow + cc * 32, 64)) {
           uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
 #pragma unroll
           for (int e = 0; e < 4; ++e)
             dst[e] = make_uint4(packed[4 * e], packed[4 * e + 1], packed[4 * e + 2], packed[4 * e + 3]);
         }
       }
-      if (valid) p.lse[(long long)(si.qrow0 + i) * g.nh_q + qhead] = l > 0.f ? m * g.scale + logf(l) : -INFINITY;
+      float* lse_at = p.lse + (long long)(si.qrow0 + i) * g.nh_q + qhead;
+      if (valid && SDPA_ADDR_OK(g.chk, lse_at, 4)) *lse_at = l > 0.f ? m * g.scale + logf(l) : -INFINITY;
     }
   }
 

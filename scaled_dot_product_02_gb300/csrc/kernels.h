@@ -177,6 +177,6 @@ int launch_dq_finalize(const Geom& g, const float* dq_acc, void* dq, const int* 
 
 // Log-sum-exp merge of partial results over a split of the keys (merge.cu).
 int launch_merge(const void* o_parts, const float* lse_parts, void* o, float* lse, long long items, int head_dim,
-                 int n_parts, bool bf16, cudaStream_t s);
+                 int n_parts, bool bf16, AddrTable* chk, cudaStream_t s);
 
 }  // namespace sdpa

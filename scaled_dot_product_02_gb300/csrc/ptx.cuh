@@ -147,6 +147,13 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+// Complete `bytes` of an mbarrier's expected transaction count without a copy
+// (a bulk load the address-checked build skipped).
+__device__ __forceinline__ void mbar_complete_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+
 // Bulk reduce-add of fp32 values shared -> global (addresses 16-byte
 // aligned, size multiple of 16), tracked by the bulk async-group.
 __device__ __forceinline__ void bulk_reduce_add_f32(float* gdst, const void* ssrc, uint32_t bytes) {

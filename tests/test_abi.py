@@ -40,10 +40,32 @@ def test_library_exports_every_declared_symbol(pkg):
     assert set(declared_functions()) <= set(pkg.EXPORTS)
 
 
+def test_checked_library_exports_every_declared_symbol(pkg):
+    """The address-checked build (same sources, SDPA_ADDR_CHECK) is a drop-in
+    for libsdpa.so: the same entry points and the same host-side checks."""
+    lib = ctypes.CDLL(pkg.CHECKED_LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    with pkg.address_checked():
+        assert pkg.lib()._name == pkg.CHECKED_LIB_PATH
+        assert pkg.lib().sdpa_check_problem(ctypes.byref(problem(pkg))) == 0
+        assert pkg.lib().sdpa_check_problem(ctypes.byref(problem(pkg, head_dim=96))) == 2
+        assert pkg.lib().sdpa_debug_address_shrink(-1) == 1  # SDPA_ERR_INVALID_ARG
+        assert pkg.lib().sdpa_debug_address_shrink(0) == 0
+    assert pkg.lib()._name == pkg.LIB_PATH
+
+
+def test_normal_library_declines_the_address_checks(pkg):
+    assert pkg.lib().sdpa_debug_address_shrink(0) == 2  # SDPA_ERR_UNSUPPORTED
+    v = ctypes.c_ulonglong(0)
+    assert pkg.lib().sdpa_debug_address_report(ctypes.byref(v), None, None) == 2
+
+
 def test_error_strings(pkg):
-    for code in range(9):
+    for code in range(10):
         assert pkg.error_string(code)
     assert pkg.error_string(0) == "ok"
+    assert "address" in pkg.error_string(9)
 
 
 def problem(pkg, **kw):
