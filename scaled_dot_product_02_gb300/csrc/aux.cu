@@ -98,86 +98,106 @@ int launch_guard(const Geom& g, int total_q, int total_kv, int* guard, int* err,
   return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }
 
-// One block row per sequence (blockIdx.y = b). One group of G lanes per
-// (query, head) item of that sequence; each lane owns D/(8G) 16-byte vectors
-// of O and dO. The statistics go to srow0 + s (see SeqInfo); the rows between this
-// sequence's block and the next one's (alignment gaps and the final padding)
-// get lse2 = -inf and delta = 0, so every row a tile can read is finite.
+// Statistics row of generic query row `row` (its query position in its
+// sequence, plus the sequence's block start SeqInfo::srow0): BSHD and SBHD by
+// arithmetic, THD by a binary search of cu_seqlens_q (rows are tokens).
+__device__ __forceinline__ int stat_row(const Geom& g, int row) {
+  if (g.layout == SDPA_SBHD) return row;
+  if (g.layout == SDPA_BSHD) {
+    const int b = row / g.sq;
+    return b * ((g.sq + 3) & ~3) + (row - b * g.sq);
+  }
+  int lo = 0, hi = g.batch;  // the b with cu_q[b] <= row < cu_q[b + 1]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (SDPA_ADDR_OK(g.chk, g.cu_q + mid, 4) && g.cu_q[mid] <= row)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  const int c0 = SDPA_ADDR_OK(g.chk, g.cu_q + lo, 4) ? g.cu_q[lo] : 0;
+  return ((c0 + 3) & ~3) + 4 * lo + (row - c0);
+}
+
+// delta = rowsum(dO * O) and -LSE*log2(e) for every (query row, head) item of
+// the generic view. The items of O, dO and the token-major LSE are contiguous
+// in every layout (item = row * nh_q + head), so the whole grid strides over
+// them evenly whatever the sequence lengths; G lanes share an item, each lane
+// holding two 16-byte vectors of O and of dO. The statistics rows that belong
+// to no query (after each sequence's rows up to the next sequence's block, and
+// to stat_rows at the end) get lse2 = -inf and delta = 0, so every row a tile
+// can read is finite. Then the dQ accumulator is zeroed.
 template <bool BF16, int D>
 __global__ void __launch_bounds__(256) preprocess_kernel(const PrepParams p) {
   using E = Elem<BF16>;
-  constexpr int VPR = D / 8;                 // 16-byte vectors per row
-  constexpr int G = VPR < 32 ? VPR : 32;     // lanes per item
-  constexpr int PER = VPR / G;               // vectors per lane
+  constexpr int VPR = D / 8;                        // 16-byte vectors per row
+  constexpr int G = VPR / 2 < 32 ? VPR / 2 : 32;    // lanes per item
+  constexpr int PER = VPR / G;                      // vectors per lane (2 for D = 128, 256, 512)
+  constexpr int PER_WARP = 32 / G;                  // items one warp handles per step
   const Geom& g = p.g;
   // THD metadata that failed the guard is not used for addressing
   if (p.guard && *reinterpret_cast<volatile const int*>(p.guard)) return;
-  // one block row per sequence (more sequences than grid rows: each row takes several)
-  for (int b = blockIdx.y; b < g.batch; b += gridDim.y) {
-    const SeqInfo si = seq_info(g, b);
-    const int sb = si.srow0;
-    const int lane = threadIdx.x % 32;
-    const int sub = lane % G;
-    constexpr int PER_WARP = 32 / G;  // items one warp handles per step
-    const int items = si.lq * g.hq;  // < 2^30 (checked on the host)
-    const int warp_id = (blockIdx.x * blockDim.x + threadIdx.x) / 32;
-    const int n_warps = gridDim.x * blockDim.x / 32;
-    // warp-uniform trip count, so the shuffles below always see all 32 lanes
-    for (int base = warp_id * PER_WARP; base < items; base += n_warps * PER_WARP) {
-      const int it = base + lane / G;
-      const bool live = it < items;
-      // (row, head) of O, dO and LSE: for THD and BSHD the items of a sequence
-      // are contiguous in the generic view, so no division is on the load path
-      long long oi = (long long)si.qrow0 * g.nh_q + it;
-      if (g.layout == SDPA_SBHD) {
-        const int s = it / g.hq;
-        oi = (long long)s * g.nh_q + si.qhead0 + (it - s * g.hq);
+  const int lane = threadIdx.x % 32;
+  const int sub = lane % G;
+  const long long items = (long long)g.rows_q * g.nh_q;
+  const long long warp_id = ((long long)blockIdx.x * blockDim.x + threadIdx.x) / 32;
+  const long long n_warps = (long long)gridDim.x * blockDim.x / 32;
+  // warp-uniform trip count, so the shuffles below always see all 32 lanes
+  for (long long base = warp_id * PER_WARP; base < items; base += n_warps * PER_WARP) {
+    const long long it = base + lane / G;
+    const bool live = it < items;
+    float acc = 0.f;
+    if (live) {
+      const uint4* o4 = reinterpret_cast<const uint4*>(p.o) + it * VPR;
+      const uint4* d4 = reinterpret_cast<const uint4*>(p.dout) + it * VPR;
+      uint4 a[PER], c[PER];
+      const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int v = 0; v < PER; ++v) {
+        a[v] = SDPA_ADDR_OK(g.chk, o4 + sub + v * G, 16) ? o4[sub + v * G] : z;
+        c[v] = SDPA_ADDR_OK(g.chk, d4 + sub + v * G, 16) ? d4[sub + v * G] : z;
       }
-      float acc = 0.f;
-      if (live) {
-        const uint4* o4 = reinterpret_cast<const uint4*>(p.o) + oi * VPR;
-        const uint4* d4 = reinterpret_cast<const uint4*>(p.dout) + oi * VPR;
 #pragma unroll
-        for (int v = 0; v < PER; ++v) {
-          const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-          const uint4 a = SDPA_ADDR_OK(g.chk, o4 + sub + v * G, 16) ? o4[sub + v * G] : z;
-          const uint4 c = SDPA_ADDR_OK(g.chk, d4 + sub + v * G, 16) ? d4[sub + v * G] : z;
-          const uint32_t au[4] = {a.x, a.y, a.z, a.w}, cu[4] = {c.x, c.y, c.z, c.w};
+      for (int v = 0; v < PER; ++v) {
+        const uint32_t au[4] = {a[v].x, a[v].y, a[v].z, a[v].w}, cu[4] = {c[v].x, c[v].y, c[v].z, c[v].w};
 #pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const float2 fa = E::unpack(au[e]), fc = E::unpack(cu[e]);
-            acc = fmaf(fa.x, fc.x, acc);
-            acc = fmaf(fa.y, fc.y, acc);
-          }
+        for (int e = 0; e < 4; ++e) {
+          const float2 fa = E::unpack(au[e]), fc = E::unpack(cu[e]);
+          acc = fmaf(fa.x, fc.x, acc);
+          acc = fmaf(fa.y, fc.y, acc);
         }
       }
-#pragma unroll
-      for (int sh = G / 2; sh > 0; sh /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, sh, G);
-      if (live && sub == 0) {
-        const int s = it / g.hq, h = it - s * g.hq;
-        const float l = SDPA_ADDR_OK(g.chk, p.lse + oi, 4) ? p.lse[oi] : -INFINITY;
-        const long long st = (long long)(si.qhead0 + h) * p.stat_rows + sb + s;
-        if (SDPA_ADDR_OK(g.chk, p.delta + st, 4)) p.delta[st] = acc;
-        if (SDPA_ADDR_OK(g.chk, p.lse2 + st, 4)) p.lse2[st] = (l == -INFINITY) ? -INFINITY : -l * 1.4426950408889634f;
-      }
     }
-    // rows after this sequence's block up to the next block (or the end)
-    const int end = (g.layout == SDPA_SBHD || b + 1 == g.batch) ? p.stat_rows : seq_info(g, b + 1).srow0;
-    const int gap = end - (sb + si.lq);
-    const long long pad_items = gap > 0 ? (long long)g.hq * gap : 0;
-    for (long long it = (long long)blockIdx.x * blockDim.x + threadIdx.x; it < pad_items;
-         it += (long long)gridDim.x * blockDim.x) {
-      const int h = (int)(it / gap);
-      const long long st = (long long)(si.qhead0 + h) * p.stat_rows + sb + si.lq + (int)(it % gap);
+#pragma unroll
+    for (int sh = G / 2; sh > 0; sh /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, sh, G);
+    if (live && sub == 0) {
+      const int row = (int)(it / g.nh_q), hg = (int)(it - (long long)row * g.nh_q);
+      const float l = SDPA_ADDR_OK(g.chk, p.lse + it, 4) ? p.lse[it] : -INFINITY;
+      const long long st = (long long)hg * p.stat_rows + stat_row(g, row);
+      if (SDPA_ADDR_OK(g.chk, p.delta + st, 4)) p.delta[st] = acc;
+      if (SDPA_ADDR_OK(g.chk, p.lse2 + st, 4)) p.lse2[st] = (l == -INFINITY) ? -INFINITY : -l * 1.4426950408889634f;
+    }
+  }
+  const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  const long long nthreads = (long long)gridDim.x * blockDim.x;
+  // statistics rows of no query: per (sequence, generic head); SBHD keeps its
+  // batches apart through the generic head, so it has one "sequence"
+  const int nseq = g.layout == SDPA_SBHD ? 1 : g.batch;
+  const int heads = g.layout == SDPA_SBHD ? g.nh_q : g.hq;
+  for (long long it = tid; it < (long long)nseq * heads; it += nthreads) {
+    const int b = (int)(it / heads), hg = (int)(it - (long long)b * heads);
+    const SeqInfo si = seq_info(g, b);
+    const int a = si.srow0 + si.lq;
+    const int e = (b + 1 == nseq) ? p.stat_rows : seq_info(g, b + 1).srow0;
+    for (int r = a; r < e; ++r) {
+      const long long st = (long long)hg * p.stat_rows + r;
       if (SDPA_ADDR_OK(g.chk, p.delta + st, 4)) p.delta[st] = 0.f;
       if (SDPA_ADDR_OK(g.chk, p.lse2 + st, 4)) p.lse2[st] = -INFINITY;
     }
   }
-  // zero the dQ accumulator (all block rows share the work)
+  // zero the dQ accumulator
   const long long n4 = p.dq_acc ? (long long)g.nh_q * g.rows_q * g.d / 4 : 0;
   float4* acc4 = reinterpret_cast<float4*>(p.dq_acc);
-  const long long tid = ((long long)blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x;
-  const long long nthreads = (long long)gridDim.x * gridDim.y * blockDim.x;
   for (long long it = tid; it < n4; it += nthreads)
     if (SDPA_ADDR_OK(g.chk, acc4 + it, 16)) acc4[it] = make_float4(0.f, 0.f, 0.f, 0.f);
 }
@@ -193,9 +213,7 @@ static int sm_count() {
 
 int launch_preprocess(const PrepParams& pp, bool bf16, cudaStream_t s) {
   if (pp.g.batch <= 0) return SDPA_OK;
-  if ((long long)pp.g.sq * pp.g.hq >= (1LL << 30)) return SDPA_ERR_UNSUPPORTED;
-  const int rows = std::min(pp.g.batch, 65535);
-  const dim3 grid((unsigned)std::max(4, (sm_count() * 8 + rows - 1) / rows), (unsigned)rows);
+  const unsigned grid = (unsigned)sm_count() * 8;  // 8 blocks of 256 threads per SM, grid-stride
   const int d = pp.g.d;
 #define PREP(B, DD) preprocess_kernel<B, DD><<<grid, 256, 0, s>>>(pp)
   if (d == 128) { if (bf16) PREP(true, 128); else PREP(false, 128); }
