@@ -24,8 +24,14 @@
 // of Vt (TMA's alignment rule for the innermost coordinate), and the gaps
 // between sequences hold zeros.
 //
-// Roles (256 threads): warp 0 TMA producer, warp 1 TMEM allocator and MMA
-// issuer, warps 4-7 softmax and epilogue (one thread per query row).
+// Roles (384 threads): warp 0 TMA producer, warp 1 TMEM allocator and MMA
+// issuer, warps 4-7 and 8-11 softmax and epilogue: one thread per query row
+// in each warpgroup, warpgroup `half` owning the keys [64*half, 64*half+64)
+// of every key tile and the value columns [64*half, 64*half+64) of O. Each
+// keeps a partial row max (pass 1) and sum (pass 2) over its keys; the two
+// are combined through shared memory once per query tile. A warpgroup
+// packs its P8 into the first 16 columns of its own 64 of the S buffer, so
+// neither overwrites scores the other has not read.
 // TMEM: O [0,128), S/P buffers [128,256) and [256,384).
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -41,8 +47,10 @@ namespace {
 constexpr int F8_BM = 128, F8_BN = 128, F8_D = 128;
 constexpr int F8_TILE = 16384;  // 128 rows x 128 one-byte columns
 constexpr int F8_NST = 8;
-constexpr int F8_NBARS = 2 * F8_NST + 7;
-constexpr int F8_SMEM = 1024 + F8_TILE + F8_NST * F8_TILE + F8_NBARS * 8 + 16;
+constexpr int F8_NBARS = 2 * F8_NST + 9;
+constexpr int F8_XCH = 2 * 2 * F8_BM * 4;  // [max, sum][half][row] partials of the two warpgroups
+constexpr int F8_SMEM = 1024 + F8_TILE + F8_NST * F8_TILE + F8_XCH + F8_NBARS * 8 + 16;
+constexpr int F8_THREADS = 384;
 constexpr int F8_TM_O = 0, F8_TM_S = 128;
 
 // Instruction descriptor for kind::f8f6f4 with E4M3 A and B (format code 0),
@@ -130,7 +138,7 @@ __global__ void __launch_bounds__(256) vt_kernel(const Fp8Params p) {
 }
 
 template <bool BF16>
-__global__ void __launch_bounds__(256, 1)
+__global__ void __launch_bounds__(F8_THREADS, 1)
     fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmVt, const __grid_constant__ Fp8Params p) {
   using E = Elem<BF16>;
@@ -162,13 +170,15 @@ __global__ void __launch_bounds__(256, 1)
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sQ = smem;
   uint8_t* sStage = smem + F8_TILE;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sStage + F8_NST * F8_TILE);
+  float* xch = reinterpret_cast<float*>(sStage + F8_NST * F8_TILE);  // [2][2][F8_BM]
+  uint64_t* full = reinterpret_cast<uint64_t*>(sStage + F8_NST * F8_TILE + F8_XCH);
   uint64_t* empty = full + F8_NST;
   uint64_t* bar_q = empty + F8_NST;
   uint64_t* bar_s = bar_q + 1;  // [2] S of a step ready
   uint64_t* bar_p = bar_s + 2;  // [2] the softmax is done with a step's buffer (pass 2: P8 written)
   uint64_t* bar_o = bar_p + 2;  // the last P8 V (and so every MMA) complete
   uint64_t* bar_drain = bar_o + 1;
+  uint64_t* bar_x = bar_drain + 1;  // [2] the max / sum partials of both warpgroups are written
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -181,8 +191,10 @@ __global__ void __launch_bounds__(256, 1)
     mbar_init(bar_q, 1);
     mbar_init(&bar_s[0], 1);
     mbar_init(&bar_s[1], 1);
-    mbar_init(&bar_p[0], 128);
-    mbar_init(&bar_p[1], 128);
+    mbar_init(&bar_p[0], 256);
+    mbar_init(&bar_p[1], 256);
+    mbar_init(&bar_x[0], 256);
+    mbar_init(&bar_x[1], 256);
     mbar_init(bar_o, 1);
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
@@ -262,9 +274,9 @@ __global__ void __launch_bounds__(256, 1)
         const uint32_t vb = smem_u32(sStage + slot * F8_TILE);
         const uint32_t pcol = tmem + F8_TM_S + (u & 1) * 128;
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)  // 32 keys per MMA: 8 TMEM columns of packed P8
-          mma_f8_ts(tmem + F8_TM_O, pcol + ks * 8, smem_desc_sw128(vb + ks * 32, 16, 1024), IDESC,
-                    (u - n) > 0 || ks != 0);
+        for (int ks = 0; ks < 4; ++ks)  // 32 keys per MMA: 8 TMEM columns of packed P8 (each half's first 16)
+          mma_f8_ts(tmem + F8_TM_O, pcol + (ks >> 1) * 64 + (ks & 1) * 8, smem_desc_sw128(vb + ks * 32, 16, 1024),
+                    IDESC, (u - n) > 0 || ks != 0);
         mma_commit(&empty[slot]);
         if (u == steps - 1) mma_commit(bar_o);  // one completion: every P8 V is done
         ++c;
@@ -290,15 +302,18 @@ __global__ void __launch_bounds__(256, 1)
       }
     }
   } else if (warp >= 4) {
-    const int wq = warp - 4;
+    const int half = (warp - 4) >> 2;  // this warpgroup's keys and O columns: [64*half, 64*half+64)
+    const int wq = warp & 3;
     const int r = wq * 32 + lane;
     const int i = q0 + r;
     const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
     const float sl2 = g.scale_log2;
     const int lo_i = kr.lo(i), hi_i = kr.hi(i);
     const int lo_last = kr.lo(q_last), hi_first = kr.hi(q0);
-    float m = -INFINITY;  // pass 1: the row max (raw score units)
-    float mb = 0.f, l = 0.f;  // pass 2: m * scale * log2e, and the sum of P~
+    // pass 1: the row max over this half's keys, four independent chains
+    float mm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    float m = -INFINITY;  // the row max over all keys (raw score units), after pass 1
+    float mb = 0.f, l = 0.f;  // pass 2: m * scale * log2e, and the sum of P~ over this half's keys
     bool ok = true;
     for (int u = 0; u < steps; ++u) {
       if (!__all_sync(0xffffffffu, mbar_wait(&bar_s[u & 1], (u >> 1) & 1, abort_flag))) {
@@ -306,55 +321,66 @@ __global__ void __launch_bounds__(256, 1)
         break;
       }
       tc_fence_after();
-      const uint32_t scol = lane_base + F8_TM_S + (u & 1) * 128;
-      float s[128];
+      const uint32_t scol = lane_base + F8_TM_S + (u & 1) * 128 + half * 64;
+      float s[64];
       {
-        uint32_t u0[32], u1[32], u2[32], u3[32];
+        uint32_t u0[32], u1[32];
         tmem_ld32(scol, u0);
         tmem_ld32(scol + 32, u1);
-        tmem_ld32(scol + 64, u2);
-        tmem_ld32(scol + 96, u3);
         tmem_wait_ld();
         reg_fence(u0);
         reg_fence(u1);
-        reg_fence(u2);
-        reg_fence(u3);
 #pragma unroll
         for (int cc = 0; cc < 32; ++cc) {
           s[cc] = __uint_as_float(u0[cc]);
           s[32 + cc] = __uint_as_float(u1[cc]);
-          s[64 + cc] = __uint_as_float(u2[cc]);
-          s[96 + cc] = __uint_as_float(u3[cc]);
         }
       }
-      const int kb = (t_lo + (u < n ? u : u - n)) * F8_BN;
-      if (!(lo_last <= kb && hi_first >= kb + F8_BN)) {  // edge tile (uniform branch)
+      const int kt0 = (t_lo + (u < n ? u : u - n)) * F8_BN;  // the key tile's first key
+      const int kb = kt0 + half * 64;                         // this half's first key
+      if (!(lo_last <= kt0 && hi_first >= kt0 + F8_BN)) {  // edge tile (uniform branch)
 #pragma unroll
-        for (int cc = 0; cc < 128; ++cc) s[cc] = in_range(kb + cc, lo_i, hi_i) ? s[cc] : -INFINITY;
+        for (int cc = 0; cc < 64; ++cc) s[cc] = in_range(kb + cc, lo_i, hi_i) ? s[cc] : -INFINITY;
       }
       if (u < n) {
 #pragma unroll
-        for (int cc = 0; cc < 128; ++cc) m = fmaxf(m, s[cc]);
-        if (u == n - 1) mb = m == -INFINITY ? 0.f : m * sl2;
+        for (int cc = 0; cc < 64; ++cc) mm[cc & 3] = fmaxf(mm[cc & 3], s[cc]);
+        if (u == n - 1) {
+          // both halves' maxima: the row max the definition normalises by
+          const float mine = fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3]));
+          xch[half * F8_BM + r] = mine;
+          mbar_arrive(&bar_x[0]);
+          if (!__all_sync(0xffffffffu, mbar_wait(&bar_x[0], 0, abort_flag))) {
+            ok = false;
+            break;
+          }
+          m = fmaxf(mine, xch[(half ^ 1) * F8_BM + r]);
+          mb = m == -INFINITY ? 0.f : m * sl2;
+        }
       } else {
-        uint32_t pk[32];
+        uint32_t pk[16];
         float rs = 0.f;
 #pragma unroll
-        for (int cc = 0; cc < 32; ++cc) {
+        for (int cc = 0; cc < 16; ++cc) {
           const float p0 = ex2(fmaf(s[4 * cc], sl2, -mb)), p1 = ex2(fmaf(s[4 * cc + 1], sl2, -mb));
           const float p2 = ex2(fmaf(s[4 * cc + 2], sl2, -mb)), p3 = ex2(fmaf(s[4 * cc + 3], sl2, -mb));
           rs += (p0 + p1) + (p2 + p3);
           pk[cc] = pack_e4m3x4(p0 * 448.f, p1 * 448.f, p2 * 448.f, p3 * 448.f);
         }
         l += rs;
-        tmem_st32(scol, pk);
+        tmem_st16(scol, pk);
         tmem_wait_st();
       }
       tc_fence_before();
       mbar_arrive(&bar_p[u & 1]);
     }
     if (ok && n > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_o, 0, abort_flag));
+      // the row sum over both halves
+      xch[(2 + half) * F8_BM + r] = l;
+      mbar_arrive(&bar_x[1]);
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar_x[1], 0, abort_flag)) &&
+           __all_sync(0xffffffffu, mbar_wait(bar_o, 0, abort_flag));
+      l += xch[(2 + (half ^ 1)) * F8_BM + r];
       tc_fence_after();
     }
     if (!ok) {
@@ -364,13 +390,13 @@ __global__ void __launch_bounds__(256, 1)
       const bool valid = i < si.lq;
       const float mul = l > 0.f ? p.o_scale / l : 0.f;
       using T = typename E::T;
-      T* orow = reinterpret_cast<T*>(p.o) + ((long long)(si.qrow0 + i) * g.nh_q + qhead) * F8_D;
+      T* orow = reinterpret_cast<T*>(p.o) + ((long long)(si.qrow0 + i) * g.nh_q + qhead) * F8_D + half * 64;
 #pragma unroll 1
-      for (int cc = 0; cc < F8_D / 32; ++cc) {
+      for (int cc = 0; cc < 2; ++cc) {
         uint32_t packed[16];
         if (n > 0) {
           uint32_t uu[32];
-          tmem_ld32(lane_base + F8_TM_O + cc * 32, uu);
+          tmem_ld32(lane_base + F8_TM_O + half * 64 + cc * 32, uu);
           tmem_wait_ld();
           reg_fence(uu);
 #pragma unroll
@@ -388,7 +414,7 @@ __global__ void __launch_bounds__(256, 1)
         }
       }
       float* lse_at = p.lse + (long long)(si.qrow0 + i) * g.nh_q + qhead;
-      if (valid && SDPA_ADDR_OK(g.chk, lse_at, 4)) *lse_at = l > 0.f ? m * g.scale + logf(l) : -INFINITY;
+      if (half == 0 && valid && SDPA_ADDR_OK(g.chk, lse_at, 4)) *lse_at = l > 0.f ? m * g.scale + logf(l) : -INFINITY;
     }
   }
 
@@ -418,7 +444,7 @@ int launch_fwd_fp8(const Fp8Launch& L, bool bf16) {
   return launch_in_grids(grid, [&](long long off, long long count) {
     Fp8Params pp = p;
     pp.item_offset = (int)off;
-    kern<<<(unsigned)count, 256, F8_SMEM, L.stream>>>(L.tmQ, L.tmK, L.tmVt, pp);
+    kern<<<(unsigned)count, F8_THREADS, F8_SMEM, L.stream>>>(L.tmQ, L.tmK, L.tmVt, pp);
     return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
   });
 }
