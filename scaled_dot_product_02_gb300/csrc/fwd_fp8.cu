@@ -33,6 +33,8 @@
 // packs its P8 into the first 16 columns of its own 64 of the S buffer, so
 // neither overwrites scores the other has not read.
 // TMEM: O [0,128), S/P buffers [128,256) and [256,384).
+#include <algorithm>
+
 #include <cuda.h>
 #include <cuda_runtime.h>
 
@@ -47,8 +49,8 @@ namespace {
 constexpr int F8_BM = 128, F8_BN = 128, F8_D = 128;
 constexpr int F8_TILE = 16384;  // 128 rows x 128 one-byte columns
 constexpr int F8_NST = 8;
-constexpr int F8_NBARS = 2 * F8_NST + 9;
-constexpr int F8_XCH = 2 * 2 * F8_BM * 4;  // [max, sum][half][row] partials of the two warpgroups
+constexpr int F8_NBARS = 2 * F8_NST + 11;
+constexpr int F8_XCH = 2 * 2 * 2 * F8_BM * 4;  // [tile parity][max, sum][half][row] partials of the two warpgroups
 constexpr int F8_SMEM = 1024 + F8_TILE + F8_NST * F8_TILE + F8_XCH + F8_NBARS * 8 + 16;
 constexpr int F8_THREADS = 384;
 constexpr int F8_TM_O = 0, F8_TM_S = 128;
@@ -137,49 +139,67 @@ __global__ void __launch_bounds__(256) vt_kernel(const Fp8Params p) {
   }
 }
 
+// A query tile of the heaviest-first order (the last query tiles of every
+// sequence first, GQA heads adjacent) and the key tiles it sees.
+struct Fp8Tile {
+  int q0, q_last, t_lo, n, qhead, khead, vrow0;
+  SeqInfo si;
+  KeyRange kr;
+};
+
+__device__ __forceinline__ bool fp8_tile(const Fp8Params& p, int idx, Fp8Tile& t) {
+  const Geom& g = p.g;
+  const int h = idx % g.hq;
+  idx /= g.hq;
+  const int b = idx % g.batch;
+  idx /= g.batch;
+  t.q0 = (p.n_q_tiles - 1 - idx) * F8_BM;
+  t.si = seq_info(g, b);
+  if (t.q0 >= t.si.lq) return false;
+  t.kr = key_range(g, t.si.lq, t.si.lk);
+  t.q_last = min(t.q0 + F8_BM - 1, t.si.lq - 1);
+  const int lo = t.kr.lo(t.q0), hi = t.kr.hi(t.q_last);
+  t.t_lo = lo / F8_BN;
+  t.n = hi > lo ? (hi + F8_BN - 1) / F8_BN - t.t_lo : 0;
+  t.qhead = t.si.qhead0 + h;
+  t.khead = t.si.khead0 + h / (g.hq / g.hkv);
+  t.vrow0 = vt_row0(g, b, t.si);
+  return true;
+}
+
+// Persistent: CTA c takes the tiles c, c + gridDim.x, ... of the order, and
+// every role walks that same sequence, so no tile is handed between them.
+// Barrier phases run on across tiles (the steps of all tiles so far, and the
+// tiles with keys so far). Q has one buffer: the producer loads the next
+// tile's Q as soon as this tile's last S MMA is done (q_free), while its
+// P8 V MMAs still run. O is overwritten by a tile's first P8 V only after the
+// epilogue of the tile before has read it out of TMEM (o_free), and that
+// epilogue's global stores overlap the next tile's first S MMAs.
 template <bool BF16>
 __global__ void __launch_bounds__(F8_THREADS, 1)
     fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmVt, const __grid_constant__ Fp8Params p) {
   using E = Elem<BF16>;
   const Geom& g = p.g;
-
-  // ---- which tile: heaviest (last) query tiles first, GQA heads adjacent
-  int idx = blockIdx.x + p.item_offset;
-  const int h = idx % g.hq;
-  idx /= g.hq;
-  const int b = idx % g.batch;
-  idx /= g.batch;
-  const int qt = p.n_q_tiles - 1 - idx;
-  const SeqInfo si = seq_info(g, b);
-  const int q0 = qt * F8_BM;
-  if (q0 >= si.lq) return;
   if (p.guard && *reinterpret_cast<volatile const int*>(p.guard)) return;
-
-  const KeyRange kr = key_range(g, si.lq, si.lk);
-  const int q_last = min(q0 + F8_BM - 1, si.lq - 1);
-  const int kv_lo = kr.lo(q0), kv_hi = kr.hi(q_last);
-  const int t_lo = kv_lo / F8_BN;
-  const int n = (kv_hi > kv_lo) ? (kv_hi + F8_BN - 1) / F8_BN - t_lo : 0;
-  const int steps = 2 * n;  // pass 1 (max, sum) then pass 2 (P8, P8 V) over the same key tiles
-  const int qhead = si.qhead0 + h;
-  const int khead = si.khead0 + h / (g.hq / g.hkv);
-  const int vrow0 = vt_row0(g, b, si);
+  const int total = p.total_tiles;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint8_t* sQ = smem;
   uint8_t* sStage = smem + F8_TILE;
-  float* xch = reinterpret_cast<float*>(sStage + F8_NST * F8_TILE);  // [2][2][F8_BM]
+  float* xch = reinterpret_cast<float*>(sStage + F8_NST * F8_TILE);  // [tile parity][max, sum][half][row]
   uint64_t* full = reinterpret_cast<uint64_t*>(sStage + F8_NST * F8_TILE + F8_XCH);
   uint64_t* empty = full + F8_NST;
   uint64_t* bar_q = empty + F8_NST;
   uint64_t* bar_s = bar_q + 1;  // [2] S of a step ready
   uint64_t* bar_p = bar_s + 2;  // [2] the softmax is done with a step's buffer (pass 2: P8 written)
-  uint64_t* bar_o = bar_p + 2;  // the last P8 V (and so every MMA) complete
+  uint64_t* bar_o = bar_p + 2;  // a tile's last P8 V (and so every MMA of it) complete
   uint64_t* bar_drain = bar_o + 1;
   uint64_t* bar_x = bar_drain + 1;  // [2] the max / sum partials of both warpgroups are written
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_drain + 1);
+  uint64_t* q_free = bar_x + 2;     // a tile's last S MMA is done: Q may be replaced
+  uint64_t* o_free = q_free + 1;    // the epilogue has read O out of TMEM
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(o_free + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
@@ -193,10 +213,12 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
     mbar_init(&bar_s[1], 1);
     mbar_init(&bar_p[0], 256);
     mbar_init(&bar_p[1], 256);
-    mbar_init(&bar_x[0], 256);
-    mbar_init(&bar_x[1], 256);
     mbar_init(bar_o, 1);
     mbar_init(bar_drain, 1);
+    mbar_init(&bar_x[0], 256);
+    mbar_init(&bar_x[1], 256);
+    mbar_init(q_free, 1);
+    mbar_init(o_free, 256);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -209,34 +231,44 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  // Ring order (the MMA warp consumes in the same order): K of steps 0 and 1;
-  // then for every step u, Vt of its key tile if u is a pass-2 step, and K of
-  // step u + 2. Step u covers key tile (u < n ? u : u - n).
+  // Ring order (the MMA warp consumes in the same order), per tile: K of steps
+  // 0 and 1; then for every step u, Vt of its key tile if u is a pass-2 step,
+  // and K of step u + 2. Step u covers key tile (u < n ? u : u - n).
   if (warp == 0) {
-    if (elect_one() && n > 0) {
+    if (elect_one()) {
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmVt);
-      mbar_arrive_expect_tx(bar_q, F8_TILE);
-      tma_load_3d(&tmQ, bar_q, sQ, 0, qhead, si.qrow0 + q0);
-      int c = 0;
+      int c = 0, nq = 0;
       bool ok = true;
-      auto load = [&](bool v_tile, int tile) -> bool {
-        const int slot = c % F8_NST;
-        if (!mbar_wait(&empty[slot], ((c / F8_NST) & 1) ^ 1, abort_flag)) return false;
-        mbar_arrive_expect_tx(&full[slot], F8_TILE);
-        uint8_t* dst = sStage + slot * F8_TILE;
-        if (v_tile)
-          tma_load_3d(&tmVt, &full[slot], dst, vrow0 + (t_lo + tile) * F8_BN, 0, khead);
-        else
-          tma_load_3d(&tmK, &full[slot], dst, 0, khead, si.krow0 + (t_lo + tile) * F8_BN);
-        ++c;
-        return true;
-      };
-      for (int u = 0; u < 2 && u < steps && ok; ++u) ok = load(false, u < n ? u : u - n);
-      for (int u = 0; u < steps && ok; ++u) {
-        if (u >= n) ok = load(true, u - n);
-        if (ok && u + 2 < steps) ok = load(false, u + 2 < n ? u + 2 : u + 2 - n);
+      for (int idx = blockIdx.x; idx < total && ok; idx += gridDim.x) {
+        Fp8Tile t;
+        if (!fp8_tile(p, idx, t) || t.n == 0) continue;
+        const int n = t.n, steps = 2 * n;
+        if (nq > 0 && !mbar_wait(q_free, (nq - 1) & 1, abort_flag)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(bar_q, F8_TILE);
+        tma_load_3d(&tmQ, bar_q, sQ, 0, t.qhead, t.si.qrow0 + t.q0);
+        ++nq;
+        auto load = [&](bool v_tile, int tile) -> bool {
+          const int slot = c % F8_NST;
+          if (!mbar_wait(&empty[slot], ((c / F8_NST) & 1) ^ 1, abort_flag)) return false;
+          mbar_arrive_expect_tx(&full[slot], F8_TILE);
+          uint8_t* dst = sStage + slot * F8_TILE;
+          if (v_tile)
+            tma_load_3d(&tmVt, &full[slot], dst, t.vrow0 + (t.t_lo + tile) * F8_BN, 0, t.khead);
+          else
+            tma_load_3d(&tmK, &full[slot], dst, 0, t.khead, t.si.krow0 + (t.t_lo + tile) * F8_BN);
+          ++c;
+          return true;
+        };
+        for (int u = 0; u < 2 && u < steps && ok; ++u) ok = load(false, u < n ? u : u - n);
+        for (int u = 0; u < steps && ok; ++u) {
+          if (u >= n) ok = load(true, u - n);
+          if (ok && u + 2 < steps) ok = load(false, u + 2 < n ? u + 2 : u + 2 - n);
+        }
       }
       if (!ok) {
         *abort_flag = 1;
@@ -244,55 +276,72 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
       }
       const int first = c > F8_NST ? c - F8_NST : 0;
       for (int k = first; k < c; ++k) mbar_wait_drain(&full[k % F8_NST], (k / F8_NST) & 1);
-      mbar_wait_drain(bar_q, 0);
+      if (nq > 0) mbar_wait_drain(bar_q, (nq - 1) & 1);
     }
   } else if (warp == 1) {
-    if (elect_one() && n > 0) {
+    if (elect_one()) {
       constexpr uint32_t IDESC = idesc_e4m3(128, 128);
-      int c = 0;
-      bool ok = mbar_wait(bar_q, 0, abort_flag);
-      tc_fence_after();
       const uint32_t q_base = smem_u32(sQ);
-      auto mma_s = [&](int u) -> bool {
-        const int slot = c % F8_NST;
-        if (!mbar_wait(&full[slot], (c / F8_NST) & 1, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t kb = smem_u32(sStage + slot * F8_TILE);
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)  // 32 one-byte columns per MMA
-          mma_f8_ss(tmem + F8_TM_S + (u & 1) * 128, smem_desc_sw128(q_base + ks * 32, 16, 1024),
-                    smem_desc_sw128(kb + ks * 32, 16, 1024), IDESC, ks != 0);
-        mma_commit(&empty[slot]);
-        mma_commit(&bar_s[u & 1]);
-        ++c;
-        return true;
-      };
-      auto mma_o = [&](int u) -> bool {
-        const int slot = c % F8_NST;
-        if (!mbar_wait(&full[slot], (c / F8_NST) & 1, abort_flag)) return false;
-        tc_fence_after();
-        const uint32_t vb = smem_u32(sStage + slot * F8_TILE);
-        const uint32_t pcol = tmem + F8_TM_S + (u & 1) * 128;
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks)  // 32 keys per MMA: 8 TMEM columns of packed P8 (each half's first 16)
-          mma_f8_ts(tmem + F8_TM_O, pcol + (ks >> 1) * 64 + (ks & 1) * 8, smem_desc_sw128(vb + ks * 32, 16, 1024),
-                    IDESC, (u - n) > 0 || ks != 0);
-        mma_commit(&empty[slot]);
-        if (u == steps - 1) mma_commit(bar_o);  // one completion: every P8 V is done
-        ++c;
-        return true;
-      };
-      for (int u = 0; u < 2 && u < steps && ok; ++u) ok = mma_s(u);
-      for (int u = 0; u < steps && ok; ++u) {
-        if (!mbar_wait(&bar_p[u & 1], (u >> 1) & 1, abort_flag)) {
+      int c = 0, nq = 0, gu = 0, no = 0;
+      bool ok = true;
+      for (int idx = blockIdx.x; idx < total && ok; idx += gridDim.x) {
+        Fp8Tile t;
+        if (!fp8_tile(p, idx, t) || t.n == 0) continue;
+        const int n = t.n, steps = 2 * n;
+        if (!mbar_wait(bar_q, nq & 1, abort_flag)) {
           ok = false;
           break;
         }
+        ++nq;
         tc_fence_after();
-        if (u >= n) ok = mma_o(u);
-        // S of step u + 2 reuses step u's buffer: the MMAs run in issue order, so
-        // it lands after P8 V of step u has read the buffer
-        if (ok && u + 2 < steps) ok = mma_s(u + 2);
+        auto mma_s = [&](int u) -> bool {
+          const int slot = c % F8_NST;
+          if (!mbar_wait(&full[slot], (c / F8_NST) & 1, abort_flag)) return false;
+          tc_fence_after();
+          const uint32_t kb = smem_u32(sStage + slot * F8_TILE);
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)  // 32 one-byte columns per MMA
+            mma_f8_ss(tmem + F8_TM_S + ((gu + u) & 1) * 128, smem_desc_sw128(q_base + ks * 32, 16, 1024),
+                      smem_desc_sw128(kb + ks * 32, 16, 1024), IDESC, ks != 0);
+          mma_commit(&empty[slot]);
+          mma_commit(&bar_s[(gu + u) & 1]);
+          if (u == steps - 1) mma_commit(q_free);  // the tile's last read of Q
+          ++c;
+          return true;
+        };
+        auto mma_o = [&](int u) -> bool {
+          if (u == n && no > 0) {  // O still holds the previous tile until its epilogue read it
+            if (!mbar_wait(o_free, (no - 1) & 1, abort_flag)) return false;
+            tc_fence_after();
+          }
+          const int slot = c % F8_NST;
+          if (!mbar_wait(&full[slot], (c / F8_NST) & 1, abort_flag)) return false;
+          tc_fence_after();
+          const uint32_t vb = smem_u32(sStage + slot * F8_TILE);
+          const uint32_t pcol = tmem + F8_TM_S + ((gu + u) & 1) * 128;
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)  // 32 keys per MMA: 8 TMEM columns of packed P8 (each half's first 16)
+            mma_f8_ts(tmem + F8_TM_O, pcol + (ks >> 1) * 64 + (ks & 1) * 8, smem_desc_sw128(vb + ks * 32, 16, 1024),
+                      IDESC, (u - n) > 0 || ks != 0);
+          mma_commit(&empty[slot]);
+          if (u == steps - 1) mma_commit(bar_o);  // one completion: every P8 V of the tile is done
+          ++c;
+          return true;
+        };
+        for (int u = 0; u < 2 && u < steps && ok; ++u) ok = mma_s(u);
+        for (int u = 0; u < steps && ok; ++u) {
+          if (!mbar_wait(&bar_p[(gu + u) & 1], ((gu + u) >> 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (u >= n) ok = mma_o(u);
+          // S of step u + 2 reuses step u's buffer: the MMAs run in issue order, so
+          // it lands after P8 V of step u has read the buffer
+          if (ok && u + 2 < steps) ok = mma_s(u + 2);
+        }
+        gu += steps;
+        ++no;
       }
       if (!ok) {
         *abort_flag = 1;
@@ -305,116 +354,135 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
     const int half = (warp - 4) >> 2;  // this warpgroup's keys and O columns: [64*half, 64*half+64)
     const int wq = warp & 3;
     const int r = wq * 32 + lane;
-    const int i = q0 + r;
     const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
     const float sl2 = g.scale_log2;
-    const int lo_i = kr.lo(i), hi_i = kr.hi(i);
-    const int lo_last = kr.lo(q_last), hi_first = kr.hi(q0);
-    // pass 1: the row max over this half's keys, four independent chains
-    float mm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-    float m = -INFINITY;  // the row max over all keys (raw score units), after pass 1
-    float mb = 0.f, l = 0.f;  // pass 2: m * scale * log2e, and the sum of P~ over this half's keys
+    using T = typename E::T;
+    int gu = 0, nt = 0;
     bool ok = true;
-    for (int u = 0; u < steps; ++u) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&bar_s[u & 1], (u >> 1) & 1, abort_flag))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t scol = lane_base + F8_TM_S + (u & 1) * 128 + half * 64;
-      float s[64];
-      {
-        uint32_t u0[32], u1[32];
-        tmem_ld32(scol, u0);
-        tmem_ld32(scol + 32, u1);
-        tmem_wait_ld();
-        reg_fence(u0);
-        reg_fence(u1);
+    for (int idx = blockIdx.x; idx < total && ok; idx += gridDim.x) {
+      Fp8Tile t;
+      if (!fp8_tile(p, idx, t)) continue;
+      const int n = t.n, steps = 2 * n;
+      const int i = t.q0 + r;
+      const bool valid = i < t.si.lq;
+      const int lo_i = t.kr.lo(i), hi_i = t.kr.hi(i);
+      const int lo_last = t.kr.lo(t.q_last), hi_first = t.kr.hi(t.q0);
+      T* orow = reinterpret_cast<T*>(p.o) + ((long long)(t.si.qrow0 + i) * g.nh_q + t.qhead) * F8_D + half * 64;
+      float* lse_at = p.lse + (long long)(t.si.qrow0 + i) * g.nh_q + t.qhead;
+      if (n == 0) {  // no key for any row of the tile: O = 0, LSE = -inf
+        if (valid && SDPA_ADDR_OK(g.chk, orow, 128)) {
+          uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
-        for (int cc = 0; cc < 32; ++cc) {
-          s[cc] = __uint_as_float(u0[cc]);
-          s[32 + cc] = __uint_as_float(u1[cc]);
+          for (int e = 0; e < 8; ++e) dst[e] = make_uint4(0u, 0u, 0u, 0u);
         }
+        if (half == 0 && valid && SDPA_ADDR_OK(g.chk, lse_at, 4)) *lse_at = -INFINITY;
+        continue;
       }
-      const int kt0 = (t_lo + (u < n ? u : u - n)) * F8_BN;  // the key tile's first key
-      const int kb = kt0 + half * 64;                         // this half's first key
-      if (!(lo_last <= kt0 && hi_first >= kt0 + F8_BN)) {  // edge tile (uniform branch)
+      float* xm = xch + (nt & 1) * 4 * F8_BM;  // this tile's partials: [max, sum][half][row]
+      // pass 1: the row max over this half's keys, four independent chains
+      float mm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      float m = -INFINITY;      // the row max over all keys (raw score units), after pass 1
+      float mb = 0.f, l = 0.f;  // pass 2: m * scale * log2e, and the sum of P~ over this half's keys
+      for (int u = 0; u < steps; ++u) {
+        const int su = gu + u;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bar_s[su & 1], (su >> 1) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t scol = lane_base + F8_TM_S + (su & 1) * 128 + half * 64;
+        float s[64];
+        {
+          uint32_t u0[32], u1[32];
+          tmem_ld32(scol, u0);
+          tmem_ld32(scol + 32, u1);
+          tmem_wait_ld();
+          reg_fence(u0);
+          reg_fence(u1);
 #pragma unroll
-        for (int cc = 0; cc < 64; ++cc) s[cc] = in_range(kb + cc, lo_i, hi_i) ? s[cc] : -INFINITY;
-      }
-      if (u < n) {
-#pragma unroll
-        for (int cc = 0; cc < 64; ++cc) mm[cc & 3] = fmaxf(mm[cc & 3], s[cc]);
-        if (u == n - 1) {
-          // both halves' maxima: the row max the definition normalises by
-          const float mine = fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3]));
-          xch[half * F8_BM + r] = mine;
-          mbar_arrive(&bar_x[0]);
-          if (!__all_sync(0xffffffffu, mbar_wait(&bar_x[0], 0, abort_flag))) {
-            ok = false;
-            break;
+          for (int cc = 0; cc < 32; ++cc) {
+            s[cc] = __uint_as_float(u0[cc]);
+            s[32 + cc] = __uint_as_float(u1[cc]);
           }
-          m = fmaxf(mine, xch[(half ^ 1) * F8_BM + r]);
-          mb = m == -INFINITY ? 0.f : m * sl2;
         }
-      } else {
-        uint32_t pk[16];
-        float rs = 0.f;
+        const int kt0 = (t.t_lo + (u < n ? u : u - n)) * F8_BN;  // the key tile's first key
+        const int kb = kt0 + half * 64;                           // this half's first key
+        if (!(lo_last <= kt0 && hi_first >= kt0 + F8_BN)) {    // edge tile (uniform branch)
 #pragma unroll
-        for (int cc = 0; cc < 16; ++cc) {
-          const float p0 = ex2(fmaf(s[4 * cc], sl2, -mb)), p1 = ex2(fmaf(s[4 * cc + 1], sl2, -mb));
-          const float p2 = ex2(fmaf(s[4 * cc + 2], sl2, -mb)), p3 = ex2(fmaf(s[4 * cc + 3], sl2, -mb));
-          rs += (p0 + p1) + (p2 + p3);
-          pk[cc] = pack_e4m3x4(p0 * 448.f, p1 * 448.f, p2 * 448.f, p3 * 448.f);
+          for (int cc = 0; cc < 64; ++cc) s[cc] = in_range(kb + cc, lo_i, hi_i) ? s[cc] : -INFINITY;
         }
-        l += rs;
-        tmem_st16(scol, pk);
-        tmem_wait_st();
+        if (u < n) {
+#pragma unroll
+          for (int cc = 0; cc < 64; ++cc) mm[cc & 3] = fmaxf(mm[cc & 3], s[cc]);
+          if (u == n - 1) {
+            // both halves' maxima: the row max the definition normalises by
+            const float mine = fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3]));
+            xm[half * F8_BM + r] = mine;
+            mbar_arrive(&bar_x[0]);
+            if (!__all_sync(0xffffffffu, mbar_wait(&bar_x[0], nt & 1, abort_flag))) {
+              ok = false;
+              break;
+            }
+            m = fmaxf(mine, xm[(half ^ 1) * F8_BM + r]);
+            mb = m == -INFINITY ? 0.f : m * sl2;
+          }
+        } else {
+          uint32_t pk[16];
+          float rs = 0.f;
+#pragma unroll
+          for (int cc = 0; cc < 16; ++cc) {
+            const float p0 = ex2(fmaf(s[4 * cc], sl2, -mb)), p1 = ex2(fmaf(s[4 * cc + 1], sl2, -mb));
+            const float p2 = ex2(fmaf(s[4 * cc + 2], sl2, -mb)), p3 = ex2(fmaf(s[4 * cc + 3], sl2, -mb));
+            rs += (p0 + p1) + (p2 + p3);
+            pk[cc] = pack_e4m3x4(p0 * 448.f, p1 * 448.f, p2 * 448.f, p3 * 448.f);
+          }
+          l += rs;
+          tmem_st16(scol, pk);
+          tmem_wait_st();
+        }
+        tc_fence_before();
+        mbar_arrive(&bar_p[su & 1]);
       }
-      tc_fence_before();
-      mbar_arrive(&bar_p[u & 1]);
-    }
-    if (ok && n > 0) {
-      // the row sum over both halves
-      xch[(2 + half) * F8_BM + r] = l;
+      if (!ok) break;
+      // the row sum over both halves, then every P8 V of the tile
+      xm[(2 + half) * F8_BM + r] = l;
       mbar_arrive(&bar_x[1]);
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar_x[1], 0, abort_flag)) &&
-           __all_sync(0xffffffffu, mbar_wait(bar_o, 0, abort_flag));
-      l += xch[(2 + (half ^ 1)) * F8_BM + r];
+      ok = __all_sync(0xffffffffu, mbar_wait(&bar_x[1], nt & 1, abort_flag)) &&
+           __all_sync(0xffffffffu, mbar_wait(bar_o, nt & 1, abort_flag));
+      if (!ok) break;
+      l += xm[(2 + (half ^ 1)) * F8_BM + r];
       tc_fence_after();
+      uint32_t ua[32], ub[32];
+      tmem_ld32(lane_base + F8_TM_O + half * 64, ua);
+      tmem_ld32(lane_base + F8_TM_O + half * 64 + 32, ub);
+      tmem_wait_ld();
+      reg_fence(ua);
+      reg_fence(ub);
+      tc_fence_before();
+      mbar_arrive(o_free);  // the next tile's P8 V may overwrite O
+      const float mul = l > 0.f ? p.o_scale / l : 0.f;
+      if (valid && SDPA_ADDR_OK(g.chk, orow, 128)) {
+        uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          dst[e] = make_uint4(E::pack(__uint_as_float(ua[8 * e]) * mul, __uint_as_float(ua[8 * e + 1]) * mul),
+                              E::pack(__uint_as_float(ua[8 * e + 2]) * mul, __uint_as_float(ua[8 * e + 3]) * mul),
+                              E::pack(__uint_as_float(ua[8 * e + 4]) * mul, __uint_as_float(ua[8 * e + 5]) * mul),
+                              E::pack(__uint_as_float(ua[8 * e + 6]) * mul, __uint_as_float(ua[8 * e + 7]) * mul));
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          dst[4 + e] = make_uint4(E::pack(__uint_as_float(ub[8 * e]) * mul, __uint_as_float(ub[8 * e + 1]) * mul),
+                                  E::pack(__uint_as_float(ub[8 * e + 2]) * mul, __uint_as_float(ub[8 * e + 3]) * mul),
+                                  E::pack(__uint_as_float(ub[8 * e + 4]) * mul, __uint_as_float(ub[8 * e + 5]) * mul),
+                                  E::pack(__uint_as_float(ub[8 * e + 6]) * mul, __uint_as_float(ub[8 * e + 7]) * mul));
+      }
+      if (half == 0 && valid && SDPA_ADDR_OK(g.chk, lse_at, 4)) *lse_at = l > 0.f ? m * g.scale + logf(l) : -INFINITY;
+      gu += steps;
+      ++nt;
     }
     if (!ok) {
       *abort_flag = 1;
       record_error(p.err, SDPA_ERR_TIMEOUT);
-    } else {
-      const bool valid = i < si.lq;
-      const float mul = l > 0.f ? p.o_scale / l : 0.f;
-      using T = typename E::T;
-      T* orow = reinterpret_cast<T*>(p.o) + ((long long)(si.qrow0 + i) * g.nh_q + qhead) * F8_D + half * 64;
-#pragma unroll 1
-      for (int cc = 0; cc < 2; ++cc) {
-        uint32_t packed[16];
-        if (n > 0) {
-          uint32_t uu[32];
-          tmem_ld32(lane_base + F8_TM_O + half * 64 + cc * 32, uu);
-          tmem_wait_ld();
-          reg_fence(uu);
-#pragma unroll
-          for (int e = 0; e < 16; ++e)
-            packed[e] = E::pack(__uint_as_float(uu[2 * e]) * mul, __uint_as_float(uu[2 * e + 1]) * mul);
-        } else {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) packed[e] = 0u;
-        }
-        if (valid && SDPA_ADDR_OK(g.chk, orow + cc * 32, 64)) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
-#pragma unroll
-          for (int e = 0; e < 4; ++e)
-            dst[e] = make_uint4(packed[4 * e], packed[4 * e + 1], packed[4 * e + 2], packed[4 * e + 3]);
-        }
-      }
-      float* lse_at = p.lse + (long long)(si.qrow0 + i) * g.nh_q + qhead;
-      if (half == 0 && valid && SDPA_ADDR_OK(g.chk, lse_at, 4)) *lse_at = l > 0.f ? m * g.scale + logf(l) : -INFINITY;
     }
   }
 
@@ -436,17 +504,20 @@ int launch_vt(const Fp8Params& p, cudaStream_t stream) {
 }
 
 int launch_fwd_fp8(const Fp8Launch& L, bool bf16) {
-  const Fp8Params& p = L.p;
-  const long long grid = (long long)p.n_q_tiles * p.g.hq * p.g.batch;
-  if (grid > 0x7fffffffLL) return SDPA_ERR_UNSUPPORTED;
+  const long long tiles = (long long)L.p.n_q_tiles * L.p.g.hq * L.p.g.batch;
+  if (tiles <= 0) return SDPA_OK;
+  if (tiles > 0x7fffffffLL - 4096) return SDPA_ERR_UNSUPPORTED;
   auto kern = bf16 ? fwd_fp8_kernel<true> : fwd_fp8_kernel<false>;
   if (const int rc = set_kernel_smem(reinterpret_cast<const void*>(kern), F8_SMEM, -1)) return rc;
-  return launch_in_grids(grid, [&](long long off, long long count) {
-    Fp8Params pp = p;
-    pp.item_offset = (int)off;
-    kern<<<(unsigned)count, F8_THREADS, F8_SMEM, L.stream>>>(L.tmQ, L.tmK, L.tmVt, pp);
-    return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
-  });
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return SDPA_ERR_CUDA;
+  Fp8Params p = L.p;
+  p.total_tiles = (int)tiles;
+  long long grid = std::min<long long>(tiles, sms);
+  if (debug_max_ctas() > 0) grid = std::min<long long>(grid, debug_max_ctas());  // the CTAs stride over every tile
+  kern<<<(unsigned)grid, F8_THREADS, F8_SMEM, L.stream>>>(L.tmQ, L.tmK, L.tmVt, p);
+  return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }
 
 }  // namespace sdpa
