@@ -29,10 +29,13 @@
 // in each warpgroup, warpgroup `half` owning the keys [64*half, 64*half+64)
 // of every key tile and the value columns [64*half, 64*half+64) of O. Each
 // keeps a partial row max (pass 1) and sum (pass 2) over its keys; the two
-// are combined through shared memory once per query tile. A warpgroup
-// packs its P8 into the first 16 columns of its own 64 of the S buffer, so
-// neither overwrites scores the other has not read.
-// TMEM: O [0,128), S/P buffers [128,256) and [256,384).
+// are combined through shared memory once per query tile.
+// A warpgroup releases a step's S buffer as soon as it has loaded the scores
+// into registers, so the S MMA two steps ahead runs during this step's
+// softmax; P8 has buffers of its own, released by the P8 V MMA that read
+// them.
+// TMEM: O [0,128), S buffers [128,256) and [256,384), P8 buffers [384,416)
+// and [416,448) (16 columns per warpgroup: 64 keys of one byte).
 #include <algorithm>
 
 #include <cuda.h>
@@ -49,11 +52,13 @@ namespace {
 constexpr int F8_BM = 128, F8_BN = 128, F8_D = 128;
 constexpr int F8_TILE = 16384;  // 128 rows x 128 one-byte columns
 constexpr int F8_NST = 8;
-constexpr int F8_NBARS = 2 * F8_NST + 11;
+constexpr int F8_NBARS = 2 * F8_NST + 15;
 constexpr int F8_XCH = 2 * 2 * 2 * F8_BM * 4;  // [tile parity][max, sum][half][row] partials of the two warpgroups
 constexpr int F8_SMEM = 1024 + F8_TILE + F8_NST * F8_TILE + F8_XCH + F8_NBARS * 8 + 16;
 constexpr int F8_THREADS = 384;
-constexpr int F8_TM_O = 0, F8_TM_S = 128;
+constexpr int F8_TM_O = 0, F8_TM_S = 128, F8_TM_P = 384;
+constexpr float kLog2_448 = 8.807354922057604f;  // log2(448)
+constexpr float kLn448 = 6.104793232414985f;     // ln(448)
 
 // Instruction descriptor for kind::f8f6f4 with E4M3 A and B (format code 0),
 // both K-major, fp32 accumulator.
@@ -192,9 +197,11 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
   uint64_t* full = reinterpret_cast<uint64_t*>(sStage + F8_NST * F8_TILE + F8_XCH);
   uint64_t* empty = full + F8_NST;
   uint64_t* bar_q = empty + F8_NST;
-  uint64_t* bar_s = bar_q + 1;  // [2] S of a step ready
-  uint64_t* bar_p = bar_s + 2;  // [2] the softmax is done with a step's buffer (pass 2: P8 written)
-  uint64_t* bar_o = bar_p + 2;  // a tile's last P8 V (and so every MMA of it) complete
+  uint64_t* bar_s = bar_q + 1;   // [2] S of a step ready (by S buffer)
+  uint64_t* bar_sf = bar_s + 2;  // [2] the softmax has loaded a step's S: its buffer is free
+  uint64_t* bar_pr = bar_sf + 2; // [2] P8 of a pass-2 step written (by P8 buffer)
+  uint64_t* bar_pf = bar_pr + 2; // [2] the P8 V MMA has read a P8 buffer
+  uint64_t* bar_o = bar_pf + 2;  // a tile's last P8 V (and so every MMA of it) complete
   uint64_t* bar_drain = bar_o + 1;
   uint64_t* bar_x = bar_drain + 1;  // [2] the max / sum partials of both warpgroups are written
   uint64_t* q_free = bar_x + 2;     // a tile's last S MMA is done: Q may be replaced
@@ -211,8 +218,11 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
     mbar_init(bar_q, 1);
     mbar_init(&bar_s[0], 1);
     mbar_init(&bar_s[1], 1);
-    mbar_init(&bar_p[0], 256);
-    mbar_init(&bar_p[1], 256);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&bar_sf[b], 256);
+      mbar_init(&bar_pr[b], 256);
+      mbar_init(&bar_pf[b], 1);
+    }
     mbar_init(bar_o, 1);
     mbar_init(bar_drain, 1);
     mbar_init(&bar_x[0], 256);
@@ -232,8 +242,8 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
   const uint32_t tmem = *tmem_holder;
 
   // Ring order (the MMA warp consumes in the same order), per tile: K of steps
-  // 0 and 1; then for every step u, Vt of its key tile if u is a pass-2 step,
-  // and K of step u + 2. Step u covers key tile (u < n ? u : u - n).
+  // 0 and 1; then for every step u, K of step u + 2, and Vt of its key tile
+  // if u is a pass-2 step. Step u covers key tile (u < n ? u : u - n).
   if (warp == 0) {
     if (elect_one()) {
       prefetch_tmap(&tmQ);
@@ -266,8 +276,8 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
         };
         for (int u = 0; u < 2 && u < steps && ok; ++u) ok = load(false, u < n ? u : u - n);
         for (int u = 0; u < steps && ok; ++u) {
-          if (u >= n) ok = load(true, u - n);
-          if (ok && u + 2 < steps) ok = load(false, u + 2 < n ? u + 2 : u + 2 - n);
+          if (u + 2 < steps) ok = load(false, u + 2 < n ? u + 2 : u + 2 - n);
+          if (ok && u >= n) ok = load(true, u - n);
         }
       }
       if (!ok) {
@@ -282,7 +292,7 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
     if (elect_one()) {
       constexpr uint32_t IDESC = idesc_e4m3(128, 128);
       const uint32_t q_base = smem_u32(sQ);
-      int c = 0, nq = 0, gu = 0, no = 0;
+      int c = 0, nq = 0, gu = 0, gp = 0, no = 0;  // ring loads, Q loads, steps, pass-2 steps, tiles so far
       bool ok = true;
       for (int idx = blockIdx.x; idx < total && ok; idx += gridDim.x) {
         Fp8Tile t;
@@ -294,51 +304,53 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
         }
         ++nq;
         tc_fence_after();
+        // S of step u into S buffer (gu + u) & 1, once the softmax has loaded
+        // that buffer's previous scores (step gu + u - 2)
         auto mma_s = [&](int u) -> bool {
+          const int su = gu + u;
+          if (su >= 2 && !mbar_wait(&bar_sf[su & 1], ((su - 2) >> 1) & 1, abort_flag)) return false;
           const int slot = c % F8_NST;
           if (!mbar_wait(&full[slot], (c / F8_NST) & 1, abort_flag)) return false;
           tc_fence_after();
           const uint32_t kb = smem_u32(sStage + slot * F8_TILE);
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)  // 32 one-byte columns per MMA
-            mma_f8_ss(tmem + F8_TM_S + ((gu + u) & 1) * 128, smem_desc_sw128(q_base + ks * 32, 16, 1024),
+            mma_f8_ss(tmem + F8_TM_S + (su & 1) * 128, smem_desc_sw128(q_base + ks * 32, 16, 1024),
                       smem_desc_sw128(kb + ks * 32, 16, 1024), IDESC, ks != 0);
           mma_commit(&empty[slot]);
-          mma_commit(&bar_s[(gu + u) & 1]);
+          mma_commit(&bar_s[su & 1]);
           if (u == steps - 1) mma_commit(q_free);  // the tile's last read of Q
           ++c;
           return true;
         };
+        // O += P8 V for pass-2 step u, once its P8 is written
         auto mma_o = [&](int u) -> bool {
           if (u == n && no > 0) {  // O still holds the previous tile until its epilogue read it
             if (!mbar_wait(o_free, (no - 1) & 1, abort_flag)) return false;
-            tc_fence_after();
           }
+          if (!mbar_wait(&bar_pr[gp & 1], (gp >> 1) & 1, abort_flag)) return false;
           const int slot = c % F8_NST;
           if (!mbar_wait(&full[slot], (c / F8_NST) & 1, abort_flag)) return false;
           tc_fence_after();
           const uint32_t vb = smem_u32(sStage + slot * F8_TILE);
-          const uint32_t pcol = tmem + F8_TM_S + ((gu + u) & 1) * 128;
+          const uint32_t pcol = tmem + F8_TM_P + (gp & 1) * 32;
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks)  // 32 keys per MMA: 8 TMEM columns of packed P8 (each half's first 16)
-            mma_f8_ts(tmem + F8_TM_O, pcol + (ks >> 1) * 64 + (ks & 1) * 8, smem_desc_sw128(vb + ks * 32, 16, 1024),
-                      IDESC, (u - n) > 0 || ks != 0);
+          for (int ks = 0; ks < 4; ++ks)  // 32 keys per MMA: 8 TMEM columns of packed P8
+            mma_f8_ts(tmem + F8_TM_O, pcol + ks * 8, smem_desc_sw128(vb + ks * 32, 16, 1024), IDESC,
+                      (u - n) > 0 || ks != 0);
           mma_commit(&empty[slot]);
+          mma_commit(&bar_pf[gp & 1]);
           if (u == steps - 1) mma_commit(bar_o);  // one completion: every P8 V of the tile is done
           ++c;
+          ++gp;
           return true;
         };
+        // Issue order: S(0), S(1); then per step u: S(u + 2) (as soon as the
+        // softmax has loaded S(u)), P8 V(u) (once it has written P8(u)).
         for (int u = 0; u < 2 && u < steps && ok; ++u) ok = mma_s(u);
         for (int u = 0; u < steps && ok; ++u) {
-          if (!mbar_wait(&bar_p[(gu + u) & 1], ((gu + u) >> 1) & 1, abort_flag)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          if (u >= n) ok = mma_o(u);
-          // S of step u + 2 reuses step u's buffer: the MMAs run in issue order, so
-          // it lands after P8 V of step u has read the buffer
-          if (ok && u + 2 < steps) ok = mma_s(u + 2);
+          if (u + 2 < steps) ok = mma_s(u + 2);
+          if (ok && u >= n) ok = mma_o(u);
         }
         gu += steps;
         ++no;
@@ -357,7 +369,7 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
     const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
     const float sl2 = g.scale_log2;
     using T = typename E::T;
-    int gu = 0, nt = 0;
+    int gu = 0, gp = 0, nt = 0;  // steps, pass-2 steps, tiles with keys so far
     bool ok = true;
     for (int idx = blockIdx.x; idx < total && ok; idx += gridDim.x) {
       Fp8Tile t;
@@ -381,8 +393,11 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
       float* xm = xch + (nt & 1) * 4 * F8_BM;  // this tile's partials: [max, sum][half][row]
       // pass 1: the row max over this half's keys, four independent chains
       float mm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      float m = -INFINITY;      // the row max over all keys (raw score units), after pass 1
-      float mb = 0.f, l = 0.f;  // pass 2: m * scale * log2e, and the sum of P~ over this half's keys
+      float m = -INFINITY;  // the row max over all keys (raw score units), after pass 1
+      // pass 2: the exponent's bias log2(448) - m * scale * log2e, so exp2 gives
+      // 448 P~ directly, and the sum of 448 P~ over this half's keys (two lanes)
+      float2 nb2 = make_float2(0.f, 0.f);
+      float2 l2 = make_float2(0.f, 0.f);
       for (int u = 0; u < steps; ++u) {
         const int su = gu + u;
         if (!__all_sync(0xffffffffu, mbar_wait(&bar_s[su & 1], (su >> 1) & 1, abort_flag))) {
@@ -405,6 +420,8 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
             s[32 + cc] = __uint_as_float(u1[cc]);
           }
         }
+        tc_fence_before();
+        mbar_arrive(&bar_sf[su & 1]);  // the S MMA two steps ahead may overwrite the buffer
         const int kt0 = (t.t_lo + (u < n ? u : u - n)) * F8_BN;  // the key tile's first key
         const int kb = kt0 + half * 64;                           // this half's first key
         if (!(lo_last <= kt0 && hi_first >= kt0 + F8_BN)) {    // edge tile (uniform branch)
@@ -424,27 +441,39 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
               break;
             }
             m = fmaxf(mine, xm[(half ^ 1) * F8_BM + r]);
-            mb = m == -INFINITY ? 0.f : m * sl2;
+            const float nb = kLog2_448 - (m == -INFINITY ? 0.f : m * sl2);
+            nb2 = make_float2(nb, nb);
           }
         } else {
           uint32_t pk[16];
-          float rs = 0.f;
+          const float2 sc2 = make_float2(sl2, sl2);
+          float2 ra = make_float2(0.f, 0.f), rb = make_float2(0.f, 0.f);
 #pragma unroll
           for (int cc = 0; cc < 16; ++cc) {
-            const float p0 = ex2(fmaf(s[4 * cc], sl2, -mb)), p1 = ex2(fmaf(s[4 * cc + 1], sl2, -mb));
-            const float p2 = ex2(fmaf(s[4 * cc + 2], sl2, -mb)), p3 = ex2(fmaf(s[4 * cc + 3], sl2, -mb));
-            rs += (p0 + p1) + (p2 + p3);
-            pk[cc] = pack_e4m3x4(p0 * 448.f, p1 * 448.f, p2 * 448.f, p3 * 448.f);
+            const float2 ta = ffma2(make_float2(s[4 * cc], s[4 * cc + 1]), sc2, nb2);
+            const float2 tb = ffma2(make_float2(s[4 * cc + 2], s[4 * cc + 3]), sc2, nb2);
+            const float2 pa = make_float2(ex2(ta.x), ex2(ta.y)), pb = make_float2(ex2(tb.x), ex2(tb.y));
+            ra = fadd2(ra, pa);
+            rb = fadd2(rb, pb);
+            pk[cc] = pack_e4m3x4(pa.x, pa.y, pb.x, pb.y);  // 448 P~, rounded once to E4M3
           }
-          l += rs;
-          tmem_st16(scol, pk);
+          l2 = fadd2(l2, fadd2(ra, rb));
+          // P8 buffer gp & 1, once the P8 V MMA two pass-2 steps back has read it
+          if (!__all_sync(0xffffffffu, mbar_wait(&bar_pf[gp & 1], ((gp >> 1) & 1) ^ 1, abort_flag))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          tmem_st16(lane_base + F8_TM_P + (gp & 1) * 32 + half * 16, pk);
           tmem_wait_st();
+          tc_fence_before();
+          mbar_arrive(&bar_pr[gp & 1]);
+          ++gp;
         }
-        tc_fence_before();
-        mbar_arrive(&bar_p[su & 1]);
       }
       if (!ok) break;
-      // the row sum over both halves, then every P8 V of the tile
+      // the row sum (of 448 P~) over both halves, then every P8 V of the tile
+      float l = l2.x + l2.y;
       xm[(2 + half) * F8_BM + r] = l;
       mbar_arrive(&bar_x[1]);
       ok = __all_sync(0xffffffffu, mbar_wait(&bar_x[1], nt & 1, abort_flag)) &&
@@ -460,7 +489,7 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
       reg_fence(ub);
       tc_fence_before();
       mbar_arrive(o_free);  // the next tile's P8 V may overwrite O
-      const float mul = l > 0.f ? p.o_scale / l : 0.f;
+      const float mul = l > 0.f ? p.o_scale * 448.f / l : 0.f;  // o_scale = d_v / 448
       if (valid && SDPA_ADDR_OK(g.chk, orow, 128)) {
         uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
@@ -476,7 +505,8 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
                                   E::pack(__uint_as_float(ub[8 * e + 4]) * mul, __uint_as_float(ub[8 * e + 5]) * mul),
                                   E::pack(__uint_as_float(ub[8 * e + 6]) * mul, __uint_as_float(ub[8 * e + 7]) * mul));
       }
-      if (half == 0 && valid && SDPA_ADDR_OK(g.chk, lse_at, 4)) *lse_at = l > 0.f ? m * g.scale + logf(l) : -INFINITY;
+      if (half == 0 && valid && SDPA_ADDR_OK(g.chk, lse_at, 4))
+        *lse_at = l > 0.f ? m * g.scale + (logf(l) - kLn448) : -INFINITY;
       gu += steps;
       ++nt;
     }
