@@ -676,32 +676,17 @@ constexpr int GB_NST = 2;
 constexpr int GB_NBARS = 2 * GB_NST + 3;
 constexpr int GB_SMEM = 1024 + GB_NST * GB_STAGE + GB_NBARS * 8 + 16;
 
-// One output tile of one mode. MODE 0: dQ. MODE 1: dV. MODE 2: dK. `idx`
-// numbers the tiles of that mode; tmB is the mode's B operand (K, dO or Q
-// with 64-row boxes).
+// One output tile of one mode. MODE 0: dQ. MODE 1: dV. MODE 2: dK. head: the
+// q head (dQ) or kv head (dV/dK); t_own: the tile's own 128-row index (a
+// query tile for dQ, a key tile of the chunk for dV/dK); split: its 256-column
+// slice of the head dim. tmB is the mode's B operand (K, dO or Q with 64-row
+// boxes).
 template <int MODE, bool BF16>
-__device__ __forceinline__ void gemm_tile(const CUtensorMap* tmB, const BigBwdParams& p, int idx) {
+__device__ __forceinline__ void gemm_tile(const CUtensorMap* tmB, const BigBwdParams& p, int split, int b, int head,
+                                          int t_own) {
   using E = Elem<BF16>;
   using T = typename E::T;
   const Geom& g = p.g;
-  const int splits = g.d / 256;
-  int split, b, head, t_own;  // head: q head (dQ) or kv head (dV/dK); t_own: own 128-row tile
-  if (MODE == 0) {
-    split = idx % splits;
-    idx /= splits;
-    head = idx % g.hq;
-    idx /= g.hq;
-    b = idx % g.batch;
-    t_own = p.n_q_tiles - 1 - idx / g.batch;
-  } else {
-    const int chunk_tiles = p.chunk_hi - p.chunk_lo;  // the key tiles of this chunk
-    t_own = p.chunk_lo + idx % chunk_tiles;
-    idx /= chunk_tiles;
-    split = idx % splits;
-    idx /= splits;
-    head = idx % g.hkv;
-    b = idx / g.hkv;
-  }
   const SeqInfo si = seq_info(g, b);
   const int r0 = t_own * 128;
   if (r0 >= (MODE == 0 ? si.lq : si.lk)) return;
@@ -920,22 +905,69 @@ __device__ __forceinline__ void gemm_tile(const CUtensorMap* tmB, const BigBwdPa
   }
 }
 
-// Phase 2 of one chunk in one launch: the dV tiles, then the dK tiles (the
-// longer K-loops, over every q head of the group and every query tile that
-// sees the key tile), then the dQ tiles. The three modes only read the
-// chunk's P / dS images and Q, dO, K, so they run side by side and the grid
-// fills the GPU even when a chunk holds few key tiles.
+// Phase 2 of one chunk in one launch. The three modes only read the chunk's
+// P / dS images and Q, dO, K, so they run side by side. Two grid orders:
+//  * by mode (unbounded masks): dV and dK of every key tile of the chunk, then
+//    dQ of every query tile. A dK/dV CTA loops over every query tile of its
+//    group, several times a dQ CTA's key tiles, and these long CTAs start first.
+//  * by (batch, kv head) block (a bounded window): a block holds dV and dK of
+//    the chunk's key tiles, then dQ of its query tiles for the q heads of the
+//    group. The window keeps a block's dS band small, so dQ reads the images
+//    dK has just read while they are still in L2; the CTAs are of similar
+//    length.
 template <bool BF16>
 __global__ void __launch_bounds__(256, 2)
     gemm_kernel(const __grid_constant__ CUtensorMap tmK64, const __grid_constant__ CUtensorMap tmDO64,
-                const __grid_constant__ CUtensorMap tmQ64, const __grid_constant__ BigBwdParams p, int n_kv_ctas) {
-  const int idx = blockIdx.x + p.item_offset;
-  if (idx < n_kv_ctas)
-    gemm_tile<1, BF16>(&tmDO64, p, idx);
-  else if (idx < 2 * n_kv_ctas)
-    gemm_tile<2, BF16>(&tmQ64, p, idx - n_kv_ctas);
-  else
-    gemm_tile<0, BF16>(&tmK64, p, idx - 2 * n_kv_ctas);
+                const __grid_constant__ CUtensorMap tmQ64, const __grid_constant__ BigBwdParams p, int n_q_tiles) {
+  const Geom& g = p.g;
+  const int splits = g.d / 256, group = g.hq / g.hkv;
+  const int n_kv = p.chunk_hi - p.chunk_lo;
+  int idx = blockIdx.x + p.item_offset;
+  if (p.block_major) {
+    const int kv_ctas = 2 * splits * n_kv;
+    const int per_block = kv_ctas + group * splits * n_q_tiles;
+    int r = idx % per_block;
+    idx /= per_block;
+    const int kvh = idx % g.hkv;
+    const int b = idx / g.hkv;
+    if (r < kv_ctas) {  // dV and dK of key tile chunk_lo + r / (2 * splits)
+      const int t = r / (2 * splits);
+      r %= 2 * splits;
+      if (r < splits)
+        gemm_tile<1, BF16>(&tmDO64, p, r, b, kvh, p.chunk_lo + t);
+      else
+        gemm_tile<2, BF16>(&tmQ64, p, r - splits, b, kvh, p.chunk_lo + t);
+    } else {  // dQ of query tile t for the q heads of the group
+      r -= kv_ctas;
+      const int t = r / (group * splits);
+      r %= group * splits;
+      gemm_tile<0, BF16>(&tmK64, p, r % splits, b, kvh * group + r / splits, t);
+    }
+    return;
+  }
+  // by mode: every dV tile (key tile fastest), every dK tile, then every dQ
+  // tile (heaviest query tiles first)
+  const int kv_mode = n_kv * splits * g.hkv * g.batch;
+  if (idx < 2 * kv_mode) {
+    const bool dk = idx >= kv_mode;
+    int x = dk ? idx - kv_mode : idx;
+    const int t = x % n_kv;
+    x /= n_kv;
+    const int split = x % splits;
+    x /= splits;
+    if (dk)
+      gemm_tile<2, BF16>(&tmQ64, p, split, x / g.hkv, x % g.hkv, p.chunk_lo + t);
+    else
+      gemm_tile<1, BF16>(&tmDO64, p, split, x / g.hkv, x % g.hkv, p.chunk_lo + t);
+  } else {
+    int x = idx - 2 * kv_mode;
+    const int split = x % splits;
+    x /= splits;
+    const int head = x % g.hq;
+    x /= g.hq;
+    const int b = x % g.batch;
+    gemm_tile<0, BF16>(&tmK64, p, split, b, head, n_q_tiles - 1 - x / g.batch);
+  }
 }
 
 // ====================================================================== launch
@@ -966,7 +998,6 @@ static int launch_big_t(const BigBwdLaunch& L, int* launches) {
     BigBwdParams p = p0;
     p.chunk_lo = lo;
     p.chunk_hi = std::min(lo + p0.chunk, p0.n_kv_tiles);
-    const long long gkv_c = (long long)(p.chunk_hi - p.chunk_lo) * splits * p.g.hkv * p.g.batch;
     int rc = SDPA_OK;
     if (g1 > 0) {  // phase 1: P and dS tiles of this chunk from S and dP
       rc = launch_in_grids(g1, [&](long long off, long long cnt) {
@@ -978,12 +1009,16 @@ static int launch_big_t(const BigBwdLaunch& L, int* launches) {
       });
       if (rc) return rc;
     }
-    const long long g2 = 2 * gkv_c + (g1 > 0 ? gq : 0);
+    const int nq2 = g1 > 0 ? p.n_q_tiles : 0;  // query tiles whose dQ part this chunk adds
+    p.block_major = p.g.wl >= 0;
+    const long long g2 = ((long long)2 * (p.chunk_hi - p.chunk_lo) + (long long)(p.g.hq / p.g.hkv) * nq2) * splits *
+                         p.g.hkv * p.g.batch;
+    if (g2 > 0x7fffffffLL) return SDPA_ERR_UNSUPPORTED;
     if (g2 > 0) {  // phase 2: dV, dK of the chunk's key tiles, its part of dQ
       rc = launch_in_grids(g2, [&](long long off, long long cnt) {
         BigBwdParams pp = p;
         pp.item_offset = (int)off;
-        gm<<<(unsigned)cnt, 256, GB_SMEM, L.stream>>>(L.tmK64, L.tmDO64, L.tmQ64, pp, (int)gkv_c);
+        gm<<<(unsigned)cnt, 256, GB_SMEM, L.stream>>>(L.tmK64, L.tmDO64, L.tmQ64, pp, nq2);
         ++n;
         return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
       });

@@ -122,6 +122,7 @@ struct BigBwdParams {
   float* dq_acc;           // [nh_q][rows_q][D] fp32 dQ sum over chunks, zeroed by the
                            // preprocess; nullptr when one chunk covers every key tile
   int item_offset;       // added to blockIdx.x (launches split under a CTA cap)
+  int block_major;       // phase-2 grid by (batch, kv head) block (bounded window) or by mode
 };
 
 struct BigBwdLaunch {
