@@ -1,10 +1,11 @@
 // fwd.cu -- fused attention forward for sm_103a.
 //
-// One CTA owns one 128-row query tile of one (batch, q head) and, for
-// head_dim 512, one half of the value columns (the "D-split": both halves
-// recompute S = Q K^T over the full head dim, each accumulates half of O, so
-// O never needs more than 256 TMEM columns). The same kernel serves
-// head_dim 256, 512 and the asymmetric pair Q/K 192, V/O 128.
+// fwd_kernel: a persistent CTA per SM walks work items, each one 128-row
+// query tile of one (batch, q head) and, for head_dim 512, one half of the
+// value columns (the "D-split": both halves recompute S = Q K^T over the full
+// head dim, each accumulates half of O, so O never needs more than 256 TMEM
+// columns). The same kernel serves head_dim 256, 512 and the asymmetric pair
+// Q/K 192, V/O 128.
 //
 // Roles (256 threads):
 //   warp 0      TMA producer: Q once, then K/V tiles through a ring of 32 KB
@@ -41,7 +42,7 @@ struct FwdCfg {
   static constexpr int STAGE_BYTES = 32768;
   static constexpr int Q_BYTES = DQK * 256;  // 128 rows x DQK x 2 bytes
   static_assert(DQK % 64 == 0 && DV % 64 == 0, "head dims are whole 64-column swizzle atoms");
-  static constexpr int NSTAGES = DQK <= 192 ? 5 : (DQK == 256 ? 4 : 3);
+  static constexpr int NSTAGES = DQK <= 192 ? 5 : (DQK == 256 ? 5 : 3);
   static constexpr int KST = (DQK + 127) / 128;            // K stages per tile (128 keys x up to 128 d each)
   // 64-column atoms of K stage kb (two, or one for the last stage of DQK = 192)
   static __device__ __forceinline__ constexpr int k_atoms(int kb) { return DQK / 64 - 2 * kb >= 2 ? 2 : 1; }
@@ -49,10 +50,47 @@ struct FwdCfg {
   static constexpr int VST = BN / VROWS;                   // V stages per tile
   static constexpr int V_ATOM_BYTES = VROWS * 128;         // one 64-column swizzle atom of a V stage
   static constexpr int TMEM_O = 0, TMEM_S = DV;
-  static constexpr int NBARS = 2 * NSTAGES + 7;
+  static constexpr int NBARS = 2 * NSTAGES + 9;
   static constexpr int SMEM_BYTES = 1024 + Q_BYTES + NSTAGES * STAGE_BYTES + NBARS * 8 + 16;
 };
 
+// A work item of the order: a query tile (heaviest, i.e. last, first; GQA
+// heads adjacent) and the value-column split this CTA accumulates.
+struct FwdItem {
+  int split, q0, q_last, t_lo, n, qhead, khead;
+  SeqInfo si;
+  KeyRange kr;
+};
+
+template <int DQK, int DV>
+__device__ __forceinline__ bool fwd_item(const FwdParams& p, int idx, FwdItem& t) {
+  using C = FwdCfg<DQK, DV>;
+  const Geom& g = p.g;
+  t.split = idx % p.dv_splits;
+  idx /= p.dv_splits;
+  const int h = idx % g.hq;
+  idx /= g.hq;
+  const int b = idx % g.batch;
+  idx /= g.batch;
+  t.q0 = (p.n_q_tiles - 1 - idx) * C::BM;
+  t.si = seq_info(g, b);
+  if (t.q0 >= t.si.lq) return false;
+  t.kr = key_range(g, t.si.lq, t.si.lk);
+  t.q_last = min(t.q0 + C::BM - 1, t.si.lq - 1);
+  const int kv_lo = t.kr.lo(t.q0), kv_hi = t.kr.hi(t.q_last);
+  t.t_lo = kv_lo / C::BN;
+  t.n = (kv_hi > kv_lo) ? (kv_hi + C::BN - 1) / C::BN - t.t_lo : 0;
+  t.qhead = t.si.qhead0 + h;
+  t.khead = t.si.khead0 + h / (g.hq / g.hkv);
+  return true;
+}
+
+// Persistent: CTA c takes the items c, c + gridDim.x, ... of the order and
+// every role walks that same sequence. Barrier phases run on across items
+// (S/P by step, O by P V, Q and the item's end by item). The next item's Q
+// is loaded as soon as this item's last S is done (q_free); its first P V,
+// which overwrites O, waits for the epilogue to have read O (o_free), so the
+// next item's first S MMAs run during this item's epilogue.
 template <int DQK, int DV, bool BF16>
 __global__ void __launch_bounds__(256, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -60,28 +98,8 @@ __global__ void __launch_bounds__(256, 1)
   using C = FwdCfg<DQK, DV>;
   using E = Elem<BF16>;
   const Geom& g = p.g;
-
-  // ---- which tile: heaviest (last) query tiles first, GQA heads adjacent
-  int idx = blockIdx.x + p.item_offset;
-  const int split = idx % p.dv_splits;
-  idx /= p.dv_splits;
-  const int h = idx % g.hq;
-  idx /= g.hq;
-  const int b = idx % g.batch;
-  idx /= g.batch;
-  const int qt = p.n_q_tiles - 1 - idx;
-  const SeqInfo si = seq_info(g, b);
-  const int q0 = qt * C::BM;
-  if (q0 >= si.lq) return;
   if (p.guard && *reinterpret_cast<volatile const int*>(p.guard)) return;
-
-  const KeyRange kr = key_range(g, si.lq, si.lk);
-  const int q_last = min(q0 + C::BM - 1, si.lq - 1);
-  const int kv_lo = kr.lo(q0), kv_hi = kr.hi(q_last);
-  const int t_lo = kv_lo / C::BN;
-  const int n_tiles = (kv_hi > kv_lo) ? (kv_hi + C::BN - 1) / C::BN - t_lo : 0;
-  const int qhead = si.qhead0 + h;
-  const int khead = si.khead0 + h / (g.hq / g.hkv);
+  const int total = p.total_tiles;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);  // stays a shared-space pointer
@@ -94,7 +112,9 @@ __global__ void __launch_bounds__(256, 1)
   uint64_t* bar_p = bar_s + 2;  // [2]
   uint64_t* bar_o = bar_p + 2;
   uint64_t* bar_drain = bar_o + 1;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_drain + 1);
+  uint64_t* q_free = bar_drain + 1;  // an item's last S MMA is done: Q may be replaced
+  uint64_t* o_free = q_free + 1;     // the epilogue has read O out of TMEM
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(o_free + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
@@ -111,6 +131,8 @@ __global__ void __launch_bounds__(256, 1)
     mbar_init(&bar_p[1], 128);
     mbar_init(bar_o, 1);
     mbar_init(bar_drain, 1);
+    mbar_init(q_free, 1);
+    mbar_init(o_free, 128);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -125,49 +147,59 @@ __global__ void __launch_bounds__(256, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (elect_one() && n_tiles > 0) {
+    if (elect_one()) {
       prefetch_tmap(&tmQ);
       prefetch_tmap(&tmK);
       prefetch_tmap(&tmV);
-      mbar_arrive_expect_tx(bar_q, C::Q_BYTES);
-      for (int a = 0; a < DQK / 64; ++a) tma_load_3d(&tmQ, bar_q, sQ + a * 16384, a * 64, qhead, si.qrow0 + q0);
-      int c = 0;
+      int c = 0, nq = 0;
       bool ok = true;
-      auto next_slot = [&](int& slot, uint32_t bytes) -> bool {
-        slot = c % C::NSTAGES;
-        const uint32_t ph = (c / C::NSTAGES) & 1;
-        if (!mbar_wait(&empty[slot], ph ^ 1, abort_flag)) return false;
-        mbar_arrive_expect_tx(&full[slot], bytes);
-        return true;
-      };
-      auto load_k = [&](int j) -> bool {
-        const int key0 = si.krow0 + (t_lo + j) * C::BN;
-        for (int kb = 0; kb < C::KST; ++kb, ++c) {
-          int slot;
-          const int atoms = C::k_atoms(kb);
-          if (!next_slot(slot, atoms * 16384)) return false;
-          uint8_t* dst = sStage + slot * C::STAGE_BYTES;
-          tma_load_3d(&tmK, &full[slot], dst, kb * 128, khead, key0);
-          if (atoms == 2) tma_load_3d(&tmK, &full[slot], dst + 16384, kb * 128 + 64, khead, key0);
+      for (int idx = blockIdx.x; idx < total && ok; idx += gridDim.x) {
+        FwdItem t;
+        if (!fwd_item<DQK, DV>(p, idx, t) || t.n == 0) continue;
+        if (nq > 0 && !mbar_wait(q_free, (nq - 1) & 1, abort_flag)) {
+          ok = false;
+          break;
         }
-        return true;
-      };
-      auto load_v = [&](int j) -> bool {
-        for (int vs = 0; vs < C::VST; ++vs, ++c) {
-          int slot;
-          if (!next_slot(slot, C::STAGE_BYTES)) return false;
-          uint8_t* dst = sStage + slot * C::STAGE_BYTES;
-          const int key0 = si.krow0 + (t_lo + j) * C::BN + vs * C::VROWS;
-          for (int a = 0; a < DV / 64; ++a)
-            tma_load_3d(&tmV, &full[slot], dst + a * C::V_ATOM_BYTES, split * DV + a * 64, khead, key0);
+        mbar_arrive_expect_tx(bar_q, C::Q_BYTES);
+        for (int a = 0; a < DQK / 64; ++a)
+          tma_load_3d(&tmQ, bar_q, sQ + a * 16384, a * 64, t.qhead, t.si.qrow0 + t.q0);
+        ++nq;
+        auto next_slot = [&](int& slot, uint32_t bytes) -> bool {
+          slot = c % C::NSTAGES;
+          const uint32_t ph = (c / C::NSTAGES) & 1;
+          if (!mbar_wait(&empty[slot], ph ^ 1, abort_flag)) return false;
+          mbar_arrive_expect_tx(&full[slot], bytes);
+          return true;
+        };
+        auto load_k = [&](int j) -> bool {
+          const int key0 = t.si.krow0 + (t.t_lo + j) * C::BN;
+          for (int kb = 0; kb < C::KST; ++kb, ++c) {
+            int slot;
+            const int atoms = C::k_atoms(kb);
+            if (!next_slot(slot, atoms * 16384)) return false;
+            uint8_t* dst = sStage + slot * C::STAGE_BYTES;
+            tma_load_3d(&tmK, &full[slot], dst, kb * 128, t.khead, key0);
+            if (atoms == 2) tma_load_3d(&tmK, &full[slot], dst + 16384, kb * 128 + 64, t.khead, key0);
+          }
+          return true;
+        };
+        auto load_v = [&](int j) -> bool {
+          for (int vs = 0; vs < C::VST; ++vs, ++c) {
+            int slot;
+            if (!next_slot(slot, C::STAGE_BYTES)) return false;
+            uint8_t* dst = sStage + slot * C::STAGE_BYTES;
+            const int key0 = t.si.krow0 + (t.t_lo + j) * C::BN + vs * C::VROWS;
+            for (int a = 0; a < DV / 64; ++a)
+              tma_load_3d(&tmV, &full[slot], dst + a * C::V_ATOM_BYTES, t.split * DV + a * 64, t.khead, key0);
+          }
+          return true;
+        };
+        for (int j = 0; j < t.n && ok; ++j) {
+          ok = load_k(j);
+          if (ok && j >= 1) ok = load_v(j - 1);
         }
-        return true;
-      };
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        ok = load_k(j);
-        if (ok && j >= 1) ok = load_v(j - 1);
+        if (ok) ok = load_v(t.n - 1);
       }
-      if (ok) ok = load_v(n_tiles - 1);
       if (!ok) {
         *abort_flag = 1;
         record_error(p.err, SDPA_ERR_TIMEOUT);
@@ -176,63 +208,80 @@ __global__ void __launch_bounds__(256, 1)
       // stages (or fewer) are the only ones that can still be in flight.
       const int first = c > C::NSTAGES ? c - C::NSTAGES : 0;
       for (int k = first; k < c; ++k) mbar_wait_drain(&full[k % C::NSTAGES], (k / C::NSTAGES) & 1);
-      mbar_wait_drain(bar_q, 0);
+      if (nq > 0) mbar_wait_drain(bar_q, (nq - 1) & 1);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (elect_one() && n_tiles > 0) {
+    if (elect_one()) {
       constexpr uint32_t IDESC_S = idesc_f16(128, 128, BF16, false, false);
       constexpr uint32_t IDESC_O = idesc_f16(128, DV, BF16, false, true);
-      int c = 0;
-      bool ok = mbar_wait(bar_q, 0, abort_flag);
-      tc_fence_after();
+      int c = 0, nq = 0, gs = 0;  // ring stages, items with keys, steps of earlier items
+      bool ok = true;
       const uint32_t q_base = smem_u32(sQ);
-      auto mma_s = [&](int j) -> bool {
-        const uint32_t d = tmem + C::TMEM_S + (j & 1) * 128;
-        for (int kb = 0; kb < C::KST; ++kb, ++c) {
-          const int slot = c % C::NSTAGES;
-          if (!mbar_wait(&full[slot], (c / C::NSTAGES) & 1, abort_flag)) return false;
-          tc_fence_after();
-          const uint32_t k_base = smem_u32(sStage + slot * C::STAGE_BYTES);
-          const uint32_t qa = q_base + kb * 2 * 16384;
-          const int n_ks = 4 * C::k_atoms(kb);  // 16-column K steps held by this stage
-#pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
-            if (ks >= n_ks) break;
-            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
-            mma_ss(d, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(k_base + off, 16, 1024), IDESC_S,
-                   (kb | ks) != 0);
-          }
-          mma_commit(&empty[slot]);
+      for (int idx = blockIdx.x; idx < total && ok; idx += gridDim.x) {
+        FwdItem t;
+        if (!fwd_item<DQK, DV>(p, idx, t) || t.n == 0) continue;
+        const int n = t.n;
+        if (!mbar_wait(bar_q, nq & 1, abort_flag)) {
+          ok = false;
+          break;
         }
-        mma_commit(&bar_s[j & 1]);
-        return true;
-      };
-      auto mma_o = [&](int j) -> bool {
-        if (!mbar_wait(&bar_p[j & 1], (j >> 1) & 1, abort_flag)) return false;
+        ++nq;
         tc_fence_after();
-        const uint32_t pcol = tmem + C::TMEM_S + (j & 1) * 128;
-        for (int vs = 0; vs < C::VST; ++vs, ++c) {
-          const int slot = c % C::NSTAGES;
-          if (!mbar_wait(&full[slot], (c / C::NSTAGES) & 1, abort_flag)) return false;
-          tc_fence_after();
-          const uint32_t v_base = smem_u32(sStage + slot * C::STAGE_BYTES);
+        auto mma_s = [&](int j) -> bool {
+          const int sj = gs + j;
+          const uint32_t d = tmem + C::TMEM_S + (sj & 1) * 128;
+          for (int kb = 0; kb < C::KST; ++kb, ++c) {
+            const int slot = c % C::NSTAGES;
+            if (!mbar_wait(&full[slot], (c / C::NSTAGES) & 1, abort_flag)) return false;
+            tc_fence_after();
+            const uint32_t k_base = smem_u32(sStage + slot * C::STAGE_BYTES);
+            const uint32_t qa = q_base + kb * 2 * 16384;
+            const int n_ks = 4 * C::k_atoms(kb);  // 16-column K steps held by this stage
 #pragma unroll
-          for (int ks = 0; ks < C::VROWS / 16; ++ks) {
-            const int key_local = vs * C::VROWS + ks * 16;
-            mma_ts(tmem + C::TMEM_O, pcol + key_local / 2, smem_desc_sw128(v_base + ks * 2048, C::V_ATOM_BYTES, 1024),
-                   IDESC_O, (j | vs | ks) != 0);
+            for (int ks = 0; ks < 8; ++ks) {
+              if (ks >= n_ks) break;
+              const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+              mma_ss(d, smem_desc_sw128(qa + off, 16, 1024), smem_desc_sw128(k_base + off, 16, 1024), IDESC_S,
+                     (kb | ks) != 0);
+            }
+            mma_commit(&empty[slot]);
           }
-          mma_commit(&empty[slot]);
+          mma_commit(&bar_s[sj & 1]);
+          if (j == n - 1) mma_commit(q_free);  // the item's last read of Q
+          return true;
+        };
+        auto mma_o = [&](int j) -> bool {
+          const int sj = gs + j;
+          if (j == 0 && nq > 1) {  // O still holds the previous item until its epilogue read it
+            if (!mbar_wait(o_free, (nq - 2) & 1, abort_flag)) return false;
+          }
+          if (!mbar_wait(&bar_p[sj & 1], (sj >> 1) & 1, abort_flag)) return false;
+          tc_fence_after();
+          const uint32_t pcol = tmem + C::TMEM_S + (sj & 1) * 128;
+          for (int vs = 0; vs < C::VST; ++vs, ++c) {
+            const int slot = c % C::NSTAGES;
+            if (!mbar_wait(&full[slot], (c / C::NSTAGES) & 1, abort_flag)) return false;
+            tc_fence_after();
+            const uint32_t v_base = smem_u32(sStage + slot * C::STAGE_BYTES);
+#pragma unroll
+            for (int ks = 0; ks < C::VROWS / 16; ++ks) {
+              const int key_local = vs * C::VROWS + ks * 16;
+              mma_ts(tmem + C::TMEM_O, pcol + key_local / 2,
+                     smem_desc_sw128(v_base + ks * 2048, C::V_ATOM_BYTES, 1024), IDESC_O, (j | vs | ks) != 0);
+            }
+            mma_commit(&empty[slot]);
+          }
+          mma_commit(bar_o);
+          return true;
+        };
+        for (int j = 0; j < n && ok; ++j) {
+          ok = mma_s(j);
+          if (ok && j >= 1) ok = mma_o(j - 1);
         }
-        mma_commit(bar_o);
-        return true;
-      };
-      for (int j = 0; j < n_tiles && ok; ++j) {
-        ok = mma_s(j);
-        if (ok && j >= 1) ok = mma_o(j - 1);
+        if (ok) ok = mma_o(n - 1);
+        gs += n;
       }
-      if (ok) ok = mma_o(n_tiles - 1);
       if (!ok) {
         *abort_flag = 1;
         record_error(p.err, SDPA_ERR_TIMEOUT);
@@ -245,110 +294,116 @@ __global__ void __launch_bounds__(256, 1)
     // ------------------------------------------------------------ softmax
     const int wq = warp - 4;
     const int r = wq * 32 + lane;
-    const int i = q0 + r;
     const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
     const float sl2 = g.scale_log2;
-    const int lo_i = kr.lo(i), hi_i = kr.hi(i);
-    const int lo_last = kr.lo(q_last), hi_first = kr.hi(q0);
-    float m_used = -INFINITY, l = 0.f;
+    using T = typename E::T;
+    int gs = 0;  // steps (= P V MMAs) of earlier items
     bool ok = true;
-    for (int j = 0; j < n_tiles; ++j) {
-      if (!__all_sync(0xffffffffu, mbar_wait(&bar_s[j & 1], (j >> 1) & 1, abort_flag))) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const uint32_t scol = lane_base + C::TMEM_S + (j & 1) * 128;
-      float s[128];
-      {
-        uint32_t u0[32], u1[32], u2[32], u3[32];
-        tmem_ld32(scol, u0);
-        tmem_ld32(scol + 32, u1);
-        tmem_ld32(scol + 64, u2);
-        tmem_ld32(scol + 96, u3);
-        tmem_wait_ld();
-        reg_fence(u0);
-        reg_fence(u1);
-        reg_fence(u2);
-        reg_fence(u3);
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          s[c] = __uint_as_float(u0[c]);
-          s[32 + c] = __uint_as_float(u1[c]);
-          s[64 + c] = __uint_as_float(u2[c]);
-          s[96 + c] = __uint_as_float(u3[c]);
-        }
-      }
-      const int kb = (t_lo + j) * C::BN;
-      if (!(lo_last <= kb && hi_first >= kb + C::BN)) {  // edge tile (uniform branch)
-#pragma unroll
-        for (int c = 0; c < 128; ++c) s[c] = in_range(kb + c, lo_i, hi_i) ? s[c] : -INFINITY;
-      }
-      float mt = s[0];
-#pragma unroll
-      for (int c = 1; c < 128; ++c) mt = fmaxf(mt, s[c]);
-      const float m_new = fmaxf(m_used, mt);
-      bool need = false;
-      float f = 1.f;
-      if (m_used == -INFINITY) {
-        m_used = m_new;  // nothing accumulated yet for this row
-      } else if ((m_new - m_used) * sl2 > 8.f) {
-        need = true;
-        f = ex2((m_used - m_new) * sl2);
-        m_used = m_new;
-      }
-      const float mb = (m_used == -INFINITY) ? 0.f : m_used * sl2;
-      float rs = 0.f;
-#pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t pk[32];
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float p0 = ex2(fmaf(s[half * 64 + 2 * c], sl2, -mb));
-          const float p1 = ex2(fmaf(s[half * 64 + 2 * c + 1], sl2, -mb));
-          rs += p0 + p1;
-          pk[c] = E::pack(p0, p1);
-        }
-        tmem_st32(scol + half * 32, pk);
-      }
-      l = l * f + rs;
-      if (j >= 1) {
-        // PV_{j-1} must be complete before O is touched (and before P_j is
-        // released, which keeps this wait in step with every completion).
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_o, (j - 1) & 1, abort_flag))) {
+    for (int idx = blockIdx.x; idx < total && ok; idx += gridDim.x) {
+      FwdItem t;
+      if (!fwd_item<DQK, DV>(p, idx, t)) continue;
+      const int n_tiles = t.n;
+      const int i = t.q0 + r;
+      const int lo_i = t.kr.lo(i), hi_i = t.kr.hi(i);
+      const int lo_last = t.kr.lo(t.q_last), hi_first = t.kr.hi(t.q0);
+      float m_used = -INFINITY, l = 0.f;
+      for (int j = 0; j < n_tiles; ++j) {
+        const int sj = gs + j;
+        if (!__all_sync(0xffffffffu, mbar_wait(&bar_s[sj & 1], (sj >> 1) & 1, abort_flag))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        if (__any_sync(0xffffffffu, need)) {
-#pragma unroll 1
-          for (int c = 0; c < DV / 32; ++c) {
-            uint32_t u[32];
-            tmem_ld32(lane_base + C::TMEM_O + c * 32, u);
-            tmem_wait_ld();
-            reg_fence(u);
+        const uint32_t scol = lane_base + C::TMEM_S + (sj & 1) * 128;
+        float s[128];
+        {
+          uint32_t u0[32], u1[32], u2[32], u3[32];
+          tmem_ld32(scol, u0);
+          tmem_ld32(scol + 32, u1);
+          tmem_ld32(scol + 64, u2);
+          tmem_ld32(scol + 96, u3);
+          tmem_wait_ld();
+          reg_fence(u0);
+          reg_fence(u1);
+          reg_fence(u2);
+          reg_fence(u3);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * f);
-            tmem_st32(lane_base + C::TMEM_O + c * 32, u);
+          for (int c = 0; c < 32; ++c) {
+            s[c] = __uint_as_float(u0[c]);
+            s[32 + c] = __uint_as_float(u1[c]);
+            s[64 + c] = __uint_as_float(u2[c]);
+            s[96 + c] = __uint_as_float(u3[c]);
           }
         }
+        const int kb = (t.t_lo + j) * C::BN;
+        if (!(lo_last <= kb && hi_first >= kb + C::BN)) {  // edge tile (uniform branch)
+#pragma unroll
+          for (int c = 0; c < 128; ++c) s[c] = in_range(kb + c, lo_i, hi_i) ? s[c] : -INFINITY;
+        }
+        float mt = s[0];
+#pragma unroll
+        for (int c = 1; c < 128; ++c) mt = fmaxf(mt, s[c]);
+        const float m_new = fmaxf(m_used, mt);
+        bool need = false;
+        float f = 1.f;
+        if (m_used == -INFINITY) {
+          m_used = m_new;  // nothing accumulated yet for this row
+        } else if ((m_new - m_used) * sl2 > 8.f) {
+          need = true;
+          f = ex2((m_used - m_new) * sl2);
+          m_used = m_new;
+        }
+        const float mb = (m_used == -INFINITY) ? 0.f : m_used * sl2;
+        float rs = 0.f;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t pk[32];
+#pragma unroll
+          for (int c = 0; c < 32; ++c) {
+            const float p0 = ex2(fmaf(s[half * 64 + 2 * c], sl2, -mb));
+            const float p1 = ex2(fmaf(s[half * 64 + 2 * c + 1], sl2, -mb));
+            rs += p0 + p1;
+            pk[c] = E::pack(p0, p1);
+          }
+          tmem_st32(scol + half * 32, pk);
+        }
+        l = l * f + rs;
+        if (j >= 1) {
+          // PV_{j-1} must be complete before O is touched (and before P_j is
+          // released, which keeps this wait in step with every completion).
+          if (!__all_sync(0xffffffffu, mbar_wait(bar_o, (sj - 1) & 1, abort_flag))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          if (__any_sync(0xffffffffu, need)) {
+#pragma unroll 1
+            for (int c = 0; c < DV / 32; ++c) {
+              uint32_t u[32];
+              tmem_ld32(lane_base + C::TMEM_O + c * 32, u);
+              tmem_wait_ld();
+              reg_fence(u);
+#pragma unroll
+              for (int e = 0; e < 32; ++e) u[e] = __float_as_uint(__uint_as_float(u[e]) * f);
+              tmem_st32(lane_base + C::TMEM_O + c * 32, u);
+            }
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive(&bar_p[sj & 1]);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bar_p[j & 1]);
-    }
-    if (ok && n_tiles > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(bar_o, (n_tiles - 1) & 1, abort_flag));
-      tc_fence_after();
-    }
-    if (!ok) {
-      *abort_flag = 1;
-      record_error(p.err, SDPA_ERR_TIMEOUT);
-    } else {
-      const bool valid = i < si.lq;
+      if (!ok) break;
+      if (n_tiles > 0) {
+        if (!__all_sync(0xffffffffu, mbar_wait(bar_o, (gs + n_tiles - 1) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+      }
+      const bool valid = i < t.si.lq;
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      using T = typename E::T;
-      T* orow = reinterpret_cast<T*>(p.o) + ((int64_t)(si.qrow0 + i) * g.nh_q + qhead) * g.dv + split * DV;
+      T* orow = reinterpret_cast<T*>(p.o) + ((int64_t)(t.si.qrow0 + i) * g.nh_q + t.qhead) * g.dv + t.split * DV;
 #pragma unroll 1
       for (int c = 0; c < DV / 32; ++c) {
         uint32_t packed[16];
@@ -357,6 +412,10 @@ __global__ void __launch_bounds__(256, 1)
           tmem_ld32(lane_base + C::TMEM_O + c * 32, u);
           tmem_wait_ld();
           reg_fence(u);
+          if (c == DV / 32 - 1) {  // every column of O is read: the next item's P V may overwrite it
+            tc_fence_before();
+            mbar_arrive(o_free);
+          }
 #pragma unroll
           for (int e = 0; e < 16; ++e)
             packed[e] = E::pack(__uint_as_float(u[2 * e]) * inv, __uint_as_float(u[2 * e + 1]) * inv);
@@ -371,9 +430,14 @@ __global__ void __launch_bounds__(256, 1)
             dst[e] = make_uint4(packed[4 * e], packed[4 * e + 1], packed[4 * e + 2], packed[4 * e + 3]);
         }
       }
-      float* lse_at = p.lse + (int64_t)(si.qrow0 + i) * g.nh_q + qhead;
-      if (valid && split == 0 && SDPA_ADDR_OK(g.chk, lse_at, 4))
+      float* lse_at = p.lse + (int64_t)(t.si.qrow0 + i) * g.nh_q + t.qhead;
+      if (valid && t.split == 0 && SDPA_ADDR_OK(g.chk, lse_at, 4))
         *lse_at = l > 0.f ? m_used * g.scale + logf(l) : -INFINITY;
+      gs += n_tiles;
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      record_error(p.err, SDPA_ERR_TIMEOUT);
     }
   }
 
@@ -926,15 +990,18 @@ static int launch_fwd_t(const FwdLaunch& L) {
   using C = FwdCfg<DQK, DV>;
   auto kern = fwd_kernel<DQK, DV, BF16>;
   if (const int rc = set_kernel_smem(reinterpret_cast<const void*>(kern), C::SMEM_BYTES, -1)) return rc;
-  const long long grid = (long long)L.p.n_q_tiles * L.p.g.hq * L.p.g.batch * L.p.dv_splits;
-  if (grid <= 0) return SDPA_OK;
-  if (grid > 0x7fffffffLL) return SDPA_ERR_UNSUPPORTED;
-  return launch_in_grids(grid, [&](long long off, long long n) {
-    FwdParams p = L.p;
-    p.item_offset = (int)off;
-    kern<<<(unsigned)n, 256, C::SMEM_BYTES, L.stream>>>(L.tmQ, L.tmK, L.tmV, p);
-    return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
-  });
+  const long long items = (long long)L.p.n_q_tiles * L.p.g.hq * L.p.g.batch * L.p.dv_splits;
+  if (items <= 0) return SDPA_OK;
+  if (items > 0x7fffffffLL - 4096) return SDPA_ERR_UNSUPPORTED;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return SDPA_ERR_CUDA;
+  FwdParams p = L.p;
+  p.total_tiles = (int)items;
+  long long grid = std::min<long long>(items, sms);
+  if (debug_max_ctas() > 0) grid = std::min<long long>(grid, debug_max_ctas());  // the CTAs stride over every item
+  kern<<<(unsigned)grid, 256, C::SMEM_BYTES, L.stream>>>(L.tmQ, L.tmK, L.tmV, p);
+  return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }
 
 int launch_fwd(const FwdLaunch& L, int head_dim, int head_dim_v, bool bf16) {
