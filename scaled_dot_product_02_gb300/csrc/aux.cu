@@ -142,24 +142,34 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const PrepParams p) {
   const long long items = (long long)g.rows_q * g.nh_q;
   const long long warp_id = ((long long)blockIdx.x * blockDim.x + threadIdx.x) / 32;
   const long long n_warps = (long long)gridDim.x * blockDim.x / 32;
-  // warp-uniform trip count, so the shuffles below always see all 32 lanes
-  for (long long base = warp_id * PER_WARP; base < items; base += n_warps * PER_WARP) {
-    const long long it = base + lane / G;
-    const bool live = it < items;
-    float acc = 0.f;
-    if (live) {
-      const uint4* o4 = reinterpret_cast<const uint4*>(p.o) + it * VPR;
-      const uint4* d4 = reinterpret_cast<const uint4*>(p.dout) + it * VPR;
-      uint4 a[PER], c[PER];
+  // Below head_dim 512, two items per lane group and step (U), their loads
+  // issued together, so each thread keeps 4 * PER 16-byte loads in flight (at
+  // 512 the doubled registers cost more occupancy than they gain). Warp-
+  // uniform trip count, so the shuffles below always see all 32 lanes.
+  constexpr int U = D < 512 ? 2 : 1;
+  for (long long base = warp_id * PER_WARP * U; base < items; base += n_warps * PER_WARP * U) {
+    uint4 a[U][PER], c[U][PER];
+    long long its[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      its[u] = base + u * PER_WARP + lane / G;
+      const uint4* o4 = reinterpret_cast<const uint4*>(p.o) + its[u] * VPR;
+      const uint4* d4 = reinterpret_cast<const uint4*>(p.dout) + its[u] * VPR;
       const uint4 z = make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
       for (int v = 0; v < PER; ++v) {
-        a[v] = SDPA_ADDR_OK(g.chk, o4 + sub + v * G, 16) ? o4[sub + v * G] : z;
-        c[v] = SDPA_ADDR_OK(g.chk, d4 + sub + v * G, 16) ? d4[sub + v * G] : z;
+        const bool live = its[u] < items;
+        a[u][v] = live && SDPA_ADDR_OK(g.chk, o4 + sub + v * G, 16) ? o4[sub + v * G] : z;
+        c[u][v] = live && SDPA_ADDR_OK(g.chk, d4 + sub + v * G, 16) ? d4[sub + v * G] : z;
       }
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      float acc = 0.f;
 #pragma unroll
       for (int v = 0; v < PER; ++v) {
-        const uint32_t au[4] = {a[v].x, a[v].y, a[v].z, a[v].w}, cu[4] = {c[v].x, c[v].y, c[v].z, c[v].w};
+        const uint32_t au[4] = {a[u][v].x, a[u][v].y, a[u][v].z, a[u][v].w};
+        const uint32_t cu[4] = {c[u][v].x, c[u][v].y, c[u][v].z, c[u][v].w};
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float2 fa = E::unpack(au[e]), fc = E::unpack(cu[e]);
@@ -167,15 +177,16 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const PrepParams p) {
           acc = fmaf(fa.y, fc.y, acc);
         }
       }
-    }
 #pragma unroll
-    for (int sh = G / 2; sh > 0; sh /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, sh, G);
-    if (live && sub == 0) {
-      const int row = (int)(it / g.nh_q), hg = (int)(it - (long long)row * g.nh_q);
-      const float l = SDPA_ADDR_OK(g.chk, p.lse + it, 4) ? p.lse[it] : -INFINITY;
-      const long long st = (long long)hg * p.stat_rows + stat_row(g, row);
-      if (SDPA_ADDR_OK(g.chk, p.delta + st, 4)) p.delta[st] = acc;
-      if (SDPA_ADDR_OK(g.chk, p.lse2 + st, 4)) p.lse2[st] = (l == -INFINITY) ? -INFINITY : -l * 1.4426950408889634f;
+      for (int sh = G / 2; sh > 0; sh /= 2) acc += __shfl_xor_sync(0xffffffffu, acc, sh, G);
+      const long long it = its[u];
+      if (it < items && sub == 0) {
+        const int row = (int)(it / g.nh_q), hg = (int)(it - (long long)row * g.nh_q);
+        const float l = SDPA_ADDR_OK(g.chk, p.lse + it, 4) ? p.lse[it] : -INFINITY;
+        const long long st = (long long)hg * p.stat_rows + stat_row(g, row);
+        if (SDPA_ADDR_OK(g.chk, p.delta + st, 4)) p.delta[st] = acc;
+        if (SDPA_ADDR_OK(g.chk, p.lse2 + st, 4)) p.lse2[st] = (l == -INFINITY) ? -INFINITY : -l * 1.4426950408889634f;
+      }
     }
   }
   const long long tid = (long long)blockIdx.x * blockDim.x + threadIdx.x;
@@ -198,8 +209,14 @@ __global__ void __launch_bounds__(256) preprocess_kernel(const PrepParams p) {
   // zero the dQ accumulator
   const long long n4 = p.dq_acc ? (long long)g.nh_q * g.rows_q * g.d / 4 : 0;
   float4* acc4 = reinterpret_cast<float4*>(p.dq_acc);
-  for (long long it = tid; it < n4; it += nthreads)
-    if (SDPA_ADDR_OK(g.chk, acc4 + it, 16)) acc4[it] = make_float4(0.f, 0.f, 0.f, 0.f);
+  constexpr int UZ = D < 512 ? 4 : 1;  // stores per thread and step (chosen by measurement, as U)
+  for (long long it = tid; it < n4; it += UZ * nthreads) {
+#pragma unroll
+    for (int u = 0; u < UZ; ++u) {
+      const long long x = it + u * nthreads;
+      if (x < n4 && SDPA_ADDR_OK(g.chk, acc4 + x, 16)) acc4[x] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
 }
 
 // SMs of the current device (queried per call: a process may drive several GPUs).
