@@ -705,6 +705,7 @@ int sdpa_fwd_fp8(const sdpa_problem* p, const void* q8, const void* k8, const vo
   L.p.g.scale_log2 = L.p.g.scale * 1.4426950408889634f;
   L.p.v = static_cast<const uint8_t*>(v8);
   L.p.vt = ws + 256;
+  L.p.tile_counter = reinterpret_cast<int*>(ws + 128);
   L.p.vt_rows = (int)fp8_vt_rows(p);
   L.p.o = o;
   L.p.lse = lse;

@@ -51,12 +51,17 @@ namespace {
 
 constexpr int F8_BM = 128, F8_BN = 128, F8_D = 128;
 constexpr int F8_TILE = 16384;  // 128 rows x 128 one-byte columns
-constexpr int F8_NST = 8;
-constexpr int F8_NBARS = 2 * F8_NST + 15;
-constexpr int F8_XCH = 2 * 2 * 2 * F8_BM * 4;  // [tile parity][max, sum][half][row] partials of the two warpgroups
-constexpr int F8_SMEM = 1024 + F8_TILE + F8_NST * F8_TILE + F8_XCH + F8_NBARS * 8 + 16;
+// Two query-tile pipelines per CTA (as the head_dim 128 bf16 forward): each
+// with its Q tile, a ring of F8_NST K / Vt tiles, and in TMEM its O and one S
+// buffer (P8 is written back into the S buffer for the P8 V MMA).
+constexpr int F8_NST = 4;
+constexpr int F8_PIPE_BYTES = F8_TILE + F8_NST * F8_TILE;  // per pipeline, 1024-aligned
+constexpr int F8_PIPE_BARS = 2 * F8_NST + 12;             // mbarriers + queue per pipeline (8 bytes each)
+constexpr int F8_SMEM = 1024 + 2 * F8_PIPE_BYTES + 2 * F8_PIPE_BARS * 8 + 32;
 constexpr int F8_THREADS = 384;
-constexpr int F8_TM_O = 0, F8_TM_S = 128, F8_TM_P = 384;
+constexpr int F8_REGS_SOFTMAX = 192, F8_REGS_OTHER = 120;
+static_assert(2 * F8_REGS_SOFTMAX + F8_REGS_OTHER <= 3 * 168, "register split");
+constexpr uint32_t F8_TM_O = 0, F8_TM_S = 128, F8_TM_PIPE = 256;
 constexpr float kLog2_448 = 8.807354922057604f;  // log2(448)
 constexpr float kLn448 = 6.104793232414985f;     // ln(448)
 
@@ -172,14 +177,53 @@ __device__ __forceinline__ bool fp8_tile(const Fp8Params& p, int idx, Fp8Tile& t
   return true;
 }
 
-// Persistent: CTA c takes the tiles c, c + gridDim.x, ... of the order, and
-// every role walks that same sequence, so no tile is handed between them.
-// Barrier phases run on across tiles (the steps of all tiles so far, and the
-// tiles with keys so far). Q has one buffer: the producer loads the next
-// tile's Q as soon as this tile's last S MMA is done (q_free), while its
-// P8 V MMAs still run. O is overwritten by a tile's first P8 V only after the
-// epilogue of the tile before has read it out of TMEM (o_free), and that
-// epilogue's global stores overlap the next tile's first S MMAs.
+// Shared-memory objects of one pipeline.
+struct Pipe8 {
+  uint8_t* sQ;
+  uint8_t* sStage;
+  uint64_t* full;         // [F8_NST]
+  uint64_t* empty;        // [F8_NST]
+  uint64_t* bar_q;        // Q of a tile landed
+  uint64_t* bar_s;        // S of a step ready
+  uint64_t* bar_p;        // the softmax is done with a step (pass 2: P8 written)
+  uint64_t* bar_o;        // a tile's last P8 V done
+  uint64_t* q_free;       // a tile's last S done: Q may be replaced
+  uint64_t* o_free;       // the epilogue has read O
+  uint64_t* sched_full;   // [2] a tile published
+  uint64_t* sched_empty;  // [2] its entry read by the MMA issuer and the softmax warps
+  int* sched;             // [2] ticket, or -1 when the work is out
+};
+
+__device__ __forceinline__ Pipe8 pipe8_at(uint8_t* smem, int x) {
+  Pipe8 P;
+  P.sQ = smem + x * F8_PIPE_BYTES;
+  P.sStage = P.sQ + F8_TILE;
+  uint64_t* b = reinterpret_cast<uint64_t*>(smem + 2 * F8_PIPE_BYTES) + x * F8_PIPE_BARS;
+  P.full = b;
+  P.empty = b + F8_NST;
+  P.bar_q = b + 2 * F8_NST;
+  P.bar_s = P.bar_q + 1;
+  P.bar_p = P.bar_q + 2;
+  P.bar_o = P.bar_q + 3;
+  P.q_free = P.bar_q + 4;
+  P.o_free = P.bar_q + 5;
+  P.sched_full = P.bar_q + 6;
+  P.sched_empty = P.bar_q + 8;
+  P.sched = reinterpret_cast<int*>(P.bar_q + 10);
+  return P;
+}
+
+// Persistent, one CTA per SM with two query-tile pipelines. Each pipeline
+// takes query tiles (heaviest first) from an atomic ticket counter; a tile
+// runs 2n steps (pass 1 over its n key tiles: S and the row max; pass 2: S
+// again, P8 = E4M3(448 P~), O += P8 V), each step S -> softmax -> (P8 V) in
+// turn through the pipeline's single S buffer. The single MMA issuer serves
+// the two pipelines strictly in turn, so one pipeline's softmax runs while
+// the tensor pipe works on the other's MMAs.
+// Roles: warps 0-3 / 4-7 softmax + epilogue of pipeline 0 / 1 (one thread per
+// query row, all 128 keys of a step), warps 8 / 9 TMA producer and scheduler
+// of pipeline 0 / 1, warp 10 TMEM allocator + MMA issuer, warp 11 only
+// completes the third warpgroup. Every barrier phase counts across tiles.
 template <bool BF16>
 __global__ void __launch_bounds__(F8_THREADS, 1)
     fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -187,52 +231,37 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
   using E = Elem<BF16>;
   const Geom& g = p.g;
   if (p.guard && *reinterpret_cast<volatile const int*>(p.guard)) return;
-  const int total = p.total_tiles;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint8_t* sQ = smem;
-  uint8_t* sStage = smem + F8_TILE;
-  float* xch = reinterpret_cast<float*>(sStage + F8_NST * F8_TILE);  // [tile parity][max, sum][half][row]
-  uint64_t* full = reinterpret_cast<uint64_t*>(sStage + F8_NST * F8_TILE + F8_XCH);
-  uint64_t* empty = full + F8_NST;
-  uint64_t* bar_q = empty + F8_NST;
-  uint64_t* bar_s = bar_q + 1;   // [2] S of a step ready (by S buffer)
-  uint64_t* bar_sf = bar_s + 2;  // [2] the softmax has loaded a step's S: its buffer is free
-  uint64_t* bar_pr = bar_sf + 2; // [2] P8 of a pass-2 step written (by P8 buffer)
-  uint64_t* bar_pf = bar_pr + 2; // [2] the P8 V MMA has read a P8 buffer
-  uint64_t* bar_o = bar_pf + 2;  // a tile's last P8 V (and so every MMA of it) complete
-  uint64_t* bar_drain = bar_o + 1;
-  uint64_t* bar_x = bar_drain + 1;  // [2] the max / sum partials of both warpgroups are written
-  uint64_t* q_free = bar_x + 2;     // a tile's last S MMA is done: Q may be replaced
-  uint64_t* o_free = q_free + 1;    // the epilogue has read O out of TMEM
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(o_free + 1);
+  uint64_t* bar_drain = reinterpret_cast<uint64_t*>(smem + 2 * F8_PIPE_BYTES) + 2 * F8_PIPE_BARS;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < F8_NST; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
+    for (int x = 0; x < 2; ++x) {
+      const Pipe8 P = pipe8_at(smem, x);
+      for (int i = 0; i < F8_NST; ++i) {
+        mbar_init(&P.full[i], 1);
+        mbar_init(&P.empty[i], 1);
+      }
+      mbar_init(P.bar_q, 1);
+      mbar_init(P.bar_s, 1);
+      mbar_init(P.bar_p, 128);
+      mbar_init(P.bar_o, 1);
+      mbar_init(P.q_free, 1);
+      mbar_init(P.o_free, 128);
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&P.sched_full[i], 1);
+        mbar_init(&P.sched_empty[i], 129);
+      }
     }
-    mbar_init(bar_q, 1);
-    mbar_init(&bar_s[0], 1);
-    mbar_init(&bar_s[1], 1);
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(&bar_sf[b], 256);
-      mbar_init(&bar_pr[b], 256);
-      mbar_init(&bar_pf[b], 1);
-    }
-    mbar_init(bar_o, 1);
     mbar_init(bar_drain, 1);
-    mbar_init(&bar_x[0], 256);
-    mbar_init(&bar_x[1], 256);
-    mbar_init(q_free, 1);
-    mbar_init(o_free, 256);
     *abort_flag = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == 10) {
     tmem_alloc(tmem_holder, 512);
     tmem_relinquish();
   }
@@ -241,215 +270,272 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_holder;
 
-  // Ring order (the MMA warp consumes in the same order), per tile: K of steps
-  // 0 and 1; then for every step u, K of step u + 2, and Vt of its key tile
-  // if u is a pass-2 step. Step u covers key tile (u < n ? u : u - n).
-  if (warp == 0) {
-    if (elect_one()) {
-      prefetch_tmap(&tmQ);
-      prefetch_tmap(&tmK);
-      prefetch_tmap(&tmVt);
-      int c = 0, nq = 0;
-      bool ok = true;
-      for (int idx = blockIdx.x; idx < total && ok; idx += gridDim.x) {
-        Fp8Tile t;
-        if (!fp8_tile(p, idx, t) || t.n == 0) continue;
-        const int n = t.n, steps = 2 * n;
-        if (nq > 0 && !mbar_wait(q_free, (nq - 1) & 1, abort_flag)) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(bar_q, F8_TILE);
-        tma_load_3d(&tmQ, bar_q, sQ, 0, t.qhead, t.si.qrow0 + t.q0);
-        ++nq;
-        auto load = [&](bool v_tile, int tile) -> bool {
+  if (warp >= 8) {
+    regs_dec<F8_REGS_OTHER>();
+    if (warp == 8 || warp == 9) {
+      // ---------------------------------------------------------- scheduler + producer of pipeline warp - 8
+      if (elect_one()) {
+        const Pipe8 P = pipe8_at(smem, warp - 8);
+        prefetch_tmap(&tmQ);
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmVt);
+        int c = 0, nq = 0, w = 0;
+        bool ok = true;
+        // the next ticket (a counter the address check rejects hands out none)
+        auto take = [&]() {
+          return SDPA_ADDR_OK(g.chk, p.tile_counter, 4) ? atomicAdd(p.tile_counter, 1) : p.total_tiles;
+        };
+        auto load = [&](const CUtensorMap* m, int c0, int c1, int c2) -> bool {
           const int slot = c % F8_NST;
-          if (!mbar_wait(&empty[slot], ((c / F8_NST) & 1) ^ 1, abort_flag)) return false;
-          mbar_arrive_expect_tx(&full[slot], F8_TILE);
-          uint8_t* dst = sStage + slot * F8_TILE;
-          if (v_tile)
-            tma_load_3d(&tmVt, &full[slot], dst, t.vrow0 + (t.t_lo + tile) * F8_BN, 0, t.khead);
-          else
-            tma_load_3d(&tmK, &full[slot], dst, 0, t.khead, t.si.krow0 + (t.t_lo + tile) * F8_BN);
+          if (!mbar_wait(&P.empty[slot], ((c / F8_NST) & 1) ^ 1, abort_flag)) return false;
+          mbar_arrive_expect_tx(&P.full[slot], F8_TILE);
+          tma_load_3d(m, &P.full[slot], P.sStage + slot * F8_TILE, c0, c1, c2);
           ++c;
           return true;
         };
-        for (int u = 0; u < 2 && u < steps && ok; ++u) ok = load(false, u < n ? u : u - n);
-        for (int u = 0; u < steps && ok; ++u) {
-          if (u + 2 < steps) ok = load(false, u + 2 < n ? u + 2 : u + 2 - n);
-          if (ok && u >= n) ok = load(true, u - n);
+        int ticket = take();
+        while (true) {
+          Fp8Tile t;
+          while (ticket < p.total_tiles && !fp8_tile(p, ticket, t)) ticket = take();
+          const int item = ticket < p.total_tiles ? ticket : -1;
+          const int e = w & 1;
+          if (!mbar_wait(&P.sched_empty[e], ((w >> 1) & 1) ^ 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          P.sched[e] = item;
+          mbar_arrive(&P.sched_full[e]);
+          ++w;
+          if (item < 0) break;
+          ticket = take();  // in flight while this tile's loads are issued
+          if (t.n == 0) continue;
+          if (nq > 0 && !mbar_wait(P.q_free, (nq - 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(P.bar_q, F8_TILE);
+          tma_load_3d(&tmQ, P.bar_q, P.sQ, 0, t.qhead, t.si.qrow0 + t.q0);
+          ++nq;
+          // in the order the MMA issuer consumes: per step, K of its key tile
+          // and, in pass 2, then Vt of it
+          for (int u = 0; u < 2 * t.n && ok; ++u) {
+            const int j = u < t.n ? u : u - t.n;
+            ok = load(&tmK, 0, t.khead, t.si.krow0 + (t.t_lo + j) * F8_BN);
+            if (ok && u >= t.n) ok = load(&tmVt, t.vrow0 + (t.t_lo + j) * F8_BN, 0, t.khead);
+          }
+          if (!ok) break;
         }
-      }
-      if (!ok) {
-        *abort_flag = 1;
-        record_error(p.err, SDPA_ERR_TIMEOUT);
-      }
-      const int first = c > F8_NST ? c - F8_NST : 0;
-      for (int k = first; k < c; ++k) mbar_wait_drain(&full[k % F8_NST], (k / F8_NST) & 1);
-      if (nq > 0) mbar_wait_drain(bar_q, (nq - 1) & 1);
-    }
-  } else if (warp == 1) {
-    if (elect_one()) {
-      constexpr uint32_t IDESC = idesc_e4m3(128, 128);
-      const uint32_t q_base = smem_u32(sQ);
-      int c = 0, nq = 0, gu = 0, gp = 0, no = 0;  // ring loads, Q loads, steps, pass-2 steps, tiles so far
-      bool ok = true;
-      for (int idx = blockIdx.x; idx < total && ok; idx += gridDim.x) {
-        Fp8Tile t;
-        if (!fp8_tile(p, idx, t) || t.n == 0) continue;
-        const int n = t.n, steps = 2 * n;
-        if (!mbar_wait(bar_q, nq & 1, abort_flag)) {
-          ok = false;
-          break;
+        if (!ok) {
+          *abort_flag = 1;
+          record_error(p.err, SDPA_ERR_TIMEOUT);
         }
-        ++nq;
-        tc_fence_after();
-        // S of step u into S buffer (gu + u) & 1, once the softmax has loaded
-        // that buffer's previous scores (step gu + u - 2)
-        auto mma_s = [&](int u) -> bool {
-          const int su = gu + u;
-          if (su >= 2 && !mbar_wait(&bar_sf[su & 1], ((su - 2) >> 1) & 1, abort_flag)) return false;
-          const int slot = c % F8_NST;
-          if (!mbar_wait(&full[slot], (c / F8_NST) & 1, abort_flag)) return false;
+        const int first = c > F8_NST ? c - F8_NST : 0;
+        for (int k = first; k < c; ++k) mbar_wait_drain(&P.full[k % F8_NST], (k / F8_NST) & 1);
+        if (nq > 0) mbar_wait_drain(P.bar_q, (nq - 1) & 1);
+      }
+    } else if (warp == 10) {
+      // ---------------------------------------------------------- MMA issuer for both pipelines
+      if (elect_one()) {
+        constexpr uint32_t IDESC = idesc_e4m3(128, 128);
+        struct State {
+          int w, c, nq, steps, no, n, u;
+          bool done;
+        };
+        State st[2];
+        for (int x = 0; x < 2; ++x) st[x] = State{0, 0, 0, 0, 0, 0, 0, false};
+        bool ok = true;
+        // next tile with keys of pipeline x (false: its work is out, or a wait failed)
+        auto next_item = [&](int x) -> bool {
+          const Pipe8 P = pipe8_at(smem, x);
+          State& m = st[x];
+          while (true) {
+            const int e = m.w & 1;
+            if (!mbar_wait(&P.sched_full[e], (m.w >> 1) & 1, abort_flag)) {
+              ok = false;
+              return false;
+            }
+            const int item = *reinterpret_cast<volatile int*>(&P.sched[e]);
+            mbar_arrive(&P.sched_empty[e]);
+            ++m.w;
+            if (item < 0) {
+              m.done = true;
+              return false;
+            }
+            Fp8Tile t;
+            fp8_tile(p, item, t);
+            if (t.n == 0) continue;
+            if (!mbar_wait(P.bar_q, m.nq & 1, abort_flag)) {
+              ok = false;
+              return false;
+            }
+            ++m.nq;
+            tc_fence_after();
+            m.n = t.n;
+            m.u = 0;
+            return true;
+          }
+        };
+        // S of step u of pipeline x (its previous step's P8 V has been issued,
+        // so P8 in the S buffer is consumed first)
+        auto issue_s = [&](int x) -> bool {
+          const Pipe8 P = pipe8_at(smem, x);
+          State& m = st[x];
+          const int slot = m.c % F8_NST;
+          if (!mbar_wait(&P.full[slot], (m.c / F8_NST) & 1, abort_flag)) return false;
           tc_fence_after();
-          const uint32_t kb = smem_u32(sStage + slot * F8_TILE);
+          const uint32_t q_base = smem_u32(P.sQ), kb = smem_u32(P.sStage + slot * F8_TILE);
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)  // 32 one-byte columns per MMA
-            mma_f8_ss(tmem + F8_TM_S + (su & 1) * 128, smem_desc_sw128(q_base + ks * 32, 16, 1024),
+            mma_f8_ss(tmem + x * F8_TM_PIPE + F8_TM_S, smem_desc_sw128(q_base + ks * 32, 16, 1024),
                       smem_desc_sw128(kb + ks * 32, 16, 1024), IDESC, ks != 0);
-          mma_commit(&empty[slot]);
-          mma_commit(&bar_s[su & 1]);
-          if (u == steps - 1) mma_commit(q_free);  // the tile's last read of Q
-          ++c;
+          mma_commit(&P.empty[slot]);
+          if (m.u == 2 * m.n - 1) mma_commit(P.q_free);
+          mma_commit(P.bar_s);
+          ++m.c;
           return true;
         };
-        // O += P8 V for pass-2 step u, once its P8 is written
-        auto mma_o = [&](int u) -> bool {
-          if (u == n && no > 0) {  // O still holds the previous tile until its epilogue read it
-            if (!mbar_wait(o_free, (no - 1) & 1, abort_flag)) return false;
-          }
-          if (!mbar_wait(&bar_pr[gp & 1], (gp >> 1) & 1, abort_flag)) return false;
-          const int slot = c % F8_NST;
-          if (!mbar_wait(&full[slot], (c / F8_NST) & 1, abort_flag)) return false;
+        // once the softmax is done with step u: in pass 2, O += P8 V (the
+        // tile's first P8 V overwrites O, which the previous tile's epilogue
+        // must have read)
+        auto after_softmax = [&](int x) -> bool {
+          const Pipe8 P = pipe8_at(smem, x);
+          State& m = st[x];
+          if (m.u == m.n && m.no > 0 && !mbar_wait(P.o_free, (m.no - 1) & 1, abort_flag)) return false;
+          if (!mbar_wait(P.bar_p, m.steps & 1, abort_flag)) return false;
+          ++m.steps;
+          if (m.u < m.n) return true;  // pass 1: the max only
+          const int slot = m.c % F8_NST;
+          if (!mbar_wait(&P.full[slot], (m.c / F8_NST) & 1, abort_flag)) return false;
           tc_fence_after();
-          const uint32_t vb = smem_u32(sStage + slot * F8_TILE);
-          const uint32_t pcol = tmem + F8_TM_P + (gp & 1) * 32;
+          const uint32_t vb = smem_u32(P.sStage + slot * F8_TILE);
+          const uint32_t pcol = tmem + x * F8_TM_PIPE + F8_TM_S;
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks)  // 32 keys per MMA: 8 TMEM columns of packed P8
-            mma_f8_ts(tmem + F8_TM_O, pcol + ks * 8, smem_desc_sw128(vb + ks * 32, 16, 1024), IDESC,
-                      (u - n) > 0 || ks != 0);
-          mma_commit(&empty[slot]);
-          mma_commit(&bar_pf[gp & 1]);
-          if (u == steps - 1) mma_commit(bar_o);  // one completion: every P8 V of the tile is done
-          ++c;
-          ++gp;
+            mma_f8_ts(tmem + x * F8_TM_PIPE + F8_TM_O, pcol + ks * 8, smem_desc_sw128(vb + ks * 32, 16, 1024),
+                      IDESC, (m.u - m.n) > 0 || ks != 0);
+          mma_commit(&P.empty[slot]);
+          ++m.c;
           return true;
         };
-        // Issue order: S(0), S(1); then per step u: S(u + 2) (as soon as the
-        // softmax has loaded S(u)), P8 V(u) (once it has written P8(u)).
-        for (int u = 0; u < 2 && u < steps && ok; ++u) ok = mma_s(u);
-        for (int u = 0; u < steps && ok; ++u) {
-          if (u + 2 < steps) ok = mma_s(u + 2);
-          if (ok && u >= n) ok = mma_o(u);
+        for (int x = 0; x < 2 && ok; ++x)
+          if (next_item(x) && !issue_s(x)) ok = false;
+        while (ok && !(st[0].done && st[1].done)) {
+          for (int x = 0; x < 2 && ok; ++x) {
+            State& m = st[x];
+            if (m.done) continue;
+            if (!after_softmax(x)) {
+              ok = false;
+              break;
+            }
+            if (m.u == 2 * m.n - 1) {
+              mma_commit(pipe8_at(smem, x).bar_o);
+              ++m.no;
+              if (!next_item(x)) continue;  // out of work (or ok cleared)
+            } else {
+              ++m.u;
+            }
+            if (!issue_s(x)) ok = false;
+          }
         }
-        gu += steps;
-        ++no;
-      }
-      if (!ok) {
-        *abort_flag = 1;
-        record_error(p.err, SDPA_ERR_TIMEOUT);
-        mma_commit(bar_drain);
-        mbar_wait_drain(bar_drain, 0);
+        if (!ok) {
+          *abort_flag = 1;
+          record_error(p.err, SDPA_ERR_TIMEOUT);
+          mma_commit(bar_drain);
+          mbar_wait_drain(bar_drain, 0);
+        }
       }
     }
-  } else if (warp >= 4) {
-    const int half = (warp - 4) >> 2;  // this warpgroup's keys and O columns: [64*half, 64*half+64)
-    const int wq = warp & 3;
-    const int r = wq * 32 + lane;
-    const uint32_t lane_base = tmem + ((uint32_t)(wq * 32) << 16);
+  } else {
+    regs_inc<F8_REGS_SOFTMAX>();
+    // ------------------------------------------------------------ softmax + epilogue of pipeline warp / 4
+    const int x = warp >> 2;
+    const Pipe8 P = pipe8_at(smem, x);
+    const int r = (warp & 3) * 32 + lane;
+    const uint32_t lane_base = tmem + x * F8_TM_PIPE + ((uint32_t)((warp & 3) * 32) << 16);
+    const uint32_t scol = lane_base + F8_TM_S;
     const float sl2 = g.scale_log2;
     using T = typename E::T;
-    int gu = 0, gp = 0, nt = 0;  // steps, pass-2 steps, tiles with keys so far
+    int w = 0, steps = 0, no = 0;
     bool ok = true;
-    for (int idx = blockIdx.x; idx < total && ok; idx += gridDim.x) {
+    while (ok) {
+      const int e = w & 1;
+      if (!__all_sync(0xffffffffu, mbar_wait(&P.sched_full[e], (w >> 1) & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      const int item = *reinterpret_cast<volatile int*>(&P.sched[e]);
+      mbar_arrive(&P.sched_empty[e]);
+      ++w;
+      if (item < 0) break;
       Fp8Tile t;
-      if (!fp8_tile(p, idx, t)) continue;
-      const int n = t.n, steps = 2 * n;
+      fp8_tile(p, item, t);
+      const int n = t.n;
       const int i = t.q0 + r;
       const bool valid = i < t.si.lq;
       const int lo_i = t.kr.lo(i), hi_i = t.kr.hi(i);
       const int lo_last = t.kr.lo(t.q_last), hi_first = t.kr.hi(t.q0);
-      T* orow = reinterpret_cast<T*>(p.o) + ((long long)(t.si.qrow0 + i) * g.nh_q + t.qhead) * F8_D + half * 64;
+      T* orow = reinterpret_cast<T*>(p.o) + ((long long)(t.si.qrow0 + i) * g.nh_q + t.qhead) * F8_D;
       float* lse_at = p.lse + (long long)(t.si.qrow0 + i) * g.nh_q + t.qhead;
       if (n == 0) {  // no key for any row of the tile: O = 0, LSE = -inf
-        if (valid && SDPA_ADDR_OK(g.chk, orow, 128)) {
+        if (valid && SDPA_ADDR_OK(g.chk, orow, 256)) {
           uint4* dst = reinterpret_cast<uint4*>(orow);
 #pragma unroll
-          for (int e = 0; e < 8; ++e) dst[e] = make_uint4(0u, 0u, 0u, 0u);
+          for (int k2 = 0; k2 < 16; ++k2) dst[k2] = make_uint4(0u, 0u, 0u, 0u);
         }
-        if (half == 0 && valid && SDPA_ADDR_OK(g.chk, lse_at, 4)) *lse_at = -INFINITY;
+        if (valid && SDPA_ADDR_OK(g.chk, lse_at, 4)) *lse_at = -INFINITY;
         continue;
       }
-      float* xm = xch + (nt & 1) * 4 * F8_BM;  // this tile's partials: [max, sum][half][row]
-      // pass 1: the row max over this half's keys, four independent chains
+      // pass 1: the row max, four independent chains; pass 2: the exponent's
+      // bias log2(448) - m * scale * log2e, so exp2 gives 448 P~ directly,
+      // and the sum of 448 P~ (two lanes)
       float mm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      float m = -INFINITY;  // the row max over all keys (raw score units), after pass 1
-      // pass 2: the exponent's bias log2(448) - m * scale * log2e, so exp2 gives
-      // 448 P~ directly, and the sum of 448 P~ over this half's keys (two lanes)
-      float2 nb2 = make_float2(0.f, 0.f);
+      float m = -INFINITY, nb = 0.f;
       float2 l2 = make_float2(0.f, 0.f);
-      for (int u = 0; u < steps; ++u) {
-        const int su = gu + u;
-        if (!__all_sync(0xffffffffu, mbar_wait(&bar_s[su & 1], (su >> 1) & 1, abort_flag))) {
+      for (int u = 0; u < 2 * n; ++u) {
+        if (!__all_sync(0xffffffffu, mbar_wait(P.bar_s, steps & 1, abort_flag))) {
           ok = false;
           break;
         }
+        ++steps;
         tc_fence_after();
-        const uint32_t scol = lane_base + F8_TM_S + (su & 1) * 128 + half * 64;
-        float s[64];
+        float s[128];
         {
-          uint32_t u0[32], u1[32];
+          uint32_t u0[32], u1[32], u2[32], u3[32];
           tmem_ld32(scol, u0);
           tmem_ld32(scol + 32, u1);
+          tmem_ld32(scol + 64, u2);
+          tmem_ld32(scol + 96, u3);
           tmem_wait_ld();
           reg_fence(u0);
           reg_fence(u1);
+          reg_fence(u2);
+          reg_fence(u3);
 #pragma unroll
           for (int cc = 0; cc < 32; ++cc) {
             s[cc] = __uint_as_float(u0[cc]);
             s[32 + cc] = __uint_as_float(u1[cc]);
+            s[64 + cc] = __uint_as_float(u2[cc]);
+            s[96 + cc] = __uint_as_float(u3[cc]);
           }
         }
-        tc_fence_before();
-        mbar_arrive(&bar_sf[su & 1]);  // the S MMA two steps ahead may overwrite the buffer
-        const int kt0 = (t.t_lo + (u < n ? u : u - n)) * F8_BN;  // the key tile's first key
-        const int kb = kt0 + half * 64;                           // this half's first key
-        if (!(lo_last <= kt0 && hi_first >= kt0 + F8_BN)) {    // edge tile (uniform branch)
+        const int kb = (t.t_lo + (u < n ? u : u - n)) * F8_BN;
+        if (!(lo_last <= kb && hi_first >= kb + F8_BN)) {  // edge tile (uniform branch)
 #pragma unroll
-          for (int cc = 0; cc < 64; ++cc) s[cc] = in_range(kb + cc, lo_i, hi_i) ? s[cc] : -INFINITY;
+          for (int cc = 0; cc < 128; ++cc) s[cc] = in_range(kb + cc, lo_i, hi_i) ? s[cc] : -INFINITY;
         }
         if (u < n) {
 #pragma unroll
-          for (int cc = 0; cc < 64; ++cc) mm[cc & 3] = fmaxf(mm[cc & 3], s[cc]);
+          for (int cc = 0; cc < 128; ++cc) mm[cc & 3] = fmaxf(mm[cc & 3], s[cc]);
           if (u == n - 1) {
-            // both halves' maxima: the row max the definition normalises by
-            const float mine = fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3]));
-            xm[half * F8_BM + r] = mine;
-            mbar_arrive(&bar_x[0]);
-            if (!__all_sync(0xffffffffu, mbar_wait(&bar_x[0], nt & 1, abort_flag))) {
-              ok = false;
-              break;
-            }
-            m = fmaxf(mine, xm[(half ^ 1) * F8_BM + r]);
-            const float nb = kLog2_448 - (m == -INFINITY ? 0.f : m * sl2);
-            nb2 = make_float2(nb, nb);
+            m = fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3]));
+            nb = kLog2_448 - (m == -INFINITY ? 0.f : m * sl2);
           }
         } else {
-          uint32_t pk[16];
-          const float2 sc2 = make_float2(sl2, sl2);
+          uint32_t pk[32];
+          const float2 sc2 = make_float2(sl2, sl2), nb2 = make_float2(nb, nb);
           float2 ra = make_float2(0.f, 0.f), rb = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int cc = 0; cc < 16; ++cc) {
+          for (int cc = 0; cc < 32; ++cc) {
             const float2 ta = ffma2(make_float2(s[4 * cc], s[4 * cc + 1]), sc2, nb2);
             const float2 tb = ffma2(make_float2(s[4 * cc + 2], s[4 * cc + 3]), sc2, nb2);
             const float2 pa = make_float2(ex2(ta.x), ex2(ta.y)), pb = make_float2(ex2(tb.x), ex2(tb.y));
@@ -458,57 +544,46 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
             pk[cc] = pack_e4m3x4(pa.x, pa.y, pb.x, pb.y);  // 448 P~, rounded once to E4M3
           }
           l2 = fadd2(l2, fadd2(ra, rb));
-          // P8 buffer gp & 1, once the P8 V MMA two pass-2 steps back has read it
-          if (!__all_sync(0xffffffffu, mbar_wait(&bar_pf[gp & 1], ((gp >> 1) & 1) ^ 1, abort_flag))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          tmem_st16(lane_base + F8_TM_P + (gp & 1) * 32 + half * 16, pk);
+          tmem_st32(scol, pk);  // P8 into the S buffer's first 32 columns
           tmem_wait_st();
+        }
+        tc_fence_before();
+        mbar_arrive(P.bar_p);
+      }
+      if (!ok) break;
+      // epilogue: O / the row sum, 32 columns at a time; O is free for the
+      // next tile's first P8 V once the last chunk has been read
+      if (!__all_sync(0xffffffffu, mbar_wait(P.bar_o, no & 1, abort_flag))) {
+        ok = false;
+        break;
+      }
+      ++no;
+      tc_fence_after();
+      const float l = l2.x + l2.y;  // the sum of 448 P~
+      const float mul = l > 0.f ? p.o_scale * 448.f / l : 0.f;  // o_scale = d_v / 448
+#pragma unroll 1
+      for (int cc = 0; cc < 4; ++cc) {
+        uint32_t uu[32];
+        tmem_ld32(lane_base + F8_TM_O + cc * 32, uu);
+        tmem_wait_ld();
+        reg_fence(uu);
+        if (cc == 3) {
           tc_fence_before();
-          mbar_arrive(&bar_pr[gp & 1]);
-          ++gp;
+          mbar_arrive(P.o_free);
+        }
+        uint32_t packed[16];
+#pragma unroll
+        for (int k2 = 0; k2 < 16; ++k2)
+          packed[k2] = E::pack(__uint_as_float(uu[2 * k2]) * mul, __uint_as_float(uu[2 * k2 + 1]) * mul);
+        if (valid && SDPA_ADDR_OK(g.chk, orow + cc * 32, 64)) {
+          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+          for (int k2 = 0; k2 < 4; ++k2)
+            dst[k2] = make_uint4(packed[4 * k2], packed[4 * k2 + 1], packed[4 * k2 + 2], packed[4 * k2 + 3]);
         }
       }
-      if (!ok) break;
-      // the row sum (of 448 P~) over both halves, then every P8 V of the tile
-      float l = l2.x + l2.y;
-      xm[(2 + half) * F8_BM + r] = l;
-      mbar_arrive(&bar_x[1]);
-      ok = __all_sync(0xffffffffu, mbar_wait(&bar_x[1], nt & 1, abort_flag)) &&
-           __all_sync(0xffffffffu, mbar_wait(bar_o, nt & 1, abort_flag));
-      if (!ok) break;
-      l += xm[(2 + (half ^ 1)) * F8_BM + r];
-      tc_fence_after();
-      uint32_t ua[32], ub[32];
-      tmem_ld32(lane_base + F8_TM_O + half * 64, ua);
-      tmem_ld32(lane_base + F8_TM_O + half * 64 + 32, ub);
-      tmem_wait_ld();
-      reg_fence(ua);
-      reg_fence(ub);
-      tc_fence_before();
-      mbar_arrive(o_free);  // the next tile's P8 V may overwrite O
-      const float mul = l > 0.f ? p.o_scale * 448.f / l : 0.f;  // o_scale = d_v / 448
-      if (valid && SDPA_ADDR_OK(g.chk, orow, 128)) {
-        uint4* dst = reinterpret_cast<uint4*>(orow);
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          dst[e] = make_uint4(E::pack(__uint_as_float(ua[8 * e]) * mul, __uint_as_float(ua[8 * e + 1]) * mul),
-                              E::pack(__uint_as_float(ua[8 * e + 2]) * mul, __uint_as_float(ua[8 * e + 3]) * mul),
-                              E::pack(__uint_as_float(ua[8 * e + 4]) * mul, __uint_as_float(ua[8 * e + 5]) * mul),
-                              E::pack(__uint_as_float(ua[8 * e + 6]) * mul, __uint_as_float(ua[8 * e + 7]) * mul));
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          dst[4 + e] = make_uint4(E::pack(__uint_as_float(ub[8 * e]) * mul, __uint_as_float(ub[8 * e + 1]) * mul),
-                                  E::pack(__uint_as_float(ub[8 * e + 2]) * mul, __uint_as_float(ub[8 * e + 3]) * mul),
-                                  E::pack(__uint_as_float(ub[8 * e + 4]) * mul, __uint_as_float(ub[8 * e + 5]) * mul),
-                                  E::pack(__uint_as_float(ub[8 * e + 6]) * mul, __uint_as_float(ub[8 * e + 7]) * mul));
-      }
-      if (half == 0 && valid && SDPA_ADDR_OK(g.chk, lse_at, 4))
+      if (valid && SDPA_ADDR_OK(g.chk, lse_at, 4))
         *lse_at = l > 0.f ? m * g.scale + (logf(l) - kLn448) : -INFINITY;
-      gu += steps;
-      ++nt;
     }
     if (!ok) {
       *abort_flag = 1;
@@ -518,7 +593,7 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 10) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
@@ -538,14 +613,15 @@ int launch_fwd_fp8(const Fp8Launch& L, bool bf16) {
   if (tiles <= 0) return SDPA_OK;
   if (tiles > 0x7fffffffLL - 4096) return SDPA_ERR_UNSUPPORTED;
   auto kern = bf16 ? fwd_fp8_kernel<true> : fwd_fp8_kernel<false>;
-  if (const int rc = set_kernel_smem(reinterpret_cast<const void*>(kern), F8_SMEM, -1)) return rc;
+  if (const int rc = set_kernel_smem(reinterpret_cast<const void*>(kern), F8_SMEM, 100)) return rc;
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
     return SDPA_ERR_CUDA;
   Fp8Params p = L.p;
   p.total_tiles = (int)tiles;
-  long long grid = std::min<long long>(tiles, sms);
-  if (debug_max_ctas() > 0) grid = std::min<long long>(grid, debug_max_ctas());  // the CTAs stride over every tile
+  long long grid = std::min<long long>((tiles + 1) / 2, sms);
+  if (debug_max_ctas() > 0) grid = std::min<long long>(grid, debug_max_ctas());  // tickets cover every tile
+  if (cudaMemsetAsync(p.tile_counter, 0, sizeof(int), L.stream) != cudaSuccess) return SDPA_ERR_CUDA;
   kern<<<(unsigned)grid, F8_THREADS, F8_SMEM, L.stream>>>(L.tmQ, L.tmK, L.tmVt, p);
   return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }

@@ -147,7 +147,8 @@ struct Fp8Params {
   const int* guard;
   int n_q_tiles;
   float o_scale;        // d_v / 448 (the epilogue divides by the row sum as well)
-  int total_tiles;      // query tiles of the order (the persistent forward strides over them)
+  int total_tiles;      // query tiles of the order (tickets of the persistent forward)
+  int* tile_counter;    // ticket counter in the workspace (zeroed per call)
 };
 struct Fp8Launch {
   CUtensorMap tmQ, tmK, tmVt;  // E4M3 128-byte rows, 128-row boxes; Vt 128 keys x 128 d boxes
