@@ -306,9 +306,10 @@ SDPA_API int sdpa_merge(const sdpa_merge_problem* p, const void* o_parts, const 
  * p->head_dim must be 128 (head_dim_v 0 or 128), else SDPA_ERR_UNSUPPORTED;
  * p->dtype is O's type. Descales: finite and > 0, else SDPA_ERR_INVALID_ARG.
  * workspace: at least sdpa_fwd_fp8_workspace_size bytes, 256-byte aligned
- * (the THD guard word and V transposed to [Hkv][128][keys], one byte per key,
- * every sequence starting on a 16-byte boundary). Launches (THD guard), the
- * transpose and the attention kernel on `stream`; errors as sdpa_fwd. */
+ * (the THD guard word, the query-tile ticket counter, and V transposed to
+ * [Hkv][128][keys], one byte per key, every sequence starting on a 16-byte
+ * boundary). Launches (THD guard), the transpose, a 4-byte memset of the ticket
+ * counter and the attention kernel on `stream`; errors as sdpa_fwd. */
 SDPA_API size_t sdpa_fwd_fp8_workspace_size(const sdpa_problem* p);
 SDPA_API int sdpa_fwd_fp8(const sdpa_problem* p, const void* q8, const void* k8, const void* v8, float descale_q,
                           float descale_k, float descale_v, void* o, float* lse, const int32_t* cu_seqlens_q,
