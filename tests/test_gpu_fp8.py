@@ -124,3 +124,53 @@ def test_fp8_forward_matches_oracle(case):
           f"median bound={np.median(bound):.3e}; LSE err={lse_err:.3e} ({int(empty.sum())} empty rows)")
     assert lse_err <= 1e-4
     assert worst <= 1.0, f"O exceeds its bound by {worst:.2f}x"
+
+
+FULL = [workloads.VARLEN_THD, workloads.LONG_FP16]
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("w", FULL, ids=lambda w: w.name)
+def test_fp8_full_size_sampled_rows(w):
+    """The FP8 forward at the full workload shapes, in the configuration the
+    benchmark times (bf16 O), checked on sampled query rows. Under top-left
+    causal, row i of a sequence sees exactly its keys 0..i, so the oracle
+    checks each sampled row as a one-query problem over those keys with no
+    mask, under the same bound as the small cases."""
+    import torch
+
+    from oracle import oracle
+    from parity import gpu_kwargs, kv_token_row, sample_rows, token_row
+    from scaled_dot_product_02_gb300 import sdpa_fwd_fp8, sdpa_get_device_error
+
+    assert w.mask == "causal" and w.window == (-1, -1) and w.head_dim == 128
+    inp = workloads.fp8_inputs(w)
+    kw = gpu_kwargs(w, inp)
+    q8, k8, v8 = (torch.from_numpy(inp[x]).cuda() for x in ("q8", "k8", "v8"))
+    o, lse = sdpa_fwd_fp8(q8, k8, v8, descale=workloads.FP8_DESCALE, out_dtype=torch.bfloat16, **kw)
+    assert sdpa_get_device_error() == 0
+    o = o.float().cpu().numpy().astype(np.float64).reshape(-1, w.heads_q, 128)
+    lse = lse.cpu().numpy().astype(np.float64).reshape(-1, w.heads_q)
+    del q8, k8, v8
+    torch.cuda.empty_cache()
+
+    group = w.heads_q // w.heads_kv
+    qs, ks, vs = (inp[x].reshape(-1, n, 128) for x, n in (("q8", w.heads_q), ("k8", w.heads_kv), ("v8", w.heads_kv)))
+    dq, dk, _ = workloads.FP8_DESCALE
+    okw = dict(layout="bshd", mask="none", scale=w.scale)
+    worst, lse_err = 0.0, 0.0
+    rows = sample_rows(w, inp, 40, seed=17)
+    for b, h, i in rows:
+        t = token_row(w, inp, int(b), int(i))
+        kv = np.array([kv_token_row(w, inp, int(b), j) for j in range(int(i) + 1)])
+        sub = {"q8": qs[t, h][None, None, None, :], "k8": ks[kv, h // group][None, :, None, :],
+               "v8": vs[kv, h // group][None, :, None, :]}
+        sw = Workload("row", "bshd", "none", 1, 1, len(kv), 1, 1, 128, "bf16")
+        o_ref, l_ref = oracle.fwd_fp8(sub["q8"], sub["k8"], sub["v8"], descale=workloads.FP8_DESCALE, **okw)
+        probs = oracle.probs(oracle.e4m3_decode(sub["q8"]) * dq, oracle.e4m3_decode(sub["k8"]) * dk, **okw)
+        bound = _bound(sw, sub, probs, o_ref, oracle.e4m3_decode(sub["v8"])).reshape(128)
+        worst = max(worst, float(np.max(np.abs(o[t, h] - o_ref.reshape(128)) / bound)))
+        lse_err = max(lse_err, abs(float(lse[t, h]) - float(np.ravel(l_ref)[0])))
+    print(f"[{w.name} fp8, {len(rows)} sampled rows] worst err/bound={worst:.3f}; LSE err={lse_err:.3e}")
+    assert lse_err <= 1e-4
+    assert worst <= 1.0, f"O exceeds its bound by {worst:.2f}x"
