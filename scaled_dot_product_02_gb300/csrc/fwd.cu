@@ -316,17 +316,21 @@ __global__ void __launch_bounds__(256, 1)
         tc_fence_after();
         const uint32_t scol = lane_base + C::TMEM_S + (sj & 1) * 128;
         float s[128];
+        float mt;  // the tile's row max (the loads return it for an unmasked tile)
         {
           uint32_t u0[32], u1[32], u2[32], u3[32];
-          tmem_ld32(scol, u0);
-          tmem_ld32(scol + 32, u1);
-          tmem_ld32(scol + 64, u2);
-          tmem_ld32(scol + 96, u3);
+          float x0, x1, x2, x3;
+          tmem_ld32_max(scol, u0, x0);
+          tmem_ld32_max(scol + 32, u1, x1);
+          tmem_ld32_max(scol + 64, u2, x2);
+          tmem_ld32_max(scol + 96, u3, x3);
           tmem_wait_ld();
           reg_fence(u0);
           reg_fence(u1);
           reg_fence(u2);
           reg_fence(u3);
+          asm volatile("" : "+f"(x0), "+f"(x1), "+f"(x2), "+f"(x3));
+          mt = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
 #pragma unroll
           for (int c = 0; c < 32; ++c) {
             s[c] = __uint_as_float(u0[c]);
@@ -339,10 +343,11 @@ __global__ void __launch_bounds__(256, 1)
         if (!(lo_last <= kb && hi_first >= kb + C::BN)) {  // edge tile (uniform branch)
 #pragma unroll
           for (int c = 0; c < 128; ++c) s[c] = in_range(kb + c, lo_i, hi_i) ? s[c] : -INFINITY;
-        }
-        float mt = s[0];
+          float mc[4] = {s[0], s[1], s[2], s[3]};
 #pragma unroll
-        for (int c = 1; c < 128; ++c) mt = fmaxf(mt, s[c]);
+          for (int c = 4; c < 128; ++c) mc[c & 3] = fmaxf(mc[c & 3], s[c]);
+          mt = fmaxf(fmaxf(mc[0], mc[1]), fmaxf(mc[2], mc[3]));
+        }
         const float m_new = fmaxf(m_used, mt);
         bool need = false;
         float f = 1.f;
@@ -485,9 +490,19 @@ __device__ __forceinline__ void p_pass(uint32_t scol, float sl2, float mb, int k
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     uint32_t u[32];
-    tmem_ld32(scol + c * 32, u);
+    float cmax = 0.f;
+    if (MASK)
+      tmem_ld32(scol + c * 32, u);
+    else
+      tmem_ld32_max(scol + c * 32, u, cmax);
     tmem_wait_ld();
     reg_fence(u);
+    if (!MASK) {
+      // the load returned the chunk's max score; the rounding of the exponent
+      // being monotone, fma(max, scale*log2e, -mb) is the chunk's largest one
+      asm volatile("" : "+f"(cmax));
+      tmax = fmaxf(tmax, __fmaf_rn(cmax, sl2, -mb));
+    }
 #pragma unroll
     for (int e = 0; e < 32; e += 2) {
       float2 t = ffma2(make_float2(__uint_as_float(u[e]), __uint_as_float(u[e + 1])), sc, nm);
@@ -495,8 +510,8 @@ __device__ __forceinline__ void p_pass(uint32_t scol, float sl2, float mb, int k
         const int key = kb + c * 32 + e;
         t.x = in_range(key, lo, hi) ? t.x : -INFINITY;
         t.y = in_range(key + 1, lo, hi) ? t.y : -INFINITY;
+        tmax = fmaxf(tmax, fmaxf(t.x, t.y));
       }
-      tmax = fmaxf(tmax, fmaxf(t.x, t.y));
       const float2 p = make_float2(ex2(t.x), ex2(t.y));
       pk[c * 16 + e / 2] = E::pack(p.x, p.y);
       acc = fadd2(acc, p);

@@ -498,54 +498,71 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
         }
         ++steps;
         tc_fence_after();
-        float s[128];
-        {
-          uint32_t u0[32], u1[32], u2[32], u3[32];
-          tmem_ld32(scol, u0);
-          tmem_ld32(scol + 32, u1);
-          tmem_ld32(scol + 64, u2);
-          tmem_ld32(scol + 96, u3);
-          tmem_wait_ld();
-          reg_fence(u0);
-          reg_fence(u1);
-          reg_fence(u2);
-          reg_fence(u3);
-#pragma unroll
-          for (int cc = 0; cc < 32; ++cc) {
-            s[cc] = __uint_as_float(u0[cc]);
-            s[32 + cc] = __uint_as_float(u1[cc]);
-            s[64 + cc] = __uint_as_float(u2[cc]);
-            s[96 + cc] = __uint_as_float(u3[cc]);
-          }
-        }
         const int kb = (t.t_lo + (u < n ? u : u - n)) * F8_BN;
-        if (!(lo_last <= kb && hi_first >= kb + F8_BN)) {  // edge tile (uniform branch)
-#pragma unroll
-          for (int cc = 0; cc < 128; ++cc) s[cc] = in_range(kb + cc, lo_i, hi_i) ? s[cc] : -INFINITY;
-        }
-        if (u < n) {
-#pragma unroll
-          for (int cc = 0; cc < 128; ++cc) mm[cc & 3] = fmaxf(mm[cc & 3], s[cc]);
-          if (u == n - 1) {
-            m = fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3]));
-            nb = kLog2_448 - (m == -INFINITY ? 0.f : m * sl2);
-          }
+        const bool edge = !(lo_last <= kb && hi_first >= kb + F8_BN);  // uniform across the tile
+        if (u < n && !edge) {
+          // interior pass-1 step: the row max comes with the loads
+          uint32_t u0[32], u1[32], u2[32], u3[32];
+          float x0, x1, x2, x3;
+          tmem_ld32_max(scol, u0, x0);
+          tmem_ld32_max(scol + 32, u1, x1);
+          tmem_ld32_max(scol + 64, u2, x2);
+          tmem_ld32_max(scol + 96, u3, x3);
+          tmem_wait_ld();
+          asm volatile("" : "+f"(x0), "+f"(x1), "+f"(x2), "+f"(x3));
+          mm[0] = fmaxf(mm[0], x0);
+          mm[1] = fmaxf(mm[1], x1);
+          mm[2] = fmaxf(mm[2], x2);
+          mm[3] = fmaxf(mm[3], x3);
         } else {
-          uint32_t pk[32];
-          const float2 sc2 = make_float2(sl2, sl2), nb2 = make_float2(nb, nb);
-          float2 ra = make_float2(0.f, 0.f), rb = make_float2(0.f, 0.f);
+          float s[128];
+          {
+            uint32_t u0[32], u1[32], u2[32], u3[32];
+            tmem_ld32(scol, u0);
+            tmem_ld32(scol + 32, u1);
+            tmem_ld32(scol + 64, u2);
+            tmem_ld32(scol + 96, u3);
+            tmem_wait_ld();
+            reg_fence(u0);
+            reg_fence(u1);
+            reg_fence(u2);
+            reg_fence(u3);
 #pragma unroll
-          for (int cc = 0; cc < 32; ++cc) {
-            const float2 ta = ffma2(make_float2(s[4 * cc], s[4 * cc + 1]), sc2, nb2);
-            const float2 tb = ffma2(make_float2(s[4 * cc + 2], s[4 * cc + 3]), sc2, nb2);
-            const float2 pa = make_float2(ex2(ta.x), ex2(ta.y)), pb = make_float2(ex2(tb.x), ex2(tb.y));
-            ra = fadd2(ra, pa);
-            rb = fadd2(rb, pb);
-            pk[cc] = pack_e4m3x4(pa.x, pa.y, pb.x, pb.y);  // 448 P~, rounded once to E4M3
+            for (int cc = 0; cc < 32; ++cc) {
+              s[cc] = __uint_as_float(u0[cc]);
+              s[32 + cc] = __uint_as_float(u1[cc]);
+              s[64 + cc] = __uint_as_float(u2[cc]);
+              s[96 + cc] = __uint_as_float(u3[cc]);
+            }
           }
-          l2 = fadd2(l2, fadd2(ra, rb));
-          tmem_st32(scol, pk);  // P8 into the S buffer's first 32 columns
-          tmem_wait_st();
+          if (edge) {
+#pragma unroll
+            for (int cc = 0; cc < 128; ++cc) s[cc] = in_range(kb + cc, lo_i, hi_i) ? s[cc] : -INFINITY;
+          }
+          if (u < n) {
+#pragma unroll
+            for (int cc = 0; cc < 128; ++cc) mm[cc & 3] = fmaxf(mm[cc & 3], s[cc]);
+          } else {
+            uint32_t pk[32];
+            const float2 sc2 = make_float2(sl2, sl2), nb2 = make_float2(nb, nb);
+            float2 ra = make_float2(0.f, 0.f), rb = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int cc = 0; cc < 32; ++cc) {
+              const float2 ta = ffma2(make_float2(s[4 * cc], s[4 * cc + 1]), sc2, nb2);
+              const float2 tb = ffma2(make_float2(s[4 * cc + 2], s[4 * cc + 3]), sc2, nb2);
+              const float2 pa = make_float2(ex2(ta.x), ex2(ta.y)), pb = make_float2(ex2(tb.x), ex2(tb.y));
+              ra = fadd2(ra, pa);
+              rb = fadd2(rb, pb);
+              pk[cc] = pack_e4m3x4(pa.x, pa.y, pb.x, pb.y);  // 448 P~, rounded once to E4M3
+            }
+            l2 = fadd2(l2, fadd2(ra, rb));
+            tmem_st32(scol, pk);  // P8 into the S buffer's first 32 columns
+            tmem_wait_st();
+          }
+        }
+        if (u == n - 1) {
+          m = fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3]));
+          nb = kLog2_448 - (m == -INFINITY ? 0.f : m * sl2);
         }
         tc_fence_before();
         mbar_arrive(P.bar_p);
