@@ -19,6 +19,7 @@ BWD_CASES = [
     # head_dim 256 / 512: two-phase backward (score tiles + GEMMs)
     Workload("window_d256", "bshd", "causal", 1, 400, 400, 2, 1, 256, "bf16", window=(100, 0)),
     Workload("d256_fp16_sbhd_window", "sbhd", "causal", 2, 260, 260, 2, 1, 256, "fp16", window=(64, 0)),
+    Workload("window_d256_gqa_three_kv_heads", "bshd", "causal", 1, 450, 450, 6, 3, 256, "bf16", window=(150, 0)),
     Workload("d256_thd_varlen", "thd", "causal", 3, 300, 300, 4, 2, 256, "bf16", len_range=(1, 300)),
     Workload("d512_br", "bshd", "causal_br", 1, 130, 300, 2, 1, 512, "bf16"),
     Workload("d512_nomask_gqa", "bshd", "none", 1, 129, 257, 4, 2, 512, "bf16"),
