@@ -24,18 +24,17 @@
 // of Vt (TMA's alignment rule for the innermost coordinate), and the gaps
 // between sequences hold zeros.
 //
-// Roles (384 threads): warp 0 TMA producer, warp 1 TMEM allocator and MMA
-// issuer, warps 4-7 and 8-11 softmax and epilogue: one thread per query row
-// in each warpgroup, warpgroup `half` owning the keys [64*half, 64*half+64)
-// of every key tile and the value columns [64*half, 64*half+64) of O. Each
-// keeps a partial row max (pass 1) and sum (pass 2) over its keys; the two
-// are combined through shared memory once per query tile.
-// A warpgroup releases a step's S buffer as soon as it has loaded the scores
-// into registers, so the S MMA two steps ahead runs during this step's
-// softmax; P8 has buffers of its own, released by the P8 V MMA that read
-// them.
-// TMEM: O [0,128), S buffers [128,256) and [256,384), P8 buffers [384,416)
-// and [416,448) (16 columns per warpgroup: 64 keys of one byte).
+// The kernel is persistent (one CTA per SM) with two query-tile pipelines,
+// tiles taken heaviest first from an atomic ticket counter. Roles (384
+// threads): warps 0-3 / 4-7 softmax and epilogue of pipeline 0 / 1 (one
+// thread per query row, all 128 keys of a step), warps 8 / 9 TMA producer and
+// scheduler of pipeline 0 / 1, warp 10 TMEM allocator and MMA issuer serving
+// the two pipelines strictly in turn (so one pipeline's softmax runs under the
+// other's MMAs), warp 11 completes the third warpgroup. Per pipeline: a Q
+// tile and a four-stage K / Vt ring in shared memory; in TMEM its O (128
+// columns) and one S buffer (128), into whose first 32 columns the softmax
+// writes P8 for the P8 V MMA. On unmasked key tiles pass 1 takes each
+// 32-column chunk's max from the TMEM load itself (load with max reduction).
 #include <algorithm>
 
 #include <cuda.h>
