@@ -662,7 +662,7 @@ def fp8_oracle_sample(w, inp8, seconds_target):
             kw = dict(layout="sbhd")
         q8, k8, v8 = (np.ascontiguousarray(x) for x in (q8, k8, v8))
         t0 = time.perf_counter()
-        oracle.fwd_fp8(q8, k8, v8, descale=workloads.FP8_DESCALE, mask=w.mask, scale=w.scale, **kw)
+        oracle.fwd_fp8(q8, k8, v8, descale=workloads.FP8_DESCALE, mask=w.mask, scale=w.scale, window=w.window, **kw)
         dt = time.perf_counter() - t0
         sub = w.replace(layout="bshd", batch=1, seqlen_q=lq, seqlen_kv=lq, heads_q=group, heads_kv=1)
         _, fl = flops(sub, {})
@@ -681,8 +681,8 @@ def fp8_arm(args, w, inp):
 
     import scaled_dot_product_02_gb300 as sdpa
 
-    if w.head_dim != 128 or w.dv != 128:
-        raise SystemExit("--op fp8 needs a head_dim 128 workload")
+    if w.head_dim not in (128, 256) or w.dv != w.head_dim:
+        raise SystemExit("--op fp8 needs a head_dim 128 or 256 workload")
     world, rank, local = rank_env()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
@@ -698,7 +698,7 @@ def fp8_arm(args, w, inp):
                   max_seqlen_q=int(np.max(np.diff(inp8["cu_seqlens_q"]))),
                   max_seqlen_kv=int(np.max(np.diff(inp8["cu_seqlens_kv"]))))
     o = torch.empty(tuple(q8.shape), dtype=torch.bfloat16, device=dev)
-    rows_q = q8.numel() // (w.heads_q * 128)
+    rows_q = q8.numel() // (w.heads_q * w.head_dim)
     lse = torch.empty((rows_q, w.heads_q), dtype=torch.float32, device=dev)
     batch = len(inp8["cu_seqlens_q"]) - 1 if w.layout == "thd" else None
     prob = sdpa.make_problem(q8, k8, layout=w.layout, mask=w.mask, window=w.window, scale=w.scale, batch=batch,
@@ -772,7 +772,7 @@ def fp8_arm(args, w, inp):
             "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "e4m3 (fp32 accumulate, bf16 O)", "data": "synthetic",
             "config": {"workload": f"{w.name}_fp8", "layout": w.layout, "mask": w.mask, "heads_q": w.heads_q,
-                       "heads_kv": w.heads_kv, "head_dim": 128, "descale": list(workloads.FP8_DESCALE),
+                       "heads_kv": w.heads_kv, "head_dim": w.head_dim, "descale": list(workloads.FP8_DESCALE),
                        "inputs": "E4M3 codes of the workload's seeded N(0,1) masters times 3",
                        "l2": "flushed between timed steps (256 MiB write, outside the events)",
                        "parallelism": f"replicas x{world} (no collective)"},
@@ -824,7 +824,7 @@ def main():
     ap.add_argument("--op", default="step", choices=["step", "fwd", "merge", "fp8"],
                     help="step: the fwd+bwd hot path (the headline; the forward alone for forward-only "
                          "workloads); fwd: the forward alone; merge: the LSE merge of key-split results; "
-                         "fp8: the FP8 E4M3 forward (head_dim 128 workloads)")
+                         "fp8: the FP8 E4M3 forward (head_dim 128 or 256 workloads)")
     ap.add_argument("--merge-parts", type=int, default=4)
     ap.add_argument("--kv-chunk", type=int, default=0,
                     help="head_dim 256/512 backward: key positions per chunk (multiple of 128; 0 = library choice)")

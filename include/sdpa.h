@@ -290,24 +290,26 @@ typedef struct {
 SDPA_API int sdpa_merge(const sdpa_merge_problem* p, const void* o_parts, const float* lse_parts, void* o, float* lse,
                void* stream);
 
-/* FP8 E4M3 forward, head_dim 128 (TransformerEngine PR #3705's closing note
+/* FP8 E4M3 forward, head_dim 128 or 256 (TransformerEngine PR #3705's closing note
  * on FP8: with E4M3 inputs the softmax output is stored in E4M3 under the
  * fixed scale 448, so no amax of it is needed; PR #3527 "Scope" lists the
- * FP8 fused path). Computes, with the decoded values of the codes,
+ * FP8 fused path at head dims up to 256). Computes, with the decoded values
+ * of the codes,
  *   S = softmax_scale * descale_q * descale_k * Q8 K8^T, masked as sdpa_fwd;
  *   m = max_j S_ij, l = sum_j exp(S_ij - m), LSE = m + ln l   (float32,
  *       token-major, as sdpa_fwd);
  *   P8  = E4M3(exp(S - m) * 448)   (round to nearest even; the row's largest
  *         probability is stored as 448, so no amax is needed);
  *   O   = P8 V8 * descale_v / (448 * l)   (written in p->dtype: bf16 or fp16).
- * q8 [.., Hq, 128], k8 and v8 [.., Hkv, 128]: device E4M3 codes (the finite-
+ * q8 [.., Hq, D], k8 and v8 [.., Hkv, D]: device E4M3 codes (the finite-
  * only OCP format: bias 7, largest 448, S.1111.111 = NaN), one byte each, in
- * p->layout; o [.., Hq, 128] and lse as for sdpa_fwd (device, written).
- * p->head_dim must be 128 (head_dim_v 0 or 128), else SDPA_ERR_UNSUPPORTED;
+ * p->layout; o [.., Hq, D] and lse as for sdpa_fwd (device, written).
+ * p->head_dim = D must be 128 or 256 (head_dim_v 0 or D), else
+ * SDPA_ERR_UNSUPPORTED;
  * p->dtype is O's type. Descales: finite and > 0, else SDPA_ERR_INVALID_ARG.
  * workspace: at least sdpa_fwd_fp8_workspace_size bytes, 256-byte aligned
  * (the THD guard word, the query-tile ticket counter, and V transposed to
- * [Hkv][128][keys], one byte per key, every sequence starting on a 16-byte
+ * [Hkv][D][keys], one byte per key, every sequence starting on a 16-byte
  * boundary). Launches (THD guard), the transpose, a 4-byte memset of the ticket
  * counter and the attention kernel on `stream`; errors as sdpa_fwd. */
 SDPA_API size_t sdpa_fwd_fp8_workspace_size(const sdpa_problem* p);

@@ -349,7 +349,7 @@ def sdpa_fwd_fp8_workspace_size(p: Problem) -> int:
 def sdpa_fwd_fp8(q8, k8, v8, *, descale=(1.0, 1.0, 1.0), layout="bshd", mask="none", window=(-1, -1), scale=None,
                  cu_seqlens_q=None, cu_seqlens_kv=None, max_seqlen_q=None, max_seqlen_kv=None, out_dtype=None,
                  out=None, lse=None, workspace=None, stream=None):
-    """FP8 E4M3 forward (head_dim 128). q8, k8, v8: torch.uint8 codes or
+    """FP8 E4M3 forward (head_dim 128 or 256). q8, k8, v8: torch.uint8 codes or
     torch.float8_e4m3fn tensors in `layout`; descale = (d_q, d_k, d_v), the
     per-tensor factors that turn codes into values. The softmax output is
     stored as E4M3(exp(S - m) * 448), m the row's final maximum, and O divides

@@ -271,12 +271,12 @@ size_t fp8_vt_rows(const sdpa_problem* p) {
   return round_up((size_t)p->seqlen_kv, 16);
 }
 
-// FP8 forward: head_dim 128 only (PR #3527 "Scope" serves FP8 at head dims up
-// to 256; this library builds the 128 of the benchmark workloads).
+// FP8 forward: head_dim 128 or 256, equal for Q/K and V (PR #3527 "Scope"
+// serves FP8 at head dims up to 256).
 int check_fp8(const sdpa_problem* p) {
   const int rc = check(p);
   if (rc) return rc;
-  return (p->head_dim == 128 && dv_of(p) == 128) ? SDPA_OK : SDPA_ERR_UNSUPPORTED;
+  return ((p->head_dim == 128 || p->head_dim == 256) && dv_of(p) == p->head_dim) ? SDPA_OK : SDPA_ERR_UNSUPPORTED;
 }
 
 // Key tiles one 128-row query tile can touch (the slot count of the head_dim
@@ -657,7 +657,7 @@ size_t sdpa_fwd_fp8_workspace_size(const sdpa_problem* p) {
   if (check_fp8(p) != SDPA_OK) return 0;
   int rq, rk, hq, hk;
   view(p, rq, rk, hq, hk);
-  return 256 + (size_t)hk * 128 * fp8_vt_rows(p);
+  return 256 + (size_t)hk * p->head_dim * fp8_vt_rows(p);
 }
 
 int sdpa_fwd_fp8(const sdpa_problem* p, const void* q8, const void* k8, const void* v8, float descale_q,
@@ -680,7 +680,8 @@ int sdpa_fwd_fp8(const sdpa_problem* p, const void* q8, const void* k8, const vo
   const size_t need = sdpa_fwd_fp8_workspace_size(p);
   if (ws_bytes < need || !workspace) return SDPA_ERR_WORKSPACE_TOO_SMALL;
   if (reinterpret_cast<uintptr_t>(workspace) & 255u) return SDPA_ERR_ALIGNMENT;
-  const size_t qb = (size_t)rq * hq * 128, kb = (size_t)rk * hk * 128, ob = (size_t)rq * hq * 128 * 2;
+  const size_t D = (size_t)p->head_dim;
+  const size_t qb = (size_t)rq * hq * D, kb = (size_t)rk * hk * D, ob = (size_t)rq * hq * D * 2;
   const Extent outs[3] = {extent(o, ob), extent(lse, (size_t)rq * hq * 4), extent(workspace, need)};
   const Extent ins[3] = {extent(q8, qb), extent(k8, kb), extent(v8, kb)};
   for (int x = 0; x < 3; ++x) {
@@ -714,15 +715,16 @@ int sdpa_fwd_fp8(const sdpa_problem* p, const void* q8, const void* k8, const vo
   L.p.n_q_tiles = (p->seqlen_q + 127) / 128;
   L.p.o_scale = descale_v / 448.f;
   L.stream = s;
-  if ((size_t)L.p.vt_rows * hk * 128 >= (1ull << 40)) return SDPA_ERR_UNSUPPORTED;
+  if ((size_t)L.p.vt_rows * hk * D >= (1ull << 40)) return SDPA_ERR_UNSUPPORTED;
   {
-    const cuuint64_t dq[3] = {128, (cuuint64_t)hq, (cuuint64_t)(rq > 0 ? rq : 1)};
-    const cuuint64_t sq[2] = {128, (cuuint64_t)hq * 128};
-    const cuuint64_t dk[3] = {128, (cuuint64_t)hk, (cuuint64_t)(rk > 0 ? rk : 1)};
-    const cuuint64_t sk[2] = {128, (cuuint64_t)hk * 128};
-    const cuuint64_t dvt[3] = {(cuuint64_t)L.p.vt_rows, 128, (cuuint64_t)hk};
-    const cuuint64_t svt[2] = {(cuuint64_t)L.p.vt_rows, (cuuint64_t)L.p.vt_rows * 128};
-    const cuuint32_t box_rows[3] = {128, 1, 128}, box_vt[3] = {128, 128, 1};
+    // Q, K: boxes of 128 one-byte columns (a head_dim 256 tile is two); Vt: one box of D rows
+    const cuuint64_t dq[3] = {D, (cuuint64_t)hq, (cuuint64_t)(rq > 0 ? rq : 1)};
+    const cuuint64_t sq[2] = {D, (cuuint64_t)hq * D};
+    const cuuint64_t dk[3] = {D, (cuuint64_t)hk, (cuuint64_t)(rk > 0 ? rk : 1)};
+    const cuuint64_t sk[2] = {D, (cuuint64_t)hk * D};
+    const cuuint64_t dvt[3] = {(cuuint64_t)L.p.vt_rows, D, (cuuint64_t)hk};
+    const cuuint64_t svt[2] = {(cuuint64_t)L.p.vt_rows, (cuuint64_t)L.p.vt_rows * D};
+    const cuuint32_t box_rows[3] = {128, 1, 128}, box_vt[3] = {128, (cuuint32_t)D, 1};
     if ((rc = encode_u8(&L.tmQ, q8, dq, sq, box_rows))) return rc;
     if ((rc = encode_u8(&L.tmK, k8, dk, sk, box_rows))) return rc;
     if ((rc = encode_u8(&L.tmVt, L.p.vt, dvt, svt, box_vt))) return rc;

@@ -48,19 +48,29 @@ namespace sdpa {
 
 namespace {
 
-constexpr int F8_BM = 128, F8_BN = 128, F8_D = 128;
-constexpr int F8_TILE = 16384;  // 128 rows x 128 one-byte columns
-// Two query-tile pipelines per CTA (as the head_dim 128 bf16 forward): each
-// with its Q tile, a ring of F8_NST K / Vt tiles, and in TMEM its O and one S
-// buffer (P8 is written back into the S buffer for the P8 V MMA).
-constexpr int F8_NST = 4;
-constexpr int F8_PIPE_BYTES = F8_TILE + F8_NST * F8_TILE;  // per pipeline, 1024-aligned
-constexpr int F8_PIPE_BARS = 2 * F8_NST + 12;             // mbarriers + queue per pipeline (8 bytes each)
-constexpr int F8_SMEM = 1024 + 2 * F8_PIPE_BYTES + 2 * F8_PIPE_BARS * 8 + 32;
+constexpr int F8_BM = 128, F8_BN = 128;
+// Per head_dim D (128 or 256): two query-tile pipelines at D = 128 (as the
+// head_dim 128 bf16 forward), one at D = 256 (its O takes 256 TMEM columns).
+// Each pipeline has its Q tile, a ring of NST K / Vt tiles and, in TMEM, its
+// O (D columns) and one S buffer (128; P8 is written back into it for the
+// P8 V MMA). A Q or K tile is D / 128 atoms of 128 rows x 128 one-byte
+// columns; a Vt tile is D rows of 128 keys.
+template <int D>
+struct F8Cfg {
+  static constexpr int NPIPE = D == 128 ? 2 : 1;
+  static constexpr int ATOMS = D / 128;
+  static constexpr int TILE = 128 * D;  // bytes of a Q, K or Vt tile
+  static constexpr int NST = 4;
+  static constexpr int PIPE_BYTES = TILE + NST * TILE;  // per pipeline, 1024-aligned
+  static constexpr int PIPE_BARS = 2 * NST + 12;         // mbarriers + queue per pipeline (8 bytes each)
+  static constexpr int SMEM = 1024 + NPIPE * PIPE_BYTES + NPIPE * PIPE_BARS * 8 + 32;
+  static constexpr uint32_t TM_O = 0, TM_S = D, TM_PIPE = 256;
+  static_assert(SMEM <= 232448, "shared memory per CTA");
+  static_assert(NPIPE * (D + 128) <= 512, "TMEM columns");
+};
 constexpr int F8_THREADS = 384;
 constexpr int F8_REGS_SOFTMAX = 192, F8_REGS_OTHER = 120;
 static_assert(2 * F8_REGS_SOFTMAX + F8_REGS_OTHER <= 3 * 168, "register split");
-constexpr uint32_t F8_TM_O = 0, F8_TM_S = 128, F8_TM_PIPE = 256;
 constexpr float kLog2_448 = 8.807354922057604f;  // log2(448)
 constexpr float kLn448 = 6.104793232414985f;     // ln(448)
 
@@ -111,11 +121,12 @@ __device__ __forceinline__ int vt_row0(const Geom& g, int b, const SeqInfo& si) 
 // Vt[head][d][vt_row0(b) + key] = V[key row][head][d] for every key of every
 // sequence; the rows from the end of a sequence's keys up to the next
 // sequence's first row (and up to vt_rows after the last) are zeroed. One
-// block per (128-key slice, kv head, sequence).
+// block per (128-key slice, (kv head, 128-column slice of d), sequence).
 __global__ void __launch_bounds__(256) vt_kernel(const Fp8Params p) {
   const Geom& g = p.g;
   if (p.guard && *reinterpret_cast<volatile const int*>(p.guard)) return;
-  const int b = blockIdx.z, h = blockIdx.y, k0 = blockIdx.x * 128;
+  const int dsl = g.d / 128;
+  const int b = blockIdx.z, h = blockIdx.y / dsl, d0 = (blockIdx.y % dsl) * 128, k0 = blockIdx.x * 128;
   const SeqInfo si = seq_info(g, b);
   const int r0 = vt_row0(g, b, si);
   int seg;  // rows of this sequence's segment of Vt (a multiple of 16)
@@ -130,7 +141,7 @@ __global__ void __launch_bounds__(256) vt_kernel(const Fp8Params p) {
     const int kk = it >> 3, c = it & 7;
     const int key = k0 + kk;
     uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    const uint8_t* src = p.v + ((long long)(si.krow0 + key) * g.nh_kv + kh) * F8_D + c * 16;
+    const uint8_t* src = p.v + ((long long)(si.krow0 + key) * g.nh_kv + kh) * g.d + d0 + c * 16;
     if (key < si.lk && SDPA_ADDR_OK(g.chk, src, 16)) v = *reinterpret_cast<const uint4*>(src);
     *reinterpret_cast<uint4*>(&t[kk][c * 16]) = v;
   }
@@ -143,7 +154,7 @@ __global__ void __launch_bounds__(256) vt_kernel(const Fp8Params p) {
     for (int e = 0; e < 4; ++e)
       w[e] = (uint32_t)t[c * 16 + 4 * e][d] | ((uint32_t)t[c * 16 + 4 * e + 1][d] << 8) |
              ((uint32_t)t[c * 16 + 4 * e + 2][d] << 16) | ((uint32_t)t[c * 16 + 4 * e + 3][d] << 24);
-    uint8_t* dst = p.vt + ((long long)kh * F8_D + d) * p.vt_rows + r0 + k0 + c * 16;
+    uint8_t* dst = p.vt + ((long long)kh * g.d + d0 + d) * p.vt_rows + r0 + k0 + c * 16;
     if (SDPA_ADDR_OK(g.chk, dst, 16)) *reinterpret_cast<uint4*>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
   }
 }
@@ -180,8 +191,8 @@ __device__ __forceinline__ bool fp8_tile(const Fp8Params& p, int idx, Fp8Tile& t
 struct Pipe8 {
   uint8_t* sQ;
   uint8_t* sStage;
-  uint64_t* full;         // [F8_NST]
-  uint64_t* empty;        // [F8_NST]
+  uint64_t* full;         // [NST]
+  uint64_t* empty;        // [NST]
   uint64_t* bar_q;        // Q of a tile landed
   uint64_t* bar_s;        // S of a step ready
   uint64_t* bar_p;        // the softmax is done with a step (pass 2: P8 written)
@@ -193,14 +204,16 @@ struct Pipe8 {
   int* sched;             // [2] ticket, or -1 when the work is out
 };
 
+template <int D>
 __device__ __forceinline__ Pipe8 pipe8_at(uint8_t* smem, int x) {
+  using C = F8Cfg<D>;
   Pipe8 P;
-  P.sQ = smem + x * F8_PIPE_BYTES;
-  P.sStage = P.sQ + F8_TILE;
-  uint64_t* b = reinterpret_cast<uint64_t*>(smem + 2 * F8_PIPE_BYTES) + x * F8_PIPE_BARS;
+  P.sQ = smem + x * C::PIPE_BYTES;
+  P.sStage = P.sQ + C::TILE;
+  uint64_t* b = reinterpret_cast<uint64_t*>(smem + C::NPIPE * C::PIPE_BYTES) + x * C::PIPE_BARS;
   P.full = b;
-  P.empty = b + F8_NST;
-  P.bar_q = b + 2 * F8_NST;
+  P.empty = b + C::NST;
+  P.bar_q = b + 2 * C::NST;
   P.bar_s = P.bar_q + 1;
   P.bar_p = P.bar_q + 2;
   P.bar_o = P.bar_q + 3;
@@ -223,25 +236,26 @@ __device__ __forceinline__ Pipe8 pipe8_at(uint8_t* smem, int x) {
 // query row, all 128 keys of a step), warps 8 / 9 TMA producer and scheduler
 // of pipeline 0 / 1, warp 10 TMEM allocator + MMA issuer, warp 11 only
 // completes the third warpgroup. Every barrier phase counts across tiles.
-template <bool BF16>
+template <bool BF16, int D>
 __global__ void __launch_bounds__(F8_THREADS, 1)
     fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmVt, const __grid_constant__ Fp8Params p) {
   using E = Elem<BF16>;
+  using C = F8Cfg<D>;
   const Geom& g = p.g;
   if (p.guard && *reinterpret_cast<volatile const int*>(p.guard)) return;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint64_t* bar_drain = reinterpret_cast<uint64_t*>(smem + 2 * F8_PIPE_BYTES) + 2 * F8_PIPE_BARS;
+  uint64_t* bar_drain = reinterpret_cast<uint64_t*>(smem + C::NPIPE * C::PIPE_BYTES) + C::NPIPE * C::PIPE_BARS;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
-    for (int x = 0; x < 2; ++x) {
-      const Pipe8 P = pipe8_at(smem, x);
-      for (int i = 0; i < F8_NST; ++i) {
+    for (int x = 0; x < C::NPIPE; ++x) {
+      const Pipe8 P = pipe8_at<D>(smem, x);
+      for (int i = 0; i < C::NST; ++i) {
         mbar_init(&P.full[i], 1);
         mbar_init(&P.empty[i], 1);
       }
@@ -271,10 +285,10 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
 
   if (warp >= 8) {
     regs_dec<F8_REGS_OTHER>();
-    if (warp == 8 || warp == 9) {
+    if (warp == 8 || (warp == 9 && C::NPIPE == 2)) {
       // ---------------------------------------------------------- scheduler + producer of pipeline warp - 8
       if (elect_one()) {
-        const Pipe8 P = pipe8_at(smem, warp - 8);
+        const Pipe8 P = pipe8_at<D>(smem, warp - 8);
         prefetch_tmap(&tmQ);
         prefetch_tmap(&tmK);
         prefetch_tmap(&tmVt);
@@ -284,11 +298,17 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
         auto take = [&]() {
           return SDPA_ADDR_OK(g.chk, p.tile_counter, 4) ? atomicAdd(p.tile_counter, 1) : p.total_tiles;
         };
-        auto load = [&](const CUtensorMap* m, int c0, int c1, int c2) -> bool {
-          const int slot = c % F8_NST;
-          if (!mbar_wait(&P.empty[slot], ((c / F8_NST) & 1) ^ 1, abort_flag)) return false;
-          mbar_arrive_expect_tx(&P.full[slot], F8_TILE);
-          tma_load_3d(m, &P.full[slot], P.sStage + slot * F8_TILE, c0, c1, c2);
+        // one ring stage: a K tile (D / 128 boxes of 128 columns) or a Vt tile (one box of D rows)
+        auto load = [&](bool vt, int c0, int c1, int c2) -> bool {
+          const int slot = c % C::NST;
+          if (!mbar_wait(&P.empty[slot], ((c / C::NST) & 1) ^ 1, abort_flag)) return false;
+          mbar_arrive_expect_tx(&P.full[slot], C::TILE);
+          uint8_t* dst = P.sStage + slot * C::TILE;
+          if (vt) {
+            tma_load_3d(&tmVt, &P.full[slot], dst, c0, c1, c2);
+          } else {
+            for (int a = 0; a < C::ATOMS; ++a) tma_load_3d(&tmK, &P.full[slot], dst + a * 16384, c0 + a * 128, c1, c2);
+          }
           ++c;
           return true;
         };
@@ -312,15 +332,16 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(P.bar_q, F8_TILE);
-          tma_load_3d(&tmQ, P.bar_q, P.sQ, 0, t.qhead, t.si.qrow0 + t.q0);
+          mbar_arrive_expect_tx(P.bar_q, C::TILE);
+          for (int a = 0; a < C::ATOMS; ++a)
+            tma_load_3d(&tmQ, P.bar_q, P.sQ + a * 16384, a * 128, t.qhead, t.si.qrow0 + t.q0);
           ++nq;
           // in the order the MMA issuer consumes: per step, K of its key tile
           // and, in pass 2, then Vt of it
           for (int u = 0; u < 2 * t.n && ok; ++u) {
             const int j = u < t.n ? u : u - t.n;
-            ok = load(&tmK, 0, t.khead, t.si.krow0 + (t.t_lo + j) * F8_BN);
-            if (ok && u >= t.n) ok = load(&tmVt, t.vrow0 + (t.t_lo + j) * F8_BN, 0, t.khead);
+            ok = load(false, 0, t.khead, t.si.krow0 + (t.t_lo + j) * F8_BN);
+            if (ok && u >= t.n) ok = load(true, t.vrow0 + (t.t_lo + j) * F8_BN, 0, t.khead);
           }
           if (!ok) break;
         }
@@ -328,24 +349,24 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
           *abort_flag = 1;
           record_error(p.err, SDPA_ERR_TIMEOUT);
         }
-        const int first = c > F8_NST ? c - F8_NST : 0;
-        for (int k = first; k < c; ++k) mbar_wait_drain(&P.full[k % F8_NST], (k / F8_NST) & 1);
+        const int first = c > C::NST ? c - C::NST : 0;
+        for (int k = first; k < c; ++k) mbar_wait_drain(&P.full[k % C::NST], (k / C::NST) & 1);
         if (nq > 0) mbar_wait_drain(P.bar_q, (nq - 1) & 1);
       }
     } else if (warp == 10) {
       // ---------------------------------------------------------- MMA issuer for both pipelines
       if (elect_one()) {
-        constexpr uint32_t IDESC = idesc_e4m3(128, 128);
+        constexpr uint32_t IDESC_S = idesc_e4m3(128, 128), IDESC_O = idesc_e4m3(128, D);
         struct State {
           int w, c, nq, steps, no, n, u;
           bool done;
         };
         State st[2];
-        for (int x = 0; x < 2; ++x) st[x] = State{0, 0, 0, 0, 0, 0, 0, false};
+        for (int x = 0; x < 2; ++x) st[x] = State{0, 0, 0, 0, 0, 0, 0, x >= C::NPIPE};
         bool ok = true;
         // next tile with keys of pipeline x (false: its work is out, or a wait failed)
         auto next_item = [&](int x) -> bool {
-          const Pipe8 P = pipe8_at(smem, x);
+          const Pipe8 P = pipe8_at<D>(smem, x);
           State& m = st[x];
           while (true) {
             const int e = m.w & 1;
@@ -377,16 +398,18 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
         // S of step u of pipeline x (its previous step's P8 V has been issued,
         // so P8 in the S buffer is consumed first)
         auto issue_s = [&](int x) -> bool {
-          const Pipe8 P = pipe8_at(smem, x);
+          const Pipe8 P = pipe8_at<D>(smem, x);
           State& m = st[x];
-          const int slot = m.c % F8_NST;
-          if (!mbar_wait(&P.full[slot], (m.c / F8_NST) & 1, abort_flag)) return false;
+          const int slot = m.c % C::NST;
+          if (!mbar_wait(&P.full[slot], (m.c / C::NST) & 1, abort_flag)) return false;
           tc_fence_after();
-          const uint32_t q_base = smem_u32(P.sQ), kb = smem_u32(P.sStage + slot * F8_TILE);
+          const uint32_t q_base = smem_u32(P.sQ), kb = smem_u32(P.sStage + slot * C::TILE);
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks)  // 32 one-byte columns per MMA
-            mma_f8_ss(tmem + x * F8_TM_PIPE + F8_TM_S, smem_desc_sw128(q_base + ks * 32, 16, 1024),
-                      smem_desc_sw128(kb + ks * 32, 16, 1024), IDESC, ks != 0);
+          for (int ks = 0; ks < D / 32; ++ks) {  // 32 one-byte columns per MMA, four per 128-column atom
+            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+            mma_f8_ss(tmem + x * C::TM_PIPE + C::TM_S, smem_desc_sw128(q_base + off, 16, 1024),
+                      smem_desc_sw128(kb + off, 16, 1024), IDESC_S, ks != 0);
+          }
           mma_commit(&P.empty[slot]);
           if (m.u == 2 * m.n - 1) mma_commit(P.q_free);
           mma_commit(P.bar_s);
@@ -397,26 +420,26 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
         // tile's first P8 V overwrites O, which the previous tile's epilogue
         // must have read)
         auto after_softmax = [&](int x) -> bool {
-          const Pipe8 P = pipe8_at(smem, x);
+          const Pipe8 P = pipe8_at<D>(smem, x);
           State& m = st[x];
           if (m.u == m.n && m.no > 0 && !mbar_wait(P.o_free, (m.no - 1) & 1, abort_flag)) return false;
           if (!mbar_wait(P.bar_p, m.steps & 1, abort_flag)) return false;
           ++m.steps;
           if (m.u < m.n) return true;  // pass 1: the max only
-          const int slot = m.c % F8_NST;
-          if (!mbar_wait(&P.full[slot], (m.c / F8_NST) & 1, abort_flag)) return false;
+          const int slot = m.c % C::NST;
+          if (!mbar_wait(&P.full[slot], (m.c / C::NST) & 1, abort_flag)) return false;
           tc_fence_after();
-          const uint32_t vb = smem_u32(P.sStage + slot * F8_TILE);
-          const uint32_t pcol = tmem + x * F8_TM_PIPE + F8_TM_S;
+          const uint32_t vb = smem_u32(P.sStage + slot * C::TILE);
+          const uint32_t pcol = tmem + x * C::TM_PIPE + C::TM_S;
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks)  // 32 keys per MMA: 8 TMEM columns of packed P8
-            mma_f8_ts(tmem + x * F8_TM_PIPE + F8_TM_O, pcol + ks * 8, smem_desc_sw128(vb + ks * 32, 16, 1024),
-                      IDESC, (m.u - m.n) > 0 || ks != 0);
+          for (int ks = 0; ks < 4; ++ks)  // 32 keys per MMA: 8 TMEM columns of packed P8; N = D rows of Vt
+            mma_f8_ts(tmem + x * C::TM_PIPE + C::TM_O, pcol + ks * 8, smem_desc_sw128(vb + ks * 32, 16, 1024),
+                      IDESC_O, (m.u - m.n) > 0 || ks != 0);
           mma_commit(&P.empty[slot]);
           ++m.c;
           return true;
         };
-        for (int x = 0; x < 2 && ok; ++x)
+        for (int x = 0; x < C::NPIPE && ok; ++x)
           if (next_item(x) && !issue_s(x)) ok = false;
         while (ok && !(st[0].done && st[1].done)) {
           for (int x = 0; x < 2 && ok; ++x) {
@@ -427,7 +450,7 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
               break;
             }
             if (m.u == 2 * m.n - 1) {
-              mma_commit(pipe8_at(smem, x).bar_o);
+              mma_commit(pipe8_at<D>(smem, x).bar_o);
               ++m.no;
               if (!next_item(x)) continue;  // out of work (or ok cleared)
             } else {
@@ -447,163 +470,166 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
   } else {
     regs_inc<F8_REGS_SOFTMAX>();
     // ------------------------------------------------------------ softmax + epilogue of pipeline warp / 4
+    // (one pipeline at head_dim 256: warps 4-7 have no work)
     const int x = warp >> 2;
-    const Pipe8 P = pipe8_at(smem, x);
-    const int r = (warp & 3) * 32 + lane;
-    const uint32_t lane_base = tmem + x * F8_TM_PIPE + ((uint32_t)((warp & 3) * 32) << 16);
-    const uint32_t scol = lane_base + F8_TM_S;
-    const float sl2 = g.scale_log2;
-    using T = typename E::T;
-    int w = 0, steps = 0, no = 0;
-    bool ok = true;
-    while (ok) {
-      const int e = w & 1;
-      if (!__all_sync(0xffffffffu, mbar_wait(&P.sched_full[e], (w >> 1) & 1, abort_flag))) {
-        ok = false;
-        break;
-      }
-      const int item = *reinterpret_cast<volatile int*>(&P.sched[e]);
-      mbar_arrive(&P.sched_empty[e]);
-      ++w;
-      if (item < 0) break;
-      Fp8Tile t;
-      fp8_tile(p, item, t);
-      const int n = t.n;
-      const int i = t.q0 + r;
-      const bool valid = i < t.si.lq;
-      const int lo_i = t.kr.lo(i), hi_i = t.kr.hi(i);
-      const int lo_last = t.kr.lo(t.q_last), hi_first = t.kr.hi(t.q0);
-      T* orow = reinterpret_cast<T*>(p.o) + ((long long)(t.si.qrow0 + i) * g.nh_q + t.qhead) * F8_D;
-      float* lse_at = p.lse + (long long)(t.si.qrow0 + i) * g.nh_q + t.qhead;
-      if (n == 0) {  // no key for any row of the tile: O = 0, LSE = -inf
-        if (valid && SDPA_ADDR_OK(g.chk, orow, 256)) {
-          uint4* dst = reinterpret_cast<uint4*>(orow);
-#pragma unroll
-          for (int k2 = 0; k2 < 16; ++k2) dst[k2] = make_uint4(0u, 0u, 0u, 0u);
-        }
-        if (valid && SDPA_ADDR_OK(g.chk, lse_at, 4)) *lse_at = -INFINITY;
-        continue;
-      }
-      // pass 1: the row max, four independent chains; pass 2: the exponent's
-      // bias log2(448) - m * scale * log2e, so exp2 gives 448 P~ directly,
-      // and the sum of 448 P~ (two lanes)
-      float mm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      float m = -INFINITY, nb = 0.f;
-      float2 l2 = make_float2(0.f, 0.f);
-      for (int u = 0; u < 2 * n; ++u) {
-        if (!__all_sync(0xffffffffu, mbar_wait(P.bar_s, steps & 1, abort_flag))) {
+    if (x < C::NPIPE) {
+      const Pipe8 P = pipe8_at<D>(smem, x);
+      const int r = (warp & 3) * 32 + lane;
+      const uint32_t lane_base = tmem + x * C::TM_PIPE + ((uint32_t)((warp & 3) * 32) << 16);
+      const uint32_t scol = lane_base + C::TM_S;
+      const float sl2 = g.scale_log2;
+      using T = typename E::T;
+      int w = 0, steps = 0, no = 0;
+      bool ok = true;
+      while (ok) {
+        const int e = w & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(&P.sched_full[e], (w >> 1) & 1, abort_flag))) {
           ok = false;
           break;
         }
-        ++steps;
-        tc_fence_after();
-        const int kb = (t.t_lo + (u < n ? u : u - n)) * F8_BN;
-        const bool edge = !(lo_last <= kb && hi_first >= kb + F8_BN);  // uniform across the tile
-        if (u < n && !edge) {
-          // interior pass-1 step: the row max comes with the loads
-          uint32_t u0[32], u1[32], u2[32], u3[32];
-          float x0, x1, x2, x3;
-          tmem_ld32_max(scol, u0, x0);
-          tmem_ld32_max(scol + 32, u1, x1);
-          tmem_ld32_max(scol + 64, u2, x2);
-          tmem_ld32_max(scol + 96, u3, x3);
-          tmem_wait_ld();
-          asm volatile("" : "+f"(x0), "+f"(x1), "+f"(x2), "+f"(x3));
-          mm[0] = fmaxf(mm[0], x0);
-          mm[1] = fmaxf(mm[1], x1);
-          mm[2] = fmaxf(mm[2], x2);
-          mm[3] = fmaxf(mm[3], x3);
-        } else {
-          float s[128];
-          {
+        const int item = *reinterpret_cast<volatile int*>(&P.sched[e]);
+        mbar_arrive(&P.sched_empty[e]);
+        ++w;
+        if (item < 0) break;
+        Fp8Tile t;
+        fp8_tile(p, item, t);
+        const int n = t.n;
+        const int i = t.q0 + r;
+        const bool valid = i < t.si.lq;
+        const int lo_i = t.kr.lo(i), hi_i = t.kr.hi(i);
+        const int lo_last = t.kr.lo(t.q_last), hi_first = t.kr.hi(t.q0);
+        T* orow = reinterpret_cast<T*>(p.o) + ((long long)(t.si.qrow0 + i) * g.nh_q + t.qhead) * D;
+        float* lse_at = p.lse + (long long)(t.si.qrow0 + i) * g.nh_q + t.qhead;
+        if (n == 0) {  // no key for any row of the tile: O = 0, LSE = -inf
+          if (valid && SDPA_ADDR_OK(g.chk, orow, 2 * D)) {
+            uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+            for (int k2 = 0; k2 < D / 8; ++k2) dst[k2] = make_uint4(0u, 0u, 0u, 0u);
+          }
+          if (valid && SDPA_ADDR_OK(g.chk, lse_at, 4)) *lse_at = -INFINITY;
+          continue;
+        }
+        // pass 1: the row max, four independent chains; pass 2: the exponent's
+        // bias log2(448) - m * scale * log2e, so exp2 gives 448 P~ directly,
+        // and the sum of 448 P~ (two lanes)
+        float mm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        float m = -INFINITY, nb = 0.f;
+        float2 l2 = make_float2(0.f, 0.f);
+        for (int u = 0; u < 2 * n; ++u) {
+          if (!__all_sync(0xffffffffu, mbar_wait(P.bar_s, steps & 1, abort_flag))) {
+            ok = false;
+            break;
+          }
+          ++steps;
+          tc_fence_after();
+          const int kb = (t.t_lo + (u < n ? u : u - n)) * F8_BN;
+          const bool edge = !(lo_last <= kb && hi_first >= kb + F8_BN);  // uniform across the tile
+          if (u < n && !edge) {
+            // interior pass-1 step: the row max comes with the loads
             uint32_t u0[32], u1[32], u2[32], u3[32];
-            tmem_ld32(scol, u0);
-            tmem_ld32(scol + 32, u1);
-            tmem_ld32(scol + 64, u2);
-            tmem_ld32(scol + 96, u3);
+            float x0, x1, x2, x3;
+            tmem_ld32_max(scol, u0, x0);
+            tmem_ld32_max(scol + 32, u1, x1);
+            tmem_ld32_max(scol + 64, u2, x2);
+            tmem_ld32_max(scol + 96, u3, x3);
             tmem_wait_ld();
-            reg_fence(u0);
-            reg_fence(u1);
-            reg_fence(u2);
-            reg_fence(u3);
-#pragma unroll
-            for (int cc = 0; cc < 32; ++cc) {
-              s[cc] = __uint_as_float(u0[cc]);
-              s[32 + cc] = __uint_as_float(u1[cc]);
-              s[64 + cc] = __uint_as_float(u2[cc]);
-              s[96 + cc] = __uint_as_float(u3[cc]);
-            }
-          }
-          if (edge) {
-#pragma unroll
-            for (int cc = 0; cc < 128; ++cc) s[cc] = in_range(kb + cc, lo_i, hi_i) ? s[cc] : -INFINITY;
-          }
-          if (u < n) {
-#pragma unroll
-            for (int cc = 0; cc < 128; ++cc) mm[cc & 3] = fmaxf(mm[cc & 3], s[cc]);
+            asm volatile("" : "+f"(x0), "+f"(x1), "+f"(x2), "+f"(x3));
+            mm[0] = fmaxf(mm[0], x0);
+            mm[1] = fmaxf(mm[1], x1);
+            mm[2] = fmaxf(mm[2], x2);
+            mm[3] = fmaxf(mm[3], x3);
           } else {
-            uint32_t pk[32];
-            const float2 sc2 = make_float2(sl2, sl2), nb2 = make_float2(nb, nb);
-            float2 ra = make_float2(0.f, 0.f), rb = make_float2(0.f, 0.f);
+            float s[128];
+            {
+              uint32_t u0[32], u1[32], u2[32], u3[32];
+              tmem_ld32(scol, u0);
+              tmem_ld32(scol + 32, u1);
+              tmem_ld32(scol + 64, u2);
+              tmem_ld32(scol + 96, u3);
+              tmem_wait_ld();
+              reg_fence(u0);
+              reg_fence(u1);
+              reg_fence(u2);
+              reg_fence(u3);
 #pragma unroll
-            for (int cc = 0; cc < 32; ++cc) {
-              const float2 ta = ffma2(make_float2(s[4 * cc], s[4 * cc + 1]), sc2, nb2);
-              const float2 tb = ffma2(make_float2(s[4 * cc + 2], s[4 * cc + 3]), sc2, nb2);
-              const float2 pa = make_float2(ex2(ta.x), ex2(ta.y)), pb = make_float2(ex2(tb.x), ex2(tb.y));
-              ra = fadd2(ra, pa);
-              rb = fadd2(rb, pb);
-              pk[cc] = pack_e4m3x4(pa.x, pa.y, pb.x, pb.y);  // 448 P~, rounded once to E4M3
+              for (int cc = 0; cc < 32; ++cc) {
+                s[cc] = __uint_as_float(u0[cc]);
+                s[32 + cc] = __uint_as_float(u1[cc]);
+                s[64 + cc] = __uint_as_float(u2[cc]);
+                s[96 + cc] = __uint_as_float(u3[cc]);
+              }
             }
-            l2 = fadd2(l2, fadd2(ra, rb));
-            tmem_st32(scol, pk);  // P8 into the S buffer's first 32 columns
-            tmem_wait_st();
+            if (edge) {
+#pragma unroll
+              for (int cc = 0; cc < 128; ++cc) s[cc] = in_range(kb + cc, lo_i, hi_i) ? s[cc] : -INFINITY;
+            }
+            if (u < n) {
+#pragma unroll
+              for (int cc = 0; cc < 128; ++cc) mm[cc & 3] = fmaxf(mm[cc & 3], s[cc]);
+            } else {
+              uint32_t pk[32];
+              const float2 sc2 = make_float2(sl2, sl2), nb2 = make_float2(nb, nb);
+              float2 ra = make_float2(0.f, 0.f), rb = make_float2(0.f, 0.f);
+#pragma unroll
+              for (int cc = 0; cc < 32; ++cc) {
+                const float2 ta = ffma2(make_float2(s[4 * cc], s[4 * cc + 1]), sc2, nb2);
+                const float2 tb = ffma2(make_float2(s[4 * cc + 2], s[4 * cc + 3]), sc2, nb2);
+                const float2 pa = make_float2(ex2(ta.x), ex2(ta.y)), pb = make_float2(ex2(tb.x), ex2(tb.y));
+                ra = fadd2(ra, pa);
+                rb = fadd2(rb, pb);
+                pk[cc] = pack_e4m3x4(pa.x, pa.y, pb.x, pb.y);  // 448 P~, rounded once to E4M3
+              }
+              l2 = fadd2(l2, fadd2(ra, rb));
+              tmem_st32(scol, pk);  // P8 into the S buffer's first 32 columns
+              tmem_wait_st();
+            }
+          }
+          if (u == n - 1) {
+            m = fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3]));
+            nb = kLog2_448 - (m == -INFINITY ? 0.f : m * sl2);
+          }
+          tc_fence_before();
+          mbar_arrive(P.bar_p);
+        }
+        if (!ok) break;
+        // epilogue: O / the row sum, 32 columns at a time; O is free for the
+        // next tile's first P8 V once the last chunk has been read
+        if (!__all_sync(0xffffffffu, mbar_wait(P.bar_o, no & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        ++no;
+        tc_fence_after();
+        const float l = l2.x + l2.y;  // the sum of 448 P~
+        const float mul = l > 0.f ? p.o_scale * 448.f / l : 0.f;  // o_scale = d_v / 448
+#pragma unroll 1
+        for (int cc = 0; cc < D / 32; ++cc) {
+          uint32_t uu[32];
+          tmem_ld32(lane_base + C::TM_O + cc * 32, uu);
+          tmem_wait_ld();
+          reg_fence(uu);
+          if (cc == D / 32 - 1) {
+            tc_fence_before();
+            mbar_arrive(P.o_free);
+          }
+          uint32_t packed[16];
+#pragma unroll
+          for (int k2 = 0; k2 < 16; ++k2)
+            packed[k2] = E::pack(__uint_as_float(uu[2 * k2]) * mul, __uint_as_float(uu[2 * k2 + 1]) * mul);
+          if (valid && SDPA_ADDR_OK(g.chk, orow + cc * 32, 64)) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+#pragma unroll
+            for (int k2 = 0; k2 < 4; ++k2)
+              dst[k2] = make_uint4(packed[4 * k2], packed[4 * k2 + 1], packed[4 * k2 + 2], packed[4 * k2 + 3]);
           }
         }
-        if (u == n - 1) {
-          m = fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3]));
-          nb = kLog2_448 - (m == -INFINITY ? 0.f : m * sl2);
-        }
-        tc_fence_before();
-        mbar_arrive(P.bar_p);
+        if (valid && SDPA_ADDR_OK(g.chk, lse_at, 4))
+          *lse_at = l > 0.f ? m * g.scale + (logf(l) - kLn448) : -INFINITY;
       }
-      if (!ok) break;
-      // epilogue: O / the row sum, 32 columns at a time; O is free for the
-      // next tile's first P8 V once the last chunk has been read
-      if (!__all_sync(0xffffffffu, mbar_wait(P.bar_o, no & 1, abort_flag))) {
-        ok = false;
-        break;
+      if (!ok) {
+        *abort_flag = 1;
+        record_error(p.err, SDPA_ERR_TIMEOUT);
       }
-      ++no;
-      tc_fence_after();
-      const float l = l2.x + l2.y;  // the sum of 448 P~
-      const float mul = l > 0.f ? p.o_scale * 448.f / l : 0.f;  // o_scale = d_v / 448
-#pragma unroll 1
-      for (int cc = 0; cc < 4; ++cc) {
-        uint32_t uu[32];
-        tmem_ld32(lane_base + F8_TM_O + cc * 32, uu);
-        tmem_wait_ld();
-        reg_fence(uu);
-        if (cc == 3) {
-          tc_fence_before();
-          mbar_arrive(P.o_free);
-        }
-        uint32_t packed[16];
-#pragma unroll
-        for (int k2 = 0; k2 < 16; ++k2)
-          packed[k2] = E::pack(__uint_as_float(uu[2 * k2]) * mul, __uint_as_float(uu[2 * k2 + 1]) * mul);
-        if (valid && SDPA_ADDR_OK(g.chk, orow + cc * 32, 64)) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
-#pragma unroll
-          for (int k2 = 0; k2 < 4; ++k2)
-            dst[k2] = make_uint4(packed[4 * k2], packed[4 * k2 + 1], packed[4 * k2 + 2], packed[4 * k2 + 3]);
-        }
-      }
-      if (valid && SDPA_ADDR_OK(g.chk, lse_at, 4))
-        *lse_at = l > 0.f ? m * g.scale + (logf(l) - kLn448) : -INFINITY;
-    }
-    if (!ok) {
-      *abort_flag = 1;
-      record_error(p.err, SDPA_ERR_TIMEOUT);
     }
   }
 
@@ -619,8 +645,26 @@ int launch_vt(const Fp8Params& p, cudaStream_t stream) {
   const int max_seg = p.g.layout == SDPA_THD ? p.g.sk + 32 : ((p.g.sk + 15) & ~15);
   if (p.g.batch <= 0 || max_seg <= 0) return SDPA_OK;
   if (p.g.batch > 65535 || p.g.hkv > 65535) return SDPA_ERR_UNSUPPORTED;
-  const dim3 grid((unsigned)((max_seg + 127) / 128), (unsigned)p.g.hkv, (unsigned)p.g.batch);
+  if ((long long)p.g.hkv * (p.g.d / 128) > 65535) return SDPA_ERR_UNSUPPORTED;
+  const dim3 grid((unsigned)((max_seg + 127) / 128), (unsigned)(p.g.hkv * (p.g.d / 128)), (unsigned)p.g.batch);
   vt_kernel<<<grid, 256, 0, stream>>>(p);
+  return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+}
+
+template <bool BF16, int D>
+static int launch_fwd_fp8_t(const Fp8Launch& L, long long tiles) {
+  using C = F8Cfg<D>;
+  auto kern = fwd_fp8_kernel<BF16, D>;
+  if (const int rc = set_kernel_smem(reinterpret_cast<const void*>(kern), C::SMEM, 100)) return rc;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return SDPA_ERR_CUDA;
+  Fp8Params p = L.p;
+  p.total_tiles = (int)tiles;
+  long long grid = std::min<long long>((tiles + C::NPIPE - 1) / C::NPIPE, sms);
+  if (debug_max_ctas() > 0) grid = std::min<long long>(grid, debug_max_ctas());  // tickets cover every tile
+  if (cudaMemsetAsync(p.tile_counter, 0, sizeof(int), L.stream) != cudaSuccess) return SDPA_ERR_CUDA;
+  kern<<<(unsigned)grid, F8_THREADS, C::SMEM, L.stream>>>(L.tmQ, L.tmK, L.tmVt, p);
   return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }
 
@@ -628,18 +672,9 @@ int launch_fwd_fp8(const Fp8Launch& L, bool bf16) {
   const long long tiles = (long long)L.p.n_q_tiles * L.p.g.hq * L.p.g.batch;
   if (tiles <= 0) return SDPA_OK;
   if (tiles > 0x7fffffffLL - 4096) return SDPA_ERR_UNSUPPORTED;
-  auto kern = bf16 ? fwd_fp8_kernel<true> : fwd_fp8_kernel<false>;
-  if (const int rc = set_kernel_smem(reinterpret_cast<const void*>(kern), F8_SMEM, 100)) return rc;
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-    return SDPA_ERR_CUDA;
-  Fp8Params p = L.p;
-  p.total_tiles = (int)tiles;
-  long long grid = std::min<long long>((tiles + 1) / 2, sms);
-  if (debug_max_ctas() > 0) grid = std::min<long long>(grid, debug_max_ctas());  // tickets cover every tile
-  if (cudaMemsetAsync(p.tile_counter, 0, sizeof(int), L.stream) != cudaSuccess) return SDPA_ERR_CUDA;
-  kern<<<(unsigned)grid, F8_THREADS, F8_SMEM, L.stream>>>(L.tmQ, L.tmK, L.tmVt, p);
-  return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
+  if (L.p.g.d == 128) return bf16 ? launch_fwd_fp8_t<true, 128>(L, tiles) : launch_fwd_fp8_t<false, 128>(L, tiles);
+  if (L.p.g.d == 256) return bf16 ? launch_fwd_fp8_t<true, 256>(L, tiles) : launch_fwd_fp8_t<false, 256>(L, tiles);
+  return SDPA_ERR_UNSUPPORTED;
 }
 
 }  // namespace sdpa

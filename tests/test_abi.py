@@ -153,6 +153,18 @@ def test_workspace_sizes(pkg):
     assert 0 < det < ws and ws - det >= 2 * 256 * 8 * 128 * 4
 
 
+def test_fp8_workspace_sizes(pkg):
+    # guard word and ticket counter (256 bytes), then V transposed to [Hkv][D][keys]: BSHD rounds each
+    # sequence's keys up to 16
+    for d in (128, 256):
+        assert pkg.sdpa_fwd_fp8_workspace_size(problem(pkg, head_dim=d, seqlen_kv=250)) == 256 + 2 * d * 2 * 256
+    # THD: every sequence starts on a multiple of 16 (total + 16 per sequence, rounded up)
+    t = problem(pkg, head_dim=256, layout=2, total_q=1000, total_kv=1000)
+    assert pkg.sdpa_fwd_fp8_workspace_size(t) == 256 + 2 * 256 * 1040
+    for d, dv in ((512, 0), (192, 128), (256, 128)):
+        assert pkg.sdpa_fwd_fp8_workspace_size(problem(pkg, head_dim=d, head_dim_v=dv)) == 0
+
+
 def test_kv_chunk_is_validated(pkg):
     for bad in (-128, 1, 100, 129):
         assert pkg.sdpa_check_problem(problem(pkg, head_dim=512, kv_chunk=bad)) == 1

@@ -97,11 +97,15 @@ def test_checked_library_other_entry_points():
     w = Workload("noalloc_thd", "thd", "causal", 3, 200, 200, 4, 2, 128, "bf16", len_range=(1, 200))
     inp = workloads.make_inputs(w, seed=85)
     ref = _fwd_bwd(w, inp, {}, noalloc=True)
-    # FP8 forward
+    # FP8 forward, head_dim 128 and 256
     wf = Workload("fp8_thd", "thd", "causal", 3, 300, 300, 4, 2, 128, "bf16", len_range=(1, 300))
     f8 = workloads.fp8_inputs(wf, seed=87)
     q8, k8, v8 = (torch.from_numpy(f8[x]).cuda() for x in ("q8", "k8", "v8"))
     ref8 = sdpa.sdpa_fwd_fp8(q8, k8, v8, descale=workloads.FP8_DESCALE, **gpu_kwargs(wf, f8))
+    wf2 = Workload("fp8_d256_bshd", "bshd", "causal", 2, 300, 300, 4, 2, 256, "bf16")
+    f82 = workloads.fp8_inputs(wf2, seed=88)
+    q82, k82, v82 = (torch.from_numpy(f82[x]).cuda() for x in ("q8", "k8", "v8"))
+    ref82 = sdpa.sdpa_fwd_fp8(q82, k82, v82, descale=workloads.FP8_DESCALE, **gpu_kwargs(wf2, f82))
     # 192/128 forward
     wa = Workload("asym", "thd", "causal", 3, 200, 200, 4, 2, 192, "bf16", len_range=(1, 200), head_dim_v=128)
     ia = workloads.make_inputs(wa, seed=89)
@@ -118,12 +122,15 @@ def test_checked_library_other_entry_points():
         _no_violations()
         got8 = sdpa.sdpa_fwd_fp8(q8, k8, v8, descale=workloads.FP8_DESCALE, **gpu_kwargs(wf, f8))
         _no_violations()
+        got82 = sdpa.sdpa_fwd_fp8(q82, k82, v82, descale=workloads.FP8_DESCALE, **gpu_kwargs(wf2, f82))
+        _no_violations()
         gota = sdpa.sdpa_fwd(qa, ka, va, **gpu_kwargs(wa, ia))
         _no_violations()
         gotm = sdpa.sdpa_merge(parts, lses)
         _no_violations()
     _same(got[:2] + got[3:], ref[:2] + ref[3:])
     _same(got8, ref8)
+    _same(got82, ref82)
     _same(gota, refa)
     _same(gotm, refm)
 

@@ -1,4 +1,4 @@
-"""FP8 E4M3 forward (sdpa_fwd_fp8, head_dim 128) against the float64 oracle.
+"""FP8 E4M3 forward (sdpa_fwd_fp8, head_dim 128 and 256) against the float64 oracle.
 
 The kernel follows the oracle's definition step for step (TransformerEngine
 PR #3705, closing note on FP8: the softmax output is stored in E4M3 under the
@@ -32,6 +32,11 @@ CASES = [
     (Workload("fp8_window", "bshd", "causal", 1, 400, 400, 2, 2, 128, "bf16", window=(100, 0)), None),
     (Workload("fp8_thd_unequal_bottom_right", "thd", "causal_br", 5, 300, 333, 4, 2, 128, "bf16"),
      ([300, 1, 129, 200, 64], [140, 250, 129, 333, 1])),
+    # head_dim 256 (one query-tile pipeline per CTA)
+    (Workload("fp8_d256_bshd_causal_gqa", "bshd", "causal", 2, 300, 300, 4, 2, 256, "bf16"), None),
+    (Workload("fp8_d256_thd_varlen", "thd", "causal", 4, 300, 300, 4, 1, 256, "bf16", len_range=(1, 300)), None),
+    (Workload("fp8_d256_sbhd_window_fp16", "sbhd", "causal", 2, 400, 400, 2, 2, 256, "fp16", window=(100, 0)), None),
+    (Workload("fp8_d256_bottom_right_nomask_rect", "bshd", "none", 1, 200, 333, 2, 1, 256, "bf16"), None),
 ]
 UNIT = {"bf16": 2.0 ** -8, "fp16": 2.0 ** -11}  # unit roundoff of the output format
 
@@ -126,7 +131,7 @@ def test_fp8_forward_matches_oracle(case):
     assert worst <= 1.0, f"O exceeds its bound by {worst:.2f}x"
 
 
-FULL = [workloads.VARLEN_THD, workloads.LONG_FP16]
+FULL = [workloads.VARLEN_THD, workloads.LONG_FP16, workloads.SLIDING]
 
 
 @pytest.mark.slow
@@ -134,42 +139,45 @@ FULL = [workloads.VARLEN_THD, workloads.LONG_FP16]
 def test_fp8_full_size_sampled_rows(w):
     """The FP8 forward at the full workload shapes, in the configuration the
     benchmark times (bf16 O), checked on sampled query rows. Under top-left
-    causal, row i of a sequence sees exactly its keys 0..i, so the oracle
-    checks each sampled row as a one-query problem over those keys with no
-    mask, under the same bound as the small cases."""
+    causal, row i of a sequence sees exactly its keys 0..i (max(0, i - w) ..
+    i under a left window w), so the oracle checks each sampled row as a
+    one-query problem over those keys with no mask, under the same bound as
+    the small cases."""
     import torch
 
     from oracle import oracle
     from parity import gpu_kwargs, kv_token_row, sample_rows, token_row
     from scaled_dot_product_02_gb300 import sdpa_fwd_fp8, sdpa_get_device_error
 
-    assert w.mask == "causal" and w.window == (-1, -1) and w.head_dim == 128
+    assert w.mask == "causal" and w.window[1] in (-1, 0) and w.head_dim in (128, 256)
+    D = w.head_dim
     inp = workloads.fp8_inputs(w)
     kw = gpu_kwargs(w, inp)
     q8, k8, v8 = (torch.from_numpy(inp[x]).cuda() for x in ("q8", "k8", "v8"))
     o, lse = sdpa_fwd_fp8(q8, k8, v8, descale=workloads.FP8_DESCALE, out_dtype=torch.bfloat16, **kw)
     assert sdpa_get_device_error() == 0
-    o = o.float().cpu().numpy().astype(np.float64).reshape(-1, w.heads_q, 128)
+    o = o.float().cpu().numpy().astype(np.float64).reshape(-1, w.heads_q, D)
     lse = lse.cpu().numpy().astype(np.float64).reshape(-1, w.heads_q)
     del q8, k8, v8
     torch.cuda.empty_cache()
 
     group = w.heads_q // w.heads_kv
-    qs, ks, vs = (inp[x].reshape(-1, n, 128) for x, n in (("q8", w.heads_q), ("k8", w.heads_kv), ("v8", w.heads_kv)))
+    qs, ks, vs = (inp[x].reshape(-1, n, D) for x, n in (("q8", w.heads_q), ("k8", w.heads_kv), ("v8", w.heads_kv)))
     dq, dk, _ = workloads.FP8_DESCALE
     okw = dict(layout="bshd", mask="none", scale=w.scale)
     worst, lse_err = 0.0, 0.0
     rows = sample_rows(w, inp, 40, seed=17)
     for b, h, i in rows:
         t = token_row(w, inp, int(b), int(i))
-        kv = np.array([kv_token_row(w, inp, int(b), j) for j in range(int(i) + 1)])
+        j0 = max(0, int(i) - w.window[0]) if w.window[0] >= 0 else 0
+        kv = np.array([kv_token_row(w, inp, int(b), j) for j in range(j0, int(i) + 1)])
         sub = {"q8": qs[t, h][None, None, None, :], "k8": ks[kv, h // group][None, :, None, :],
                "v8": vs[kv, h // group][None, :, None, :]}
-        sw = Workload("row", "bshd", "none", 1, 1, len(kv), 1, 1, 128, "bf16")
+        sw = Workload("row", "bshd", "none", 1, 1, len(kv), 1, 1, D, "bf16")
         o_ref, l_ref = oracle.fwd_fp8(sub["q8"], sub["k8"], sub["v8"], descale=workloads.FP8_DESCALE, **okw)
         probs = oracle.probs(oracle.e4m3_decode(sub["q8"]) * dq, oracle.e4m3_decode(sub["k8"]) * dk, **okw)
-        bound = _bound(sw, sub, probs, o_ref, oracle.e4m3_decode(sub["v8"])).reshape(128)
-        worst = max(worst, float(np.max(np.abs(o[t, h] - o_ref.reshape(128)) / bound)))
+        bound = _bound(sw, sub, probs, o_ref, oracle.e4m3_decode(sub["v8"])).reshape(D)
+        worst = max(worst, float(np.max(np.abs(o[t, h] - o_ref.reshape(D)) / bound)))
         lse_err = max(lse_err, abs(float(lse[t, h]) - float(np.ravel(l_ref)[0])))
     print(f"[{w.name} fp8, {len(rows)} sampled rows] worst err/bound={worst:.3f}; LSE err={lse_err:.3e}")
     assert lse_err <= 1e-4

@@ -73,13 +73,14 @@ def test_results_do_not_depend_on_how_many_ctas_run(case):
         sdpa.sdpa_debug_set_max_ctas(0)
 
 
-def test_fp8_forward_does_not_depend_on_how_many_ctas_run():
+@pytest.mark.parametrize("head_dim", [128, 256])
+def test_fp8_forward_does_not_depend_on_how_many_ctas_run(head_dim):
     import torch
 
     import scaled_dot_product_02_gb300 as sdpa
     from parity import gpu_kwargs
 
-    w = Workload("fp8_thd", "thd", "causal", 3, 300, 300, 4, 2, 128, "bf16", len_range=(1, 300))
+    w = Workload("fp8_thd", "thd", "causal", 3, 300, 300, 4, 2, head_dim, "bf16", len_range=(1, 300))
     inp = workloads.fp8_inputs(w, seed=73)
     q8, k8, v8 = (torch.from_numpy(inp[x]).cuda() for x in ("q8", "k8", "v8"))
     kw = gpu_kwargs(w, inp)
