@@ -27,6 +27,13 @@ BWD_CASES = [
     Workload("d512_fp16_br", "bshd", "causal_br", 1, 200, 333, 2, 1, 512, "fp16", std=0.5),
     Workload("d512_thd_varlen", "thd", "causal", 3, 260, 260, 2, 1, 512, "bf16", len_range=(1, 260)),
     Workload("d256_fp16_thd_nomask", "thd", "none", 3, 200, 200, 2, 2, 256, "fp16", len_range=(1, 200)),
+    # windows at every head dim: two-sided (no causal mask, Sq == Sk), causal at D512, and a
+    # left window measured from the bottom-right diagonal
+    Workload("d256_two_sided_window", "bshd", "none", 1, 300, 300, 2, 2, 256, "bf16", window=(70, 45)),
+    Workload("d512_causal_window", "bshd", "causal", 1, 400, 400, 2, 1, 512, "bf16", window=(150, 0)),
+    Workload("d512_two_sided_window_gqa", "bshd", "none", 1, 260, 260, 4, 2, 512, "bf16", window=(40, 90)),
+    Workload("br_window_d128", "bshd", "causal_br", 1, 200, 333, 2, 1, 128, "bf16", window=(60, 0)),
+    Workload("br_window_d256", "bshd", "causal_br", 1, 200, 333, 2, 1, 256, "bf16", window=(90, 0)),
 ]
 
 

@@ -37,6 +37,8 @@ CASES = [
     (Workload("fp8_d256_thd_varlen", "thd", "causal", 4, 300, 300, 4, 1, 256, "bf16", len_range=(1, 300)), None),
     (Workload("fp8_d256_sbhd_window_fp16", "sbhd", "causal", 2, 400, 400, 2, 2, 256, "fp16", window=(100, 0)), None),
     (Workload("fp8_d256_bottom_right_nomask_rect", "bshd", "none", 1, 200, 333, 2, 1, 256, "bf16"), None),
+    (Workload("fp8_two_sided_window", "bshd", "none", 1, 300, 300, 2, 2, 128, "bf16", window=(70, 45)), None),
+    (Workload("fp8_d256_br_window", "bshd", "causal_br", 1, 200, 333, 2, 1, 256, "bf16", window=(90, 0)), None),
 ]
 UNIT = {"bf16": 2.0 ** -8, "fp16": 2.0 ** -11}  # unit roundoff of the output format
 
