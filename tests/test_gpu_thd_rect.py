@@ -7,7 +7,8 @@ Per sequence b the bottom-right diagonal of query i is key i + Lk_b - Lq_b
 (PR #3527, "Verification": rectangular bottom-right cases), so the lengths
 mix Lq_b > Lk_b (bottom-right: the first Lq_b - Lk_b rows see no key and
 must come back as O = 0, LSE = -inf, dQ = 0), Lq_b < Lk_b, equal lengths, a
-single query and a single key, at head_dim 128, 256 and 512, with GQA.
+single query and a single key, at head_dim 128, 256 and 512, with GQA (up to
+8:1), windows, and empty sequences between live ones.
 """
 import numpy as np
 import pytest
@@ -38,6 +39,12 @@ CASES = [
     _case("d512_bottom_right", "causal_br", 512, heads=(2, 1)),
     _case("d512_top_left", "causal", 512, heads=(2, 2)),
     _case("d512_nomask_fp16", "none", 512, heads=(2, 1), dtype="fp16"),
+    _case("d256_top_left_window", "causal", 256, window=(100, 0)),
+    _case("d512_bottom_right_window", "causal_br", 512, heads=(2, 1), window=(80, 0)),
+    _case("d128_gqa_8_to_1", "causal", 128, heads=(8, 1)),
+    # empty sequences (no query and no key) between live ones
+    _case("d256_with_empty", "causal", 256, heads=(2, 1), lens=([150, 0, 37, 0, 90], [150, 0, 60, 0, 90])),
+    _case("d512_with_empty_br", "causal_br", 512, heads=(2, 2), lens=([0, 120, 0, 33], [0, 200, 0, 33])),
 ]
 
 
@@ -64,7 +71,7 @@ def test_thd_unequal_lengths_match_oracle(case):
     o, lse, dq, dk, dv = _run(w, inp)
     res = check_fwd(w, inp, o, lse) + check_bwd(w, inp, dq, dk, dv)
     report(w.name, res)
-    if w.mask == "causal_br":
+    if w.mask == "causal_br" and lens[0][0] == 300 and lens[1][0] == 140:
         # sequence 0: Lq 300 > Lk 140, so its first 160 rows see no key
         a = int(inp["cu_seqlens_q"][0])
         assert np.all(np.isneginf(lse[a:a + 160])) and np.all(o[a:a + 160] == 0) and np.all(dq[a:a + 160] == 0)
