@@ -39,6 +39,11 @@ CASES = [
     (Workload("fp8_d256_bottom_right_nomask_rect", "bshd", "none", 1, 200, 333, 2, 1, 256, "bf16"), None),
     (Workload("fp8_two_sided_window", "bshd", "none", 1, 300, 300, 2, 2, 128, "bf16", window=(70, 45)), None),
     (Workload("fp8_d256_br_window", "bshd", "causal_br", 1, 200, 333, 2, 1, 256, "bf16", window=(90, 0)), None),
+    # empty sequences between live ones
+    (Workload("fp8_thd_with_empty", "thd", "causal", 5, 150, 150, 4, 2, 128, "bf16"),
+     ([150, 0, 37, 0, 90], [150, 0, 37, 0, 90])),
+    (Workload("fp8_d256_thd_with_empty_br", "thd", "causal_br", 4, 120, 200, 2, 1, 256, "bf16"),
+     ([0, 120, 0, 33], [0, 200, 0, 33])),
 ]
 UNIT = {"bf16": 2.0 ** -8, "fp16": 2.0 ** -11}  # unit roundoff of the output format
 
