@@ -839,6 +839,9 @@ __global__ void __launch_bounds__(Fwd2Cfg::THREADS, 1)
       ++w;
       if (item < 0) break;
       int lo_i, hi_i, lo_last, hi_first, t_lo, n;
+      bool valid;
+      typename E::T* orow;  // this row's output and LSE, kept for the epilogue
+      float* lse_at;
       {
         Tile128 t;
         decode_tile(p, item, t);
@@ -849,6 +852,10 @@ __global__ void __launch_bounds__(Fwd2Cfg::THREADS, 1)
         hi_first = t.kr.hi(t.q0);
         t_lo = t.t_lo;
         n = t.n;
+        valid = i < t.si.lq;
+        const int qhead = t.si.qhead0 + t.h;
+        orow = reinterpret_cast<typename E::T*>(p.o) + ((int64_t)(t.si.qrow0 + i) * g.nh_q + qhead) * 128;
+        lse_at = p.lse + (int64_t)(t.si.qrow0 + i) * g.nh_q + qhead;
       }
       float mbs = -INFINITY, l = 0.f;  // running max of S*scale*log2e, and the row sum
       for (int j = 0; j < n; ++j) {
@@ -930,14 +937,6 @@ __global__ void __launch_bounds__(Fwd2Cfg::THREADS, 1)
         ++no;
         tc_fence_after();
       }
-      // the tile's geometry again (cheaper than keeping it live through the loop)
-      Tile128 t;
-      decode_tile(p, item, t);
-      const int i = t.q0 + r;
-      const int qhead = t.si.qhead0 + t.h;
-      const bool valid = i < t.si.lq;
-      using T = typename E::T;
-      T* orow = reinterpret_cast<T*>(p.o) + ((int64_t)(t.si.qrow0 + i) * g.nh_q + qhead) * 128;
 #pragma unroll 1
       for (int cc = 0; cc < 4; ++cc) {
         uint32_t packed[16];
@@ -964,7 +963,6 @@ __global__ void __launch_bounds__(Fwd2Cfg::THREADS, 1)
             dst[k2] = make_uint4(packed[4 * k2], packed[4 * k2 + 1], packed[4 * k2 + 2], packed[4 * k2 + 3]);
         }
       }
-      float* lse_at = p.lse + (int64_t)(t.si.qrow0 + i) * g.nh_q + qhead;
       if (valid && SDPA_ADDR_OK(g.chk, lse_at, 4)) *lse_at = l > 0.f ? mbs * 0.6931471805599453f + logf(l) : -INFINITY;
     }
     if (!ok) {
