@@ -526,7 +526,8 @@ struct Fwd2Cfg {
   static constexpr int NSTAGES = 2;
   static constexpr int PIPE_BYTES = Q_BYTES + NSTAGES * STAGE_BYTES;  // per pipeline, 1024-aligned
   static constexpr int PIPE_BARS = 16;                                // mbarriers + queue per pipeline (8 bytes each)
-  static constexpr int SMEM_BYTES = 1024 + 2 * PIPE_BYTES + 2 * PIPE_BARS * 8 + 32;
+  static constexpr int STG_BYTES = 8 * 2048;  // per softmax warp: 32 rows x 64 bytes of output
+  static constexpr int SMEM_BYTES = 1024 + 2 * PIPE_BYTES + 2 * PIPE_BARS * 8 + 32 + STG_BYTES;
   static constexpr uint32_t TMEM_O = 0, TMEM_S = 128, TMEM_PIPE = 256;
   static constexpr int THREADS = 384;
   static constexpr int REGS_SOFTMAX = 192, REGS_OTHER = 120;
@@ -609,6 +610,7 @@ __global__ void __launch_bounds__(Fwd2Cfg::THREADS, 1)
   uint64_t* bar_drain = reinterpret_cast<uint64_t*>(smem + 2 * C::PIPE_BYTES) + 2 * C::PIPE_BARS;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  uint8_t* stg = reinterpret_cast<uint8_t*>(bar_drain) + 32;  // [8 softmax warps][2 KB] output staging
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
@@ -937,6 +939,9 @@ __global__ void __launch_bounds__(Fwd2Cfg::THREADS, 1)
         ++no;
         tc_fence_after();
       }
+      // 32 columns (64 bytes of a row) at a time, staged in shared memory so
+      // that each store writes eight rows' 64 contiguous bytes
+      uint8_t* wst = stg + warp * 2048;
 #pragma unroll 1
       for (int cc = 0; cc < 4; ++cc) {
         uint32_t packed[16];
@@ -956,12 +961,23 @@ __global__ void __launch_bounds__(Fwd2Cfg::THREADS, 1)
 #pragma unroll
           for (int k2 = 0; k2 < 16; ++k2) packed[k2] = 0u;
         }
-        if (valid && SDPA_ADDR_OK(g.chk, orow + cc * 32, 64)) {
-          uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
+        // segment k2 of row `lane` at position k2 ^ (lane % 4): four wavefronts a store
 #pragma unroll
-          for (int k2 = 0; k2 < 4; ++k2)
-            dst[k2] = make_uint4(packed[4 * k2], packed[4 * k2 + 1], packed[4 * k2 + 2], packed[4 * k2 + 3]);
+        for (int k2 = 0; k2 < 4; ++k2)
+          *reinterpret_cast<uint4*>(wst + lane * 64 + ((k2 ^ (lane & 3)) << 4)) =
+              make_uint4(packed[4 * k2], packed[4 * k2 + 1], packed[4 * k2 + 2], packed[4 * k2 + 3]);
+        __syncwarp();
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int rr = k * 8 + (lane >> 2), seg = lane & 3;  // row of the warp, 16-byte segment
+          const uint4 v4 = *reinterpret_cast<const uint4*>(wst + rr * 64 + ((seg ^ (rr & 3)) << 4));
+          typename E::T* dst = reinterpret_cast<typename E::T*>(
+              __shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(orow), rr));
+          const bool vr = __shfl_sync(0xffffffffu, valid ? 1 : 0, rr) != 0;
+          if (vr && SDPA_ADDR_OK(g.chk, dst + cc * 32 + seg * 8, 16))
+            *reinterpret_cast<uint4*>(dst + cc * 32 + seg * 8) = v4;
         }
+        __syncwarp();
       }
       if (valid && SDPA_ADDR_OK(g.chk, lse_at, 4)) *lse_at = l > 0.f ? mbs * 0.6931471805599453f + logf(l) : -INFINITY;
     }
