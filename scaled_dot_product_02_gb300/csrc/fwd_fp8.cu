@@ -63,7 +63,8 @@ struct F8Cfg {
   static constexpr int NST = 4;
   static constexpr int PIPE_BYTES = TILE + NST * TILE;  // per pipeline, 1024-aligned
   static constexpr int PIPE_BARS = 2 * NST + 12;         // mbarriers + queue per pipeline (8 bytes each)
-  static constexpr int SMEM = 1024 + NPIPE * PIPE_BYTES + NPIPE * PIPE_BARS * 8 + 32;
+  static constexpr int STG_BYTES = 8 * 2048;  // per softmax warp: 32 rows x 64 bytes of output
+  static constexpr int SMEM = 1024 + NPIPE * PIPE_BYTES + NPIPE * PIPE_BARS * 8 + 32 + STG_BYTES;
   static constexpr uint32_t TM_O = 0, TM_S = D, TM_PIPE = 256;
   static_assert(SMEM <= 232448, "shared memory per CTA");
   static_assert(NPIPE * (D + 128) <= 512, "TMEM columns");
@@ -250,6 +251,7 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
   uint64_t* bar_drain = reinterpret_cast<uint64_t*>(smem + C::NPIPE * C::PIPE_BYTES) + C::NPIPE * C::PIPE_BARS;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bar_drain + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  uint8_t* stg = reinterpret_cast<uint8_t*>(bar_drain) + 32;  // [8 softmax warps][2 KB] output staging
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
 
   if (threadIdx.x == 0) {
@@ -602,6 +604,10 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
         tc_fence_after();
         const float l = l2.x + l2.y;  // the sum of 448 P~
         const float mul = l > 0.f ? p.o_scale * 448.f / l : 0.f;  // o_scale = d_v / 448
+        // 32 columns (64 bytes of a row) at a time, staged in shared memory so
+        // that each store writes eight rows' 64 contiguous bytes; segment k of
+        // row `lane` at k ^ (lane % 4)
+        uint8_t* wst = stg + warp * 2048;
 #pragma unroll 1
         for (int cc = 0; cc < D / 32; ++cc) {
           uint32_t uu[32];
@@ -616,12 +622,21 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
 #pragma unroll
           for (int k2 = 0; k2 < 16; ++k2)
             packed[k2] = E::pack(__uint_as_float(uu[2 * k2]) * mul, __uint_as_float(uu[2 * k2 + 1]) * mul);
-          if (valid && SDPA_ADDR_OK(g.chk, orow + cc * 32, 64)) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + cc * 32);
 #pragma unroll
-            for (int k2 = 0; k2 < 4; ++k2)
-              dst[k2] = make_uint4(packed[4 * k2], packed[4 * k2 + 1], packed[4 * k2 + 2], packed[4 * k2 + 3]);
+          for (int k2 = 0; k2 < 4; ++k2)
+            *reinterpret_cast<uint4*>(wst + lane * 64 + ((k2 ^ (lane & 3)) << 4)) =
+                make_uint4(packed[4 * k2], packed[4 * k2 + 1], packed[4 * k2 + 2], packed[4 * k2 + 3]);
+          __syncwarp();
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const int rr = k * 8 + (lane >> 2), seg = lane & 3;  // row of the warp, 16-byte segment
+            const uint4 v4 = *reinterpret_cast<const uint4*>(wst + rr * 64 + ((seg ^ (rr & 3)) << 4));
+            T* drow = reinterpret_cast<T*>(__shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(orow), rr));
+            const bool vr = __shfl_sync(0xffffffffu, valid ? 1 : 0, rr) != 0;
+            if (vr && SDPA_ADDR_OK(g.chk, drow + cc * 32 + seg * 8, 16))
+              *reinterpret_cast<uint4*>(drow + cc * 32 + seg * 8) = v4;
           }
+          __syncwarp();
         }
         if (valid && SDPA_ADDR_OK(g.chk, lse_at, 4))
           *lse_at = l > 0.f ? m * g.scale + (logf(l) - kLn448) : -INFINITY;
