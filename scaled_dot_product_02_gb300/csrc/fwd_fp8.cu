@@ -1,4 +1,4 @@
-// fwd_fp8.cu -- FP8 (E4M3) attention forward for sm_103a, head_dim 128.
+// fwd_fp8.cu -- FP8 (E4M3) attention forward for sm_103a, head_dim 128 and 256.
 //
 // Reading of TransformerEngine PR #3705's closing note on FP8 ("Amax S"):
 // with E4M3 inputs the softmax output is stored in E4M3 under the fixed
@@ -24,17 +24,25 @@
 // of Vt (TMA's alignment rule for the innermost coordinate), and the gaps
 // between sequences hold zeros.
 //
-// The kernel is persistent (one CTA per SM) with two query-tile pipelines,
-// tiles taken heaviest first from an atomic ticket counter. Roles (384
-// threads): warps 0-3 / 4-7 softmax and epilogue of pipeline 0 / 1 (one
-// thread per query row, all 128 keys of a step), warps 8 / 9 TMA producer and
-// scheduler of pipeline 0 / 1, warp 10 TMEM allocator and MMA issuer serving
-// the two pipelines strictly in turn (so one pipeline's softmax runs under the
-// other's MMAs), warp 11 completes the third warpgroup. Per pipeline: a Q
-// tile and a four-stage K / Vt ring in shared memory; in TMEM its O (128
-// columns) and one S buffer (128), into whose first 32 columns the softmax
-// writes P8 for the P8 V MMA. On unmasked key tiles pass 1 takes each
-// 32-column chunk's max from the TMEM load itself (load with max reduction).
+// The kernel is persistent (one CTA per SM), tiles taken heaviest first from
+// an atomic ticket counter. At head_dim 128 it runs two query-tile pipelines.
+// Roles (384 threads): warps 0-3 / 4-7 softmax and epilogue of pipeline 0 / 1
+// (one thread per query row, all 128 keys of a step), warps 8 / 9 TMA
+// producer and scheduler of pipeline 0 / 1, warp 10 TMEM allocator and MMA
+// issuer serving the two pipelines strictly in turn (so one pipeline's
+// softmax runs under the other's MMAs), warp 11 completes the third
+// warpgroup. Per pipeline: a Q tile and a four-stage K / Vt ring in shared
+// memory; in TMEM its O (128 columns) and one S buffer (128), into whose
+// first 32 columns the softmax writes P8 for the P8 V MMA.
+// At head_dim 256 O takes 256 TMEM columns, so there is one pipeline with two
+// S buffers: step u of a tile runs in buffer u % 2 on softmax warpgroup
+// u % 2, and S of step u + 2 is computed while the other warpgroup works on
+// step u + 1. Pass 2 needs no running max (the max is final), so the two
+// warpgroups' steps are independent; they exchange their partial row maxima
+// before pass 2 and their row sums before the epilogue (shared memory, an
+// mbarrier each), and each stores half of O.
+// On unmasked key tiles pass 1 takes each 32-column chunk's max from the TMEM
+// load itself (load with max reduction).
 #include <algorithm>
 
 #include <cuda.h>
@@ -58,16 +66,22 @@ constexpr int F8_BM = 128, F8_BN = 128;
 template <int D>
 struct F8Cfg {
   static constexpr int NPIPE = D == 128 ? 2 : 1;
+  // softmax warpgroups per pipeline: at D = 256 both serve the one pipeline,
+  // taking its steps in turn, each with its own S buffer
+  static constexpr int NSM = D == 128 ? 1 : 2;
   static constexpr int ATOMS = D / 128;
   static constexpr int TILE = 128 * D;  // bytes of a Q, K or Vt tile
   static constexpr int NST = 4;
   static constexpr int PIPE_BYTES = TILE + NST * TILE;  // per pipeline, 1024-aligned
-  static constexpr int PIPE_BARS = 2 * NST + 12;         // mbarriers + queue per pipeline (8 bytes each)
+  static constexpr int PIPE_BARS = 2 * NST + 16;         // mbarriers + queue per pipeline (8 bytes each)
   static constexpr int STG_BYTES = 8 * 2048;  // per softmax warp: 32 rows x 64 bytes of output
-  static constexpr int SMEM = 1024 + NPIPE * PIPE_BYTES + NPIPE * PIPE_BARS * 8 + 32 + STG_BYTES;
+  // row max / row sum exchange of the two warpgroups: [tile parity][max, sum][warpgroup][row]
+  static constexpr int XCH_BYTES = NSM == 2 ? 2 * 2 * 2 * 128 * 4 : 0;
+  static constexpr int SMEM = 1024 + NPIPE * PIPE_BYTES + NPIPE * PIPE_BARS * 8 + 32 + STG_BYTES + XCH_BYTES;
   static constexpr uint32_t TM_O = 0, TM_S = D, TM_PIPE = 256;
   static_assert(SMEM <= 232448, "shared memory per CTA");
-  static_assert(NPIPE * (D + 128) <= 512, "TMEM columns");
+  static_assert(NPIPE * (D + 128 * NSM) <= 512, "TMEM columns");
+  static_assert(NPIPE * NSM == 2, "two softmax warpgroups");
 };
 constexpr int F8_THREADS = 384;
 constexpr int F8_REGS_SOFTMAX = 192, F8_REGS_OTHER = 120;
@@ -195,14 +209,16 @@ struct Pipe8 {
   uint64_t* full;         // [NST]
   uint64_t* empty;        // [NST]
   uint64_t* bar_q;        // Q of a tile landed
-  uint64_t* bar_s;        // S of a step ready
-  uint64_t* bar_p;        // the softmax is done with a step (pass 2: P8 written)
+  uint64_t* bar_s;        // [2] S of a step ready, per S buffer
+  uint64_t* bar_p;        // [2] the softmax is done with a step (pass 2: P8 written), per S buffer
   uint64_t* bar_o;        // a tile's last P8 V done
   uint64_t* q_free;       // a tile's last S done: Q may be replaced
   uint64_t* o_free;       // the epilogue has read O
   uint64_t* sched_full;   // [2] a tile published
   uint64_t* sched_empty;  // [2] its entry read by the MMA issuer and the softmax warps
   int* sched;             // [2] ticket, or -1 when the work is out
+  uint64_t* bar_xm;       // two softmax warpgroups: pass-1 row maxima exchanged
+  uint64_t* bar_xl;       // two softmax warpgroups: row sums exchanged
 };
 
 template <int D>
@@ -216,27 +232,30 @@ __device__ __forceinline__ Pipe8 pipe8_at(uint8_t* smem, int x) {
   P.empty = b + C::NST;
   P.bar_q = b + 2 * C::NST;
   P.bar_s = P.bar_q + 1;
-  P.bar_p = P.bar_q + 2;
-  P.bar_o = P.bar_q + 3;
-  P.q_free = P.bar_q + 4;
-  P.o_free = P.bar_q + 5;
-  P.sched_full = P.bar_q + 6;
-  P.sched_empty = P.bar_q + 8;
-  P.sched = reinterpret_cast<int*>(P.bar_q + 10);
+  P.bar_p = P.bar_q + 3;
+  P.bar_o = P.bar_q + 5;
+  P.q_free = P.bar_q + 6;
+  P.o_free = P.bar_q + 7;
+  P.sched_full = P.bar_q + 8;
+  P.sched_empty = P.bar_q + 10;
+  P.sched = reinterpret_cast<int*>(P.bar_q + 12);
+  P.bar_xm = P.bar_q + 13;
+  P.bar_xl = P.bar_q + 14;
   return P;
 }
 
-// Persistent, one CTA per SM with two query-tile pipelines. Each pipeline
-// takes query tiles (heaviest first) from an atomic ticket counter; a tile
-// runs 2n steps (pass 1 over its n key tiles: S and the row max; pass 2: S
-// again, P8 = E4M3(448 P~), O += P8 V), each step S -> softmax -> (P8 V) in
-// turn through the pipeline's single S buffer. The single MMA issuer serves
-// the two pipelines strictly in turn, so one pipeline's softmax runs while
-// the tensor pipe works on the other's MMAs.
-// Roles: warps 0-3 / 4-7 softmax + epilogue of pipeline 0 / 1 (one thread per
-// query row, all 128 keys of a step), warps 8 / 9 TMA producer and scheduler
-// of pipeline 0 / 1, warp 10 TMEM allocator + MMA issuer, warp 11 only
-// completes the third warpgroup. Every barrier phase counts across tiles.
+// Persistent, one CTA per SM. Each pipeline takes query tiles (heaviest
+// first) from an atomic ticket counter; a tile runs 2n steps (pass 1 over its
+// n key tiles: S and the row max; pass 2: S again, P8 = E4M3(448 P~),
+// O += P8 V). Head_dim 128: two pipelines, each step S -> softmax -> (P8 V)
+// in turn through the pipeline's single S buffer; the single MMA issuer
+// serves the two pipelines strictly in turn, so one pipeline's softmax runs
+// while the tensor pipe works on the other's MMAs. Head_dim 256: one
+// pipeline, two S buffers, the two softmax warpgroups taking its steps in
+// turn. Roles: warps 0-7 softmax + epilogue, warps 8 (/ 9) TMA producer and
+// scheduler of pipeline 0 (/ 1), warp 10 TMEM allocator + MMA issuer, warp
+// 11 only completes the third warpgroup. Every barrier phase counts across
+// tiles.
 template <bool BF16, int D>
 __global__ void __launch_bounds__(F8_THREADS, 1)
     fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -262,15 +281,19 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
         mbar_init(&P.empty[i], 1);
       }
       mbar_init(P.bar_q, 1);
-      mbar_init(P.bar_s, 1);
-      mbar_init(P.bar_p, 128);
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&P.bar_s[i], 1);
+        mbar_init(&P.bar_p[i], 128);
+      }
       mbar_init(P.bar_o, 1);
       mbar_init(P.q_free, 1);
-      mbar_init(P.o_free, 128);
+      mbar_init(P.o_free, 128 * C::NSM);
       for (int i = 0; i < 2; ++i) {
         mbar_init(&P.sched_full[i], 1);
-        mbar_init(&P.sched_empty[i], 129);
+        mbar_init(&P.sched_empty[i], 1 + 128 * C::NSM);
       }
+      mbar_init(P.bar_xm, 256);
+      mbar_init(P.bar_xl, 256);
     }
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
@@ -338,12 +361,25 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
           for (int a = 0; a < C::ATOMS; ++a)
             tma_load_3d(&tmQ, P.bar_q, P.sQ + a * 16384, a * 128, t.qhead, t.si.qrow0 + t.q0);
           ++nq;
-          // in the order the MMA issuer consumes: per step, K of its key tile
-          // and, in pass 2, then Vt of it
-          for (int u = 0; u < 2 * t.n && ok; ++u) {
-            const int j = u < t.n ? u : u - t.n;
-            ok = load(false, 0, t.khead, t.si.krow0 + (t.t_lo + j) * F8_BN);
-            if (ok && u >= t.n) ok = load(true, t.vrow0 + (t.t_lo + j) * F8_BN, 0, t.khead);
+          // in the order the MMA issuer consumes them (K of step u: key tile
+          // u, or u - n in pass 2; Vt of a pass-2 step u: key tile u - n)
+          auto load_k = [&](int u) {
+            return load(false, 0, t.khead, t.si.krow0 + (t.t_lo + (u < t.n ? u : u - t.n)) * F8_BN);
+          };
+          auto load_v = [&](int u) { return load(true, t.vrow0 + (t.t_lo + u - t.n) * F8_BN, 0, t.khead); };
+          if constexpr (C::NSM == 1) {
+            // per step: K, then in pass 2 Vt
+            for (int u = 0; u < 2 * t.n && ok; ++u) {
+              ok = load_k(u);
+              if (ok && u >= t.n) ok = load_v(u);
+            }
+          } else {
+            // K of steps 0 and 1; then per step u: Vt in pass 2, K of step u + 2
+            ok = load_k(0) && load_k(1);
+            for (int u = 0; u < 2 * t.n && ok; ++u) {
+              if (u >= t.n) ok = load_v(u);
+              if (ok && u + 2 < 2 * t.n) ok = load_k(u + 2);
+            }
           }
           if (!ok) break;
         }
@@ -357,7 +393,7 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
       }
     } else if (warp == 10) {
       // ---------------------------------------------------------- MMA issuer for both pipelines
-      if (elect_one()) {
+      if (C::NSM == 1 && elect_one()) {
         constexpr uint32_t IDESC_S = idesc_e4m3(128, 128), IDESC_O = idesc_e4m3(128, D);
         struct State {
           int w, c, nq, steps, no, n, u;
@@ -414,7 +450,7 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
           }
           mma_commit(&P.empty[slot]);
           if (m.u == 2 * m.n - 1) mma_commit(P.q_free);
-          mma_commit(P.bar_s);
+          mma_commit(&P.bar_s[0]);
           ++m.c;
           return true;
         };
@@ -425,7 +461,7 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
           const Pipe8 P = pipe8_at<D>(smem, x);
           State& m = st[x];
           if (m.u == m.n && m.no > 0 && !mbar_wait(P.o_free, (m.no - 1) & 1, abort_flag)) return false;
-          if (!mbar_wait(P.bar_p, m.steps & 1, abort_flag)) return false;
+          if (!mbar_wait(&P.bar_p[0], m.steps & 1, abort_flag)) return false;
           ++m.steps;
           if (m.u < m.n) return true;  // pass 1: the max only
           const int slot = m.c % C::NST;
@@ -467,21 +503,110 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
           mma_commit(bar_drain);
           mbar_wait_drain(bar_drain, 0);
         }
+      } else if (C::NSM == 2 && elect_one()) {
+        // ---- one pipeline, two S buffers: step u of a tile runs in buffer
+        // u % 2 and on softmax warpgroup u % 2. Per tile: S of steps 0 and 1,
+        // then for each step u once its softmax is done: P8 V (pass 2) and S
+        // of step u + 2 into the buffer just freed, so the tensor pipe works
+        // on the next steps while the other warpgroup's softmax runs.
+        constexpr uint32_t IDESC_S = idesc_e4m3(128, 128), IDESC_O = idesc_e4m3(128, D);
+        const Pipe8 P = pipe8_at<D>(smem, 0);
+        int w = 0, c = 0, nq = 0, no = 0;
+        int base = 0;  // steps each S buffer served in earlier tiles (n per tile)
+        bool ok = true;
+        auto issue_s = [&](int u, int n) -> bool {
+          const int slot = c % C::NST;
+          if (!mbar_wait(&P.full[slot], (c / C::NST) & 1, abort_flag)) return false;
+          tc_fence_after();
+          const uint32_t q_base = smem_u32(P.sQ), kb = smem_u32(P.sStage + slot * C::TILE);
+          const uint32_t dcol = tmem + C::TM_S + (uint32_t)(u & 1) * 128;
+#pragma unroll
+          for (int ks = 0; ks < D / 32; ++ks) {
+            const uint32_t off = (ks >> 2) * 16384 + (ks & 3) * 32;
+            mma_f8_ss(dcol, smem_desc_sw128(q_base + off, 16, 1024), smem_desc_sw128(kb + off, 16, 1024), IDESC_S,
+                      ks != 0);
+          }
+          mma_commit(&P.empty[slot]);
+          if (u == 2 * n - 1) mma_commit(P.q_free);
+          mma_commit(&P.bar_s[u & 1]);
+          ++c;
+          return true;
+        };
+        // the tile's first P8 V overwrites O, which the previous tile's
+        // epilogue must have read
+        auto issue_pv = [&](int u, int n) -> bool {
+          if (u == n && no > 0 && !mbar_wait(P.o_free, (no - 1) & 1, abort_flag)) return false;
+          const int slot = c % C::NST;
+          if (!mbar_wait(&P.full[slot], (c / C::NST) & 1, abort_flag)) return false;
+          tc_fence_after();
+          const uint32_t vb = smem_u32(P.sStage + slot * C::TILE);
+          const uint32_t pcol = tmem + C::TM_S + (uint32_t)(u & 1) * 128;
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks)
+            mma_f8_ts(tmem + C::TM_O, pcol + ks * 8, smem_desc_sw128(vb + ks * 32, 16, 1024), IDESC_O,
+                      u > n || ks != 0);
+          mma_commit(&P.empty[slot]);
+          ++c;
+          return true;
+        };
+        while (ok) {
+          const int e = w & 1;
+          if (!mbar_wait(&P.sched_full[e], (w >> 1) & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          const int item = *reinterpret_cast<volatile int*>(&P.sched[e]);
+          mbar_arrive(&P.sched_empty[e]);
+          ++w;
+          if (item < 0) break;
+          Fp8Tile t;
+          fp8_tile(p, item, t);
+          const int n = t.n;
+          if (n == 0) continue;
+          if (!mbar_wait(P.bar_q, nq & 1, abort_flag)) {
+            ok = false;
+            break;
+          }
+          ++nq;
+          tc_fence_after();
+          ok = issue_s(0, n) && issue_s(1, n);
+          for (int u = 0; u < 2 * n && ok; ++u) {
+            ok = mbar_wait(&P.bar_p[u & 1], (base + (u >> 1)) & 1, abort_flag);
+            if (ok && u >= n) ok = issue_pv(u, n);
+            if (ok && u + 2 < 2 * n) ok = issue_s(u + 2, n);
+          }
+          if (!ok) break;
+          base += n;
+          mma_commit(P.bar_o);
+          ++no;
+        }
+        if (!ok) {
+          *abort_flag = 1;
+          record_error(p.err, SDPA_ERR_TIMEOUT);
+          mma_commit(bar_drain);
+          mbar_wait_drain(bar_drain, 0);
+        }
       }
     }
   } else {
     regs_inc<F8_REGS_SOFTMAX>();
-    // ------------------------------------------------------------ softmax + epilogue of pipeline warp / 4
-    // (one pipeline at head_dim 256: warps 4-7 have no work)
-    const int x = warp >> 2;
-    if (x < C::NPIPE) {
+    // ------------------------------------------------------------ softmax + epilogue
+    // head_dim 128: warpgroup wg serves pipeline wg, every step of its tiles.
+    // head_dim 256: both serve the one pipeline, warpgroup wg the steps u with
+    // u % 2 == wg in S buffer wg; they exchange the pass-1 row maxima before
+    // pass 2 and the row sums before the epilogue, and each stores half of O.
+    const int wg = warp >> 2;
+    const int x = C::NSM == 2 ? 0 : wg, sb = C::NSM == 2 ? wg : 0;
+    {
       const Pipe8 P = pipe8_at<D>(smem, x);
       const int r = (warp & 3) * 32 + lane;
       const uint32_t lane_base = tmem + x * C::TM_PIPE + ((uint32_t)((warp & 3) * 32) << 16);
-      const uint32_t scol = lane_base + C::TM_S;
+      const uint32_t scol = lane_base + C::TM_S + (uint32_t)sb * 128;
+      float* xch = reinterpret_cast<float*>(stg + C::STG_BYTES);  // [tile parity][max, sum][warpgroup][row]
+      constexpr int OCH = D / 32 / C::NSM;                       // 32-column chunks of O per warpgroup
       const float sl2 = g.scale_log2;
       using T = typename E::T;
-      int w = 0, steps = 0, no = 0;
+      int w = 0, steps = 0, no = 0, xt = 0;
       bool ok = true;
       while (ok) {
         const int e = w & 1;
@@ -503,12 +628,12 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
         T* orow = reinterpret_cast<T*>(p.o) + ((long long)(t.si.qrow0 + i) * g.nh_q + t.qhead) * D;
         float* lse_at = p.lse + (long long)(t.si.qrow0 + i) * g.nh_q + t.qhead;
         if (n == 0) {  // no key for any row of the tile: O = 0, LSE = -inf
-          if (valid && SDPA_ADDR_OK(g.chk, orow, 2 * D)) {
-            uint4* dst = reinterpret_cast<uint4*>(orow);
+          if (valid && SDPA_ADDR_OK(g.chk, orow + sb * (D / C::NSM), 2 * D / C::NSM)) {
+            uint4* dst = reinterpret_cast<uint4*>(orow + sb * (D / C::NSM));
 #pragma unroll
-            for (int k2 = 0; k2 < D / 8; ++k2) dst[k2] = make_uint4(0u, 0u, 0u, 0u);
+            for (int k2 = 0; k2 < D / 8 / C::NSM; ++k2) dst[k2] = make_uint4(0u, 0u, 0u, 0u);
           }
-          if (valid && SDPA_ADDR_OK(g.chk, lse_at, 4)) *lse_at = -INFINITY;
+          if (sb == 0 && valid && SDPA_ADDR_OK(g.chk, lse_at, 4)) *lse_at = -INFINITY;
           continue;
         }
         // pass 1: the row max, four independent chains; pass 2: the exponent's
@@ -517,8 +642,28 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
         float mm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         float m = -INFINITY, nb = 0.f;
         float2 l2 = make_float2(0.f, 0.f);
-        for (int u = 0; u < 2 * n; ++u) {
-          if (!__all_sync(0xffffffffu, mbar_wait(P.bar_s, steps & 1, abort_flag))) {
+        bool have_m = false;
+        // the row max once pass 1 is done (with two warpgroups: the larger of
+        // the two partial maxima) and the exponent's bias from it
+        auto final_max = [&]() -> bool {
+          m = fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3]));
+          if constexpr (C::NSM == 2) {
+            float* xm = xch + (xt & 1) * 512;
+            xm[wg * 128 + r] = m;
+            mbar_arrive(P.bar_xm);
+            if (!__all_sync(0xffffffffu, mbar_wait(P.bar_xm, xt & 1, abort_flag))) return false;
+            m = fmaxf(m, xm[(1 - wg) * 128 + r]);
+          }
+          nb = kLog2_448 - (m == -INFINITY ? 0.f : m * sl2);
+          have_m = true;
+          return true;
+        };
+        for (int u = sb; u < 2 * n; u += C::NSM) {
+          if (u >= n && !have_m && !final_max()) {
+            ok = false;
+            break;
+          }
+          if (!__all_sync(0xffffffffu, mbar_wait(&P.bar_s[sb], steps & 1, abort_flag))) {
             ok = false;
             break;
           }
@@ -586,14 +731,23 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
               tmem_wait_st();
             }
           }
-          if (u == n - 1) {
-            m = fmaxf(fmaxf(mm[0], mm[1]), fmaxf(mm[2], mm[3]));
-            nb = kLog2_448 - (m == -INFINITY ? 0.f : m * sl2);
-          }
           tc_fence_before();
-          mbar_arrive(P.bar_p);
+          mbar_arrive(&P.bar_p[sb]);
         }
+        if (ok && !have_m && !final_max()) ok = false;  // a warpgroup with no pass-2 step
         if (!ok) break;
+        float l = l2.x + l2.y;  // the sum of 448 P~ (over this warpgroup's steps)
+        if constexpr (C::NSM == 2) {
+          float* xl = xch + (xt & 1) * 512 + 256;
+          xl[wg * 128 + r] = l;
+          mbar_arrive(P.bar_xl);
+          if (!__all_sync(0xffffffffu, mbar_wait(P.bar_xl, xt & 1, abort_flag))) {
+            ok = false;
+            break;
+          }
+          l = xl[r] + xl[128 + r];
+        }
+        ++xt;
         // epilogue: O / the row sum, 32 columns at a time; O is free for the
         // next tile's first P8 V once the last chunk has been read
         if (!__all_sync(0xffffffffu, mbar_wait(P.bar_o, no & 1, abort_flag))) {
@@ -602,19 +756,18 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
         }
         ++no;
         tc_fence_after();
-        const float l = l2.x + l2.y;  // the sum of 448 P~
         const float mul = l > 0.f ? p.o_scale * 448.f / l : 0.f;  // o_scale = d_v / 448
         // 32 columns (64 bytes of a row) at a time, staged in shared memory so
         // that each store writes eight rows' 64 contiguous bytes; segment k of
         // row `lane` at k ^ (lane % 4)
         uint8_t* wst = stg + warp * 2048;
 #pragma unroll 1
-        for (int cc = 0; cc < D / 32; ++cc) {
+        for (int cc = sb * OCH; cc < (sb + 1) * OCH; ++cc) {
           uint32_t uu[32];
           tmem_ld32(lane_base + C::TM_O + cc * 32, uu);
           tmem_wait_ld();
           reg_fence(uu);
-          if (cc == D / 32 - 1) {
+          if (cc == (sb + 1) * OCH - 1) {
             tc_fence_before();
             mbar_arrive(P.o_free);
           }
@@ -638,7 +791,7 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
           }
           __syncwarp();
         }
-        if (valid && SDPA_ADDR_OK(g.chk, lse_at, 4))
+        if (sb == 0 && valid && SDPA_ADDR_OK(g.chk, lse_at, 4))
           *lse_at = l > 0.f ? m * g.scale + (logf(l) - kLn448) : -INFINITY;
       }
       if (!ok) {
