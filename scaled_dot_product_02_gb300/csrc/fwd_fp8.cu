@@ -79,13 +79,16 @@ struct F8Cfg {
   static constexpr int XCH_BYTES = NSM == 2 ? 2 * 2 * 2 * 128 * 4 : 0;
   static constexpr int SMEM = 1024 + NPIPE * PIPE_BYTES + NPIPE * PIPE_BARS * 8 + 32 + STG_BYTES + XCH_BYTES;
   static constexpr uint32_t TM_O = 0, TM_S = D, TM_PIPE = 256;
+  // threads: softmax warpgroups, the producer / issuer warpgroup and, with
+  // two softmax warpgroups on one pipeline, an epilogue warpgroup
+  static constexpr int THREADS = NSM == 2 ? 512 : 384;
+  static constexpr int REGS_SOFTMAX = NSM == 2 ? 184 : 192, REGS_OTHER = NSM == 2 ? 72 : 120;
+  static_assert(2 * REGS_SOFTMAX + (THREADS / 128 - 2) * REGS_OTHER <= 65536 / THREADS * (THREADS / 128),
+                "register split");
   static_assert(SMEM <= 232448, "shared memory per CTA");
   static_assert(NPIPE * (D + 128 * NSM) <= 512, "TMEM columns");
   static_assert(NPIPE * NSM == 2, "two softmax warpgroups");
 };
-constexpr int F8_THREADS = 384;
-constexpr int F8_REGS_SOFTMAX = 192, F8_REGS_OTHER = 120;
-static_assert(2 * F8_REGS_SOFTMAX + F8_REGS_OTHER <= 3 * 168, "register split");
 constexpr float kLog2_448 = 8.807354922057604f;  // log2(448)
 constexpr float kLn448 = 6.104793232414985f;     // ln(448)
 
@@ -218,7 +221,7 @@ struct Pipe8 {
   uint64_t* sched_empty;  // [2] its entry read by the MMA issuer and the softmax warps
   int* sched;             // [2] ticket, or -1 when the work is out
   uint64_t* bar_xm;       // two softmax warpgroups: pass-1 row maxima exchanged
-  uint64_t* bar_xl;       // two softmax warpgroups: row sums exchanged
+  uint64_t* bar_stats;    // two softmax warpgroups: a tile's row maxima and partial sums in place
 };
 
 template <int D>
@@ -240,8 +243,59 @@ __device__ __forceinline__ Pipe8 pipe8_at(uint8_t* smem, int x) {
   P.sched_empty = P.bar_q + 10;
   P.sched = reinterpret_cast<int*>(P.bar_q + 12);
   P.bar_xm = P.bar_q + 13;
-  P.bar_xl = P.bar_q + 14;
+  P.bar_stats = P.bar_q + 14;
   return P;
+}
+
+// One warp's 32 rows of O (row `lane` at TMEM lanes ocol): all D columns of
+// the accumulator times mul, 32 at a time, staged in shared memory (wst,
+// 2 KB; segment k of row `lane` at k ^ (lane % 4)) so that each store writes
+// eight rows' 64 contiguous bytes. Arrives on o_free once the last chunk has
+// been read from TMEM.
+template <typename E, int D>
+__device__ __forceinline__ void store_o_rows(const Geom& g, uint32_t ocol, float mul, typename E::T* orow, bool valid,
+                                             uint8_t* wst, uint64_t* o_free, int lane) {
+  using T = typename E::T;
+#pragma unroll 1
+  for (int cc = 0; cc < D / 32; ++cc) {
+    uint32_t uu[32];
+    tmem_ld32(ocol + cc * 32, uu);
+    tmem_wait_ld();
+    reg_fence(uu);
+    if (cc == D / 32 - 1) {
+      tc_fence_before();
+      mbar_arrive(o_free);
+    }
+    uint32_t packed[16];
+#pragma unroll
+    for (int k2 = 0; k2 < 16; ++k2)
+      packed[k2] = E::pack(__uint_as_float(uu[2 * k2]) * mul, __uint_as_float(uu[2 * k2 + 1]) * mul);
+#pragma unroll
+    for (int k2 = 0; k2 < 4; ++k2)
+      *reinterpret_cast<uint4*>(wst + lane * 64 + ((k2 ^ (lane & 3)) << 4)) =
+          make_uint4(packed[4 * k2], packed[4 * k2 + 1], packed[4 * k2 + 2], packed[4 * k2 + 3]);
+    __syncwarp();
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int rr = k * 8 + (lane >> 2), seg = lane & 3;  // row of the warp, 16-byte segment
+      const uint4 v4 = *reinterpret_cast<const uint4*>(wst + rr * 64 + ((seg ^ (rr & 3)) << 4));
+      T* drow = reinterpret_cast<T*>(__shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(orow), rr));
+      const bool vr = __shfl_sync(0xffffffffu, valid ? 1 : 0, rr) != 0;
+      if (vr && SDPA_ADDR_OK(g.chk, drow + cc * 32 + seg * 8, 16)) *reinterpret_cast<uint4*>(drow + cc * 32 + seg * 8) = v4;
+    }
+    __syncwarp();
+  }
+}
+
+// A row with no key: O = 0, LSE = -inf.
+template <typename T, int D>
+__device__ __forceinline__ void store_empty_row(const Geom& g, T* orow, float* lse_at, bool valid) {
+  if (valid && SDPA_ADDR_OK(g.chk, orow, 2 * D)) {
+    uint4* dst = reinterpret_cast<uint4*>(orow);
+#pragma unroll
+    for (int k2 = 0; k2 < D / 8; ++k2) dst[k2] = make_uint4(0u, 0u, 0u, 0u);
+  }
+  if (valid && SDPA_ADDR_OK(g.chk, lse_at, 4)) *lse_at = -INFINITY;
 }
 
 // Persistent, one CTA per SM. Each pipeline takes query tiles (heaviest
@@ -257,7 +311,7 @@ __device__ __forceinline__ Pipe8 pipe8_at(uint8_t* smem, int x) {
 // 11 only completes the third warpgroup. Every barrier phase counts across
 // tiles.
 template <bool BF16, int D>
-__global__ void __launch_bounds__(F8_THREADS, 1)
+__global__ void __launch_bounds__(F8Cfg<D>::THREADS, 1)
     fwd_fp8_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                    const __grid_constant__ CUtensorMap tmVt, const __grid_constant__ Fp8Params p) {
   using E = Elem<BF16>;
@@ -287,13 +341,13 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
       }
       mbar_init(P.bar_o, 1);
       mbar_init(P.q_free, 1);
-      mbar_init(P.o_free, 128 * C::NSM);
+      mbar_init(P.o_free, 128);
       for (int i = 0; i < 2; ++i) {
         mbar_init(&P.sched_full[i], 1);
-        mbar_init(&P.sched_empty[i], 1 + 128 * C::NSM);
+        mbar_init(&P.sched_empty[i], C::NSM == 2 ? 1 + 256 + 128 : 1 + 128);
       }
       mbar_init(P.bar_xm, 256);
-      mbar_init(P.bar_xl, 256);
+      mbar_init(P.bar_stats, 256);
     }
     mbar_init(bar_drain, 1);
     *abort_flag = 0;
@@ -309,7 +363,7 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
   const uint32_t tmem = *tmem_holder;
 
   if (warp >= 8) {
-    regs_dec<F8_REGS_OTHER>();
+    regs_dec<C::REGS_OTHER>();
     if (warp == 8 || (warp == 9 && C::NPIPE == 2)) {
       // ---------------------------------------------------------- scheduler + producer of pipeline warp - 8
       if (elect_one()) {
@@ -587,9 +641,68 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
           mbar_wait_drain(bar_drain, 0);
         }
       }
+    } else if (C::NSM == 2 && warp >= 12) {
+      // ---------------------------------------------------------- epilogue warpgroup (two softmax warpgroups)
+      // Per tile: the row's max and sum from the two softmax warpgroups'
+      // stats, then O / the row sum from TMEM and the LSE; the softmax
+      // warpgroups meanwhile run the next tile's pass 1. Its tile-queue entry
+      // is released only after the stats are read, so no stats slot is
+      // rewritten (by the tile after next) before that.
+      using T = typename E::T;
+      const Pipe8 P = pipe8_at<D>(smem, 0);
+      const int r = (warp & 3) * 32 + lane;
+      const uint32_t ocol = tmem + C::TM_O + ((uint32_t)((warp & 3) * 32) << 16);
+      const float* xch = reinterpret_cast<const float*>(stg + C::STG_BYTES);
+      int w = 0, no = 0;
+      bool ok = true;
+      while (ok) {
+        const int e = w & 1;
+        if (!__all_sync(0xffffffffu, mbar_wait(&P.sched_full[e], (w >> 1) & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        const int item = *reinterpret_cast<volatile int*>(&P.sched[e]);
+        ++w;
+        if (item < 0) {
+          mbar_arrive(&P.sched_empty[e]);
+          break;
+        }
+        Fp8Tile t;
+        fp8_tile(p, item, t);
+        const int i = t.q0 + r;
+        const bool valid = i < t.si.lq;
+        T* orow = reinterpret_cast<T*>(p.o) + ((long long)(t.si.qrow0 + i) * g.nh_q + t.qhead) * D;
+        float* lse_at = p.lse + (long long)(t.si.qrow0 + i) * g.nh_q + t.qhead;
+        if (t.n == 0) {
+          mbar_arrive(&P.sched_empty[e]);
+          store_empty_row<T, D>(g, orow, lse_at, valid);
+          continue;
+        }
+        if (!__all_sync(0xffffffffu, mbar_wait(P.bar_stats, no & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        const float* xs = xch + (no & 1) * 512;
+        const float m = fmaxf(xs[r], xs[128 + r]), l = xs[256 + r] + xs[384 + r];
+        mbar_arrive(&P.sched_empty[e]);
+        if (!__all_sync(0xffffffffu, mbar_wait(P.bar_o, no & 1, abort_flag))) {
+          ok = false;
+          break;
+        }
+        ++no;
+        tc_fence_after();
+        const float mul = l > 0.f ? p.o_scale * 448.f / l : 0.f;  // o_scale = d_v / 448
+        store_o_rows<E, D>(g, ocol, mul, orow, valid, stg + (warp - 12) * 2048, P.o_free, lane);
+        if (valid && SDPA_ADDR_OK(g.chk, lse_at, 4))
+          *lse_at = l > 0.f ? m * g.scale + (logf(l) - kLn448) : -INFINITY;
+      }
+      if (!ok) {
+        *abort_flag = 1;
+        record_error(p.err, SDPA_ERR_TIMEOUT);
+      }
     }
   } else {
-    regs_inc<F8_REGS_SOFTMAX>();
+    regs_inc<C::REGS_SOFTMAX>();
     // ------------------------------------------------------------ softmax + epilogue
     // head_dim 128: warpgroup wg serves pipeline wg, every step of its tiles.
     // head_dim 256: both serve the one pipeline, warpgroup wg the steps u with
@@ -603,7 +716,6 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
       const uint32_t lane_base = tmem + x * C::TM_PIPE + ((uint32_t)((warp & 3) * 32) << 16);
       const uint32_t scol = lane_base + C::TM_S + (uint32_t)sb * 128;
       float* xch = reinterpret_cast<float*>(stg + C::STG_BYTES);  // [tile parity][max, sum][warpgroup][row]
-      constexpr int OCH = D / 32 / C::NSM;                       // 32-column chunks of O per warpgroup
       const float sl2 = g.scale_log2;
       using T = typename E::T;
       int w = 0, steps = 0, no = 0, xt = 0;
@@ -627,13 +739,8 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
         const int lo_last = t.kr.lo(t.q_last), hi_first = t.kr.hi(t.q0);
         T* orow = reinterpret_cast<T*>(p.o) + ((long long)(t.si.qrow0 + i) * g.nh_q + t.qhead) * D;
         float* lse_at = p.lse + (long long)(t.si.qrow0 + i) * g.nh_q + t.qhead;
-        if (n == 0) {  // no key for any row of the tile: O = 0, LSE = -inf
-          if (valid && SDPA_ADDR_OK(g.chk, orow + sb * (D / C::NSM), 2 * D / C::NSM)) {
-            uint4* dst = reinterpret_cast<uint4*>(orow + sb * (D / C::NSM));
-#pragma unroll
-            for (int k2 = 0; k2 < D / 8 / C::NSM; ++k2) dst[k2] = make_uint4(0u, 0u, 0u, 0u);
-          }
-          if (sb == 0 && valid && SDPA_ADDR_OK(g.chk, lse_at, 4)) *lse_at = -INFINITY;
+        if (n == 0) {  // no key for any row of the tile (the epilogue warpgroup's, if there is one)
+          if (C::NSM == 1) store_empty_row<T, D>(g, orow, lse_at, valid);
           continue;
         }
         // pass 1: the row max, four independent chains; pass 2: the exponent's
@@ -736,63 +843,26 @@ __global__ void __launch_bounds__(F8_THREADS, 1)
         }
         if (ok && !have_m && !final_max()) ok = false;  // a warpgroup with no pass-2 step
         if (!ok) break;
-        float l = l2.x + l2.y;  // the sum of 448 P~ (over this warpgroup's steps)
+        const float l = l2.x + l2.y;  // the sum of 448 P~ over this warpgroup's steps
         if constexpr (C::NSM == 2) {
-          float* xl = xch + (xt & 1) * 512 + 256;
-          xl[wg * 128 + r] = l;
-          mbar_arrive(P.bar_xl);
-          if (!__all_sync(0xffffffffu, mbar_wait(P.bar_xl, xt & 1, abort_flag))) {
+          // the partial sum beside the maxima, for the epilogue warpgroup
+          xch[(xt & 1) * 512 + 256 + wg * 128 + r] = l;
+          mbar_arrive(P.bar_stats);
+          ++xt;
+        } else {
+          // epilogue: O / the row sum; O is free for the next tile's first
+          // P8 V once its last chunk has been read
+          if (!__all_sync(0xffffffffu, mbar_wait(P.bar_o, no & 1, abort_flag))) {
             ok = false;
             break;
           }
-          l = xl[r] + xl[128 + r];
+          ++no;
+          tc_fence_after();
+          const float mul = l > 0.f ? p.o_scale * 448.f / l : 0.f;  // o_scale = d_v / 448
+          store_o_rows<E, D>(g, lane_base + C::TM_O, mul, orow, valid, stg + warp * 2048, P.o_free, lane);
+          if (valid && SDPA_ADDR_OK(g.chk, lse_at, 4))
+            *lse_at = l > 0.f ? m * g.scale + (logf(l) - kLn448) : -INFINITY;
         }
-        ++xt;
-        // epilogue: O / the row sum, 32 columns at a time; O is free for the
-        // next tile's first P8 V once the last chunk has been read
-        if (!__all_sync(0xffffffffu, mbar_wait(P.bar_o, no & 1, abort_flag))) {
-          ok = false;
-          break;
-        }
-        ++no;
-        tc_fence_after();
-        const float mul = l > 0.f ? p.o_scale * 448.f / l : 0.f;  // o_scale = d_v / 448
-        // 32 columns (64 bytes of a row) at a time, staged in shared memory so
-        // that each store writes eight rows' 64 contiguous bytes; segment k of
-        // row `lane` at k ^ (lane % 4)
-        uint8_t* wst = stg + warp * 2048;
-#pragma unroll 1
-        for (int cc = sb * OCH; cc < (sb + 1) * OCH; ++cc) {
-          uint32_t uu[32];
-          tmem_ld32(lane_base + C::TM_O + cc * 32, uu);
-          tmem_wait_ld();
-          reg_fence(uu);
-          if (cc == (sb + 1) * OCH - 1) {
-            tc_fence_before();
-            mbar_arrive(P.o_free);
-          }
-          uint32_t packed[16];
-#pragma unroll
-          for (int k2 = 0; k2 < 16; ++k2)
-            packed[k2] = E::pack(__uint_as_float(uu[2 * k2]) * mul, __uint_as_float(uu[2 * k2 + 1]) * mul);
-#pragma unroll
-          for (int k2 = 0; k2 < 4; ++k2)
-            *reinterpret_cast<uint4*>(wst + lane * 64 + ((k2 ^ (lane & 3)) << 4)) =
-                make_uint4(packed[4 * k2], packed[4 * k2 + 1], packed[4 * k2 + 2], packed[4 * k2 + 3]);
-          __syncwarp();
-#pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            const int rr = k * 8 + (lane >> 2), seg = lane & 3;  // row of the warp, 16-byte segment
-            const uint4 v4 = *reinterpret_cast<const uint4*>(wst + rr * 64 + ((seg ^ (rr & 3)) << 4));
-            T* drow = reinterpret_cast<T*>(__shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(orow), rr));
-            const bool vr = __shfl_sync(0xffffffffu, valid ? 1 : 0, rr) != 0;
-            if (vr && SDPA_ADDR_OK(g.chk, drow + cc * 32 + seg * 8, 16))
-              *reinterpret_cast<uint4*>(drow + cc * 32 + seg * 8) = v4;
-          }
-          __syncwarp();
-        }
-        if (sb == 0 && valid && SDPA_ADDR_OK(g.chk, lse_at, 4))
-          *lse_at = l > 0.f ? m * g.scale + (logf(l) - kLn448) : -INFINITY;
       }
       if (!ok) {
         *abort_flag = 1;
@@ -832,7 +902,7 @@ static int launch_fwd_fp8_t(const Fp8Launch& L, long long tiles) {
   long long grid = std::min<long long>((tiles + C::NPIPE - 1) / C::NPIPE, sms);
   if (debug_max_ctas() > 0) grid = std::min<long long>(grid, debug_max_ctas());  // tickets cover every tile
   if (cudaMemsetAsync(p.tile_counter, 0, sizeof(int), L.stream) != cudaSuccess) return SDPA_ERR_CUDA;
-  kern<<<(unsigned)grid, F8_THREADS, C::SMEM, L.stream>>>(L.tmQ, L.tmK, L.tmVt, p);
+  kern<<<(unsigned)grid, C::THREADS, C::SMEM, L.stream>>>(L.tmQ, L.tmK, L.tmVt, p);
   return cudaGetLastError() == cudaSuccess ? SDPA_OK : SDPA_ERR_CUDA;
 }
 
