@@ -780,7 +780,7 @@ def fp8_arm(args, w, inp):
             "e2e": {"value": job_tflops(world, exact, 1, e2e_ms), "unit": "TFLOP/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms, "overlap": "none (serial copies)"},
             "roofline": {"bound": "tensor", "kernel": "fwd_fp8_kernel", "achieved": achieved, "peak": peak,
-                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": None,
+                         "unit": "TFLOP/s", "frac": achieved / peak, "traffic": traffic_for("fwd_fp8", w.name),
                          "peak_source": f"{pk_kind} bf16_tflops x 2 (nominal dense fp8/bf16 ratio 4.5/2.25)",
                          "algorithmic_flops_per_launch": exact, "executed_flops_per_launch": 1.5 * exact},
             "cpu_baseline": cpu,
