@@ -34,6 +34,14 @@ BWD_CASES = [
     Workload("d512_two_sided_window_gqa", "bshd", "none", 1, 260, 260, 4, 2, 512, "bf16", window=(40, 90)),
     Workload("br_window_d128", "bshd", "causal_br", 1, 200, 333, 2, 1, 128, "bf16", window=(60, 0)),
     Workload("br_window_d256", "bshd", "causal_br", 1, 200, 333, 2, 1, 256, "bf16", window=(90, 0)),
+    # a diagonal-only window: every row sees its own key alone (P = 1, so dS, dQ and dK vanish and
+    # dV = dO). The kernels' dQ and dK are then the rounding residues of dP - delta (two fp32 sums of
+    # the same D products), held to the 1e-5 margin of a tensor whose reference is exactly zero;
+    # std 0.5 keeps those products, and so the residues, at a quarter of unit-variance inputs' at
+    # head_dim 256 and 512
+    Workload("diagonal_window_d128", "bshd", "causal", 1, 300, 300, 2, 2, 128, "bf16", window=(0, 0)),
+    Workload("diagonal_window_d256", "bshd", "causal", 1, 300, 300, 2, 1, 256, "bf16", window=(0, 0), std=0.5),
+    Workload("diagonal_window_d512", "bshd", "causal", 1, 300, 300, 2, 1, 512, "bf16", window=(0, 0), std=0.5),
 ]
 
 

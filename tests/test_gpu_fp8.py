@@ -39,6 +39,11 @@ CASES = [
     (Workload("fp8_d256_bottom_right_nomask_rect", "bshd", "none", 1, 200, 333, 2, 1, 256, "bf16"), None),
     (Workload("fp8_two_sided_window", "bshd", "none", 1, 300, 300, 2, 2, 128, "bf16", window=(70, 45)), None),
     (Workload("fp8_d256_br_window", "bshd", "causal_br", 1, 200, 333, 2, 1, 256, "bf16", window=(90, 0)), None),
+    # every row sees only its own key: each query tile has one key tile, so at
+    # head_dim 256 one softmax warpgroup has no pass-1 step and the other no
+    # pass-2 step, tile after tile
+    (Workload("fp8_diagonal_window", "bshd", "causal", 2, 600, 600, 4, 2, 128, "bf16", window=(0, 0)), None),
+    (Workload("fp8_d256_diagonal_window", "bshd", "causal", 2, 600, 600, 4, 2, 256, "bf16", window=(0, 0)), None),
     # empty sequences between live ones
     (Workload("fp8_thd_with_empty", "thd", "causal", 5, 150, 150, 4, 2, 128, "bf16"),
      ([150, 0, 37, 0, 90], [150, 0, 37, 0, 90])),

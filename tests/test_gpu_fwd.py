@@ -32,6 +32,10 @@ FWD_CASES = [
     Workload("d512_two_sided_window_gqa", "bshd", "none", 1, 260, 260, 4, 2, 512, "bf16", window=(40, 90)),
     Workload("br_window_d128", "bshd", "causal_br", 1, 200, 333, 2, 1, 128, "bf16", window=(60, 0)),
     Workload("br_window_d256", "bshd", "causal_br", 1, 200, 333, 2, 1, 256, "bf16", window=(90, 0)),
+    # a diagonal-only window: every row sees its own key alone (P = 1, O = V)
+    Workload("diagonal_window_d128", "bshd", "causal", 1, 300, 300, 2, 2, 128, "bf16", window=(0, 0)),
+    Workload("diagonal_window_d256", "bshd", "causal", 1, 300, 300, 2, 1, 256, "bf16", window=(0, 0)),
+    Workload("diagonal_window_d512", "bshd", "causal", 1, 300, 300, 2, 1, 512, "bf16", window=(0, 0)),
 ]
 
 

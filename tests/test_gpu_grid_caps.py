@@ -74,13 +74,20 @@ def test_results_do_not_depend_on_how_many_ctas_run(case):
 
 
 @pytest.mark.parametrize("head_dim", [128, 256])
-def test_fp8_forward_does_not_depend_on_how_many_ctas_run(head_dim):
+@pytest.mark.parametrize("shape", ["thd_varlen", "diagonal_window"])
+def test_fp8_forward_does_not_depend_on_how_many_ctas_run(head_dim, shape):
+    """With one or two CTAs every CTA runs many tiles back to back; the
+    diagonal window gives every query tile a single key tile, so at head_dim
+    256 consecutive tiles reuse the row-stats slots as fast as they can."""
     import torch
 
     import scaled_dot_product_02_gb300 as sdpa
     from parity import gpu_kwargs
 
-    w = Workload("fp8_thd", "thd", "causal", 3, 300, 300, 4, 2, head_dim, "bf16", len_range=(1, 300))
+    if shape == "thd_varlen":
+        w = Workload("fp8_thd", "thd", "causal", 3, 300, 300, 4, 2, head_dim, "bf16", len_range=(1, 300))
+    else:
+        w = Workload("fp8_diag", "bshd", "causal", 2, 600, 600, 4, 2, head_dim, "bf16", window=(0, 0))
     inp = workloads.fp8_inputs(w, seed=73)
     q8, k8, v8 = (torch.from_numpy(inp[x]).cuda() for x in ("q8", "k8", "v8"))
     kw = gpu_kwargs(w, inp)

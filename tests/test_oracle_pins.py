@@ -138,6 +138,24 @@ def test_single_key_and_dominant_key():
     np.testing.assert_allclose(o2[0, 0, 0], v2[0, 3, 0], atol=1e-20)
 
 
+def test_diagonal_window_reduces_to_the_identity():
+    # causal with a left window of 0: row i sees key i alone, so P = 1, O = V,
+    # LSE = the score s_ii, dS = P (dP - delta) = 0 (hence dQ = dK = 0) and dV = dO;
+    # with GQA a kv head's dV sums the dO of its query heads
+    r = rng(17)
+    q, k, v, do = (r.standard_normal(s) for s in [(2, 9, 4, 8), (2, 9, 2, 8), (2, 9, 2, 8), (2, 9, 4, 8)])
+    scale = 0.4
+    out = oracle.bwd(q, k, v, do, mask="causal", scale=scale, window=(0, 0))
+    o, lse = oracle.fwd(q, k, v, mask="causal", scale=scale, window=(0, 0))
+    vq = np.repeat(v, 2, axis=2)  # query head h reads kv head h // 2
+    np.testing.assert_allclose(o, vq, atol=1e-15)
+    s_ii = scale * np.einsum("bshd,bshd->bsh", q, np.repeat(k, 2, axis=2))
+    np.testing.assert_allclose(lse, s_ii.reshape(-1, 4), atol=1e-13)
+    np.testing.assert_allclose(out["dq"], 0.0, atol=1e-13)
+    np.testing.assert_allclose(out["dk"], 0.0, atol=1e-13)
+    np.testing.assert_allclose(out["dv"], do.reshape(2, 9, 2, 2, 8).sum(axis=3), atol=1e-13)
+
+
 def test_lse_rows_of_p_and_delta_identities():
     r = rng(8)
     q, k, v, do = (r.standard_normal(s) for s in [(1, 8, 2, 4), (1, 8, 2, 4), (1, 8, 2, 4), (1, 8, 2, 4)])
