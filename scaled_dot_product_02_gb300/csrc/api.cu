@@ -75,19 +75,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-int* error_word() {
-  static std::mutex mu;
-  static int* ptrs[128] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!ptrs[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_sdpa_error_word) != cudaSuccess) return nullptr;
-    ptrs[dev] = static_cast<int*>(p);
-  }
-  return ptrs[dev];
-}
+int* error_word() { return static_cast<int*>(device_symbol_address(&g_sdpa_error_word)); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -107,19 +95,7 @@ constexpr bool kAddrCheck = true;
 static __device__ AddrTable g_sdpa_addr_table;
 std::atomic<long long> g_addr_shrink{0};
 
-AddrTable* addr_table() {
-  static std::mutex mu;
-  static AddrTable* ptrs[128] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return nullptr;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!ptrs[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_sdpa_addr_table) != cudaSuccess) return nullptr;
-    ptrs[dev] = static_cast<AddrTable*>(p);
-  }
-  return ptrs[dev];
-}
+AddrTable* addr_table() { return static_cast<AddrTable*>(device_symbol_address(&g_sdpa_addr_table)); }
 
 // Writes the call's extents (less the debug shrink) ahead of its kernels on
 // stream s; the violation counters are left as they are.
@@ -395,6 +371,61 @@ int bwd_head_block(const sdpa_problem* p) {
 
 static std::atomic<int> g_max_ctas{0};
 int debug_max_ctas() { return g_max_ctas.load(std::memory_order_relaxed); }
+
+// Unique ID of the calling thread's current context (cuCtxGetId; IDs are not
+// reused within a process), 0 when there is none or the driver lacks the call.
+static unsigned long long current_context_id() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  using GetId = CUresult (*)(CUcontext, unsigned long long*);
+  static GetCurrent get_current = nullptr;
+  static GetId get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &ptr, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<GetCurrent>(ptr);
+    ptr = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &ptr, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<GetId>(ptr);
+  });
+  if (!get_current || !get_id) return 0;
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+  return id;
+}
+
+void* device_symbol_address(const void* symbol) {
+  struct Entry {
+    const void* symbol;
+    int dev;
+    unsigned long long ctx;
+    void* addr;
+  };
+  static std::mutex mu;
+  static Entry cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  const unsigned long long ctx = current_context_id();
+  Entry* slot = nullptr;
+  for (Entry& e : cache) {
+    if (e.symbol == symbol && e.dev == dev) {
+      slot = &e;
+      break;
+    }
+    if (!slot && !e.symbol) slot = &e;  // first free entry, unless a match follows
+  }
+  if (slot && slot->symbol == symbol && slot->dev == dev && ctx != 0 && slot->ctx == ctx) return slot->addr;
+  void* addr = nullptr;
+  if (cudaGetSymbolAddress(&addr, symbol) != cudaSuccess || !addr) return nullptr;
+  const unsigned long long now = current_context_id();  // the lookup may have made the context current
+  if (slot && now != 0) *slot = Entry{symbol, dev, now, addr};
+  return addr;
+}
 
 int set_kernel_smem(const void* kernel, int bytes, int carveout) {
   static std::mutex mu;

@@ -33,6 +33,11 @@ int launch_in_grids(long long total, F&& fn) {
 // instance of the module, and several host threads may make their first call
 // at the same time. Returns an sdpa_status.
 int set_kernel_smem(const void* kernel, int bytes, int carveout);
+// Device address of a __device__ variable (its host-side stand-in `symbol`)
+// on the current device, cached per device for the context it was taken in: a
+// context created later (after cudaDeviceReset) looks the address up again.
+// nullptr on failure.
+void* device_symbol_address(const void* symbol);
 
 struct FwdParams {
   Geom g;

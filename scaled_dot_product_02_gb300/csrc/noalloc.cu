@@ -23,27 +23,18 @@
 #include <mutex>
 
 #include "../../include/sdpa.h"
+#include "kernels.h"
 
 static __device__ __align__(256) unsigned char g_bwd_scratch[SDPA_BWD_NOALLOC_MAX_BYTES];
 
 namespace {
 
 // Device address of g_bwd_scratch on the current device. In host code the
-// symbol is only a host-side stand-in, so the address must come from
-// cudaGetSymbolAddress, once per device, with that device current.
+// symbol is only a host-side stand-in, so the address comes from
+// cudaGetSymbolAddress (cached per device and context).
 int scratch_address(void** out) {
-  static std::mutex mu;
-  static void* addr[128] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 128) return SDPA_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(mu);
-  if (!addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess || !p) return SDPA_ERR_CUDA;
-    addr[dev] = p;
-  }
-  *out = addr[dev];
-  return SDPA_OK;
+  *out = sdpa::device_symbol_address(&g_bwd_scratch);
+  return *out ? SDPA_OK : SDPA_ERR_CUDA;
 }
 
 }  // namespace
