@@ -247,44 +247,51 @@ __device__ __forceinline__ Pipe8 pipe8_at(uint8_t* smem, int x) {
   return P;
 }
 
-// One warp's 32 rows of O (row `lane` at TMEM lanes ocol): all D columns of
-// the accumulator times mul, 32 at a time, staged in shared memory (wst,
-// 2 KB; segment k of row `lane` at k ^ (lane % 4)) so that each store writes
-// eight rows' 64 contiguous bytes. Arrives on o_free once the last chunk has
-// been read from TMEM.
+// Columns [32 cc, 32 cc + 32) of one warp's 32 rows of O (row `lane` at TMEM
+// lanes ocol) times mul, staged in shared memory (wst, 2 KB; segment k of
+// row `lane` at k ^ (lane % 4)) so that each store writes eight rows' 64
+// contiguous bytes. Arrives on o_free (if given) once the chunk has been read
+// from TMEM.
+template <typename E, int D>
+__device__ __forceinline__ void store_o_chunk(const Geom& g, uint32_t ocol, int cc, float mul, typename E::T* orow,
+                                              bool valid, uint8_t* wst, uint64_t* o_free, int lane) {
+  using T = typename E::T;
+  uint32_t uu[32];
+  tmem_ld32(ocol + cc * 32, uu);
+  tmem_wait_ld();
+  reg_fence(uu);
+  if (o_free) {
+    tc_fence_before();
+    mbar_arrive(o_free);
+  }
+  uint32_t packed[16];
+#pragma unroll
+  for (int k2 = 0; k2 < 16; ++k2)
+    packed[k2] = E::pack(__uint_as_float(uu[2 * k2]) * mul, __uint_as_float(uu[2 * k2 + 1]) * mul);
+#pragma unroll
+  for (int k2 = 0; k2 < 4; ++k2)
+    *reinterpret_cast<uint4*>(wst + lane * 64 + ((k2 ^ (lane & 3)) << 4)) =
+        make_uint4(packed[4 * k2], packed[4 * k2 + 1], packed[4 * k2 + 2], packed[4 * k2 + 3]);
+  __syncwarp();
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int rr = k * 8 + (lane >> 2), seg = lane & 3;  // row of the warp, 16-byte segment
+    const uint4 v4 = *reinterpret_cast<const uint4*>(wst + rr * 64 + ((seg ^ (rr & 3)) << 4));
+    T* drow = reinterpret_cast<T*>(__shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(orow), rr));
+    const bool vr = __shfl_sync(0xffffffffu, valid ? 1 : 0, rr) != 0;
+    if (vr && SDPA_ADDR_OK(g.chk, drow + cc * 32 + seg * 8, 16)) *reinterpret_cast<uint4*>(drow + cc * 32 + seg * 8) = v4;
+  }
+  __syncwarp();
+}
+
+// All D columns of one warp's 32 rows of O, chunk by chunk; o_free after the
+// last chunk has been read.
 template <typename E, int D>
 __device__ __forceinline__ void store_o_rows(const Geom& g, uint32_t ocol, float mul, typename E::T* orow, bool valid,
                                              uint8_t* wst, uint64_t* o_free, int lane) {
-  using T = typename E::T;
 #pragma unroll 1
-  for (int cc = 0; cc < D / 32; ++cc) {
-    uint32_t uu[32];
-    tmem_ld32(ocol + cc * 32, uu);
-    tmem_wait_ld();
-    reg_fence(uu);
-    if (cc == D / 32 - 1) {
-      tc_fence_before();
-      mbar_arrive(o_free);
-    }
-    uint32_t packed[16];
-#pragma unroll
-    for (int k2 = 0; k2 < 16; ++k2)
-      packed[k2] = E::pack(__uint_as_float(uu[2 * k2]) * mul, __uint_as_float(uu[2 * k2 + 1]) * mul);
-#pragma unroll
-    for (int k2 = 0; k2 < 4; ++k2)
-      *reinterpret_cast<uint4*>(wst + lane * 64 + ((k2 ^ (lane & 3)) << 4)) =
-          make_uint4(packed[4 * k2], packed[4 * k2 + 1], packed[4 * k2 + 2], packed[4 * k2 + 3]);
-    __syncwarp();
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const int rr = k * 8 + (lane >> 2), seg = lane & 3;  // row of the warp, 16-byte segment
-      const uint4 v4 = *reinterpret_cast<const uint4*>(wst + rr * 64 + ((seg ^ (rr & 3)) << 4));
-      T* drow = reinterpret_cast<T*>(__shfl_sync(0xffffffffu, reinterpret_cast<unsigned long long>(orow), rr));
-      const bool vr = __shfl_sync(0xffffffffu, valid ? 1 : 0, rr) != 0;
-      if (vr && SDPA_ADDR_OK(g.chk, drow + cc * 32 + seg * 8, 16)) *reinterpret_cast<uint4*>(drow + cc * 32 + seg * 8) = v4;
-    }
-    __syncwarp();
-  }
+  for (int cc = 0; cc < D / 32; ++cc)
+    store_o_chunk<E, D>(g, ocol, cc, mul, orow, valid, wst, cc == D / 32 - 1 ? o_free : nullptr, lane);
 }
 
 // A row with no key: O = 0, LSE = -inf.
@@ -720,6 +727,26 @@ __global__ void __launch_bounds__(F8Cfg<D>::THREADS, 1)
       using T = typename E::T;
       int w = 0, steps = 0, no = 0, xt = 0;
       bool ok = true;
+      // head_dim 128: a finished tile's O is stored one 32-column chunk per
+      // pass-1 step of the pipeline's next tile (pass 1 does not touch O), the
+      // rest before its first pass-2 step (whose P8 V needs o_free)
+      int pend = 0;  // chunks of the previous tile's O still to store
+      bool pneed_o = false;
+      float pmul = 0.f;
+      T* porow = nullptr;
+      bool pvalid = false;
+      auto drain_one = [&]() -> bool {
+        if (pneed_o) {  // that tile's last P8 V is done (this keeps every bar_o phase waited in turn)
+          if (!__all_sync(0xffffffffu, mbar_wait(P.bar_o, no & 1, abort_flag))) return false;
+          ++no;
+          tc_fence_after();
+          pneed_o = false;
+        }
+        store_o_chunk<E, D>(g, lane_base + C::TM_O, D / 32 - pend, pmul, porow, pvalid, stg + warp * 2048,
+                            pend == 1 ? P.o_free : nullptr, lane);
+        --pend;
+        return true;
+      };
       while (ok) {
         const int e = w & 1;
         if (!__all_sync(0xffffffffu, mbar_wait(&P.sched_full[e], (w >> 1) & 1, abort_flag))) {
@@ -769,6 +796,10 @@ __global__ void __launch_bounds__(F8Cfg<D>::THREADS, 1)
           if (u >= n && !have_m && !final_max()) {
             ok = false;
             break;
+          }
+          if (C::NSM == 1 && u == n) {
+            while (pend > 0 && ok) ok = drain_one();
+            if (!ok) break;
           }
           if (!__all_sync(0xffffffffu, mbar_wait(&P.bar_s[sb], steps & 1, abort_flag))) {
             ok = false;
@@ -840,6 +871,10 @@ __global__ void __launch_bounds__(F8Cfg<D>::THREADS, 1)
           }
           tc_fence_before();
           mbar_arrive(&P.bar_p[sb]);
+          if (C::NSM == 1 && u < n && pend > 0 && !drain_one()) {
+            ok = false;
+            break;
+          }
         }
         if (ok && !have_m && !final_max()) ok = false;  // a warpgroup with no pass-2 step
         if (!ok) break;
@@ -850,20 +885,17 @@ __global__ void __launch_bounds__(F8Cfg<D>::THREADS, 1)
           mbar_arrive(P.bar_stats);
           ++xt;
         } else {
-          // epilogue: O / the row sum; O is free for the next tile's first
-          // P8 V once its last chunk has been read
-          if (!__all_sync(0xffffffffu, mbar_wait(P.bar_o, no & 1, abort_flag))) {
-            ok = false;
-            break;
-          }
-          ++no;
-          tc_fence_after();
-          const float mul = l > 0.f ? p.o_scale * 448.f / l : 0.f;  // o_scale = d_v / 448
-          store_o_rows<E, D>(g, lane_base + C::TM_O, mul, orow, valid, stg + warp * 2048, P.o_free, lane);
+          // the LSE now; O / the row sum during the pipeline's next tile
           if (valid && SDPA_ADDR_OK(g.chk, lse_at, 4))
             *lse_at = l > 0.f ? m * g.scale + (logf(l) - kLn448) : -INFINITY;
+          pend = D / 32;
+          pneed_o = true;
+          pmul = l > 0.f ? p.o_scale * 448.f / l : 0.f;  // o_scale = d_v / 448
+          porow = orow;
+          pvalid = valid;
         }
       }
+      while (ok && pend > 0) ok = drain_one();  // the pipeline's last tile
       if (!ok) {
         *abort_flag = 1;
         record_error(p.err, SDPA_ERR_TIMEOUT);
