@@ -33,6 +33,7 @@ CASES = [
     W("one_key", "bshd", "causal_br", 1, 130, 1, 2, 2),
     W("tiny_thd_sequences", "thd", "causal", 40, 3, 3, 2, 1, len_range=(1, 3)),
     W("gqa_16_to_1_fp16", "bshd", "causal", 1, 256, 256, 16, 1, "fp16"),
+    W("diagonal_window", "bshd", "causal", 1, 300, 300, 2, 2, window=(0, 0)),  # every row sees its own key alone
 ]
 
 
@@ -62,6 +63,23 @@ def test_asymmetric_forward_with_empty_thd_sequences():
 
     w = W("thd_with_empty", "thd", "causal", 4, 150, 150, 2, 2)
     inp = workloads.make_inputs(w, seed=32, lengths=np.array([150, 0, 37, 0]))
+    o, lse = _fwd(w, inp)
+    results = check_fwd(w, inp, o, lse)
+    report(w.name, results)
+
+
+@pytest.mark.parametrize("mask", ["causal_br", "causal", "none"])
+def test_asymmetric_forward_with_unequal_thd_lengths(mask):
+    # per-sequence query and key lengths differ (cu_seqlens_q != cu_seqlens_kv): a
+    # sequence with more queries than keys (its first rows see no key under the
+    # bottom-right mask), one with a single query, equal lengths, fewer queries than
+    # keys and a single key
+    from parity import check_fwd, report
+
+    lq, lk = [300, 1, 129, 200, 64], [140, 250, 129, 333, 1]
+    w = W(f"thd_unequal_{mask}", "thd", mask, len(lq), max(lq), max(lk), 4, 2)
+    inp = workloads.make_inputs(w, seed=41, lengths=(np.array(lq), np.array(lk)))
+    assert not np.array_equal(inp["cu_seqlens_q"], inp["cu_seqlens_kv"])
     o, lse = _fwd(w, inp)
     results = check_fwd(w, inp, o, lse)
     report(w.name, results)
