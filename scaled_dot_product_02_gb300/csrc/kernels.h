@@ -44,7 +44,7 @@ struct FwdParams {
   void* o;
   float* lse;
   int* err;          // sticky per-device error word
-  const int* guard;  // per-call metadata-guard verdict (THD) or nullptr
+  const int* guard;  // per-call metadata-guard result (THD) or nullptr
   int n_q_tiles;     // ceil(seqlen_q / 128)
   int dv_splits;     // 1, or 2 when each CTA owns half of the value columns
   int* tile_counter;  // head_dim 128: ticket counter in the workspace (zeroed per call)

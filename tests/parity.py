@@ -84,7 +84,7 @@ def _item_err(got, ref):
     return d
 
 
-def judge(name, got, ref_master, ref_rounded, dtype, cap=None, round_out=True, edge=None):
+def check_tensor(name, got, ref_master, ref_rounded, dtype, cap=None, round_out=True, edge=None):
     """Returns (ok, message) for one tensor.
 
     `edge` marks the edge items (boolean, the tensor's shape without its last
@@ -178,8 +178,8 @@ def check_fwd(w, inp, o_gpu, lse_gpu, rows=None):
     o_m, l_m = oracle.fwd(inp["q"], inp["k"], inp["v"], **kw)
     o_r, l_r = oracle.fwd(rin["q"], rin["k"], rin["v"], **kw)
     eq, _ = edge_items(w, inp, backward=False)
-    res = [judge("O", o_gpu, o_m, o_r, w.dtype, O_CAP[w.dtype], edge=_q_items(eq, o_m, w.heads_q)),
-           judge("LSE", lse_gpu, l_m, l_r, w.dtype, LSE_CAP, round_out=False, edge=eq)]
+    res = [check_tensor("O", o_gpu, o_m, o_r, w.dtype, O_CAP[w.dtype], edge=_q_items(eq, o_m, w.heads_q)),
+           check_tensor("LSE", lse_gpu, l_m, l_r, w.dtype, LSE_CAP, round_out=False, edge=eq)]
     empty = np.isneginf(l_r)
     if empty.any():
         res.append((bool(np.all(np.isneginf(lse_gpu[empty]))), "empty rows have LSE = -inf"))
@@ -195,9 +195,9 @@ def check_bwd(w, inp, dq, dk, dv):
     eq, ek = edge_items(w, inp)
     ekk = ek.reshape(np.shape(m["dk"])[:-2] + (w.heads_kv,))
     return [
-        judge("dQ", dq, m["dq"], r["dq"], w.dtype, edge=_q_items(eq, m["dq"], w.heads_q)),
-        judge("dK", dk, m["dk"], r["dk"], w.dtype, edge=ekk),
-        judge("dV", dv, m["dv"], r["dv"], w.dtype, edge=ekk),
+        check_tensor("dQ", dq, m["dq"], r["dq"], w.dtype, edge=_q_items(eq, m["dq"], w.heads_q)),
+        check_tensor("dK", dk, m["dk"], r["dk"], w.dtype, edge=ekk),
+        check_tensor("dV", dv, m["dv"], r["dv"], w.dtype, edge=ekk),
     ]
 
 
@@ -296,20 +296,20 @@ def check_sampled(w, inp, out, n_rows=40, n_keys=12, seed=0, backward=True):
     nh = w.heads_q
     o_g = np.stack([out["o"].reshape(-1, nh, w.dv)[t, h] for t, (_, h, _) in zip(tr, bhi)])
     l_g = np.array([out["lse"][t, h] for t, (_, h, _) in zip(tr, bhi)])
-    res = [judge("O", o_g, o_m, o_r, w.dtype, O_CAP[w.dtype], edge=q_edge),
-           judge("LSE", l_g, l_m, l_r, w.dtype, LSE_CAP, round_out=False, edge=q_edge)]
+    res = [check_tensor("O", o_g, o_m, o_r, w.dtype, O_CAP[w.dtype], edge=q_edge),
+           check_tensor("LSE", l_g, l_m, l_r, w.dtype, LSE_CAP, round_out=False, edge=q_edge)]
     if not backward:
         return res
     dq_m = oracle.dq_rows(inp["q"], inp["k"], inp["v"], inp["do"], bhi, **kw)
     dq_r = oracle.dq_rows(rin["q"], rin["k"], rin["v"], rin["do"], bhi, **kw)
     dq_g = np.stack([out["dq"].reshape(-1, nh, w.head_dim)[t, h] for t, (_, h, _) in zip(tr, bhi)])
-    res.append(judge("dQ", dq_g, dq_m, dq_r, w.dtype, edge=q_edge))
+    res.append(check_tensor("dQ", dq_g, dq_m, dq_r, w.dtype, edge=q_edge))
     kt = [kv_token_row(w, inp, b, j) for b, _, j in bgj]
     dk_m, dv_m = oracle.dkdv_rows(inp["q"], inp["k"], inp["v"], inp["do"], bgj, **kw)
     dk_r, dv_r = oracle.dkdv_rows(rin["q"], rin["k"], rin["v"], rin["do"], bgj, **kw)
     nkv = w.heads_kv
     dk_g = np.stack([out["dk"].reshape(-1, nkv, w.head_dim)[t, g] for t, (_, g, _) in zip(kt, bgj)])
     dv_g = np.stack([out["dv"].reshape(-1, nkv, w.head_dim)[t, g] for t, (_, g, _) in zip(kt, bgj)])
-    res.append(judge("dK", dk_g, dk_m, dk_r, w.dtype, edge=k_edge))
-    res.append(judge("dV", dv_g, dv_m, dv_r, w.dtype, edge=k_edge))
+    res.append(check_tensor("dK", dk_g, dk_m, dk_r, w.dtype, edge=k_edge))
+    res.append(check_tensor("dV", dv_g, dv_m, dv_r, w.dtype, edge=k_edge))
     return res
