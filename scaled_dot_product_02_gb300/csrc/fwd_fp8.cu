@@ -177,6 +177,16 @@ __global__ void __launch_bounds__(256) vt_kernel(const Fp8Params p) {
   }
 }
 
+// Key tile (counted from the tile's first) of step k of a pass over n key
+// tiles. With two softmax warpgroups taking the steps in turn, the two masked
+// edge tiles (the first and the last) go first, one to each warpgroup:
+// 0, n - 1, 1, 2, ..., n - 2; with one, in order.
+template <int NSM>
+__device__ __forceinline__ int key_tile_of(int k, int n) {
+  if (NSM == 1 || n < 3) return k;
+  return k == 0 ? 0 : (k == 1 ? n - 1 : k - 1);
+}
+
 // A query tile of the heaviest-first order (the last query tiles of every
 // sequence first, GQA heads adjacent) and the key tiles it sees.
 struct Fp8Tile {
@@ -425,9 +435,12 @@ __global__ void __launch_bounds__(F8Cfg<D>::THREADS, 1)
           // in the order the MMA issuer consumes them (K of step u: key tile
           // u, or u - n in pass 2; Vt of a pass-2 step u: key tile u - n)
           auto load_k = [&](int u) {
-            return load(false, 0, t.khead, t.si.krow0 + (t.t_lo + (u < t.n ? u : u - t.n)) * F8_BN);
+            const int j = key_tile_of<C::NSM>(u < t.n ? u : u - t.n, t.n);
+            return load(false, 0, t.khead, t.si.krow0 + (t.t_lo + j) * F8_BN);
           };
-          auto load_v = [&](int u) { return load(true, t.vrow0 + (t.t_lo + u - t.n) * F8_BN, 0, t.khead); };
+          auto load_v = [&](int u) {
+            return load(true, t.vrow0 + (t.t_lo + key_tile_of<C::NSM>(u - t.n, t.n)) * F8_BN, 0, t.khead);
+          };
           if constexpr (C::NSM == 1) {
             // per step: K, then in pass 2 Vt
             for (int u = 0; u < 2 * t.n && ok; ++u) {
@@ -807,7 +820,7 @@ __global__ void __launch_bounds__(F8Cfg<D>::THREADS, 1)
           }
           ++steps;
           tc_fence_after();
-          const int kb = (t.t_lo + (u < n ? u : u - n)) * F8_BN;
+          const int kb = (t.t_lo + key_tile_of<C::NSM>(u < n ? u : u - n, n)) * F8_BN;
           const bool edge = !(lo_last <= kb && hi_first >= kb + F8_BN);  // uniform across the tile
           if (u < n && !edge) {
             // interior pass-1 step: the row max comes with the loads
